@@ -1,0 +1,171 @@
+/*
+ * zsolve -- mixed-precision dense complex-symmetric frequency sweeps on GB300.
+ *
+ * At each frequency the library solves Z(omega) x = b with
+ *     Z(omega) = j*omega*L - j*Psi/omega + Zs(omega)*G,
+ * L, Psi, G real, symmetric and independent of frequency
+ * (malusrfworks.com, "Solving Dense Matrices Fast in the Browser", section
+ * "Fewer frequency points: adaptive frequency sampling", the form of Z).
+ * The method is mixed-precision iterative refinement (same page, section
+ * "Double-precision answers from a GPU without double precision", steps 1-4):
+ *   1. factorise Z in low precision without pivoting, LU in blocks of 32;
+ *   2. solve with those factors for a first x;
+ *   3. form r = b - Z x in double precision;
+ *   4. solve for a correction d with the low-precision factors, x += d, and
+ *      repeat 3-4 until ||d|| / ||x|| < tol;
+ * and a frequency whose refinement does not converge is solved alone by a
+ * double-precision LU with partial pivoting (same section, the paragraph
+ * after the steps; section "Measure first" for partial pivoting as the
+ * fallback).  All of it runs on one GPU.
+ *
+ * Conventions for every entry point:
+ *  - Matrices are n x n, row-major, dense.  L, Psi, G are real float64.
+ *    Complex vectors are interleaved (re, im) float64 ("c128"); a block of
+ *    nrhs right-hand sides is nrhs rows of n c128 values.
+ *  - Pointers to matrices and vectors are DEVICE pointers unless the name of
+ *    the entry point ends in _host.  They are borrowed for the duration of
+ *    the call; the library keeps no reference to them.
+ *  - Work is enqueued on the context's stream (zsolve_set_stream; default
+ *    the legacy default stream).  zsolve_assemble and zsolve_factor return
+ *    without synchronising.  zsolve_refine, zsolve_sweep and the other
+ *    solve calls synchronise the stream once per refinement step (to read
+ *    the convergence test) and return with their outputs complete.
+ *  - The context owns every workspace (about 24 n^2 bytes per concurrently
+ *    factored frequency plus O(n * nrhs)); nothing is allocated after
+ *    zsolve_create except the fallback workspace on its first use.
+ *  - A context is not thread-safe; use one per host thread.
+ *  - Every call returns ZSOLVE_OK (0) or a negative status; the message of
+ *    the last failure is kept in the context (zsolve_last_error).  After
+ *    ZSOLVE_ECUDA the CUDA context may be unusable.
+ */
+#ifndef ZSOLVE_H
+#define ZSOLVE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* status codes */
+#define ZSOLVE_OK 0
+#define ZSOLVE_EINVAL (-1)     /* invalid argument (n <= 0, nrhs > nrhs_max, NULL, omega <= 0) */
+#define ZSOLVE_ENOMEM (-2)     /* device or host allocation failed */
+#define ZSOLVE_ECUDA (-3)      /* CUDA runtime error */
+#define ZSOLVE_ESTATE (-4)     /* call out of order: not assembled / not factored */
+#define ZSOLVE_ENONFINITE (-5) /* non-finite value in an input */
+#define ZSOLVE_ESINGULAR (-6)  /* the double-precision fallback met an exactly zero pivot column */
+#define ZSOLVE_ETIMEOUT (-7)   /* a bounded device-side wait gave up (dependency never satisfied) */
+
+/* arithmetic of the trailing (Schur) update of the low-precision factorisation */
+#define ZSOLVE_GEMM_AUTO 0   /* TF32X3 */
+#define ZSOLVE_GEMM_TF32 1   /* one tf32 tensor-core product per term (tcgen05) */
+#define ZSOLVE_GEMM_TF32X3 2 /* split hi/lo tf32, three products per term (tcgen05) */
+#define ZSOLVE_GEMM_FFMA 3   /* FP32 fused multiply-add on the CUDA cores */
+
+typedef struct zsolve_ctx zsolve_ctx; /* opaque */
+
+typedef struct {
+    double tol;         /* stop when every RHS has ||d||_2/||x||_2 < tol (default 1e-11) */
+    int max_iter;       /* corrections after the first solve before declaring a stall (10) */
+    int gemm;           /* ZSOLVE_GEMM_* (default AUTO) */
+    int outer_block;    /* columns per outer block of the factorisation; 128 (only value) */
+    int batch;          /* frequencies factored together by zsolve_sweep; 0 = automatic */
+    int force_fallback; /* testing aid: treat every frequency as stalled (default 0) */
+} zsolve_opts;
+
+typedef struct {
+    int iters;         /* corrections applied after the first solve */
+    int fallback;      /* 1 if x came from the double-precision pivoted LU */
+    int status;        /* ZSOLVE_OK, or the error that ended this frequency */
+    int pivot_flag;    /* 1 if the low-precision factorisation met a tiny or non-finite pivot */
+    double relcorr;    /* final max over RHS of ||d||_2/||x||_2 (0 after a fallback) */
+    float ms_assemble; /* device time of the stages (batched: the batch's time / batch size) */
+    float ms_factor;
+    float ms_refine;
+} zsolve_info;
+
+/* Fill *opts with the defaults listed above. */
+int zsolve_default_opts(zsolve_opts *opts);
+
+/* Create a context for n x n systems with up to nrhs_max right-hand sides.
+ * opts may be NULL (defaults).  Allocates the device workspaces. */
+int zsolve_create(zsolve_ctx **ctx, int64_t n, int nrhs_max, const zsolve_opts *opts);
+
+/* Enqueue subsequent work on `stream` (a cudaStream_t; NULL = default stream). */
+int zsolve_set_stream(zsolve_ctx *ctx, void *stream);
+
+/* Z(omega) = j*omega*L - j*Psi/omega + Zs*G, written in float64 (kept for the
+ * residual) and rounded to complex float32 (to be factorised), in one pass
+ * over L, Psi, G (device, n x n float64).  omega > 0; zs_re + j*zs_im is
+ * Zs(omega), computed by the caller. */
+int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G,
+                    double omega, double zs_re, double zs_im);
+
+/* Unpivoted LU of the complex float32 copy of the assembled Z, in place:
+ * 32-column panels inside 128-column outer blocks, trailing update by the
+ * opts.gemm arithmetic.  Records whether a pivot was tiny or non-finite. */
+int zsolve_factor(zsolve_ctx *ctx);
+
+/* Refine x for nrhs right-hand sides b (device c128, nrhs x n) against the
+ * assembled and factored Z; x (device c128, nrhs x n) is output only.  A
+ * stalled refinement or a flagged pivot switches this call to the float64
+ * pivoted LU (info->fallback = 1).  info (host) may be NULL. */
+int zsolve_refine(zsolve_ctx *ctx, const void *b, void *x, int nrhs, zsolve_info *info);
+
+/* The whole sweep: for each of nf frequencies omega[f] (host array) with
+ * surface impedance zs[2f] + j*zs[2f+1] (host array), assemble, factor and
+ * refine.  b (device c128, nrhs x n) is shared by all frequencies; x (device
+ * c128, nf x nrhs x n) receives the solutions; info (host, nf entries) may be
+ * NULL.  Frequencies are processed opts.batch at a time.  Returns the first
+ * error; a frequency that needed the fallback is not an error. */
+int zsolve_sweep(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G,
+                 const double *omega, const double *zs, int nf, const void *b, void *x,
+                 int nrhs, zsolve_info *info);
+
+/* zsolve_sweep with HOST pointers for L, Psi, G, b and x: copies the inputs
+ * to context-owned device buffers, sweeps, and copies the solutions back.
+ * Pinned host memory gives overlapped, full-speed copies. */
+int zsolve_sweep_host(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G,
+                      const double *omega, const double *zs, int nf, const void *b, void *x,
+                      int nrhs, zsolve_info *info);
+
+/* ---- stage-level calls on the single system of zsolve_assemble/factor ---- */
+
+/* r = b - Z x with the float64 Z (step 3).  b, x, r: device c128, nrhs x n. */
+int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int nrhs);
+
+/* d = (L U)^-1 v with the low-precision factors (steps 2 and 4): v is
+ * rounded to complex float32, solved in float32, and d returned as c128.
+ * v, d: device c128, nrhs x n. */
+int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs);
+
+/* x = Z^-1 b by the float64 LU with partial pivoting of the assembled Z (the
+ * fallback on its own).  b, x: device c128, nrhs x n. */
+int zsolve_fallback_solve(zsolve_ctx *ctx, const void *b, void *x, int nrhs);
+
+/* Copy the float64 Z (device c128, n x n) of the single system to dst. */
+int zsolve_get_z64(zsolve_ctx *ctx, void *dst);
+
+/* Copy the complex float32 matrix of the single system -- Z after
+ * zsolve_assemble, the packed L\U factors after zsolve_factor -- into the
+ * device float planes re and im (n x n each, row-major). */
+int zsolve_get_z32(zsolve_ctx *ctx, float *re, float *im);
+
+/* Tiny or non-finite pivot seen by the last zsolve_factor (0 or 1) in *flag. */
+int zsolve_pivot_flag(zsolve_ctx *ctx, int *flag);
+
+/* Static string for a status code. */
+const char *zsolve_strerror(int status);
+
+/* Message of the last failure in this context ("" if none). */
+const char *zsolve_last_error(const zsolve_ctx *ctx);
+
+/* Release every workspace.  NULL is allowed. */
+void zsolve_destroy(zsolve_ctx *ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZSOLVE_H */

@@ -1,0 +1,143 @@
+// Shared device helpers and launcher declarations for the zsolve kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define ZS_NB 128           // outer block: columns factored per step of the blocked LU
+#define ZS_PANEL 32         // panel width inside the outer block ("LU in blocks of 32")
+#define ZS_TB 64            // row block of the triangular solves
+#define ZS_SPIN_LIMIT (1u << 26)  // bounded waits: iterations before a wait gives up
+
+// device status bits (one word per context)
+#define ZS_DEV_TIMEOUT 1u
+
+namespace zs {
+
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
+struct cf {  // complex float
+    float re, im;
+};
+
+__device__ __forceinline__ cf cmul(cf a, cf b) {
+    return {a.re * b.re - a.im * b.im, a.re * b.im + a.im * b.re};
+}
+
+// a - b*c
+__device__ __forceinline__ cf cfms(cf a, cf b, cf c) {
+    return {fmaf(-b.re, c.re, fmaf(b.im, c.im, a.re)), fmaf(-b.re, c.im, fmaf(-b.im, c.re, a.im))};
+}
+
+// 1/p with a scale to keep the squared modulus in range
+__device__ __forceinline__ cf crecip(cf p) {
+    float s = fmaxf(fabsf(p.re), fabsf(p.im));
+    float a = p.re / s, b = p.im / s;
+    float d = s * (a * a + b * b);
+    return {a / d, -b / d};
+}
+
+__device__ __forceinline__ bool cfinite(cf a) { return isfinite(a.re) && isfinite(a.im); }
+
+// Bounded wait until *flag == want.  Returns false (and raises the timeout bit
+// in *status) if it never happens within ZS_SPIN_LIMIT polls.
+__device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned want, unsigned *status) {
+    unsigned it = 0;
+    while (true) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v == want) return true;
+        if (++it > ZS_SPIN_LIMIT) {
+            atomicOr(status, ZS_DEV_TIMEOUT);
+            return false;
+        }
+        // another wait already gave up: stop too, so the launch ends promptly
+        if ((it & 1023u) == 0 && (*(volatile const unsigned *)status & ZS_DEV_TIMEOUT)) return false;
+        if (it > 64) __nanosleep(64);
+    }
+}
+
+__device__ __forceinline__ void set_flag(unsigned *flag, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ bool timed_out(const unsigned *status) {
+    return (*(volatile const unsigned *)status & ZS_DEV_TIMEOUT) != 0;
+}
+
+}  // namespace zs
+
+// Per-slot parameters of a batch (one slot = one frequency being solved).
+struct ZsSlotParam {
+    double omega, zs_re, zs_im, pad;
+};
+
+// ---------------------------------------------------------------- launchers
+// All return cudaGetLastError() of the launch.  Matrices of a batch are
+// strided by the given slot strides (elements).
+
+// Z64 (c128, ld n) and the complex float32 planes (re at z32, im at z32 + plane).
+cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n,
+                               const ZsSlotParam *params, int nslot, double2 *z64, int64_t z64_stride,
+                               float *z32, int64_t ld, int64_t plane, int64_t z32_stride,
+                               cudaStream_t st);
+
+// Factorisation steps at outer-block column J for nslot slots listed in slots[].
+cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                              int64_t J, int nb, const int *slots, int nslot, int *pivflag,
+                              cudaStream_t st);
+// mode: 0 = pack plain fp32 (FFMA), 1 = tf32 rounded (TF32), 2 = tf32 hi + lo (TF32X3)
+cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
+                             int nslot, cudaStream_t st);
+cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
+                             int nslot, cudaStream_t st);
+cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                                 int64_t J, const float *pack, int64_t pack_stride, const int *slots,
+                                 int nslot, cudaStream_t st);
+
+// Pack layout (floats), per slot: six planes of n rows x 2*NB:
+//   A_hi, A_lo, Br_hi, Br_lo, Bi_hi, Bi_lo
+// A row i   = [Re L21(i,:) | Im L21(i,:)]
+// Br row j  = [Re U12(:,j) | -Im U12(:,j)]   (Cr = A . Br)
+// Bi row j  = [Im U12(:,j) |  Re U12(:,j)]   (Ci = A . Bi)
+#define ZS_PACK_K (2 * ZS_NB)
+__host__ __device__ inline int64_t zs_pack_plane(int64_t n) { return n * (int64_t)ZS_PACK_K; }
+
+// Triangular solves with the float32 factors: v (c64 interleaved, per active
+// slot nrhs rows of n) is overwritten by (LU)^-1 v.
+cudaError_t zs_launch_trsv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                           float2 *v, int64_t v_stride, int nrhs, const int *slots, int nslot,
+                           unsigned *flags, int64_t flags_stride, unsigned epoch, unsigned *ticket,
+                           unsigned *status, int num_sms, cudaStream_t st);
+
+// r = b - Z64 x.  out_c64 != NULL: writes float2 (rounded); else writes c128 to out_c128.
+cudaError_t zs_launch_residual(const double2 *z64, int64_t z64_stride, int64_t n, const double2 *b,
+                               const double2 *x, int64_t x_stride, int nrhs, float2 *out_c64,
+                               int64_t out64_stride, double2 *out_c128, int64_t out128_stride,
+                               const int *slots, int nslot, cudaStream_t st);
+
+// v = (float2) b for every listed slot
+cudaError_t zs_launch_cast_rhs(const double2 *b, int64_t n, int nrhs, float2 *v, int64_t v_stride,
+                               const int *slots, int nslot, cudaStream_t st);
+
+// x = d (assign) or x += d; partial sums of |d|^2 and |x|^2 per (slot, rhs, chunk)
+cudaError_t zs_launch_update(double2 *x, int64_t x_stride, const float2 *d, int64_t d_stride,
+                             int64_t n, int nrhs, int assign, double *partials, int nchunks,
+                             const int *slots, int nslot, cudaStream_t st);
+// relcorr[slot*nrhs + r] = sqrt(sum|d|^2 / sum|x|^2) (inf/nan if non-finite)
+cudaError_t zs_launch_relcorr(const double *partials, int nchunks, int nrhs, double *relcorr,
+                              const int *slots, int nslot, cudaStream_t st);
+int zs_update_chunks(int64_t n);
+
+// d (c128) from v (c64) for the stage-level solve call
+cudaError_t zs_launch_widen(const float2 *v, double2 *d, int64_t count, cudaStream_t st);
+cudaError_t zs_launch_narrow(const double2 *d, float2 *v, int64_t count, cudaStream_t st);
+cudaError_t zs_launch_copy_z32_out(const float *z32, int64_t ld, int64_t plane, int64_t n, float *re,
+                                   float *im, cudaStream_t st);
+
+// float64 LU with partial pivoting (the fallback) on a c128 matrix with ld n.
+cudaError_t zs_lu64_factor(double2 *a, int64_t n, int64_t *piv, int *info, cudaStream_t st);
+cudaError_t zs_lu64_solve(const double2 *lu, int64_t n, const int64_t *piv, double2 *x, int nrhs,
+                          cudaStream_t st);

@@ -1,0 +1,495 @@
+// Low-precision unpivoted blocked LU of the complex float32 matrix
+// (malusrfworks.com, "Solving Dense Matrices Fast in the Browser", section
+// "Double-precision answers from a GPU without double precision", step 1:
+// single-precision factorisation on the GPU, LU in blocks of 32; the same
+// paragraph states that it does not pivot).
+//
+// The host walks the matrix in outer blocks of ZS_NB = 128 columns.  At
+// outer column J:
+//   k_diag_lu   factors the 128 x 128 diagonal block in shared memory, one
+//               32-column panel at a time: panel factor (rows held in
+//               registers, the multiplier broadcast by warp shuffle), the
+//               panel's row block of U, and the block's own trailing update;
+//   k_trsm_l    L21 = A21 U11^-1, one row per warp (row-oriented solve);
+//   k_trsm_u    U12 = L11^-1 A12, one column per warp;
+//   k_schur_*   A22 -= L21 U12 (this file: FP32 FFMA; schur_tc.cu: tcgen05).
+// k_trsm_l / k_trsm_u also write L21 and U12 as K-major operand packs for
+// the trailing update: A = [Re L21 | Im L21], Br = [Re U12^T | -Im U12^T],
+// Bi = [Im U12^T | Re U12^T], so that Re(L21 U12) = A Br^T and
+// Im(L21 U12) = A Bi^T are plain real products with K = 2*128.
+#include "common.cuh"
+
+namespace {
+
+using zs::cf;
+
+constexpr int NB = ZS_NB;
+constexpr int P = ZS_PANEL;
+constexpr int LDS = NB + 1;  // padded shared row
+
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// Write one float of an operand pack in the requested arithmetic mode.
+__device__ __forceinline__ void pack_put(float *hi, float *lo, int64_t off, float v, int mode) {
+    if (mode == 0) {
+        hi[off] = v;
+    } else if (mode == 1) {
+        hi[off] = tf32_rna(v);
+    } else {
+        float h = tf32_rna(v);
+        hi[off] = h;
+        lo[off] = tf32_rna(v - h);
+    }
+}
+
+// ---------------------------------------------------------------- diagonal block
+
+constexpr int kDiagThreads = 512;  // 16 warps
+
+__global__ void __launch_bounds__(kDiagThreads, 1)
+k_diag_lu(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
+          const int *__restrict__ slots, int *__restrict__ pivflag) {
+    extern __shared__ float sm[];
+    float *sre = sm;                   // [NB][LDS]
+    float *sim = sm + NB * LDS;        // [NB][LDS]
+    float *prow = sm + 2 * NB * LDS;   // [2][2][P]: double-buffered pivot row (re, im)
+    __shared__ unsigned s_amax;
+    const int slot = slots[blockIdx.x];
+    float *re = z32 + (int64_t)slot * z32_stride;
+    float *im = re + plane;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) s_amax = 0u;
+    __syncthreads();
+    float amax = 0.f;
+    for (int idx = tid; idx < nb * nb; idx += kDiagThreads) {
+        int i = idx / nb, j = idx - i * nb;
+        int64_t g = (J + i) * ld + J + j;
+        float a = re[g], b = im[g];
+        sre[i * LDS + j] = a;
+        sim[i * LDS + j] = b;
+        amax = fmaxf(amax, fabsf(a) + fabsf(b));
+    }
+    if (!(amax <= 3.0e38f)) amax = 3.0e38f;  // non-finite inputs: the pivot test flags them
+    atomicMax(&s_amax, __float_as_uint(amax));
+    __syncthreads();
+    const float tiny = 1e-30f * __uint_as_float(s_amax);
+    bool flagged = false;
+
+    for (int p = 0; p < nb; p += P) {
+        const int pw = min(P, nb - p);
+        // -- panel factor: rows p..nb-1, columns p..p+pw-1.  Warp w holds rows
+        //    p + w + 16 t in registers, lane = column.
+        cf a[NB / 16];
+#pragma unroll
+        for (int t = 0; t < NB / 16; t++) {
+            int r = p + warp + 16 * t;
+            a[t] = (r < nb && lane < pw) ? cf{sre[r * LDS + p + lane], sim[r * LDS + p + lane]}
+                                         : cf{0.f, 0.f};
+        }
+        for (int k = 0; k < pw; k++) {
+            const int kk = p + k;
+            float *pr = prow + (k & 1) * 2 * P;
+            if (warp == (k & 15)) {  // owner of row kk publishes it
+                const int t = k >> 4;
+                cf v = a[0];
+#pragma unroll
+                for (int q = 0; q < NB / 16; q++)
+                    if (q == t) v = a[q];
+                pr[lane] = v.re;
+                pr[P + lane] = v.im;
+            }
+            __syncthreads();
+            const cf piv = {pr[k], pr[P + k]};
+            const cf inv = zs::crecip(piv);
+            if (tid == 0 && (!zs::cfinite(piv) || fabsf(piv.re) + fabsf(piv.im) <= tiny))
+                flagged = true;
+            const cf u = (lane < pw) ? cf{pr[lane], pr[P + lane]} : cf{0.f, 0.f};
+#pragma unroll
+            for (int t = 0; t < NB / 16; t++) {
+                const int r = p + warp + 16 * t;
+                if (r > kk && r < nb) {  // warp-uniform condition
+                    cf l;
+                    l.re = __shfl_sync(0xffffffffu, a[t].re, k);
+                    l.im = __shfl_sync(0xffffffffu, a[t].im, k);
+                    l = zs::cmul(l, inv);
+                    if (lane == k) a[t] = l;
+                    else if (lane > k && lane < pw) a[t] = zs::cfms(a[t], l, u);
+                }
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < NB / 16; t++) {
+            int r = p + warp + 16 * t;
+            if (r < nb && lane < pw) {
+                sre[r * LDS + p + lane] = a[t].re;
+                sim[r * LDS + p + lane] = a[t].im;
+            }
+        }
+        __syncthreads();
+        const int c0 = p + pw;
+        if (c0 >= nb) break;
+        // -- row block of U inside the diagonal block: rows p..p+pw-1, columns
+        //    c0..nb-1.  Warp per column, lane = row; unit-lower panel L11.
+        for (int c = c0 + warp; c < nb; c += 16) {
+            cf v = (lane < pw) ? cf{sre[(p + lane) * LDS + c], sim[(p + lane) * LDS + c]} : cf{0.f, 0.f};
+            for (int k = 0; k < pw - 1; k++) {
+                cf uk;
+                uk.re = __shfl_sync(0xffffffffu, v.re, k);
+                uk.im = __shfl_sync(0xffffffffu, v.im, k);
+                if (lane > k && lane < pw) {
+                    cf l = {sre[(p + lane) * LDS + p + k], sim[(p + lane) * LDS + p + k]};
+                    v = zs::cfms(v, l, uk);
+                }
+            }
+            if (lane < pw) {
+                sre[(p + lane) * LDS + c] = v.re;
+                sim[(p + lane) * LDS + c] = v.im;
+            }
+        }
+        __syncthreads();
+        // -- trailing update of the diagonal block: rows/cols c0..nb-1, K = pw,
+        //    4x4 register tiles.
+        const int m = nb - c0;
+        const int tiles_1d = (m + 3) / 4;
+        for (int tix = tid; tix < tiles_1d * tiles_1d; tix += kDiagThreads) {
+            const int ti = tix / tiles_1d, tj = tix - ti * tiles_1d;
+            const int i0 = c0 + 4 * ti, j0 = c0 + 4 * tj;
+            cf acc[4][4];
+#pragma unroll
+            for (int x = 0; x < 4; x++)
+#pragma unroll
+                for (int y = 0; y < 4; y++) acc[x][y] = cf{0.f, 0.f};
+            for (int k = 0; k < pw; k++) {
+                cf lv[4], uv[4];
+#pragma unroll
+                for (int x = 0; x < 4; x++) {
+                    int i = min(i0 + x, nb - 1);
+                    lv[x] = cf{sre[i * LDS + p + k], sim[i * LDS + p + k]};
+                    int j = min(j0 + x, nb - 1);
+                    uv[x] = cf{sre[(p + k) * LDS + j], sim[(p + k) * LDS + j]};
+                }
+#pragma unroll
+                for (int x = 0; x < 4; x++)
+#pragma unroll
+                    for (int y = 0; y < 4; y++) {
+                        acc[x][y].re = fmaf(lv[x].re, uv[y].re, fmaf(-lv[x].im, uv[y].im, acc[x][y].re));
+                        acc[x][y].im = fmaf(lv[x].re, uv[y].im, fmaf(lv[x].im, uv[y].re, acc[x][y].im));
+                    }
+            }
+#pragma unroll
+            for (int x = 0; x < 4; x++)
+#pragma unroll
+                for (int y = 0; y < 4; y++) {
+                    int i = i0 + x, j = j0 + y;
+                    if (i < nb && j < nb) {
+                        sre[i * LDS + j] -= acc[x][y].re;
+                        sim[i * LDS + j] -= acc[x][y].im;
+                    }
+                }
+        }
+        __syncthreads();
+    }
+    for (int idx = tid; idx < nb * nb; idx += kDiagThreads) {
+        int i = idx / nb, j = idx - i * nb;
+        int64_t g = (J + i) * ld + J + j;
+        re[g] = sre[i * LDS + j];
+        im[g] = sim[i * LDS + j];
+    }
+    if (tid == 0 && flagged) pivflag[slot] = 1;
+}
+
+// ---------------------------------------------------------------- L21 = A21 U11^-1
+
+constexpr int kTrsmThreads = 512;  // 16 warps
+constexpr int kTrsmLRows = 64;     // rows per CTA
+
+__global__ void __launch_bounds__(kTrsmThreads, 1)
+k_trsm_l(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
+         float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
+    extern __shared__ float sm[];
+    float *ure = sm;                // [NB][NB] upper factor, row k contiguous
+    float *uim = sm + NB * NB;
+    float *rinv = sm + 2 * NB * NB;  // [2][NB] reciprocals of the diagonal
+    const int slot = slots[blockIdx.y];
+    float *re = z32 + (int64_t)slot * z32_stride;
+    float *im = re + plane;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int idx = tid; idx < NB * NB; idx += kTrsmThreads) {
+        int i = idx / NB, j = idx - i * NB;
+        int64_t g = (J + i) * ld + J + j;
+        ure[idx] = (j >= i) ? re[g] : 0.f;
+        uim[idx] = (j >= i) ? im[g] : 0.f;
+    }
+    __syncthreads();
+    if (tid < NB) {
+        cf r = zs::crecip(cf{ure[tid * NB + tid], uim[tid * NB + tid]});
+        rinv[tid] = r.re;
+        rinv[NB + tid] = r.im;
+    }
+    __syncthreads();
+    float *pA_hi = pack + (int64_t)slot * pack_stride;
+    float *pA_lo = pA_hi + zs_pack_plane(n);
+    const int64_t row0 = J + NB + (int64_t)blockIdx.x * kTrsmLRows;
+    for (int rr = warp; rr < kTrsmLRows; rr += 16) {
+        const int64_t r = row0 + rr;
+        if (r >= n) break;
+        cf v[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) v[q] = cf{re[r * ld + J + lane + 32 * q], im[r * ld + J + lane + 32 * q]};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            for (int kl = 0; kl < 32; kl++) {
+                const int k = 32 * q + kl;
+                cf x;
+                x.re = __shfl_sync(0xffffffffu, v[q].re, kl);
+                x.im = __shfl_sync(0xffffffffu, v[q].im, kl);
+                x = zs::cmul(x, cf{rinv[k], rinv[NB + k]});
+                if (lane == kl) v[q] = x;
+#pragma unroll
+                for (int q2 = q; q2 < 4; q2++) {
+                    const int j = lane + 32 * q2;
+                    if (j > k) v[q2] = zs::cfms(v[q2], x, cf{ure[k * NB + j], uim[k * NB + j]});
+                }
+            }
+        }
+        float *ah = pA_hi + r * ZS_PACK_K, *al = pA_lo + r * ZS_PACK_K;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int c = lane + 32 * q;
+            re[r * ld + J + c] = v[q].re;
+            im[r * ld + J + c] = v[q].im;
+            pack_put(ah, al, c, v[q].re, mode);
+            pack_put(ah, al, NB + c, v[q].im, mode);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- U12 = L11^-1 A12
+
+constexpr int kTrsmUCols = 32;  // columns per CTA
+
+__global__ void __launch_bounds__(kTrsmThreads, 1)
+k_trsm_u(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
+         float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
+    extern __shared__ float sm[];
+    float *lre = sm;                 // [NB][LDS] strictly lower factor, column access
+    float *lim = sm + NB * LDS;
+    float *tre = sm + 2 * NB * LDS;  // [NB][33] tile of A12
+    float *tim = tre + NB * 33;
+    const int slot = slots[blockIdx.y];
+    float *re = z32 + (int64_t)slot * z32_stride;
+    float *im = re + plane;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t c0 = J + NB + (int64_t)blockIdx.x * kTrsmUCols;
+    const int ncol = (int)zs::min64(kTrsmUCols, n - c0);
+    for (int idx = tid; idx < NB * NB; idx += kTrsmThreads) {
+        int i = idx / NB, j = idx - i * NB;
+        int64_t g = (J + i) * ld + J + j;
+        lre[i * LDS + j] = (i > j) ? re[g] : 0.f;
+        lim[i * LDS + j] = (i > j) ? im[g] : 0.f;
+    }
+    for (int idx = tid; idx < NB * kTrsmUCols; idx += kTrsmThreads) {
+        int i = idx >> 5, c = idx & 31;
+        if (c < ncol) {
+            int64_t g = (J + i) * ld + c0 + c;
+            tre[i * 33 + c] = re[g];
+            tim[i * 33 + c] = im[g];
+        }
+    }
+    __syncthreads();
+    float *pBr_hi = pack + (int64_t)slot * pack_stride + 2 * zs_pack_plane(n);
+    float *pBr_lo = pBr_hi + zs_pack_plane(n);
+    float *pBi_hi = pBr_hi + 2 * zs_pack_plane(n);
+    float *pBi_lo = pBr_hi + 3 * zs_pack_plane(n);
+    for (int c = warp; c < ncol; c += 16) {
+        cf v[4];
+#pragma unroll
+        for (int q = 0; q < 4; q++) v[q] = cf{tre[(lane + 32 * q) * 33 + c], tim[(lane + 32 * q) * 33 + c]};
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            for (int kl = 0; kl < 32; kl++) {
+                const int k = 32 * q + kl;
+                cf u;
+                u.re = __shfl_sync(0xffffffffu, v[q].re, kl);
+                u.im = __shfl_sync(0xffffffffu, v[q].im, kl);
+#pragma unroll
+                for (int q2 = q; q2 < 4; q2++) {
+                    const int i = lane + 32 * q2;
+                    if (i > k) v[q2] = zs::cfms(v[q2], cf{lre[i * LDS + k], lim[i * LDS + k]}, u);
+                }
+            }
+        }
+        const int64_t j = c0 + c;
+        float *brh = pBr_hi + j * ZS_PACK_K, *brl = pBr_lo + j * ZS_PACK_K;
+        float *bih = pBi_hi + j * ZS_PACK_K, *bil = pBi_lo + j * ZS_PACK_K;
+#pragma unroll
+        for (int q = 0; q < 4; q++) {
+            const int i = lane + 32 * q;
+            tre[i * 33 + c] = v[q].re;
+            tim[i * 33 + c] = v[q].im;
+            pack_put(brh, brl, i, v[q].re, mode);
+            pack_put(brh, brl, NB + i, -v[q].im, mode);
+            pack_put(bih, bil, i, v[q].im, mode);
+            pack_put(bih, bil, NB + i, v[q].re, mode);
+        }
+    }
+    __syncthreads();
+    for (int idx = tid; idx < NB * kTrsmUCols; idx += kTrsmThreads) {
+        int i = idx >> 5, c = idx & 31;
+        if (c < ncol) {
+            int64_t g = (J + i) * ld + c0 + c;
+            re[g] = tre[i * 33 + c];
+            im[g] = tim[i * 33 + c];
+        }
+    }
+}
+
+// ---------------------------------------------------------------- SIMT trailing update
+
+constexpr int kST = 64;        // output tile (complex entries per side)
+constexpr int kSK = 32;        // K chunk (real, of the 2*NB packed K)
+constexpr int kSPad = kST + 4;
+
+__global__ void __launch_bounds__(256)
+k_schur_simt(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
+             const float *__restrict__ pack, int64_t pack_stride, const int *__restrict__ slots) {
+    __shared__ __align__(16) float As[kSK][kSPad];
+    __shared__ __align__(16) float Brs[kSK][kSPad];
+    __shared__ __align__(16) float Bis[kSK][kSPad];
+    const int slot = slots[blockIdx.z];
+    const int64_t base = J + NB;
+    const int64_t i0 = base + (int64_t)blockIdx.y * kST, j0 = base + (int64_t)blockIdx.x * kST;
+    const float *pA = pack + (int64_t)slot * pack_stride;
+    const float *pBr = pA + 2 * zs_pack_plane(n);
+    const float *pBi = pA + 4 * zs_pack_plane(n);
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    float accr[4][4], acci[4][4];
+#pragma unroll
+    for (int x = 0; x < 4; x++)
+#pragma unroll
+        for (int y = 0; y < 4; y++) accr[x][y] = acci[x][y] = 0.f;
+    const int lr = tid >> 2, lk = (tid & 3) * 8;  // loader: row lr, k lk..lk+7
+    const int64_t ar = zs::min64(i0 + lr, n - 1), br = zs::min64(j0 + lr, n - 1);
+    for (int kc = 0; kc < ZS_PACK_K; kc += kSK) {
+        const float4 *a4 = reinterpret_cast<const float4 *>(pA + ar * ZS_PACK_K + kc + lk);
+        const float4 *r4 = reinterpret_cast<const float4 *>(pBr + br * ZS_PACK_K + kc + lk);
+        const float4 *m4 = reinterpret_cast<const float4 *>(pBi + br * ZS_PACK_K + kc + lk);
+        float4 av[2] = {a4[0], a4[1]}, rv[2] = {r4[0], r4[1]}, mv[2] = {m4[0], m4[1]};
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < 2; h++) {
+            As[lk + 4 * h + 0][lr] = av[h].x;
+            As[lk + 4 * h + 1][lr] = av[h].y;
+            As[lk + 4 * h + 2][lr] = av[h].z;
+            As[lk + 4 * h + 3][lr] = av[h].w;
+            Brs[lk + 4 * h + 0][lr] = rv[h].x;
+            Brs[lk + 4 * h + 1][lr] = rv[h].y;
+            Brs[lk + 4 * h + 2][lr] = rv[h].z;
+            Brs[lk + 4 * h + 3][lr] = rv[h].w;
+            Bis[lk + 4 * h + 0][lr] = mv[h].x;
+            Bis[lk + 4 * h + 1][lr] = mv[h].y;
+            Bis[lk + 4 * h + 2][lr] = mv[h].z;
+            Bis[lk + 4 * h + 3][lr] = mv[h].w;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int k = 0; k < kSK; k++) {
+            float4 a = *reinterpret_cast<const float4 *>(&As[k][ty * 4]);
+            float4 b = *reinterpret_cast<const float4 *>(&Brs[k][tx * 4]);
+            float4 c = *reinterpret_cast<const float4 *>(&Bis[k][tx * 4]);
+            float av4[4] = {a.x, a.y, a.z, a.w}, bv4[4] = {b.x, b.y, b.z, b.w}, cv4[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+            for (int x = 0; x < 4; x++)
+#pragma unroll
+                for (int y = 0; y < 4; y++) {
+                    accr[x][y] = fmaf(av4[x], bv4[y], accr[x][y]);
+                    acci[x][y] = fmaf(av4[x], cv4[y], acci[x][y]);
+                }
+        }
+    }
+    float *re = z32 + (int64_t)slot * z32_stride;
+    float *im = re + plane;
+#pragma unroll
+    for (int x = 0; x < 4; x++) {
+        const int64_t i = i0 + ty * 4 + x;
+        if (i >= n) continue;
+#pragma unroll
+        for (int y = 0; y < 4; y++) {
+            const int64_t j = j0 + tx * 4 + y;
+            if (j < n) {
+                re[i * ld + j] -= accr[x][y];
+                im[i * ld + j] -= acci[x][y];
+            }
+        }
+    }
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+}  // namespace
+
+cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                              int64_t J, int nb, const int *slots, int nslot, int *pivflag,
+                              cudaStream_t st) {
+    (void)n;
+    const size_t smem = (2 * NB * LDS + 4 * P) * sizeof(float);
+    static bool init = false;
+    if (!init) {
+        cudaError_t e = set_smem(k_diag_lu, smem);
+        if (e != cudaSuccess) return e;
+        init = true;
+    }
+    k_diag_lu<<<nslot, kDiagThreads, smem, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag);
+    return cudaGetLastError();
+}
+
+cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
+                             int nslot, cudaStream_t st) {
+    const size_t smem = (2 * NB * NB + 2 * NB) * sizeof(float);
+    static bool init = false;
+    if (!init) {
+        cudaError_t e = set_smem(k_trsm_l, smem);
+        if (e != cudaSuccess) return e;
+        init = true;
+    }
+    const int64_t m2 = n - J - NB;
+    dim3 grid((unsigned)((m2 + kTrsmLRows - 1) / kTrsmLRows), nslot);
+    k_trsm_l<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode,
+                                                slots);
+    return cudaGetLastError();
+}
+
+cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
+                             int nslot, cudaStream_t st) {
+    const size_t smem = (2 * NB * LDS + 2 * NB * 33) * sizeof(float);
+    static bool init = false;
+    if (!init) {
+        cudaError_t e = set_smem(k_trsm_u, smem);
+        if (e != cudaSuccess) return e;
+        init = true;
+    }
+    const int64_t m2 = n - J - NB;
+    dim3 grid((unsigned)((m2 + kTrsmUCols - 1) / kTrsmUCols), nslot);
+    k_trsm_u<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode,
+                                                slots);
+    return cudaGetLastError();
+}
+
+cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                                 int64_t J, const float *pack, int64_t pack_stride, const int *slots,
+                                 int nslot, cudaStream_t st) {
+    const int64_t m2 = n - J - NB;
+    const unsigned t = (unsigned)((m2 + kST - 1) / kST);
+    dim3 grid(t, t, nslot);
+    k_schur_simt<<<grid, 256, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, slots);
+    return cudaGetLastError();
+}

@@ -1,0 +1,627 @@
+// C-ABI of the frequency-sweep solver: context, workspaces, the blocked
+// factorisation loop, the refinement loop with its convergence and stall
+// tests, the fallback trigger and the batched sweep.  See include/zsolve.h
+// for the contract of every entry point.
+//
+// Method (malusrfworks.com, "Solving Dense Matrices Fast in the Browser",
+// section "Double-precision answers from a GPU without double precision"):
+// factorise in low precision (step 1), solve for x (step 2), form the
+// residual in double precision (step 3), solve for a correction with the
+// low-precision factors and add it (step 4), repeating steps 3-4 -- the
+// page's "go back to step 2" is read as returning to the residual, since the
+// first solve happens once -- until the relative correction is below tol.
+// A frequency whose refinement does not converge is solved alone by the
+// double-precision pivoted LU (same section, paragraph after the steps).
+//
+// A sweep factors `batch` frequencies together: every launch of the
+// factorisation, the solves and the residual covers all of them, so the
+// panel and triangular-solve latencies of one frequency overlap with the
+// work of the others.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "../../include/zsolve.h"
+#include "common.cuh"
+
+cudaError_t zs_launch_schur_tc(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                               int64_t J, const float *pack, int64_t pack_stride, int split,
+                               const int *slots, int nslot, cudaStream_t st);
+
+struct zsolve_ctx {
+    int64_t n = 0;
+    int nrhs_max = 0;
+    zsolve_opts opts{};
+    int device = 0, num_sms = 0;
+    cudaStream_t stream = nullptr;
+    int S = 1;  // frequencies held at once
+    int64_t ld = 0, plane = 0, z32_stride = 0, z64_stride = 0, pack_stride = 0, v_stride = 0;
+    double2 *z64 = nullptr;
+    float *z32 = nullptr;
+    float *pack = nullptr;
+    float2 *v = nullptr;
+    double *partials = nullptr;
+    int nchunks = 0;
+    double *d_relcorr = nullptr, *h_relcorr = nullptr;
+    ZsSlotParam *d_params = nullptr, *h_params = nullptr;
+    int *d_all = nullptr;    // 0..S-1
+    int *d_active = nullptr, *h_active = nullptr;
+    int *d_pivflag = nullptr, *h_pivflag = nullptr;
+    unsigned *flags = nullptr;
+    int64_t flags_stride = 0;
+    unsigned epoch = 0;
+    unsigned *ticket = nullptr;
+    unsigned *d_status = nullptr, *h_status = nullptr;
+    // fallback workspace (allocated on first use)
+    double2 *fb_a = nullptr;
+    int64_t *fb_piv = nullptr;
+    int *fb_info = nullptr, *h_fb_info = nullptr;
+    // device copies for the host-pointer sweep (allocated on first use)
+    double *hd_L = nullptr, *hd_Psi = nullptr, *hd_G = nullptr;
+    double2 *hd_b = nullptr, *hd_x = nullptr;
+    size_t hd_x_cap = 0;
+    int hd_nrhs_cap = 0;
+    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+    int assembled = 0, factored = 0, fb_ready = 0;
+    char err[512] = {0};
+};
+
+namespace {
+
+int fail(zsolve_ctx *c, int code, const char *fmt, ...) {
+    if (c) {
+        va_list ap;
+        va_start(ap, fmt);
+        vsnprintf(c->err, sizeof(c->err), fmt, ap);
+        va_end(ap);
+    }
+    return code;
+}
+
+#define ZS_CU(call)                                                                             \
+    do {                                                                                        \
+        cudaError_t e_ = (call);                                                                \
+        if (e_ != cudaSuccess)                                                                  \
+            return fail(ctx, ZSOLVE_ECUDA, "%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), \
+                        __FILE__, __LINE__);                                                    \
+    } while (0)
+
+#define ZS_TRY(expr)            \
+    do {                        \
+        int s_ = (expr);        \
+        if (s_ != ZSOLVE_OK) return s_; \
+    } while (0)
+
+int gemm_mode(const zsolve_opts &o) {
+    switch (o.gemm) {
+        case ZSOLVE_GEMM_TF32: return 1;
+        case ZSOLVE_GEMM_TF32X3: return 2;
+        default: return 0;  // FFMA and AUTO
+    }
+}
+
+size_t slot_bytes(int64_t n, int64_t ld) {
+    return (size_t)n * n * sizeof(double2) + (size_t)2 * n * ld * sizeof(float) +
+           (size_t)6 * zs_pack_plane(n) * sizeof(float);
+}
+
+// ------------------------------------------------------------------ factor
+
+int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
+    const int64_t n = ctx->n;
+    const int mode = gemm_mode(ctx->opts);
+    ZS_CU(cudaMemsetAsync(ctx->d_pivflag, 0, sizeof(int) * ctx->S, ctx->stream));
+    for (int64_t J = 0; J < n; J += ZS_NB) {
+        const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
+        ZS_CU(zs_launch_diag_lu(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, nb, slots, nslot,
+                                ctx->d_pivflag, ctx->stream));
+        if (J + nb >= n) break;
+        ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                               ctx->pack_stride, mode, slots, nslot, ctx->stream));
+        ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                               ctx->pack_stride, mode, slots, nslot, ctx->stream));
+        if (mode == 0)
+            ZS_CU(zs_launch_schur_simt(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                                       ctx->pack_stride, slots, nslot, ctx->stream));
+        else
+            ZS_CU(zs_launch_schur_tc(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                                     ctx->pack_stride, mode == 2 ? 1 : 0, slots, nslot, ctx->stream));
+    }
+    return ZSOLVE_OK;
+}
+
+// ------------------------------------------------------------------ solves
+
+// v <- (LU)^-1 v for the listed slots, right-hand sides in chunks of 8/4/2/1
+int lowprec_solve_slots(zsolve_ctx *ctx, int nrhs, const int *slots, int nslot) {
+    int r0 = 0;
+    while (r0 < nrhs) {
+        const int left = nrhs - r0;
+        const int R = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
+        ctx->epoch++;
+        ZS_CU(zs_launch_trsv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->v + (int64_t)r0 * ctx->n,
+                             ctx->v_stride, R, slots, nslot, ctx->flags, ctx->flags_stride, ctx->epoch,
+                             ctx->ticket, ctx->d_status, ctx->num_sms, ctx->stream));
+        r0 += R;
+    }
+    return ZSOLVE_OK;
+}
+
+int check_device_status(zsolve_ctx *ctx) {
+    ZS_CU(cudaMemcpyAsync(ctx->h_status, ctx->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost, ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    if (*ctx->h_status & ZS_DEV_TIMEOUT) {
+        *ctx->h_status = 0;
+        ZS_CU(cudaMemsetAsync(ctx->d_status, 0, sizeof(unsigned), ctx->stream));
+        return fail(ctx, ZSOLVE_ETIMEOUT, "a device-side wait in the triangular solve gave up");
+    }
+    return ZSOLVE_OK;
+}
+
+int ensure_fallback(zsolve_ctx *ctx) {
+    if (ctx->fb_ready) return ZSOLVE_OK;
+    const int64_t n = ctx->n;
+    if (cudaMalloc(&ctx->fb_a, (size_t)n * n * sizeof(double2)) != cudaSuccess ||
+        cudaMalloc(&ctx->fb_piv, (size_t)n * sizeof(int64_t)) != cudaSuccess ||
+        cudaMalloc(&ctx->fb_info, sizeof(int)) != cudaSuccess ||
+        cudaMallocHost(&ctx->h_fb_info, sizeof(int)) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(ctx, ZSOLVE_ENOMEM, "fallback workspace allocation failed (n=%lld)", (long long)n);
+    }
+    ctx->fb_ready = 1;
+    return ZSOLVE_OK;
+}
+
+// x (nrhs x n, device) = Z64[slot]^-1 b by the float64 pivoted LU
+int fallback_slot(zsolve_ctx *ctx, int slot, const double2 *b, double2 *x, int nrhs) {
+    ZS_TRY(ensure_fallback(ctx));
+    const int64_t n = ctx->n;
+    ZS_CU(cudaMemcpyAsync(ctx->fb_a, ctx->z64 + (int64_t)slot * ctx->z64_stride, (size_t)n * n * sizeof(double2),
+                          cudaMemcpyDeviceToDevice, ctx->stream));
+    ZS_CU(zs_lu64_factor(ctx->fb_a, n, ctx->fb_piv, ctx->fb_info, ctx->stream));
+    ZS_CU(cudaMemcpyAsync(ctx->h_fb_info, ctx->fb_info, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    if (*ctx->h_fb_info != 0)
+        return fail(ctx, ZSOLVE_ESINGULAR, "double-precision LU: zero pivot column at %d", *ctx->h_fb_info - 1);
+    if (x != b)
+        ZS_CU(cudaMemcpyAsync(x, b, (size_t)nrhs * n * sizeof(double2), cudaMemcpyDeviceToDevice, ctx->stream));
+    for (int r0 = 0; r0 < nrhs; r0 += 32)
+        ZS_CU(zs_lu64_solve(ctx->fb_a, n, ctx->fb_piv, x + (int64_t)r0 * n, std::min(32, nrhs - r0), ctx->stream));
+    return ZSOLVE_OK;
+}
+
+// Refinement of slots 0..count-1 with x for slot s at x + s*x_stride.
+int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride, int nrhs, int count,
+                 zsolve_info *info) {
+    const int64_t n = ctx->n;
+    const zsolve_opts &o = ctx->opts;
+    std::vector<int> active, stalled;
+    std::vector<double> prev(count, INFINITY), last(count, 1.0);
+    std::vector<int> grow(count, 0), iters(count, 0);
+    // slots whose factorisation met a bad pivot go straight to the fallback
+    ZS_CU(cudaMemcpyAsync(ctx->h_pivflag, ctx->d_pivflag, sizeof(int) * count, cudaMemcpyDeviceToHost, ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    for (int s = 0; s < count; s++) {
+        if (info) info[s].pivot_flag = ctx->h_pivflag[s];
+        if (ctx->h_pivflag[s] || o.force_fallback) stalled.push_back(s);
+        else active.push_back(s);
+    }
+    auto upload_active = [&]() -> int {
+        for (size_t i = 0; i < active.size(); i++) ctx->h_active[i] = active[i];
+        ZS_CU(cudaMemcpyAsync(ctx->d_active, ctx->h_active, sizeof(int) * active.size(), cudaMemcpyHostToDevice,
+                              ctx->stream));
+        return ZSOLVE_OK;
+    };
+    if (!active.empty()) {
+        ZS_TRY(upload_active());
+        const int na = (int)active.size();
+        // step 2: first solve with the low-precision factors
+        ZS_CU(zs_launch_cast_rhs(b, n, nrhs, ctx->v, ctx->v_stride, ctx->d_active, na, ctx->stream));
+        ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_active, na));
+        ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 1, ctx->partials, ctx->nchunks,
+                               ctx->d_active, na, ctx->stream));
+    }
+    for (int it = 1; it <= o.max_iter && !active.empty(); it++) {
+        const int na = (int)active.size();
+        // step 3: residual in double precision, rounded for the low-precision solve
+        ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, b, x, x_stride, nrhs, ctx->v, ctx->v_stride, nullptr,
+                                 0, ctx->d_active, na, ctx->stream));
+        // step 4: correction and update
+        ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_active, na));
+        ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 0, ctx->partials, ctx->nchunks,
+                               ctx->d_active, na, ctx->stream));
+        ZS_CU(zs_launch_relcorr(ctx->partials, ctx->nchunks, nrhs, ctx->d_relcorr, ctx->d_active, na, ctx->stream));
+        ZS_CU(cudaMemcpyAsync(ctx->h_relcorr, ctx->d_relcorr, sizeof(double) * (size_t)count * nrhs,
+                              cudaMemcpyDeviceToHost, ctx->stream));
+        ZS_TRY(check_device_status(ctx));  // synchronises
+        std::vector<int> next;
+        for (int s : active) {
+            double rc = 0.0;
+            bool bad = false;
+            for (int r = 0; r < nrhs; r++) {
+                const double v = ctx->h_relcorr[(int64_t)s * nrhs + r];
+                if (!isfinite(v)) bad = true;
+                else rc = std::max(rc, v);
+            }
+            iters[s] = it;
+            last[s] = bad ? NAN : rc;
+            if (bad) {
+                stalled.push_back(s);
+                continue;
+            }
+            if (rc < o.tol) continue;  // converged
+            grow[s] = (rc > prev[s]) ? grow[s] + 1 : 0;
+            prev[s] = rc;
+            if (grow[s] >= 2) stalled.push_back(s);  // diverging
+            else next.push_back(s);
+        }
+        active.swap(next);
+        if (!active.empty() && it < o.max_iter) ZS_TRY(upload_active());
+    }
+    for (int s : active) stalled.push_back(s);  // not converged after max_iter corrections
+    std::sort(stalled.begin(), stalled.end());
+    for (int s = 0; s < count; s++)
+        if (info) {
+            info[s].iters = iters[s];
+            info[s].relcorr = last[s];
+            info[s].fallback = 0;
+            info[s].status = ZSOLVE_OK;
+        }
+    for (int s : stalled) {
+        int st = fallback_slot(ctx, s, b, x + (int64_t)s * x_stride, nrhs);
+        if (info) {
+            info[s].fallback = 1;
+            info[s].status = st;
+            info[s].relcorr = 0.0;
+        }
+        if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
+        if (st == ZSOLVE_ESINGULAR && !info) return st;
+    }
+    return ZSOLVE_OK;
+}
+
+int check_nrhs(zsolve_ctx *ctx, int nrhs) {
+    if (nrhs < 1 || nrhs > ctx->nrhs_max)
+        return fail(ctx, ZSOLVE_EINVAL, "nrhs=%d outside 1..%d", nrhs, ctx->nrhs_max);
+    return ZSOLVE_OK;
+}
+
+int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const double *omega,
+               const double *zs, int nf, const double2 *b, double2 *x, int nrhs, zsolve_info *info) {
+    const int64_t n = ctx->n;
+    for (int f = 0; f < nf; f++)
+        if (!(omega[f] > 0.0) || !isfinite(omega[f]) || !isfinite(zs[2 * f]) || !isfinite(zs[2 * f + 1]))
+            return fail(ctx, ZSOLVE_EINVAL, "frequency %d: omega must be positive and finite, Zs finite", f);
+    int first_err = ZSOLVE_OK;
+    for (int f0 = 0; f0 < nf; f0 += ctx->S) {
+        const int count = std::min(ctx->S, nf - f0);
+        for (int s = 0; s < count; s++) ctx->h_params[s] = ZsSlotParam{omega[f0 + s], zs[2 * (f0 + s)], zs[2 * (f0 + s) + 1], 0.0};
+        ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam) * count, cudaMemcpyHostToDevice,
+                              ctx->stream));
+        ZS_CU(cudaEventRecord(ctx->ev[0], ctx->stream));
+        ZS_CU(zs_launch_assemble(L, Psi, G, n, ctx->d_params, count, ctx->z64, ctx->z64_stride, ctx->z32, ctx->ld,
+                                 ctx->plane, ctx->z32_stride, ctx->stream));
+        ZS_CU(cudaEventRecord(ctx->ev[1], ctx->stream));
+        ZS_TRY(factor_slots(ctx, ctx->d_all, count));
+        ZS_CU(cudaEventRecord(ctx->ev[2], ctx->stream));
+        zsolve_info *inf = info ? info + f0 : nullptr;
+        int st = refine_batch(ctx, b, x + (int64_t)f0 * nrhs * n, (int64_t)nrhs * n, nrhs, count, inf);
+        if (st != ZSOLVE_OK && first_err == ZSOLVE_OK) first_err = st;
+        if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
+        ZS_CU(cudaEventRecord(ctx->ev[3], ctx->stream));
+        ZS_CU(cudaEventSynchronize(ctx->ev[3]));
+        if (info) {
+            float a = 0, fct = 0, r = 0;
+            cudaEventElapsedTime(&a, ctx->ev[0], ctx->ev[1]);
+            cudaEventElapsedTime(&fct, ctx->ev[1], ctx->ev[2]);
+            cudaEventElapsedTime(&r, ctx->ev[2], ctx->ev[3]);
+            for (int s = 0; s < count; s++) {
+                info[f0 + s].ms_assemble = a / count;
+                info[f0 + s].ms_factor = fct / count;
+                info[f0 + s].ms_refine = r / count;
+            }
+        }
+    }
+    ctx->assembled = 0;  // slot 0 now holds the last batch's first frequency, not a single system
+    ctx->factored = 0;
+    return first_err;
+}
+
+void free_all(zsolve_ctx *c) {
+    cudaFree(c->z64);
+    cudaFree(c->z32);
+    cudaFree(c->pack);
+    cudaFree(c->v);
+    cudaFree(c->partials);
+    cudaFree(c->d_relcorr);
+    cudaFreeHost(c->h_relcorr);
+    cudaFree(c->d_params);
+    cudaFreeHost(c->h_params);
+    cudaFree(c->d_all);
+    cudaFree(c->d_active);
+    cudaFreeHost(c->h_active);
+    cudaFree(c->d_pivflag);
+    cudaFreeHost(c->h_pivflag);
+    cudaFree(c->flags);
+    cudaFree(c->ticket);
+    cudaFree(c->d_status);
+    cudaFreeHost(c->h_status);
+    cudaFree(c->fb_a);
+    cudaFree(c->fb_piv);
+    cudaFree(c->fb_info);
+    cudaFreeHost(c->h_fb_info);
+    cudaFree(c->hd_L);
+    cudaFree(c->hd_Psi);
+    cudaFree(c->hd_G);
+    cudaFree(c->hd_b);
+    cudaFree(c->hd_x);
+    for (auto &e : c->ev)
+        if (e) cudaEventDestroy(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+int zsolve_default_opts(zsolve_opts *opts) {
+    if (!opts) return ZSOLVE_EINVAL;
+    opts->tol = 1e-11;
+    opts->max_iter = 10;
+    opts->gemm = ZSOLVE_GEMM_AUTO;
+    opts->outer_block = ZS_NB;
+    opts->batch = 0;
+    opts->force_fallback = 0;
+    return ZSOLVE_OK;
+}
+
+int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *opts) {
+    if (!out || n <= 0 || nrhs_max < 1 || nrhs_max > 64) return ZSOLVE_EINVAL;
+    *out = nullptr;
+    zsolve_ctx *ctx = new (std::nothrow) zsolve_ctx();
+    if (!ctx) return ZSOLVE_ENOMEM;
+    if (opts) ctx->opts = *opts;
+    else zsolve_default_opts(&ctx->opts);
+    if (ctx->opts.outer_block == 0) ctx->opts.outer_block = ZS_NB;
+    if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
+        ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0) {
+        delete ctx;
+        return ZSOLVE_EINVAL;
+    }
+    ctx->n = n;
+    ctx->nrhs_max = nrhs_max;
+    auto bail = [&](int code) {
+        free_all(ctx);
+        delete ctx;
+        return code;
+    };
+    if (cudaGetDevice(&ctx->device) != cudaSuccess) return bail(ZSOLVE_ECUDA);
+    cudaDeviceGetAttribute(&ctx->num_sms, cudaDevAttrMultiProcessorCount, ctx->device);
+    ctx->ld = (n + 31) / 32 * 32;
+    ctx->plane = n * ctx->ld;
+    ctx->z32_stride = 2 * ctx->plane;
+    ctx->z64_stride = n * n;
+    ctx->pack_stride = 6 * zs_pack_plane(n);
+    ctx->v_stride = (int64_t)nrhs_max * n;
+    if (ctx->opts.batch > 0) {
+        ctx->S = ctx->opts.batch;
+    } else {
+        size_t budget = (size_t)8 << 30;
+        size_t sb = slot_bytes(n, ctx->ld);
+        ctx->S = (int)std::max<size_t>(1, std::min<size_t>(32, budget / sb));
+    }
+    if (ctx->S > 64) ctx->S = 64;
+    const int S = ctx->S;
+    const int64_t nblk = (n + ZS_TB - 1) / ZS_TB;
+    ctx->flags_stride = 2 * nblk;
+    ctx->nchunks = zs_update_chunks(n);
+#define ALLOC(p, bytes) \
+    if (cudaMalloc(&(p), (bytes)) != cudaSuccess) return bail(ZSOLVE_ENOMEM)
+#define ALLOCH(p, bytes) \
+    if (cudaMallocHost(&(p), (bytes)) != cudaSuccess) return bail(ZSOLVE_ENOMEM)
+    ALLOC(ctx->z64, (size_t)S * ctx->z64_stride * sizeof(double2));
+    ALLOC(ctx->z32, (size_t)S * ctx->z32_stride * sizeof(float));
+    ALLOC(ctx->pack, (size_t)S * ctx->pack_stride * sizeof(float));
+    ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
+    ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
+    ALLOC(ctx->d_relcorr, (size_t)S * nrhs_max * sizeof(double));
+    ALLOCH(ctx->h_relcorr, (size_t)S * nrhs_max * sizeof(double));
+    ALLOC(ctx->d_params, S * sizeof(ZsSlotParam));
+    ALLOCH(ctx->h_params, S * sizeof(ZsSlotParam));
+    ALLOC(ctx->d_all, S * sizeof(int));
+    ALLOC(ctx->d_active, S * sizeof(int));
+    ALLOCH(ctx->h_active, S * sizeof(int));
+    ALLOC(ctx->d_pivflag, S * sizeof(int));
+    ALLOCH(ctx->h_pivflag, S * sizeof(int));
+    ALLOC(ctx->flags, (size_t)S * ctx->flags_stride * sizeof(unsigned));
+    ALLOC(ctx->ticket, sizeof(unsigned));
+    ALLOC(ctx->d_status, sizeof(unsigned));
+    ALLOCH(ctx->h_status, sizeof(unsigned));
+#undef ALLOC
+#undef ALLOCH
+    for (auto &e : ctx->ev)
+        if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
+    std::vector<int> all(S);
+    for (int s = 0; s < S; s++) all[s] = s;
+    if (cudaMemcpy(ctx->d_all, all.data(), S * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(ctx->flags, 0, (size_t)S * ctx->flags_stride * sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(ctx->d_status, 0, sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(ctx->d_pivflag, 0, S * sizeof(int)) != cudaSuccess ||
+        cudaMemset(ctx->z32, 0, (size_t)S * ctx->z32_stride * sizeof(float)) != cudaSuccess)
+        return bail(ZSOLVE_ECUDA);
+    *ctx->h_status = 0;
+    *out = ctx;
+    return ZSOLVE_OK;
+}
+
+int zsolve_set_stream(zsolve_ctx *ctx, void *stream) {
+    if (!ctx) return ZSOLVE_EINVAL;
+    ctx->stream = (cudaStream_t)stream;
+    return ZSOLVE_OK;
+}
+
+int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, double omega,
+                    double zs_re, double zs_im) {
+    if (!ctx || !L || !Psi || !G) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    if (!(omega > 0.0) || !isfinite(omega) || !isfinite(zs_re) || !isfinite(zs_im))
+        return fail(ctx, ZSOLVE_EINVAL, "omega must be positive and finite, Zs finite");
+    ctx->h_params[0] = ZsSlotParam{omega, zs_re, zs_im, 0.0};
+    ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
+    ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32, ctx->ld,
+                             ctx->plane, ctx->z32_stride, ctx->stream));
+    ctx->assembled = 1;
+    ctx->factored = 0;
+    return ZSOLVE_OK;
+}
+
+int zsolve_factor(zsolve_ctx *ctx) {
+    if (!ctx) return ZSOLVE_EINVAL;
+    if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_factor before zsolve_assemble");
+    if (ctx->factored) return ZSOLVE_OK;
+    ZS_TRY(factor_slots(ctx, ctx->d_all, 1));
+    ctx->factored = 1;
+    return ZSOLVE_OK;
+}
+
+int zsolve_refine(zsolve_ctx *ctx, const void *b, void *x, int nrhs, zsolve_info *info) {
+    if (!ctx || !b || !x) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "zsolve_refine before zsolve_factor");
+    zsolve_info tmp{};
+    ZS_CU(cudaEventRecord(ctx->ev[2], ctx->stream));
+    int st = refine_batch(ctx, (const double2 *)b, (double2 *)x, 0, nrhs, 1, &tmp);
+    ZS_CU(cudaEventRecord(ctx->ev[3], ctx->stream));
+    ZS_CU(cudaEventSynchronize(ctx->ev[3]));
+    cudaEventElapsedTime(&tmp.ms_refine, ctx->ev[2], ctx->ev[3]);
+    if (info) *info = tmp;
+    if (st != ZSOLVE_OK) return st;
+    return tmp.status;
+}
+
+int zsolve_sweep(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const double *omega,
+                 const double *zs, int nf, const void *b, void *x, int nrhs, zsolve_info *info) {
+    if (!ctx || !L || !Psi || !G || !omega || !zs || !b || !x || nf < 0)
+        return fail(ctx, ZSOLVE_EINVAL, "NULL argument or nf < 0");
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    return sweep_impl(ctx, L, Psi, G, omega, zs, nf, (const double2 *)b, (double2 *)x, nrhs, info);
+}
+
+int zsolve_sweep_host(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const double *omega,
+                      const double *zs, int nf, const void *b, void *x, int nrhs, zsolve_info *info) {
+    if (!ctx || !L || !Psi || !G || !omega || !zs || !b || !x || nf < 0)
+        return fail(ctx, ZSOLVE_EINVAL, "NULL argument or nf < 0");
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    const int64_t n = ctx->n;
+    const size_t mb = (size_t)n * n * sizeof(double);
+    if (!ctx->hd_L) {
+        if (cudaMalloc(&ctx->hd_L, mb) != cudaSuccess || cudaMalloc(&ctx->hd_Psi, mb) != cudaSuccess ||
+            cudaMalloc(&ctx->hd_G, mb) != cudaSuccess ||
+            cudaMalloc(&ctx->hd_b, (size_t)ctx->nrhs_max * n * sizeof(double2)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ctx, ZSOLVE_ENOMEM, "device buffers for host inputs");
+        }
+    }
+    const size_t xb = (size_t)nf * nrhs * n * sizeof(double2);
+    if (xb > ctx->hd_x_cap) {
+        cudaFree(ctx->hd_x);
+        ctx->hd_x = nullptr;
+        ctx->hd_x_cap = 0;
+        if (xb && cudaMalloc(&ctx->hd_x, xb) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(ctx, ZSOLVE_ENOMEM, "device buffer for host solutions");
+        }
+        ctx->hd_x_cap = xb;
+    }
+    ZS_CU(cudaMemcpyAsync(ctx->hd_L, L, mb, cudaMemcpyHostToDevice, ctx->stream));
+    ZS_CU(cudaMemcpyAsync(ctx->hd_Psi, Psi, mb, cudaMemcpyHostToDevice, ctx->stream));
+    ZS_CU(cudaMemcpyAsync(ctx->hd_G, G, mb, cudaMemcpyHostToDevice, ctx->stream));
+    ZS_CU(cudaMemcpyAsync(ctx->hd_b, b, (size_t)nrhs * n * sizeof(double2), cudaMemcpyHostToDevice, ctx->stream));
+    int st = sweep_impl(ctx, ctx->hd_L, ctx->hd_Psi, ctx->hd_G, omega, zs, nf, ctx->hd_b, ctx->hd_x, nrhs, info);
+    if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
+    if (xb) ZS_CU(cudaMemcpyAsync(x, ctx->hd_x, xb, cudaMemcpyDeviceToHost, ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    return st;
+}
+
+int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int nrhs) {
+    if (!ctx || !b || !x || !r) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_residual before zsolve_assemble");
+    ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, ctx->n, (const double2 *)b, (const double2 *)x, 0, nrhs,
+                             nullptr, 0, (double2 *)r, 0, ctx->d_all, 1, ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    return ZSOLVE_OK;
+}
+
+int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs) {
+    if (!ctx || !v || !d) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "zsolve_lowprec_solve before zsolve_factor");
+    const int64_t cnt = (int64_t)nrhs * ctx->n;
+    ZS_CU(zs_launch_narrow((const double2 *)v, ctx->v, cnt, ctx->stream));
+    ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_all, 1));
+    ZS_CU(zs_launch_widen(ctx->v, (double2 *)d, cnt, ctx->stream));
+    return check_device_status(ctx);
+}
+
+int zsolve_fallback_solve(zsolve_ctx *ctx, const void *b, void *x, int nrhs) {
+    if (!ctx || !b || !x) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    if (nrhs < 1 || nrhs > ctx->nrhs_max) return fail(ctx, ZSOLVE_EINVAL, "bad nrhs");
+    if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_fallback_solve before zsolve_assemble");
+    ZS_TRY(fallback_slot(ctx, 0, (const double2 *)b, (double2 *)x, nrhs));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    return ZSOLVE_OK;
+}
+
+int zsolve_get_z64(zsolve_ctx *ctx, void *dst) {
+    if (!ctx || !dst) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "nothing assembled");
+    ZS_CU(cudaMemcpyAsync(dst, ctx->z64, (size_t)ctx->n * ctx->n * sizeof(double2), cudaMemcpyDeviceToDevice,
+                          ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    return ZSOLVE_OK;
+}
+
+int zsolve_get_z32(zsolve_ctx *ctx, float *re, float *im) {
+    if (!ctx || !re || !im) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "nothing assembled");
+    ZS_CU(zs_launch_copy_z32_out(ctx->z32, ctx->ld, ctx->plane, ctx->n, re, im, ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    return ZSOLVE_OK;
+}
+
+int zsolve_pivot_flag(zsolve_ctx *ctx, int *flag) {
+    if (!ctx || !flag) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "not factored");
+    ZS_CU(cudaMemcpyAsync(ctx->h_pivflag, ctx->d_pivflag, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    *flag = ctx->h_pivflag[0];
+    return ZSOLVE_OK;
+}
+
+const char *zsolve_strerror(int status) {
+    switch (status) {
+        case ZSOLVE_OK: return "ok";
+        case ZSOLVE_EINVAL: return "invalid argument";
+        case ZSOLVE_ENOMEM: return "out of memory";
+        case ZSOLVE_ECUDA: return "CUDA error";
+        case ZSOLVE_ESTATE: return "call out of order (not assembled or not factored)";
+        case ZSOLVE_ENONFINITE: return "non-finite input";
+        case ZSOLVE_ESINGULAR: return "matrix is singular in double precision";
+        case ZSOLVE_ETIMEOUT: return "device-side wait gave up";
+        default: return "unknown status";
+    }
+}
+
+const char *zsolve_last_error(const zsolve_ctx *ctx) { return ctx ? ctx->err : "no context"; }
+
+void zsolve_destroy(zsolve_ctx *ctx) {
+    if (!ctx) return;
+    free_all(ctx);
+    delete ctx;
+}
+
+}  // extern "C"

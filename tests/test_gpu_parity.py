@@ -1,0 +1,363 @@
+"""Parity of the CUDA path (through the C-ABI) with the CPU oracle.
+
+Every input comes from the seeded generator in `workload`; every expected
+value comes from `oracle`.  Bars: the float64 assembly is bit-identical to
+the oracle's (both round each operation of the formula separately and in the
+same order) and its float32 copy is the round-to-nearest cast of it; the
+solutions agree with the oracle's complex128 direct solve to <= 1e-10
+relative l2 per (frequency, right-hand side).
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import workload
+
+pytestmark = pytest.mark.gpu
+
+PARITY = 1e-10
+
+
+@pytest.fixture(scope="module")
+def zs():
+    import mixed_precision_refinement_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    return t
+
+
+def dev(torch, a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.to(dtype)
+    return t.cuda()
+
+
+def rel_err(x, ref):
+    x = np.atleast_2d(x)
+    ref = np.atleast_2d(ref)
+    return np.linalg.norm(x - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+
+
+def solve_single(zs, torch, wl, f, gemm, nrhs=None, **opts):
+    B = wl.B if nrhs is None else wl.B[:nrhs]
+    s = zs.Solver(wl.n, B.shape[0], gemm=gemm, **opts)
+    try:
+        L, P, G = dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G)
+        zs.zsolve_assemble(s.ctx, L, P, G, wl.omega[f], wl.zs[f].real, wl.zs[f].imag)
+        zs.zsolve_factor(s.ctx)
+        b = dev(torch, B)
+        x = torch.empty_like(b)
+        info = zs.zsolve_refine(s.ctx, b, x)
+        torch.cuda.synchronize()
+        return x.cpu().numpy(), info
+    finally:
+        s.close()
+
+
+# ---------------------------------------------------------------- assembly (bit-exact)
+
+
+@pytest.mark.parametrize("n", [1, 2, 33, 130, 256, 301])
+def test_assemble_bit_exact(zs, torch, n):
+    wl = workload.make_small(n, seed=n, nf=2)
+    s = zs.Solver(n, 1)
+    try:
+        L, P, G = dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G)
+        for f in range(2):
+            zs.zsolve_assemble(s.ctx, L, P, G, wl.omega[f], wl.zs[f].real, wl.zs[f].imag)
+            z = torch.empty((n, n), dtype=torch.complex128, device="cuda")
+            zs.zsolve_get_z64(s.ctx, z)
+            ref = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[f], wl.zs[f])
+            got = z.cpu().numpy()
+            assert np.array_equal(got.view(np.float64), ref.view(np.float64))
+            re = torch.empty((n, n), dtype=torch.float32, device="cuda")
+            im = torch.empty((n, n), dtype=torch.float32, device="cuda")
+            zs.zsolve_get_z32(s.ctx, re, im)
+            c64 = oracle.cast_c64(ref)
+            assert np.array_equal(re.cpu().numpy(), c64.real) and np.array_equal(im.cpu().numpy(), c64.imag)
+    finally:
+        s.close()
+
+
+def test_assemble_term_isolation(zs, torch):
+    # L = 0, G = 0, and a balanced scaling: each term of Z must appear exactly
+    n = 70
+    wl = workload.make_small(n, seed=5, nf=1)
+    O = np.zeros((n, n))
+    cases = [(O, wl.Psi, wl.G), (wl.L, wl.Psi, O), (wl.L * 1e-9, wl.Psi * 1e9, wl.G * 1e3), (O, O, wl.G)]
+    s = zs.Solver(n, 1)
+    try:
+        for L, P, G in cases:
+            zs.zsolve_assemble(s.ctx, dev(torch, L), dev(torch, P), dev(torch, G), wl.omega[0], wl.zs[0].real,
+                               wl.zs[0].imag)
+            z = torch.empty((n, n), dtype=torch.complex128, device="cuda")
+            zs.zsolve_get_z64(s.ctx, z)
+            ref = oracle.assemble(L, P, G, wl.omega[0], wl.zs[0])
+            assert np.array_equal(z.cpu().numpy().view(np.float64), ref.view(np.float64))
+    finally:
+        s.close()
+
+
+# ---------------------------------------------------------------- stages
+
+
+@pytest.mark.parametrize("n,nrhs", [(1, 1), (64, 2), (257, 3), (300, 8)])
+def test_residual_against_oracle(zs, torch, n, nrhs):
+    wl = workload.make_small(n, seed=10 + n, nf=1, nrhs=nrhs)
+    X = workload.random_rhs(n, nrhs, seed=3)
+    s = zs.Solver(n, nrhs)
+    try:
+        zs.zsolve_assemble(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega[0],
+                           wl.zs[0].real, wl.zs[0].imag)
+        b, x = dev(torch, wl.B), dev(torch, X)
+        r = torch.empty_like(b)
+        zs.zsolve_residual(s.ctx, b, x, r)
+        Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0])
+        ref = oracle.residual(Z, X, wl.B)
+        # different summation order: bounded by a few ulps of sum |z||x| per row
+        scale = np.abs(X) @ np.abs(Z).T + np.abs(wl.B)
+        assert np.all(np.abs(r.cpu().numpy() - ref) <= 4 * n * 2.3e-16 * scale + 1e-300)
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("n", [1, 31, 128, 129, 300, 513])
+def test_factor_reconstructs_z32(zs, torch, n):
+    wl = workload.make_small(n, seed=20 + n, nf=1)
+    s = zs.Solver(n, 1, gemm=zs.ZSOLVE_GEMM_FFMA)
+    try:
+        zs.zsolve_assemble(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega[0],
+                           wl.zs[0].real, wl.zs[0].imag)
+        re = torch.empty((n, n), dtype=torch.float32, device="cuda")
+        im = torch.empty_like(re)
+        zs.zsolve_get_z32(s.ctx, re, im)
+        Z32 = (re.cpu().numpy() + 1j * im.cpu().numpy()).astype(np.complex128)
+        zs.zsolve_factor(s.ctx)
+        assert zs.zsolve_pivot_flag(s.ctx) == 0
+        zs.zsolve_get_z32(s.ctx, re, im)
+        LU = re.cpu().numpy().astype(np.float64) + 1j * im.cpu().numpy()
+        Lf = np.tril(LU, -1) + np.eye(n)
+        Uf = np.triu(LU)
+        err = np.linalg.norm(Lf @ Uf - Z32) / np.linalg.norm(Z32)
+        assert err < 2e-6
+        # and the factors are those of the unpivoted LU up to float32 rounding
+        LUo, st = oracle.lu_nopiv(Z32)
+        assert st == 0
+        assert np.linalg.norm(LU - LUo) / np.linalg.norm(LUo) < 1e-3
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("n,nrhs", [(1, 1), (65, 1), (200, 2), (300, 4), (129, 8), (150, 3)])
+def test_lowprec_solve(zs, torch, n, nrhs):
+    wl = workload.make_small(n, seed=30 + n, nf=1, nrhs=nrhs)
+    s = zs.Solver(n, nrhs, gemm=zs.ZSOLVE_GEMM_FFMA)
+    try:
+        zs.zsolve_assemble(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega[0],
+                           wl.zs[0].real, wl.zs[0].imag)
+        zs.zsolve_factor(s.ctx)
+        re = torch.empty((n, n), dtype=torch.float32, device="cuda")
+        im = torch.empty_like(re)
+        zs.zsolve_get_z32(s.ctx, re, im)
+        LU = re.cpu().numpy().astype(np.float64) + 1j * im.cpu().numpy()
+        v = dev(torch, wl.B)
+        d = torch.empty_like(v)
+        zs.zsolve_lowprec_solve(s.ctx, v, d)
+        D = d.cpu().numpy()
+        # the solve with the float32 factors: compare with the same factors in complex128
+        ref = oracle.lu_solve(LU, None, oracle.cast_c64(wl.B).astype(np.complex128))
+        assert np.all(rel_err(D, ref) < 1e-4)
+    finally:
+        s.close()
+
+
+# ---------------------------------------------------------------- end to end
+
+
+@pytest.mark.parametrize("gemm", ["FFMA"])
+def test_refine_config0_every_frequency(zs, torch, gemm):
+    wl = workload.make(0)
+    ref = oracle.solve_sweep(wl)
+    for f in range(len(wl.omega)):
+        x, info = solve_single(zs, torch, wl, f, getattr(zs, "ZSOLVE_GEMM_" + gemm))
+        assert info.fallback == 0 and 1 <= info.iters <= 10
+        assert np.all(rel_err(x, ref[f]) <= PARITY), (f, rel_err(x, ref[f]), info.as_dict())
+
+
+@pytest.mark.parametrize("n,nrhs,nf,batch", [(1, 1, 2, 0), (33, 2, 3, 2), (130, 3, 4, 3), (301, 4, 3, 0),
+                                              (257, 8, 2, 1)])
+def test_sweep_ragged_parity(zs, torch, n, nrhs, nf, batch):
+    wl = workload.make_small(n, seed=40 + n, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
+    ref = oracle.solve_sweep(wl)
+    s = zs.Solver(n, nrhs, gemm=zs.ZSOLVE_GEMM_FFMA, batch=batch)
+    try:
+        x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+        infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
+                                dev(torch, wl.B), x)
+        X = x.cpu().numpy()
+        for f in range(nf):
+            assert infos[f].status == 0
+            assert np.all(rel_err(X[f], ref[f]) <= PARITY), (f, rel_err(X[f], ref[f]), infos[f].as_dict())
+    finally:
+        s.close()
+
+
+def test_sweep_term_isolation_parity(zs, torch):
+    # the Psi/omega and Zs*G terms are tiny next to j*omega*L in the benchmark
+    # configurations; solve systems where they dominate or vanish
+    n = 150
+    wl = workload.make_small(n, seed=7, nf=2)
+    O = np.zeros((n, n))
+    cases = [(wl.L * 1e-9, wl.Psi * 1e9, wl.G * 1e3), (wl.L, O, wl.G), (O, wl.Psi + 0 * wl.L, wl.G * 1e2)]
+    s = zs.Solver(n, 1, gemm=zs.ZSOLVE_GEMM_FFMA)
+    try:
+        for L, P, G in cases:
+            x = torch.empty((2, 1, n), dtype=torch.complex128, device="cuda")
+            infos = zs.zsolve_sweep(s.ctx, dev(torch, L), dev(torch, P), dev(torch, G), wl.omega, wl.zs,
+                                    dev(torch, wl.B), x)
+            X = x.cpu().numpy()
+            for f in range(2):
+                Z = oracle.assemble(L, P, G, wl.omega[f], wl.zs[f])
+                ref = oracle.solve(Z, wl.B)
+                assert np.all(rel_err(X[f], ref) <= PARITY), (f, infos[f].as_dict())
+    finally:
+        s.close()
+
+
+def test_sweep_host_matches_device(zs, torch):
+    wl = workload.make_small(200, seed=50, nf=3, nrhs=2)
+    s = zs.Solver(200, 2, gemm=zs.ZSOLVE_GEMM_FFMA)
+    try:
+        x = torch.empty((3, 2, 200), dtype=torch.complex128, device="cuda")
+        zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
+                        dev(torch, wl.B), x)
+        xh = np.zeros((3, 2, 200), dtype=np.complex128)
+        zs.zsolve_sweep_host(s.ctx, wl.L, wl.Psi, wl.G, wl.omega, wl.zs, wl.B, xh)
+        assert np.array_equal(xh, x.cpu().numpy())
+    finally:
+        s.close()
+
+
+# ---------------------------------------------------------------- fallback
+
+
+def test_fallback_solve_direct(zs, torch):
+    wl = workload.make_small(160, seed=60, nf=1, nrhs=3)
+    s = zs.Solver(160, 3)
+    try:
+        zs.zsolve_assemble(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega[0],
+                           wl.zs[0].real, wl.zs[0].imag)
+        b = dev(torch, wl.B)
+        x = torch.empty_like(b)
+        zs.zsolve_fallback_solve(s.ctx, b, x)
+        ref = oracle.solve(oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0]), wl.B)
+        assert np.all(rel_err(x.cpu().numpy(), ref) <= 1e-12)
+    finally:
+        s.close()
+
+
+def test_forced_fallback_sweep(zs, torch):
+    wl = workload.make_small(97, seed=61, nf=2, nrhs=2)
+    s = zs.Solver(97, 2, gemm=zs.ZSOLVE_GEMM_FFMA, force_fallback=1)
+    try:
+        x = torch.empty((2, 2, 97), dtype=torch.complex128, device="cuda")
+        infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
+                                dev(torch, wl.B), x)
+        ref = oracle.solve_sweep(wl)
+        for f in range(2):
+            assert infos[f].fallback == 1 and infos[f].status == 0
+            assert np.all(rel_err(x.cpu().numpy()[f], ref[f]) <= 1e-12)
+    finally:
+        s.close()
+
+
+def test_zero_pivot_triggers_fallback(zs, torch):
+    # L = [[0,1],[1,0]] (+) I with Psi = G = 0: Z = j*omega*L has a zero leading
+    # pivot, so the unpivoted factorisation flags it and the pivoted LU solves
+    n = 40
+    L = np.eye(n)
+    L[:2, :2] = [[0.0, 1.0], [1.0, 0.0]]
+    O = np.zeros((n, n))
+    w = 2 * math.pi * 1e9
+    B = workload.random_rhs(n, 1, seed=62)
+    s = zs.Solver(n, 1, gemm=zs.ZSOLVE_GEMM_FFMA)
+    try:
+        zs.zsolve_assemble(s.ctx, dev(torch, L), dev(torch, O), dev(torch, O), w, 0.0, 0.0)
+        zs.zsolve_factor(s.ctx)
+        assert zs.zsolve_pivot_flag(s.ctx) == 1
+        b = dev(torch, B)
+        x = torch.empty_like(b)
+        info = zs.zsolve_refine(s.ctx, b, x)
+        assert info.fallback == 1 and info.pivot_flag == 1
+        ref = oracle.solve(oracle.assemble(L, O, O, w, 0j), B)
+        assert np.all(rel_err(x.cpu().numpy(), ref) <= 1e-13)
+    finally:
+        s.close()
+
+
+def test_singular_reported(zs, torch):
+    n = 8
+    O = np.zeros((n, n))
+    s = zs.Solver(n, 1, gemm=zs.ZSOLVE_GEMM_FFMA)
+    try:
+        zs.zsolve_assemble(s.ctx, dev(torch, O), dev(torch, O), dev(torch, O), 1e9, 0.0, 0.0)
+        zs.zsolve_factor(s.ctx)
+        b = dev(torch, workload.random_rhs(n, 1, seed=1))
+        x = torch.empty_like(b)
+        with pytest.raises(zs.ZsolveError) as e:
+            zs.zsolve_refine(s.ctx, b, x)
+        assert e.value.status == zs.ZSOLVE_ESINGULAR
+    finally:
+        s.close()
+
+
+# ---------------------------------------------------------------- argument errors
+
+
+def test_argument_errors(zs, torch):
+    s = zs.Solver(16, 2)
+    try:
+        lib = zs.raw_lib()
+        assert lib.zsolve_factor(s.ctx) == zs.ZSOLVE_ESTATE
+        L = dev(torch, np.eye(16))
+        assert lib.zsolve_assemble(s.ctx, L.data_ptr(), L.data_ptr(), L.data_ptr(), -1.0, 0.0, 0.0) == zs.ZSOLVE_EINVAL
+        assert lib.zsolve_assemble(s.ctx, L.data_ptr(), L.data_ptr(), L.data_ptr(), 1e9, 0.0, 0.0) == 0
+        b = torch.zeros((3, 16), dtype=torch.complex128, device="cuda")
+        assert lib.zsolve_refine(s.ctx, b.data_ptr(), b.data_ptr(), 3, None) == zs.ZSOLVE_EINVAL
+        assert lib.zsolve_refine(s.ctx, b.data_ptr(), b.data_ptr(), 1, None) == zs.ZSOLVE_ESTATE
+        assert "before" in zs.zsolve_last_error(s.ctx)
+    finally:
+        s.close()
+
+
+# ---------------------------------------------------------------- full size (the benchmark launch)
+
+
+def test_config1_full_sweep_sampled(zs, torch):
+    """N=2157, all 21 frequencies in one batched sweep (as the benchmark runs
+    it): oracle direct solves on a sample of frequencies, and for every
+    frequency the oracle's double-precision backward error of the returned x."""
+    wl = workload.make(1)
+    nf = len(wl.omega)
+    s = zs.Solver(wl.n, 1, batch=nf)
+    try:
+        x = torch.empty((nf, 1, wl.n), dtype=torch.complex128, device="cuda")
+        infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
+                                dev(torch, wl.B), x)
+        X = x.cpu().numpy()
+        for f in range(nf):
+            assert infos[f].status == 0 and infos[f].fallback == 0, infos[f].as_dict()
+            Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[f], wl.zs[f])
+            assert np.all(oracle.backward_error(Z, X[f], wl.B) < 1e-13)
+        for f in (0, nf // 2, nf - 1):
+            ref = oracle.solve_sweep(wl, [f])[0]
+            assert np.all(rel_err(X[f], ref) <= PARITY)
+    finally:
+        s.close()
