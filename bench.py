@@ -1,0 +1,343 @@
+"""Benchmark: solved frequency points per second of the mixed-precision sweep.
+
+One step = one zsolve_sweep over the whole frequency list of the workload
+(assembly, low-precision factorisation, refinement, any fallback) with the
+inputs already resident in HBM.  The default workload is the N=2157,
+21-frequency (1-10 GHz), 1-RHS sweep; --config picks another of the five
+synthetic workloads in `workload`.  Inputs are synthetic (seeded generator).
+
+Prints ONE JSON line on rank 0.  Under torchrun each rank solves the same
+sweep on its own GPU (weak scaling, no collective on the data path); the
+barrier-bracketed time is the max over ranks.
+
+--impl reference times the CPU oracle (complex128 pivoted LU) on bounded
+samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workload  # noqa: E402
+
+METRIC = "solved freq points/s at N=2157; LU TFLOP/s; FP64 residual GEMV HBM GB/s"
+UNIT = "freq points/s"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
+TF32_OVER_BF16 = 1.1 / 2.25  # nominal dense tf32 / bf16 tensor rates
+FP64_NOMINAL_TFLOPS = 1.25   # nominal FP64 rate of the part
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(PEAKS_FALLBACK), "fallback"
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def workload_name(cfg):
+    c = workload.CONFIGS[cfg]
+    return (f"dense complex-symmetric sweep N={c.n}, {c.nf} frequencies {c.f_lo / 1e9:g}-{c.f_hi / 1e9:g} GHz, "
+            f"{c.nrhs} RHS, Z = jwL - jPsi/w + Zs G")
+
+
+def schur_flops(n, nb=128):
+    """Useful real flops of all trailing updates of one factorisation."""
+    tot = 0
+    J = 0
+    while J + nb < n:
+        m2 = n - J - nb
+        tot += 8 * m2 * m2 * nb
+        J += nb
+    return tot
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                smax = max(smax, float(r[2]))
+            except (ValueError, IndexError):
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_baseline(cfg, budget_s=10.0, max_freqs=None):
+    """The oracle, as it stands, on a bounded sample of the workload's frequencies."""
+    import oracle
+
+    wl = workload.make(cfg)
+    nf = len(wl.omega) if max_freqs is None else min(max_freqs, len(wl.omega))
+    t0 = time.perf_counter()
+    done = 0
+    for f in range(nf):
+        Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[f], wl.zs[f])
+        oracle.solve(Z, wl.B)
+        done += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": done / dt, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} of {len(wl.omega)} frequencies of N={wl.n} (assemble + complex128 pivoted LU + "
+                      f"substitution, {wl.B.shape[0]} RHS), {dt:.1f} s"}
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+
+    wl = workload.make(args.config)
+    per_step = 1  # frequencies per step: one direct solve each
+    times = []
+    for i in range(args.warmup + args.steps):
+        f = i % len(wl.omega)
+        t0 = time.perf_counter()
+        for _ in range(per_step):
+            Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[f], wl.zs[f])
+            oracle.solve(Z, wl.B)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    tot = sum(times)
+    value = per_step * len(times) / tot
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_name(args.config), "step": "one frequency"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+                             "sample": f"{per_step} frequency per step of N={wl.n}"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import mixed_precision_refinement_gb300 as zs
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    cfg = workload.CONFIGS[args.config]
+    wl = workload.make(args.config)
+    n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
+    gemm = getattr(zs, "ZSOLVE_GEMM_" + args.gemm)
+    solver = zs.Solver(n, nrhs, gemm=gemm, batch=args.batch or nf, profile=1)
+    ctx = solver.ctx
+    L = torch.from_numpy(wl.L).cuda()
+    P = torch.from_numpy(wl.Psi).cuda()
+    G = torch.from_numpy(wl.G).cuda()
+    b = torch.from_numpy(wl.B).cuda()
+    x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")  # > L2 (129 MB)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        return zs.zsolve_sweep(ctx, L, P, G, wl.omega, wl.zs, b, x)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    zs.zsolve_reset_profile(ctx)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    infos = None
+    for i in range(args.steps):
+        flush.zero_()  # evict L2 between timed steps (outside the measured span)
+        ev[i][0].record(stream)
+        infos = step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop() if sampler else None
+    ms = sum(a.elapsed_time(bb) for a, bb in ev)
+    prof = zs.zsolve_get_profile(ctx).as_dict()
+    if dist:
+        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+    value = ws * nf / (ms_step / 1e3)
+
+    # e2e: the public host-pointer API, host<->device copies inside the timed span
+    Lh = torch.from_numpy(wl.L).pin_memory()
+    Ph = torch.from_numpy(wl.Psi).pin_memory()
+    Gh = torch.from_numpy(wl.G).pin_memory()
+    bh = torch.from_numpy(wl.B).pin_memory()
+    xh = torch.empty((nf, nrhs, n), dtype=torch.complex128).pin_memory()
+    zs.zsolve_sweep_host(ctx, Lh, Ph, Gh, wl.omega, wl.zs, bh, xh)  # warm the host path once
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        zs.zsolve_sweep_host(ctx, Lh, Ph, Gh, wl.omega, wl.zs, bh, xh)
+    e2e_s = (time.perf_counter() - t0) / args.steps
+    if dist:
+        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    if dist:
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    # --------------------------------------------------------------- derived numbers
+    peaks, peak_src = load_peaks()
+    iters = [i.iters for i in infos]
+    n_res_calls = sum(iters)  # residual evaluations per step (one per correction)
+    st = {k: v for k, v in prof.items()}
+    steps = args.steps
+    schur_f = schur_flops(n) * nf
+    fac_ms = (st["diag"]["ms"] + st["trsm"]["ms"] + st["schur"]["ms"]) / steps
+    lu_tflops = (8.0 * n ** 3 / 3.0 * nf) / (fac_ms / 1e3) / 1e12 if fac_ms > 0 else None
+    res_bytes = n_res_calls * (16.0 * n * n + 32.0 * n * nrhs)
+    res_ms = st["residual"]["ms"] / steps
+    res_gbs = res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None
+    asm_bytes = 24.0 * n * n + 24.0 * n * n * nf
+    stage_ms = {k: v["ms"] / steps for k, v in st.items()}
+    dominant = max(stage_ms, key=stage_ms.get)
+    fp32_peak = SMS * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12
+    fp64_peak = FP64_NOMINAL_TFLOPS
+    tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
+    roof = {}
+    if dominant == "schur":
+        per_launch_ms = st["schur"]["ms"] / max(1, st["schur"]["launches"])
+        launches_per_step = st["schur"]["launches"] / steps
+        flops_per_launch = schur_f / launches_per_step
+        ach = flops_per_launch / (per_launch_ms / 1e3) / 1e12
+        if args.gemm == "FFMA":
+            roof = {"kernel": "k_schur_simt", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                    "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
+        else:
+            roof = {"kernel": "k_schur_tc", "bound": "tensor", "achieved": ach, "peak": tf32_peak, "unit": "TFLOP/s",
+                    "peak_source": f"tf32 = {peak_src} bf16 {peaks['bf16_tflops']} x 1.1/2.25"}
+    elif dominant == "residual":
+        ach = res_gbs
+        roof = {"kernel": "k_residual", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{peak_src} hbm_gbs"}
+    elif dominant == "assemble":
+        ach = asm_bytes / (stage_ms["assemble"] / 1e3) / 1e9
+        roof = {"kernel": "k_assemble", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{peak_src} hbm_gbs"}
+    else:
+        roof = {"kernel": dominant, "bound": "latency", "achieved": None, "peak": None, "unit": None}
+    if roof.get("achieved") and roof.get("peak"):
+        roof["frac"] = roof["achieved"] / roof["peak"]
+    else:
+        roof["frac"] = None
+    roof["traffic"] = None
+    launches = sum(v["launches"] for v in st.values())
+    h2d = 3 * 8 * n * n + 16 * n * nrhs
+    d2h = 16 * nf * nrhs * n
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32 factor + f64 refine", "data": "synthetic",
+        "config": {"workload": workload_name(args.config), "n": n, "nf": nf, "nrhs": nrhs, "gemm": args.gemm,
+                   "batch": args.batch or nf, "l2": "flushed between steps (512 MB write)",
+                   "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
+        "lu_tflops": lu_tflops, "resid_gbs": res_gbs,
+        "resid_fp64_alu_bound_gbs": fp64_peak * 1e12 / 8.0 * 16.0 / nrhs / 1e9,
+        "roofline": roof,
+        "stage_ms_per_step": stage_ms,
+        "iters": iters, "fallbacks": sum(i.fallback for i in infos),
+        "gpu_launches": int(launches),
+        "e2e": {"value": ws * nf / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "clocks": clocks, "wall_s": wall,
+    }
+    solver.close()
+    if args.cpu_baseline and args.gpus <= 1 and ws == 1:
+        line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--gemm", default="FFMA", choices=["TF32", "TF32X3", "FFMA"])
+    ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -72,7 +72,24 @@ typedef struct {
     int outer_block;    /* columns per outer block of the factorisation; 128 (only value) */
     int batch;          /* frequencies factored together by zsolve_sweep; 0 = automatic */
     int force_fallback; /* testing aid: treat every frequency as stalled (default 0) */
+    int profile;        /* 1: time every stage with CUDA events (zsolve_get_profile); default 0 */
 } zsolve_opts;
+
+/* stages of the path, for zsolve_get_profile */
+#define ZSOLVE_STAGE_ASSEMBLE 0 /* fused float64 assembly + float32 cast */
+#define ZSOLVE_STAGE_DIAG 1     /* diagonal-block LU, 32-column panels */
+#define ZSOLVE_STAGE_TRSM 2     /* L21 = A21 U11^-1 and U12 = L11^-1 A12 */
+#define ZSOLVE_STAGE_SCHUR 3    /* trailing update A22 -= L21 U12 */
+#define ZSOLVE_STAGE_TRSV 4     /* forward/back substitution with the float32 factors */
+#define ZSOLVE_STAGE_RESIDUAL 5 /* r = b - Z x in float64 */
+#define ZSOLVE_STAGE_UPDATE 6   /* rounding of b, x += d, correction norms */
+#define ZSOLVE_STAGE_FALLBACK 7 /* float64 pivoted LU and its substitution */
+#define ZSOLVE_NSTAGE 8
+
+typedef struct {
+    int64_t launches[ZSOLVE_NSTAGE]; /* kernels launched per stage (always counted) */
+    double ms[ZSOLVE_NSTAGE];        /* device time per stage (only with opts.profile = 1) */
+} zsolve_profile;
 
 typedef struct {
     int iters;         /* corrections applied after the first solve */
@@ -154,6 +171,14 @@ int zsolve_get_z32(zsolve_ctx *ctx, float *re, float *im);
 
 /* Tiny or non-finite pivot seen by the last zsolve_factor (0 or 1) in *flag. */
 int zsolve_pivot_flag(zsolve_ctx *ctx, int *flag);
+
+/* Launch counts and (with opts.profile) per-stage device times accumulated
+ * since zsolve_create or the last zsolve_reset_profile.  Synchronises the
+ * context's stream to resolve pending timings. */
+int zsolve_get_profile(zsolve_ctx *ctx, zsolve_profile *out);
+
+/* Zero the counters of zsolve_get_profile. */
+int zsolve_reset_profile(zsolve_ctx *ctx);
 
 /* Static string for a status code. */
 const char *zsolve_strerror(int status);

@@ -39,7 +39,18 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 
 class zsolve_opts(ctypes.Structure):
     _fields_ = [("tol", ctypes.c_double), ("max_iter", ctypes.c_int), ("gemm", ctypes.c_int),
-                ("outer_block", ctypes.c_int), ("batch", ctypes.c_int), ("force_fallback", ctypes.c_int)]
+                ("outer_block", ctypes.c_int), ("batch", ctypes.c_int), ("force_fallback", ctypes.c_int),
+                ("profile", ctypes.c_int)]
+
+
+STAGES = ("assemble", "diag", "trsm", "schur", "trsv", "residual", "update", "fallback")
+
+
+class zsolve_profile(ctypes.Structure):
+    _fields_ = [("launches", ctypes.c_int64 * len(STAGES)), ("ms", ctypes.c_double * len(STAGES))]
+
+    def as_dict(self):
+        return {st: {"launches": int(self.launches[i]), "ms": float(self.ms[i])} for i, st in enumerate(STAGES)}
 
 
 class zsolve_info(ctypes.Structure):
@@ -76,6 +87,8 @@ def _load():
         "zsolve_get_z64": (I, [P, P]),
         "zsolve_get_z32": (I, [P, P, P]),
         "zsolve_pivot_flag": (I, [P, ctypes.POINTER(I)]),
+        "zsolve_get_profile": (I, [P, ctypes.POINTER(zsolve_profile)]),
+        "zsolve_reset_profile": (I, [P]),
         "zsolve_strerror": (ctypes.c_char_p, [I]),
         "zsolve_last_error": (ctypes.c_char_p, [P]),
         "zsolve_destroy": (None, [P]),
@@ -246,6 +259,16 @@ def zsolve_pivot_flag(ctx) -> int:
     f = ctypes.c_int()
     _check(ctx, _lib.zsolve_pivot_flag(ctx, ctypes.byref(f)))
     return f.value
+
+
+def zsolve_get_profile(ctx) -> zsolve_profile:
+    p = zsolve_profile()
+    _check(ctx, _lib.zsolve_get_profile(ctx, ctypes.byref(p)))
+    return p
+
+
+def zsolve_reset_profile(ctx) -> None:
+    _check(ctx, _lib.zsolve_reset_profile(ctx))
 
 
 def zsolve_strerror(status: int) -> str:

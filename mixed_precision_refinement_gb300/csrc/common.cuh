@@ -113,10 +113,19 @@ cudaError_t zs_launch_trsv(const float *z32, int64_t ld, int64_t plane, int64_t 
                            unsigned *status, int num_sms, cudaStream_t st);
 
 // r = b - Z64 x.  out_c64 != NULL: writes float2 (rounded); else writes c128 to out_c128.
+// Launches one kernel per chunk of 8/4/2/1 right-hand sides (zs_rhs_chunks).
 cudaError_t zs_launch_residual(const double2 *z64, int64_t z64_stride, int64_t n, const double2 *b,
                                const double2 *x, int64_t x_stride, int nrhs, float2 *out_c64,
                                int64_t out64_stride, double2 *out_c128, int64_t out128_stride,
                                const int *slots, int nslot, cudaStream_t st);
+inline int zs_rhs_chunks(int nrhs) {
+    int c = 0;
+    while (nrhs > 0) {
+        nrhs -= nrhs >= 8 ? 8 : nrhs >= 4 ? 4 : nrhs >= 2 ? 2 : 1;
+        c++;
+    }
+    return c;
+}
 
 // v = (float2) b for every listed slot
 cudaError_t zs_launch_cast_rhs(const double2 *b, int64_t n, int nrhs, float2 *v, int64_t v_stride,
@@ -138,6 +147,7 @@ cudaError_t zs_launch_copy_z32_out(const float *z32, int64_t ld, int64_t plane, 
                                    float *im, cudaStream_t st);
 
 // float64 LU with partial pivoting (the fallback) on a c128 matrix with ld n.
-cudaError_t zs_lu64_factor(double2 *a, int64_t n, int64_t *piv, int *info, cudaStream_t st);
+// *launches (if not NULL) is increased by the number of kernels launched.
+cudaError_t zs_lu64_factor(double2 *a, int64_t n, int64_t *piv, int *info, cudaStream_t st, int64_t *launches);
 cudaError_t zs_lu64_solve(const double2 *lu, int64_t n, const int64_t *piv, double2 *x, int nrhs,
-                          cudaStream_t st);
+                          cudaStream_t st, int64_t *launches);

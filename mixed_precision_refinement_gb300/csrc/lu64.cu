@@ -252,40 +252,48 @@ __global__ void k_lu64_trsv_update(const double2 *__restrict__ lu, int64_t n, do
 
 }  // namespace
 
-cudaError_t zs_lu64_factor(double2 *a, int64_t n, int64_t *piv, int *info, cudaStream_t st) {
+cudaError_t zs_lu64_factor(double2 *a, int64_t n, int64_t *piv, int *info, cudaStream_t st, int64_t *launches) {
+    int64_t cnt = 0;
     cudaError_t e = cudaMemsetAsync(info, 0, sizeof(int), st);
     if (e != cudaSuccess) return e;
     for (int64_t k0 = 0; k0 < n; k0 += W) {
         const int w = (int)((n - k0) < W ? (n - k0) : W);
         k_lu64_panel<<<1, kPanelThreads, 0, st>>>(a, n, k0, w, piv, info);
         k_lu64_swap<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(a, n, k0, w, piv, info);
+        cnt += 2;
         const int64_t m = n - k0 - w;
         if (m > 0) {
             k_lu64_trsm<<<(unsigned)((m + 127) / 128), 128, 0, st>>>(a, n, k0, w, info);
             const unsigned t = (unsigned)((m + kGT - 1) / kGT);
             k_lu64_gemm<<<dim3(t, t), 256, 0, st>>>(a, n, k0, w, info);
+            cnt += 2;
         }
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    if (launches) *launches += cnt;
     return cudaSuccess;
 }
 
 cudaError_t zs_lu64_solve(const double2 *lu, int64_t n, const int64_t *piv, double2 *x, int nrhs,
-                          cudaStream_t st) {
+                          cudaStream_t st, int64_t *launches) {
     if (nrhs > 32) return cudaErrorInvalidValue;
+    int64_t cnt = 1;
     k_lu64_apply_piv<<<nrhs, 32, 0, st>>>(x, n, piv);
     for (int64_t r0 = 0; r0 < n; r0 += W) {  // forward, unit lower
         const int bw = (int)((n - r0) < W ? (n - r0) : W);
         k_lu64_trsv_diag<<<1, 32, 0, st>>>(lu, n, x, nrhs, r0, bw, 0);
         const int64_t rows = n - r0 - bw;
+        cnt += 1 + (rows > 0);
         if (rows > 0) k_lu64_trsv_update<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(lu, n, x, nrhs, r0, bw, 0);
     }
     const int64_t last = ((n - 1) / W) * W;
     for (int64_t r0 = last; r0 >= 0; r0 -= W) {  // backward, upper
         const int bw = (int)((n - r0) < W ? (n - r0) : W);
         k_lu64_trsv_diag<<<1, 32, 0, st>>>(lu, n, x, nrhs, r0, bw, 1);
+        cnt += 1 + (r0 > 0);
         if (r0 > 0) k_lu64_trsv_update<<<(unsigned)((r0 + 7) / 8), 256, 0, st>>>(lu, n, x, nrhs, r0, bw, 1);
     }
+    if (launches) *launches += cnt;
     return cudaGetLastError();
 }

@@ -67,6 +67,15 @@ struct zsolve_ctx {
     int hd_nrhs_cap = 0;
     cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
     int assembled = 0, factored = 0, fb_ready = 0;
+    // stage profile: launch counts always, event-timed spans with opts.profile
+    int64_t prof_launches[ZSOLVE_NSTAGE] = {};
+    double prof_ms[ZSOLVE_NSTAGE] = {};
+    struct Span {
+        int stage;
+        cudaEvent_t a, b;
+    };
+    std::vector<cudaEvent_t> ev_pool;
+    std::vector<Span> pending;
     char err[512] = {0};
 };
 
@@ -96,6 +105,60 @@ int fail(zsolve_ctx *c, int code, const char *fmt, ...) {
         if (s_ != ZSOLVE_OK) return s_; \
     } while (0)
 
+// ------------------------------------------------------------------ stage profile
+
+int prof_resolve(zsolve_ctx *ctx) {
+    for (auto &sp : ctx->pending) {
+        ZS_CU(cudaEventSynchronize(sp.b));
+        float ms = 0.f;
+        ZS_CU(cudaEventElapsedTime(&ms, sp.a, sp.b));
+        ctx->prof_ms[sp.stage] += ms;
+        ctx->ev_pool.push_back(sp.a);
+        ctx->ev_pool.push_back(sp.b);
+    }
+    ctx->pending.clear();
+    return ZSOLVE_OK;
+}
+
+cudaEvent_t prof_take(zsolve_ctx *ctx) {
+    if (ctx->ev_pool.empty() && ctx->pending.size() >= 4096) prof_resolve(ctx);
+    if (!ctx->ev_pool.empty()) {
+        cudaEvent_t e = ctx->ev_pool.back();
+        ctx->ev_pool.pop_back();
+        return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+}
+
+// Brackets the launches of one stage: counts them and, with opts.profile,
+// records a pair of events around them on the context's stream.
+struct StageSpan {
+    zsolve_ctx *c;
+    int stage;
+    cudaEvent_t a = nullptr;
+    StageSpan(zsolve_ctx *ctx, int st) : c(ctx), stage(st) {
+        if (c->opts.profile) {
+            a = prof_take(c);
+            if (a) cudaEventRecord(a, c->stream);
+        }
+    }
+    void done(int64_t launches) {
+        c->prof_launches[stage] += launches;
+        if (a) {
+            cudaEvent_t b = prof_take(c);
+            if (b) {
+                cudaEventRecord(b, c->stream);
+                c->pending.push_back({stage, a, b});
+            } else {
+                c->ev_pool.push_back(a);
+            }
+            a = nullptr;
+        }
+    }
+};
+
 int gemm_mode(const zsolve_opts &o) {
     switch (o.gemm) {
         case ZSOLVE_GEMM_TF32: return 1;
@@ -117,19 +180,29 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
     ZS_CU(cudaMemsetAsync(ctx->d_pivflag, 0, sizeof(int) * ctx->S, ctx->stream));
     for (int64_t J = 0; J < n; J += ZS_NB) {
         const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
-        ZS_CU(zs_launch_diag_lu(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, nb, slots, nslot,
-                                ctx->d_pivflag, ctx->stream));
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
+            ZS_CU(zs_launch_diag_lu(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, nb, slots, nslot,
+                                    ctx->d_pivflag, ctx->stream));
+            sp.done(1);
+        }
         if (J + nb >= n) break;
-        ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                               ctx->pack_stride, mode, slots, nslot, ctx->stream));
-        ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                               ctx->pack_stride, mode, slots, nslot, ctx->stream));
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
+            ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                                   ctx->pack_stride, mode, slots, nslot, ctx->stream));
+            ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                                   ctx->pack_stride, mode, slots, nslot, ctx->stream));
+            sp.done(2);
+        }
+        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
         if (mode == 0)
             ZS_CU(zs_launch_schur_simt(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
                                        ctx->pack_stride, slots, nslot, ctx->stream));
         else
             ZS_CU(zs_launch_schur_tc(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
                                      ctx->pack_stride, mode == 2 ? 1 : 0, slots, nslot, ctx->stream));
+        sp.done(1);
     }
     return ZSOLVE_OK;
 }
@@ -143,9 +216,11 @@ int lowprec_solve_slots(zsolve_ctx *ctx, int nrhs, const int *slots, int nslot) 
         const int left = nrhs - r0;
         const int R = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
         ctx->epoch++;
+        StageSpan sp(ctx, ZSOLVE_STAGE_TRSV);
         ZS_CU(zs_launch_trsv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->v + (int64_t)r0 * ctx->n,
                              ctx->v_stride, R, slots, nslot, ctx->flags, ctx->flags_stride, ctx->epoch,
                              ctx->ticket, ctx->d_status, ctx->num_sms, ctx->stream));
+        sp.done(1);
         r0 += R;
     }
     return ZSOLVE_OK;
@@ -182,15 +257,22 @@ int fallback_slot(zsolve_ctx *ctx, int slot, const double2 *b, double2 *x, int n
     const int64_t n = ctx->n;
     ZS_CU(cudaMemcpyAsync(ctx->fb_a, ctx->z64 + (int64_t)slot * ctx->z64_stride, (size_t)n * n * sizeof(double2),
                           cudaMemcpyDeviceToDevice, ctx->stream));
-    ZS_CU(zs_lu64_factor(ctx->fb_a, n, ctx->fb_piv, ctx->fb_info, ctx->stream));
+    int64_t cnt = 0;
+    StageSpan sp(ctx, ZSOLVE_STAGE_FALLBACK);
+    ZS_CU(zs_lu64_factor(ctx->fb_a, n, ctx->fb_piv, ctx->fb_info, ctx->stream, &cnt));
+    sp.done(cnt);
     ZS_CU(cudaMemcpyAsync(ctx->h_fb_info, ctx->fb_info, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
     ZS_CU(cudaStreamSynchronize(ctx->stream));
     if (*ctx->h_fb_info != 0)
         return fail(ctx, ZSOLVE_ESINGULAR, "double-precision LU: zero pivot column at %d", *ctx->h_fb_info - 1);
     if (x != b)
         ZS_CU(cudaMemcpyAsync(x, b, (size_t)nrhs * n * sizeof(double2), cudaMemcpyDeviceToDevice, ctx->stream));
+    cnt = 0;
+    StageSpan sp2(ctx, ZSOLVE_STAGE_FALLBACK);
     for (int r0 = 0; r0 < nrhs; r0 += 32)
-        ZS_CU(zs_lu64_solve(ctx->fb_a, n, ctx->fb_piv, x + (int64_t)r0 * n, std::min(32, nrhs - r0), ctx->stream));
+        ZS_CU(zs_lu64_solve(ctx->fb_a, n, ctx->fb_piv, x + (int64_t)r0 * n, std::min(32, nrhs - r0), ctx->stream,
+                            &cnt));
+    sp2.done(cnt);
     return ZSOLVE_OK;
 }
 
@@ -220,21 +302,36 @@ int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride
         ZS_TRY(upload_active());
         const int na = (int)active.size();
         // step 2: first solve with the low-precision factors
-        ZS_CU(zs_launch_cast_rhs(b, n, nrhs, ctx->v, ctx->v_stride, ctx->d_active, na, ctx->stream));
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
+            ZS_CU(zs_launch_cast_rhs(b, n, nrhs, ctx->v, ctx->v_stride, ctx->d_active, na, ctx->stream));
+            sp.done(1);
+        }
         ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_active, na));
+        StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
         ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 1, ctx->partials, ctx->nchunks,
                                ctx->d_active, na, ctx->stream));
+        sp.done(1);
     }
     for (int it = 1; it <= o.max_iter && !active.empty(); it++) {
         const int na = (int)active.size();
         // step 3: residual in double precision, rounded for the low-precision solve
-        ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, b, x, x_stride, nrhs, ctx->v, ctx->v_stride, nullptr,
-                                 0, ctx->d_active, na, ctx->stream));
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL);
+            ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, b, x, x_stride, nrhs, ctx->v, ctx->v_stride,
+                                     nullptr, 0, ctx->d_active, na, ctx->stream));
+            sp.done(zs_rhs_chunks(nrhs));
+        }
         // step 4: correction and update
         ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_active, na));
-        ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 0, ctx->partials, ctx->nchunks,
-                               ctx->d_active, na, ctx->stream));
-        ZS_CU(zs_launch_relcorr(ctx->partials, ctx->nchunks, nrhs, ctx->d_relcorr, ctx->d_active, na, ctx->stream));
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
+            ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 0, ctx->partials, ctx->nchunks,
+                                   ctx->d_active, na, ctx->stream));
+            ZS_CU(zs_launch_relcorr(ctx->partials, ctx->nchunks, nrhs, ctx->d_relcorr, ctx->d_active, na,
+                                    ctx->stream));
+            sp.done(2);
+        }
         ZS_CU(cudaMemcpyAsync(ctx->h_relcorr, ctx->d_relcorr, sizeof(double) * (size_t)count * nrhs,
                               cudaMemcpyDeviceToHost, ctx->stream));
         ZS_TRY(check_device_status(ctx));  // synchronises
@@ -303,8 +400,12 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
         ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam) * count, cudaMemcpyHostToDevice,
                               ctx->stream));
         ZS_CU(cudaEventRecord(ctx->ev[0], ctx->stream));
-        ZS_CU(zs_launch_assemble(L, Psi, G, n, ctx->d_params, count, ctx->z64, ctx->z64_stride, ctx->z32, ctx->ld,
-                                 ctx->plane, ctx->z32_stride, ctx->stream));
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE);
+            ZS_CU(zs_launch_assemble(L, Psi, G, n, ctx->d_params, count, ctx->z64, ctx->z64_stride, ctx->z32,
+                                     ctx->ld, ctx->plane, ctx->z32_stride, ctx->stream));
+            sp.done(1);
+        }
         ZS_CU(cudaEventRecord(ctx->ev[1], ctx->stream));
         ZS_TRY(factor_slots(ctx, ctx->d_all, count));
         ZS_CU(cudaEventRecord(ctx->ev[2], ctx->stream));
@@ -361,6 +462,13 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->hd_x);
     for (auto &e : c->ev)
         if (e) cudaEventDestroy(e);
+    for (auto &sp : c->pending) {
+        cudaEventDestroy(sp.a);
+        cudaEventDestroy(sp.b);
+    }
+    for (auto e : c->ev_pool) cudaEventDestroy(e);
+    c->pending.clear();
+    c->ev_pool.clear();
 }
 
 }  // namespace
@@ -375,6 +483,7 @@ int zsolve_default_opts(zsolve_opts *opts) {
     opts->outer_block = ZS_NB;
     opts->batch = 0;
     opts->force_fallback = 0;
+    opts->profile = 0;
     return ZSOLVE_OK;
 }
 
@@ -470,8 +579,10 @@ int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const d
         return fail(ctx, ZSOLVE_EINVAL, "omega must be positive and finite, Zs finite");
     ctx->h_params[0] = ZsSlotParam{omega, zs_re, zs_im, 0.0};
     ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
+    StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE);
     ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32, ctx->ld,
                              ctx->plane, ctx->z32_stride, ctx->stream));
+    sp.done(1);
     ctx->assembled = 1;
     ctx->factored = 0;
     return ZSOLVE_OK;
@@ -550,8 +661,10 @@ int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int 
     if (!ctx || !b || !x || !r) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
     ZS_TRY(check_nrhs(ctx, nrhs));
     if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_residual before zsolve_assemble");
+    StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL);
     ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, ctx->n, (const double2 *)b, (const double2 *)x, 0, nrhs,
                              nullptr, 0, (double2 *)r, 0, ctx->d_all, 1, ctx->stream));
+    sp.done(zs_rhs_chunks(nrhs));
     ZS_CU(cudaStreamSynchronize(ctx->stream));
     return ZSOLVE_OK;
 }
@@ -561,9 +674,15 @@ int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs) {
     ZS_TRY(check_nrhs(ctx, nrhs));
     if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "zsolve_lowprec_solve before zsolve_factor");
     const int64_t cnt = (int64_t)nrhs * ctx->n;
-    ZS_CU(zs_launch_narrow((const double2 *)v, ctx->v, cnt, ctx->stream));
+    {
+        StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
+        ZS_CU(zs_launch_narrow((const double2 *)v, ctx->v, cnt, ctx->stream));
+        sp.done(1);
+    }
     ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_all, 1));
+    StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
     ZS_CU(zs_launch_widen(ctx->v, (double2 *)d, cnt, ctx->stream));
+    sp.done(1);
     return check_device_status(ctx);
 }
 
@@ -599,6 +718,26 @@ int zsolve_pivot_flag(zsolve_ctx *ctx, int *flag) {
     ZS_CU(cudaMemcpyAsync(ctx->h_pivflag, ctx->d_pivflag, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
     ZS_CU(cudaStreamSynchronize(ctx->stream));
     *flag = ctx->h_pivflag[0];
+    return ZSOLVE_OK;
+}
+
+int zsolve_get_profile(zsolve_ctx *ctx, zsolve_profile *out) {
+    if (!ctx || !out) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    ZS_TRY(prof_resolve(ctx));
+    for (int i = 0; i < ZSOLVE_NSTAGE; i++) {
+        out->launches[i] = ctx->prof_launches[i];
+        out->ms[i] = ctx->prof_ms[i];
+    }
+    return ZSOLVE_OK;
+}
+
+int zsolve_reset_profile(zsolve_ctx *ctx) {
+    if (!ctx) return ZSOLVE_EINVAL;
+    ZS_TRY(prof_resolve(ctx));
+    for (int i = 0; i < ZSOLVE_NSTAGE; i++) {
+        ctx->prof_launches[i] = 0;
+        ctx->prof_ms[i] = 0.0;
+    }
     return ZSOLVE_OK;
 }
 
