@@ -57,6 +57,35 @@ __device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned want, u
     }
 }
 
+// In-order progress counters: the 64-bit word holds (epoch << 32) | count,
+// where count blocks of this launch's epoch are complete.  Returns the count
+// once it exceeds `need` (bounded wait as above), or -1 on give-up.
+__device__ __forceinline__ long long progress_read(const unsigned long long *p, unsigned epoch) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return (unsigned)(v >> 32) == epoch ? (long long)(v & 0xffffffffull) : 0;
+}
+
+__device__ __forceinline__ long long progress_wait(const unsigned long long *p, unsigned epoch, long long need,
+                                                   unsigned *status) {
+    unsigned it = 0;
+    while (true) {
+        long long c = progress_read(p, epoch);
+        if (c > need) return c;
+        if (++it > ZS_SPIN_LIMIT) {
+            atomicOr(status, ZS_DEV_TIMEOUT);
+            return -1;
+        }
+        if ((it & 1023u) == 0 && (*(volatile const unsigned *)status & ZS_DEV_TIMEOUT)) return -1;
+        if (it > 32) __nanosleep(32);
+    }
+}
+
+__device__ __forceinline__ void progress_set(unsigned long long *p, unsigned epoch, unsigned count) {
+    unsigned long long v = ((unsigned long long)epoch << 32) | count;
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ void set_flag(unsigned *flag, unsigned v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
 }
@@ -107,9 +136,10 @@ __host__ __device__ inline int64_t zs_pack_plane(int64_t n) { return n * (int64_
 
 // Triangular solves with the float32 factors: v (c64 interleaved, per active
 // slot nrhs rows of n) is overwritten by (LU)^-1 v.
+// prog: two in-order progress words (forward, backward) per slot.
 cudaError_t zs_launch_trsv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                            float2 *v, int64_t v_stride, int nrhs, const int *slots, int nslot,
-                           unsigned *flags, int64_t flags_stride, unsigned epoch, unsigned *ticket,
+                           unsigned long long *prog, unsigned epoch, unsigned *ticket,
                            unsigned *status, int num_sms, cudaStream_t st);
 
 // r = b - Z64 x.  out_c64 != NULL: writes float2 (rounded); else writes c128 to out_c128.

@@ -1,7 +1,407 @@
-// tcgen05 trailing update: placeholder until the tensor-core kernel lands.
+// Trailing (Schur) update of the low-precision LU on the 5th-generation
+// tensor cores: A22 -= L21 U12 (malusrfworks.com, "Solving Dense Matrices
+// Fast in the Browser", section "Double-precision answers from a GPU without
+// double precision", step 1: the factorisation's matrix products, done there
+// in 64x64 tiles).
+//
+// The complex product is two real products over the operand packs written by
+// the block triangular solves (K = 2 x 128 real):
+//   Re(L21 U12) = A . Br^T,  Im(L21 U12) = A . Bi^T,
+//   A = [Re L21 | Im L21],  Br = [Re U12^T | -Im U12^T],  Bi = [Im U12^T | Re U12^T].
+// One CTA owns a 128-row x 128-column complex output tile: a single
+// tcgen05.mma of shape M=128, N=256 covers both the real part (columns 0-127
+// of the accumulator, B rows from Br) and the imaginary part (columns
+// 128-255, B rows from Bi) in one fp32 TMEM accumulator of 256 columns.
+//   split = 0: kind::tf32, operands rounded to tf32 once;
+//   split = 1: 3xTF32 -- x = hi + lo with hi, lo tf32; the product is formed
+//              as hi.hi + hi.lo + lo.hi (the lo.lo term is below fp32
+//              rounding), which restores float32-class accuracy (Ootomo and
+//              Yokota, "Recovering single precision accuracy from Tensor
+//              Cores while surpassing the FP32 theoretical peak
+//              performance", IJHPCA 2022).
+//
+// Warp roles (192 threads, persistent over the tiles of every frequency in
+// the batch): warp 0 issues TMA loads (128B-swizzled K-major tiles of 32
+// fp32) into a ring of shared-memory stages; warp 1 owns TMEM (512 columns:
+// two accumulators, so the epilogue of one tile overlaps the MMAs of the
+// next) and issues the MMAs from one thread; warps 2-5 drain the accumulator
+// with tcgen05.ld and subtract it from the float32 trailing matrix.  Every
+// mbarrier wait is bounded: on give-up the kernel raises a status bit, stops
+// all roles, waits (bounded) for its own copies and MMAs and frees TMEM.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
-cudaError_t zs_launch_schur_tc(float *, int64_t, int64_t, int64_t, int64_t, int64_t, const float *, int64_t, int,
-                               const int *, int, cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int NB = ZS_NB;
+constexpr int KTOT = ZS_PACK_K;   // 256 real K per tile
+constexpr int KC = 32;            // fp32 per 128-byte swizzle row
+constexpr int NKC = KTOT / KC;    // 8 K chunks
+constexpr int TM = 128, TN = 128; // complex output tile
+constexpr int kThreads = 192;
+constexpr int A_BYTES = TM * KC * 4;       // 16 KB
+constexpr int B_BYTES = 2 * TN * KC * 4;   // 32 KB (Br rows then Bi rows)
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t kWaitLimit = 1u << 26;
+
+enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
+
+template <int SPLIT>
+struct Cfg {
+    static constexpr int STAGE_BYTES = SPLIT ? 2 * (A_BYTES + B_BYTES) : (A_BYTES + B_BYTES);
+    static constexpr int STAGES = SPLIT ? 2 : 4;
+    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; gives up if another role already did (abort flag) or after
+// kWaitLimit polls, raising the device status bit.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                          unsigned *status) {
+    uint32_t it = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (++it > kWaitLimit) {
+            *abort_flag = 1;
+            atomicOr(status, ZS_DEV_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row core groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);           // start address
+    d |= (uint64_t)1 << 16;                          // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;                // stride byte offset
+    d |= (uint64_t)1 << 46;                          // descriptor version
+    d |= (uint64_t)2 << 61;                          // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::tf32: D fp32, A/B tf32, both K-major, M=128, N=256.
+constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(256 >> 3) << 17) |
+                            ((uint32_t)(128 >> 4) << 24);
+
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive fp32 columns of the accumulator
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+          "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+          "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
+}
+
+template <int SPLIT>
+__global__ void __launch_bounds__(kThreads, 1)
+k_schur_tc(const __grid_constant__ CUtensorMap tmap, float *__restrict__ z32, int64_t ld, int64_t plane,
+           int64_t z32_stride, int64_t n, int64_t J, const int *__restrict__ slots, int nslot,
+           unsigned *__restrict__ status) {
+    using C = Cfg<SPLIT>;
+    extern __shared__ uint8_t smem_raw[];
+    __shared__ __align__(8) uint64_t bar_full[C::STAGES], bar_empty[C::STAGES], bar_accf[2], bar_acce[2], bar_drain;
+    __shared__ uint32_t s_tmem;
+    __shared__ volatile int s_abort;
+    const uint32_t base_addr = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int64_t base = J + NB;
+    const int64_t m2 = n - base;
+    const int tiles = (int)((m2 + TM - 1) / TM);
+    const int per_slot = tiles * tiles;
+    const int total = per_slot * nslot;
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int s = 0; s < C::STAGES; s++) {
+            mbar_init(smem_u32(&bar_full[s]), 1);
+            mbar_init(smem_u32(&bar_empty[s]), 1);
+        }
+        for (int b = 0; b < 2; b++) {
+            mbar_init(smem_u32(&bar_accf[b]), 1);
+            mbar_init(smem_u32(&bar_acce[b]), 4);
+        }
+        mbar_init(smem_u32(&bar_drain), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
+            uint32_t g = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+                const int si = t / per_slot, rem = t - si * per_slot;
+                const int tm = rem / tiles, tn = rem - tm * tiles;
+                const int slot = slots[si];
+                const int ra = (int)(base + (int64_t)tm * TM), rb = (int)(base + (int64_t)tn * TN);
+                for (int kc = 0; kc < NKC; kc++, g++) {
+                    const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&bar_empty[st]), ph ^ 1u, &s_abort, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&bar_full[st]);
+                    mbar_expect_tx(fb, C::STAGE_BYTES);
+                    const uint32_t sa = base_addr + st * C::STAGE_BYTES;
+                    const int k0 = kc * KC;
+                    tma_load_4d(sa, &tmap, k0, ra, PL_A_HI, slot, fb);
+                    tma_load_4d(sa + A_BYTES, &tmap, k0, rb, PL_BR_HI, slot, fb);
+                    tma_load_4d(sa + A_BYTES + B_BYTES / 2, &tmap, k0, rb, PL_BI_HI, slot, fb);
+                    if (SPLIT) {
+                        const uint32_t sl = sa + A_BYTES + B_BYTES;
+                        tma_load_4d(sl, &tmap, k0, ra, PL_A_LO, slot, fb);
+                        tma_load_4d(sl + A_BYTES, &tmap, k0, rb, PL_BR_LO, slot, fb);
+                        tma_load_4d(sl + A_BYTES + B_BYTES / 2, &tmap, k0, rb, PL_BI_LO, slot, fb);
+                    }
+                }
+            }
+            // our own copies in flight: wait (bounded) for the last stages to land
+            const uint32_t issued = g;
+            for (uint32_t q = issued > (uint32_t)C::STAGES ? issued - C::STAGES : 0; q < issued; q++) {
+                uint32_t it = 0;
+                while (!mbar_try_wait(smem_u32(&bar_full[q % C::STAGES]), (q / C::STAGES) & 1u) &&
+                       ++it < kWaitLimit) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t g = 0, it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, it++) {
+                const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&bar_acce[buf]), aph ^ 1u, &s_abort, status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + buf * 256u;
+                for (int kc = 0; kc < NKC; kc++, g++) {
+                    const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
+                    if (!mbar_wait(smem_u32(&bar_full[st]), ph, &s_abort, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = base_addr + st * C::STAGE_BYTES;
+#pragma unroll
+                    for (int ks = 0; ks < KC / 8; ks++) {
+                        const uint64_t ah = smem_desc(sa + ks * 32);
+                        const uint64_t bh = smem_desc(sa + A_BYTES + ks * 32);
+                        const uint32_t acc = (kc | ks) ? 1u : 0u;
+                        if (SPLIT) {
+                            const uint32_t sl = sa + A_BYTES + B_BYTES;
+                            const uint64_t al = smem_desc(sl + ks * 32);
+                            const uint64_t bl = smem_desc(sl + A_BYTES + ks * 32);
+                            mma_tf32(d, al, bh, acc);
+                            mma_tf32(d, ah, bl, 1u);
+                            mma_tf32(d, ah, bh, 1u);
+                        } else {
+                            mma_tf32(d, ah, bh, acc);
+                        }
+                    }
+                    mma_commit(smem_u32(&bar_empty[st]));  // stage free once these MMAs finish
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&bar_accf[buf]));  // accumulator ready
+            }
+            // drain: every MMA issued so far completes before TMEM is freed
+            mma_commit(smem_u32(&bar_drain));
+            uint32_t w = 0;
+            while (!mbar_try_wait(smem_u32(&bar_drain), 0) && ++w < kWaitLimit) {
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5)
+        const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
+        uint32_t it = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x, it++) {
+            const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+            const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status);
+            if (!__all_sync(0xffffffffu, ok)) break;
+            tc_fence_after();
+            const int si = t / per_slot, rem = t - si * per_slot;
+            const int tm = rem / tiles, tn = rem - tm * tiles;
+            const int slot = slots[si];
+            float *cre = z32 + (int64_t)slot * z32_stride;
+            const int64_t row = base + (int64_t)tm * TM + quad * 32 + lane;
+            const int64_t col0 = base + (int64_t)tn * TN;
+#pragma unroll 1
+            for (int c = 0; c < 8; c++) {
+                float v[32];
+                tmem_ld32(tmem + buf * 256u + (uint32_t)(c * 32) + ((uint32_t)(quad * 32) << 16), v);
+                if (row < n) {
+                    float *dst = cre + (c >= 4 ? plane : 0) + row * ld + col0 + (c & 3) * 32;
+                    const int64_t cbeg = col0 + (c & 3) * 32;
+                    if (cbeg + 32 <= n) {
+                        float4 *d4 = reinterpret_cast<float4 *>(dst);
+#pragma unroll
+                        for (int q = 0; q < 8; q++) {
+                            float4 o = d4[q];
+                            o.x -= v[4 * q];
+                            o.y -= v[4 * q + 1];
+                            o.z -= v[4 * q + 2];
+                            o.w -= v[4 * q + 3];
+                            d4[q] = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 32; q++)
+                            if (cbeg + q < n) dst[q] -= v[q];
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)p;
+    }
+    return fn;
+}
+
+template <int SPLIT>
+cudaError_t launch_split(const CUtensorMap &map, float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                         int64_t J, const int *slots, int nslot, unsigned *status, int num_sms, cudaStream_t st) {
+    using C = Cfg<SPLIT>;
+    static bool init = false;
+    if (!init) {
+        cudaError_t e = cudaFuncSetAttribute(k_schur_tc<SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        if (e != cudaSuccess) return e;
+        init = true;
+    }
+    const int64_t m2 = n - J - NB;
+    const int64_t tiles = (m2 + TM - 1) / TM;
+    int64_t total = tiles * tiles * nslot;
+    int grid = (int)(total < num_sms ? total : num_sms);
+    k_schur_tc<SPLIT><<<grid, kThreads, C::SMEM, st>>>(map, z32, ld, plane, z32_stride, n, J, slots, nslot, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// Tensor map over the operand packs: dims (K = 256, rows = n, plane = 6, slot = S).
+cudaError_t zs_schur_tc_map(const float *pack, int64_t n, int nslots, int64_t pack_stride, void *map_out) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap *map = reinterpret_cast<CUtensorMap *>(map_out);
+    cuuint64_t dims[4] = {(cuuint64_t)KTOT, (cuuint64_t)n, 6, (cuuint64_t)nslots};
+    cuuint64_t strides[3] = {(cuuint64_t)KTOT * 4, (cuuint64_t)zs_pack_plane(n) * 4, (cuuint64_t)pack_stride * 4};
+    cuuint32_t box[4] = {KC, TM, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (void *)pack, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t zs_launch_schur_tc(const void *map, float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                               int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
+                               cudaStream_t st) {
+    const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
+    if (split) return launch_split<1>(m, z32, ld, plane, z32_stride, n, J, slots, nslot, status, num_sms, st);
+    return launch_split<0>(m, z32, ld, plane, z32_stride, n, J, slots, nslot, status, num_sms, st);
 }

@@ -8,13 +8,15 @@
 // items ("tasks") are the forward blocks 0..nb-1 followed by the backward
 // blocks nb-1..0, interleaved over the frequencies of the batch; a CTA takes
 // the next task from a ticket counter.  Task (b) accumulates the products of
-// its 64 rows of L (or U) with the already-solved blocks, waiting on each
-// block's completion flag, then solves its own 64 x 64 triangle in shared
-// memory and raises its flag.  Every task waits only on tasks with smaller
+// its 64 rows of L (or U) with the already-solved blocks, oldest first,
+// then solves its own 64 x 64 triangle in shared memory.  Blocks of one
+// (frequency, direction) complete in order, so each publishes a single
+// progress word (epoch, blocks done): one acquire load tells a task how many
+// solved blocks it may read.  Every task waits only on tasks with smaller
 // tickets, which were claimed by CTAs already running, so the wait chain
 // always ends; each wait is also bounded (ZS_SPIN_LIMIT) and raises a status
-// bit instead of hanging.  Flags hold the launch's epoch, so they are never
-// cleared.
+// bit instead of hanging.  The words carry the launch's epoch, so they are
+// never cleared.
 //
 // Bound: HBM (each launch reads both triangles once: 8 n^2 bytes per
 // frequency) plus the latency of the dependency chain.
@@ -30,20 +32,22 @@ constexpr int TB = ZS_TB;
 constexpr int kThreads = 256;  // 8 warps, 8 rows each
 constexpr int kLdd = TB + 1;
 
-__device__ __forceinline__ bool warp_wait(const unsigned *flag, unsigned want, unsigned *status, int lane) {
-    int ok = 1;
-    if (lane == 0) ok = zs::wait_flag(flag, want, status) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
+// lane 0 of the warp waits until more than `need` blocks are complete; the
+// warp barrier orders the other lanes' loads after its acquire
+__device__ __forceinline__ long long warp_progress(const unsigned long long *p, unsigned epoch, long long need,
+                                                   unsigned *status, int lane) {
+    long long c = 0;
+    if (lane == 0) c = zs::progress_wait(p, epoch, need, status);
+    c = __shfl_sync(0xffffffffu, c, 0);
     __syncwarp();
-    return ok != 0;
+    return c;
 }
 
 template <int R>
 __global__ void __launch_bounds__(kThreads)
 k_trsv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
        float2 *__restrict__ v, int64_t v_stride, const int *__restrict__ slots, int nslot,
-       unsigned *__restrict__ flags, int64_t flags_stride, unsigned epoch, unsigned *ticket,
-       unsigned *status) {
+       unsigned long long *__restrict__ prog, unsigned epoch, unsigned *ticket, unsigned *status) {
     __shared__ float dre[TB * kLdd], dim_[TB * kLdd];  // diagonal block
     __shared__ cf part[TB][R];                         // accumulated off-diagonal products
     __shared__ unsigned s_task, s_stop;
@@ -68,7 +72,7 @@ k_trsv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
         const float *re = z32 + (int64_t)slot * z32_stride;
         const float *im = re + plane;
         float2 *vs = v + (int64_t)slot * v_stride;
-        unsigned *fl = flags + (int64_t)slot * flags_stride;
+        unsigned long long *pf = prog + 2 * (int64_t)slot, *pb = pf + 1;
         const int64_t r0 = (int64_t)b * TB;
         const int rows = (int)zs::min64(TB, n - r0);
         // diagonal block into shared memory (independent of other tasks)
@@ -88,35 +92,44 @@ k_trsv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
         for (int i = 0; i < 8; i++)
 #pragma unroll
             for (int r = 0; r < R; r++) acc[i][r] = cf{0.f, 0.f};
-        // lane 0 of each warp polls a flag (acquire) and the warp barrier
-        // orders the other lanes' loads after it
+        // solved blocks, oldest first: forward c = 0..b-1, backward c = nblk-1..b+1
         bool ok = true;
-        if (phase == 1) ok = warp_wait(&fl[b], epoch, status, lane);  // own forward result
-        const int cbeg = phase == 0 ? 0 : b + 1;
-        const int cend = phase == 0 ? b : nblk;
-        for (int c = cbeg; c < cend && ok; c++) {
-            ok = warp_wait(&fl[(phase == 0 ? 0 : nblk) + c], epoch, status, lane);
-            if (!ok) break;
+        if (phase == 1) ok = warp_progress(pf, epoch, b, status, lane) >= 0;  // own forward result
+        const int nchunk = phase == 0 ? b : nblk - 1 - b;
+        long long ready = 0;
+        for (int q = 0; q < nchunk && ok;) {
+            if (q >= ready) {
+                ready = warp_progress(phase == 0 ? pf : pb, epoch, q, status, lane);
+                if (ready < 0) {
+                    ok = false;
+                    break;
+                }
+            }
+            const int qend = (int)(ready < nchunk ? ready : nchunk);
+#pragma unroll 2
+            for (; q < qend; q++) {
+                const int c = phase == 0 ? q : nblk - 1 - q;
 #pragma unroll
-            for (int q = 0; q < 2; q++) {
-                const int64_t col = (int64_t)c * TB + lane + 32 * q;
-                if (col < n) {
-                    cf y[R];
+                for (int h = 0; h < 2; h++) {
+                    const int64_t col = (int64_t)c * TB + lane + 32 * h;
+                    if (col < n) {
+                        cf y[R];
 #pragma unroll
-                    for (int r = 0; r < R; r++) {
-                        float2 t2 = __ldcg(&vs[r * n + col]);
-                        y[r] = cf{t2.x, t2.y};
-                    }
+                        for (int r = 0; r < R; r++) {
+                            float2 t2 = __ldcg(&vs[r * n + col]);
+                            y[r] = cf{t2.x, t2.y};
+                        }
 #pragma unroll
-                    for (int i = 0; i < 8; i++) {
-                        const int li = warp * 8 + i;
-                        if (li < rows) {
-                            const int64_t g = (r0 + li) * ld + col;
-                            const cf a = cf{__ldg(re + g), __ldg(im + g)};
+                        for (int i = 0; i < 8; i++) {
+                            const int li = warp * 8 + i;
+                            if (li < rows) {
+                                const int64_t g = (r0 + li) * ld + col;
+                                const cf a = cf{__ldg(re + g), __ldg(im + g)};
 #pragma unroll
-                            for (int r = 0; r < R; r++) {
-                                acc[i][r].re = fmaf(a.re, y[r].re, fmaf(-a.im, y[r].im, acc[i][r].re));
-                                acc[i][r].im = fmaf(a.re, y[r].im, fmaf(a.im, y[r].re, acc[i][r].im));
+                                for (int r = 0; r < R; r++) {
+                                    acc[i][r].re = fmaf(a.re, y[r].re, fmaf(-a.im, y[r].im, acc[i][r].re));
+                                    acc[i][r].im = fmaf(a.re, y[r].im, fmaf(a.im, y[r].re, acc[i][r].im));
+                                }
                             }
                         }
                     }
@@ -204,14 +217,14 @@ k_trsv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
             }
             __threadfence();
             __syncwarp();
-            if (lane == 0) zs::set_flag(&fl[(phase == 0 ? 0 : nblk) + b], epoch);
+            if (lane == 0) zs::progress_set(phase == 0 ? pf : pb, epoch, (unsigned)(phase == 0 ? b + 1 : bq + 1));
         }
     }
 }
 
 template <int R>
 cudaError_t launch_r(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, float2 *v,
-                     int64_t v_stride, const int *slots, int nslot, unsigned *flags, int64_t flags_stride,
+                     int64_t v_stride, const int *slots, int nslot, unsigned long long *prog,
                      unsigned epoch, unsigned *ticket, unsigned *status, int num_sms, cudaStream_t st) {
     int per_sm = 0;
     cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_trsv<R>, kThreads, 0);
@@ -224,8 +237,8 @@ cudaError_t launch_r(const float *z32, int64_t ld, int64_t plane, int64_t z32_st
     e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return e;
     void *args[] = {(void *)&z32, (void *)&ld, (void *)&plane, (void *)&z32_stride, (void *)&n,
-                    (void *)&v, (void *)&v_stride, (void *)&slots, (void *)&nslot, (void *)&flags,
-                    (void *)&flags_stride, (void *)&epoch, (void *)&ticket, (void *)&status};
+                    (void *)&v, (void *)&v_stride, (void *)&slots, (void *)&nslot, (void *)&prog,
+                    (void *)&epoch, (void *)&ticket, (void *)&status};
     e = cudaLaunchCooperativeKernel((const void *)k_trsv<R>, dim3((unsigned)grid), dim3(kThreads), args, 0, st);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
@@ -235,20 +248,20 @@ cudaError_t launch_r(const float *z32, int64_t ld, int64_t plane, int64_t z32_st
 
 cudaError_t zs_launch_trsv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                            float2 *v, int64_t v_stride, int nrhs, const int *slots, int nslot,
-                           unsigned *flags, int64_t flags_stride, unsigned epoch, unsigned *ticket,
+                           unsigned long long *prog, unsigned epoch, unsigned *ticket,
                            unsigned *status, int num_sms, cudaStream_t st) {
     switch (nrhs) {
         case 1:
-            return launch_r<1>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, flags, flags_stride,
+            return launch_r<1>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         case 2:
-            return launch_r<2>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, flags, flags_stride,
+            return launch_r<2>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         case 4:
-            return launch_r<4>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, flags, flags_stride,
+            return launch_r<4>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         case 8:
-            return launch_r<8>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, flags, flags_stride,
+            return launch_r<8>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         default:
             return cudaErrorInvalidValue;

@@ -28,9 +28,10 @@
 #include "../../include/zsolve.h"
 #include "common.cuh"
 
-cudaError_t zs_launch_schur_tc(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                               int64_t J, const float *pack, int64_t pack_stride, int split,
-                               const int *slots, int nslot, cudaStream_t st);
+cudaError_t zs_schur_tc_map(const float *pack, int64_t n, int nslots, int64_t pack_stride, void *map_out);
+cudaError_t zs_launch_schur_tc(const void *map, float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                               int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
+                               cudaStream_t st);
 
 struct zsolve_ctx {
     int64_t n = 0;
@@ -43,6 +44,7 @@ struct zsolve_ctx {
     double2 *z64 = nullptr;
     float *z32 = nullptr;
     float *pack = nullptr;
+    alignas(64) unsigned char pack_map[128] = {};  // TMA tensor map over the operand packs
     float2 *v = nullptr;
     double *partials = nullptr;
     int nchunks = 0;
@@ -51,8 +53,7 @@ struct zsolve_ctx {
     int *d_all = nullptr;    // 0..S-1
     int *d_active = nullptr, *h_active = nullptr;
     int *d_pivflag = nullptr, *h_pivflag = nullptr;
-    unsigned *flags = nullptr;
-    int64_t flags_stride = 0;
+    unsigned long long *prog = nullptr;  // triangular-solve progress words, 2 per slot
     unsigned epoch = 0;
     unsigned *ticket = nullptr;
     unsigned *d_status = nullptr, *h_status = nullptr;
@@ -200,8 +201,8 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
             ZS_CU(zs_launch_schur_simt(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
                                        ctx->pack_stride, slots, nslot, ctx->stream));
         else
-            ZS_CU(zs_launch_schur_tc(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                                     ctx->pack_stride, mode == 2 ? 1 : 0, slots, nslot, ctx->stream));
+            ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J,
+                                     mode == 2 ? 1 : 0, slots, nslot, ctx->d_status, ctx->num_sms, ctx->stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
@@ -218,8 +219,8 @@ int lowprec_solve_slots(zsolve_ctx *ctx, int nrhs, const int *slots, int nslot) 
         ctx->epoch++;
         StageSpan sp(ctx, ZSOLVE_STAGE_TRSV);
         ZS_CU(zs_launch_trsv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->v + (int64_t)r0 * ctx->n,
-                             ctx->v_stride, R, slots, nslot, ctx->flags, ctx->flags_stride, ctx->epoch,
-                             ctx->ticket, ctx->d_status, ctx->num_sms, ctx->stream));
+                             ctx->v_stride, R, slots, nslot, ctx->prog, ctx->epoch, ctx->ticket, ctx->d_status,
+                             ctx->num_sms, ctx->stream));
         sp.done(1);
         r0 += R;
     }
@@ -232,7 +233,7 @@ int check_device_status(zsolve_ctx *ctx) {
     if (*ctx->h_status & ZS_DEV_TIMEOUT) {
         *ctx->h_status = 0;
         ZS_CU(cudaMemsetAsync(ctx->d_status, 0, sizeof(unsigned), ctx->stream));
-        return fail(ctx, ZSOLVE_ETIMEOUT, "a device-side wait in the triangular solve gave up");
+        return fail(ctx, ZSOLVE_ETIMEOUT, "a bounded device-side wait gave up (triangular solve or trailing update)");
     }
     return ZSOLVE_OK;
 }
@@ -447,7 +448,7 @@ void free_all(zsolve_ctx *c) {
     cudaFreeHost(c->h_active);
     cudaFree(c->d_pivflag);
     cudaFreeHost(c->h_pivflag);
-    cudaFree(c->flags);
+    cudaFree(c->prog);
     cudaFree(c->ticket);
     cudaFree(c->d_status);
     cudaFreeHost(c->h_status);
@@ -524,8 +525,6 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     }
     if (ctx->S > 64) ctx->S = 64;
     const int S = ctx->S;
-    const int64_t nblk = (n + ZS_TB - 1) / ZS_TB;
-    ctx->flags_stride = 2 * nblk;
     ctx->nchunks = zs_update_chunks(n);
 #define ALLOC(p, bytes) \
     if (cudaMalloc(&(p), (bytes)) != cudaSuccess) return bail(ZSOLVE_ENOMEM)
@@ -545,7 +544,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOCH(ctx->h_active, S * sizeof(int));
     ALLOC(ctx->d_pivflag, S * sizeof(int));
     ALLOCH(ctx->h_pivflag, S * sizeof(int));
-    ALLOC(ctx->flags, (size_t)S * ctx->flags_stride * sizeof(unsigned));
+    ALLOC(ctx->prog, (size_t)S * 2 * sizeof(unsigned long long));
     ALLOC(ctx->ticket, sizeof(unsigned));
     ALLOC(ctx->d_status, sizeof(unsigned));
     ALLOCH(ctx->h_status, sizeof(unsigned));
@@ -553,10 +552,13 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
 #undef ALLOCH
     for (auto &e : ctx->ev)
         if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
+    if (gemm_mode(ctx->opts) != 0 &&
+        zs_schur_tc_map(ctx->pack, n, S, ctx->pack_stride, ctx->pack_map) != cudaSuccess)
+        return bail(ZSOLVE_ECUDA);
     std::vector<int> all(S);
     for (int s = 0; s < S; s++) all[s] = s;
     if (cudaMemcpy(ctx->d_all, all.data(), S * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(ctx->flags, 0, (size_t)S * ctx->flags_stride * sizeof(unsigned)) != cudaSuccess ||
+        cudaMemset(ctx->prog, 0, (size_t)S * 2 * sizeof(unsigned long long)) != cudaSuccess ||
         cudaMemset(ctx->d_status, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(ctx->d_pivflag, 0, S * sizeof(int)) != cudaSuccess ||
         cudaMemset(ctx->z32, 0, (size_t)S * ctx->z32_stride * sizeof(float)) != cudaSuccess)
