@@ -327,7 +327,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=1)
-    ap.add_argument("--gemm", default="FFMA", choices=["TF32", "TF32X3", "FFMA"])
+    ap.add_argument("--gemm", default="TF32X3", choices=["TF32", "TF32X3", "FFMA"])
     ap.add_argument("--batch", type=int, default=0)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

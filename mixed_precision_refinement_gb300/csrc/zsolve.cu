@@ -162,9 +162,9 @@ struct StageSpan {
 
 int gemm_mode(const zsolve_opts &o) {
     switch (o.gemm) {
+        case ZSOLVE_GEMM_FFMA: return 0;
         case ZSOLVE_GEMM_TF32: return 1;
-        case ZSOLVE_GEMM_TF32X3: return 2;
-        default: return 0;  // FFMA and AUTO
+        default: return 2;  // TF32X3 and AUTO
     }
 }
 
