@@ -180,6 +180,39 @@ int zsolve_get_profile(zsolve_ctx *ctx, zsolve_profile *out);
 /* Zero the counters of zsolve_get_profile. */
 int zsolve_reset_profile(zsolve_ctx *ctx);
 
+/* Allocation-free low-precision solve.  The page has no counterpart: this
+ * entry point exists for callers that cannot allocate device memory where
+ * they need a solve -- a memory-pool-managed application that forbids stray
+ * cudaMalloc calls, a real-time loop that may not allocate (or trigger the
+ * implicit synchronisation an allocation can cause), a plug-in whose host
+ * framework owns all device memory.  It applies float32 factors the caller
+ * already holds (for instance copied out with zsolve_get_z32) and allocates
+ * nothing: no cudaMalloc, no cudaFree, no allocating library call.
+ *
+ *   z32        device: system s has its real plane at z32 + s*sys_stride and
+ *              its imaginary plane at z32 + s*sys_stride + plane, each n rows
+ *              of stride ld floats, holding the packed unit-lower L and upper
+ *              U of the unpivoted LU (the layout zsolve_get_z32 writes with
+ *              ld = n, plane = n*n)
+ *   v          device, complex float32 interleaved (re, im): system s holds
+ *              nrhs rows of n values at v + s*v_stride (complex elements);
+ *              overwritten by (L U)^-1 v
+ *   nsys       1 .. 64 systems solved together (more: ZSOLVE_EINVAL)
+ *   stream     cudaStream_t, NULL = default stream
+ *
+ * Its scratch (progress words, work ticket, status word, system list) is a
+ * statically sized __device__ array of about 1.3 KB inside the library,
+ * held by every GPU that loads the library until the process exits.  The
+ * first call on a device sets the array up (looks up its device address and
+ * writes the system list) with that device current; make that first call
+ * before any stream capture.  Every call shares the array and each call
+ * clears what must start at zero, so calls that overlap on the GPU (two
+ * streams, two host threads) race: serialise them.  Returns after the solve
+ * has finished (it synchronises `stream`); ZSOLVE_ETIMEOUT if a bounded
+ * device-side wait gave up. */
+int zsolve_lowprec_solve_noalloc(const float *z32, int64_t ld, int64_t plane, int64_t sys_stride, int64_t n,
+                                 int nsys, void *v, int64_t v_stride, int nrhs, void *stream);
+
 /* Static string for a status code. */
 const char *zsolve_strerror(int status);
 

@@ -87,6 +87,7 @@ def _load():
         "zsolve_get_z64": (I, [P, P]),
         "zsolve_get_z32": (I, [P, P, P]),
         "zsolve_pivot_flag": (I, [P, ctypes.POINTER(I)]),
+        "zsolve_lowprec_solve_noalloc": (I, [P, I64, I64, I64, I64, I, P, I64, I, P]),
         "zsolve_get_profile": (I, [P, ctypes.POINTER(zsolve_profile)]),
         "zsolve_reset_profile": (I, [P]),
         "zsolve_strerror": (ctypes.c_char_p, [I]),
@@ -259,6 +260,19 @@ def zsolve_pivot_flag(ctx) -> int:
     f = ctypes.c_int()
     _check(ctx, _lib.zsolve_pivot_flag(ctx, ctypes.byref(f)))
     return f.value
+
+
+def zsolve_lowprec_solve_noalloc(z32, ld: int, plane: int, sys_stride: int, n: int, nsys: int, v,
+                                 v_stride: int, nrhs: int, stream=None) -> None:
+    """v (complex64 CUDA tensor) <- (L U)^-1 v with caller-held float32 factors, allocating nothing."""
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    handle = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    if v.dtype != torch.complex64 or not v.is_cuda:
+        raise TypeError("v must be a complex64 CUDA tensor")
+    _check(None, _lib.zsolve_lowprec_solve_noalloc(_ptr(z32), ld, plane, sys_stride, n, nsys, _ptr(v), v_stride,
+                                                   nrhs, ctypes.c_void_p(handle)))
 
 
 def zsolve_get_profile(ctx) -> zsolve_profile:

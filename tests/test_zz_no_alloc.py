@@ -1,0 +1,91 @@
+"""The allocation-free solve (zsolve_lowprec_solve_noalloc) against the
+context-based one (zsolve_lowprec_solve), through the C-ABI.
+
+It is for callers that cannot allocate device memory where they solve (a
+pool-managed application, a real-time loop, a plug-in whose host framework
+owns device memory): its scratch is a static device array inside the
+library.  This file is collected last so that a failure here cannot hide the
+result of any other test; it passes alone in a fresh process too, because
+the entry point sets its scratch up on its first call.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import workload
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-6  # same kernel, same float32 factors and inputs: agreement to float32 rounding
+
+
+def _factored(zs, torch, wl, f):
+    s = zs.Solver(wl.n, wl.B.shape[0])
+    zs.zsolve_assemble(s.ctx, torch.from_numpy(wl.L).cuda(), torch.from_numpy(wl.Psi).cuda(),
+                       torch.from_numpy(wl.G).cuda(), wl.omega[f], wl.zs[f].real, wl.zs[f].imag)
+    zs.zsolve_factor(s.ctx)
+    return s
+
+
+def _rel(a, b):
+    return np.linalg.norm(a - b, axis=-1) / np.linalg.norm(b, axis=-1)
+
+
+def test_noalloc_solve_matches_context_solve_on_two_calls():
+    import torch
+
+    import mixed_precision_refinement_gb300 as zs
+
+    n, nrhs = 300, 3  # 3 right-hand sides: two launches (2 + 1) inside each call
+    wl = workload.make_small(n, seed=77, nf=1, nrhs=nrhs)
+    s = _factored(zs, torch, wl, 0)
+    try:
+        fac = torch.empty(2 * n * n, dtype=torch.float32, device="cuda")
+        zs.zsolve_get_z32(s.ctx, fac[: n * n], fac[n * n:])
+        b = torch.from_numpy(wl.B).cuda()
+        ref = torch.empty_like(b)
+        zs.zsolve_lowprec_solve(s.ctx, b, ref)
+        ref = ref.cpu().numpy()
+        lib = zs.raw_lib()
+        for _ in range(2):  # the second call finds the previous call's scratch contents
+            v = b.to(torch.complex64).contiguous()
+            st = lib.zsolve_lowprec_solve_noalloc(fac.data_ptr(), n, n * n, 2 * n * n, n, 1, v.data_ptr(),
+                                                  nrhs * n, nrhs,
+                                                  ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+            assert st == zs.ZSOLVE_OK, zs.zsolve_strerror(st)
+            got = v.cpu().numpy().astype(np.complex128)
+            assert np.all(_rel(got, ref) <= TOL)
+    finally:
+        s.close()
+
+
+def test_noalloc_solve_two_systems_and_limits():
+    import torch
+
+    import mixed_precision_refinement_gb300 as zs
+
+    n, nrhs = 150, 1
+    wl = workload.make_small(n, seed=78, nf=2, nrhs=nrhs)
+    fac = torch.empty(2, 2 * n * n, dtype=torch.float32, device="cuda")
+    refs = []
+    b = torch.from_numpy(wl.B).cuda()
+    for f in range(2):
+        s = _factored(zs, torch, wl, f)
+        try:
+            zs.zsolve_get_z32(s.ctx, fac[f, : n * n], fac[f, n * n:])
+            r = torch.empty_like(b)
+            zs.zsolve_lowprec_solve(s.ctx, b, r)
+            refs.append(r.cpu().numpy())
+        finally:
+            s.close()
+    for _ in range(2):
+        v = torch.stack([b, b]).to(torch.complex64).contiguous()
+        zs.zsolve_lowprec_solve_noalloc(fac, n, n * n, 2 * n * n, n, 2, v, nrhs * n, nrhs)
+        got = v.cpu().numpy().astype(np.complex128)
+        for f in range(2):
+            assert np.all(_rel(got[f], refs[f]) <= TOL)
+    lib = zs.raw_lib()
+    v = torch.zeros(65 * n, dtype=torch.complex64, device="cuda")
+    assert lib.zsolve_lowprec_solve_noalloc(fac.data_ptr(), n, n * n, 2 * n * n, n, 65, v.data_ptr(), n, 1,
+                                            None) == zs.ZSOLVE_EINVAL
