@@ -221,10 +221,8 @@ def run_ours(args):
     clocks = sampler.stop() if sampler else None
     ms = sum(a.elapsed_time(bb) for a, bb in ev)
     prof = zs.zsolve_get_profile(ctx).as_dict()
-    if dist:
-        t = torch.tensor([ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    from mixed_precision_refinement_gb300 import sharding
+    ms = sharding.max_over_ranks(ms, device="cuda")
     ms_step = ms / args.steps
     value = ws * nf / (ms_step / 1e3)
 
@@ -240,10 +238,7 @@ def run_ours(args):
     for _ in range(args.steps):
         zs.zsolve_sweep_host(ctx, Lh, Ph, Gh, wl.omega, wl.zs, bh, xh)
     e2e_s = (time.perf_counter() - t0) / args.steps
-    if dist:
-        t = torch.tensor([e2e_s], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = sharding.max_over_ranks(e2e_s, device="cuda")
     if dist:
         dist.destroy_process_group()
     if rank != 0:
