@@ -25,7 +25,10 @@
 // fp32) into a ring of shared-memory stages; warp 1 owns TMEM (512 columns:
 // two accumulators, so the epilogue of one tile overlaps the MMAs of the
 // next) and issues the MMAs from one thread; warps 2-5 drain the accumulator
-// with tcgen05.ld and subtract it from the float32 trailing matrix.  Every
+// with tcgen05.ld, stage the negated values in shared memory (128B swizzle,
+// double-buffered per warp) and subtract them from the float32 trailing
+// matrix with TMA reduce-add stores, so the L2 does the read-modify-write and
+// the epilogue issues no global loads.  Every
 // mbarrier wait is bounded: on give-up the kernel raises a status bit, stops
 // all roles, waits (bounded) for its own copies and MMAs and frees TMEM.
 #include <cuda.h>
@@ -48,11 +51,14 @@ constexpr uint32_t kWaitLimit = 1u << 26;
 
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
 
+constexpr int EPI_BOX = 32 * 32 * 4;  // one 32-row x 32-column fp32 box (4 KB)
+constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;  // 4 epilogue warps x 2 staging buffers
+
 template <int SPLIT>
 struct Cfg {
     static constexpr int STAGE_BYTES = SPLIT ? 2 * (A_BYTES + B_BYTES) : (A_BYTES + B_BYTES);
     static constexpr int STAGES = SPLIT ? 2 : 4;
-    static constexpr int SMEM = STAGES * STAGE_BYTES + 1024;  // + alignment slack
+    static constexpr int SMEM = STAGES * STAGE_BYTES + EPI_BYTES + 1024;  // + alignment slack
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -107,6 +113,26 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map
         "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
         : "memory");
 }
+
+// Subtract a staged 32x32 box from the trailing matrix: TMA reduce-add (fp32)
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2,
+                                                  int c3) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%1, %2, %3, %4}], [%5];" ::"l"((uint64_t)map),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// wait until at most N committed groups are still reading their shared source
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
 // 128 bytes, 8-row core groups 1024 bytes apart.
@@ -167,9 +193,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 
 template <int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
-k_schur_tc(const __grid_constant__ CUtensorMap tmap, float *__restrict__ z32, int64_t ld, int64_t plane,
-           int64_t z32_stride, int64_t n, int64_t J, const int *__restrict__ slots, int nslot,
-           unsigned *__restrict__ status) {
+k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap cmap, int64_t n,
+           int64_t J, const int *__restrict__ slots, int nslot, unsigned *__restrict__ status) {
     using C = Cfg<SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[C::STAGES], bar_empty[C::STAGES], bar_accf[2], bar_acce[2], bar_drain;
@@ -300,7 +325,9 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, float *__restrict__ z32, in
     } else {
         // ------------------------------------------------ epilogue (warps 2-5)
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
-        uint32_t it = 0;
+        const uint32_t stage0 = base_addr + C::STAGES * C::STAGE_BYTES + (uint32_t)(warp - 2) * 2u * EPI_BOX;
+        uint32_t it = 0, nbox = 0;
+        if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&cmap) : "memory");
         for (int t = blockIdx.x; t < total; t += gridDim.x, it++) {
             const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
             const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status);
@@ -309,38 +336,38 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, float *__restrict__ z32, in
             const int si = t / per_slot, rem = t - si * per_slot;
             const int tm = rem / tiles, tn = rem - tm * tiles;
             const int slot = slots[si];
-            float *cre = z32 + (int64_t)slot * z32_stride;
-            const int64_t row = base + (int64_t)tm * TM + quad * 32 + lane;
-            const int64_t col0 = base + (int64_t)tn * TN;
+            const int row0 = (int)(base + (int64_t)tm * TM) + quad * 32;
+            const int col0 = (int)(base + (int64_t)tn * TN);
 #pragma unroll 1
-            for (int c = 0; c < 8; c++) {
+            for (int c = 0; c < 8; c++, nbox++) {
                 float v[32];
                 tmem_ld32(tmem + buf * 256u + (uint32_t)(c * 32) + ((uint32_t)(quad * 32) << 16), v);
-                if (row < n) {
-                    float *dst = cre + (c >= 4 ? plane : 0) + row * ld + col0 + (c & 3) * 32;
-                    const int64_t cbeg = col0 + (c & 3) * 32;
-                    if (cbeg + 32 <= n) {
-                        float4 *d4 = reinterpret_cast<float4 *>(dst);
+                if (c == 7) {  // accumulator fully read: hand it back to the MMA warp
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
+                }
+                const uint32_t sb = stage0 + (nbox & 1u) * EPI_BOX;
+                if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read its source
+                __syncwarp();
+                // row `lane` of the box, 128B-swizzled: 16-byte unit j at (j ^ (row & 7))
 #pragma unroll
-                        for (int q = 0; q < 8; q++) {
-                            float4 o = d4[q];
-                            o.x -= v[4 * q];
-                            o.y -= v[4 * q + 1];
-                            o.z -= v[4 * q + 2];
-                            o.w -= v[4 * q + 3];
-                            d4[q] = o;
-                        }
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < 32; q++)
-                            if (cbeg + q < n) dst[q] -= v[q];
-                    }
+                for (int j = 0; j < 8; j++) {
+                    const uint32_t a = sb + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16);
+                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(-v[4 * j]),
+                                 "f"(-v[4 * j + 1]), "f"(-v[4 * j + 2]), "f"(-v[4 * j + 3])
+                                 : "memory");
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    tma_reduce_add_4d(&cmap, sb, col0 + (c & 3) * 32, row0, c >> 2, slot);
+                    bulk_commit();
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
         }
+        if (lane == 0) bulk_wait_all();  // our own stores are complete before exit
+        __syncwarp();
     }
     tc_fence_before();
     __syncthreads();
@@ -364,8 +391,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 }
 
 template <int SPLIT>
-cudaError_t launch_split(const CUtensorMap &map, float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                         int64_t J, const int *slots, int nslot, unsigned *status, int num_sms, cudaStream_t st) {
+cudaError_t launch_split(const CUtensorMap &map, const CUtensorMap &cmap, int64_t n, int64_t J, const int *slots,
+                         int nslot, unsigned *status, int num_sms, cudaStream_t st) {
     using C = Cfg<SPLIT>;
     static bool init = false;
     if (!init) {
@@ -377,7 +404,7 @@ cudaError_t launch_split(const CUtensorMap &map, float *z32, int64_t ld, int64_t
     const int64_t tiles = (m2 + TM - 1) / TM;
     int64_t total = tiles * tiles * nslot;
     int grid = (int)(total < num_sms ? total : num_sms);
-    k_schur_tc<SPLIT><<<grid, kThreads, C::SMEM, st>>>(map, z32, ld, plane, z32_stride, n, J, slots, nslot, status);
+    k_schur_tc<SPLIT><<<grid, kThreads, C::SMEM, st>>>(map, cmap, n, J, slots, nslot, status);
     return cudaGetLastError();
 }
 
@@ -398,10 +425,27 @@ cudaError_t zs_schur_tc_map(const float *pack, int64_t n, int nslots, int64_t pa
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t zs_launch_schur_tc(const void *map, float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                               int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
-                               cudaStream_t st) {
+// Tensor map over the float32 trailing matrix: dims (column = n, row = n,
+// plane = 2 (re, im), slot = S), boxes of 32 x 32 for the reduce-add epilogue.
+cudaError_t zs_schur_tc_cmap(const float *z32, int64_t n, int64_t ld, int64_t plane, int nslots, int64_t z32_stride,
+                             void *map_out) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap *map = reinterpret_cast<CUtensorMap *>(map_out);
+    cuuint64_t dims[4] = {(cuuint64_t)n, (cuuint64_t)n, 2, (cuuint64_t)nslots};
+    cuuint64_t strides[3] = {(cuuint64_t)ld * 4, (cuuint64_t)plane * 4, (cuuint64_t)z32_stride * 4};
+    cuuint32_t box[4] = {32, 32, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (void *)z32, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
+                               int nslot, unsigned *status, int num_sms, cudaStream_t st) {
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
-    if (split) return launch_split<1>(m, z32, ld, plane, z32_stride, n, J, slots, nslot, status, num_sms, st);
-    return launch_split<0>(m, z32, ld, plane, z32_stride, n, J, slots, nslot, status, num_sms, st);
+    const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
+    if (split) return launch_split<1>(m, c, n, J, slots, nslot, status, num_sms, st);
+    return launch_split<0>(m, c, n, J, slots, nslot, status, num_sms, st);
 }

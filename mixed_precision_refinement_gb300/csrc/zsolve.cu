@@ -29,9 +29,10 @@
 #include "common.cuh"
 
 cudaError_t zs_schur_tc_map(const float *pack, int64_t n, int nslots, int64_t pack_stride, void *map_out);
-cudaError_t zs_launch_schur_tc(const void *map, float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                               int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
-                               cudaStream_t st);
+cudaError_t zs_schur_tc_cmap(const float *z32, int64_t n, int64_t ld, int64_t plane, int nslots, int64_t z32_stride,
+                             void *map_out);
+cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
+                               int nslot, unsigned *status, int num_sms, cudaStream_t st);
 
 struct zsolve_ctx {
     int64_t n = 0;
@@ -45,6 +46,7 @@ struct zsolve_ctx {
     float *z32 = nullptr;
     float *pack = nullptr;
     alignas(64) unsigned char pack_map[128] = {};  // TMA tensor map over the operand packs
+    alignas(64) unsigned char z32_map[128] = {};   // TMA tensor map over the float32 matrices
     float2 *v = nullptr;
     double *partials = nullptr;
     int nchunks = 0;
@@ -201,8 +203,8 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
             ZS_CU(zs_launch_schur_simt(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
                                        ctx->pack_stride, slots, nslot, ctx->stream));
         else
-            ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J,
-                                     mode == 2 ? 1 : 0, slots, nslot, ctx->d_status, ctx->num_sms, ctx->stream));
+            ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, mode == 2 ? 1 : 0, slots, nslot,
+                                     ctx->d_status, ctx->num_sms, ctx->stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
@@ -553,7 +555,8 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     for (auto &e : ctx->ev)
         if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
     if (gemm_mode(ctx->opts) != 0 &&
-        zs_schur_tc_map(ctx->pack, n, S, ctx->pack_stride, ctx->pack_map) != cudaSuccess)
+        (zs_schur_tc_map(ctx->pack, n, S, ctx->pack_stride, ctx->pack_map) != cudaSuccess ||
+         zs_schur_tc_cmap(ctx->z32, n, ctx->ld, ctx->plane, S, ctx->z32_stride, ctx->z32_map) != cudaSuccess))
         return bail(ZSOLVE_ECUDA);
     std::vector<int> all(S);
     for (int s = 0; s < S; s++) all[s] = s;
