@@ -6,13 +6,26 @@
 // One pass reads L, Psi, G once and, for every frequency of the batch, writes
 // the float64 matrix (interleaved complex, kept for the double-precision
 // residual) and its round-to-nearest complex float32 copy (two planes, padded
-// rows, to be factorised).  Every float64 operation is rounded separately and
-// in the order the formula is written -- Zs.re*G for the real part,
-// (omega*L - Psi/omega) + Zs.im*G for the imaginary part -- so the float64
-// matrix is the correctly rounded evaluation of that expression.
+// rows, to be factorised).  The float64 matrix is the correctly rounded
+// evaluation of the formula in the order it is written -- Zs.re*G for the
+// real part, (omega*L - Psi/omega) + Zs.im*G for the imaginary part, each
+// operation rounded once -- computed with few FP64-pipe instructions, since
+// that pipe, not HBM, bounds this kernel on GB300:
+//  - Psi/omega: q0 = Psi*r with r = RN(1/omega) from the host, then one
+//    correction q = RN(q0 + (Psi - omega*q0)*r) with the remainder exact by
+//    FMA; this gives the correctly rounded quotient (P. Markstein, "Computation
+//    of elementary functions on the IBM RISC System/6000 processor", IBM J.
+//    Res. Dev. 1990, the division theorem); a zero q0 is returned as is, so a
+//    -0 dividend keeps its sign;
+//  - where G_ij = 0 (all but three diagonals in the generated workloads)
+//    Zs*G is an exact zero, so the products are skipped and only the sign of
+//    zero they would produce is reproduced (integer ops);
+//  - float64 -> float32 round-to-nearest-even is done on the integer bit
+//    pattern, with the hardware conversion kept for subnormal results,
+//    overflow and NaN.
 //
-// Bound: HBM.  Algorithmic bytes per launch = 24 n^2 (read) + 24 n^2 per
-// frequency (16 written as float64 complex, 8 as float32 complex).
+// Bound: FP64 pipe (then HBM).  Algorithmic bytes per launch = 24 n^2 (read)
+// + 24 n^2 per frequency (16 written as float64 complex, 8 as float32 complex).
 #include "common.cuh"
 
 namespace {
@@ -20,11 +33,51 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxSlots = 64;
 
+// round-to-nearest-even float64 -> float32 from the bit pattern
+__device__ __forceinline__ float d2f_rn(double x) {
+    const unsigned long long b = (unsigned long long)__double_as_longlong(x);
+    const unsigned hi = (unsigned)(b >> 32), lo = (unsigned)b;
+    if ((b << 1) == 0) return __uint_as_float(hi & 0x80000000u);  // signed zero
+    const unsigned e = (hi >> 20) & 0x7FFu;
+    if (e < 897u || e > 1150u) return __double2float_rn(x);  // subnormal result, overflow, inf/nan
+    const unsigned fm = ((hi & 0xFFFFFu) << 3) | (lo >> 29);  // top 23 mantissa bits
+    const unsigned rest = lo & 0x1FFFFFFFu;                    // 29 bits rounded away
+    unsigned f = ((e - 896u) << 23) | fm;
+    f += (rest > 0x10000000u || (rest == 0x10000000u && (fm & 1u))) ? 1u : 0u;  // carry may bump the exponent
+    return __uint_as_float(f | (hi & 0x80000000u));
+}
+
+// Z64[e] and both float32 planes for one frequency
+__device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, double p, double g, bool gzero,
+                                          double2 *__restrict__ z64e, float *__restrict__ z32e, int64_t plane) {
+    const double w = sp.omega, r = sp.pad;  // pad holds RN(1/omega)
+    const double q0 = __dmul_rn(p, r);
+    // RN(p / w); a zero first quotient is already exact (and keeps its sign)
+    const double q = (__double_as_longlong(q0) & 0x7FFFFFFFFFFFFFFFll) == 0 ? q0 : __fma_rn(__fma_rn(-w, q0, p), r, q0);
+    const double t = __dsub_rn(__dmul_rn(w, l), q);
+    double re, im;
+    if (gzero) {
+        // Zs.re * (+-0) and t + Zs.im * (+-0): exact zeros; only signs of zero to reproduce
+        const long long gs = __double_as_longlong(g) & (long long)0x8000000000000000ull;
+        const long long zr = (__double_as_longlong(sp.zs_re) & (long long)0x8000000000000000ull) ^ gs;
+        const long long zi = (__double_as_longlong(sp.zs_im) & (long long)0x8000000000000000ull) ^ gs;
+        re = __longlong_as_double(zr);
+        const long long tb = __double_as_longlong(t);
+        // t + z: equals t unless t is a zero; (-0) + (-0) = -0, any other pair of zeros = +0
+        im = ((tb & 0x7FFFFFFFFFFFFFFFll) != 0) ? t : __longlong_as_double(tb & zi);
+    } else {
+        re = __dmul_rn(sp.zs_re, g);
+        im = __dadd_rn(t, __dmul_rn(sp.zs_im, g));
+    }
+    __stcs(z64e, make_double2(re, im));
+    __stcs(z32e, d2f_rn(re));
+    __stcs(z32e + plane, d2f_rn(im));
+}
+
 __global__ void __launch_bounds__(kThreads)
-k_assemble(const double *__restrict__ L, const double *__restrict__ Psi,
-           const double *__restrict__ G, int64_t n, const ZsSlotParam *__restrict__ params,
-           int nslot, double2 *__restrict__ z64, int64_t z64_stride, float *__restrict__ z32,
-           int64_t ld, int64_t plane, int64_t z32_stride) {
+k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const double *__restrict__ G, int64_t n,
+           const ZsSlotParam *__restrict__ params, int nslot, double2 *__restrict__ z64, int64_t z64_stride,
+           float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride) {
     __shared__ ZsSlotParam sp[kMaxSlots];
     for (int s = threadIdx.x; s < nslot; s += blockDim.x) sp[s] = params[s];
     __syncthreads();
@@ -33,17 +86,19 @@ k_assemble(const double *__restrict__ L, const double *__restrict__ Psi,
         for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
             const int64_t e = row + j, o32 = row32 + j;
             const double l = __ldcs(L + e), p = __ldcs(Psi + e), g = __ldcs(G + e);
+            const bool gzero = (__double_as_longlong(g) & 0x7FFFFFFFFFFFFFFFll) == 0;
+            // four frequencies at a time: independent FP64 chains to cover the unit's latency
+            int s = 0;
 #pragma unroll 1
-            for (int s = 0; s < nslot; s++) {
-                const double w = sp[s].omega;
-                const double re = __dmul_rn(sp[s].zs_re, g);
-                const double im = __dadd_rn(__dsub_rn(__dmul_rn(w, l), __ddiv_rn(p, w)),
-                                            __dmul_rn(sp[s].zs_im, g));
-                __stcs(z64 + s * z64_stride + e, make_double2(re, im));
-                float *zr = z32 + s * z32_stride;
-                __stcs(zr + o32, __double2float_rn(re));
-                __stcs(zr + plane + o32, __double2float_rn(im));
+            for (; s + 4 <= nslot; s += 4) {
+#pragma unroll
+                for (int u = 0; u < 4; u++) one_entry(sp[s + u], l, p, g, gzero, z64 + (s + u) * z64_stride + e,
+                                                      z32 + (s + u) * z32_stride + o32, plane);
             }
+#pragma unroll 1
+            for (; s < nslot; s++)
+                one_entry(sp[s], l, p, g, gzero, z64 + s * z64_stride + e, z32 + s * z32_stride + o32, plane);
+
         }
     }
 }

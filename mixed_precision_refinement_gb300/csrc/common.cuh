@@ -6,8 +6,9 @@
 
 #define ZS_NB 128           // outer block: columns factored per step of the blocked LU
 #define ZS_PANEL 32         // panel width inside the outer block ("LU in blocks of 32")
-#define ZS_TB 64            // row block of the triangular solves
-#define ZS_SPIN_LIMIT (1u << 26)  // bounded waits: iterations before a wait gives up
+#define ZS_TB 64            // row block of the sequential-diagonal triangular solve
+#define ZS_TB2 128          // row block of the inverse-diagonal triangular solve
+#define ZS_SPIN_LIMIT (1u << 22)  // bounded waits: polls (>= 64 ns apart) before a wait gives up
 
 // device status bits (one word per context)
 #define ZS_DEV_TIMEOUT 1u
@@ -53,7 +54,7 @@ __device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned want, u
         }
         // another wait already gave up: stop too, so the launch ends promptly
         if ((it & 1023u) == 0 && (*(volatile const unsigned *)status & ZS_DEV_TIMEOUT)) return false;
-        if (it > 64) __nanosleep(64);
+        if (it > 64) __nanosleep(256);
     }
 }
 
@@ -77,7 +78,7 @@ __device__ __forceinline__ long long progress_wait(const unsigned long long *p, 
             return -1;
         }
         if ((it & 1023u) == 0 && (*(volatile const unsigned *)status & ZS_DEV_TIMEOUT)) return -1;
-        if (it > 32) __nanosleep(32);
+        if (it > 32) __nanosleep(it > 4096 ? 256 : 32);
     }
 }
 
@@ -96,7 +97,8 @@ __device__ __forceinline__ bool timed_out(const unsigned *status) {
 
 }  // namespace zs
 
-// Per-slot parameters of a batch (one slot = one frequency being solved).
+// Per-slot parameters of a batch (one slot = one frequency being solved);
+// pad carries RN(1/omega), computed on the host.
 struct ZsSlotParam {
     double omega, zs_re, zs_im, pad;
 };
@@ -112,16 +114,19 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
                                cudaStream_t st);
 
 // Factorisation steps at outer-block column J for nslot slots listed in slots[].
+// inv32: per slot ZS_INV32_STRIDE floats, [sub-block kb][U, L][re, im][32][32]:
+// inverses of the four 32x32 diagonal sub-blocks of U11 and of L11.
+#define ZS_INV32_STRIDE (4 * 2 * 2 * 32 * 32)
 cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                              int64_t J, int nb, const int *slots, int nslot, int *pivflag,
+                              int64_t J, int nb, const int *slots, int nslot, int *pivflag, float *inv32,
                               cudaStream_t st);
 // mode: 0 = pack plain fp32 (FFMA), 1 = tf32 rounded (TF32), 2 = tf32 hi + lo (TF32X3)
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
-                             int nslot, cudaStream_t st);
+                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
+                             const int *slots, int nslot, cudaStream_t st);
 cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
-                             int nslot, cudaStream_t st);
+                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
+                             const int *slots, int nslot, cudaStream_t st);
 cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                  int64_t J, const float *pack, int64_t pack_stride, const int *slots,
                                  int nslot, cudaStream_t st);
@@ -137,10 +142,22 @@ __host__ __device__ inline int64_t zs_pack_plane(int64_t n) { return n * (int64_
 // Triangular solves with the float32 factors: v (c64 interleaved, per active
 // slot nrhs rows of n) is overwritten by (LU)^-1 v.
 // prog: two in-order progress words (forward, backward) per slot.
-cudaError_t zs_launch_trsv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+// Sequential 64x64 diagonal solves; needs no data beyond the factors.
+cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                            float2 *v, int64_t v_stride, int nrhs, const int *slots, int nslot,
                            unsigned long long *prog, unsigned epoch, unsigned *ticket,
                            unsigned *status, int num_sms, cudaStream_t st);
+
+// Inverses of the 128x128 diagonal blocks of L (unit lower) and U (upper):
+// per slot [block][L, U][re, im][128][128] floats.
+cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, float *dinv,
+                               int64_t dinv_stride, const int *slots, int nslot, cudaStream_t st);
+inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }
+// Triangular solves with 128-row blocks and the inverse diagonal blocks; nrhs 1, 2 or 4 per launch.
+cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                               const float *dinv, int64_t dinv_stride, float2 *v, int64_t v_stride, int nrhs,
+                               const int *slots, int nslot, unsigned long long *prog, unsigned epoch, unsigned *ticket,
+                               unsigned *status, int num_sms, cudaStream_t st);
 
 // r = b - Z64 x.  out_c64 != NULL: writes float2 (rounded); else writes c128 to out_c128.
 // Launches one kernel per chunk of 8/4/2/1 right-hand sides (zs_rhs_chunks).

@@ -52,7 +52,7 @@ constexpr int kDiagThreads = 512;  // 16 warps
 
 __global__ void __launch_bounds__(kDiagThreads, 1)
 k_diag_lu(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
-          const int *__restrict__ slots, int *__restrict__ pivflag) {
+          const int *__restrict__ slots, int *__restrict__ pivflag, float *__restrict__ inv32) {
     extern __shared__ float sm[];
     float *sre = sm;                   // [NB][LDS]
     float *sim = sm + NB * LDS;        // [NB][LDS]
@@ -200,150 +200,303 @@ k_diag_lu(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride
         im[g] = sim[i * LDS + j];
     }
     if (tid == 0 && flagged) pivflag[slot] = 1;
+    if (nb < NB) return;  // last block: no block solves follow
+    // Inverses of the four 32x32 diagonal sub-blocks of U11 (upper) and of
+    // L11 (unit lower), for the block triangular solves.  Warp w inverts
+    // sub-block w/2 (0-3: U, 4-7: L), rows (w & 1) + 2t, two rows at a time;
+    // one row of the inverse per solve (x^T U = e_i^T resp. x^T L = e_i^T),
+    // lane = column; the diagonal reciprocals are formed once per lane.
+    {
+        const int blk = warp >> 1, upper = blk < 4, kb = blk & 3;
+        const int o = kb * P;
+        float *dst = inv32 + (int64_t)slot * ZS_INV32_STRIDE + (kb * 2 + (upper ? 0 : 1)) * 2 * P * P;
+        const cf dl = upper ? zs::crecip(cf{sre[(o + lane) * LDS + o + lane], sim[(o + lane) * LDS + o + lane]})
+                            : cf{1.f, 0.f};
+        for (int i0 = (warp & 1); i0 < P; i0 += 4) {
+            const int i1 = i0 + 2;  // second row of the pair
+            cf x0 = cf{lane == i0 ? 1.f : 0.f, 0.f}, x1 = cf{lane == i1 ? 1.f : 0.f, 0.f};
+            if (upper) {
+                for (int k = i0; k < P; k++) {
+                    if (lane == k) {
+                        x0 = zs::cmul(x0, dl);
+                        if (k >= i1) x1 = zs::cmul(x1, dl);
+                    }
+                    cf a, b;
+                    a.re = __shfl_sync(0xffffffffu, x0.re, k);
+                    a.im = __shfl_sync(0xffffffffu, x0.im, k);
+                    b.re = __shfl_sync(0xffffffffu, x1.re, k);
+                    b.im = __shfl_sync(0xffffffffu, x1.im, k);
+                    if (lane > k) {
+                        const cf u = cf{sre[(o + k) * LDS + o + lane], sim[(o + k) * LDS + o + lane]};
+                        x0 = zs::cfms(x0, a, u);
+                        if (k >= i1) x1 = zs::cfms(x1, b, u);
+                    }
+                }
+            } else {
+                for (int k = i1; k > 0; k--) {
+                    cf a, b;
+                    a.re = __shfl_sync(0xffffffffu, x0.re, k);
+                    a.im = __shfl_sync(0xffffffffu, x0.im, k);
+                    b.re = __shfl_sync(0xffffffffu, x1.re, k);
+                    b.im = __shfl_sync(0xffffffffu, x1.im, k);
+                    if (lane < k) {
+                        const cf l = cf{sre[(o + k) * LDS + o + lane], sim[(o + k) * LDS + o + lane]};
+                        x1 = zs::cfms(x1, b, l);
+                        if (k <= i0) x0 = zs::cfms(x0, a, l);
+                    }
+                }
+            }
+            dst[i0 * P + lane] = x0.re;
+            dst[P * P + i0 * P + lane] = x0.im;
+            dst[i1 * P + lane] = x1.re;
+            dst[P * P + i1 * P + lane] = x1.im;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- L21 = A21 U11^-1
 
+// Both block solves run in four 32-column steps with the inverted 32x32
+// diagonal sub-blocks from k_diag_lu: for step kb, x_kb = r_kb . inv(U_kb,kb)
+// (resp. inv(L_kb,kb) . r_kb), then the later sub-blocks are updated with the
+// off-diagonal blocks of U11 (resp. L11).  Every product is a register-tiled
+// multiply-add with operands broadcast from shared memory; no step is a
+// sequential substitution.
+
 constexpr int kTrsmThreads = 512;  // 16 warps
-constexpr int kTrsmLRows = 64;     // rows per CTA
+constexpr int kTLRows = 128;       // L21 rows per CTA (8 per warp)
 
 __global__ void __launch_bounds__(kTrsmThreads, 1)
 k_trsm_l(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-         float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
+         const float *__restrict__ inv32, float *__restrict__ pack, int64_t pack_stride, int mode,
+         const int *__restrict__ slots) {
     extern __shared__ float sm[];
-    float *ure = sm;                // [NB][NB] upper factor, row k contiguous
+    float *ure = sm;                 // [NB][NB]: U11 above the diagonal blocks, inv(U_kb,kb) on them
     float *uim = sm + NB * NB;
-    float *rinv = sm + 2 * NB * NB;  // [2][NB] reciprocals of the diagonal
+    cf *xs = reinterpret_cast<cf *>(sm + 2 * NB * NB);  // [16 warps][8 rows][32] broadcast buffer
     const int slot = slots[blockIdx.y];
     float *re = z32 + (int64_t)slot * z32_stride;
     float *im = re + plane;
+    const float *inv = inv32 + (int64_t)slot * ZS_INV32_STRIDE;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int idx = tid; idx < NB * NB; idx += kTrsmThreads) {
-        int i = idx / NB, j = idx - i * NB;
-        int64_t g = (J + i) * ld + J + j;
-        ure[idx] = (j >= i) ? re[g] : 0.f;
-        uim[idx] = (j >= i) ? im[g] : 0.f;
+        const int i = idx >> 7, j = idx & (NB - 1);
+        float a = 0.f, b = 0.f;
+        if ((i >> 5) == (j >> 5)) {
+            const float *u = inv + ((i >> 5) * 2 + 0) * 2 * P * P;
+            a = u[(i & 31) * P + (j & 31)];
+            b = u[P * P + (i & 31) * P + (j & 31)];
+        } else if (j > i) {
+            const int64_t g = (J + i) * ld + J + j;
+            a = re[g];
+            b = im[g];
+        }
+        ure[idx] = a;
+        uim[idx] = b;
     }
     __syncthreads();
-    if (tid < NB) {
-        cf r = zs::crecip(cf{ure[tid * NB + tid], uim[tid * NB + tid]});
-        rinv[tid] = r.re;
-        rinv[NB + tid] = r.im;
+    cf *xw = xs + warp * 8 * 32;
+    const int64_t r0 = J + NB + (int64_t)blockIdx.x * kTLRows + warp * 8;
+    cf v[8][4];
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const int64_t r = r0 + t;
+#pragma unroll
+        for (int h = 0; h < 4; h++) {
+            const int64_t g = r * ld + J + 32 * h + lane;
+            v[t][h] = (r < n) ? cf{re[g], im[g]} : cf{0.f, 0.f};
+        }
     }
-    __syncthreads();
-    float *pA_hi = pack + (int64_t)slot * pack_stride;
-    float *pA_lo = pA_hi + zs_pack_plane(n);
-    const int64_t row0 = J + NB + (int64_t)blockIdx.x * kTrsmLRows;
-    for (int rr = warp; rr < kTrsmLRows; rr += 16) {
-        const int64_t r = row0 + rr;
-        if (r >= n) break;
-        cf v[4];
 #pragma unroll
-        for (int q = 0; q < 4; q++) v[q] = cf{re[r * ld + J + lane + 32 * q], im[r * ld + J + lane + 32 * q]};
+    for (int kb = 0; kb < 4; kb++) {
+        // x_kb = r_kb . inv(U_kb,kb): lane = output column
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            for (int kl = 0; kl < 32; kl++) {
-                const int k = 32 * q + kl;
-                cf x;
-                x.re = __shfl_sync(0xffffffffu, v[q].re, kl);
-                x.im = __shfl_sync(0xffffffffu, v[q].im, kl);
-                x = zs::cmul(x, cf{rinv[k], rinv[NB + k]});
-                if (lane == kl) v[q] = x;
+        for (int t = 0; t < 8; t++) xw[t * 32 + lane] = v[t][kb];
+        __syncwarp();
+        cf acc[8];
 #pragma unroll
-                for (int q2 = q; q2 < 4; q2++) {
-                    const int j = lane + 32 * q2;
-                    if (j > k) v[q2] = zs::cfms(v[q2], x, cf{ure[k * NB + j], uim[k * NB + j]});
+        for (int t = 0; t < 8; t++) acc[t] = cf{0.f, 0.f};
+#pragma unroll 4
+        for (int k = 0; k < 32; k++) {
+            const cf w = cf{ure[(kb * 32 + k) * NB + kb * 32 + lane], uim[(kb * 32 + k) * NB + kb * 32 + lane]};
+#pragma unroll
+            for (int t = 0; t < 8; t++) {
+                const cf rk = xw[t * 32 + k];
+                acc[t].re = fmaf(rk.re, w.re, fmaf(-rk.im, w.im, acc[t].re));
+                acc[t].im = fmaf(rk.re, w.im, fmaf(rk.im, w.re, acc[t].im));
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < 8; t++) {
+            v[t][kb] = acc[t];
+            xw[t * 32 + lane] = acc[t];
+        }
+        __syncwarp();
+        // later sub-blocks: r_h -= x_kb . U(kb, h)
+        if (kb < 3) {
+#pragma unroll 4
+            for (int k = 0; k < 32; k++) {
+                cf xk[8];
+#pragma unroll
+                for (int t = 0; t < 8; t++) xk[t] = xw[t * 32 + k];
+#pragma unroll
+                for (int h = kb + 1; h < 4; h++) {
+                    const cf u = cf{ure[(kb * 32 + k) * NB + h * 32 + lane], uim[(kb * 32 + k) * NB + h * 32 + lane]};
+#pragma unroll
+                    for (int t = 0; t < 8; t++) v[t][h] = zs::cfms(v[t][h], xk[t], u);
                 }
             }
         }
+        __syncwarp();
+    }
+    float *pA_hi = pack + (int64_t)slot * pack_stride;
+    float *pA_lo = pA_hi + zs_pack_plane(n);
+#pragma unroll
+    for (int t = 0; t < 8; t++) {
+        const int64_t r = r0 + t;
+        if (r >= n) break;
         float *ah = pA_hi + r * ZS_PACK_K, *al = pA_lo + r * ZS_PACK_K;
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int c = lane + 32 * q;
-            re[r * ld + J + c] = v[q].re;
-            im[r * ld + J + c] = v[q].im;
-            pack_put(ah, al, c, v[q].re, mode);
-            pack_put(ah, al, NB + c, v[q].im, mode);
+        for (int h = 0; h < 4; h++) {
+            const int c = 32 * h + lane;
+            re[r * ld + J + c] = v[t][h].re;
+            im[r * ld + J + c] = v[t][h].im;
+            pack_put(ah, al, c, v[t][h].re, mode);
+            pack_put(ah, al, NB + c, v[t][h].im, mode);
         }
     }
 }
 
 // ---------------------------------------------------------------- U12 = L11^-1 A12
 
-constexpr int kTrsmUCols = 32;  // columns per CTA
+constexpr int kTUCols = 64;  // U12 columns per CTA (4 per warp)
+constexpr int kTUPad = kTUCols + 1;
 
 __global__ void __launch_bounds__(kTrsmThreads, 1)
 k_trsm_u(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-         float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
+         const float *__restrict__ inv32, float *__restrict__ pack, int64_t pack_stride, int mode,
+         const int *__restrict__ slots) {
     extern __shared__ float sm[];
-    float *lre = sm;                 // [NB][LDS] strictly lower factor, column access
+    float *lre = sm;                 // [NB][LDS]: L11 below the diagonal blocks, inv(L_kb,kb) on them
     float *lim = sm + NB * LDS;
-    float *tre = sm + 2 * NB * LDS;  // [NB][33] tile of A12
-    float *tim = tre + NB * 33;
+    float *tre = sm + 2 * NB * LDS;  // [NB][kTUPad] tile of A12 / U12
+    float *tim = tre + NB * kTUPad;
+    cf *xs = reinterpret_cast<cf *>(tim + NB * kTUPad);  // [16 warps][4 cols][32]
     const int slot = slots[blockIdx.y];
     float *re = z32 + (int64_t)slot * z32_stride;
     float *im = re + plane;
+    const float *inv = inv32 + (int64_t)slot * ZS_INV32_STRIDE;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t c0 = J + NB + (int64_t)blockIdx.x * kTrsmUCols;
-    const int ncol = (int)zs::min64(kTrsmUCols, n - c0);
+    const int64_t c0 = J + NB + (int64_t)blockIdx.x * kTUCols;
+    const int ncol = (int)zs::min64(kTUCols, n - c0);
     for (int idx = tid; idx < NB * NB; idx += kTrsmThreads) {
-        int i = idx / NB, j = idx - i * NB;
-        int64_t g = (J + i) * ld + J + j;
-        lre[i * LDS + j] = (i > j) ? re[g] : 0.f;
-        lim[i * LDS + j] = (i > j) ? im[g] : 0.f;
-    }
-    for (int idx = tid; idx < NB * kTrsmUCols; idx += kTrsmThreads) {
-        int i = idx >> 5, c = idx & 31;
-        if (c < ncol) {
-            int64_t g = (J + i) * ld + c0 + c;
-            tre[i * 33 + c] = re[g];
-            tim[i * 33 + c] = im[g];
+        const int i = idx >> 7, j = idx & (NB - 1);
+        float a = 0.f, b = 0.f;
+        if ((i >> 5) == (j >> 5)) {
+            const float *l = inv + ((i >> 5) * 2 + 1) * 2 * P * P;
+            a = l[(i & 31) * P + (j & 31)];
+            b = l[P * P + (i & 31) * P + (j & 31)];
+        } else if (i > j) {
+            const int64_t g = (J + i) * ld + J + j;
+            a = re[g];
+            b = im[g];
         }
+        lre[i * LDS + j] = a;
+        lim[i * LDS + j] = b;
+    }
+    for (int idx = tid; idx < NB * kTUCols; idx += kTrsmThreads) {
+        const int i = idx >> 6, c = idx & (kTUCols - 1);
+        float a = 0.f, b = 0.f;
+        if (c < ncol) {
+            const int64_t g = (J + i) * ld + c0 + c;
+            a = re[g];
+            b = im[g];
+        }
+        tre[i * kTUPad + c] = a;
+        tim[i * kTUPad + c] = b;
     }
     __syncthreads();
+    cf *xw = xs + warp * 4 * 32;
+    // warp w: columns 4w..4w+3; lane holds rows 32h + lane
+    cf v[4][4];
+#pragma unroll
+    for (int c = 0; c < 4; c++)
+#pragma unroll
+        for (int h = 0; h < 4; h++)
+            v[c][h] = cf{tre[(32 * h + lane) * kTUPad + warp * 4 + c], tim[(32 * h + lane) * kTUPad + warp * 4 + c]};
+#pragma unroll
+    for (int kb = 0; kb < 4; kb++) {
+        // u_kb = inv(L_kb,kb) . a_kb: lane = output row
+#pragma unroll
+        for (int c = 0; c < 4; c++) xw[c * 32 + lane] = v[c][kb];
+        __syncwarp();
+        cf acc[4];
+#pragma unroll
+        for (int c = 0; c < 4; c++) acc[c] = cf{0.f, 0.f};
+#pragma unroll 4
+        for (int k = 0; k < 32; k++) {
+            const cf w = cf{lre[(kb * 32 + lane) * LDS + kb * 32 + k], lim[(kb * 32 + lane) * LDS + kb * 32 + k]};
+#pragma unroll
+            for (int c = 0; c < 4; c++) {
+                const cf ak = xw[c * 32 + k];
+                acc[c].re = fmaf(w.re, ak.re, fmaf(-w.im, ak.im, acc[c].re));
+                acc[c].im = fmaf(w.re, ak.im, fmaf(w.im, ak.re, acc[c].im));
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 4; c++) {
+            v[c][kb] = acc[c];
+            xw[c * 32 + lane] = acc[c];
+        }
+        __syncwarp();
+        if (kb < 3) {
+#pragma unroll 4
+            for (int k = 0; k < 32; k++) {
+                cf uk[4];
+#pragma unroll
+                for (int c = 0; c < 4; c++) uk[c] = xw[c * 32 + k];
+#pragma unroll
+                for (int h = kb + 1; h < 4; h++) {
+                    const cf l = cf{lre[(h * 32 + lane) * LDS + kb * 32 + k], lim[(h * 32 + lane) * LDS + kb * 32 + k]};
+#pragma unroll
+                    for (int c = 0; c < 4; c++) v[c][h] = zs::cfms(v[c][h], l, uk[c]);
+                }
+            }
+        }
+        __syncwarp();
+    }
     float *pBr_hi = pack + (int64_t)slot * pack_stride + 2 * zs_pack_plane(n);
     float *pBr_lo = pBr_hi + zs_pack_plane(n);
     float *pBi_hi = pBr_hi + 2 * zs_pack_plane(n);
     float *pBi_lo = pBr_hi + 3 * zs_pack_plane(n);
-    for (int c = warp; c < ncol; c += 16) {
-        cf v[4];
 #pragma unroll
-        for (int q = 0; q < 4; q++) v[q] = cf{tre[(lane + 32 * q) * 33 + c], tim[(lane + 32 * q) * 33 + c]};
+    for (int c = 0; c < 4; c++) {
+        const int cc = warp * 4 + c;
+        if (cc < ncol) {
+            const int64_t j = c0 + cc;
+            float *brh = pBr_hi + j * ZS_PACK_K, *brl = pBr_lo + j * ZS_PACK_K;
+            float *bih = pBi_hi + j * ZS_PACK_K, *bil = pBi_lo + j * ZS_PACK_K;
 #pragma unroll
-        for (int q = 0; q < 4; q++) {
-            for (int kl = 0; kl < 32; kl++) {
-                const int k = 32 * q + kl;
-                cf u;
-                u.re = __shfl_sync(0xffffffffu, v[q].re, kl);
-                u.im = __shfl_sync(0xffffffffu, v[q].im, kl);
-#pragma unroll
-                for (int q2 = q; q2 < 4; q2++) {
-                    const int i = lane + 32 * q2;
-                    if (i > k) v[q2] = zs::cfms(v[q2], cf{lre[i * LDS + k], lim[i * LDS + k]}, u);
-                }
+            for (int h = 0; h < 4; h++) {
+                const int i = 32 * h + lane;
+                tre[i * kTUPad + cc] = v[c][h].re;
+                tim[i * kTUPad + cc] = v[c][h].im;
+                pack_put(brh, brl, i, v[c][h].re, mode);
+                pack_put(brh, brl, NB + i, -v[c][h].im, mode);
+                pack_put(bih, bil, i, v[c][h].im, mode);
+                pack_put(bih, bil, NB + i, v[c][h].re, mode);
             }
-        }
-        const int64_t j = c0 + c;
-        float *brh = pBr_hi + j * ZS_PACK_K, *brl = pBr_lo + j * ZS_PACK_K;
-        float *bih = pBi_hi + j * ZS_PACK_K, *bil = pBi_lo + j * ZS_PACK_K;
-#pragma unroll
-        for (int q = 0; q < 4; q++) {
-            const int i = lane + 32 * q;
-            tre[i * 33 + c] = v[q].re;
-            tim[i * 33 + c] = v[q].im;
-            pack_put(brh, brl, i, v[q].re, mode);
-            pack_put(brh, brl, NB + i, -v[q].im, mode);
-            pack_put(bih, bil, i, v[q].im, mode);
-            pack_put(bih, bil, NB + i, v[q].re, mode);
         }
     }
     __syncthreads();
-    for (int idx = tid; idx < NB * kTrsmUCols; idx += kTrsmThreads) {
-        int i = idx >> 5, c = idx & 31;
+    for (int idx = tid; idx < NB * kTUCols; idx += kTrsmThreads) {
+        const int i = idx >> 6, c = idx & (kTUCols - 1);
         if (c < ncol) {
-            int64_t g = (J + i) * ld + c0 + c;
-            re[g] = tre[i * 33 + c];
-            im[g] = tim[i * 33 + c];
+            const int64_t g = (J + i) * ld + c0 + c;
+            re[g] = tre[i * kTUPad + c];
+            im[g] = tim[i * kTUPad + c];
         }
     }
 }
@@ -436,7 +589,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 }  // namespace
 
 cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                              int64_t J, int nb, const int *slots, int nslot, int *pivflag,
+                              int64_t J, int nb, const int *slots, int nslot, int *pivflag, float *inv32,
                               cudaStream_t st) {
     (void)n;
     const size_t smem = (2 * NB * LDS + 4 * P) * sizeof(float);
@@ -446,14 +599,14 @@ cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32
         if (e != cudaSuccess) return e;
         init = true;
     }
-    k_diag_lu<<<nslot, kDiagThreads, smem, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag);
+    k_diag_lu<<<nslot, kDiagThreads, smem, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag, inv32);
     return cudaGetLastError();
 }
 
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
-                             int nslot, cudaStream_t st) {
-    const size_t smem = (2 * NB * NB + 2 * NB) * sizeof(float);
+                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
+                             const int *slots, int nslot, cudaStream_t st) {
+    const size_t smem = (2 * NB * NB) * sizeof(float) + 16 * 8 * 32 * sizeof(cf);
     static bool init = false;
     if (!init) {
         cudaError_t e = set_smem(k_trsm_l, smem);
@@ -461,16 +614,16 @@ cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_
         init = true;
     }
     const int64_t m2 = n - J - NB;
-    dim3 grid((unsigned)((m2 + kTrsmLRows - 1) / kTrsmLRows), nslot);
-    k_trsm_l<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode,
+    dim3 grid((unsigned)((m2 + kTLRows - 1) / kTLRows), nslot);
+    k_trsm_l<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, pack, pack_stride, mode,
                                                 slots);
     return cudaGetLastError();
 }
 
 cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots,
-                             int nslot, cudaStream_t st) {
-    const size_t smem = (2 * NB * LDS + 2 * NB * 33) * sizeof(float);
+                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
+                             const int *slots, int nslot, cudaStream_t st) {
+    const size_t smem = (2 * NB * LDS + 2 * NB * kTUPad) * sizeof(float) + 16 * 4 * 32 * sizeof(cf);
     static bool init = false;
     if (!init) {
         cudaError_t e = set_smem(k_trsm_u, smem);
@@ -478,8 +631,8 @@ cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_
         init = true;
     }
     const int64_t m2 = n - J - NB;
-    dim3 grid((unsigned)((m2 + kTrsmUCols - 1) / kTrsmUCols), nslot);
-    k_trsm_u<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode,
+    dim3 grid((unsigned)((m2 + kTUCols - 1) / kTUCols), nslot);
+    k_trsm_u<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, pack, pack_stride, mode,
                                                 slots);
     return cudaGetLastError();
 }

@@ -87,7 +87,7 @@ extern "C" int zsolve_lowprec_solve_noalloc(const float *z32, int64_t ld, int64_
         const int left = nrhs - r0;
         const int R = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
         epoch++;
-        if (zs_launch_trsv(z32, ld, plane, sys_stride, n, vv + (int64_t)r0 * n, v_stride, R, sp->slots, nsys,
+        if (zs_launch_trsv_seq(z32, ld, plane, sys_stride, n, vv + (int64_t)r0 * n, v_stride, R, sp->slots, nsys,
                            sp->prog, epoch, &sp->ticket, &sp->status, sms, s) != cudaSuccess)
             return ZSOLVE_ECUDA;
         r0 += R;

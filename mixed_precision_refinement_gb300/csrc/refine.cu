@@ -4,11 +4,15 @@
 // x += d; the stopping test on the size of the correction).
 //
 // k_residual: one warp per row of the float64 matrix, lanes stride the row
-// with 16-byte loads (coalesced), four DFMA per complex entry per right-hand
-// side, warp-shuffle reduction; the result is written rounded to complex
-// float32 (the input of the next low-precision solve) or, for the stage-level
-// call, in float64.  Bound: HBM or the FP64 pipe, whichever is lower -- the
-// kernel moves 16 n^2 bytes per frequency and issues 4 n^2 DFMA per RHS.
+// with 16-byte loads (coalesced), warp-shuffle reduction; the result is
+// written rounded to complex float32 (the input of the next low-precision
+// solve) or, for the stage-level call, in float64.  A complex entry costs
+// four DFMA per right-hand side; a warp step of 128 entries whose real parts
+// are all exact zeros (Re Z_ij = Zs.re G_ij vanishes wherever G_ij = 0) takes
+// a branch with two.  The skipped products are exact zeros added to the
+// running sums, so the float64 result is the one the four-DFMA sequence in
+// the same order gives (finite x).  Bound: HBM or the FP64
+// pipe, whichever is lower -- the kernel moves 16 n^2 bytes per frequency.
 //
 // k_update / k_relcorr: x (float64) += d (float32), and per (frequency, RHS)
 // ||d||_2 / ||x||_2 from per-block partial sums reduced in a fixed order, so
@@ -31,42 +35,71 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
     if (row >= n) return;
     const double2 *zr = z64 + (int64_t)slot * z64_stride + row * n;
     const double2 *xs = x + (int64_t)slot * x_stride;
-    double ar[R], ai[R];
+    // NA independent accumulator pairs per right-hand side (sub-step u uses
+    // u % NA): the FP64 unit's latency is long, so each warp needs about eight
+    // independent chains; with several right-hand sides they come from R
+    constexpr int NA = R >= 4 ? 1 : 4 / R;
+    double ar[NA][R], ai[NA][R];
 #pragma unroll
-    for (int r = 0; r < R; r++) ar[r] = ai[r] = 0.0;
-    int64_t j = lane;
-    for (; j + 96 < n; j += 128) {
+    for (int u = 0; u < NA; u++)
+#pragma unroll
+        for (int r = 0; r < R; r++) ar[u][r] = ai[u][r] = 0.0;
+    // full 128-entry steps first: the bound is the same for every lane, so the
+    // warp vote below always sees the whole warp
+    int64_t base = 0;
+    for (; base + 128 <= n; base += 128) {
+        const int64_t j = base + lane;
         double2 z[4];
 #pragma unroll
         for (int u = 0; u < 4; u++) z[u] = __ldcs(zr + j + 32 * u);
+        // warp-uniform test: every real part in these 128 entries an exact zero
+        bool re0 = true;
 #pragma unroll
-        for (int u = 0; u < 4; u++)
+        for (int u = 0; u < 4; u++) re0 = re0 && ((__double_as_longlong(z[u].x) << 1) == 0);
+        if (__all_sync(0xffffffffu, re0)) {
 #pragma unroll
-            for (int r = 0; r < R; r++) {
-                const double2 xv = __ldg(xs + r * n + j + 32 * u);
-                ar[r] = fma(z[u].x, xv.x, ar[r]);
-                ar[r] = fma(-z[u].y, xv.y, ar[r]);
-                ai[r] = fma(z[u].x, xv.y, ai[r]);
-                ai[r] = fma(z[u].y, xv.x, ai[r]);
-            }
+            for (int u = 0; u < 4; u++)
+#pragma unroll
+                for (int r = 0; r < R; r++) {
+                    const double2 xv = __ldg(xs + r * n + j + 32 * u);
+                    ar[u % NA][r] = fma(-z[u].y, xv.y, ar[u % NA][r]);
+                    ai[u % NA][r] = fma(z[u].y, xv.x, ai[u % NA][r]);
+                }
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; u++)
+#pragma unroll
+                for (int r = 0; r < R; r++) {
+                    const double2 xv = __ldg(xs + r * n + j + 32 * u);
+                    ar[u % NA][r] = fma(z[u].x, xv.x, ar[u % NA][r]);
+                    ai[u % NA][r] = fma(z[u].x, xv.y, ai[u % NA][r]);
+                    ar[u % NA][r] = fma(-z[u].y, xv.y, ar[u % NA][r]);
+                    ai[u % NA][r] = fma(z[u].y, xv.x, ai[u % NA][r]);
+                }
+        }
     }
-    for (; j < n; j += 32) {
+    for (int64_t j = base + lane; j < n; j += 32) {
         const double2 z = __ldcs(zr + j);
 #pragma unroll
         for (int r = 0; r < R; r++) {
             const double2 xv = __ldg(xs + r * n + j);
-            ar[r] = fma(z.x, xv.x, ar[r]);
-            ar[r] = fma(-z.y, xv.y, ar[r]);
-            ai[r] = fma(z.x, xv.y, ai[r]);
-            ai[r] = fma(z.y, xv.x, ai[r]);
+            ar[0][r] = fma(z.x, xv.x, ar[0][r]);
+            ai[0][r] = fma(z.x, xv.y, ai[0][r]);
+            ar[0][r] = fma(-z.y, xv.y, ar[0][r]);
+            ai[0][r] = fma(z.y, xv.x, ai[0][r]);
         }
     }
 #pragma unroll
     for (int r = 0; r < R; r++) {
 #pragma unroll
+        for (int u = 1; u < NA; u++) {
+            ar[0][r] += ar[u][r];
+            ai[0][r] += ai[u][r];
+        }
+#pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            ar[r] += __shfl_xor_sync(0xffffffffu, ar[r], o);
-            ai[r] += __shfl_xor_sync(0xffffffffu, ai[r], o);
+            ar[0][r] += __shfl_xor_sync(0xffffffffu, ar[0][r], o);
+            ai[0][r] += __shfl_xor_sync(0xffffffffu, ai[0][r], o);
         }
     }
     if (lane < R) {
@@ -74,8 +107,8 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
 #pragma unroll
         for (int r = 0; r < R; r++)
             if (r == lane) {
-                vr = ar[r];
-                vi = ai[r];
+                vr = ar[0][r];
+                vi = ai[0][r];
             }
         const double2 bv = b[(int64_t)lane * n + row];
         const double rr = bv.x - vr, ri = bv.y - vi;

@@ -47,7 +47,7 @@ constexpr int kThreads = 192;
 constexpr int A_BYTES = TM * KC * 4;       // 16 KB
 constexpr int B_BYTES = 2 * TN * KC * 4;   // 32 KB (Br rows then Bi rows)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t kWaitLimit = 1u << 26;
+constexpr uint32_t kWaitLimit = 1u << 24;
 
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
 

@@ -45,7 +45,7 @@ __device__ __forceinline__ long long warp_progress(const unsigned long long *p, 
 
 template <int R>
 __global__ void __launch_bounds__(kThreads)
-k_trsv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+k_trsv_seq(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
        float2 *__restrict__ v, int64_t v_stride, const int *__restrict__ slots, int nslot,
        unsigned long long *__restrict__ prog, unsigned epoch, unsigned *ticket, unsigned *status) {
     __shared__ float dre[TB * kLdd], dim_[TB * kLdd];  // diagonal block
@@ -223,11 +223,11 @@ k_trsv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
 }
 
 template <int R>
-cudaError_t launch_r(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, float2 *v,
+cudaError_t launch_seq(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, float2 *v,
                      int64_t v_stride, const int *slots, int nslot, unsigned long long *prog,
                      unsigned epoch, unsigned *ticket, unsigned *status, int num_sms, cudaStream_t st) {
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_trsv<R>, kThreads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_trsv_seq<R>, kThreads, 0);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t nblk = (n + TB - 1) / TB;
@@ -239,29 +239,29 @@ cudaError_t launch_r(const float *z32, int64_t ld, int64_t plane, int64_t z32_st
     void *args[] = {(void *)&z32, (void *)&ld, (void *)&plane, (void *)&z32_stride, (void *)&n,
                     (void *)&v, (void *)&v_stride, (void *)&slots, (void *)&nslot, (void *)&prog,
                     (void *)&epoch, (void *)&ticket, (void *)&status};
-    e = cudaLaunchCooperativeKernel((const void *)k_trsv<R>, dim3((unsigned)grid), dim3(kThreads), args, 0, st);
+    e = cudaLaunchCooperativeKernel((const void *)k_trsv_seq<R>, dim3((unsigned)grid), dim3(kThreads), args, 0, st);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t zs_launch_trsv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                            float2 *v, int64_t v_stride, int nrhs, const int *slots, int nslot,
                            unsigned long long *prog, unsigned epoch, unsigned *ticket,
                            unsigned *status, int num_sms, cudaStream_t st) {
     switch (nrhs) {
         case 1:
-            return launch_r<1>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
+            return launch_seq<1>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         case 2:
-            return launch_r<2>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
+            return launch_seq<2>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         case 4:
-            return launch_r<4>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
+            return launch_seq<4>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         case 8:
-            return launch_r<8>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
+            return launch_seq<8>(z32, ld, plane, z32_stride, n, v, v_stride, slots, nslot, prog,
                                epoch, ticket, status, num_sms, st);
         default:
             return cudaErrorInvalidValue;

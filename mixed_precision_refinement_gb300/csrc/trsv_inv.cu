@@ -1,0 +1,387 @@
+// Forward and back substitution with the complex float32 factors, using
+// explicit inverses of the 128 x 128 diagonal blocks (malusrfworks.com,
+// "Solving Dense Matrices Fast in the Browser", section "Double-precision
+// answers from a GPU without double precision", steps 2 and 4: solve with the
+// single-precision factorisation).
+//
+// k_diag_inv (once per factorisation): for every 128 x 128 diagonal block of
+// every frequency, X = L_bb^-1 (unit lower) and X = U_bb^-1 (upper), one row
+// of X per warp step (x^T L = e_i^T, resp. x^T U = e_i^T, solved along the
+// row so that both the factor reads and the result writes are contiguous).
+// Padding rows beyond n get the identity.
+//
+// k_trsv_inv (per solve): the same ticketed, in-order task scheme as the
+// sequential kernel, with 128-row blocks (half the dependency chain) and the
+// block's own triangle applied as a dense 128 x 128 product with the inverse
+// (all warps, no sequential steps) instead of a one-warp substitution.  Every
+// task waits only on tasks with smaller tickets, claimed by running CTAs; each
+// wait is bounded and raises the status bit instead of hanging.
+//
+// Bound: HBM for the off-diagonal blocks (8 n^2 bytes per frequency per
+// solve) plus the dependency chain's latency (n / 128 steps per direction).
+#include "common.cuh"
+
+namespace {
+
+using zs::cf;
+
+constexpr int TB = ZS_TB2;  // 128
+constexpr int kInvThreads = 512;
+constexpr int kLdi = TB + 1;
+
+__global__ void __launch_bounds__(kInvThreads, 1)
+k_diag_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+           float *__restrict__ dinv, int64_t dinv_stride, const int *__restrict__ slots) {
+    extern __shared__ float sm[];
+    float *are = sm, *aim = sm + TB * kLdi;
+    const int b = blockIdx.x, upper = blockIdx.y, slot = slots[blockIdx.z];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const float *re = z32 + (int64_t)slot * z32_stride;
+    const float *im = re + plane;
+    const int64_t r0 = (int64_t)b * TB;
+    const int rows = (int)zs::min64(TB, n - r0);
+    for (int idx = tid; idx < TB * TB; idx += kInvThreads) {
+        const int i = idx >> 7, j = idx & (TB - 1);
+        float a = 0.f, c = 0.f;
+        if (i < rows && j < rows) {
+            a = re[(r0 + i) * ld + r0 + j];
+            c = im[(r0 + i) * ld + r0 + j];
+        } else if (i == j) {
+            a = 1.f;  // identity padding
+        }
+        are[i * kLdi + j] = a;
+        aim[i * kLdi + j] = c;
+    }
+    __syncthreads();
+    float *xr = dinv + (int64_t)slot * dinv_stride + (int64_t)b * 4 * TB * TB + (int64_t)upper * 2 * TB * TB;
+    float *xi = xr + TB * TB;
+    // rows i0 = warp + 32 t and i1 = i0 + 16, two at a time; lane holds
+    // columns j = lane + 32 h; diagonal reciprocals formed once per lane
+    cf dl[4];
+#pragma unroll
+    for (int h = 0; h < 4; h++) {
+        const int j = lane + 32 * h;
+        dl[h] = upper ? zs::crecip(cf{are[j * kLdi + j], aim[j * kLdi + j]}) : cf{1.f, 0.f};
+    }
+    for (int i0 = warp; i0 < TB; i0 += 32) {
+        const int i1 = i0 + 16;
+        cf x[4], y[4];
+#pragma unroll
+        for (int h = 0; h < 4; h++) {
+            x[h] = cf{(lane + 32 * h == i0) ? 1.f : 0.f, 0.f};
+            y[h] = cf{(lane + 32 * h == i1) ? 1.f : 0.f, 0.f};
+        }
+        if (!upper) {
+            // x^T L = e_i^T, L unit lower: for k = i..1, x_k final; x_j -= x_k L[k][j], j < k
+#pragma unroll
+            for (int h = 3; h >= 0; h--) {
+                for (int kl = 31; kl >= 0; kl--) {
+                    const int k = 32 * h + kl;
+                    if (k > i1 || k == 0) continue;
+                    cf xk, yk;
+                    xk.re = __shfl_sync(0xffffffffu, x[h].re, kl);
+                    xk.im = __shfl_sync(0xffffffffu, x[h].im, kl);
+                    yk.re = __shfl_sync(0xffffffffu, y[h].re, kl);
+                    yk.im = __shfl_sync(0xffffffffu, y[h].im, kl);
+#pragma unroll
+                    for (int h2 = 0; h2 <= h; h2++) {
+                        const int j = lane + 32 * h2;
+                        if (j < k) {
+                            const cf lv = cf{are[k * kLdi + j], aim[k * kLdi + j]};
+                            y[h2] = zs::cfms(y[h2], yk, lv);
+                            if (k <= i0) x[h2] = zs::cfms(x[h2], xk, lv);
+                        }
+                    }
+                }
+            }
+        } else {
+            // x^T U = e_i^T, U upper: for k = i..127, x_k /= U[k][k] (final); x_j -= x_k U[k][j], j > k
+#pragma unroll
+            for (int h = 0; h < 4; h++) {
+                for (int kl = 0; kl < 32; kl++) {
+                    const int k = 32 * h + kl;
+                    if (k < i0) continue;
+                    if (lane == kl) {
+                        x[h] = zs::cmul(x[h], dl[h]);
+                        if (k >= i1) y[h] = zs::cmul(y[h], dl[h]);
+                    }
+                    cf xk, yk;
+                    xk.re = __shfl_sync(0xffffffffu, x[h].re, kl);
+                    xk.im = __shfl_sync(0xffffffffu, x[h].im, kl);
+                    yk.re = __shfl_sync(0xffffffffu, y[h].re, kl);
+                    yk.im = __shfl_sync(0xffffffffu, y[h].im, kl);
+#pragma unroll
+                    for (int h2 = h; h2 < 4; h2++) {
+                        const int j = lane + 32 * h2;
+                        if (j > k) {
+                            const cf uv = cf{are[k * kLdi + j], aim[k * kLdi + j]};
+                            x[h2] = zs::cfms(x[h2], xk, uv);
+                            if (k >= i1) y[h2] = zs::cfms(y[h2], yk, uv);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int h = 0; h < 4; h++) {
+            xr[i0 * TB + lane + 32 * h] = x[h].re;
+            xi[i0 * TB + lane + 32 * h] = x[h].im;
+            xr[i1 * TB + lane + 32 * h] = y[h].re;
+            xi[i1 * TB + lane + 32 * h] = y[h].im;
+        }
+    }
+}
+
+// lane 0 waits until more than `need` blocks are complete; the warp barrier
+// orders the other lanes' loads after its acquire
+__device__ __forceinline__ long long warp_progress(const unsigned long long *p, unsigned epoch, long long need,
+                                                   unsigned *status, int lane) {
+    long long c = 0;
+    if (lane == 0) c = zs::progress_wait(p, epoch, need, status);
+    c = __shfl_sync(0xffffffffu, c, 0);
+    __syncwarp();
+    return c;
+}
+
+constexpr int kThreads = 512;  // 16 warps, 8 rows each
+
+template <int R>
+__global__ void __launch_bounds__(kThreads, 1)
+k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+           const float *__restrict__ dinv, int64_t dinv_stride, float2 *__restrict__ v, int64_t v_stride,
+           const int *__restrict__ slots, int nslot, unsigned long long *__restrict__ prog, unsigned epoch,
+           unsigned *ticket, unsigned *status) {
+    __shared__ cf part[TB][R];
+    __shared__ cf rv[TB][R];
+    __shared__ unsigned s_task, s_stop;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nblk = (int)((n + TB - 1) / TB);
+    const unsigned total = 2u * (unsigned)nblk * (unsigned)nslot;
+    while (true) {
+        __syncthreads();
+        if (tid == 0) {
+            s_task = atomicAdd(ticket, 1u);
+            s_stop = zs::timed_out(status) ? 1u : 0u;
+        }
+        __syncthreads();
+        const unsigned t = s_task;
+        if (t >= total || s_stop) break;
+        const int phase = (int)(t / ((unsigned)nblk * nslot));
+        const unsigned rem = t - (unsigned)phase * nblk * nslot;
+        const int si = (int)(rem % (unsigned)nslot);
+        const int bq = (int)(rem / (unsigned)nslot);
+        const int b = phase == 0 ? bq : nblk - 1 - bq;
+        const int slot = slots[si];
+        const float *re = z32 + (int64_t)slot * z32_stride;
+        const float *im = re + plane;
+        const float *ir = dinv + (int64_t)slot * dinv_stride + (int64_t)b * 4 * TB * TB + (int64_t)phase * 2 * TB * TB;
+        const float *ii = ir + TB * TB;
+        float2 *vs = v + (int64_t)slot * v_stride;
+        unsigned long long *pf = prog + 2 * (int64_t)slot, *pb = pf + 1;
+        const int64_t r0 = (int64_t)b * TB;
+        const int rows = (int)zs::min64(TB, n - r0);
+        // the inverse block is needed last: start pulling it into L2 now
+        {
+            const char *p0 = reinterpret_cast<const char *>(ir);
+            for (int q = tid; q < 2 * TB * TB * 4 / 128; q += kThreads)
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(p0 + (int64_t)q * 128));
+        }
+        cf acc[8][R];
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int r = 0; r < R; r++) acc[i][r] = cf{0.f, 0.f};
+        bool ok = true;
+        if (phase == 1) ok = warp_progress(pf, epoch, b, status, lane) >= 0;  // own forward result
+        const int nchunk = phase == 0 ? b : nblk - 1 - b;
+        long long ready = 0;
+        for (int q = 0; q < nchunk && ok;) {
+            if (q >= ready) {
+                ready = warp_progress(phase == 0 ? pf : pb, epoch, q, status, lane);
+                if (ready < 0) {
+                    ok = false;
+                    break;
+                }
+            }
+            const int qend = (int)(ready < nchunk ? ready : nchunk);
+            for (; q < qend; q++) {
+                const int c = phase == 0 ? q : nblk - 1 - q;
+                // lane owns 4 consecutive columns: one 16-byte load per row and plane
+                const int64_t col = (int64_t)c * TB + 4 * lane;
+                if (col + 3 < n) {
+                    cf y[4][R];
+#pragma unroll
+                    for (int e = 0; e < 4; e++)
+#pragma unroll
+                        for (int r = 0; r < R; r++) {
+                            const float2 t2 = __ldcg(&vs[r * n + col + e]);
+                            y[e][r] = cf{t2.x, t2.y};
+                        }
+#pragma unroll
+                    for (int i = 0; i < 8; i++) {
+                        const int li = warp * 8 + i;
+                        const int64_t g = (r0 + (li < rows ? li : 0)) * ld + col;
+                        const float4 ar4 = __ldg(reinterpret_cast<const float4 *>(re + g));
+                        const float4 ai4 = __ldg(reinterpret_cast<const float4 *>(im + g));
+                        const cf a[4] = {cf{ar4.x, ai4.x}, cf{ar4.y, ai4.y}, cf{ar4.z, ai4.z}, cf{ar4.w, ai4.w}};
+#pragma unroll
+                        for (int e = 0; e < 4; e++)
+#pragma unroll
+                            for (int r = 0; r < R; r++) {
+                                acc[i][r].re = fmaf(a[e].re, y[e][r].re, fmaf(-a[e].im, y[e][r].im, acc[i][r].re));
+                                acc[i][r].im = fmaf(a[e].re, y[e][r].im, fmaf(a[e].im, y[e][r].re, acc[i][r].im));
+                            }
+                    }
+                } else {
+                    for (int e = 0; e < 4; e++) {
+                        if (col + e >= n) break;
+                        cf y[R];
+#pragma unroll
+                        for (int r = 0; r < R; r++) {
+                            const float2 t2 = __ldcg(&vs[r * n + col + e]);
+                            y[r] = cf{t2.x, t2.y};
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; i++) {
+                            const int li = warp * 8 + i;
+                            const int64_t g = (r0 + (li < rows ? li : 0)) * ld + col + e;
+                            const cf a = cf{__ldg(re + g), __ldg(im + g)};
+#pragma unroll
+                            for (int r = 0; r < R; r++) {
+                                acc[i][r].re = fmaf(a.re, y[r].re, fmaf(-a.im, y[r].im, acc[i][r].re));
+                                acc[i][r].im = fmaf(a.re, y[r].im, fmaf(a.im, y[r].re, acc[i][r].im));
+                            }
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                float x = acc[i][r].re, y = acc[i][r].im;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    x += __shfl_xor_sync(0xffffffffu, x, o);
+                    y += __shfl_xor_sync(0xffffffffu, y, o);
+                }
+                if (lane == 0) part[warp * 8 + i][r] = cf{x, y};
+            }
+        if (!__syncthreads_and(ok ? 1 : 0)) continue;  // a wait gave up: uniform skip
+        // right-hand side of the block's own triangle
+        for (int e = tid; e < TB * R; e += kThreads) {
+            const int i = e / R, r = e - i * R;
+            cf val = cf{0.f, 0.f};
+            if (i < rows) {
+                const float2 t2 = __ldcg(&vs[r * n + r0 + i]);
+                val = cf{t2.x - part[i][r].re, t2.y - part[i][r].im};
+            }
+            rv[i][r] = val;
+        }
+        __syncthreads();
+        // y = inverse block . rv: warp w rows 8w..8w+7, lanes over columns
+        cf acc2[8][R];
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int r = 0; r < R; r++) acc2[i][r] = cf{0.f, 0.f};
+        {
+            const int j0 = 4 * lane;  // 4 consecutive columns of the inverse block
+            cf y[4][R];
+#pragma unroll
+            for (int e = 0; e < 4; e++)
+#pragma unroll
+                for (int r = 0; r < R; r++) y[e][r] = rv[j0 + e][r];
+#pragma unroll
+            for (int i = 0; i < 8; i++) {
+                const int li = warp * 8 + i;
+                const float4 ar4 = __ldg(reinterpret_cast<const float4 *>(ir + li * TB + j0));
+                const float4 ai4 = __ldg(reinterpret_cast<const float4 *>(ii + li * TB + j0));
+                const cf a[4] = {cf{ar4.x, ai4.x}, cf{ar4.y, ai4.y}, cf{ar4.z, ai4.z}, cf{ar4.w, ai4.w}};
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+#pragma unroll
+                    for (int r = 0; r < R; r++) {
+                        acc2[i][r].re = fmaf(a[e].re, y[e][r].re, fmaf(-a[e].im, y[e][r].im, acc2[i][r].re));
+                        acc2[i][r].im = fmaf(a[e].re, y[e][r].im, fmaf(a[e].im, y[e][r].re, acc2[i][r].im));
+                    }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; i++)
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                float x = acc2[i][r].re, y = acc2[i][r].im;
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    x += __shfl_xor_sync(0xffffffffu, x, o);
+                    y += __shfl_xor_sync(0xffffffffu, y, o);
+                }
+                const int li = warp * 8 + i;
+                if (lane == 0 && li < rows) __stcg(&vs[r * n + r0 + li], make_float2(x, y));
+            }
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) zs::progress_set(phase == 0 ? pf : pb, epoch, (unsigned)(phase == 0 ? b + 1 : bq + 1));
+    }
+}
+
+template <int R>
+cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, const float *dinv,
+                       int64_t dinv_stride, float2 *v, int64_t v_stride, const int *slots, int nslot,
+                       unsigned long long *prog, unsigned epoch, unsigned *ticket, unsigned *status, int num_sms,
+                       cudaStream_t st) {
+    int per_sm = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_trsv_inv<R>, kThreads, 0);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    const int64_t nblk = (n + TB - 1) / TB;
+    int64_t grid = (int64_t)per_sm * num_sms;
+    const int64_t tasks = 2 * nblk * nslot;
+    if (grid > tasks) grid = tasks;
+    e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
+    if (e != cudaSuccess) return e;
+    void *args[] = {(void *)&z32, (void *)&ld,          (void *)&plane, (void *)&z32_stride, (void *)&n,
+                    (void *)&dinv, (void *)&dinv_stride, (void *)&v,     (void *)&v_stride,   (void *)&slots,
+                    (void *)&nslot, (void *)&prog,       (void *)&epoch, (void *)&ticket,     (void *)&status};
+    e = cudaLaunchCooperativeKernel((const void *)k_trsv_inv<R>, dim3((unsigned)grid), dim3(kThreads), args, 0, st);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, float *dinv,
+                               int64_t dinv_stride, const int *slots, int nslot, cudaStream_t st) {
+    const size_t smem = 2 * TB * kLdi * sizeof(float);
+    static bool init = false;
+    if (!init) {
+        cudaError_t e = cudaFuncSetAttribute(k_diag_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        init = true;
+    }
+    const int nblk = (int)((n + TB - 1) / TB);
+    k_diag_inv<<<dim3(nblk, 2, nslot), kInvThreads, smem, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride,
+                                                                 slots);
+    return cudaGetLastError();
+}
+
+cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                               const float *dinv, int64_t dinv_stride, float2 *v, int64_t v_stride, int nrhs,
+                               const int *slots, int nslot, unsigned long long *prog, unsigned epoch, unsigned *ticket,
+                               unsigned *status, int num_sms, cudaStream_t st) {
+    switch (nrhs) {
+        case 1:
+            return launch_inv<1>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
+                                 epoch, ticket, status, num_sms, st);
+        case 2:
+            return launch_inv<2>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
+                                 epoch, ticket, status, num_sms, st);
+        case 4:
+            return launch_inv<4>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
+                                 epoch, ticket, status, num_sms, st);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}

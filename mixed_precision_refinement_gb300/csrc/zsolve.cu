@@ -45,6 +45,9 @@ struct zsolve_ctx {
     double2 *z64 = nullptr;
     float *z32 = nullptr;
     float *pack = nullptr;
+    float *dinv = nullptr;  // inverses of the 128x128 diagonal blocks of L and U
+    float *inv32 = nullptr; // inverses of the 32x32 diagonal sub-blocks of the current outer block
+    int64_t dinv_stride = 0;
     alignas(64) unsigned char pack_map[128] = {};  // TMA tensor map over the operand packs
     alignas(64) unsigned char z32_map[128] = {};   // TMA tensor map over the float32 matrices
     float2 *v = nullptr;
@@ -172,7 +175,7 @@ int gemm_mode(const zsolve_opts &o) {
 
 size_t slot_bytes(int64_t n, int64_t ld) {
     return (size_t)n * n * sizeof(double2) + (size_t)2 * n * ld * sizeof(float) +
-           (size_t)6 * zs_pack_plane(n) * sizeof(float);
+           (size_t)6 * zs_pack_plane(n) * sizeof(float) + (size_t)zs_dinv_stride(n) * sizeof(float);
 }
 
 // ------------------------------------------------------------------ factor
@@ -186,15 +189,15 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
             ZS_CU(zs_launch_diag_lu(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, nb, slots, nslot,
-                                    ctx->d_pivflag, ctx->stream));
+                                    ctx->d_pivflag, ctx->inv32, ctx->stream));
             sp.done(1);
         }
         if (J + nb >= n) break;
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
-            ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+            ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, ctx->pack,
                                    ctx->pack_stride, mode, slots, nslot, ctx->stream));
-            ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+            ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, ctx->pack,
                                    ctx->pack_stride, mode, slots, nslot, ctx->stream));
             sp.done(2);
         }
@@ -207,22 +210,26 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
                                      ctx->d_status, ctx->num_sms, ctx->stream));
         sp.done(1);
     }
+    StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
+    ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->dinv, ctx->dinv_stride, slots,
+                             nslot, ctx->stream));
+    sp.done(1);
     return ZSOLVE_OK;
 }
 
 // ------------------------------------------------------------------ solves
 
-// v <- (LU)^-1 v for the listed slots, right-hand sides in chunks of 8/4/2/1
+// v <- (LU)^-1 v for the listed slots, right-hand sides in chunks of 4/2/1
 int lowprec_solve_slots(zsolve_ctx *ctx, int nrhs, const int *slots, int nslot) {
     int r0 = 0;
     while (r0 < nrhs) {
         const int left = nrhs - r0;
-        const int R = left >= 8 ? 8 : left >= 4 ? 4 : left >= 2 ? 2 : 1;
+        const int R = left >= 4 ? 4 : left >= 2 ? 2 : 1;
         ctx->epoch++;
         StageSpan sp(ctx, ZSOLVE_STAGE_TRSV);
-        ZS_CU(zs_launch_trsv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->v + (int64_t)r0 * ctx->n,
-                             ctx->v_stride, R, slots, nslot, ctx->prog, ctx->epoch, ctx->ticket, ctx->d_status,
-                             ctx->num_sms, ctx->stream));
+        ZS_CU(zs_launch_trsv_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->dinv, ctx->dinv_stride,
+                                 ctx->v + (int64_t)r0 * ctx->n, ctx->v_stride, R, slots, nslot, ctx->prog, ctx->epoch,
+                                 ctx->ticket, ctx->d_status, ctx->num_sms, ctx->stream));
         sp.done(1);
         r0 += R;
     }
@@ -399,7 +406,9 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
     int first_err = ZSOLVE_OK;
     for (int f0 = 0; f0 < nf; f0 += ctx->S) {
         const int count = std::min(ctx->S, nf - f0);
-        for (int s = 0; s < count; s++) ctx->h_params[s] = ZsSlotParam{omega[f0 + s], zs[2 * (f0 + s)], zs[2 * (f0 + s) + 1], 0.0};
+        for (int s = 0; s < count; s++)
+            ctx->h_params[s] =
+                ZsSlotParam{omega[f0 + s], zs[2 * (f0 + s)], zs[2 * (f0 + s) + 1], 1.0 / omega[f0 + s]};
         ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam) * count, cudaMemcpyHostToDevice,
                               ctx->stream));
         ZS_CU(cudaEventRecord(ctx->ev[0], ctx->stream));
@@ -439,6 +448,8 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->z64);
     cudaFree(c->z32);
     cudaFree(c->pack);
+    cudaFree(c->dinv);
+    cudaFree(c->inv32);
     cudaFree(c->v);
     cudaFree(c->partials);
     cudaFree(c->d_relcorr);
@@ -518,6 +529,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ctx->z64_stride = n * n;
     ctx->pack_stride = 6 * zs_pack_plane(n);
     ctx->v_stride = (int64_t)nrhs_max * n;
+    ctx->dinv_stride = zs_dinv_stride(n);
     if (ctx->opts.batch > 0) {
         ctx->S = ctx->opts.batch;
     } else {
@@ -535,6 +547,8 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->z64, (size_t)S * ctx->z64_stride * sizeof(double2));
     ALLOC(ctx->z32, (size_t)S * ctx->z32_stride * sizeof(float));
     ALLOC(ctx->pack, (size_t)S * ctx->pack_stride * sizeof(float));
+    ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
+    ALLOC(ctx->inv32, (size_t)S * ZS_INV32_STRIDE * sizeof(float));
     ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
     ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
     ALLOC(ctx->d_relcorr, (size_t)S * nrhs_max * sizeof(double));
@@ -582,7 +596,7 @@ int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const d
     if (!ctx || !L || !Psi || !G) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
     if (!(omega > 0.0) || !isfinite(omega) || !isfinite(zs_re) || !isfinite(zs_im))
         return fail(ctx, ZSOLVE_EINVAL, "omega must be positive and finite, Zs finite");
-    ctx->h_params[0] = ZsSlotParam{omega, zs_re, zs_im, 0.0};
+    ctx->h_params[0] = ZsSlotParam{omega, zs_re, zs_im, 1.0 / omega};
     ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
     StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE);
     ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32, ctx->ld,

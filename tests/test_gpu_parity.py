@@ -86,6 +86,48 @@ def test_assemble_bit_exact(zs, torch, n):
         s.close()
 
 
+def test_assemble_bit_exact_full_size_and_signed_zeros(zs, torch):
+    # every entry of the N=2157 workload at three frequencies, then a matrix
+    # built to hit every signed-zero case of the formula (L = -0, Psi = +-0,
+    # G = +-0) with negative and positive Zs parts
+    wl = workload.make(1)
+    s = zs.Solver(wl.n, 1)
+    try:
+        L, P, G = dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G)
+        z = torch.empty((wl.n, wl.n), dtype=torch.complex128, device="cuda")
+        for f in (0, 10, 20):
+            zs.zsolve_assemble(s.ctx, L, P, G, wl.omega[f], wl.zs[f].real, wl.zs[f].imag)
+            zs.zsolve_get_z64(s.ctx, z)
+            ref = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[f], wl.zs[f])
+            assert np.array_equal(z.cpu().numpy().view(np.float64), ref.view(np.float64))
+    finally:
+        s.close()
+    n = 64
+    rng = np.random.default_rng(3)
+    vals = np.array([0.0, -0.0, 0.25, 1.0, -0.5, 3.0])
+    L = rng.choice(vals, size=(n, n))
+    P = rng.choice(vals, size=(n, n))
+    G = rng.choice(vals, size=(n, n))
+    s = zs.Solver(n, 1)
+    try:
+        for zsv in (complex(-0.01, -0.02), complex(0.01, -0.02), complex(-0.01, 0.02), complex(0.0, 0.0)):
+            w = 2 * math.pi * 1.3e9
+            zs.zsolve_assemble(s.ctx, dev(torch, L), dev(torch, P), dev(torch, G), w, zsv.real, zsv.imag)
+            z = torch.empty((n, n), dtype=torch.complex128, device="cuda")
+            zs.zsolve_get_z64(s.ctx, z)
+            ref = oracle.assemble(L, P, G, w, zsv)
+            got = z.cpu().numpy()
+            assert np.array_equal(got.view(np.int64), ref.view(np.int64))  # signs of zero included
+            re = torch.empty((n, n), dtype=torch.float32, device="cuda")
+            im = torch.empty_like(re)
+            zs.zsolve_get_z32(s.ctx, re, im)
+            c64 = oracle.cast_c64(ref)
+            assert np.array_equal(re.cpu().numpy().view(np.int32), c64.real.copy().view(np.int32))
+            assert np.array_equal(im.cpu().numpy().view(np.int32), c64.imag.copy().view(np.int32))
+    finally:
+        s.close()
+
+
 def test_assemble_term_isolation(zs, torch):
     # L = 0, G = 0, and a balanced scaling: each term of Z must appear exactly
     n = 70
@@ -108,7 +150,7 @@ def test_assemble_term_isolation(zs, torch):
 # ---------------------------------------------------------------- stages
 
 
-@pytest.mark.parametrize("n,nrhs", [(1, 1), (64, 2), (257, 3), (300, 8)])
+@pytest.mark.parametrize("n,nrhs", [(1, 1), (64, 2), (237, 1), (257, 3), (300, 8), (2157, 1)])
 def test_residual_against_oracle(zs, torch, n, nrhs):
     wl = workload.make_small(n, seed=10 + n, nf=1, nrhs=nrhs)
     X = workload.random_rhs(n, nrhs, seed=3)

@@ -17,7 +17,10 @@ import workload
 
 pytestmark = pytest.mark.gpu
 
-TOL = 1e-6  # same kernel, same float32 factors and inputs: agreement to float32 rounding
+# the context path applies the diagonal blocks through explicit inverses and
+# the allocation-free one by substitution: both are float32 solves with the
+# same factors, held to the tolerance the low-precision solve tests use
+TOL = 1e-4
 
 
 def _factored(zs, torch, wl, f):
