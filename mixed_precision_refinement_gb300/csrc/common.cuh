@@ -114,19 +114,21 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
                                cudaStream_t st);
 
 // Factorisation steps at outer-block column J for nslot slots listed in slots[].
-// inv32: per slot ZS_INV32_STRIDE floats, [sub-block kb][U, L][re, im][32][32]:
-// inverses of the four 32x32 diagonal sub-blocks of U11 and of L11.
+// inv32: per slot and outer block, ZS_INV32_STRIDE floats:
+// [sub-block kb][U, L][re, im][32][32], the inverses of the four 32x32
+// diagonal sub-blocks of U and of L (identity padding in a partial block).
 #define ZS_INV32_STRIDE (4 * 2 * 2 * 32 * 32)
+inline int64_t zs_inv32_slot_stride(int64_t n) { return ((n + 127) / 128) * ZS_INV32_STRIDE; }
 cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                               int64_t J, int nb, const int *slots, int nslot, int *pivflag, float *inv32,
-                              cudaStream_t st);
+                              int64_t inv32_stride, cudaStream_t st);
 // mode: 0 = pack plain fp32 (FFMA), 1 = tf32 rounded (TF32), 2 = tf32 hi + lo (TF32X3)
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
-                             const int *slots, int nslot, cudaStream_t st);
+                             int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
+                             int mode, const int *slots, int nslot, cudaStream_t st);
 cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
-                             const int *slots, int nslot, cudaStream_t st);
+                             int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
+                             int mode, const int *slots, int nslot, cudaStream_t st);
 cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                  int64_t J, const float *pack, int64_t pack_stride, const int *slots,
                                  int nslot, cudaStream_t st);
@@ -150,8 +152,9 @@ cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int6
 
 // Inverses of the 128x128 diagonal blocks of L (unit lower) and U (upper):
 // per slot [block][L, U][re, im][128][128] floats.
-cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, float *dinv,
-                               int64_t dinv_stride, const int *slots, int nslot, cudaStream_t st);
+cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                               const float *inv32, int64_t inv32_stride, float *dinv, int64_t dinv_stride,
+                               const int *slots, int nslot, cudaStream_t st);
 inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }
 // Triangular solves with 128-row blocks and the inverse diagonal blocks; nrhs 1, 2 or 4 per launch.
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,

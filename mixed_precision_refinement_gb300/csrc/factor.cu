@@ -52,7 +52,7 @@ constexpr int kDiagThreads = 512;  // 16 warps
 
 __global__ void __launch_bounds__(kDiagThreads, 1)
 k_diag_lu(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
-          const int *__restrict__ slots, int *__restrict__ pivflag, float *__restrict__ inv32) {
+          const int *__restrict__ slots, int *__restrict__ pivflag, float *__restrict__ inv32, int64_t inv32_stride) {
     extern __shared__ float sm[];
     float *sre = sm;                   // [NB][LDS]
     float *sim = sm + NB * LDS;        // [NB][LDS]
@@ -200,7 +200,16 @@ k_diag_lu(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride
         im[g] = sim[i * LDS + j];
     }
     if (tid == 0 && flagged) pivflag[slot] = 1;
-    if (nb < NB) return;  // last block: no block solves follow
+    if (nb < NB) {  // last, partial block: identity padding for the sub-block inverses
+        for (int idx = tid; idx < NB * NB; idx += kDiagThreads) {
+            const int i = idx >> 7, j = idx & (NB - 1);
+            if (i >= nb || j >= nb) {
+                sre[i * LDS + j] = (i == j) ? 1.f : 0.f;
+                sim[i * LDS + j] = 0.f;
+            }
+        }
+        __syncthreads();
+    }
     // Inverses of the four 32x32 diagonal sub-blocks of U11 (upper) and of
     // L11 (unit lower), for the block triangular solves.  Warp w inverts
     // sub-block w/2 (0-3: U, 4-7: L), rows (w & 1) + 2t, two rows at a time;
@@ -209,7 +218,7 @@ k_diag_lu(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride
     {
         const int blk = warp >> 1, upper = blk < 4, kb = blk & 3;
         const int o = kb * P;
-        float *dst = inv32 + (int64_t)slot * ZS_INV32_STRIDE + (kb * 2 + (upper ? 0 : 1)) * 2 * P * P;
+        float *dst = inv32 + (int64_t)slot * inv32_stride + (J / NB) * ZS_INV32_STRIDE + (kb * 2 + (upper ? 0 : 1)) * 2 * P * P;
         const cf dl = upper ? zs::crecip(cf{sre[(o + lane) * LDS + o + lane], sim[(o + lane) * LDS + o + lane]})
                             : cf{1.f, 0.f};
         for (int i0 = (warp & 1); i0 < P; i0 += 4) {
@@ -268,8 +277,8 @@ constexpr int kTLRows = 128;       // L21 rows per CTA (8 per warp)
 
 __global__ void __launch_bounds__(kTrsmThreads, 1)
 k_trsm_l(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-         const float *__restrict__ inv32, float *__restrict__ pack, int64_t pack_stride, int mode,
-         const int *__restrict__ slots) {
+         const float *__restrict__ inv32, int64_t inv32_stride, float *__restrict__ pack, int64_t pack_stride,
+         int mode, const int *__restrict__ slots) {
     extern __shared__ float sm[];
     float *ure = sm;                 // [NB][NB]: U11 above the diagonal blocks, inv(U_kb,kb) on them
     float *uim = sm + NB * NB;
@@ -277,7 +286,7 @@ k_trsm_l(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride,
     const int slot = slots[blockIdx.y];
     float *re = z32 + (int64_t)slot * z32_stride;
     float *im = re + plane;
-    const float *inv = inv32 + (int64_t)slot * ZS_INV32_STRIDE;
+    const float *inv = inv32 + (int64_t)slot * inv32_stride + (J / NB) * ZS_INV32_STRIDE;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int idx = tid; idx < NB * NB; idx += kTrsmThreads) {
         const int i = idx >> 7, j = idx & (NB - 1);
@@ -375,8 +384,8 @@ constexpr int kTUPad = kTUCols + 1;
 
 __global__ void __launch_bounds__(kTrsmThreads, 1)
 k_trsm_u(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-         const float *__restrict__ inv32, float *__restrict__ pack, int64_t pack_stride, int mode,
-         const int *__restrict__ slots) {
+         const float *__restrict__ inv32, int64_t inv32_stride, float *__restrict__ pack, int64_t pack_stride,
+         int mode, const int *__restrict__ slots) {
     extern __shared__ float sm[];
     float *lre = sm;                 // [NB][LDS]: L11 below the diagonal blocks, inv(L_kb,kb) on them
     float *lim = sm + NB * LDS;
@@ -386,7 +395,7 @@ k_trsm_u(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride,
     const int slot = slots[blockIdx.y];
     float *re = z32 + (int64_t)slot * z32_stride;
     float *im = re + plane;
-    const float *inv = inv32 + (int64_t)slot * ZS_INV32_STRIDE;
+    const float *inv = inv32 + (int64_t)slot * inv32_stride + (J / NB) * ZS_INV32_STRIDE;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int64_t c0 = J + NB + (int64_t)blockIdx.x * kTUCols;
     const int ncol = (int)zs::min64(kTUCols, n - c0);
@@ -590,7 +599,7 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 
 cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                               int64_t J, int nb, const int *slots, int nslot, int *pivflag, float *inv32,
-                              cudaStream_t st) {
+                              int64_t inv32_stride, cudaStream_t st) {
     (void)n;
     const size_t smem = (2 * NB * LDS + 4 * P) * sizeof(float);
     static bool init = false;
@@ -599,13 +608,14 @@ cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32
         if (e != cudaSuccess) return e;
         init = true;
     }
-    k_diag_lu<<<nslot, kDiagThreads, smem, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag, inv32);
+    k_diag_lu<<<nslot, kDiagThreads, smem, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag, inv32,
+                                                  inv32_stride);
     return cudaGetLastError();
 }
 
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
-                             const int *slots, int nslot, cudaStream_t st) {
+                             int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
+                             int mode, const int *slots, int nslot, cudaStream_t st) {
     const size_t smem = (2 * NB * NB) * sizeof(float) + 16 * 8 * 32 * sizeof(cf);
     static bool init = false;
     if (!init) {
@@ -615,14 +625,14 @@ cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_
     }
     const int64_t m2 = n - J - NB;
     dim3 grid((unsigned)((m2 + kTLRows - 1) / kTLRows), nslot);
-    k_trsm_l<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, pack, pack_stride, mode,
-                                                slots);
+    k_trsm_l<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, inv32_stride, pack,
+                                                pack_stride, mode, slots);
     return cudaGetLastError();
 }
 
 cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                             int64_t J, const float *inv32, float *pack, int64_t pack_stride, int mode,
-                             const int *slots, int nslot, cudaStream_t st) {
+                             int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
+                             int mode, const int *slots, int nslot, cudaStream_t st) {
     const size_t smem = (2 * NB * LDS + 2 * NB * kTUPad) * sizeof(float) + 16 * 4 * 32 * sizeof(cf);
     static bool init = false;
     if (!init) {
@@ -632,8 +642,8 @@ cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_
     }
     const int64_t m2 = n - J - NB;
     dim3 grid((unsigned)((m2 + kTUCols - 1) / kTUCols), nslot);
-    k_trsm_u<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, pack, pack_stride, mode,
-                                                slots);
+    k_trsm_u<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, inv32_stride, pack,
+                                                pack_stride, mode, slots);
     return cudaGetLastError();
 }
 

@@ -5,10 +5,9 @@
 // single-precision factorisation).
 //
 // k_diag_inv (once per factorisation): for every 128 x 128 diagonal block of
-// every frequency, X = L_bb^-1 (unit lower) and X = U_bb^-1 (upper), one row
-// of X per warp step (x^T L = e_i^T, resp. x^T U = e_i^T, solved along the
-// row so that both the factor reads and the result writes are contiguous).
-// Padding rows beyond n get the identity.
+// every frequency, X = L_bb^-1 (unit lower) and X = U_bb^-1 (upper), built from
+// the inverses of the 32 x 32 diagonal sub-blocks the factorisation left
+// behind, by block substitution with 32 x 32 products in shared memory.
 //
 // k_trsv_inv (per solve): the same ticketed, in-order task scheme as the
 // sequential kernel, with 128-row blocks (half the dependency chain) and the
@@ -27,108 +26,108 @@ using zs::cf;
 
 constexpr int TB = ZS_TB2;  // 128
 constexpr int kInvThreads = 512;
-constexpr int kLdi = TB + 1;
+constexpr int SB = 32;       // sub-block size
+constexpr int SBP = SB + 1;  // padded sub-block row
 
+// One 32x32 complex sub-block in shared memory (two padded float planes).
+struct Blk {
+    float r[SB * SBP], i[SB * SBP];
+};
+
+// acc[2] += A . B for this thread's two entries (row t >> 4, columns 2*(t & 15) + {0, 1})
+__device__ __forceinline__ void blk_mac(const Blk &A, const Blk &B, cf (&acc)[2], int row, int c0) {
+#pragma unroll 8
+    for (int k = 0; k < SB; k++) {
+        const cf a = cf{A.r[row * SBP + k], A.i[row * SBP + k]};
+#pragma unroll
+        for (int q = 0; q < 2; q++) {
+            const cf b = cf{B.r[k * SBP + c0 + q], B.i[k * SBP + c0 + q]};
+            acc[q].re = fmaf(a.re, b.re, fmaf(-a.im, b.im, acc[q].re));
+            acc[q].im = fmaf(a.re, b.im, fmaf(a.im, b.re, acc[q].im));
+        }
+    }
+}
+
+// Inverse of a 128 x 128 diagonal block of L (unit lower) or U (upper) from
+// the inverses of its four 32 x 32 diagonal sub-blocks (written by the
+// factorisation), by block substitution: with D_i the inverted diagonal
+// sub-blocks,
+//   L: X_ii = D_i,  X_ik = -D_i sum_{m=k}^{i-1} L_im X_mk   (i > k, i ascending)
+//   U: X_ii = D_i,  X_ik = -D_i sum_{m=i+1}^{k} U_im X_mk   (i < k, i descending)
+// Padding rows beyond n are the identity.
 __global__ void __launch_bounds__(kInvThreads, 1)
 k_diag_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-           float *__restrict__ dinv, int64_t dinv_stride, const int *__restrict__ slots) {
+           const float *__restrict__ inv32, int64_t inv32_stride, float *__restrict__ dinv, int64_t dinv_stride,
+           const int *__restrict__ slots) {
     extern __shared__ float sm[];
-    float *are = sm, *aim = sm + TB * kLdi;
+    Blk *F = reinterpret_cast<Blk *>(sm);  // [6]: off-diagonal factor sub-blocks of the triangle
+    Blk *X = F + 6;                        // [10]: result sub-blocks, diagonal included
+    Blk *T = X + 10;                       // scratch
     const int b = blockIdx.x, upper = blockIdx.y, slot = slots[blockIdx.z];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int tid = threadIdx.x;
+    // packed triangle indices; (i, j) is mirrored into the lower triangle for U
+    auto fidx = [upper](int i, int j) { if (upper) { int t = i; i = j; j = t; } return i * (i - 1) / 2 + j; };
+    auto xidx = [upper](int i, int j) { if (upper) { int t = i; i = j; j = t; } return i * (i + 1) / 2 + j; };
     const float *re = z32 + (int64_t)slot * z32_stride;
     const float *im = re + plane;
+    const float *d32 = inv32 + (int64_t)slot * inv32_stride + (int64_t)b * ZS_INV32_STRIDE;
     const int64_t r0 = (int64_t)b * TB;
     const int rows = (int)zs::min64(TB, n - r0);
+    // off-diagonal factor sub-blocks of the needed triangle, diagonal inverses, zero result blocks
     for (int idx = tid; idx < TB * TB; idx += kInvThreads) {
-        const int i = idx >> 7, j = idx & (TB - 1);
-        float a = 0.f, c = 0.f;
-        if (i < rows && j < rows) {
-            a = re[(r0 + i) * ld + r0 + j];
-            c = im[(r0 + i) * ld + r0 + j];
-        } else if (i == j) {
-            a = 1.f;  // identity padding
+        const int gi = idx >> 7, gj = idx & (TB - 1);
+        const int bi = gi >> 5, bj = gj >> 5, li = gi & 31, lj = gj & 31;
+        const int o = li * SBP + lj;
+        const bool tri = upper ? (bj > bi) : (bi > bj);
+        if (tri) {
+            float a = 0.f, c = 0.f;
+            if (gi < rows && gj < rows) {
+                a = re[(r0 + gi) * ld + r0 + gj];
+                c = im[(r0 + gi) * ld + r0 + gj];
+            }
+            F[fidx(bi, bj)].r[o] = a;
+            F[fidx(bi, bj)].i[o] = c;
         }
-        are[i * kLdi + j] = a;
-        aim[i * kLdi + j] = c;
+        if (bi == bj) {
+            const float *d = d32 + (bi * 2 + (upper ? 0 : 1)) * 2 * SB * SB;
+            X[xidx(bi, bi)].r[o] = d[li * SB + lj];
+            X[xidx(bi, bi)].i[o] = d[SB * SB + li * SB + lj];
+        }
     }
     __syncthreads();
+    const int row = tid >> 4, c0 = 2 * (tid & 15);
+    for (int step = 0; step < 3; step++) {
+        const int i = upper ? 2 - step : step + 1;  // block row being formed
+        const int kbeg = upper ? i + 1 : 0, kend = upper ? 4 : i;
+        for (int k = kbeg; k < kend; k++) {
+            cf acc[2] = {cf{0.f, 0.f}, cf{0.f, 0.f}};
+            const int mbeg = upper ? i + 1 : k, mend = upper ? k + 1 : i;
+            for (int m = mbeg; m < mend; m++) blk_mac(F[fidx(i, m)], X[xidx(m, k)], acc, row, c0);
+#pragma unroll
+            for (int q = 0; q < 2; q++) {
+                T->r[row * SBP + c0 + q] = acc[q].re;
+                T->i[row * SBP + c0 + q] = acc[q].im;
+            }
+            __syncthreads();
+            cf out[2] = {cf{0.f, 0.f}, cf{0.f, 0.f}};
+            blk_mac(X[xidx(i, i)], *T, out, row, c0);
+#pragma unroll
+            for (int q = 0; q < 2; q++) {
+                X[xidx(i, k)].r[row * SBP + c0 + q] = -out[q].re;
+                X[xidx(i, k)].i[row * SBP + c0 + q] = -out[q].im;
+            }
+            __syncthreads();
+        }
+    }
     float *xr = dinv + (int64_t)slot * dinv_stride + (int64_t)b * 4 * TB * TB + (int64_t)upper * 2 * TB * TB;
     float *xi = xr + TB * TB;
-    // rows i0 = warp + 32 t and i1 = i0 + 16, two at a time; lane holds
-    // columns j = lane + 32 h; diagonal reciprocals formed once per lane
-    cf dl[4];
-#pragma unroll
-    for (int h = 0; h < 4; h++) {
-        const int j = lane + 32 * h;
-        dl[h] = upper ? zs::crecip(cf{are[j * kLdi + j], aim[j * kLdi + j]}) : cf{1.f, 0.f};
-    }
-    for (int i0 = warp; i0 < TB; i0 += 32) {
-        const int i1 = i0 + 16;
-        cf x[4], y[4];
-#pragma unroll
-        for (int h = 0; h < 4; h++) {
-            x[h] = cf{(lane + 32 * h == i0) ? 1.f : 0.f, 0.f};
-            y[h] = cf{(lane + 32 * h == i1) ? 1.f : 0.f, 0.f};
-        }
-        if (!upper) {
-            // x^T L = e_i^T, L unit lower: for k = i..1, x_k final; x_j -= x_k L[k][j], j < k
-#pragma unroll
-            for (int h = 3; h >= 0; h--) {
-                for (int kl = 31; kl >= 0; kl--) {
-                    const int k = 32 * h + kl;
-                    if (k > i1 || k == 0) continue;
-                    cf xk, yk;
-                    xk.re = __shfl_sync(0xffffffffu, x[h].re, kl);
-                    xk.im = __shfl_sync(0xffffffffu, x[h].im, kl);
-                    yk.re = __shfl_sync(0xffffffffu, y[h].re, kl);
-                    yk.im = __shfl_sync(0xffffffffu, y[h].im, kl);
-#pragma unroll
-                    for (int h2 = 0; h2 <= h; h2++) {
-                        const int j = lane + 32 * h2;
-                        if (j < k) {
-                            const cf lv = cf{are[k * kLdi + j], aim[k * kLdi + j]};
-                            y[h2] = zs::cfms(y[h2], yk, lv);
-                            if (k <= i0) x[h2] = zs::cfms(x[h2], xk, lv);
-                        }
-                    }
-                }
-            }
-        } else {
-            // x^T U = e_i^T, U upper: for k = i..127, x_k /= U[k][k] (final); x_j -= x_k U[k][j], j > k
-#pragma unroll
-            for (int h = 0; h < 4; h++) {
-                for (int kl = 0; kl < 32; kl++) {
-                    const int k = 32 * h + kl;
-                    if (k < i0) continue;
-                    if (lane == kl) {
-                        x[h] = zs::cmul(x[h], dl[h]);
-                        if (k >= i1) y[h] = zs::cmul(y[h], dl[h]);
-                    }
-                    cf xk, yk;
-                    xk.re = __shfl_sync(0xffffffffu, x[h].re, kl);
-                    xk.im = __shfl_sync(0xffffffffu, x[h].im, kl);
-                    yk.re = __shfl_sync(0xffffffffu, y[h].re, kl);
-                    yk.im = __shfl_sync(0xffffffffu, y[h].im, kl);
-#pragma unroll
-                    for (int h2 = h; h2 < 4; h2++) {
-                        const int j = lane + 32 * h2;
-                        if (j > k) {
-                            const cf uv = cf{are[k * kLdi + j], aim[k * kLdi + j]};
-                            x[h2] = zs::cfms(x[h2], xk, uv);
-                            if (k >= i1) y[h2] = zs::cfms(y[h2], yk, uv);
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int h = 0; h < 4; h++) {
-            xr[i0 * TB + lane + 32 * h] = x[h].re;
-            xi[i0 * TB + lane + 32 * h] = x[h].im;
-            xr[i1 * TB + lane + 32 * h] = y[h].re;
-            xi[i1 * TB + lane + 32 * h] = y[h].im;
-        }
+    for (int idx = tid; idx < TB * TB; idx += kInvThreads) {
+        const int gi = idx >> 7, gj = idx & (TB - 1);
+        const int bi = gi >> 5, bj = gj >> 5;
+        const bool keep = upper ? (bj >= bi) : (bi >= bj);
+        const int o = (gi & 31) * SBP + (gj & 31);
+        xr[idx] = keep ? X[xidx(bi, bj)].r[o] : 0.f;
+        xi[idx] = keep ? X[xidx(bi, bj)].i[o] : 0.f;
     }
 }
 
@@ -352,9 +351,10 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
 
 }  // namespace
 
-cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, float *dinv,
-                               int64_t dinv_stride, const int *slots, int nslot, cudaStream_t st) {
-    const size_t smem = 2 * TB * kLdi * sizeof(float);
+cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                               const float *inv32, int64_t inv32_stride, float *dinv, int64_t dinv_stride,
+                               const int *slots, int nslot, cudaStream_t st) {
+    const size_t smem = 17 * sizeof(Blk);
     static bool init = false;
     if (!init) {
         cudaError_t e = cudaFuncSetAttribute(k_diag_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -362,8 +362,8 @@ cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int6
         init = true;
     }
     const int nblk = (int)((n + TB - 1) / TB);
-    k_diag_inv<<<dim3(nblk, 2, nslot), kInvThreads, smem, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride,
-                                                                 slots);
+    k_diag_inv<<<dim3(nblk, 2, nslot), kInvThreads, smem, st>>>(z32, ld, plane, z32_stride, n, inv32, inv32_stride,
+                                                                 dinv, dinv_stride, slots);
     return cudaGetLastError();
 }
 

@@ -175,7 +175,8 @@ int gemm_mode(const zsolve_opts &o) {
 
 size_t slot_bytes(int64_t n, int64_t ld) {
     return (size_t)n * n * sizeof(double2) + (size_t)2 * n * ld * sizeof(float) +
-           (size_t)6 * zs_pack_plane(n) * sizeof(float) + (size_t)zs_dinv_stride(n) * sizeof(float);
+           (size_t)6 * zs_pack_plane(n) * sizeof(float) + (size_t)zs_dinv_stride(n) * sizeof(float) +
+           (size_t)zs_inv32_slot_stride(n) * sizeof(float);
 }
 
 // ------------------------------------------------------------------ factor
@@ -189,16 +190,18 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
             ZS_CU(zs_launch_diag_lu(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, nb, slots, nslot,
-                                    ctx->d_pivflag, ctx->inv32, ctx->stream));
+                                    ctx->d_pivflag, ctx->inv32, zs_inv32_slot_stride(n), ctx->stream));
             sp.done(1);
         }
         if (J + nb >= n) break;
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
-            ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, ctx->pack,
-                                   ctx->pack_stride, mode, slots, nslot, ctx->stream));
-            ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, ctx->pack,
-                                   ctx->pack_stride, mode, slots, nslot, ctx->stream));
+            ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
+                                   zs_inv32_slot_stride(n), ctx->pack, ctx->pack_stride, mode, slots, nslot,
+                                   ctx->stream));
+            ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
+                                   zs_inv32_slot_stride(n), ctx->pack, ctx->pack_stride, mode, slots, nslot,
+                                   ctx->stream));
             sp.done(2);
         }
         StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
@@ -211,8 +214,8 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
         sp.done(1);
     }
     StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
-    ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->dinv, ctx->dinv_stride, slots,
-                             nslot, ctx->stream));
+    ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->inv32, zs_inv32_slot_stride(n),
+                             ctx->dinv, ctx->dinv_stride, slots, nslot, ctx->stream));
     sp.done(1);
     return ZSOLVE_OK;
 }
@@ -548,7 +551,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->z32, (size_t)S * ctx->z32_stride * sizeof(float));
     ALLOC(ctx->pack, (size_t)S * ctx->pack_stride * sizeof(float));
     ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
-    ALLOC(ctx->inv32, (size_t)S * ZS_INV32_STRIDE * sizeof(float));
+    ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
     ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
     ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
     ALLOC(ctx->d_relcorr, (size_t)S * nrhs_max * sizeof(double));
