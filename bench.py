@@ -185,8 +185,10 @@ def run_ours(args):
     wl = workload.make(args.config)
     n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
     gemm = getattr(zs, "ZSOLVE_GEMM_" + args.gemm)
-    solver = zs.Solver(n, nrhs, gemm=gemm, batch=args.batch or nf, profile=1)
+    solver = zs.Solver(n, nrhs, gemm=gemm, batch=args.batch or nf, profile=1,
+                       resid=getattr(zs, "ZSOLVE_RESID_" + args.resid))
     ctx = solver.ctx
+    resid_mode = "DF" if zs.zsolve_get_resid_mode(ctx) == zs.ZSOLVE_RESID_DF else "F64"
     L = torch.from_numpy(wl.L).cuda()
     P = torch.from_numpy(wl.Psi).cuda()
     G = torch.from_numpy(wl.G).cuda()
@@ -295,8 +297,10 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32 factor + f64 refine", "data": "synthetic",
+        "dtype": "f32 factor + " + ("f64" if resid_mode == "F64" else "double-float f32x2") + " residual",
+        "data": "synthetic",
         "config": {"workload": workload_name(args.config), "n": n, "nf": nf, "nrhs": nrhs, "gemm": args.gemm,
+                   "resid": resid_mode,
                    "batch": args.batch or nf, "l2": "flushed between steps (512 MB write)",
                    "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
         "lu_tflops": lu_tflops, "resid_gbs": res_gbs,
@@ -324,6 +328,7 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--gemm", default="TF32X3", choices=["TF32", "TF32X3", "FFMA"])
     ap.add_argument("--batch", type=int, default=0)
+    ap.add_argument("--resid", default="F64", choices=["F64", "DF"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     args = ap.parse_args()

@@ -63,6 +63,11 @@ extern "C" {
 #define ZSOLVE_GEMM_TF32X3 2 /* split hi/lo tf32, three products per term (tcgen05) */
 #define ZSOLVE_GEMM_FFMA 3   /* FP32 fused multiply-add on the CUDA cores */
 
+/* arithmetic of the residual r = b - Z x (step 3) */
+#define ZSOLVE_RESID_F64 0 /* float64 multiply-adds (DFMA); default */
+#define ZSOLVE_RESID_DF 1  /* double-float on the FP32 pipes, about 46 bits (the page's GPU residual);
+                              checked against the float64 kernel when the context is created */
+
 typedef struct zsolve_ctx zsolve_ctx; /* opaque */
 
 typedef struct {
@@ -73,6 +78,7 @@ typedef struct {
     int batch;          /* frequencies factored together by zsolve_sweep; 0 = automatic */
     int force_fallback; /* testing aid: treat every frequency as stalled (default 0) */
     int profile;        /* 1: time every stage with CUDA events (zsolve_get_profile); default 0 */
+    int resid;          /* ZSOLVE_RESID_* (default F64) */
 } zsolve_opts;
 
 /* stages of the path, for zsolve_get_profile */
@@ -160,6 +166,13 @@ int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs);
 /* x = Z^-1 b by the float64 LU with partial pivoting of the assembled Z (the
  * fallback on its own).  b, x: device c128, nrhs x n. */
 int zsolve_fallback_solve(zsolve_ctx *ctx, const void *b, void *x, int nrhs);
+
+/* Residual arithmetic in use (ZSOLVE_RESID_*) in *mode.  A context created
+ * with ZSOLVE_RESID_DF first compares the double-float residual with the
+ * float64 one on a synthetic system (the page's start-up self-test, section
+ * "The shader compiler was erasing the error"); if they disagree by more than
+ * 1e-12 relative, the context uses ZSOLVE_RESID_F64. */
+int zsolve_get_resid_mode(zsolve_ctx *ctx, int *mode);
 
 /* Copy the float64 Z (device c128, n x n) of the single system to dst. */
 int zsolve_get_z64(zsolve_ctx *ctx, void *dst);

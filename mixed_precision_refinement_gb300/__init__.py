@@ -34,13 +34,16 @@ ZSOLVE_GEMM_TF32 = 1
 ZSOLVE_GEMM_TF32X3 = 2
 ZSOLVE_GEMM_FFMA = 3
 
+ZSOLVE_RESID_F64 = 0
+ZSOLVE_RESID_DF = 1
+
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zsolve.h")
 
 
 class zsolve_opts(ctypes.Structure):
     _fields_ = [("tol", ctypes.c_double), ("max_iter", ctypes.c_int), ("gemm", ctypes.c_int),
                 ("outer_block", ctypes.c_int), ("batch", ctypes.c_int), ("force_fallback", ctypes.c_int),
-                ("profile", ctypes.c_int)]
+                ("profile", ctypes.c_int), ("resid", ctypes.c_int)]
 
 
 STAGES = ("assemble", "diag", "trsm", "schur", "trsv", "residual", "update", "fallback")
@@ -89,6 +92,7 @@ def _load():
         "zsolve_pivot_flag": (I, [P, ctypes.POINTER(I)]),
         "zsolve_lowprec_solve_noalloc": (I, [P, I64, I64, I64, I64, I, P, I64, I, P]),
         "zsolve_get_profile": (I, [P, ctypes.POINTER(zsolve_profile)]),
+        "zsolve_get_resid_mode": (I, [P, ctypes.POINTER(I)]),
         "zsolve_reset_profile": (I, [P]),
         "zsolve_strerror": (ctypes.c_char_p, [I]),
         "zsolve_last_error": (ctypes.c_char_p, [P]),
@@ -279,6 +283,12 @@ def zsolve_get_profile(ctx) -> zsolve_profile:
     p = zsolve_profile()
     _check(ctx, _lib.zsolve_get_profile(ctx, ctypes.byref(p)))
     return p
+
+
+def zsolve_get_resid_mode(ctx) -> int:
+    m = ctypes.c_int()
+    _check(ctx, _lib.zsolve_get_resid_mode(ctx, ctypes.byref(m)))
+    return m.value
 
 
 def zsolve_reset_profile(ctx) -> None:

@@ -177,6 +177,15 @@ inline int zs_rhs_chunks(int nrhs) {
     return c;
 }
 
+// Double-float residual: x split into float4 (Re hi, Re lo, Im hi, Im lo) per element first.
+cudaError_t zs_launch_split_x(const double2 *x, int64_t x_stride, int64_t n, int nrhs, float4 *xs, int64_t xs_stride,
+                              const int *slots, int nslot, cudaStream_t st);
+cudaError_t zs_launch_residual_df(const double2 *z64, int64_t z64_stride, int64_t n, const double2 *b, const float4 *xs,
+                                  int64_t xs_stride, int nrhs, float2 *out_c64, int64_t out64_stride,
+                                  double2 *out_c128, int64_t out128_stride, const int *slots, int nslot,
+                                  cudaStream_t st);
+cudaError_t zs_launch_selftest_fill(double2 *z, double2 *x, int64_t n, int zero_re, cudaStream_t st);
+
 // v = (float2) b for every listed slot
 cudaError_t zs_launch_cast_rhs(const double2 *b, int64_t n, int nrhs, float2 *v, int64_t v_stride,
                                const int *slots, int nslot, cudaStream_t st);

@@ -51,6 +51,8 @@ struct zsolve_ctx {
     alignas(64) unsigned char pack_map[128] = {};  // TMA tensor map over the operand packs
     alignas(64) unsigned char z32_map[128] = {};   // TMA tensor map over the float32 matrices
     float2 *v = nullptr;
+    float4 *xs = nullptr;  // double-float split of x (residual mode DF)
+    int resid_mode = ZSOLVE_RESID_F64;
     double *partials = nullptr;
     int nchunks = 0;
     double *d_relcorr = nullptr, *h_relcorr = nullptr;
@@ -289,6 +291,66 @@ int fallback_slot(zsolve_ctx *ctx, int slot, const double2 *b, double2 *x, int n
     return ZSOLVE_OK;
 }
 
+// r = b - Z x for the listed slots in the context's residual arithmetic.
+int residual_slots(zsolve_ctx *ctx, const double2 *b, const double2 *x, int64_t x_stride, int nrhs, float2 *o64,
+                   int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot, StageSpan *sp) {
+    const int64_t n = ctx->n;
+    if (ctx->resid_mode == ZSOLVE_RESID_DF) {
+        const int64_t xs_stride = (int64_t)ctx->nrhs_max * n;
+        ZS_CU(zs_launch_split_x(x, x_stride, n, nrhs, ctx->xs, xs_stride, slots, nslot, ctx->stream));
+        ZS_CU(zs_launch_residual_df(ctx->z64, ctx->z64_stride, n, b, ctx->xs, xs_stride, nrhs, o64, o64s, o128, o128s,
+                                    slots, nslot, ctx->stream));
+        int chunks = 0;
+        for (int r = nrhs; r > 0; chunks++) r -= r >= 4 ? 4 : r >= 2 ? 2 : 1;
+        sp->done(1 + chunks);
+    } else {
+        ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, b, x, x_stride, nrhs, o64, o64s, o128, o128s, slots,
+                                 nslot, ctx->stream));
+        sp->done(zs_rhs_chunks(nrhs));
+    }
+    return ZSOLVE_OK;
+}
+
+// Start-up check of the double-float residual against the float64 one on a
+// synthetic positive system (two cases: with and without real parts).
+int resid_selftest(zsolve_ctx *ctx) {
+    const int64_t n = ctx->n;
+    double2 *tx = nullptr, *tr = nullptr, *tb = nullptr;
+    std::vector<double2> h1(n), h2(n);
+    int ok = 1;
+    if (cudaMalloc(&tx, n * sizeof(double2)) != cudaSuccess || cudaMalloc(&tr, 2 * n * sizeof(double2)) != cudaSuccess ||
+        cudaMalloc(&tb, n * sizeof(double2)) != cudaSuccess) {
+        cudaFree(tx);
+        cudaFree(tr);
+        cudaFree(tb);
+        cudaGetLastError();
+        return fail(ctx, ZSOLVE_ENOMEM, "residual self-test buffers");
+    }
+    for (int zero_re = 0; zero_re < 2 && ok; zero_re++) {
+        ZS_CU(cudaMemsetAsync(tb, 0, n * sizeof(double2), ctx->stream));
+        ZS_CU(zs_launch_selftest_fill(ctx->z64, tx, n, zero_re, ctx->stream));
+        ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, tb, tx, 0, 1, nullptr, 0, tr, 0, ctx->d_all, 1,
+                                 ctx->stream));
+        ZS_CU(zs_launch_split_x(tx, 0, n, 1, ctx->xs, 0, ctx->d_all, 1, ctx->stream));
+        ZS_CU(zs_launch_residual_df(ctx->z64, ctx->z64_stride, n, tb, ctx->xs, 0, 1, nullptr, 0, tr + n, 0, ctx->d_all,
+                                    1, ctx->stream));
+        ZS_CU(cudaMemcpyAsync(h1.data(), tr, n * sizeof(double2), cudaMemcpyDeviceToHost, ctx->stream));
+        ZS_CU(cudaMemcpyAsync(h2.data(), tr + n, n * sizeof(double2), cudaMemcpyDeviceToHost, ctx->stream));
+        ZS_CU(cudaStreamSynchronize(ctx->stream));
+        double err = 0.0, scale = 0.0;
+        for (int64_t i = 0; i < n; i++) {
+            err = std::max(err, std::max(fabs(h1[i].x - h2[i].x), fabs(h1[i].y - h2[i].y)));
+            scale = std::max(scale, std::max(fabs(h1[i].x), fabs(h1[i].y)));
+        }
+        if (!(err <= 1e-12 * scale)) ok = 0;
+    }
+    cudaFree(tx);
+    cudaFree(tr);
+    cudaFree(tb);
+    ctx->resid_mode = ok ? ZSOLVE_RESID_DF : ZSOLVE_RESID_F64;
+    return ZSOLVE_OK;
+}
+
 // Refinement of slots 0..count-1 with x for slot s at x + s*x_stride.
 int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride, int nrhs, int count,
                  zsolve_info *info) {
@@ -331,9 +393,8 @@ int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride
         // step 3: residual in double precision, rounded for the low-precision solve
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL);
-            ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, b, x, x_stride, nrhs, ctx->v, ctx->v_stride,
-                                     nullptr, 0, ctx->d_active, na, ctx->stream));
-            sp.done(zs_rhs_chunks(nrhs));
+            ZS_TRY(residual_slots(ctx, b, x, x_stride, nrhs, ctx->v, ctx->v_stride, nullptr, 0, ctx->d_active, na,
+                                  &sp));
         }
         // step 4: correction and update
         ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_active, na));
@@ -454,6 +515,7 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->dinv);
     cudaFree(c->inv32);
     cudaFree(c->v);
+    cudaFree(c->xs);
     cudaFree(c->partials);
     cudaFree(c->d_relcorr);
     cudaFreeHost(c->h_relcorr);
@@ -501,6 +563,7 @@ int zsolve_default_opts(zsolve_opts *opts) {
     opts->batch = 0;
     opts->force_fallback = 0;
     opts->profile = 0;
+    opts->resid = ZSOLVE_RESID_F64;
     return ZSOLVE_OK;
 }
 
@@ -513,7 +576,8 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     else zsolve_default_opts(&ctx->opts);
     if (ctx->opts.outer_block == 0) ctx->opts.outer_block = ZS_NB;
     if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
-        ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0) {
+        ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0 || ctx->opts.resid < 0 ||
+        ctx->opts.resid > ZSOLVE_RESID_DF) {
         delete ctx;
         return ZSOLVE_EINVAL;
     }
@@ -584,6 +648,10 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
         cudaMemset(ctx->z32, 0, (size_t)S * ctx->z32_stride * sizeof(float)) != cudaSuccess)
         return bail(ZSOLVE_ECUDA);
     *ctx->h_status = 0;
+    if (ctx->opts.resid == ZSOLVE_RESID_DF) {
+        if (cudaMalloc(&ctx->xs, (size_t)S * nrhs_max * n * sizeof(float4)) != cudaSuccess) return bail(ZSOLVE_ENOMEM);
+        if (resid_selftest(ctx) != ZSOLVE_OK) return bail(ZSOLVE_ECUDA);
+    }
     *out = ctx;
     return ZSOLVE_OK;
 }
@@ -684,9 +752,8 @@ int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int 
     ZS_TRY(check_nrhs(ctx, nrhs));
     if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_residual before zsolve_assemble");
     StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL);
-    ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, ctx->n, (const double2 *)b, (const double2 *)x, 0, nrhs,
-                             nullptr, 0, (double2 *)r, 0, ctx->d_all, 1, ctx->stream));
-    sp.done(zs_rhs_chunks(nrhs));
+    ZS_TRY(residual_slots(ctx, (const double2 *)b, (const double2 *)x, 0, nrhs, nullptr, 0, (double2 *)r, 0,
+                          ctx->d_all, 1, &sp));
     ZS_CU(cudaStreamSynchronize(ctx->stream));
     return ZSOLVE_OK;
 }
@@ -760,6 +827,12 @@ int zsolve_reset_profile(zsolve_ctx *ctx) {
         ctx->prof_launches[i] = 0;
         ctx->prof_ms[i] = 0.0;
     }
+    return ZSOLVE_OK;
+}
+
+int zsolve_get_resid_mode(zsolve_ctx *ctx, int *mode) {
+    if (!ctx || !mode) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    *mode = ctx->resid_mode;
     return ZSOLVE_OK;
 }
 

@@ -174,6 +174,44 @@ def test_residual_against_oracle(zs, torch, n, nrhs):
 FACTOR_TOL = {"FFMA": 2e-6, "TF32X3": 2e-5, "TF32": 3e-3}
 
 
+@pytest.mark.parametrize("n,nrhs", [(1, 1), (237, 1), (300, 3), (2157, 1), (513, 8)])
+def test_residual_double_float_against_oracle(zs, torch, n, nrhs):
+    wl = workload.make_small(n, seed=70 + n, nf=1, nrhs=nrhs)
+    X = workload.random_rhs(n, nrhs, seed=4)
+    s = zs.Solver(n, nrhs, resid=zs.ZSOLVE_RESID_DF)
+    try:
+        assert zs.zsolve_get_resid_mode(s.ctx) == zs.ZSOLVE_RESID_DF  # start-up self-test passed
+        zs.zsolve_assemble(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega[0],
+                           wl.zs[0].real, wl.zs[0].imag)
+        b, x = dev(torch, wl.B), dev(torch, X)
+        r = torch.empty_like(b)
+        zs.zsolve_residual(s.ctx, b, x, r)
+        Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0])
+        ref = oracle.residual(Z, X, wl.B)
+        # double-float: about 2^-46 per product, accumulated per lane
+        scale = np.abs(X) @ np.abs(Z).T + np.abs(wl.B)
+        assert np.all(np.abs(r.cpu().numpy() - ref) <= 1e-12 * scale + 1e-300)
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("n,nrhs,nf", [(130, 2, 3), (700, 1, 3), (301, 4, 2)])
+def test_sweep_parity_double_float_residual(zs, torch, n, nrhs, nf):
+    wl = workload.make_small(n, seed=80 + n, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
+    ref = oracle.solve_sweep(wl)
+    s = zs.Solver(n, nrhs, resid=zs.ZSOLVE_RESID_DF)
+    try:
+        x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+        infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
+                                dev(torch, wl.B), x)
+        X = x.cpu().numpy()
+        for f in range(nf):
+            assert infos[f].status == 0 and infos[f].fallback == 0, infos[f].as_dict()
+            assert np.all(rel_err(X[f], ref[f]) <= PARITY), (f, rel_err(X[f], ref[f]))
+    finally:
+        s.close()
+
+
 @pytest.mark.parametrize("gemm", ["FFMA", "TF32X3", "TF32"])
 @pytest.mark.parametrize("n", [1, 31, 128, 129, 300, 513, 1000])
 def test_factor_reconstructs_z32(zs, torch, n, gemm):
@@ -388,14 +426,14 @@ def test_argument_errors(zs, torch):
 # ---------------------------------------------------------------- full size (the benchmark launch)
 
 
-@pytest.mark.parametrize("gemm", ["FFMA", "TF32X3"])
-def test_config1_full_sweep_sampled(zs, torch, gemm):
+@pytest.mark.parametrize("gemm,resid", [("FFMA", "F64"), ("TF32X3", "F64"), ("TF32X3", "DF")])
+def test_config1_full_sweep_sampled(zs, torch, gemm, resid):
     """N=2157, all 21 frequencies in one batched sweep (as the benchmark runs
     it): oracle direct solves on a sample of frequencies, and for every
     frequency the oracle's double-precision backward error of the returned x."""
     wl = workload.make(1)
     nf = len(wl.omega)
-    s = zs.Solver(wl.n, 1, batch=nf, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm))
+    s = zs.Solver(wl.n, 1, batch=nf, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm), resid=getattr(zs, "ZSOLVE_RESID_" + resid))
     try:
         x = torch.empty((nf, 1, wl.n), dtype=torch.complex128, device="cuda")
         infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
