@@ -139,6 +139,46 @@ def cpu_baseline(cfg, budget_s=10.0, max_freqs=None):
                       f"substitution, {wl.B.shape[0]} RHS), {dt:.1f} s"}
 
 
+def sweep_variant(zs, torch, wl, args, resid):
+    """The same timed sweep with another residual arithmetic: points/s and the
+    residual stage's HBM rate (16 n^2 + 32 n nrhs bytes per evaluation over
+    its CUDA-event time)."""
+    n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
+    s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm), batch=args.batch or nf, profile=1,
+                  resid=getattr(zs, "ZSOLVE_RESID_" + resid))
+    try:
+        mode = "DF" if zs.zsolve_get_resid_mode(s.ctx) == zs.ZSOLVE_RESID_DF else "F64"
+        L = torch.from_numpy(wl.L).cuda()
+        P = torch.from_numpy(wl.Psi).cuda()
+        G = torch.from_numpy(wl.G).cuda()
+        b = torch.from_numpy(wl.B).cuda()
+        x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+        for _ in range(args.warmup):
+            zs.zsolve_sweep(s.ctx, L, P, G, wl.omega, wl.zs, b, x)
+        torch.cuda.synchronize()
+        zs.zsolve_reset_profile(s.ctx)
+        st = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        iters = 0
+        for _ in range(args.steps):
+            infos = zs.zsolve_sweep(s.ctx, L, P, G, wl.omega, wl.zs, b, x)
+            iters += sum(i.iters for i in infos)
+        e1.record(st)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        prof = zs.zsolve_get_profile(s.ctx).as_dict()
+        res_ms = prof["residual"]["ms"] / args.steps
+        res_bytes = iters / args.steps * (16.0 * n * n + 32.0 * n * nrhs)
+        peaks, _ = load_peaks()
+        gbs = res_bytes / (res_ms / 1e3) / 1e9
+        return {"mode_in_use": mode, "points_per_s": nf / (ms / 1e3), "resid_gbs": gbs,
+                "resid_hbm_frac": gbs / peaks["hbm_gbs"],
+                "arith": "float64 DFMA" if mode == "F64" else "double-float (2 x float32, ~46 bits)"}
+    finally:
+        s.close()
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -313,6 +353,11 @@ def run_ours(args):
         "clocks": clocks, "wall_s": wall,
     }
     solver.close()
+    other = "DF" if args.resid == "F64" else "F64"
+    line["resid_variants"] = {
+        args.resid: {"mode_in_use": resid_mode, "points_per_s": value / ws, "resid_gbs": res_gbs,
+                     "resid_hbm_frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None},
+        other: sweep_variant(zs, torch, wl, args, other)}
     if args.cpu_baseline and args.gpus <= 1 and ws == 1:
         line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)

@@ -75,6 +75,9 @@ __global__ void k_split_x(const double2 *__restrict__ x, int64_t x_stride, int64
     }
 }
 
+// Two rows per warp: every split-x load serves both rows.
+constexpr int kRowsPerWarp = 2;
+
 template <int R>
 __global__ void __launch_bounds__(kResThreads)
 k_residual_df(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const double2 *__restrict__ b,
@@ -82,97 +85,111 @@ k_residual_df(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, co
               double2 *__restrict__ out128, int64_t out128_stride, const int *__restrict__ slots) {
     const int slot = slots[blockIdx.y];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t row = (int64_t)blockIdx.x * (kResThreads / 32) + warp;
-    if (row >= n) return;
-    const double2 *zr = z64 + (int64_t)slot * z64_stride + row * n;
+    const int64_t row0 = ((int64_t)blockIdx.x * (kResThreads / 32) + warp) * kRowsPerWarp;
+    if (row0 >= n) return;  // whole warp
+    const int nrow = (int)zs::min64(kRowsPerWarp, n - row0);
+    const double2 *zr[kRowsPerWarp];
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; q++)
+        zr[q] = z64 + (int64_t)slot * z64_stride + (row0 + (q < nrow ? q : 0)) * n;
     const float4 *xsl = xs + (int64_t)slot * xs_stride;
-    constexpr int NA = R >= 2 ? 1 : 2;  // independent accumulator sets
-    float Sr[NA][R], Cr[NA][R], Si[NA][R], Ci[NA][R];
+    float Sr[kRowsPerWarp][R], Cr[kRowsPerWarp][R], Si[kRowsPerWarp][R], Ci[kRowsPerWarp][R];
 #pragma unroll
-    for (int a = 0; a < NA; a++)
+    for (int q = 0; q < kRowsPerWarp; q++)
 #pragma unroll
-        for (int r = 0; r < R; r++) Sr[a][r] = Cr[a][r] = Si[a][r] = Ci[a][r] = 0.f;
+        for (int r = 0; r < R; r++) Sr[q][r] = Cr[q][r] = Si[q][r] = Ci[q][r] = 0.f;
     int64_t base = 0;
     for (; base + 128 <= n; base += 128) {  // bound uniform across the warp
         const int64_t j = base + lane;
-        double2 z[4];
+        double2 z[kRowsPerWarp][4];
 #pragma unroll
-        for (int u = 0; u < 4; u++) z[u] = __ldcs(zr + j + 32 * u);
+        for (int q = 0; q < kRowsPerWarp; q++)
+#pragma unroll
+            for (int u = 0; u < 4; u++) z[q][u] = __ldcs(zr[q] + j + 32 * u);
         bool re0 = true;
 #pragma unroll
-        for (int u = 0; u < 4; u++) re0 = re0 && ((__double_as_longlong(z[u].x) << 1) == 0);
+        for (int q = 0; q < kRowsPerWarp; q++)
+#pragma unroll
+            for (int u = 0; u < 4; u++) re0 = re0 && ((__double_as_longlong(z[q][u].x) << 1) == 0);
         const bool skip = __all_sync(0xffffffffu, re0);
 #pragma unroll
         for (int u = 0; u < 4; u++) {
-            float yh, yl, xh = 0.f, xl = 0.f;
-            split_f64(z[u].y, yh, yl);
-            if (!skip) split_f64(z[u].x, xh, xl);
+            float4 xv[R];
 #pragma unroll
-            for (int r = 0; r < R; r++) {
-                const float4 xv = __ldg(xsl + r * n + j + 32 * u);
-                const int a = u % NA;
-                // re += Re z Re x - Im z Im x ; im += Re z Im x + Im z Re x
-                df_mac(Sr[a][r], Cr[a][r], -yh, -yl, xv.z, xv.w);
-                df_mac(Si[a][r], Ci[a][r], yh, yl, xv.x, xv.y);
-                if (!skip) {
-                    df_mac(Sr[a][r], Cr[a][r], xh, xl, xv.x, xv.y);
-                    df_mac(Si[a][r], Ci[a][r], xh, xl, xv.z, xv.w);
+            for (int r = 0; r < R; r++) xv[r] = __ldg(xsl + r * n + j + 32 * u);
+#pragma unroll
+            for (int q = 0; q < kRowsPerWarp; q++) {
+                float yh, yl, xh = 0.f, xl = 0.f;
+                split_f64(z[q][u].y, yh, yl);
+                if (!skip) split_f64(z[q][u].x, xh, xl);
+#pragma unroll
+                for (int r = 0; r < R; r++) {
+                    // re += Re z Re x - Im z Im x ; im += Re z Im x + Im z Re x
+                    df_mac(Sr[q][r], Cr[q][r], -yh, -yl, xv[r].z, xv[r].w);
+                    df_mac(Si[q][r], Ci[q][r], yh, yl, xv[r].x, xv[r].y);
+                    if (!skip) {
+                        df_mac(Sr[q][r], Cr[q][r], xh, xl, xv[r].x, xv[r].y);
+                        df_mac(Si[q][r], Ci[q][r], xh, xl, xv[r].z, xv[r].w);
+                    }
                 }
             }
         }
     }
     for (int64_t j = base + lane; j < n; j += 32) {
-        const double2 z = __ldcs(zr + j);
-        float yh, yl, xh, xl;
-        split_f64(z.y, yh, yl);
-        split_f64(z.x, xh, xl);
+#pragma unroll
+        for (int q = 0; q < kRowsPerWarp; q++) {
+            const double2 z = __ldcs(zr[q] + j);
+            float yh, yl, xh, xl;
+            split_f64(z.y, yh, yl);
+            split_f64(z.x, xh, xl);
+#pragma unroll
+            for (int r = 0; r < R; r++) {
+                const float4 xv = __ldg(xsl + r * n + j);
+                df_mac(Sr[q][r], Cr[q][r], -yh, -yl, xv.z, xv.w);
+                df_mac(Si[q][r], Ci[q][r], yh, yl, xv.x, xv.y);
+                df_mac(Sr[q][r], Cr[q][r], xh, xl, xv.x, xv.y);
+                df_mac(Si[q][r], Ci[q][r], xh, xl, xv.z, xv.w);
+            }
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kRowsPerWarp; q++) {
+        double ar[R], ai[R];
 #pragma unroll
         for (int r = 0; r < R; r++) {
-            const float4 xv = __ldg(xsl + r * n + j);
-            df_mac(Sr[0][r], Cr[0][r], -yh, -yl, xv.z, xv.w);
-            df_mac(Si[0][r], Ci[0][r], yh, yl, xv.x, xv.y);
-            df_mac(Sr[0][r], Cr[0][r], xh, xl, xv.x, xv.y);
-            df_mac(Si[0][r], Ci[0][r], xh, xl, xv.z, xv.w);
-        }
-    }
-    double ar[R], ai[R];
+            ar[r] = (double)Sr[q][r] + (double)Cr[q][r];
+            ai[r] = (double)Si[q][r] + (double)Ci[q][r];
 #pragma unroll
-    for (int r = 0; r < R; r++) {
-        ar[r] = 0.0;
-        ai[r] = 0.0;
-#pragma unroll
-        for (int a = 0; a < NA; a++) {
-            ar[r] += (double)Sr[a][r] + (double)Cr[a][r];
-            ai[r] += (double)Si[a][r] + (double)Ci[a][r];
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            ar[r] += __shfl_xor_sync(0xffffffffu, ar[r], o);
-            ai[r] += __shfl_xor_sync(0xffffffffu, ai[r], o);
-        }
-    }
-    if (lane < R) {
-        double vr = 0.0, vi = 0.0;
-#pragma unroll
-        for (int r = 0; r < R; r++)
-            if (r == lane) {
-                vr = ar[r];
-                vi = ai[r];
+            for (int o = 16; o > 0; o >>= 1) {
+                ar[r] += __shfl_xor_sync(0xffffffffu, ar[r], o);
+                ai[r] += __shfl_xor_sync(0xffffffffu, ai[r], o);
             }
-        const double2 bv = b[(int64_t)lane * n + row];
-        const double rr = bv.x - vr, ri = bv.y - vi;
-        if (out64)
-            out64[(int64_t)slot * out64_stride + (int64_t)lane * n + row] =
-                make_float2(__double2float_rn(rr), __double2float_rn(ri));
-        else
-            out128[(int64_t)slot * out128_stride + (int64_t)lane * n + row] = make_double2(rr, ri);
+        }
+        const int64_t row = row0 + q;
+        if (lane < R && q < nrow) {
+            double vr = 0.0, vi = 0.0;
+#pragma unroll
+            for (int r = 0; r < R; r++)
+                if (r == lane) {
+                    vr = ar[r];
+                    vi = ai[r];
+                }
+            const double2 bv = b[(int64_t)lane * n + row];
+            const double rr = bv.x - vr, ri = bv.y - vi;
+            if (out64)
+                out64[(int64_t)slot * out64_stride + (int64_t)lane * n + row] =
+                    make_float2(__double2float_rn(rr), __double2float_rn(ri));
+            else
+                out128[(int64_t)slot * out128_stride + (int64_t)lane * n + row] = make_double2(rr, ri);
+        }
     }
 }
 
 template <int R>
 void launch_df(const double2 *z64, int64_t z64_stride, int64_t n, const double2 *b, const float4 *xs, int64_t xs_stride,
                float2 *o64, int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot, cudaStream_t st) {
-    dim3 grid((unsigned)((n + 7) / 8), nslot);
+    const int64_t rows_per_cta = (kResThreads / 32) * kRowsPerWarp;
+    dim3 grid((unsigned)((n + rows_per_cta - 1) / rows_per_cta), nslot);
     k_residual_df<R><<<grid, kResThreads, 0, st>>>(z64, z64_stride, n, b, xs, xs_stride, o64, o64s, o128, o128s,
                                                    slots);
 }
