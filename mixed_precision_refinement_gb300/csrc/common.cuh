@@ -133,6 +133,29 @@ cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t 
                                  int64_t J, const float *pack, int64_t pack_stride, const int *slots,
                                  int nslot, cudaStream_t st);
 
+// Operand packs of the block triangular solves on the tensor cores, at outer
+// column J: A planes rows i >= J+NB = [Re A21(i,:) | Im A21(i,:)], Br planes
+// rows j >= J+NB = [Re A12(:,j) | Im A12(:,j)] (mode 1: tf32 hi; 2: hi + lo).
+cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                                int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots, int nslot,
+                                cudaStream_t st);
+
+// tcgen05 kernels (schur_tc.cu).  Tensor maps are 128-byte CUtensorMap
+// objects in host memory, passed by value to the kernels.
+cudaError_t zs_tc_pack_map(const float *pack, int64_t n, int nslots, int64_t pack_stride, int box_rows,
+                           void *map_out);
+cudaError_t zs_tc_winv_map(const float *winv, int nslots, void *map_out);
+cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane, int nslots, int64_t z32_stride,
+                          void *map_out);
+// A22 -= L21 U12 for every listed slot (split: 3xTF32)
+cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
+                               int nslot, unsigned *status, int num_sms, cudaStream_t st);
+// L21 = A21 U11^-1 and U12 = L11^-1 A12 from the packs of zs_launch_pack_trsm
+// and zs_launch_diag_inv; writes L21, U12 into z32 and their operand packs
+cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
+                              int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
+                              cudaStream_t st);
+
 // Pack layout (floats), per slot: six planes of n rows x 2*NB:
 //   A_hi, A_lo, Br_hi, Br_lo, Bi_hi, Bi_lo
 // A row i   = [Re L21(i,:) | Im L21(i,:)]
@@ -151,10 +174,19 @@ cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int6
                            unsigned *status, int num_sms, cudaStream_t st);
 
 // Inverses of the 128x128 diagonal blocks of L (unit lower) and U (upper):
-// per slot [block][L, U][re, im][128][128] floats.
+// per slot [block][L, U][re, im][128][128] floats, for blocks b0 .. b0+nblk-1
+// (nblk <= 0: every block from b0 on).  winv != NULL additionally writes the
+// inverses as tensor-core operand packs (mode 1: tf32 hi; 2: hi + lo), per
+// slot ZS_WINV_STRIDE floats = 8 planes of 128 rows x 256:
+//   planes 0-3 W = U^-1: Br(j) = [Re W(:,j) | -Im W(:,j)], Bi(j) = [Im W(:,j) | Re W(:,j)]  (hi, lo each)
+//   planes 4-7 V = L^-1: Br(k) = [Re V(k,:) | -Im V(k,:)], Bi(k) = [Im V(k,:) | Re V(k,:)]
+// in the order Br hi, Br lo, Bi hi, Bi lo; only one block (nblk = 1) may write packs.
+#define ZS_WINV_PLANE (ZS_NB * ZS_PACK_K)
+#define ZS_WINV_STRIDE (8 * ZS_WINV_PLANE)
 cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                const float *inv32, int64_t inv32_stride, float *dinv, int64_t dinv_stride,
-                               const int *slots, int nslot, cudaStream_t st);
+                               int b0, int nblk, float *winv, int mode, const int *slots, int nslot,
+                               cudaStream_t st);
 inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }
 // Triangular solves with 128-row blocks and the inverse diagonal blocks; nrhs 1, 2 or 4 per launch.
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,

@@ -590,6 +590,48 @@ k_schur_simt(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
     }
 }
 
+// ---------------------------------------------------------------- packs for the tensor-core solves
+
+// Operand packs of the block triangular solves (blockIdx.y = 0: rows of A21
+// into the A planes; 1: columns of A12, transposed through shared memory,
+// into the Br planes), 32 rows or columns per CTA.
+constexpr int kPackThreads = 256;
+
+__global__ void __launch_bounds__(kPackThreads)
+k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
+            float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
+    __shared__ float s[ZS_PACK_K][33];
+    const int slot = slots[blockIdx.z];
+    const float *re = z32 + (int64_t)slot * z32_stride;
+    const float *im = re + plane;
+    float *pk = pack + (int64_t)slot * pack_stride;
+    const int64_t pp = zs_pack_plane(n);
+    const int64_t r0 = J + NB + 32 * (int64_t)blockIdx.x;
+    const int tid = threadIdx.x;
+    if (blockIdx.y == 0) {
+        for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
+            const int r = idx >> 8, k = idx & (ZS_PACK_K - 1);
+            const int64_t i = r0 + r;
+            if (i >= n) break;  // later idx only move to later rows
+            const float v = (k < NB ? re : im)[i * ld + J + (k & (NB - 1))];
+            pack_put(pk, pk + pp, i * ZS_PACK_K + k, v, mode);
+        }
+    } else {
+        for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
+            const int k = idx >> 5, c = idx & 31;
+            const int64_t j = r0 + c;
+            s[k][c] = j < n ? (k < NB ? re : im)[(J + (k & (NB - 1))) * ld + j] : 0.f;
+        }
+        __syncthreads();
+        for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
+            const int c = idx >> 8, k = idx & (ZS_PACK_K - 1);
+            const int64_t j = r0 + c;
+            if (j >= n) break;
+            pack_put(pk + 2 * pp, pk + 3 * pp, j * ZS_PACK_K + k, s[k][c], mode);
+        }
+    }
+}
+
 template <typename K>
 cudaError_t set_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
@@ -654,5 +696,16 @@ cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t 
     const unsigned t = (unsigned)((m2 + kST - 1) / kST);
     dim3 grid(t, t, nslot);
     k_schur_simt<<<grid, 256, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, slots);
+    return cudaGetLastError();
+}
+
+cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
+                                int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots, int nslot,
+                                cudaStream_t st) {
+    const int64_t m2 = n - J - NB;
+    if (m2 <= 0 || nslot <= 0) return cudaSuccess;
+    if (mode != 1 && mode != 2) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)((m2 + 31) / 32), 2, (unsigned)nslot);
+    k_pack_trsm<<<grid, kPackThreads, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode, slots);
     return cudaGetLastError();
 }

@@ -20,6 +20,20 @@
 //              Cores while surpassing the FP32 theoretical peak
 //              performance", IJHPCA 2022).
 //
+// The same kernel runs the two block triangular solves of each step as
+// products with the explicit inverses of the diagonal block (kind TRSM):
+//   L21   = A21 U11^-1:   A rows i = [Re A21(i,:) | Im A21(i,:)] (A planes),
+//                         B = W = U11^-1 as Br(j) = [Re W(:,j) | -Im W(:,j)],
+//                         Bi(j) = [Im W(:,j) | Re W(:,j)];
+//   U12^T = A12^T L11^-T: A rows j = [Re A12(:,j) | Im A12(:,j)] (Br planes),
+//                         B = V = L11^-1 as Br(k) = [Re V(k,:) | -Im V(k,:)],
+//                         Bi(k) = [Im V(k,:) | Re V(k,:)].
+// Its epilogue stores the result twice with TMA tile stores: into the float32
+// factor (U12 transposed on the way through shared memory) and, rounded to
+// tf32 hi (+ lo), into the operand packs the trailing update reads next.  A
+// tile's epilogue overwrites the very pack rows its own MMAs consumed, which
+// is safe: the accumulator is complete only after every load of the tile.
+//
 // Warp roles (192 threads, persistent over the tiles of every frequency in
 // the batch): warp 0 issues TMA loads (128B-swizzled K-major tiles of 32
 // fp32) into a ring of shared-memory stages; warp 1 owns TMEM (512 columns:
@@ -50,6 +64,9 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t kWaitLimit = 1u << 24;
 
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
+// inverse packs: W = U11^-1 in planes 0-3, V = L11^-1 in planes 4-7 (Br hi, Br lo, Bi hi, Bi lo)
+enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_BI_HI = 2, WP_BI_LO = 3, WP_V = 4 };
+enum { KIND_SCHUR = 0, KIND_TRSM = 1 };
 
 constexpr int EPI_BOX = 32 * 32 * 4;  // one 32-row x 32-column fp32 box (4 KB)
 constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;  // 4 epilogue warps x 2 staging buffers
@@ -124,6 +141,42 @@ __device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap *map, uint32
         : "memory");
 }
 
+// Store a staged 32x32 box (TMA tile store; rows/columns beyond the tensor are dropped)
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, uint32_t src, int c0, int c1, int c2, int c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.tile.bulk_group"
+        " [%0, {%1, %2, %3, %4}], [%5];" ::"l"((uint64_t)map),
+        "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
+// Row `lane` of a 32x32 fp32 box in 128B-swizzled shared memory: 16-byte unit
+// j of row r sits at unit (j ^ (r & 7)).  sgn = -1 stores the negated values.
+__device__ __forceinline__ void stage_row(uint32_t sb, int lane, const float (&v)[32], float sgn) {
+#pragma unroll
+    for (int j = 0; j < 8; j++) {
+        const uint32_t a = sb + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16);
+        asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(sgn * v[4 * j]),
+                     "f"(sgn * v[4 * j + 1]), "f"(sgn * v[4 * j + 2]), "f"(sgn * v[4 * j + 3])
+                     : "memory");
+    }
+}
+
+// Column `lane` of the same box layout (element (t, lane) = v[t]): the transpose.
+__device__ __forceinline__ void stage_col(uint32_t sb, int lane, const float (&v)[32]) {
+#pragma unroll
+    for (int t = 0; t < 32; t++) {
+        const uint32_t a = sb + (uint32_t)t * 128u + (uint32_t)((((lane >> 2) ^ (t & 7)) * 16) + (lane & 3) * 4);
+        asm volatile("st.shared.f32 [%0], %1;" ::"r"(a), "f"(v[t]) : "memory");
+    }
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 // wait until at most N committed groups are still reading their shared source
@@ -191,10 +244,38 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     for (int i = 0; i < 32; i++) v[i] = __uint_as_float(r[i]);
 }
 
-template <int SPLIT>
+// Tile t of the launch: frequency slot, output row tile, column tile
+// (KIND_SCHUR) or solve (KIND_TRSM: 0 = L21, 1 = U12^T, interleaved).
+struct Tile {
+    int slot, ra, u, rb;
+};
+
+template <int KIND>
+__device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const int *slots) {
+    Tile x;
+    const int per_slot = KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles;
+    const int si = t / per_slot, rem = t - si * per_slot;
+    x.slot = slots[si];
+    if (KIND == KIND_SCHUR) {
+        const int tm = rem / tiles, tn = rem - tm * tiles;
+        x.ra = (int)(base + (int64_t)tm * TM);
+        x.rb = (int)(base + (int64_t)tn * TN);
+        x.u = 0;
+    } else {
+        x.u = rem & 1;
+        x.ra = (int)(base + (int64_t)(rem >> 1) * TM);
+        x.rb = 0;
+    }
+    return x;
+}
+
+// tmap: operand packs (boxes 32 x 128); wmap: inverse packs (KIND_TRSM);
+// cmap: float32 matrices (boxes 32 x 32); pmap: operand packs (boxes 32 x 32, KIND_TRSM stores).
+template <int SPLIT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
-k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap cmap, int64_t n,
-           int64_t J, const int *__restrict__ slots, int nslot, unsigned *__restrict__ status) {
+k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap wmap,
+           const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap pmap, int64_t n, int64_t J,
+           const int *__restrict__ slots, int nslot, unsigned *__restrict__ status) {
     using C = Cfg<SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[C::STAGES], bar_empty[C::STAGES], bar_accf[2], bar_acce[2], bar_drain;
@@ -206,7 +287,7 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
     const int64_t base = J + NB;
     const int64_t m2 = n - base;
     const int tiles = (int)((m2 + TM - 1) / TM);
-    const int per_slot = tiles * tiles;
+    const int per_slot = KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles;
     const int total = per_slot * nslot;
 
     if (threadIdx.x == 0) {
@@ -237,13 +318,17 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
+            if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&wmap) : "memory");
             uint32_t g = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const int si = t / per_slot, rem = t - si * per_slot;
-                const int tm = rem / tiles, tn = rem - tm * tiles;
-                const int slot = slots[si];
-                const int ra = (int)(base + (int64_t)tm * TM), rb = (int)(base + (int64_t)tn * TN);
+                const Tile x = tile_of<KIND>(t, tiles, base, slots);
+                // A rows: L21 / A21 (A planes) or A12^T (Br planes); B: the pack's
+                // own Br/Bi rows, or W / V from the inverse packs
+                const int pa = (KIND == KIND_TRSM && x.u) ? PL_BR_HI : PL_A_HI;
+                const CUtensorMap *bm = KIND == KIND_SCHUR ? &tmap : &wmap;
+                const int pbr = KIND == KIND_SCHUR ? PL_BR_HI : (x.u ? WP_V : 0) + WP_BR_HI;
+                const int pbi = KIND == KIND_SCHUR ? PL_BI_HI : (x.u ? WP_V : 0) + WP_BI_HI;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
                     if (!mbar_wait(smem_u32(&bar_empty[st]), ph ^ 1u, &s_abort, status)) {
@@ -254,14 +339,14 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     mbar_expect_tx(fb, C::STAGE_BYTES);
                     const uint32_t sa = base_addr + st * C::STAGE_BYTES;
                     const int k0 = kc * KC;
-                    tma_load_4d(sa, &tmap, k0, ra, PL_A_HI, slot, fb);
-                    tma_load_4d(sa + A_BYTES, &tmap, k0, rb, PL_BR_HI, slot, fb);
-                    tma_load_4d(sa + A_BYTES + B_BYTES / 2, &tmap, k0, rb, PL_BI_HI, slot, fb);
-                    if (SPLIT) {
+                    tma_load_4d(sa, &tmap, k0, x.ra, pa, x.slot, fb);
+                    tma_load_4d(sa + A_BYTES, bm, k0, x.rb, pbr, x.slot, fb);
+                    tma_load_4d(sa + A_BYTES + B_BYTES / 2, bm, k0, x.rb, pbi, x.slot, fb);
+                    if (SPLIT) {  // lo planes follow their hi planes
                         const uint32_t sl = sa + A_BYTES + B_BYTES;
-                        tma_load_4d(sl, &tmap, k0, ra, PL_A_LO, slot, fb);
-                        tma_load_4d(sl + A_BYTES, &tmap, k0, rb, PL_BR_LO, slot, fb);
-                        tma_load_4d(sl + A_BYTES + B_BYTES / 2, &tmap, k0, rb, PL_BI_LO, slot, fb);
+                        tma_load_4d(sl, &tmap, k0, x.ra, pa + 1, x.slot, fb);
+                        tma_load_4d(sl + A_BYTES, bm, k0, x.rb, pbr + 1, x.slot, fb);
+                        tma_load_4d(sl + A_BYTES + B_BYTES / 2, bm, k0, x.rb, pbi + 1, x.slot, fb);
                     }
                 }
             }
@@ -327,19 +412,33 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
         const uint32_t stage0 = base_addr + C::STAGES * C::STAGE_BYTES + (uint32_t)(warp - 2) * 2u * EPI_BOX;
         uint32_t it = 0, nbox = 0;
-        if (lane == 0) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&cmap) : "memory");
+        // next staging buffer of this warp's ring of two: its previous store
+        // must have finished reading it
+        auto next_box = [&]() -> uint32_t {
+            const uint32_t sb = stage0 + (nbox & 1u) * EPI_BOX;
+            nbox++;
+            if (lane == 0) bulk_wait_read<1>();
+            __syncwarp();
+            return sb;
+        };
+        // staged box complete: make it visible to the async proxy, then one lane stores it
+        auto publish = [&]() {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+        };
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&cmap) : "memory");
+            if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&pmap) : "memory");
+        }
         for (int t = blockIdx.x; t < total; t += gridDim.x, it++) {
             const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
             const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status);
             if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
-            const int si = t / per_slot, rem = t - si * per_slot;
-            const int tm = rem / tiles, tn = rem - tm * tiles;
-            const int slot = slots[si];
-            const int row0 = (int)(base + (int64_t)tm * TM) + quad * 32;
-            const int col0 = (int)(base + (int64_t)tn * TN);
+            const Tile x = tile_of<KIND>(t, tiles, base, slots);
+            const int row0 = x.ra + quad * 32;  // this warp's 32 output rows
 #pragma unroll 1
-            for (int c = 0; c < 8; c++, nbox++) {
+            for (int c = 0; c < 8; c++) {
                 float v[32];
                 tmem_ld32(tmem + buf * 256u + (uint32_t)(c * 32) + ((uint32_t)(quad * 32) << 16), v);
                 if (c == 7) {  // accumulator fully read: hand it back to the MMA warp
@@ -347,22 +446,60 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     __syncwarp();
                     if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
                 }
-                const uint32_t sb = stage0 + (nbox & 1u) * EPI_BOX;
-                if (lane == 0) bulk_wait_read<1>();  // this buffer's previous store has read its source
-                __syncwarp();
-                // row `lane` of the box, 128B-swizzled: 16-byte unit j at (j ^ (row & 7))
-#pragma unroll
-                for (int j = 0; j < 8; j++) {
-                    const uint32_t a = sb + (uint32_t)lane * 128u + (uint32_t)((j ^ (lane & 7)) * 16);
-                    asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(-v[4 * j]),
-                                 "f"(-v[4 * j + 1]), "f"(-v[4 * j + 2]), "f"(-v[4 * j + 3])
-                                 : "memory");
+                const int part = c >> 2, c32 = (c & 3) * 32;  // part 0 = real, 1 = imaginary
+                if (KIND == KIND_SCHUR) {
+                    const uint32_t sb = next_box();
+                    stage_row(sb, lane, v, -1.f);
+                    publish();
+                    if (lane == 0) {
+                        tma_reduce_add_4d(&cmap, sb, x.rb + c32, row0, part, x.slot);
+                        bulk_commit();
+                    }
+                    continue;
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
+                // ---- KIND_TRSM: the factor itself, then the trailing update's operand packs
+                uint32_t sb = next_box();
+                if (x.u == 0) stage_row(sb, lane, v, 1.f);  // L21(i, J + c32 + t)
+                else stage_col(sb, lane, v);                 // U12(J + c32 + t, j)
+                publish();
                 if (lane == 0) {
-                    tma_reduce_add_4d(&cmap, sb, col0 + (c & 3) * 32, row0, c >> 2, slot);
+                    if (x.u == 0) tma_store_4d(&cmap, sb, (int)J + c32, row0, part, x.slot);
+                    else tma_store_4d(&cmap, sb, row0, (int)J + c32, part, x.slot);
                     bulk_commit();
+                }
+                float h[32];
+#pragma unroll
+                for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q]);
+#pragma unroll 1
+                for (int lo = 0; lo <= SPLIT; lo++) {
+                    if (lo) {
+#pragma unroll
+                        for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q] - h[q]);
+                    }
+                    if (x.u == 0) {  // A row i = [Re L21 | Im L21]: K column = accumulator column
+                        sb = next_box();
+                        stage_row(sb, lane, h, 1.f);
+                        publish();
+                        if (lane == 0) {
+                            tma_store_4d(&pmap, sb, c * 32, row0, PL_A_HI + lo, x.slot);
+                            bulk_commit();
+                        }
+                    } else {  // Br row j = [Re U12^T | -Im U12^T], Bi row j = [Im U12^T | Re U12^T]
+                        sb = next_box();
+                        stage_row(sb, lane, h, part ? -1.f : 1.f);
+                        publish();
+                        if (lane == 0) {
+                            tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_BR_HI + lo, x.slot);
+                            bulk_commit();
+                        }
+                        sb = next_box();
+                        stage_row(sb, lane, h, 1.f);
+                        publish();
+                        if (lane == 0) {
+                            tma_store_4d(&pmap, sb, (1 - part) * NB + c32, row0, PL_BI_HI + lo, x.slot);
+                            bulk_commit();
+                        }
+                    }
                 }
             }
         }
@@ -376,7 +513,6 @@ k_schur_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
     }
 }
-
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -390,62 +526,85 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-template <int SPLIT>
-cudaError_t launch_split(const CUtensorMap &map, const CUtensorMap &cmap, int64_t n, int64_t J, const int *slots,
-                         int nslot, unsigned *status, int num_sms, cudaStream_t st) {
+template <int SPLIT, int KIND>
+cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const CUtensorMap &cmap,
+                        const CUtensorMap &pmap, int64_t n, int64_t J, const int *slots, int nslot, unsigned *status,
+                        int num_sms, cudaStream_t st) {
     using C = Cfg<SPLIT>;
     static bool init = false;
     if (!init) {
-        cudaError_t e = cudaFuncSetAttribute(k_schur_tc<SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        cudaError_t e =
+            cudaFuncSetAttribute(k_cgemm_tc<SPLIT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (e != cudaSuccess) return e;
         init = true;
     }
     const int64_t m2 = n - J - NB;
+    if (m2 <= 0 || nslot <= 0) return cudaSuccess;
     const int64_t tiles = (m2 + TM - 1) / TM;
-    int64_t total = tiles * tiles * nslot;
-    int grid = (int)(total < num_sms ? total : num_sms);
-    k_schur_tc<SPLIT><<<grid, kThreads, C::SMEM, st>>>(map, cmap, n, J, slots, nslot, status);
+    const int64_t total = (KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles) * nslot;
+    const int grid = (int)(total < num_sms ? total : num_sms);
+    k_cgemm_tc<SPLIT, KIND><<<grid, kThreads, C::SMEM, st>>>(tmap, wmap, cmap, pmap, n, J, slots, nslot, status);
     return cudaGetLastError();
+}
+
+cudaError_t encode_f32_4d(void *map_out, const float *base, const cuuint64_t (&dims)[4], const cuuint64_t (&strides)[3],
+                          cuuint32_t box0, cuuint32_t box1) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap *map = reinterpret_cast<CUtensorMap *>(map_out);
+    cuuint32_t box[4] = {box0, box1, 1, 1};
+    cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (void *)base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-// Tensor map over the operand packs: dims (K = 256, rows = n, plane = 6, slot = S).
-cudaError_t zs_schur_tc_map(const float *pack, int64_t n, int nslots, int64_t pack_stride, void *map_out) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
-    if (!enc) return cudaErrorNotSupported;
-    CUtensorMap *map = reinterpret_cast<CUtensorMap *>(map_out);
-    cuuint64_t dims[4] = {(cuuint64_t)KTOT, (cuuint64_t)n, 6, (cuuint64_t)nslots};
-    cuuint64_t strides[3] = {(cuuint64_t)KTOT * 4, (cuuint64_t)zs_pack_plane(n) * 4, (cuuint64_t)pack_stride * 4};
-    cuuint32_t box[4] = {KC, TM, 1, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (void *)pack, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+// Tensor map over the operand packs: dims (K = 256, rows = n, plane = 6,
+// slot = S); boxes of 32 K x box_rows rows (128 for operand loads, 32 for
+// the triangular solves' stores).
+cudaError_t zs_tc_pack_map(const float *pack, int64_t n, int nslots, int64_t pack_stride, int box_rows,
+                           void *map_out) {
+    const cuuint64_t dims[4] = {(cuuint64_t)KTOT, (cuuint64_t)n, 6, (cuuint64_t)nslots};
+    const cuuint64_t strides[3] = {(cuuint64_t)KTOT * 4, (cuuint64_t)zs_pack_plane(n) * 4,
+                                   (cuuint64_t)pack_stride * 4};
+    return encode_f32_4d(map_out, pack, dims, strides, KC, (cuuint32_t)box_rows);
 }
 
-// Tensor map over the float32 trailing matrix: dims (column = n, row = n,
-// plane = 2 (re, im), slot = S), boxes of 32 x 32 for the reduce-add epilogue.
-cudaError_t zs_schur_tc_cmap(const float *z32, int64_t n, int64_t ld, int64_t plane, int nslots, int64_t z32_stride,
-                             void *map_out) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
-    if (!enc) return cudaErrorNotSupported;
-    CUtensorMap *map = reinterpret_cast<CUtensorMap *>(map_out);
-    cuuint64_t dims[4] = {(cuuint64_t)n, (cuuint64_t)n, 2, (cuuint64_t)nslots};
-    cuuint64_t strides[3] = {(cuuint64_t)ld * 4, (cuuint64_t)plane * 4, (cuuint64_t)z32_stride * 4};
-    cuuint32_t box[4] = {32, 32, 1, 1};
-    cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, (void *)z32, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+// Tensor map over the inverse packs: dims (K = 256, rows = 128, plane = 8, slot = S), boxes of 32 x 128.
+cudaError_t zs_tc_winv_map(const float *winv, int nslots, void *map_out) {
+    const cuuint64_t dims[4] = {(cuuint64_t)KTOT, (cuuint64_t)NB, 8, (cuuint64_t)nslots};
+    const cuuint64_t strides[3] = {(cuuint64_t)KTOT * 4, (cuuint64_t)ZS_WINV_PLANE * 4,
+                                   (cuuint64_t)ZS_WINV_STRIDE * 4};
+    return encode_f32_4d(map_out, winv, dims, strides, KC, NB);
+}
+
+// Tensor map over the float32 matrices: dims (column = n, row = n,
+// plane = 2 (re, im), slot = S), boxes of 32 x 32 for the epilogue stores.
+cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane, int nslots, int64_t z32_stride,
+                          void *map_out) {
+    const cuuint64_t dims[4] = {(cuuint64_t)n, (cuuint64_t)n, 2, (cuuint64_t)nslots};
+    const cuuint64_t strides[3] = {(cuuint64_t)ld * 4, (cuuint64_t)plane * 4, (cuuint64_t)z32_stride * 4};
+    return encode_f32_4d(map_out, z32, dims, strides, 32, 32);
 }
 
 cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
                                int nslot, unsigned *status, int num_sms, cudaStream_t st) {
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
     const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
-    if (split) return launch_split<1>(m, c, n, J, slots, nslot, status, num_sms, st);
-    return launch_split<0>(m, c, n, J, slots, nslot, status, num_sms, st);
+    if (split) return launch_kind<1, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, status, num_sms, st);
+    return launch_kind<0, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, status, num_sms, st);
+}
+
+cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
+                              int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
+                              cudaStream_t st) {
+    const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
+    const CUtensorMap &w = *reinterpret_cast<const CUtensorMap *>(wmap);
+    const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
+    const CUtensorMap &p = *reinterpret_cast<const CUtensorMap *>(pmap);
+    if (split) return launch_kind<1, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, status, num_sms, st);
+    return launch_kind<0, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, status, num_sms, st);
 }

@@ -55,15 +55,21 @@ __device__ __forceinline__ void blk_mac(const Blk &A, const Blk &B, cf (&acc)[2]
 //   L: X_ii = D_i,  X_ik = -D_i sum_{m=k}^{i-1} L_im X_mk   (i > k, i ascending)
 //   U: X_ii = D_i,  X_ik = -D_i sum_{m=i+1}^{k} U_im X_mk   (i < k, i descending)
 // Padding rows beyond n are the identity.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r);
+}
+
 __global__ void __launch_bounds__(kInvThreads, 1)
 k_diag_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
            const float *__restrict__ inv32, int64_t inv32_stride, float *__restrict__ dinv, int64_t dinv_stride,
-           const int *__restrict__ slots) {
+           int b0, float *__restrict__ winv, int mode, const int *__restrict__ slots) {
     extern __shared__ float sm[];
     Blk *F = reinterpret_cast<Blk *>(sm);  // [6]: off-diagonal factor sub-blocks of the triangle
     Blk *X = F + 6;                        // [10]: result sub-blocks, diagonal included
     Blk *T = X + 10;                       // scratch
-    const int b = blockIdx.x, upper = blockIdx.y, slot = slots[blockIdx.z];
+    const int b = b0 + blockIdx.x, upper = blockIdx.y, slot = slots[blockIdx.z];
     const int tid = threadIdx.x;
     // packed triangle indices; (i, j) is mirrored into the lower triangle for U
     auto fidx = [upper](int i, int j) { if (upper) { int t = i; i = j; j = t; } return i * (i - 1) / 2 + j; };
@@ -128,6 +134,33 @@ k_diag_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
         const int o = (gi & 31) * SBP + (gj & 31);
         xr[idx] = keep ? X[xidx(bi, bj)].r[o] : 0.f;
         xi[idx] = keep ? X[xidx(bi, bj)].i[o] : 0.f;
+    }
+    if (!winv) return;
+    // Operand packs of the inverse for the tensor-core triangular solves: pack
+    // row r holds column r of W = U^-1 (row r of V = L^-1) as
+    // Br = [Re | -Im], Bi = [Im | Re], tf32 hi (+ lo).
+    float *wp = winv + (int64_t)slot * ZS_WINV_STRIDE + (int64_t)(upper ? 0 : 4) * ZS_WINV_PLANE;
+    float *brh = wp, *brl = wp + ZS_WINV_PLANE, *bih = wp + 2 * ZS_WINV_PLANE, *bil = wp + 3 * ZS_WINV_PLANE;
+    for (int idx = tid; idx < TB * TB; idx += kInvThreads) {
+        const int r = idx >> 7, m = idx & (TB - 1);
+        const int gi = upper ? m : r, gj = upper ? r : m;
+        const int bi = gi >> 5, bj = gj >> 5;
+        const bool keep = upper ? (bj >= bi) : (bi >= bj);
+        const int o = (gi & 31) * SBP + (gj & 31);
+        const float er = keep ? X[xidx(bi, bj)].r[o] : 0.f, ei = keep ? X[xidx(bi, bj)].i[o] : 0.f;
+        const float hr = tf32_rna(er), hi = tf32_rna(ei);
+        const int64_t q = (int64_t)r * (2 * TB) + m;
+        brh[q] = hr;
+        brh[q + TB] = -hi;
+        bih[q] = hi;
+        bih[q + TB] = hr;
+        if (mode == 2) {
+            const float lr = tf32_rna(er - hr), li = tf32_rna(ei - hi);
+            brl[q] = lr;
+            brl[q + TB] = -li;
+            bil[q] = li;
+            bil[q + TB] = lr;
+        }
     }
 }
 
@@ -353,7 +386,8 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
 
 cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                const float *inv32, int64_t inv32_stride, float *dinv, int64_t dinv_stride,
-                               const int *slots, int nslot, cudaStream_t st) {
+                               int b0, int nblk, float *winv, int mode, const int *slots, int nslot,
+                               cudaStream_t st) {
     const size_t smem = 17 * sizeof(Blk);
     static bool init = false;
     if (!init) {
@@ -361,9 +395,12 @@ cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int6
         if (e != cudaSuccess) return e;
         init = true;
     }
-    const int nblk = (int)((n + TB - 1) / TB);
+    const int left = (int)((n + TB - 1) / TB) - b0;
+    if (nblk <= 0 || nblk > left) nblk = left;
+    if (nblk <= 0 || nslot <= 0) return cudaSuccess;
+    if (winv && nblk != 1) return cudaErrorInvalidValue;
     k_diag_inv<<<dim3(nblk, 2, nslot), kInvThreads, smem, st>>>(z32, ld, plane, z32_stride, n, inv32, inv32_stride,
-                                                                 dinv, dinv_stride, slots);
+                                                                 dinv, dinv_stride, b0, winv, mode, slots);
     return cudaGetLastError();
 }
 

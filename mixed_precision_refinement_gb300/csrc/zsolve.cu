@@ -28,11 +28,6 @@
 #include "../../include/zsolve.h"
 #include "common.cuh"
 
-cudaError_t zs_schur_tc_map(const float *pack, int64_t n, int nslots, int64_t pack_stride, void *map_out);
-cudaError_t zs_schur_tc_cmap(const float *z32, int64_t n, int64_t ld, int64_t plane, int nslots, int64_t z32_stride,
-                             void *map_out);
-cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
-                               int nslot, unsigned *status, int num_sms, cudaStream_t st);
 
 struct zsolve_ctx {
     int64_t n = 0;
@@ -48,8 +43,11 @@ struct zsolve_ctx {
     float *dinv = nullptr;  // inverses of the 128x128 diagonal blocks of L and U
     float *inv32 = nullptr; // inverses of the 32x32 diagonal sub-blocks of the current outer block
     int64_t dinv_stride = 0;
-    alignas(64) unsigned char pack_map[128] = {};  // TMA tensor map over the operand packs
-    alignas(64) unsigned char z32_map[128] = {};   // TMA tensor map over the float32 matrices
+    float *winv = nullptr;  // tensor-core operand packs of the current diagonal block's inverses
+    alignas(64) unsigned char pack_map[128] = {};    // TMA tensor map over the operand packs (32 x 128 boxes)
+    alignas(64) unsigned char packst_map[128] = {};  // the same packs, 32 x 32 boxes for stores
+    alignas(64) unsigned char winv_map[128] = {};    // TMA tensor map over the inverse packs
+    alignas(64) unsigned char z32_map[128] = {};     // TMA tensor map over the float32 matrices
     float2 *v = nullptr;
     float4 *xs = nullptr;  // double-float split of x (residual mode DF)
     int resid_mode = ZSOLVE_RESID_F64;
@@ -178,7 +176,7 @@ int gemm_mode(const zsolve_opts &o) {
 size_t slot_bytes(int64_t n, int64_t ld) {
     return (size_t)n * n * sizeof(double2) + (size_t)2 * n * ld * sizeof(float) +
            (size_t)6 * zs_pack_plane(n) * sizeof(float) + (size_t)zs_dinv_stride(n) * sizeof(float) +
-           (size_t)zs_inv32_slot_stride(n) * sizeof(float);
+           (size_t)zs_inv32_slot_stride(n) * sizeof(float) + (size_t)ZS_WINV_STRIDE * sizeof(float);
 }
 
 // ------------------------------------------------------------------ factor
@@ -186,24 +184,38 @@ size_t slot_bytes(int64_t n, int64_t ld) {
 int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
     const int64_t n = ctx->n;
     const int mode = gemm_mode(ctx->opts);
+    const int64_t inv32_stride = zs_inv32_slot_stride(n);
     ZS_CU(cudaMemsetAsync(ctx->d_pivflag, 0, sizeof(int) * ctx->S, ctx->stream));
     for (int64_t J = 0; J < n; J += ZS_NB) {
         const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
+        const bool last = J + nb >= n;
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
             ZS_CU(zs_launch_diag_lu(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, nb, slots, nslot,
-                                    ctx->d_pivflag, ctx->inv32, zs_inv32_slot_stride(n), ctx->stream));
-            sp.done(1);
+                                    ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->stream));
+            int launches = 1;
+            if (mode != 0) {  // this block's inverses now: the tensor-core solves multiply by them
+                ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->inv32, inv32_stride,
+                                         ctx->dinv, ctx->dinv_stride, (int)(J / ZS_NB), 1,
+                                         last ? nullptr : ctx->winv, mode, slots, nslot, ctx->stream));
+                launches++;
+            }
+            sp.done(launches);
         }
-        if (J + nb >= n) break;
+        if (last) break;
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
-            ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
-                                   zs_inv32_slot_stride(n), ctx->pack, ctx->pack_stride, mode, slots, nslot,
-                                   ctx->stream));
-            ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
-                                   zs_inv32_slot_stride(n), ctx->pack, ctx->pack_stride, mode, slots, nslot,
-                                   ctx->stream));
+            if (mode == 0) {
+                ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
+                                       inv32_stride, ctx->pack, ctx->pack_stride, mode, slots, nslot, ctx->stream));
+                ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
+                                       inv32_stride, ctx->pack, ctx->pack_stride, mode, slots, nslot, ctx->stream));
+            } else {
+                ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                                          ctx->pack_stride, mode, slots, nslot, ctx->stream));
+                ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J,
+                                        mode == 2 ? 1 : 0, slots, nslot, ctx->d_status, ctx->num_sms, ctx->stream));
+            }
             sp.done(2);
         }
         StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
@@ -215,10 +227,12 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
                                      ctx->d_status, ctx->num_sms, ctx->stream));
         sp.done(1);
     }
-    StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
-    ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->inv32, zs_inv32_slot_stride(n),
-                             ctx->dinv, ctx->dinv_stride, slots, nslot, ctx->stream));
-    sp.done(1);
+    if (mode == 0) {  // the SIMT solves used the 32x32 inverses only: every block's inverse now
+        StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
+        ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->inv32, inv32_stride,
+                                 ctx->dinv, ctx->dinv_stride, 0, 0, nullptr, mode, slots, nslot, ctx->stream));
+        sp.done(1);
+    }
     return ZSOLVE_OK;
 }
 
@@ -514,6 +528,7 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->pack);
     cudaFree(c->dinv);
     cudaFree(c->inv32);
+    cudaFree(c->winv);
     cudaFree(c->v);
     cudaFree(c->xs);
     cudaFree(c->partials);
@@ -616,6 +631,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->pack, (size_t)S * ctx->pack_stride * sizeof(float));
     ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
     ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
+    if (gemm_mode(ctx->opts) != 0) ALLOC(ctx->winv, (size_t)S * ZS_WINV_STRIDE * sizeof(float));
     ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
     ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
     ALLOC(ctx->d_relcorr, (size_t)S * nrhs_max * sizeof(double));
@@ -636,8 +652,10 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     for (auto &e : ctx->ev)
         if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
     if (gemm_mode(ctx->opts) != 0 &&
-        (zs_schur_tc_map(ctx->pack, n, S, ctx->pack_stride, ctx->pack_map) != cudaSuccess ||
-         zs_schur_tc_cmap(ctx->z32, n, ctx->ld, ctx->plane, S, ctx->z32_stride, ctx->z32_map) != cudaSuccess))
+        (zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 128, ctx->pack_map) != cudaSuccess ||
+         zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 32, ctx->packst_map) != cudaSuccess ||
+         zs_tc_winv_map(ctx->winv, S, ctx->winv_map) != cudaSuccess ||
+         zs_tc_z32_map(ctx->z32, n, ctx->ld, ctx->plane, S, ctx->z32_stride, ctx->z32_map) != cudaSuccess))
         return bail(ZSOLVE_ECUDA);
     std::vector<int> all(S);
     for (int s = 0; s < S; s++) all[s] = s;
