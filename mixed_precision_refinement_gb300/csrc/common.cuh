@@ -119,9 +119,13 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
 // diagonal sub-blocks of U and of L (identity padding in a partial block).
 #define ZS_INV32_STRIDE (4 * 2 * 2 * 32 * 32)
 inline int64_t zs_inv32_slot_stride(int64_t n) { return ((n + 127) / 128) * ZS_INV32_STRIDE; }
-cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                              int64_t J, int nb, const int *slots, int nslot, int *pivflag, float *inv32,
-                              int64_t inv32_stride, cudaStream_t st);
+// Diagonal block at J (nb <= 128 columns, identity-padded to 128): its LU in
+// place in z32, the 32x32 sub-block inverses (inv32), the dense 128x128
+// inverses of L and U (dinv) and, if winv != NULL, their operand packs
+// (mode 1: tf32 hi; 2: hi + lo).  pivflag[slot] = 1 on a tiny or non-finite pivot.
+cudaError_t zs_launch_diag_block(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
+                                 const int *slots, int nslot, int *pivflag, float *inv32, int64_t inv32_stride,
+                                 float *dinv, int64_t dinv_stride, float *winv, int mode, cudaStream_t st);
 // mode: 0 = pack plain fp32 (FFMA), 1 = tf32 rounded (TF32), 2 = tf32 hi + lo (TF32X3)
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                              int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
@@ -151,7 +155,7 @@ cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane
 cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
                                int nslot, unsigned *status, int num_sms, cudaStream_t st);
 // L21 = A21 U11^-1 and U12 = L11^-1 A12 from the packs of zs_launch_pack_trsm
-// and zs_launch_diag_inv; writes L21, U12 into z32 and their operand packs
+// and zs_launch_diag_block; writes L21, U12 into z32 and their operand packs
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
                               int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
                               cudaStream_t st);
@@ -174,19 +178,14 @@ cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int6
                            unsigned *status, int num_sms, cudaStream_t st);
 
 // Inverses of the 128x128 diagonal blocks of L (unit lower) and U (upper):
-// per slot [block][L, U][re, im][128][128] floats, for blocks b0 .. b0+nblk-1
-// (nblk <= 0: every block from b0 on).  winv != NULL additionally writes the
-// inverses as tensor-core operand packs (mode 1: tf32 hi; 2: hi + lo), per
-// slot ZS_WINV_STRIDE floats = 8 planes of 128 rows x 256:
-//   planes 0-3 W = U^-1: Br(j) = [Re W(:,j) | -Im W(:,j)], Bi(j) = [Im W(:,j) | Re W(:,j)]  (hi, lo each)
+// per slot [block][L, U][re, im][128][128] floats.  Operand packs of one
+// block's inverses for the tensor-core solves, per slot ZS_WINV_STRIDE floats
+// = 8 planes of 128 rows x 256:
+//   planes 0-3 W = U^-1: Br(j) = [Re W(:,j) | -Im W(:,j)], Bi(j) = [Im W(:,j) | Re W(:,j)]
 //   planes 4-7 V = L^-1: Br(k) = [Re V(k,:) | -Im V(k,:)], Bi(k) = [Im V(k,:) | Re V(k,:)]
-// in the order Br hi, Br lo, Bi hi, Bi lo; only one block (nblk = 1) may write packs.
+// each as Br hi, Br lo, Bi hi, Bi lo.
 #define ZS_WINV_PLANE (ZS_NB * ZS_PACK_K)
 #define ZS_WINV_STRIDE (8 * ZS_WINV_PLANE)
-cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                               const float *inv32, int64_t inv32_stride, float *dinv, int64_t dinv_stride,
-                               int b0, int nblk, float *winv, int mode, const int *slots, int nslot,
-                               cudaStream_t st);
 inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }
 // Triangular solves with 128-row blocks and the inverse diagonal blocks; nrhs 1, 2 or 4 per launch.
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,

@@ -5,14 +5,15 @@
 // paragraph states that it does not pivot).
 //
 // The host walks the matrix in outer blocks of ZS_NB = 128 columns.  At
-// outer column J:
-//   k_diag_lu   factors the 128 x 128 diagonal block in shared memory, one
-//               32-column panel at a time: panel factor (rows held in
-//               registers, the multiplier broadcast by warp shuffle), the
-//               panel's row block of U, and the block's own trailing update;
+// outer column J the diagonal block is factored by k_diag_block
+// (diag_block.cu), which also leaves the inverses of its 32 x 32 diagonal
+// sub-blocks behind.  This file holds the FP32 (FFMA) kernels of the rest of
+// the step and the operand packing of the tensor-core path:
 //   k_trsm_l    L21 = A21 U11^-1, one row per warp (row-oriented solve);
 //   k_trsm_u    U12 = L11^-1 A12, one column per warp;
-//   k_schur_*   A22 -= L21 U12 (this file: FP32 FFMA; schur_tc.cu: tcgen05).
+//   k_schur_simt  A22 -= L21 U12 (FP32 FFMA; schur_tc.cu: tcgen05);
+//   k_pack_trsm A21 and A12^T as tf32 operand packs for the tensor-core
+//               block solves (schur_tc.cu).
 // k_trsm_l / k_trsm_u also write L21 and U12 as K-major operand packs for
 // the trailing update: A = [Re L21 | Im L21], Br = [Re U12^T | -Im U12^T],
 // Bi = [Im U12^T | Re U12^T], so that Re(L21 U12) = A Br^T and
@@ -46,227 +47,10 @@ __device__ __forceinline__ void pack_put(float *hi, float *lo, int64_t off, floa
     }
 }
 
-// ---------------------------------------------------------------- diagonal block
-
-constexpr int kDiagThreads = 512;  // 16 warps
-
-__global__ void __launch_bounds__(kDiagThreads, 1)
-k_diag_lu(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
-          const int *__restrict__ slots, int *__restrict__ pivflag, float *__restrict__ inv32, int64_t inv32_stride) {
-    extern __shared__ float sm[];
-    float *sre = sm;                   // [NB][LDS]
-    float *sim = sm + NB * LDS;        // [NB][LDS]
-    float *prow = sm + 2 * NB * LDS;   // [2][2][P]: double-buffered pivot row (re, im)
-    __shared__ unsigned s_amax;
-    const int slot = slots[blockIdx.x];
-    float *re = z32 + (int64_t)slot * z32_stride;
-    float *im = re + plane;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) s_amax = 0u;
-    __syncthreads();
-    float amax = 0.f;
-    for (int idx = tid; idx < nb * nb; idx += kDiagThreads) {
-        int i = idx / nb, j = idx - i * nb;
-        int64_t g = (J + i) * ld + J + j;
-        float a = re[g], b = im[g];
-        sre[i * LDS + j] = a;
-        sim[i * LDS + j] = b;
-        amax = fmaxf(amax, fabsf(a) + fabsf(b));
-    }
-    if (!(amax <= 3.0e38f)) amax = 3.0e38f;  // non-finite inputs: the pivot test flags them
-    atomicMax(&s_amax, __float_as_uint(amax));
-    __syncthreads();
-    const float tiny = 1e-30f * __uint_as_float(s_amax);
-    bool flagged = false;
-
-    for (int p = 0; p < nb; p += P) {
-        const int pw = min(P, nb - p);
-        // -- panel factor: rows p..nb-1, columns p..p+pw-1.  Warp w holds rows
-        //    p + w + 16 t in registers, lane = column.
-        cf a[NB / 16];
-#pragma unroll
-        for (int t = 0; t < NB / 16; t++) {
-            int r = p + warp + 16 * t;
-            a[t] = (r < nb && lane < pw) ? cf{sre[r * LDS + p + lane], sim[r * LDS + p + lane]}
-                                         : cf{0.f, 0.f};
-        }
-        for (int k = 0; k < pw; k++) {
-            const int kk = p + k;
-            float *pr = prow + (k & 1) * 2 * P;
-            if (warp == (k & 15)) {  // owner of row kk publishes it
-                const int t = k >> 4;
-                cf v = a[0];
-#pragma unroll
-                for (int q = 0; q < NB / 16; q++)
-                    if (q == t) v = a[q];
-                pr[lane] = v.re;
-                pr[P + lane] = v.im;
-            }
-            __syncthreads();
-            const cf piv = {pr[k], pr[P + k]};
-            const cf inv = zs::crecip(piv);
-            if (tid == 0 && (!zs::cfinite(piv) || fabsf(piv.re) + fabsf(piv.im) <= tiny))
-                flagged = true;
-            const cf u = (lane < pw) ? cf{pr[lane], pr[P + lane]} : cf{0.f, 0.f};
-#pragma unroll
-            for (int t = 0; t < NB / 16; t++) {
-                const int r = p + warp + 16 * t;
-                if (r > kk && r < nb) {  // warp-uniform condition
-                    cf l;
-                    l.re = __shfl_sync(0xffffffffu, a[t].re, k);
-                    l.im = __shfl_sync(0xffffffffu, a[t].im, k);
-                    l = zs::cmul(l, inv);
-                    if (lane == k) a[t] = l;
-                    else if (lane > k && lane < pw) a[t] = zs::cfms(a[t], l, u);
-                }
-            }
-        }
-#pragma unroll
-        for (int t = 0; t < NB / 16; t++) {
-            int r = p + warp + 16 * t;
-            if (r < nb && lane < pw) {
-                sre[r * LDS + p + lane] = a[t].re;
-                sim[r * LDS + p + lane] = a[t].im;
-            }
-        }
-        __syncthreads();
-        const int c0 = p + pw;
-        if (c0 >= nb) break;
-        // -- row block of U inside the diagonal block: rows p..p+pw-1, columns
-        //    c0..nb-1.  Warp per column, lane = row; unit-lower panel L11.
-        for (int c = c0 + warp; c < nb; c += 16) {
-            cf v = (lane < pw) ? cf{sre[(p + lane) * LDS + c], sim[(p + lane) * LDS + c]} : cf{0.f, 0.f};
-            for (int k = 0; k < pw - 1; k++) {
-                cf uk;
-                uk.re = __shfl_sync(0xffffffffu, v.re, k);
-                uk.im = __shfl_sync(0xffffffffu, v.im, k);
-                if (lane > k && lane < pw) {
-                    cf l = {sre[(p + lane) * LDS + p + k], sim[(p + lane) * LDS + p + k]};
-                    v = zs::cfms(v, l, uk);
-                }
-            }
-            if (lane < pw) {
-                sre[(p + lane) * LDS + c] = v.re;
-                sim[(p + lane) * LDS + c] = v.im;
-            }
-        }
-        __syncthreads();
-        // -- trailing update of the diagonal block: rows/cols c0..nb-1, K = pw,
-        //    4x4 register tiles.
-        const int m = nb - c0;
-        const int tiles_1d = (m + 3) / 4;
-        for (int tix = tid; tix < tiles_1d * tiles_1d; tix += kDiagThreads) {
-            const int ti = tix / tiles_1d, tj = tix - ti * tiles_1d;
-            const int i0 = c0 + 4 * ti, j0 = c0 + 4 * tj;
-            cf acc[4][4];
-#pragma unroll
-            for (int x = 0; x < 4; x++)
-#pragma unroll
-                for (int y = 0; y < 4; y++) acc[x][y] = cf{0.f, 0.f};
-            for (int k = 0; k < pw; k++) {
-                cf lv[4], uv[4];
-#pragma unroll
-                for (int x = 0; x < 4; x++) {
-                    int i = min(i0 + x, nb - 1);
-                    lv[x] = cf{sre[i * LDS + p + k], sim[i * LDS + p + k]};
-                    int j = min(j0 + x, nb - 1);
-                    uv[x] = cf{sre[(p + k) * LDS + j], sim[(p + k) * LDS + j]};
-                }
-#pragma unroll
-                for (int x = 0; x < 4; x++)
-#pragma unroll
-                    for (int y = 0; y < 4; y++) {
-                        acc[x][y].re = fmaf(lv[x].re, uv[y].re, fmaf(-lv[x].im, uv[y].im, acc[x][y].re));
-                        acc[x][y].im = fmaf(lv[x].re, uv[y].im, fmaf(lv[x].im, uv[y].re, acc[x][y].im));
-                    }
-            }
-#pragma unroll
-            for (int x = 0; x < 4; x++)
-#pragma unroll
-                for (int y = 0; y < 4; y++) {
-                    int i = i0 + x, j = j0 + y;
-                    if (i < nb && j < nb) {
-                        sre[i * LDS + j] -= acc[x][y].re;
-                        sim[i * LDS + j] -= acc[x][y].im;
-                    }
-                }
-        }
-        __syncthreads();
-    }
-    for (int idx = tid; idx < nb * nb; idx += kDiagThreads) {
-        int i = idx / nb, j = idx - i * nb;
-        int64_t g = (J + i) * ld + J + j;
-        re[g] = sre[i * LDS + j];
-        im[g] = sim[i * LDS + j];
-    }
-    if (tid == 0 && flagged) pivflag[slot] = 1;
-    if (nb < NB) {  // last, partial block: identity padding for the sub-block inverses
-        for (int idx = tid; idx < NB * NB; idx += kDiagThreads) {
-            const int i = idx >> 7, j = idx & (NB - 1);
-            if (i >= nb || j >= nb) {
-                sre[i * LDS + j] = (i == j) ? 1.f : 0.f;
-                sim[i * LDS + j] = 0.f;
-            }
-        }
-        __syncthreads();
-    }
-    // Inverses of the four 32x32 diagonal sub-blocks of U11 (upper) and of
-    // L11 (unit lower), for the block triangular solves.  Warp w inverts
-    // sub-block w/2 (0-3: U, 4-7: L), rows (w & 1) + 2t, two rows at a time;
-    // one row of the inverse per solve (x^T U = e_i^T resp. x^T L = e_i^T),
-    // lane = column; the diagonal reciprocals are formed once per lane.
-    {
-        const int blk = warp >> 1, upper = blk < 4, kb = blk & 3;
-        const int o = kb * P;
-        float *dst = inv32 + (int64_t)slot * inv32_stride + (J / NB) * ZS_INV32_STRIDE + (kb * 2 + (upper ? 0 : 1)) * 2 * P * P;
-        const cf dl = upper ? zs::crecip(cf{sre[(o + lane) * LDS + o + lane], sim[(o + lane) * LDS + o + lane]})
-                            : cf{1.f, 0.f};
-        for (int i0 = (warp & 1); i0 < P; i0 += 4) {
-            const int i1 = i0 + 2;  // second row of the pair
-            cf x0 = cf{lane == i0 ? 1.f : 0.f, 0.f}, x1 = cf{lane == i1 ? 1.f : 0.f, 0.f};
-            if (upper) {
-                for (int k = i0; k < P; k++) {
-                    if (lane == k) {
-                        x0 = zs::cmul(x0, dl);
-                        if (k >= i1) x1 = zs::cmul(x1, dl);
-                    }
-                    cf a, b;
-                    a.re = __shfl_sync(0xffffffffu, x0.re, k);
-                    a.im = __shfl_sync(0xffffffffu, x0.im, k);
-                    b.re = __shfl_sync(0xffffffffu, x1.re, k);
-                    b.im = __shfl_sync(0xffffffffu, x1.im, k);
-                    if (lane > k) {
-                        const cf u = cf{sre[(o + k) * LDS + o + lane], sim[(o + k) * LDS + o + lane]};
-                        x0 = zs::cfms(x0, a, u);
-                        if (k >= i1) x1 = zs::cfms(x1, b, u);
-                    }
-                }
-            } else {
-                for (int k = i1; k > 0; k--) {
-                    cf a, b;
-                    a.re = __shfl_sync(0xffffffffu, x0.re, k);
-                    a.im = __shfl_sync(0xffffffffu, x0.im, k);
-                    b.re = __shfl_sync(0xffffffffu, x1.re, k);
-                    b.im = __shfl_sync(0xffffffffu, x1.im, k);
-                    if (lane < k) {
-                        const cf l = cf{sre[(o + k) * LDS + o + lane], sim[(o + k) * LDS + o + lane]};
-                        x1 = zs::cfms(x1, b, l);
-                        if (k <= i0) x0 = zs::cfms(x0, a, l);
-                    }
-                }
-            }
-            dst[i0 * P + lane] = x0.re;
-            dst[P * P + i0 * P + lane] = x0.im;
-            dst[i1 * P + lane] = x1.re;
-            dst[P * P + i1 * P + lane] = x1.im;
-        }
-    }
-}
-
 // ---------------------------------------------------------------- L21 = A21 U11^-1
 
 // Both block solves run in four 32-column steps with the inverted 32x32
-// diagonal sub-blocks from k_diag_lu: for step kb, x_kb = r_kb . inv(U_kb,kb)
+// diagonal sub-blocks from k_diag_block: for step kb, x_kb = r_kb . inv(U_kb,kb)
 // (resp. inv(L_kb,kb) . r_kb), then the later sub-blocks are updated with the
 // off-diagonal blocks of U11 (resp. L11).  Every product is a register-tiled
 // multiply-add with operands broadcast from shared memory; no step is a
@@ -638,22 +422,6 @@ cudaError_t set_smem(K kernel, size_t bytes) {
 }
 
 }  // namespace
-
-cudaError_t zs_launch_diag_lu(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                              int64_t J, int nb, const int *slots, int nslot, int *pivflag, float *inv32,
-                              int64_t inv32_stride, cudaStream_t st) {
-    (void)n;
-    const size_t smem = (2 * NB * LDS + 4 * P) * sizeof(float);
-    static bool init = false;
-    if (!init) {
-        cudaError_t e = set_smem(k_diag_lu, smem);
-        if (e != cudaSuccess) return e;
-        init = true;
-    }
-    k_diag_lu<<<nslot, kDiagThreads, smem, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag, inv32,
-                                                  inv32_stride);
-    return cudaGetLastError();
-}
 
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                              int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,

@@ -4,10 +4,8 @@
 // answers from a GPU without double precision", steps 2 and 4: solve with the
 // single-precision factorisation).
 //
-// k_diag_inv (once per factorisation): for every 128 x 128 diagonal block of
-// every frequency, X = L_bb^-1 (unit lower) and X = U_bb^-1 (upper), built from
-// the inverses of the 32 x 32 diagonal sub-blocks the factorisation left
-// behind, by block substitution with 32 x 32 products in shared memory.
+// The inverses of the 128 x 128 diagonal blocks (X = L_bb^-1, unit lower, and
+// X = U_bb^-1, upper) come from the factorisation (diag_block.cu).
 //
 // k_trsv_inv (per solve): the same ticketed, in-order task scheme as the
 // sequential kernel, with 128-row blocks (half the dependency chain) and the
@@ -25,145 +23,6 @@ namespace {
 using zs::cf;
 
 constexpr int TB = ZS_TB2;  // 128
-constexpr int kInvThreads = 512;
-constexpr int SB = 32;       // sub-block size
-constexpr int SBP = SB + 1;  // padded sub-block row
-
-// One 32x32 complex sub-block in shared memory (two padded float planes).
-struct Blk {
-    float r[SB * SBP], i[SB * SBP];
-};
-
-// acc[2] += A . B for this thread's two entries (row t >> 4, columns 2*(t & 15) + {0, 1})
-__device__ __forceinline__ void blk_mac(const Blk &A, const Blk &B, cf (&acc)[2], int row, int c0) {
-#pragma unroll 8
-    for (int k = 0; k < SB; k++) {
-        const cf a = cf{A.r[row * SBP + k], A.i[row * SBP + k]};
-#pragma unroll
-        for (int q = 0; q < 2; q++) {
-            const cf b = cf{B.r[k * SBP + c0 + q], B.i[k * SBP + c0 + q]};
-            acc[q].re = fmaf(a.re, b.re, fmaf(-a.im, b.im, acc[q].re));
-            acc[q].im = fmaf(a.re, b.im, fmaf(a.im, b.re, acc[q].im));
-        }
-    }
-}
-
-// Inverse of a 128 x 128 diagonal block of L (unit lower) or U (upper) from
-// the inverses of its four 32 x 32 diagonal sub-blocks (written by the
-// factorisation), by block substitution: with D_i the inverted diagonal
-// sub-blocks,
-//   L: X_ii = D_i,  X_ik = -D_i sum_{m=k}^{i-1} L_im X_mk   (i > k, i ascending)
-//   U: X_ii = D_i,  X_ik = -D_i sum_{m=i+1}^{k} U_im X_mk   (i < k, i descending)
-// Padding rows beyond n are the identity.
-__device__ __forceinline__ float tf32_rna(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
-}
-
-__global__ void __launch_bounds__(kInvThreads, 1)
-k_diag_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-           const float *__restrict__ inv32, int64_t inv32_stride, float *__restrict__ dinv, int64_t dinv_stride,
-           int b0, float *__restrict__ winv, int mode, const int *__restrict__ slots) {
-    extern __shared__ float sm[];
-    Blk *F = reinterpret_cast<Blk *>(sm);  // [6]: off-diagonal factor sub-blocks of the triangle
-    Blk *X = F + 6;                        // [10]: result sub-blocks, diagonal included
-    Blk *T = X + 10;                       // scratch
-    const int b = b0 + blockIdx.x, upper = blockIdx.y, slot = slots[blockIdx.z];
-    const int tid = threadIdx.x;
-    // packed triangle indices; (i, j) is mirrored into the lower triangle for U
-    auto fidx = [upper](int i, int j) { if (upper) { int t = i; i = j; j = t; } return i * (i - 1) / 2 + j; };
-    auto xidx = [upper](int i, int j) { if (upper) { int t = i; i = j; j = t; } return i * (i + 1) / 2 + j; };
-    const float *re = z32 + (int64_t)slot * z32_stride;
-    const float *im = re + plane;
-    const float *d32 = inv32 + (int64_t)slot * inv32_stride + (int64_t)b * ZS_INV32_STRIDE;
-    const int64_t r0 = (int64_t)b * TB;
-    const int rows = (int)zs::min64(TB, n - r0);
-    // off-diagonal factor sub-blocks of the needed triangle, diagonal inverses, zero result blocks
-    for (int idx = tid; idx < TB * TB; idx += kInvThreads) {
-        const int gi = idx >> 7, gj = idx & (TB - 1);
-        const int bi = gi >> 5, bj = gj >> 5, li = gi & 31, lj = gj & 31;
-        const int o = li * SBP + lj;
-        const bool tri = upper ? (bj > bi) : (bi > bj);
-        if (tri) {
-            float a = 0.f, c = 0.f;
-            if (gi < rows && gj < rows) {
-                a = re[(r0 + gi) * ld + r0 + gj];
-                c = im[(r0 + gi) * ld + r0 + gj];
-            }
-            F[fidx(bi, bj)].r[o] = a;
-            F[fidx(bi, bj)].i[o] = c;
-        }
-        if (bi == bj) {
-            const float *d = d32 + (bi * 2 + (upper ? 0 : 1)) * 2 * SB * SB;
-            X[xidx(bi, bi)].r[o] = d[li * SB + lj];
-            X[xidx(bi, bi)].i[o] = d[SB * SB + li * SB + lj];
-        }
-    }
-    __syncthreads();
-    const int row = tid >> 4, c0 = 2 * (tid & 15);
-    for (int step = 0; step < 3; step++) {
-        const int i = upper ? 2 - step : step + 1;  // block row being formed
-        const int kbeg = upper ? i + 1 : 0, kend = upper ? 4 : i;
-        for (int k = kbeg; k < kend; k++) {
-            cf acc[2] = {cf{0.f, 0.f}, cf{0.f, 0.f}};
-            const int mbeg = upper ? i + 1 : k, mend = upper ? k + 1 : i;
-            for (int m = mbeg; m < mend; m++) blk_mac(F[fidx(i, m)], X[xidx(m, k)], acc, row, c0);
-#pragma unroll
-            for (int q = 0; q < 2; q++) {
-                T->r[row * SBP + c0 + q] = acc[q].re;
-                T->i[row * SBP + c0 + q] = acc[q].im;
-            }
-            __syncthreads();
-            cf out[2] = {cf{0.f, 0.f}, cf{0.f, 0.f}};
-            blk_mac(X[xidx(i, i)], *T, out, row, c0);
-#pragma unroll
-            for (int q = 0; q < 2; q++) {
-                X[xidx(i, k)].r[row * SBP + c0 + q] = -out[q].re;
-                X[xidx(i, k)].i[row * SBP + c0 + q] = -out[q].im;
-            }
-            __syncthreads();
-        }
-    }
-    float *xr = dinv + (int64_t)slot * dinv_stride + (int64_t)b * 4 * TB * TB + (int64_t)upper * 2 * TB * TB;
-    float *xi = xr + TB * TB;
-    for (int idx = tid; idx < TB * TB; idx += kInvThreads) {
-        const int gi = idx >> 7, gj = idx & (TB - 1);
-        const int bi = gi >> 5, bj = gj >> 5;
-        const bool keep = upper ? (bj >= bi) : (bi >= bj);
-        const int o = (gi & 31) * SBP + (gj & 31);
-        xr[idx] = keep ? X[xidx(bi, bj)].r[o] : 0.f;
-        xi[idx] = keep ? X[xidx(bi, bj)].i[o] : 0.f;
-    }
-    if (!winv) return;
-    // Operand packs of the inverse for the tensor-core triangular solves: pack
-    // row r holds column r of W = U^-1 (row r of V = L^-1) as
-    // Br = [Re | -Im], Bi = [Im | Re], tf32 hi (+ lo).
-    float *wp = winv + (int64_t)slot * ZS_WINV_STRIDE + (int64_t)(upper ? 0 : 4) * ZS_WINV_PLANE;
-    float *brh = wp, *brl = wp + ZS_WINV_PLANE, *bih = wp + 2 * ZS_WINV_PLANE, *bil = wp + 3 * ZS_WINV_PLANE;
-    for (int idx = tid; idx < TB * TB; idx += kInvThreads) {
-        const int r = idx >> 7, m = idx & (TB - 1);
-        const int gi = upper ? m : r, gj = upper ? r : m;
-        const int bi = gi >> 5, bj = gj >> 5;
-        const bool keep = upper ? (bj >= bi) : (bi >= bj);
-        const int o = (gi & 31) * SBP + (gj & 31);
-        const float er = keep ? X[xidx(bi, bj)].r[o] : 0.f, ei = keep ? X[xidx(bi, bj)].i[o] : 0.f;
-        const float hr = tf32_rna(er), hi = tf32_rna(ei);
-        const int64_t q = (int64_t)r * (2 * TB) + m;
-        brh[q] = hr;
-        brh[q + TB] = -hi;
-        bih[q] = hi;
-        bih[q + TB] = hr;
-        if (mode == 2) {
-            const float lr = tf32_rna(er - hr), li = tf32_rna(ei - hi);
-            brl[q] = lr;
-            brl[q + TB] = -li;
-            bil[q] = li;
-            bil[q + TB] = lr;
-        }
-    }
-}
-
 // lane 0 waits until more than `need` blocks are complete; the warp barrier
 // orders the other lanes' loads after its acquire
 __device__ __forceinline__ long long warp_progress(const unsigned long long *p, unsigned epoch, long long need,
@@ -383,26 +242,6 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
 }
 
 }  // namespace
-
-cudaError_t zs_launch_diag_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                               const float *inv32, int64_t inv32_stride, float *dinv, int64_t dinv_stride,
-                               int b0, int nblk, float *winv, int mode, const int *slots, int nslot,
-                               cudaStream_t st) {
-    const size_t smem = 17 * sizeof(Blk);
-    static bool init = false;
-    if (!init) {
-        cudaError_t e = cudaFuncSetAttribute(k_diag_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        init = true;
-    }
-    const int left = (int)((n + TB - 1) / TB) - b0;
-    if (nblk <= 0 || nblk > left) nblk = left;
-    if (nblk <= 0 || nslot <= 0) return cudaSuccess;
-    if (winv && nblk != 1) return cudaErrorInvalidValue;
-    k_diag_inv<<<dim3(nblk, 2, nslot), kInvThreads, smem, st>>>(z32, ld, plane, z32_stride, n, inv32, inv32_stride,
-                                                                 dinv, dinv_stride, b0, winv, mode, slots);
-    return cudaGetLastError();
-}
 
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                const float *dinv, int64_t dinv_stride, float2 *v, int64_t v_stride, int nrhs,

@@ -72,6 +72,9 @@ struct zsolve_ctx {
     size_t hd_x_cap = 0;
     int hd_nrhs_cap = 0;
     cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+    // side stream: packs the next block solves' operands while the diagonal block is factored
+    cudaStream_t side = nullptr;
+    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
     int assembled = 0, factored = 0, fb_ready = 0;
     // stage profile: launch counts always, event-timed spans with opts.profile
     int64_t prof_launches[ZSOLVE_NSTAGE] = {};
@@ -189,18 +192,24 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
     for (int64_t J = 0; J < n; J += ZS_NB) {
         const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
         const bool last = J + nb >= n;
+        if (mode != 0 && !last) {
+            // A21 and A12^T do not depend on the diagonal block: pack them on
+            // the side stream while it is factored
+            ZS_CU(cudaEventRecord(ctx->ev_fork, ctx->stream));
+            ZS_CU(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0));
+            ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
+                                      ctx->pack_stride, mode, slots, nslot, ctx->side));
+            ZS_CU(cudaEventRecord(ctx->ev_join, ctx->side));
+            ctx->prof_launches[ZSOLVE_STAGE_TRSM]++;
+        }
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
-            ZS_CU(zs_launch_diag_lu(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, nb, slots, nslot,
-                                    ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->stream));
-            int launches = 1;
-            if (mode != 0) {  // this block's inverses now: the tensor-core solves multiply by them
-                ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->inv32, inv32_stride,
-                                         ctx->dinv, ctx->dinv_stride, (int)(J / ZS_NB), 1,
-                                         last ? nullptr : ctx->winv, mode, slots, nslot, ctx->stream));
-                launches++;
-            }
-            sp.done(launches);
+            // the block's factors, its 32x32 and 128x128 inverses and, for the
+            // tensor-core solves that multiply by them, their operand packs
+            ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
+                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->dinv, ctx->dinv_stride,
+                                       (mode != 0 && !last) ? ctx->winv : nullptr, mode, ctx->stream));
+            sp.done(2);
         }
         if (last) break;
         {
@@ -211,12 +220,11 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
                 ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
                                        inv32_stride, ctx->pack, ctx->pack_stride, mode, slots, nslot, ctx->stream));
             } else {
-                ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                                          ctx->pack_stride, mode, slots, nslot, ctx->stream));
+                ZS_CU(cudaStreamWaitEvent(ctx->stream, ctx->ev_join, 0));  // the operand packs, from the side stream
                 ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J,
                                         mode == 2 ? 1 : 0, slots, nslot, ctx->d_status, ctx->num_sms, ctx->stream));
             }
-            sp.done(2);
+            sp.done(mode == 0 ? 2 : 1);
         }
         StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
         if (mode == 0)
@@ -225,12 +233,6 @@ int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
         else
             ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, mode == 2 ? 1 : 0, slots, nslot,
                                      ctx->d_status, ctx->num_sms, ctx->stream));
-        sp.done(1);
-    }
-    if (mode == 0) {  // the SIMT solves used the 32x32 inverses only: every block's inverse now
-        StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
-        ZS_CU(zs_launch_diag_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, ctx->inv32, inv32_stride,
-                                 ctx->dinv, ctx->dinv_stride, 0, 0, nullptr, mode, slots, nslot, ctx->stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
@@ -563,6 +565,9 @@ void free_all(zsolve_ctx *c) {
     for (auto e : c->ev_pool) cudaEventDestroy(e);
     c->pending.clear();
     c->ev_pool.clear();
+    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
+    if (c->ev_join) cudaEventDestroy(c->ev_join);
+    if (c->side) cudaStreamDestroy(c->side);
 }
 
 }  // namespace
@@ -651,6 +656,10 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
 #undef ALLOCH
     for (auto &e : ctx->ev)
         if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
+    if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming) != cudaSuccess)
+        return bail(ZSOLVE_ECUDA);
     if (gemm_mode(ctx->opts) != 0 &&
         (zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 128, ctx->pack_map) != cudaSuccess ||
          zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 32, ctx->packst_map) != cudaSuccess ||
