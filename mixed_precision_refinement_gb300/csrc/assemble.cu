@@ -20,9 +20,19 @@
 //  - where G_ij = 0 (all but three diagonals in the generated workloads)
 //    Zs*G is an exact zero, so the products are skipped and only the sign of
 //    zero they would produce is reproduced (integer ops);
+//  - zero tests and signs of zero are done on the 32-bit halves of the bit
+//    pattern (see zs::bits_of), so no FP64 compare is issued;
 //  - float64 -> float32 round-to-nearest-even is done on the integer bit
-//    pattern, with the hardware conversion kept for subnormal results,
-//    overflow and NaN.
+//    pattern; the hardware conversion (an FP64-pipe instruction) is kept for
+//    subnormal results, overflow and NaN, in a function of its own so that it
+//    is not evaluated for every entry;
+//  - every remaining product and sum is issued as a fused multiply-add with
+//    an exact second operand: RN(a*b) = fma(a, b, -0) and RN(a+b) =
+//    fma(a, 1, b), identical to IEEE multiply and add including the signs of
+//    zero.  The FP64 pipe of this GPU retires DFMA at its full rate (2 per SM
+//    per clock) but DMUL and DADD several times more slowly.  The constants
+//    -0 and 1 arrive as kernel arguments so that the compiler cannot fold
+//    the fma back into a plain multiply or add.
 //
 // Bound: FP64 pipe (then HBM).  Algorithmic bytes per launch = 24 n^2 (read)
 // + 24 n^2 per frequency (16 written as float64 complex, 8 as float32 complex).
@@ -33,13 +43,15 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kMaxSlots = 64;
 
+__device__ __noinline__ float d2f_slow(double x) { return __double2float_rn(x); }
+
 // round-to-nearest-even float64 -> float32 from the bit pattern
 __device__ __forceinline__ float d2f_rn(double x) {
-    const unsigned long long b = (unsigned long long)__double_as_longlong(x);
-    const unsigned hi = (unsigned)(b >> 32), lo = (unsigned)b;
-    if ((b << 1) == 0) return __uint_as_float(hi & 0x80000000u);  // signed zero
+    const zs::Bits64 b = zs::bits_of(x);
+    const unsigned hi = b.hi, lo = b.lo;
+    if (zs::is_zero(b)) return __uint_as_float(hi & 0x80000000u);  // signed zero
     const unsigned e = (hi >> 20) & 0x7FFu;
-    if (e < 897u || e > 1150u) return __double2float_rn(x);  // subnormal result, overflow, inf/nan
+    if (e < 897u || e > 1150u) return d2f_slow(x);  // subnormal result, overflow, inf/nan
     const unsigned fm = ((hi & 0xFFFFFu) << 3) | (lo >> 29);  // top 23 mantissa bits
     const unsigned rest = lo & 0x1FFFFFFFu;                    // 29 bits rounded away
     unsigned f = ((e - 896u) << 23) | fm;
@@ -47,27 +59,36 @@ __device__ __forceinline__ float d2f_rn(double x) {
     return __uint_as_float(f | (hi & 0x80000000u));
 }
 
+// Exact-as-IEEE product and sum on the FMA path (mz = -0.0, one = 1.0 at run time)
+struct Fp64Ops {
+    double mz, one;
+    __device__ __forceinline__ double mul(double a, double b) const { return __fma_rn(a, b, mz); }
+    __device__ __forceinline__ double add(double a, double b) const { return __fma_rn(a, one, b); }
+    __device__ __forceinline__ double sub(double a, double b) const { return __fma_rn(-b, one, a); }
+};
+
 // Z64[e] and both float32 planes for one frequency
 __device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, double p, double g, bool gzero,
-                                          double2 *__restrict__ z64e, float *__restrict__ z32e, int64_t plane) {
+                                          double2 *__restrict__ z64e, float *__restrict__ z32e, int64_t plane,
+                                          const Fp64Ops &op) {
     const double w = sp.omega, r = sp.pad;  // pad holds RN(1/omega)
-    const double q0 = __dmul_rn(p, r);
+    const double q0 = op.mul(p, r);
     // RN(p / w); a zero first quotient is already exact (and keeps its sign)
-    const double q = (__double_as_longlong(q0) & 0x7FFFFFFFFFFFFFFFll) == 0 ? q0 : __fma_rn(__fma_rn(-w, q0, p), r, q0);
-    const double t = __dsub_rn(__dmul_rn(w, l), q);
+    const double q = zs::is_zero(zs::bits_of(q0)) ? q0 : __fma_rn(__fma_rn(-w, q0, p), r, q0);
+    const double t = op.sub(op.mul(w, l), q);
     double re, im;
     if (gzero) {
         // Zs.re * (+-0) and t + Zs.im * (+-0): exact zeros; only signs of zero to reproduce
-        const long long gs = __double_as_longlong(g) & (long long)0x8000000000000000ull;
-        const long long zr = (__double_as_longlong(sp.zs_re) & (long long)0x8000000000000000ull) ^ gs;
-        const long long zi = (__double_as_longlong(sp.zs_im) & (long long)0x8000000000000000ull) ^ gs;
-        re = __longlong_as_double(zr);
-        const long long tb = __double_as_longlong(t);
+        const unsigned gs = zs::bits_of(g).hi & 0x80000000u;
+        const unsigned zr = (zs::bits_of(sp.zs_re).hi & 0x80000000u) ^ gs;
+        const unsigned zi = (zs::bits_of(sp.zs_im).hi & 0x80000000u) ^ gs;
+        re = zs::double_of(0u, zr);
+        const zs::Bits64 tb = zs::bits_of(t);
         // t + z: equals t unless t is a zero; (-0) + (-0) = -0, any other pair of zeros = +0
-        im = ((tb & 0x7FFFFFFFFFFFFFFFll) != 0) ? t : __longlong_as_double(tb & zi);
+        im = zs::is_zero(tb) ? zs::double_of(0u, tb.hi & zi) : t;
     } else {
-        re = __dmul_rn(sp.zs_re, g);
-        im = __dadd_rn(t, __dmul_rn(sp.zs_im, g));
+        re = op.mul(sp.zs_re, g);
+        im = op.add(t, op.mul(sp.zs_im, g));
     }
     __stcs(z64e, make_double2(re, im));
     __stcs(z32e, d2f_rn(re));
@@ -77,8 +98,9 @@ __device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, doubl
 __global__ void __launch_bounds__(kThreads)
 k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const double *__restrict__ G, int64_t n,
            const ZsSlotParam *__restrict__ params, int nslot, double2 *__restrict__ z64, int64_t z64_stride,
-           float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride) {
+           float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, double mz, double one) {
     __shared__ ZsSlotParam sp[kMaxSlots];
+    const Fp64Ops op{mz, one};
     for (int s = threadIdx.x; s < nslot; s += blockDim.x) sp[s] = params[s];
     __syncthreads();
     for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
@@ -86,18 +108,18 @@ k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const d
         for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
             const int64_t e = row + j, o32 = row32 + j;
             const double l = __ldcs(L + e), p = __ldcs(Psi + e), g = __ldcs(G + e);
-            const bool gzero = (__double_as_longlong(g) & 0x7FFFFFFFFFFFFFFFll) == 0;
+            const bool gzero = zs::is_zero(zs::bits_of(g));
             // four frequencies at a time: independent FP64 chains to cover the unit's latency
             int s = 0;
 #pragma unroll 1
             for (; s + 4 <= nslot; s += 4) {
 #pragma unroll
                 for (int u = 0; u < 4; u++) one_entry(sp[s + u], l, p, g, gzero, z64 + (s + u) * z64_stride + e,
-                                                      z32 + (s + u) * z32_stride + o32, plane);
+                                                      z32 + (s + u) * z32_stride + o32, plane, op);
             }
 #pragma unroll 1
             for (; s < nslot; s++)
-                one_entry(sp[s], l, p, g, gzero, z64 + s * z64_stride + e, z32 + s * z32_stride + o32, plane);
+                one_entry(sp[s], l, p, g, gzero, z64 + s * z64_stride + e, z32 + s * z32_stride + o32, plane, op);
 
         }
     }
@@ -118,6 +140,6 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     k_assemble<<<(unsigned)blocks, kThreads, 0, st>>>(L, Psi, G, n, params, nslot, z64, z64_stride,
-                                                      z32, ld, plane, z32_stride);
+                                                      z32, ld, plane, z32_stride, -0.0, 1.0);
     return cudaGetLastError();
 }

@@ -40,6 +40,25 @@ __device__ __forceinline__ cf crecip(cf p) {
 
 __device__ __forceinline__ bool cfinite(cf a) { return isfinite(a.re) && isfinite(a.im); }
 
+// The two 32-bit halves of a double, moved out through PTX so that tests on
+// the bit pattern stay integer operations: written on a 64-bit integer, a
+// test such as "all bits but the sign are zero" may be turned back into a
+// floating-point compare, which on this GPU occupies the slow FP64 pipe.
+struct Bits64 {
+    unsigned lo, hi;
+};
+__device__ __forceinline__ Bits64 bits_of(double x) {
+    Bits64 b;
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(b.lo), "=r"(b.hi) : "d"(x));
+    return b;
+}
+__device__ __forceinline__ double double_of(unsigned lo, unsigned hi) {
+    double x;
+    asm("mov.b64 %0, {%1, %2};" : "=d"(x) : "r"(lo), "r"(hi));
+    return x;
+}
+__device__ __forceinline__ bool is_zero(Bits64 b) { return ((b.hi << 1) | b.lo) == 0u; }  // +0 or -0
+
 // Bounded wait until *flag == want.  Returns false (and raises the timeout bit
 // in *status) if it never happens within ZS_SPIN_LIMIT polls.
 __device__ __forceinline__ bool wait_flag(const unsigned *flag, unsigned want, unsigned *status) {

@@ -11,8 +11,10 @@
 // are all exact zeros (Re Z_ij = Zs.re G_ij vanishes wherever G_ij = 0) takes
 // a branch with two.  The skipped products are exact zeros added to the
 // running sums, so the float64 result is the one the four-DFMA sequence in
-// the same order gives (finite x).  Bound: HBM or the FP64
-// pipe, whichever is lower -- the kernel moves 16 n^2 bytes per frequency.
+// the same order gives (finite x).  The final sums are fma(a, 1, b), the same
+// rounding as an add: the FP64 pipe here retires DFMA several times faster
+// than DADD.  Bound: HBM or the FP64 pipe, whichever is lower -- the kernel
+// moves 16 n^2 bytes per frequency.
 //
 // k_update / k_relcorr: x (float64) += d (float32), and per (frequency, RHS)
 // ||d||_2 / ||x||_2 from per-block partial sums reduced in a fixed order, so
@@ -28,7 +30,7 @@ __global__ void __launch_bounds__(kResThreads)
 k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const double2 *__restrict__ b,
            const double2 *__restrict__ x, int64_t x_stride, float2 *__restrict__ out64,
            int64_t out64_stride, double2 *__restrict__ out128, int64_t out128_stride,
-           const int *__restrict__ slots) {
+           const int *__restrict__ slots, double one) {
     const int slot = slots[blockIdx.y];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t row = (int64_t)blockIdx.x * (kResThreads / 32) + warp;
@@ -55,7 +57,7 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
         // warp-uniform test: every real part in these 128 entries an exact zero
         bool re0 = true;
 #pragma unroll
-        for (int u = 0; u < 4; u++) re0 = re0 && ((__double_as_longlong(z[u].x) << 1) == 0);
+        for (int u = 0; u < 4; u++) re0 = re0 && zs::is_zero(zs::bits_of(z[u].x));
         if (__all_sync(0xffffffffu, re0)) {
 #pragma unroll
             for (int u = 0; u < 4; u++)
@@ -91,15 +93,16 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
     }
 #pragma unroll
     for (int r = 0; r < R; r++) {
+        // sums as fma(a, 1, b): the same rounding as an add, on the full-rate DFMA path
 #pragma unroll
         for (int u = 1; u < NA; u++) {
-            ar[0][r] += ar[u][r];
-            ai[0][r] += ai[u][r];
+            ar[0][r] = fma(ar[u][r], one, ar[0][r]);
+            ai[0][r] = fma(ai[u][r], one, ai[0][r]);
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-            ar[0][r] += __shfl_xor_sync(0xffffffffu, ar[0][r], o);
-            ai[0][r] += __shfl_xor_sync(0xffffffffu, ai[0][r], o);
+            ar[0][r] = fma(__shfl_xor_sync(0xffffffffu, ar[0][r], o), one, ar[0][r]);
+            ai[0][r] = fma(__shfl_xor_sync(0xffffffffu, ai[0][r], o), one, ai[0][r]);
         }
     }
     if (lane < R) {
@@ -235,7 +238,7 @@ void launch_res(const double2 *z64, int64_t z64_stride, int64_t n, const double2
                 int nslot, cudaStream_t st) {
     dim3 grid((unsigned)((n + 7) / 8), nslot);
     k_residual<R><<<grid, kResThreads, 0, st>>>(z64, z64_stride, n, b, x, x_stride, o64, o64s, o128, o128s,
-                                                slots);
+                                                slots, 1.0);
 }
 
 }  // namespace

@@ -28,8 +28,8 @@ constexpr int kResThreads = 256;  // 8 warps, one row each
 
 // z = hi + lo exactly up to the rounding of lo (relative 2^-47 of z).
 __device__ __forceinline__ void split_f64(double z, float &hi, float &lo) {
-    const unsigned long long b = (unsigned long long)__double_as_longlong(z);
-    const unsigned hw = (unsigned)(b >> 32), lw = (unsigned)b;
+    const zs::Bits64 b = zs::bits_of(z);
+    const unsigned hw = b.hi, lw = b.lo;
     const unsigned e = (hw >> 20) & 0x7FFu;
     if (e >= 950u && e <= 1150u) {
         const unsigned sign = hw & 0x80000000u;
@@ -38,7 +38,7 @@ __device__ __forceinline__ void split_f64(double z, float &hi, float &lo) {
         const float rem = __uint2float_rn(lw & 0x1FFFFFFFu);
         const float scale = __uint_as_float(sign | ((e - 1075u + 127u) << 23));
         lo = rem * scale;
-    } else if ((b << 1) == 0) {
+    } else if (zs::is_zero(b)) {
         hi = __uint_as_float(hw & 0x80000000u);
         lo = 0.f;
     } else {  // outside the fast range: exact split with float64 arithmetic
@@ -110,7 +110,7 @@ k_residual_df(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, co
 #pragma unroll
         for (int q = 0; q < kRowsPerWarp; q++)
 #pragma unroll
-            for (int u = 0; u < 4; u++) re0 = re0 && ((__double_as_longlong(z[q][u].x) << 1) == 0);
+            for (int u = 0; u < 4; u++) re0 = re0 && zs::is_zero(zs::bits_of(z[q][u].x));
         const bool skip = __all_sync(0xffffffffu, re0);
 #pragma unroll
         for (int u = 0; u < 4; u++) {
