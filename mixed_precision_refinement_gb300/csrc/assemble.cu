@@ -64,7 +64,7 @@ struct Fp64Ops {
     double mz, one;
     __device__ __forceinline__ double mul(double a, double b) const { return __fma_rn(a, b, mz); }
     __device__ __forceinline__ double add(double a, double b) const { return __fma_rn(a, one, b); }
-    __device__ __forceinline__ double sub(double a, double b) const { return __fma_rn(-b, one, a); }
+    __device__ __forceinline__ double sub(double a, double b) const { return __fma_rn(zs::neg_bits(b), one, a); }
 };
 
 // Z64[e] and both float32 planes for one frequency
@@ -74,7 +74,7 @@ __device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, doubl
     const double w = sp.omega, r = sp.pad;  // pad holds RN(1/omega)
     const double q0 = op.mul(p, r);
     // RN(p / w); a zero first quotient is already exact (and keeps its sign)
-    const double q = zs::is_zero(zs::bits_of(q0)) ? q0 : __fma_rn(__fma_rn(-w, q0, p), r, q0);
+    const double q = zs::is_zero(zs::bits_of(q0)) ? q0 : __fma_rn(__fma_rn(zs::neg_bits(w), q0, p), r, q0);
     const double t = op.sub(op.mul(w, l), q);
     double re, im;
     if (gzero) {

@@ -58,6 +58,11 @@ __device__ __forceinline__ double double_of(unsigned lo, unsigned hi) {
     return x;
 }
 __device__ __forceinline__ bool is_zero(Bits64 b) { return ((b.hi << 1) | b.lo) == 0u; }  // +0 or -0
+// -x by flipping the sign bit on the integer side (no FP64 instruction)
+__device__ __forceinline__ double neg_bits(double x) {
+    const Bits64 b = bits_of(x);
+    return double_of(b.lo, b.hi ^ 0x80000000u);
+}
 
 // Bounded wait until *flag == want.  Returns false (and raises the timeout bit
 // in *status) if it never happens within ZS_SPIN_LIMIT polls.
@@ -139,12 +144,16 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
 #define ZS_INV32_STRIDE (4 * 2 * 2 * 32 * 32)
 inline int64_t zs_inv32_slot_stride(int64_t n) { return ((n + 127) / 128) * ZS_INV32_STRIDE; }
 // Diagonal block at J (nb <= 128 columns, identity-padded to 128): its LU in
-// place in z32, the 32x32 sub-block inverses (inv32), the dense 128x128
-// inverses of L and U (dinv) and, if winv != NULL, their operand packs
-// (mode 1: tf32 hi; 2: hi + lo).  pivflag[slot] = 1 on a tiny or non-finite pivot.
+// place in z32 and the 32x32 sub-block inverses (inv32).  pivflag[slot] = 1
+// on a tiny or non-finite pivot.
 cudaError_t zs_launch_diag_block(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
                                  const int *slots, int nslot, int *pivflag, float *inv32, int64_t inv32_stride,
-                                 float *dinv, int64_t dinv_stride, float *winv, int mode, cudaStream_t st);
+                                 cudaStream_t st);
+// The dense 128x128 inverses of the block's L and U (dinv) from the factor and
+// inv32 and, if winv != NULL, their operand packs (mode 1: tf32 hi; 2: hi + lo).
+cudaError_t zs_launch_block_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
+                                const int *slots, int nslot, const float *inv32, int64_t inv32_stride, float *dinv,
+                                int64_t dinv_stride, float *winv, int mode, cudaStream_t st);
 // mode: 0 = pack plain fp32 (FFMA), 1 = tf32 rounded (TF32), 2 = tf32 hi + lo (TF32X3)
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                              int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
@@ -170,14 +179,15 @@ cudaError_t zs_tc_pack_map(const float *pack, int64_t n, int nslots, int64_t pac
 cudaError_t zs_tc_winv_map(const float *winv, int nslots, void *map_out);
 cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane, int nslots, int64_t z32_stride,
                           void *map_out);
-// A22 -= L21 U12 for every listed slot (split: 3xTF32)
+// A22 -= L21 U12 for every listed slot (split: 3xTF32), at most max_grid
+// persistent CTAs that take tiles from *ctr (zero before the launch).
 cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
-                               int nslot, unsigned *status, int num_sms, cudaStream_t st);
+                               int nslot, unsigned *ctr, unsigned *status, int max_grid, cudaStream_t st);
 // L21 = A21 U11^-1 and U12 = L11^-1 A12 from the packs of zs_launch_pack_trsm
 // and zs_launch_diag_block; writes L21, U12 into z32 and their operand packs
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
-                              int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
-                              cudaStream_t st);
+                              int64_t J, int split, const int *slots, int nslot, unsigned *ctr, unsigned *status,
+                              int num_sms, cudaStream_t st);
 
 // Pack layout (floats), per slot: six planes of n rows x 2*NB:
 //   A_hi, A_lo, Br_hi, Br_lo, Bi_hi, Bi_lo

@@ -64,7 +64,7 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
 #pragma unroll
                 for (int r = 0; r < R; r++) {
                     const double2 xv = __ldg(xs + r * n + j + 32 * u);
-                    ar[u % NA][r] = fma(-z[u].y, xv.y, ar[u % NA][r]);
+                    ar[u % NA][r] = fma(zs::neg_bits(z[u].y), xv.y, ar[u % NA][r]);
                     ai[u % NA][r] = fma(z[u].y, xv.x, ai[u % NA][r]);
                 }
         } else {
@@ -75,7 +75,7 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
                     const double2 xv = __ldg(xs + r * n + j + 32 * u);
                     ar[u % NA][r] = fma(z[u].x, xv.x, ar[u % NA][r]);
                     ai[u % NA][r] = fma(z[u].x, xv.y, ai[u % NA][r]);
-                    ar[u % NA][r] = fma(-z[u].y, xv.y, ar[u % NA][r]);
+                    ar[u % NA][r] = fma(zs::neg_bits(z[u].y), xv.y, ar[u % NA][r]);
                     ai[u % NA][r] = fma(z[u].y, xv.x, ai[u % NA][r]);
                 }
         }
@@ -87,7 +87,7 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
             const double2 xv = __ldg(xs + r * n + j);
             ar[0][r] = fma(z.x, xv.x, ar[0][r]);
             ai[0][r] = fma(z.x, xv.y, ai[0][r]);
-            ar[0][r] = fma(-z.y, xv.y, ar[0][r]);
+            ar[0][r] = fma(zs::neg_bits(z.y), xv.y, ar[0][r]);
             ai[0][r] = fma(z.y, xv.x, ai[0][r]);
         }
     }

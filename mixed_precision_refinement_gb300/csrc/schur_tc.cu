@@ -62,6 +62,7 @@ constexpr int A_BYTES = TM * KC * 4;       // 16 KB
 constexpr int B_BYTES = 2 * TN * KC * 4;   // 32 KB (Br rows then Bi rows)
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kTq = 8;  // tile-index queue between the roles (the producer runs at most a few tiles ahead)
 
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
 // inverse packs: W = U11^-1 in planes 0-3, V = L11^-1 in planes 4-7 (Br hi, Br lo, Bi hi, Bi lo)
@@ -251,9 +252,14 @@ struct Tile {
 };
 
 template <int KIND>
+__host__ __device__ __forceinline__ int tiles_per_slot(int tiles) {
+    return KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles;
+}
+
+template <int KIND>
 __device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const int *slots) {
     Tile x;
-    const int per_slot = KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles;
+    const int per_slot = tiles_per_slot<KIND>(tiles);
     const int si = t / per_slot, rem = t - si * per_slot;
     x.slot = slots[si];
     if (KIND == KIND_SCHUR) {
@@ -275,10 +281,12 @@ template <int SPLIT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap wmap,
            const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap pmap, int64_t n, int64_t J,
-           const int *__restrict__ slots, int nslot, unsigned *__restrict__ status) {
+           const int *__restrict__ slots, int nslot, unsigned *__restrict__ ctr, unsigned *__restrict__ status) {
     using C = Cfg<SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[C::STAGES], bar_empty[C::STAGES], bar_accf[2], bar_acce[2], bar_drain;
+    __shared__ __align__(8) uint64_t bar_tq[kTq];
+    __shared__ volatile int s_tq[kTq];  // tile of local tile it at it % kTq; -1 ends the sequence
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     const uint32_t base_addr = (smem_u32(smem_raw) + 1023u) & ~1023u;
@@ -287,8 +295,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
     const int64_t base = J + NB;
     const int64_t m2 = n - base;
     const int tiles = (int)((m2 + TM - 1) / TM);
-    const int per_slot = KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles;
-    const int total = per_slot * nslot;
+    const int total = tiles_per_slot<KIND>(tiles) * nslot;
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -301,6 +308,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
             mbar_init(smem_u32(&bar_acce[b]), 4);
         }
         mbar_init(smem_u32(&bar_drain), 1);
+        for (int q = 0; q < kTq; q++) mbar_init(smem_u32(&bar_tq[q]), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == 1) {
@@ -319,9 +327,24 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
             if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&wmap) : "memory");
-            uint32_t g = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+            // Tiles are taken dynamically: the first is blockIdx.x, the next
+            // ones come from the launch's counter, so CTAs that start late
+            // (the SMs busy with another stream's kernel) simply take fewer.
+            // Each tile index is published in the queue before its loads; the
+            // end of the sequence (-1) occupies one stage with a plain arrive.
+            uint32_t g = 0, it = 0;
+            int t = (int)blockIdx.x;
+            while (true) {
+                if (t >= total) t = -1;
+                const uint32_t st0 = g % C::STAGES, ph0 = (g / C::STAGES) & 1u;
+                if (!mbar_wait(smem_u32(&bar_empty[st0]), ph0 ^ 1u, &s_abort, status)) break;
+                s_tq[it % kTq] = t;
+                mbar_arrive(smem_u32(&bar_tq[it % kTq]));
+                if (t < 0) {
+                    mbar_arrive(smem_u32(&bar_full[st0]));
+                    g++;
+                    break;
+                }
                 const Tile x = tile_of<KIND>(t, tiles, base, slots);
                 // A rows: L21 / A21 (A planes) or A12^T (Br planes); B: the pack's
                 // own Br/Bi rows, or W / V from the inverse packs
@@ -329,9 +352,10 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 const CUtensorMap *bm = KIND == KIND_SCHUR ? &tmap : &wmap;
                 const int pbr = KIND == KIND_SCHUR ? PL_BR_HI : (x.u ? WP_V : 0) + WP_BR_HI;
                 const int pbi = KIND == KIND_SCHUR ? PL_BI_HI : (x.u ? WP_V : 0) + WP_BI_HI;
+                bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
-                    if (!mbar_wait(smem_u32(&bar_empty[st]), ph ^ 1u, &s_abort, status)) {
+                    if (kc > 0 && !mbar_wait(smem_u32(&bar_empty[st]), ph ^ 1u, &s_abort, status)) {
                         ok = false;
                         break;
                     }
@@ -349,6 +373,9 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                         tma_load_4d(sl + A_BYTES + B_BYTES / 2, bm, k0, x.rb, pbi + 1, x.slot, fb);
                     }
                 }
+                if (!ok) break;
+                it++;
+                t = (int)gridDim.x + (int)atomicAdd(ctr, 1u);
             }
             // our own copies in flight: wait (bounded) for the last stages to land
             const uint32_t issued = g;
@@ -363,18 +390,23 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         // ------------------------------------------------ MMA issuer
         if (lane == 0) {
             uint32_t g = 0, it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < total && ok; t += gridDim.x, it++) {
-                const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&bar_acce[buf]), aph ^ 1u, &s_abort, status)) {
-                    ok = false;
+            while (true) {
+                // the first stage of the next tile (or the end marker) tells which
+                const uint32_t st0 = g % C::STAGES, ph0 = (g / C::STAGES) & 1u;
+                if (!mbar_wait(smem_u32(&bar_full[st0]), ph0, &s_abort, status)) break;
+                if (s_tq[it % kTq] < 0) {
+                    g++;
+                    mbar_arrive(smem_u32(&bar_accf[it & 1u]));  // the epilogue's turn to see the end
                     break;
                 }
+                const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
+                if (!mbar_wait(smem_u32(&bar_acce[buf]), aph ^ 1u, &s_abort, status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * 256u;
+                bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
-                    if (!mbar_wait(smem_u32(&bar_full[st]), ph, &s_abort, status)) {
+                    if (kc > 0 && !mbar_wait(smem_u32(&bar_full[st]), ph, &s_abort, status)) {
                         ok = false;
                         break;
                     }
@@ -400,6 +432,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 }
                 if (!ok) break;
                 mma_commit(smem_u32(&bar_accf[buf]));  // accumulator ready
+                it++;
             }
             // drain: every MMA issued so far completes before TMEM is freed
             mma_commit(smem_u32(&bar_drain));
@@ -430,10 +463,13 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&cmap) : "memory");
             if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&pmap) : "memory");
         }
-        for (int t = blockIdx.x; t < total; t += gridDim.x, it++) {
+        for (;; it++) {
+            const bool okq = mbar_wait(smem_u32(&bar_tq[it % kTq]), (it / kTq) & 1u, &s_abort, status);
+            if (!__all_sync(0xffffffffu, okq)) break;
+            const int t = s_tq[it % kTq];
             const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
             const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status);
-            if (!__all_sync(0xffffffffu, ok)) break;
+            if (!__all_sync(0xffffffffu, ok) || t < 0) break;
             tc_fence_after();
             const Tile x = tile_of<KIND>(t, tiles, base, slots);
             const int row0 = x.ra + quad * 32;  // this warp's 32 output rows
@@ -528,8 +564,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 template <int SPLIT, int KIND>
 cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const CUtensorMap &cmap,
-                        const CUtensorMap &pmap, int64_t n, int64_t J, const int *slots, int nslot, unsigned *status,
-                        int num_sms, cudaStream_t st) {
+                        const CUtensorMap &pmap, int64_t n, int64_t J, const int *slots, int nslot, unsigned *ctr,
+                        unsigned *status, int max_grid, cudaStream_t st) {
     using C = Cfg<SPLIT>;
     static bool init = false;
     if (!init) {
@@ -540,10 +576,12 @@ cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const 
     }
     const int64_t m2 = n - J - NB;
     if (m2 <= 0 || nslot <= 0) return cudaSuccess;
-    const int64_t tiles = (m2 + TM - 1) / TM;
-    const int64_t total = (KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles) * nslot;
-    const int grid = (int)(total < num_sms ? total : num_sms);
-    k_cgemm_tc<SPLIT, KIND><<<grid, kThreads, C::SMEM, st>>>(tmap, wmap, cmap, pmap, n, J, slots, nslot, status);
+    const int tiles = (int)((m2 + TM - 1) / TM);
+    const int64_t total = (int64_t)tiles_per_slot<KIND>(tiles) * nslot;
+    if (total <= 0) return cudaSuccess;
+    const int grid = (int)(total < max_grid ? total : max_grid);
+    k_cgemm_tc<SPLIT, KIND><<<grid, kThreads, C::SMEM, st>>>(tmap, wmap, cmap, pmap, n, J, slots, nslot, ctr,
+                                                             status);
     return cudaGetLastError();
 }
 
@@ -591,20 +629,22 @@ cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane
 }
 
 cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
-                               int nslot, unsigned *status, int num_sms, cudaStream_t st) {
+                               int nslot, unsigned *ctr, unsigned *status, int max_grid, cudaStream_t st) {
+    if (max_grid < 1 || !ctr) return cudaErrorInvalidValue;
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
     const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
-    if (split) return launch_kind<1, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, status, num_sms, st);
-    return launch_kind<0, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, status, num_sms, st);
+    if (split) return launch_kind<1, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
+    return launch_kind<0, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
 }
 
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
-                              int64_t J, int split, const int *slots, int nslot, unsigned *status, int num_sms,
-                              cudaStream_t st) {
+                              int64_t J, int split, const int *slots, int nslot, unsigned *ctr, unsigned *status,
+                              int num_sms, cudaStream_t st) {
+    if (!ctr) return cudaErrorInvalidValue;
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
     const CUtensorMap &w = *reinterpret_cast<const CUtensorMap *>(wmap);
     const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
     const CUtensorMap &p = *reinterpret_cast<const CUtensorMap *>(pmap);
-    if (split) return launch_kind<1, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, status, num_sms, st);
-    return launch_kind<0, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, status, num_sms, st);
+    if (split) return launch_kind<1, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
+    return launch_kind<0, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
 }

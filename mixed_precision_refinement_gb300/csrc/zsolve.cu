@@ -75,6 +75,7 @@ struct zsolve_ctx {
     // side stream: packs the next block solves' operands while the diagonal block is factored
     cudaStream_t side = nullptr;
     cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+    unsigned *tile_ctr = nullptr;  // dynamic tile counters of the tcgen05 launches
     int assembled = 0, factored = 0, fb_ready = 0;
     // stage profile: launch counts always, event-timed spans with opts.profile
     int64_t prof_launches[ZSOLVE_NSTAGE] = {};
@@ -146,11 +147,12 @@ cudaEvent_t prof_take(zsolve_ctx *ctx) {
 struct StageSpan {
     zsolve_ctx *c;
     int stage;
+    cudaStream_t s;
     cudaEvent_t a = nullptr;
-    StageSpan(zsolve_ctx *ctx, int st) : c(ctx), stage(st) {
+    StageSpan(zsolve_ctx *ctx, int st, cudaStream_t on = nullptr) : c(ctx), stage(st), s(on ? on : ctx->stream) {
         if (c->opts.profile) {
             a = prof_take(c);
-            if (a) cudaEventRecord(a, c->stream);
+            if (a) cudaEventRecord(a, s);
         }
     }
     void done(int64_t launches) {
@@ -158,7 +160,7 @@ struct StageSpan {
         if (a) {
             cudaEvent_t b = prof_take(c);
             if (b) {
-                cudaEventRecord(b, c->stream);
+                cudaEventRecord(b, s);
                 c->pending.push_back({stage, a, b});
             } else {
                 c->ev_pool.push_back(a);
@@ -184,58 +186,91 @@ size_t slot_bytes(int64_t n, int64_t ld) {
 
 // ------------------------------------------------------------------ factor
 
-int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
+// FP32 (FFMA) path: the steps one after another
+int factor_slots_simt(zsolve_ctx *ctx, const int *slots, int nslot) {
     const int64_t n = ctx->n;
-    const int mode = gemm_mode(ctx->opts);
     const int64_t inv32_stride = zs_inv32_slot_stride(n);
-    ZS_CU(cudaMemsetAsync(ctx->d_pivflag, 0, sizeof(int) * ctx->S, ctx->stream));
+    for (int64_t J = 0; J < n; J += ZS_NB) {
+        const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
+            ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
+                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->stream));
+            ZS_CU(zs_launch_block_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot, ctx->inv32,
+                                      inv32_stride, ctx->dinv, ctx->dinv_stride, nullptr, 0, ctx->stream));
+            sp.done(2);
+        }
+        if (J + nb >= n) break;
+        {
+            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
+            ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, inv32_stride,
+                                   ctx->pack, ctx->pack_stride, 0, slots, nslot, ctx->stream));
+            ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, inv32_stride,
+                                   ctx->pack, ctx->pack_stride, 0, slots, nslot, ctx->stream));
+            sp.done(2);
+        }
+        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
+        ZS_CU(zs_launch_schur_simt(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack, ctx->pack_stride,
+                                   slots, nslot, ctx->stream));
+        sp.done(1);
+    }
+    return ZSOLVE_OK;
+}
+
+// Tensor-core path, one outer block after the other.  The operand packs of
+// A21 and A12^T do not depend on the diagonal block, so they are written on
+// the side stream while the diagonal block is factored; the tcgen05 block
+// solves wait for both.  The tcgen05 kernels take tiles from per-launch
+// counters (zeroed once per factorisation).
+constexpr int kMaxCtr = 256;  // tile counters per factorisation (2 per outer block)
+
+int factor_slots_tc(zsolve_ctx *ctx, const int *slots, int nslot) {
+    const int64_t n = ctx->n;
+    const int mode = gemm_mode(ctx->opts), split = mode == 2 ? 1 : 0;
+    const int64_t inv32_stride = zs_inv32_slot_stride(n);
+    if (2 * ((n + ZS_NB - 1) / ZS_NB) > kMaxCtr) return fail(ctx, ZSOLVE_EINVAL, "n too large for the tile counters");
+    ZS_CU(cudaMemsetAsync(ctx->tile_ctr, 0, kMaxCtr * sizeof(unsigned), ctx->stream));
+    unsigned *ctr = ctx->tile_ctr;
     for (int64_t J = 0; J < n; J += ZS_NB) {
         const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
         const bool last = J + nb >= n;
-        if (mode != 0 && !last) {
-            // A21 and A12^T do not depend on the diagonal block: pack them on
-            // the side stream while it is factored
+        if (!last) {
             ZS_CU(cudaEventRecord(ctx->ev_fork, ctx->stream));
             ZS_CU(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0));
+            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ctx->side);
             ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
                                       ctx->pack_stride, mode, slots, nslot, ctx->side));
+            sp.done(1);
             ZS_CU(cudaEventRecord(ctx->ev_join, ctx->side));
-            ctx->prof_launches[ZSOLVE_STAGE_TRSM]++;
         }
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
-            // the block's factors, its 32x32 and 128x128 inverses and, for the
-            // tensor-core solves that multiply by them, their operand packs
             ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
-                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->dinv, ctx->dinv_stride,
-                                       (mode != 0 && !last) ? ctx->winv : nullptr, mode, ctx->stream));
+                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->stream));
+            ZS_CU(zs_launch_block_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot, ctx->inv32,
+                                      inv32_stride, ctx->dinv, ctx->dinv_stride, last ? nullptr : ctx->winv, mode,
+                                      ctx->stream));
             sp.done(2);
         }
         if (last) break;
         {
+            ZS_CU(cudaStreamWaitEvent(ctx->stream, ctx->ev_join, 0));
             StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
-            if (mode == 0) {
-                ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
-                                       inv32_stride, ctx->pack, ctx->pack_stride, mode, slots, nslot, ctx->stream));
-                ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32,
-                                       inv32_stride, ctx->pack, ctx->pack_stride, mode, slots, nslot, ctx->stream));
-            } else {
-                ZS_CU(cudaStreamWaitEvent(ctx->stream, ctx->ev_join, 0));  // the operand packs, from the side stream
-                ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J,
-                                        mode == 2 ? 1 : 0, slots, nslot, ctx->d_status, ctx->num_sms, ctx->stream));
-            }
-            sp.done(mode == 0 ? 2 : 1);
+            ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J, split, slots,
+                                    nslot, ctr++, ctx->d_status, ctx->num_sms, ctx->stream));
+            sp.done(1);
         }
         StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
-        if (mode == 0)
-            ZS_CU(zs_launch_schur_simt(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                                       ctx->pack_stride, slots, nslot, ctx->stream));
-        else
-            ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, mode == 2 ? 1 : 0, slots, nslot,
-                                     ctx->d_status, ctx->num_sms, ctx->stream));
+        ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, split, slots, nslot, ctr++, ctx->d_status,
+                                 ctx->num_sms, ctx->stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
+}
+
+int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
+    ZS_CU(cudaMemsetAsync(ctx->d_pivflag, 0, sizeof(int) * ctx->S, ctx->stream));
+    return gemm_mode(ctx->opts) == 0 ? factor_slots_simt(ctx, slots, nslot) : factor_slots_tc(ctx, slots, nslot);
 }
 
 // ------------------------------------------------------------------ solves
@@ -531,6 +566,7 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->dinv);
     cudaFree(c->inv32);
     cudaFree(c->winv);
+    cudaFree(c->tile_ctr);
     cudaFree(c->v);
     cudaFree(c->xs);
     cudaFree(c->partials);
@@ -637,6 +673,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
     ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
     if (gemm_mode(ctx->opts) != 0) ALLOC(ctx->winv, (size_t)S * ZS_WINV_STRIDE * sizeof(float));
+    ALLOC(ctx->tile_ctr, kMaxCtr * sizeof(unsigned));
     ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
     ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
     ALLOC(ctx->d_relcorr, (size_t)S * nrhs_max * sizeof(double));
