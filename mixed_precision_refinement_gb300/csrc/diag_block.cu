@@ -466,12 +466,9 @@ cudaError_t zs_launch_diag_block(float *z32, int64_t ld, int64_t plane, int64_t 
                                  const int *slots, int nslot, int *pivflag, float *inv32, int64_t inv32_stride,
                                  cudaStream_t st) {
     if (nb <= 0 || nb > NB || nslot <= 0) return cudaErrorInvalidValue;
-    static bool init = false;
-    if (!init) {
-        cudaError_t e = cudaFuncSetAttribute(k_diag_block, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
-        if (e != cudaSuccess) return e;
-        init = true;
-    }
+    // once per process (thread-safe initialisation of a local static)
+    static const cudaError_t attr = cudaFuncSetAttribute(k_diag_block, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (attr != cudaSuccess) return attr;
     k_diag_block<<<nslot, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag, inv32,
                                                        inv32_stride);
     return cudaGetLastError();
@@ -482,12 +479,9 @@ cudaError_t zs_launch_block_inv(const float *z32, int64_t ld, int64_t plane, int
                                 int64_t dinv_stride, float *winv, int mode, cudaStream_t st) {
     if (nb <= 0 || nb > NB || nslot <= 0) return cudaErrorInvalidValue;
     if (winv && mode != 1 && mode != 2) return cudaErrorInvalidValue;
-    static bool init = false;
-    if (!init) {
-        cudaError_t e = cudaFuncSetAttribute(k_block_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kInvSmemBytes);
-        if (e != cudaSuccess) return e;
-        init = true;
-    }
+    // once per process (thread-safe initialisation of a local static)
+    static const cudaError_t attr = cudaFuncSetAttribute(k_block_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kInvSmemBytes);
+    if (attr != cudaSuccess) return attr;
     k_block_inv<<<dim3(8, nslot), kThreads, kInvSmemBytes, st>>>(z32, ld, plane, z32_stride, J, nb, inv32,
                                                                   inv32_stride, dinv, dinv_stride, winv, mode, slots);
     return cudaGetLastError();

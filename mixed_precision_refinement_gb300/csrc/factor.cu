@@ -427,12 +427,9 @@ cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_
                              int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
                              int mode, const int *slots, int nslot, cudaStream_t st) {
     const size_t smem = (2 * NB * NB) * sizeof(float) + 16 * 8 * 32 * sizeof(cf);
-    static bool init = false;
-    if (!init) {
-        cudaError_t e = set_smem(k_trsm_l, smem);
-        if (e != cudaSuccess) return e;
-        init = true;
-    }
+    // once per process (thread-safe initialisation of a local static)
+    static const cudaError_t attr = set_smem(k_trsm_l, smem);
+    if (attr != cudaSuccess) return attr;
     const int64_t m2 = n - J - NB;
     dim3 grid((unsigned)((m2 + kTLRows - 1) / kTLRows), nslot);
     k_trsm_l<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, inv32_stride, pack,
@@ -444,12 +441,9 @@ cudaError_t zs_launch_trsm_u(float *z32, int64_t ld, int64_t plane, int64_t z32_
                              int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,
                              int mode, const int *slots, int nslot, cudaStream_t st) {
     const size_t smem = (2 * NB * LDS + 2 * NB * kTUPad) * sizeof(float) + 16 * 4 * 32 * sizeof(cf);
-    static bool init = false;
-    if (!init) {
-        cudaError_t e = set_smem(k_trsm_u, smem);
-        if (e != cudaSuccess) return e;
-        init = true;
-    }
+    // once per process (thread-safe initialisation of a local static)
+    static const cudaError_t attr = set_smem(k_trsm_u, smem);
+    if (attr != cudaSuccess) return attr;
     const int64_t m2 = n - J - NB;
     dim3 grid((unsigned)((m2 + kTUCols - 1) / kTUCols), nslot);
     k_trsm_u<<<grid, kTrsmThreads, smem, st>>>(z32, ld, plane, z32_stride, n, J, inv32, inv32_stride, pack,

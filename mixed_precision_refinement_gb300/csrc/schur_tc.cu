@@ -567,13 +567,9 @@ cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const 
                         const CUtensorMap &pmap, int64_t n, int64_t J, const int *slots, int nslot, unsigned *ctr,
                         unsigned *status, int max_grid, cudaStream_t st) {
     using C = Cfg<SPLIT>;
-    static bool init = false;
-    if (!init) {
-        cudaError_t e =
-            cudaFuncSetAttribute(k_cgemm_tc<SPLIT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-        if (e != cudaSuccess) return e;
-        init = true;
-    }
+    // once per process (thread-safe initialisation of a local static)
+    static const cudaError_t attr = cudaFuncSetAttribute(k_cgemm_tc<SPLIT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (attr != cudaSuccess) return attr;
     const int64_t m2 = n - J - NB;
     if (m2 <= 0 || nslot <= 0) return cudaSuccess;
     const int tiles = (int)((m2 + TM - 1) / TM);

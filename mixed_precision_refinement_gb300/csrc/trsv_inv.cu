@@ -233,11 +233,12 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
     if (grid > tasks) grid = tasks;
     e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
     if (e != cudaSuccess) return e;
-    void *args[] = {(void *)&z32, (void *)&ld,          (void *)&plane, (void *)&z32_stride, (void *)&n,
-                    (void *)&dinv, (void *)&dinv_stride, (void *)&v,     (void *)&v_stride,   (void *)&slots,
-                    (void *)&nslot, (void *)&prog,       (void *)&epoch, (void *)&ticket,     (void *)&status};
-    e = cudaLaunchCooperativeKernel((const void *)k_trsv_inv<R>, dim3((unsigned)grid), dim3(kThreads), args, 0, st);
-    if (e != cudaSuccess) return e;
+    // A plain launch: a task waits only on tasks with smaller tickets, which
+    // CTAs that are already running have claimed, so the solve progresses
+    // with any number of resident CTAs -- also while another stream's kernels
+    // hold part of the GPU.
+    k_trsv_inv<R><<<(unsigned)grid, kThreads, 0, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride,
+                                                       slots, nslot, prog, epoch, ticket, status);
     return cudaGetLastError();
 }
 

@@ -16,13 +16,20 @@
 // A sweep factors `batch` frequencies together: every launch of the
 // factorisation, the solves and the residual covers all of them, so the
 // panel and triangular-solve latencies of one frequency overlap with the
-// work of the others.
+// work of the others.  A batch is further split into two lanes -- each with
+// its own stream, scratch and host thread -- that run assembly,
+// factorisation and refinement side by side: the FP64-pipe-bound kernels of
+// one lane (assembly, residual) fill the SMs the other lane leaves idle
+// (diagonal blocks on one SM per frequency, tensor-core phases).
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
+#include <mutex>
+#include <thread>
 #include <vector>
 
 #include "../../include/zsolve.h"
@@ -56,12 +63,10 @@ struct zsolve_ctx {
     double *d_relcorr = nullptr, *h_relcorr = nullptr;
     ZsSlotParam *d_params = nullptr, *h_params = nullptr;
     int *d_all = nullptr;    // 0..S-1
-    int *d_active = nullptr, *h_active = nullptr;
     int *d_pivflag = nullptr, *h_pivflag = nullptr;
     unsigned long long *prog = nullptr;  // triangular-solve progress words, 2 per slot
-    unsigned epoch = 0;
-    unsigned *ticket = nullptr;
-    unsigned *d_status = nullptr, *h_status = nullptr;
+    std::atomic<unsigned> epoch{0};      // triangular-solve launches, unique across lanes
+    unsigned *d_status = nullptr;
     // fallback workspace (allocated on first use)
     double2 *fb_a = nullptr;
     int64_t *fb_piv = nullptr;
@@ -71,12 +76,24 @@ struct zsolve_ctx {
     double2 *hd_b = nullptr, *hd_x = nullptr;
     size_t hd_x_cap = 0;
     int hd_nrhs_cap = 0;
-    cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
-    // side stream: packs the next block solves' operands while the diagonal block is factored
-    cudaStream_t side = nullptr;
-    cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
-    unsigned *tile_ctr = nullptr;  // dynamic tile counters of the tcgen05 launches
+    // A lane: one group of a batch's frequencies, run on its own stream with
+    // its own scratch (lane 0 on the context's stream; lane 1, for batches of
+    // two or more, on a second stream driven by a second host thread).
+    struct Lane {
+        cudaStream_t stream = nullptr;  // lane 0: the context's stream
+        cudaStream_t side = nullptr;    // packs the next block solves' operands next to the diagonal block
+        bool own_stream = false;
+        cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+        cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+        int *d_active = nullptr, *h_active = nullptr;  // slots still refining
+        unsigned *ticket = nullptr;     // triangular-solve task tickets
+        unsigned *tile_ctr = nullptr;   // tile counters of the tcgen05 launches
+        unsigned *h_status = nullptr;   // pinned copy of the device status word
+        int tc_grid = 0;                // CTAs of this lane's tcgen05 launches
+    };
+    Lane lane[2];
     int assembled = 0, factored = 0, fb_ready = 0;
+    std::mutex err_mu, prof_mu, fb_mu;  // error text; profile records; fallback workspace
     // stage profile: launch counts always, event-timed spans with opts.profile
     int64_t prof_launches[ZSOLVE_NSTAGE] = {};
     double prof_ms[ZSOLVE_NSTAGE] = {};
@@ -93,6 +110,7 @@ namespace {
 
 int fail(zsolve_ctx *c, int code, const char *fmt, ...) {
     if (c) {
+        std::lock_guard<std::mutex> lock(c->err_mu);
         va_list ap;
         va_start(ap, fmt);
         vsnprintf(c->err, sizeof(c->err), fmt, ap);
@@ -117,7 +135,7 @@ int fail(zsolve_ctx *c, int code, const char *fmt, ...) {
 
 // ------------------------------------------------------------------ stage profile
 
-int prof_resolve(zsolve_ctx *ctx) {
+int prof_resolve_locked(zsolve_ctx *ctx) {
     for (auto &sp : ctx->pending) {
         ZS_CU(cudaEventSynchronize(sp.b));
         float ms = 0.f;
@@ -130,8 +148,13 @@ int prof_resolve(zsolve_ctx *ctx) {
     return ZSOLVE_OK;
 }
 
-cudaEvent_t prof_take(zsolve_ctx *ctx) {
-    if (ctx->ev_pool.empty() && ctx->pending.size() >= 4096) prof_resolve(ctx);
+int prof_resolve(zsolve_ctx *ctx) {
+    std::lock_guard<std::mutex> lock(ctx->prof_mu);
+    return prof_resolve_locked(ctx);
+}
+
+cudaEvent_t prof_take_locked(zsolve_ctx *ctx) {
+    if (ctx->ev_pool.empty() && ctx->pending.size() >= 4096) prof_resolve_locked(ctx);
     if (!ctx->ev_pool.empty()) {
         cudaEvent_t e = ctx->ev_pool.back();
         ctx->ev_pool.pop_back();
@@ -143,22 +166,24 @@ cudaEvent_t prof_take(zsolve_ctx *ctx) {
 }
 
 // Brackets the launches of one stage: counts them and, with opts.profile,
-// records a pair of events around them on the context's stream.
+// records a pair of events around them on the stream they go to.
 struct StageSpan {
     zsolve_ctx *c;
     int stage;
     cudaStream_t s;
     cudaEvent_t a = nullptr;
-    StageSpan(zsolve_ctx *ctx, int st, cudaStream_t on = nullptr) : c(ctx), stage(st), s(on ? on : ctx->stream) {
+    StageSpan(zsolve_ctx *ctx, int st, cudaStream_t on) : c(ctx), stage(st), s(on) {
         if (c->opts.profile) {
-            a = prof_take(c);
+            std::lock_guard<std::mutex> lock(c->prof_mu);
+            a = prof_take_locked(c);
             if (a) cudaEventRecord(a, s);
         }
     }
     void done(int64_t launches) {
+        std::lock_guard<std::mutex> lock(c->prof_mu);
         c->prof_launches[stage] += launches;
         if (a) {
-            cudaEvent_t b = prof_take(c);
+            cudaEvent_t b = prof_take_locked(c);
             if (b) {
                 cudaEventRecord(b, s);
                 c->pending.push_back({stage, a, b});
@@ -169,6 +194,8 @@ struct StageSpan {
         }
     }
 };
+
+using Lane = zsolve_ctx::Lane;
 
 int gemm_mode(const zsolve_opts &o) {
     switch (o.gemm) {
@@ -187,31 +214,31 @@ size_t slot_bytes(int64_t n, int64_t ld) {
 // ------------------------------------------------------------------ factor
 
 // FP32 (FFMA) path: the steps one after another
-int factor_slots_simt(zsolve_ctx *ctx, const int *slots, int nslot) {
+int factor_slots_simt(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     const int64_t n = ctx->n;
     const int64_t inv32_stride = zs_inv32_slot_stride(n);
     for (int64_t J = 0; J < n; J += ZS_NB) {
         const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
         {
-            StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
+            StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, ln.stream);
             ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
-                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->stream));
+                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ln.stream));
             ZS_CU(zs_launch_block_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot, ctx->inv32,
-                                      inv32_stride, ctx->dinv, ctx->dinv_stride, nullptr, 0, ctx->stream));
+                                      inv32_stride, ctx->dinv, ctx->dinv_stride, nullptr, 0, ln.stream));
             sp.done(2);
         }
         if (J + nb >= n) break;
         {
-            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
+            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.stream);
             ZS_CU(zs_launch_trsm_l(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, inv32_stride,
-                                   ctx->pack, ctx->pack_stride, 0, slots, nslot, ctx->stream));
+                                   ctx->pack, ctx->pack_stride, 0, slots, nslot, ln.stream));
             ZS_CU(zs_launch_trsm_u(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->inv32, inv32_stride,
-                                   ctx->pack, ctx->pack_stride, 0, slots, nslot, ctx->stream));
+                                   ctx->pack, ctx->pack_stride, 0, slots, nslot, ln.stream));
             sp.done(2);
         }
-        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
+        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR, ln.stream);
         ZS_CU(zs_launch_schur_simt(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack, ctx->pack_stride,
-                                   slots, nslot, ctx->stream));
+                                   slots, nslot, ln.stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
@@ -224,80 +251,82 @@ int factor_slots_simt(zsolve_ctx *ctx, const int *slots, int nslot) {
 // counters (zeroed once per factorisation).
 constexpr int kMaxCtr = 256;  // tile counters per factorisation (2 per outer block)
 
-int factor_slots_tc(zsolve_ctx *ctx, const int *slots, int nslot) {
+int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     const int64_t n = ctx->n;
     const int mode = gemm_mode(ctx->opts), split = mode == 2 ? 1 : 0;
     const int64_t inv32_stride = zs_inv32_slot_stride(n);
     if (2 * ((n + ZS_NB - 1) / ZS_NB) > kMaxCtr) return fail(ctx, ZSOLVE_EINVAL, "n too large for the tile counters");
-    ZS_CU(cudaMemsetAsync(ctx->tile_ctr, 0, kMaxCtr * sizeof(unsigned), ctx->stream));
-    unsigned *ctr = ctx->tile_ctr;
+    ZS_CU(cudaMemsetAsync(ln.tile_ctr, 0, kMaxCtr * sizeof(unsigned), ln.stream));
+    unsigned *ctr = ln.tile_ctr;
     for (int64_t J = 0; J < n; J += ZS_NB) {
         const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
         const bool last = J + nb >= n;
         if (!last) {
-            ZS_CU(cudaEventRecord(ctx->ev_fork, ctx->stream));
-            ZS_CU(cudaStreamWaitEvent(ctx->side, ctx->ev_fork, 0));
-            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ctx->side);
+            ZS_CU(cudaEventRecord(ln.ev_fork, ln.stream));
+            ZS_CU(cudaStreamWaitEvent(ln.side, ln.ev_fork, 0));
+            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.side);
             ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                                      ctx->pack_stride, mode, slots, nslot, ctx->side));
+                                      ctx->pack_stride, mode, slots, nslot, ln.side));
             sp.done(1);
-            ZS_CU(cudaEventRecord(ctx->ev_join, ctx->side));
+            ZS_CU(cudaEventRecord(ln.ev_join, ln.side));
         }
         {
-            StageSpan sp(ctx, ZSOLVE_STAGE_DIAG);
+            StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, ln.stream);
             ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
-                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->stream));
+                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ln.stream));
             ZS_CU(zs_launch_block_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot, ctx->inv32,
                                       inv32_stride, ctx->dinv, ctx->dinv_stride, last ? nullptr : ctx->winv, mode,
-                                      ctx->stream));
+                                      ln.stream));
             sp.done(2);
         }
         if (last) break;
         {
-            ZS_CU(cudaStreamWaitEvent(ctx->stream, ctx->ev_join, 0));
-            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM);
+            ZS_CU(cudaStreamWaitEvent(ln.stream, ln.ev_join, 0));
+            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.stream);
             ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J, split, slots,
-                                    nslot, ctr++, ctx->d_status, ctx->num_sms, ctx->stream));
+                                    nslot, ctr++, ctx->d_status, ln.tc_grid, ln.stream));
             sp.done(1);
         }
-        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR);
+        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR, ln.stream);
         ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, split, slots, nslot, ctr++, ctx->d_status,
-                                 ctx->num_sms, ctx->stream));
+                                 ln.tc_grid, ln.stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
 }
 
-int factor_slots(zsolve_ctx *ctx, const int *slots, int nslot) {
-    ZS_CU(cudaMemsetAsync(ctx->d_pivflag, 0, sizeof(int) * ctx->S, ctx->stream));
-    return gemm_mode(ctx->opts) == 0 ? factor_slots_simt(ctx, slots, nslot) : factor_slots_tc(ctx, slots, nslot);
+// slots: device list of nslot slot indices, the first of which is `first`
+// with the rest following it (the lane's range)
+int factor_slots(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot, int first) {
+    ZS_CU(cudaMemsetAsync(ctx->d_pivflag + first, 0, sizeof(int) * nslot, ln.stream));
+    return gemm_mode(ctx->opts) == 0 ? factor_slots_simt(ctx, ln, slots, nslot) : factor_slots_tc(ctx, ln, slots, nslot);
 }
 
 // ------------------------------------------------------------------ solves
 
 // v <- (LU)^-1 v for the listed slots, right-hand sides in chunks of 4/2/1
-int lowprec_solve_slots(zsolve_ctx *ctx, int nrhs, const int *slots, int nslot) {
+int lowprec_solve_slots(zsolve_ctx *ctx, Lane &ln, int nrhs, const int *slots, int nslot) {
     int r0 = 0;
     while (r0 < nrhs) {
         const int left = nrhs - r0;
         const int R = left >= 4 ? 4 : left >= 2 ? 2 : 1;
-        ctx->epoch++;
-        StageSpan sp(ctx, ZSOLVE_STAGE_TRSV);
+        const unsigned epoch = ctx->epoch.fetch_add(1u) + 1u;
+        StageSpan sp(ctx, ZSOLVE_STAGE_TRSV, ln.stream);
         ZS_CU(zs_launch_trsv_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->dinv, ctx->dinv_stride,
-                                 ctx->v + (int64_t)r0 * ctx->n, ctx->v_stride, R, slots, nslot, ctx->prog, ctx->epoch,
-                                 ctx->ticket, ctx->d_status, ctx->num_sms, ctx->stream));
+                                 ctx->v + (int64_t)r0 * ctx->n, ctx->v_stride, R, slots, nslot, ctx->prog, epoch,
+                                 ln.ticket, ctx->d_status, ctx->num_sms, ln.stream));
         sp.done(1);
         r0 += R;
     }
     return ZSOLVE_OK;
 }
 
-int check_device_status(zsolve_ctx *ctx) {
-    ZS_CU(cudaMemcpyAsync(ctx->h_status, ctx->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost, ctx->stream));
-    ZS_CU(cudaStreamSynchronize(ctx->stream));
-    if (*ctx->h_status & ZS_DEV_TIMEOUT) {
-        *ctx->h_status = 0;
-        ZS_CU(cudaMemsetAsync(ctx->d_status, 0, sizeof(unsigned), ctx->stream));
+int check_device_status(zsolve_ctx *ctx, Lane &ln) {
+    ZS_CU(cudaMemcpyAsync(ln.h_status, ctx->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost, ln.stream));
+    ZS_CU(cudaStreamSynchronize(ln.stream));
+    if (*ln.h_status & ZS_DEV_TIMEOUT) {
+        *ln.h_status = 0;
+        ZS_CU(cudaMemsetAsync(ctx->d_status, 0, sizeof(unsigned), ln.stream));
         return fail(ctx, ZSOLVE_ETIMEOUT, "a bounded device-side wait gave up (triangular solve or trailing update)");
     }
     return ZSOLVE_OK;
@@ -317,46 +346,50 @@ int ensure_fallback(zsolve_ctx *ctx) {
     return ZSOLVE_OK;
 }
 
-// x (nrhs x n, device) = Z64[slot]^-1 b by the float64 pivoted LU
-int fallback_slot(zsolve_ctx *ctx, int slot, const double2 *b, double2 *x, int nrhs) {
+// x (nrhs x n, device) = Z64[slot]^-1 b by the float64 pivoted LU (one
+// workspace per context: the lanes take turns)
+int fallback_slot(zsolve_ctx *ctx, Lane &ln, int slot, const double2 *b, double2 *x, int nrhs) {
+    std::lock_guard<std::mutex> lock(ctx->fb_mu);
     ZS_TRY(ensure_fallback(ctx));
     const int64_t n = ctx->n;
     ZS_CU(cudaMemcpyAsync(ctx->fb_a, ctx->z64 + (int64_t)slot * ctx->z64_stride, (size_t)n * n * sizeof(double2),
-                          cudaMemcpyDeviceToDevice, ctx->stream));
+                          cudaMemcpyDeviceToDevice, ln.stream));
     int64_t cnt = 0;
-    StageSpan sp(ctx, ZSOLVE_STAGE_FALLBACK);
-    ZS_CU(zs_lu64_factor(ctx->fb_a, n, ctx->fb_piv, ctx->fb_info, ctx->stream, &cnt));
+    StageSpan sp(ctx, ZSOLVE_STAGE_FALLBACK, ln.stream);
+    ZS_CU(zs_lu64_factor(ctx->fb_a, n, ctx->fb_piv, ctx->fb_info, ln.stream, &cnt));
     sp.done(cnt);
-    ZS_CU(cudaMemcpyAsync(ctx->h_fb_info, ctx->fb_info, sizeof(int), cudaMemcpyDeviceToHost, ctx->stream));
-    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    ZS_CU(cudaMemcpyAsync(ctx->h_fb_info, ctx->fb_info, sizeof(int), cudaMemcpyDeviceToHost, ln.stream));
+    ZS_CU(cudaStreamSynchronize(ln.stream));
     if (*ctx->h_fb_info != 0)
         return fail(ctx, ZSOLVE_ESINGULAR, "double-precision LU: zero pivot column at %d", *ctx->h_fb_info - 1);
     if (x != b)
-        ZS_CU(cudaMemcpyAsync(x, b, (size_t)nrhs * n * sizeof(double2), cudaMemcpyDeviceToDevice, ctx->stream));
+        ZS_CU(cudaMemcpyAsync(x, b, (size_t)nrhs * n * sizeof(double2), cudaMemcpyDeviceToDevice, ln.stream));
     cnt = 0;
-    StageSpan sp2(ctx, ZSOLVE_STAGE_FALLBACK);
+    StageSpan sp2(ctx, ZSOLVE_STAGE_FALLBACK, ln.stream);
     for (int r0 = 0; r0 < nrhs; r0 += 32)
-        ZS_CU(zs_lu64_solve(ctx->fb_a, n, ctx->fb_piv, x + (int64_t)r0 * n, std::min(32, nrhs - r0), ctx->stream,
+        ZS_CU(zs_lu64_solve(ctx->fb_a, n, ctx->fb_piv, x + (int64_t)r0 * n, std::min(32, nrhs - r0), ln.stream,
                             &cnt));
     sp2.done(cnt);
+    ZS_CU(cudaStreamSynchronize(ln.stream));  // the workspace is free for the other lane only when done
     return ZSOLVE_OK;
 }
 
 // r = b - Z x for the listed slots in the context's residual arithmetic.
-int residual_slots(zsolve_ctx *ctx, const double2 *b, const double2 *x, int64_t x_stride, int nrhs, float2 *o64,
-                   int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot, StageSpan *sp) {
+int residual_slots(zsolve_ctx *ctx, Lane &ln, const double2 *b, const double2 *x, int64_t x_stride, int nrhs,
+                   float2 *o64, int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot,
+                   StageSpan *sp) {
     const int64_t n = ctx->n;
     if (ctx->resid_mode == ZSOLVE_RESID_DF) {
         const int64_t xs_stride = (int64_t)ctx->nrhs_max * n;
-        ZS_CU(zs_launch_split_x(x, x_stride, n, nrhs, ctx->xs, xs_stride, slots, nslot, ctx->stream));
+        ZS_CU(zs_launch_split_x(x, x_stride, n, nrhs, ctx->xs, xs_stride, slots, nslot, ln.stream));
         ZS_CU(zs_launch_residual_df(ctx->z64, ctx->z64_stride, n, b, ctx->xs, xs_stride, nrhs, o64, o64s, o128, o128s,
-                                    slots, nslot, ctx->stream));
+                                    slots, nslot, ln.stream));
         int chunks = 0;
         for (int r = nrhs; r > 0; chunks++) r -= r >= 4 ? 4 : r >= 2 ? 2 : 1;
         sp->done(1 + chunks);
     } else {
         ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, b, x, x_stride, nrhs, o64, o64s, o128, o128s, slots,
-                                 nslot, ctx->stream));
+                                 nslot, ln.stream));
         sp->done(zs_rhs_chunks(nrhs));
     }
     return ZSOLVE_OK;
@@ -378,16 +411,16 @@ int resid_selftest(zsolve_ctx *ctx) {
         return fail(ctx, ZSOLVE_ENOMEM, "residual self-test buffers");
     }
     for (int zero_re = 0; zero_re < 2 && ok; zero_re++) {
-        ZS_CU(cudaMemsetAsync(tb, 0, n * sizeof(double2), ctx->stream));
-        ZS_CU(zs_launch_selftest_fill(ctx->z64, tx, n, zero_re, ctx->stream));
+        ZS_CU(cudaMemsetAsync(tb, 0, n * sizeof(double2), ctx->lane[0].stream));
+        ZS_CU(zs_launch_selftest_fill(ctx->z64, tx, n, zero_re, ctx->lane[0].stream));
         ZS_CU(zs_launch_residual(ctx->z64, ctx->z64_stride, n, tb, tx, 0, 1, nullptr, 0, tr, 0, ctx->d_all, 1,
-                                 ctx->stream));
-        ZS_CU(zs_launch_split_x(tx, 0, n, 1, ctx->xs, 0, ctx->d_all, 1, ctx->stream));
+                                 ctx->lane[0].stream));
+        ZS_CU(zs_launch_split_x(tx, 0, n, 1, ctx->xs, 0, ctx->d_all, 1, ctx->lane[0].stream));
         ZS_CU(zs_launch_residual_df(ctx->z64, ctx->z64_stride, n, tb, ctx->xs, 0, 1, nullptr, 0, tr + n, 0, ctx->d_all,
-                                    1, ctx->stream));
-        ZS_CU(cudaMemcpyAsync(h1.data(), tr, n * sizeof(double2), cudaMemcpyDeviceToHost, ctx->stream));
-        ZS_CU(cudaMemcpyAsync(h2.data(), tr + n, n * sizeof(double2), cudaMemcpyDeviceToHost, ctx->stream));
-        ZS_CU(cudaStreamSynchronize(ctx->stream));
+                                    1, ctx->lane[0].stream));
+        ZS_CU(cudaMemcpyAsync(h1.data(), tr, n * sizeof(double2), cudaMemcpyDeviceToHost, ctx->lane[0].stream));
+        ZS_CU(cudaMemcpyAsync(h2.data(), tr + n, n * sizeof(double2), cudaMemcpyDeviceToHost, ctx->lane[0].stream));
+        ZS_CU(cudaStreamSynchronize(ctx->lane[0].stream));
         double err = 0.0, scale = 0.0;
         for (int64_t i = 0; i < n; i++) {
             err = std::max(err, std::max(fabs(h1[i].x - h2[i].x), fabs(h1[i].y - h2[i].y)));
@@ -402,26 +435,29 @@ int resid_selftest(zsolve_ctx *ctx) {
     return ZSOLVE_OK;
 }
 
-// Refinement of slots 0..count-1 with x for slot s at x + s*x_stride.
-int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride, int nrhs, int count,
-                 zsolve_info *info) {
+// Refinement of slots first..first+count-1 on lane ln; x for slot s is at
+// x + s*x_stride (x is the batch's base).
+int refine_batch(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *x, int64_t x_stride, int nrhs, int first,
+                 int count, zsolve_info *info) {
     const int64_t n = ctx->n;
     const zsolve_opts &o = ctx->opts;
-    std::vector<int> active, stalled;
+    std::vector<int> active, stalled;  // slot indices
     std::vector<double> prev(count, INFINITY), last(count, 1.0);
     std::vector<int> grow(count, 0), iters(count, 0);
     // slots whose factorisation met a bad pivot go straight to the fallback
-    ZS_CU(cudaMemcpyAsync(ctx->h_pivflag, ctx->d_pivflag, sizeof(int) * count, cudaMemcpyDeviceToHost, ctx->stream));
-    ZS_CU(cudaStreamSynchronize(ctx->stream));
-    for (int s = 0; s < count; s++) {
-        if (info) info[s].pivot_flag = ctx->h_pivflag[s];
+    ZS_CU(cudaMemcpyAsync(ctx->h_pivflag + first, ctx->d_pivflag + first, sizeof(int) * count,
+                          cudaMemcpyDeviceToHost, ln.stream));
+    ZS_CU(cudaStreamSynchronize(ln.stream));
+    for (int i = 0; i < count; i++) {
+        const int s = first + i;
+        if (info) info[i].pivot_flag = ctx->h_pivflag[s];
         if (ctx->h_pivflag[s] || o.force_fallback) stalled.push_back(s);
         else active.push_back(s);
     }
     auto upload_active = [&]() -> int {
-        for (size_t i = 0; i < active.size(); i++) ctx->h_active[i] = active[i];
-        ZS_CU(cudaMemcpyAsync(ctx->d_active, ctx->h_active, sizeof(int) * active.size(), cudaMemcpyHostToDevice,
-                              ctx->stream));
+        for (size_t i = 0; i < active.size(); i++) ln.h_active[i] = active[i];
+        ZS_CU(cudaMemcpyAsync(ln.d_active, ln.h_active, sizeof(int) * active.size(), cudaMemcpyHostToDevice,
+                              ln.stream));
         return ZSOLVE_OK;
     };
     if (!active.empty()) {
@@ -429,39 +465,39 @@ int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride
         const int na = (int)active.size();
         // step 2: first solve with the low-precision factors
         {
-            StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
-            ZS_CU(zs_launch_cast_rhs(b, n, nrhs, ctx->v, ctx->v_stride, ctx->d_active, na, ctx->stream));
+            StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE, ln.stream);
+            ZS_CU(zs_launch_cast_rhs(b, n, nrhs, ctx->v, ctx->v_stride, ln.d_active, na, ln.stream));
             sp.done(1);
         }
-        ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_active, na));
-        StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
+        ZS_TRY(lowprec_solve_slots(ctx, ln, nrhs, ln.d_active, na));
+        StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE, ln.stream);
         ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 1, ctx->partials, ctx->nchunks,
-                               ctx->d_active, na, ctx->stream));
+                               ln.d_active, na, ln.stream));
         sp.done(1);
     }
     for (int it = 1; it <= o.max_iter && !active.empty(); it++) {
         const int na = (int)active.size();
         // step 3: residual in double precision, rounded for the low-precision solve
         {
-            StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL);
-            ZS_TRY(residual_slots(ctx, b, x, x_stride, nrhs, ctx->v, ctx->v_stride, nullptr, 0, ctx->d_active, na,
+            StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL, ln.stream);
+            ZS_TRY(residual_slots(ctx, ln, b, x, x_stride, nrhs, ctx->v, ctx->v_stride, nullptr, 0, ln.d_active, na,
                                   &sp));
         }
         // step 4: correction and update
-        ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_active, na));
+        ZS_TRY(lowprec_solve_slots(ctx, ln, nrhs, ln.d_active, na));
         {
-            StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
+            StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE, ln.stream);
             ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 0, ctx->partials, ctx->nchunks,
-                                   ctx->d_active, na, ctx->stream));
-            ZS_CU(zs_launch_relcorr(ctx->partials, ctx->nchunks, nrhs, ctx->d_relcorr, ctx->d_active, na,
-                                    ctx->stream));
+                                   ln.d_active, na, ln.stream));
+            ZS_CU(zs_launch_relcorr(ctx->partials, ctx->nchunks, nrhs, ctx->d_relcorr, ln.d_active, na, ln.stream));
             sp.done(2);
         }
-        ZS_CU(cudaMemcpyAsync(ctx->h_relcorr, ctx->d_relcorr, sizeof(double) * (size_t)count * nrhs,
-                              cudaMemcpyDeviceToHost, ctx->stream));
-        ZS_TRY(check_device_status(ctx));  // synchronises
+        ZS_CU(cudaMemcpyAsync(ctx->h_relcorr + (int64_t)first * nrhs, ctx->d_relcorr + (int64_t)first * nrhs,
+                              sizeof(double) * (size_t)count * nrhs, cudaMemcpyDeviceToHost, ln.stream));
+        ZS_TRY(check_device_status(ctx, ln));  // synchronises
         std::vector<int> next;
         for (int s : active) {
+            const int i = s - first;
             double rc = 0.0;
             bool bad = false;
             for (int r = 0; r < nrhs; r++) {
@@ -469,16 +505,16 @@ int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride
                 if (!isfinite(v)) bad = true;
                 else rc = std::max(rc, v);
             }
-            iters[s] = it;
-            last[s] = bad ? NAN : rc;
+            iters[i] = it;
+            last[i] = bad ? NAN : rc;
             if (bad) {
                 stalled.push_back(s);
                 continue;
             }
             if (rc < o.tol) continue;  // converged
-            grow[s] = (rc > prev[s]) ? grow[s] + 1 : 0;
-            prev[s] = rc;
-            if (grow[s] >= 2) stalled.push_back(s);  // diverging
+            grow[i] = (rc > prev[i]) ? grow[i] + 1 : 0;
+            prev[i] = rc;
+            if (grow[i] >= 2) stalled.push_back(s);  // diverging
             else next.push_back(s);
         }
         active.swap(next);
@@ -486,19 +522,20 @@ int refine_batch(zsolve_ctx *ctx, const double2 *b, double2 *x, int64_t x_stride
     }
     for (int s : active) stalled.push_back(s);  // not converged after max_iter corrections
     std::sort(stalled.begin(), stalled.end());
-    for (int s = 0; s < count; s++)
+    for (int i = 0; i < count; i++)
         if (info) {
-            info[s].iters = iters[s];
-            info[s].relcorr = last[s];
-            info[s].fallback = 0;
-            info[s].status = ZSOLVE_OK;
+            info[i].iters = iters[i];
+            info[i].relcorr = last[i];
+            info[i].fallback = 0;
+            info[i].status = ZSOLVE_OK;
         }
     for (int s : stalled) {
-        int st = fallback_slot(ctx, s, b, x + (int64_t)s * x_stride, nrhs);
+        const int i = s - first;
+        int st = fallback_slot(ctx, ln, s, b, x + (int64_t)s * x_stride, nrhs);
         if (info) {
-            info[s].fallback = 1;
-            info[s].status = st;
-            info[s].relcorr = 0.0;
+            info[i].fallback = 1;
+            info[i].status = st;
+            info[i].relcorr = 0.0;
         }
         if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
         if (st == ZSOLVE_ESINGULAR && !info) return st;
@@ -512,12 +549,55 @@ int check_nrhs(zsolve_ctx *ctx, int nrhs) {
     return ZSOLVE_OK;
 }
 
+// Assembly of one lane's share of a batch: slots first..first+count-1.
+int assemble_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi, const double *G, int first,
+                  int count) {
+    ZS_CU(cudaEventRecord(ln.ev[0], ln.stream));
+    StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE, ln.stream);
+    ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, ctx->d_params + first, count,
+                             ctx->z64 + (int64_t)first * ctx->z64_stride, ctx->z64_stride,
+                             ctx->z32 + (int64_t)first * ctx->z32_stride, ctx->ld, ctx->plane, ctx->z32_stride,
+                             ln.stream));
+    sp.done(1);
+    ZS_CU(cudaEventRecord(ln.ev[1], ln.stream));
+    return ZSOLVE_OK;
+}
+
+// One lane's share of a batch (frequencies f0+first.. of the sweep),
+// assembled unless `assembled`, then factored and refined on ln's stream.
+// xb and ib are the batch's base (slot 0).
+int run_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi, const double *G, const double2 *b,
+             double2 *xb, int nrhs, int first, int count, zsolve_info *ib, bool assembled) {
+    const int64_t n = ctx->n;
+    if (!assembled) ZS_TRY(assemble_lane(ctx, ln, L, Psi, G, first, count));
+    ZS_TRY(factor_slots(ctx, ln, ctx->d_all + first, count, first));
+    ZS_CU(cudaEventRecord(ln.ev[2], ln.stream));
+    zsolve_info *inf = ib ? ib + first : nullptr;
+    const int st = refine_batch(ctx, ln, b, xb, (int64_t)nrhs * n, nrhs, first, count, inf);
+    if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
+    ZS_CU(cudaEventRecord(ln.ev[3], ln.stream));
+    ZS_CU(cudaEventSynchronize(ln.ev[3]));
+    if (inf) {
+        float a = 0, fct = 0, r = 0;
+        cudaEventElapsedTime(&a, ln.ev[0], ln.ev[1]);
+        cudaEventElapsedTime(&fct, ln.ev[1], ln.ev[2]);
+        cudaEventElapsedTime(&r, ln.ev[2], ln.ev[3]);
+        for (int i = 0; i < count; i++) {
+            inf[i].ms_assemble = a / count;
+            inf[i].ms_factor = fct / count;
+            inf[i].ms_refine = r / count;
+        }
+    }
+    return st;
+}
+
 int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const double *omega,
                const double *zs, int nf, const double2 *b, double2 *x, int nrhs, zsolve_info *info) {
     const int64_t n = ctx->n;
     for (int f = 0; f < nf; f++)
         if (!(omega[f] > 0.0) || !isfinite(omega[f]) || !isfinite(zs[2 * f]) || !isfinite(zs[2 * f + 1]))
             return fail(ctx, ZSOLVE_EINVAL, "frequency %d: omega must be positive and finite, Zs finite", f);
+    Lane &l0 = ctx->lane[0], &l1 = ctx->lane[1];
     int first_err = ZSOLVE_OK;
     for (int f0 = 0; f0 < nf; f0 += ctx->S) {
         const int count = std::min(ctx->S, nf - f0);
@@ -525,34 +605,52 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
             ctx->h_params[s] =
                 ZsSlotParam{omega[f0 + s], zs[2 * (f0 + s)], zs[2 * (f0 + s) + 1], 1.0 / omega[f0 + s]};
         ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam) * count, cudaMemcpyHostToDevice,
-                              ctx->stream));
-        ZS_CU(cudaEventRecord(ctx->ev[0], ctx->stream));
-        {
-            StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE);
-            ZS_CU(zs_launch_assemble(L, Psi, G, n, ctx->d_params, count, ctx->z64, ctx->z64_stride, ctx->z32,
-                                     ctx->ld, ctx->plane, ctx->z32_stride, ctx->stream));
-            sp.done(1);
+                              l0.stream));
+        double2 *xb = x + (int64_t)f0 * nrhs * n;
+        zsolve_info *ib = info ? info + f0 : nullptr;
+        int st;
+        if (ctx->opts.lanes == 1 || count < 2) {
+            l0.tc_grid = ctx->num_sms;
+            st = run_lane(ctx, l0, L, Psi, G, b, xb, nrhs, 0, count, ib, false);
+        } else {
+            // lane 1 starts after lane 0's assembly (and everything queued
+            // before it on the context's stream: inputs, parameters), so that
+            // its own FP64-bound assembly runs under lane 0's factorisation and
+            // the two lanes' outer-block steps stay out of phase; the
+            // context's stream continues only after lane 1 has finished
+            const int h = (count + 1) / 2;
+            // each lane's persistent tcgen05 grids leave room for the other
+            // lane's diagonal blocks (one CTA per frequency)
+            l0.tc_grid = std::max(1, ctx->num_sms - (count - h));
+            l1.tc_grid = std::max(1, ctx->num_sms - h);
+            ZS_TRY(assemble_lane(ctx, l0, L, Psi, G, 0, h));
+            ZS_CU(cudaEventRecord(l0.ev_fork, l0.stream));
+            ZS_CU(cudaStreamWaitEvent(l1.stream, l0.ev_fork, 0));
+            int st1 = ZSOLVE_OK;
+            auto lane1 = [&]() {
+                if (cudaSetDevice(ctx->device) != cudaSuccess) {
+                    st1 = fail(ctx, ZSOLVE_ECUDA, "second lane: cudaSetDevice failed");
+                    return;
+                }
+                st1 = run_lane(ctx, l1, L, Psi, G, b, xb, nrhs, h, count - h, ib, false);
+            };
+            std::thread worker;
+            bool threaded = true;
+            try {
+                worker = std::thread(lane1);
+            } catch (...) {
+                threaded = false;  // no thread: the lanes run one after the other
+            }
+            const int st0 = run_lane(ctx, l0, L, Psi, G, b, xb, nrhs, 0, h, ib, true);
+            if (threaded) worker.join();
+            else lane1();
+            ZS_CU(cudaEventRecord(l1.ev_join, l1.stream));
+            ZS_CU(cudaStreamWaitEvent(l0.stream, l1.ev_join, 0));
+            const bool hard0 = st0 != ZSOLVE_OK && st0 != ZSOLVE_ESINGULAR;
+            st = hard0 ? st0 : (st1 != ZSOLVE_OK ? st1 : st0);
         }
-        ZS_CU(cudaEventRecord(ctx->ev[1], ctx->stream));
-        ZS_TRY(factor_slots(ctx, ctx->d_all, count));
-        ZS_CU(cudaEventRecord(ctx->ev[2], ctx->stream));
-        zsolve_info *inf = info ? info + f0 : nullptr;
-        int st = refine_batch(ctx, b, x + (int64_t)f0 * nrhs * n, (int64_t)nrhs * n, nrhs, count, inf);
         if (st != ZSOLVE_OK && first_err == ZSOLVE_OK) first_err = st;
         if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
-        ZS_CU(cudaEventRecord(ctx->ev[3], ctx->stream));
-        ZS_CU(cudaEventSynchronize(ctx->ev[3]));
-        if (info) {
-            float a = 0, fct = 0, r = 0;
-            cudaEventElapsedTime(&a, ctx->ev[0], ctx->ev[1]);
-            cudaEventElapsedTime(&fct, ctx->ev[1], ctx->ev[2]);
-            cudaEventElapsedTime(&r, ctx->ev[2], ctx->ev[3]);
-            for (int s = 0; s < count; s++) {
-                info[f0 + s].ms_assemble = a / count;
-                info[f0 + s].ms_factor = fct / count;
-                info[f0 + s].ms_refine = r / count;
-            }
-        }
     }
     ctx->assembled = 0;  // slot 0 now holds the last batch's first frequency, not a single system
     ctx->factored = 0;
@@ -566,7 +664,6 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->dinv);
     cudaFree(c->inv32);
     cudaFree(c->winv);
-    cudaFree(c->tile_ctr);
     cudaFree(c->v);
     cudaFree(c->xs);
     cudaFree(c->partials);
@@ -575,14 +672,10 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->d_params);
     cudaFreeHost(c->h_params);
     cudaFree(c->d_all);
-    cudaFree(c->d_active);
-    cudaFreeHost(c->h_active);
     cudaFree(c->d_pivflag);
     cudaFreeHost(c->h_pivflag);
     cudaFree(c->prog);
-    cudaFree(c->ticket);
     cudaFree(c->d_status);
-    cudaFreeHost(c->h_status);
     cudaFree(c->fb_a);
     cudaFree(c->fb_piv);
     cudaFree(c->fb_info);
@@ -592,8 +685,19 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->hd_G);
     cudaFree(c->hd_b);
     cudaFree(c->hd_x);
-    for (auto &e : c->ev)
-        if (e) cudaEventDestroy(e);
+    for (auto &ln : c->lane) {
+        cudaFree(ln.d_active);
+        cudaFreeHost(ln.h_active);
+        cudaFree(ln.ticket);
+        cudaFree(ln.tile_ctr);
+        cudaFreeHost(ln.h_status);
+        for (auto &e : ln.ev)
+            if (e) cudaEventDestroy(e);
+        if (ln.ev_fork) cudaEventDestroy(ln.ev_fork);
+        if (ln.ev_join) cudaEventDestroy(ln.ev_join);
+        if (ln.side) cudaStreamDestroy(ln.side);
+        if (ln.own_stream && ln.stream) cudaStreamDestroy(ln.stream);
+    }
     for (auto &sp : c->pending) {
         cudaEventDestroy(sp.a);
         cudaEventDestroy(sp.b);
@@ -601,9 +705,6 @@ void free_all(zsolve_ctx *c) {
     for (auto e : c->ev_pool) cudaEventDestroy(e);
     c->pending.clear();
     c->ev_pool.clear();
-    if (c->ev_fork) cudaEventDestroy(c->ev_fork);
-    if (c->ev_join) cudaEventDestroy(c->ev_join);
-    if (c->side) cudaStreamDestroy(c->side);
 }
 
 }  // namespace
@@ -620,6 +721,7 @@ int zsolve_default_opts(zsolve_opts *opts) {
     opts->force_fallback = 0;
     opts->profile = 0;
     opts->resid = ZSOLVE_RESID_F64;
+    opts->lanes = 0;
     return ZSOLVE_OK;
 }
 
@@ -633,7 +735,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (ctx->opts.outer_block == 0) ctx->opts.outer_block = ZS_NB;
     if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
         ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0 || ctx->opts.resid < 0 ||
-        ctx->opts.resid > ZSOLVE_RESID_DF) {
+        ctx->opts.resid > ZSOLVE_RESID_DF || ctx->opts.lanes < 0 || ctx->opts.lanes > 2) {
         delete ctx;
         return ZSOLVE_EINVAL;
     }
@@ -673,7 +775,6 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
     ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
     if (gemm_mode(ctx->opts) != 0) ALLOC(ctx->winv, (size_t)S * ZS_WINV_STRIDE * sizeof(float));
-    ALLOC(ctx->tile_ctr, kMaxCtr * sizeof(unsigned));
     ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
     ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
     ALLOC(ctx->d_relcorr, (size_t)S * nrhs_max * sizeof(double));
@@ -681,22 +782,35 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->d_params, S * sizeof(ZsSlotParam));
     ALLOCH(ctx->h_params, S * sizeof(ZsSlotParam));
     ALLOC(ctx->d_all, S * sizeof(int));
-    ALLOC(ctx->d_active, S * sizeof(int));
-    ALLOCH(ctx->h_active, S * sizeof(int));
     ALLOC(ctx->d_pivflag, S * sizeof(int));
     ALLOCH(ctx->h_pivflag, S * sizeof(int));
     ALLOC(ctx->prog, (size_t)S * 2 * sizeof(unsigned long long));
-    ALLOC(ctx->ticket, sizeof(unsigned));
     ALLOC(ctx->d_status, sizeof(unsigned));
-    ALLOCH(ctx->h_status, sizeof(unsigned));
+    for (int l = 0; l < 2; l++) {
+        Lane &ln = ctx->lane[l];
+        ALLOC(ln.d_active, S * sizeof(int));
+        ALLOCH(ln.h_active, S * sizeof(int));
+        ALLOC(ln.ticket, sizeof(unsigned));
+        ALLOC(ln.tile_ctr, kMaxCtr * sizeof(unsigned));
+        ALLOCH(ln.h_status, sizeof(unsigned));
+        *ln.h_status = 0;
+    }
 #undef ALLOC
 #undef ALLOCH
-    for (auto &e : ctx->ev)
-        if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
-    if (cudaStreamCreateWithFlags(&ctx->side, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ctx->ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&ctx->ev_join, cudaEventDisableTiming) != cudaSuccess)
+    for (int l = 0; l < 2; l++) {
+        Lane &ln = ctx->lane[l];
+        for (auto &e : ln.ev)
+            if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
+        if (cudaStreamCreateWithFlags(&ln.side, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ln.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ln.ev_join, cudaEventDisableTiming) != cudaSuccess)
+            return bail(ZSOLVE_ECUDA);
+    }
+    if (cudaStreamCreateWithFlags(&ctx->lane[1].stream, cudaStreamNonBlocking) != cudaSuccess)
         return bail(ZSOLVE_ECUDA);
+    ctx->lane[1].own_stream = true;
+    ctx->lane[0].stream = ctx->stream;
+    ctx->lane[0].tc_grid = ctx->lane[1].tc_grid = ctx->num_sms;
     if (gemm_mode(ctx->opts) != 0 &&
         (zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 128, ctx->pack_map) != cudaSuccess ||
          zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 32, ctx->packst_map) != cudaSuccess ||
@@ -711,7 +825,6 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
         cudaMemset(ctx->d_pivflag, 0, S * sizeof(int)) != cudaSuccess ||
         cudaMemset(ctx->z32, 0, (size_t)S * ctx->z32_stride * sizeof(float)) != cudaSuccess)
         return bail(ZSOLVE_ECUDA);
-    *ctx->h_status = 0;
     if (ctx->opts.resid == ZSOLVE_RESID_DF) {
         if (cudaMalloc(&ctx->xs, (size_t)S * nrhs_max * n * sizeof(float4)) != cudaSuccess) return bail(ZSOLVE_ENOMEM);
         if (resid_selftest(ctx) != ZSOLVE_OK) return bail(ZSOLVE_ECUDA);
@@ -723,6 +836,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
 int zsolve_set_stream(zsolve_ctx *ctx, void *stream) {
     if (!ctx) return ZSOLVE_EINVAL;
     ctx->stream = (cudaStream_t)stream;
+    ctx->lane[0].stream = ctx->stream;
     return ZSOLVE_OK;
 }
 
@@ -733,7 +847,7 @@ int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const d
         return fail(ctx, ZSOLVE_EINVAL, "omega must be positive and finite, Zs finite");
     ctx->h_params[0] = ZsSlotParam{omega, zs_re, zs_im, 1.0 / omega};
     ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
-    StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE);
+    StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE, ctx->stream);
     ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32, ctx->ld,
                              ctx->plane, ctx->z32_stride, ctx->stream));
     sp.done(1);
@@ -746,7 +860,7 @@ int zsolve_factor(zsolve_ctx *ctx) {
     if (!ctx) return ZSOLVE_EINVAL;
     if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_factor before zsolve_assemble");
     if (ctx->factored) return ZSOLVE_OK;
-    ZS_TRY(factor_slots(ctx, ctx->d_all, 1));
+    ZS_TRY(factor_slots(ctx, ctx->lane[0], ctx->d_all, 1, 0));
     ctx->factored = 1;
     return ZSOLVE_OK;
 }
@@ -756,11 +870,11 @@ int zsolve_refine(zsolve_ctx *ctx, const void *b, void *x, int nrhs, zsolve_info
     ZS_TRY(check_nrhs(ctx, nrhs));
     if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "zsolve_refine before zsolve_factor");
     zsolve_info tmp{};
-    ZS_CU(cudaEventRecord(ctx->ev[2], ctx->stream));
-    int st = refine_batch(ctx, (const double2 *)b, (double2 *)x, 0, nrhs, 1, &tmp);
-    ZS_CU(cudaEventRecord(ctx->ev[3], ctx->stream));
-    ZS_CU(cudaEventSynchronize(ctx->ev[3]));
-    cudaEventElapsedTime(&tmp.ms_refine, ctx->ev[2], ctx->ev[3]);
+    ZS_CU(cudaEventRecord(ctx->lane[0].ev[2], ctx->stream));
+    int st = refine_batch(ctx, ctx->lane[0], (const double2 *)b, (double2 *)x, 0, nrhs, 0, 1, &tmp);
+    ZS_CU(cudaEventRecord(ctx->lane[0].ev[3], ctx->stream));
+    ZS_CU(cudaEventSynchronize(ctx->lane[0].ev[3]));
+    cudaEventElapsedTime(&tmp.ms_refine, ctx->lane[0].ev[2], ctx->lane[0].ev[3]);
     if (info) *info = tmp;
     if (st != ZSOLVE_OK) return st;
     return tmp.status;
@@ -815,8 +929,8 @@ int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int 
     if (!ctx || !b || !x || !r) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
     ZS_TRY(check_nrhs(ctx, nrhs));
     if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_residual before zsolve_assemble");
-    StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL);
-    ZS_TRY(residual_slots(ctx, (const double2 *)b, (const double2 *)x, 0, nrhs, nullptr, 0, (double2 *)r, 0,
+    StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL, ctx->stream);
+    ZS_TRY(residual_slots(ctx, ctx->lane[0], (const double2 *)b, (const double2 *)x, 0, nrhs, nullptr, 0, (double2 *)r, 0,
                           ctx->d_all, 1, &sp));
     ZS_CU(cudaStreamSynchronize(ctx->stream));
     return ZSOLVE_OK;
@@ -828,22 +942,22 @@ int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs) {
     if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "zsolve_lowprec_solve before zsolve_factor");
     const int64_t cnt = (int64_t)nrhs * ctx->n;
     {
-        StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
+        StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE, ctx->stream);
         ZS_CU(zs_launch_narrow((const double2 *)v, ctx->v, cnt, ctx->stream));
         sp.done(1);
     }
-    ZS_TRY(lowprec_solve_slots(ctx, nrhs, ctx->d_all, 1));
-    StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE);
+    ZS_TRY(lowprec_solve_slots(ctx, ctx->lane[0], nrhs, ctx->d_all, 1));
+    StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE, ctx->stream);
     ZS_CU(zs_launch_widen(ctx->v, (double2 *)d, cnt, ctx->stream));
     sp.done(1);
-    return check_device_status(ctx);
+    return check_device_status(ctx, ctx->lane[0]);
 }
 
 int zsolve_fallback_solve(zsolve_ctx *ctx, const void *b, void *x, int nrhs) {
     if (!ctx || !b || !x) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
     if (nrhs < 1 || nrhs > ctx->nrhs_max) return fail(ctx, ZSOLVE_EINVAL, "bad nrhs");
     if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_fallback_solve before zsolve_assemble");
-    ZS_TRY(fallback_slot(ctx, 0, (const double2 *)b, (double2 *)x, nrhs));
+    ZS_TRY(fallback_slot(ctx, ctx->lane[0], 0, (const double2 *)b, (double2 *)x, nrhs));
     ZS_CU(cudaStreamSynchronize(ctx->stream));
     return ZSOLVE_OK;
 }
