@@ -63,6 +63,40 @@ def workload_name(cfg):
             f"{c.nrhs} RHS, Z = jwL - jPsi/w + Zs G")
 
 
+def profile_traffic(name, source):
+    """DRAM bytes per launch recorded in profiles/<name>.md by an ncu capture,
+    or None when the kernel source has changed since (the summary records the
+    sha256 of the source file it was taken with)."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    src = os.path.join(ROOT, "mixed_precision_refinement_gb300", "csrc", source)
+    if not (os.path.exists(path) and os.path.exists(src)):
+        return None
+    with open(src, "rb") as f:
+        digest = hashlib.sha256(f.read()).hexdigest()
+    rec = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- source_sha256: ") or line.startswith("- dram_bytes_per_launch: "):
+                k, v = line[2:].split(":", 1)
+                rec[k.strip()] = v.strip().strip("`")
+    if rec.get("source_sha256") != digest or "dram_bytes_per_launch" not in rec:
+        return None
+    return float(rec["dram_bytes_per_launch"])
+
+
+def trsm_flops(n, nb=128):
+    """Useful real flops of all tensor-core block solves of one factorisation
+    (L21 = A21 U11^-1 and U12 = L11^-1 A12: 2 x m2 x nb x nb complex MACs)."""
+    tot = 0
+    J = 0
+    while J + nb < n:
+        m2 = n - J - nb
+        tot += 2 * 8 * m2 * nb * nb
+        J += nb
+    return tot
+
+
 def schur_flops(n, nb=128):
     """Useful real flops of all trailing updates of one factorisation."""
     tot = 0
@@ -293,44 +327,53 @@ def run_ours(args):
     st = {k: v for k, v in prof.items()}
     steps = args.steps
     schur_f = schur_flops(n) * nf
-    fac_ms = (st["diag"]["ms"] + st["trsm"]["ms"] + st["schur"]["ms"]) / steps
+    # factorisation time per step: the lanes' factorisation spans summed (each
+    # frequency's info.ms_factor is its lane's span / the lane's frequencies),
+    # so the overlap of the two lanes is not credited
+    fac_ms = sum(i.ms_factor for i in infos)
     lu_tflops = (8.0 * n ** 3 / 3.0 * nf) / (fac_ms / 1e3) / 1e12 if fac_ms > 0 else None
     res_bytes = n_res_calls * (16.0 * n * n + 32.0 * n * nrhs)
     res_ms = st["residual"]["ms"] / steps
     res_gbs = res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None
     asm_bytes = 24.0 * n * n + 24.0 * n * n * nf
     stage_ms = {k: v["ms"] / steps for k, v in st.items()}
-    dominant = max(stage_ms, key=stage_ms.get)
     fp32_peak = SMS * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12
     fp64_peak = FP64_NOMINAL_TFLOPS
     tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
-    roof = {}
-    if dominant == "schur":
-        per_launch_ms = st["schur"]["ms"] / max(1, st["schur"]["launches"])
-        launches_per_step = st["schur"]["launches"] / steps
-        flops_per_launch = schur_f / launches_per_step
-        ach = flops_per_launch / (per_launch_ms / 1e3) / 1e12
-        if args.gemm == "FFMA":
-            roof = {"kernel": "k_schur_simt", "bound": "alu", "achieved": ach, "peak": fp32_peak, "unit": "TFLOP/s",
-                    "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
-        else:
-            roof = {"kernel": "k_schur_tc", "bound": "tensor", "achieved": ach, "peak": tf32_peak, "unit": "TFLOP/s",
-                    "peak_source": f"tf32 = {peak_src} bf16 {peaks['bf16_tflops']} x 1.1/2.25"}
-    elif dominant == "residual":
-        ach = res_gbs
-        roof = {"kernel": "k_residual", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "peak_source": f"{peak_src} hbm_gbs"}
-    elif dominant == "assemble":
-        ach = asm_bytes / (stage_ms["assemble"] / 1e3) / 1e9
-        roof = {"kernel": "k_assemble", "bound": "hbm", "achieved": ach, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "peak_source": f"{peak_src} hbm_gbs"}
+    # The roofline object covers the dominant kernel of the path: k_cgemm_tc,
+    # the tcgen05 complex-product kernel that runs both the trailing updates
+    # and the block solves (the largest share of the ncu launch list).
+    # Achieved = useful complex-product flops per launch / mean launch
+    # duration (CUDA events around every launch, on the stream it runs on;
+    # with two lanes the launches run next to the other lane's kernels).
+    tc_launches = max(1, st["schur"]["launches"] + (st["trsm"]["launches"] if args.gemm != "FFMA" else 0))
+    tc_ms_tot = st["schur"]["ms"] + (st["trsm"]["ms"] if args.gemm != "FFMA" else 0.0)
+    tc_flops_tot = (schur_f + (trsm_flops(n) * nf if args.gemm != "FFMA" else 0)) * steps
+    tc_ms = tc_ms_tot / tc_launches
+    tc_ach = (tc_flops_tot / tc_launches) / (tc_ms / 1e3) / 1e12 if tc_ms > 0 else None
+    if args.gemm == "FFMA":
+        roof = {"kernel": "k_schur_simt", "bound": "alu", "achieved": tc_ach, "peak": fp32_peak, "unit": "TFLOP/s",
+                "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
     else:
-        roof = {"kernel": dominant, "bound": "latency", "achieved": None, "peak": None, "unit": None}
-    if roof.get("achieved") and roof.get("peak"):
-        roof["frac"] = roof["achieved"] / roof["peak"]
-    else:
-        roof["frac"] = None
-    roof["traffic"] = None
+        roof = {"kernel": "k_cgemm_tc (trailing updates + block solves)", "bound": "tensor", "achieved": tc_ach,
+                "peak": tf32_peak, "unit": "TFLOP/s",
+                "peak_source": f"tf32 = {peak_src} bf16 {peaks['bf16_tflops']} x 1.1/2.25",
+                "flops": "useful complex-product flops (8 per complex MAC); the 3xTF32 split runs 3x that on the pipe"}
+    roof["frac"] = (roof["achieved"] / roof["peak"]) if roof.get("achieved") and roof.get("peak") else None
+    tb = profile_traffic("k_cgemm_tc_n2157", "schur_tc.cu") if (args.config == 1 and args.gemm == "TF32X3") else None
+    roof["traffic"] = tb
+    roof["launch_ms"] = tc_ms
+    # the other bounded kernels, for context
+    asm_ms = stage_ms["assemble"]
+    rooflines = {
+        "residual": {"kernel": "k_residual" if resid_mode == "F64" else "k_residual_df", "bound": "hbm",
+                     "achieved": res_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None},
+        "assemble": {"kernel": "k_assemble", "bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"],
+                     "achieved": asm_bytes / (asm_ms / 1e3) / 1e9 if asm_ms > 0 else None},
+    }
+    if rooflines["assemble"]["achieved"]:
+        rooflines["assemble"]["frac"] = rooflines["assemble"]["achieved"] / peaks["hbm_gbs"]
     launches = sum(v["launches"] for v in st.values())
     h2d = 3 * 8 * n * n + 16 * n * nrhs
     d2h = 16 * nf * nrhs * n
@@ -344,9 +387,11 @@ def run_ours(args):
                    "batch": args.batch or nf, "l2": "flushed between steps (512 MB write)",
                    "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
         "lu_tflops": lu_tflops, "resid_gbs": res_gbs,
-        "resid_fp64_alu_bound_gbs": fp64_peak * 1e12 / 8.0 * 16.0 / nrhs / 1e9,
         "roofline": roof,
+        "rooflines_other": rooflines,
         "stage_ms_per_step": stage_ms,
+        "stage_note": "per-stage sums of per-launch device times; the two lanes run side by side, so the "
+                      "stages add up to more than ms_per_step",
         "iters": iters, "fallbacks": sum(i.fallback for i in infos),
         "gpu_launches": int(launches),
         "e2e": {"value": ws * nf / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -92,7 +92,8 @@ typedef struct {
 #define ZSOLVE_STAGE_RESIDUAL 5 /* r = b - Z x in float64 */
 #define ZSOLVE_STAGE_UPDATE 6   /* rounding of b, x += d, correction norms */
 #define ZSOLVE_STAGE_FALLBACK 7 /* float64 pivoted LU and its substitution */
-#define ZSOLVE_NSTAGE 8
+#define ZSOLVE_STAGE_PACK 8     /* tensor-core operand packs of A21 and A12^T */
+#define ZSOLVE_NSTAGE 9
 
 typedef struct {
     int64_t launches[ZSOLVE_NSTAGE]; /* kernels launched per stage (always counted) */

@@ -46,7 +46,7 @@ class zsolve_opts(ctypes.Structure):
                 ("profile", ctypes.c_int), ("resid", ctypes.c_int), ("lanes", ctypes.c_int)]
 
 
-STAGES = ("assemble", "diag", "trsm", "schur", "trsv", "residual", "update", "fallback")
+STAGES = ("assemble", "diag", "trsm", "schur", "trsv", "residual", "update", "fallback", "pack")
 
 
 class zsolve_profile(ctypes.Structure):

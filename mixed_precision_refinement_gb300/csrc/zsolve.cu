@@ -264,7 +264,7 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
         if (!last) {
             ZS_CU(cudaEventRecord(ln.ev_fork, ln.stream));
             ZS_CU(cudaStreamWaitEvent(ln.side, ln.ev_fork, 0));
-            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.side);
+            StageSpan sp(ctx, ZSOLVE_STAGE_PACK, ln.side);
             ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
                                       ctx->pack_stride, mode, slots, nslot, ln.side));
             sp.done(1);
