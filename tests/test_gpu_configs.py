@@ -1,0 +1,89 @@
+"""The three larger workloads at full size (N = 6614 with 41 frequencies and 2
+right-hand sides, N = 8000 with 8, N = 16384 with 11 frequencies and 4), each
+run as the benchmark runs a sweep: the whole frequency list through
+zsolve_sweep with the default options (3xTF32 factors, float64 residual,
+automatic batching, two lanes where a batch holds two or more frequencies).
+
+Checked against the oracle:
+- every (frequency, right-hand side): the oracle's float64 normwise backward
+  error eta = ||b - Z x|| / (||Z||_F ||x|| + ||b||), with Z assembled by the
+  oracle, below ETA;
+- sampled frequencies of the two configurations whose complex128 pivoted LU
+  the oracle finishes in seconds: the oracle's direct solve, to the parity
+  bound 1e-10.
+
+Bound on eta: once the relative correction is below 1e-11 the backward
+error is set by the rounding of the float64 residual sums, which grows like
+sqrt(n) * 2^-53; the test allows 16 sqrt(n) 2^-53 (1.4e-13 at n = 6614,
+2.3e-13 at n = 16384).  A solution that is only float32-accurate sits near
+1e-7, six orders of magnitude above.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import workload
+
+pytestmark = pytest.mark.gpu
+
+PARITY = 1e-10
+U64 = 2.0 ** -53
+
+
+@pytest.fixture(scope="module")
+def zs():
+    import mixed_precision_refinement_gb300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def torch():
+    import torch as t
+    return t
+
+
+def rel_err(x, ref):
+    x = np.atleast_2d(x)
+    ref = np.atleast_2d(ref)
+    return np.linalg.norm(x - ref, axis=-1) / np.linalg.norm(ref, axis=-1)
+
+
+def sweep(zs, torch, wl):
+    nf, nrhs, n = len(wl.omega), wl.B.shape[0], wl.n
+    s = zs.Solver(n, nrhs)
+    try:
+        L = torch.from_numpy(wl.L).cuda()
+        P = torch.from_numpy(wl.Psi).cuda()
+        G = torch.from_numpy(wl.G).cuda()
+        B = torch.from_numpy(wl.B).cuda()
+        x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+        infos = zs.zsolve_sweep(s.ctx, L, P, G, wl.omega, wl.zs, B, x)
+        X = x.cpu().numpy()
+        del L, P, G, B, x
+    finally:
+        s.close()
+        torch.cuda.empty_cache()
+    return X, infos
+
+
+@pytest.mark.timeout(1200)
+@pytest.mark.parametrize("cfg,sampled", [(2, (0, 40)), (3, (0,)), (4, ())])
+def test_full_size_configuration(zs, torch, cfg, sampled):
+    wl = workload.make(cfg)
+    n = wl.n
+    eta_max = 16.0 * np.sqrt(n) * U64
+    X, infos = sweep(zs, torch, wl)
+    worst = 0.0
+    for f in range(len(wl.omega)):
+        assert infos[f].status == 0 and infos[f].fallback == 0, (f, infos[f].as_dict())
+        Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[f], wl.zs[f])
+        R = oracle.residual(Z, X[f], wl.B)
+        eta = np.linalg.norm(R, axis=1) / (np.linalg.norm(Z) * np.linalg.norm(X[f], axis=1)
+                                           + np.linalg.norm(wl.B, axis=1))
+        worst = max(worst, float(eta.max()))
+        assert np.all(eta < eta_max), (f, eta, eta_max)
+        if f in sampled:
+            ref = oracle.solve(Z, wl.B)
+            assert np.all(rel_err(X[f], ref) <= PARITY), (f, rel_err(X[f], ref))
+        del Z, R
+    print(f"config {cfg}: worst normwise backward error {worst:.3e} (bound {eta_max:.3e})")
