@@ -205,9 +205,9 @@ def sweep_variant(zs, torch, wl, args, resid):
         res_ms = prof["residual"]["ms"] / args.steps
         res_bytes = iters / args.steps * (16.0 * n * n + 32.0 * n * nrhs)
         peaks, _ = load_peaks()
-        gbs = res_bytes / (res_ms / 1e3) / 1e9
+        gbs = res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None
         return {"mode_in_use": mode, "points_per_s": nf / (ms / 1e3), "resid_gbs": gbs,
-                "resid_hbm_frac": gbs / peaks["hbm_gbs"],
+                "resid_hbm_frac": (gbs / peaks["hbm_gbs"]) if gbs else None,
                 "arith": "float64 DFMA" if mode == "F64" else "double-float (2 x float32, ~46 bits)"}
     finally:
         s.close()

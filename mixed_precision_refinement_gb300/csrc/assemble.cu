@@ -17,9 +17,10 @@
 //    of elementary functions on the IBM RISC System/6000 processor", IBM J.
 //    Res. Dev. 1990, the division theorem); a zero q0 is returned as is, so a
 //    -0 dividend keeps its sign;
-//  - where G_ij = 0 (all but three diagonals in the generated workloads)
-//    Zs*G is an exact zero, so the products are skipped and only the sign of
-//    zero they would produce is reproduced (integer ops);
+//  - where G_ij = 0 for all 32 entries of a warp (all but three diagonals
+//    in the generated workloads) Zs*G is an exact zero, so the products are
+//    skipped and only the sign of zero they would produce is reproduced
+//    (integer ops);
 //  - zero tests and signs of zero are done on the 32-bit halves of the bit
 //    pattern (see zs::bits_of), so no FP64 compare is issued;
 //  - float64 -> float32 round-to-nearest-even is done on the integer bit
@@ -67,17 +68,22 @@ struct Fp64Ops {
     __device__ __forceinline__ double sub(double a, double b) const { return __fma_rn(zs::neg_bits(b), one, a); }
 };
 
-// Z64[e] and both float32 planes for one frequency
-__device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, double p, double g, bool gzero,
-                                          double2 *__restrict__ z64e, float *__restrict__ z32e, int64_t plane,
-                                          const Fp64Ops &op) {
+// Z64[e] and both float32 planes for one frequency.  warp_gzero: every
+// entry this warp handles has G = +-0 (warp-uniform), so the Zs*G products
+// are exact zeros and only their signs of zero are reproduced (integer ops);
+// otherwise the whole warp multiplies, which gives the same result for the
+// entries whose G is zero.  A per-entry choice would be if-converted and the
+// FP64 pipe would issue the products for every warp with most lanes off.
+__device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, double p, double g, bool warp_gzero,
+                                          bool valid, double2 *__restrict__ z64e, float *__restrict__ z32e,
+                                          int64_t plane, const Fp64Ops &op) {
     const double w = sp.omega, r = sp.pad;  // pad holds RN(1/omega)
     const double q0 = op.mul(p, r);
     // RN(p / w); a zero first quotient is already exact (and keeps its sign)
-    const double q = zs::is_zero(zs::bits_of(q0)) ? q0 : __fma_rn(__fma_rn(zs::neg_bits(w), q0, p), r, q0);
+    const double q = zs::sel_bits(zs::is_zero(zs::bits_of(q0)), q0, __fma_rn(__fma_rn(zs::neg_bits(w), q0, p), r, q0));
     const double t = op.sub(op.mul(w, l), q);
     double re, im;
-    if (gzero) {
+    if (warp_gzero) {
         // Zs.re * (+-0) and t + Zs.im * (+-0): exact zeros; only signs of zero to reproduce
         const unsigned gs = zs::bits_of(g).hi & 0x80000000u;
         const unsigned zr = (zs::bits_of(sp.zs_re).hi & 0x80000000u) ^ gs;
@@ -85,14 +91,16 @@ __device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, doubl
         re = zs::double_of(0u, zr);
         const zs::Bits64 tb = zs::bits_of(t);
         // t + z: equals t unless t is a zero; (-0) + (-0) = -0, any other pair of zeros = +0
-        im = zs::is_zero(tb) ? zs::double_of(0u, tb.hi & zi) : t;
+        im = zs::sel_bits(zs::is_zero(tb), zs::double_of(0u, tb.hi & zi), t);
     } else {
         re = op.mul(sp.zs_re, g);
         im = op.add(t, op.mul(sp.zs_im, g));
     }
-    __stcs(z64e, make_double2(re, im));
-    __stcs(z32e, d2f_rn(re));
-    __stcs(z32e + plane, d2f_rn(im));
+    if (valid) {
+        __stcs(z64e, make_double2(re, im));
+        __stcs(z32e, d2f_rn(re));
+        __stcs(z32e + plane, d2f_rn(im));
+    }
 }
 
 __global__ void __launch_bounds__(kThreads)
@@ -101,26 +109,43 @@ k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const d
            float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, double mz, double one) {
     __shared__ ZsSlotParam sp[kMaxSlots];
     const Fp64Ops op{mz, one};
+    const int lane = threadIdx.x & 31;
     for (int s = threadIdx.x; s < nslot; s += blockDim.x) sp[s] = params[s];
     __syncthreads();
     for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
         const int64_t row = i * n, row32 = i * ld;
-        for (int64_t j = threadIdx.x; j < n; j += blockDim.x) {
+        // warp-uniform column walk (the tail lanes compute on a clamped index
+        // and do not store), so the warp vote below always sees the full warp
+        for (int64_t jw = threadIdx.x - lane; jw < n; jw += blockDim.x) {
+            const int64_t jv = jw + lane;
+            const bool valid = jv < n;
+            const int64_t j = valid ? jv : n - 1;
             const int64_t e = row + j, o32 = row32 + j;
             const double l = __ldcs(L + e), p = __ldcs(Psi + e), g = __ldcs(G + e);
-            const bool gzero = zs::is_zero(zs::bits_of(g));
-            // four frequencies at a time: independent FP64 chains to cover the unit's latency
+            const bool warp_gzero = __all_sync(0xffffffffu, zs::is_zero(zs::bits_of(g)));
+            // four frequencies at a time: independent FP64 chains to cover the
+            // unit's latency.  The per-frequency addresses advance by adding
+            // the strides: 64-bit integer products would go to the FP64 pipe.
+            double2 *zp = z64 + e;
+            float *zq = z32 + o32;
             int s = 0;
 #pragma unroll 1
             for (; s + 4 <= nslot; s += 4) {
-#pragma unroll
-                for (int u = 0; u < 4; u++) one_entry(sp[s + u], l, p, g, gzero, z64 + (s + u) * z64_stride + e,
-                                                      z32 + (s + u) * z32_stride + o32, plane, op);
+                double2 *zp1 = zp + z64_stride, *zp2 = zp1 + z64_stride, *zp3 = zp2 + z64_stride;
+                float *zq1 = zq + z32_stride, *zq2 = zq1 + z32_stride, *zq3 = zq2 + z32_stride;
+                one_entry(sp[s], l, p, g, warp_gzero, valid, zp, zq, plane, op);
+                one_entry(sp[s + 1], l, p, g, warp_gzero, valid, zp1, zq1, plane, op);
+                one_entry(sp[s + 2], l, p, g, warp_gzero, valid, zp2, zq2, plane, op);
+                one_entry(sp[s + 3], l, p, g, warp_gzero, valid, zp3, zq3, plane, op);
+                zp = zp3 + z64_stride;
+                zq = zq3 + z32_stride;
             }
 #pragma unroll 1
-            for (; s < nslot; s++)
-                one_entry(sp[s], l, p, g, gzero, z64 + s * z64_stride + e, z32 + s * z32_stride + o32, plane, op);
-
+            for (; s < nslot; s++) {
+                one_entry(sp[s], l, p, g, warp_gzero, valid, zp, zq, plane, op);
+                zp += z64_stride;
+                zq += z32_stride;
+            }
         }
     }
 }

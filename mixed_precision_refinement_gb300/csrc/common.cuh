@@ -58,6 +58,11 @@ __device__ __forceinline__ double double_of(unsigned lo, unsigned hi) {
     return x;
 }
 __device__ __forceinline__ bool is_zero(Bits64 b) { return ((b.hi << 1) | b.lo) == 0u; }  // +0 or -0
+// c ? a : b for doubles as two 32-bit integer selects (no FP64 instruction)
+__device__ __forceinline__ double sel_bits(bool c, double a, double b) {
+    const Bits64 x = bits_of(a), y = bits_of(b);
+    return double_of(c ? x.lo : y.lo, c ? x.hi : y.hi);
+}
 // -x by flipping the sign bit on the integer side (no FP64 instruction)
 __device__ __forceinline__ double neg_bits(double x) {
     const Bits64 b = bits_of(x);
