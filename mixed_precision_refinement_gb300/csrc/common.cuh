@@ -149,16 +149,14 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
 #define ZS_INV32_STRIDE (4 * 2 * 2 * 32 * 32)
 inline int64_t zs_inv32_slot_stride(int64_t n) { return ((n + 127) / 128) * ZS_INV32_STRIDE; }
 // Diagonal block at J (nb <= 128 columns, identity-padded to 128): its LU in
-// place in z32 and the 32x32 sub-block inverses (inv32).  pivflag[slot] = 1
+// place in z32; the dense 128x128 inverses of its L and U into dinv (zero
+// outside the triangles from the allocation on: only the triangles are
+// written) and, if winv != NULL, their operand packs (mode 1: tf32 hi; 2: hi
+// + lo); if inv32 != NULL, the 32x32 sub-block inverses.  pivflag[slot] = 1
 // on a tiny or non-finite pivot.
 cudaError_t zs_launch_diag_block(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
                                  const int *slots, int nslot, int *pivflag, float *inv32, int64_t inv32_stride,
-                                 cudaStream_t st);
-// The dense 128x128 inverses of the block's L and U (dinv) from the factor and
-// inv32 and, if winv != NULL, their operand packs (mode 1: tf32 hi; 2: hi + lo).
-cudaError_t zs_launch_block_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
-                                const int *slots, int nslot, const float *inv32, int64_t inv32_stride, float *dinv,
-                                int64_t dinv_stride, float *winv, int mode, cudaStream_t st);
+                                 float *dinv, int64_t dinv_stride, float *winv, int mode, cudaStream_t st);
 // mode: 0 = pack plain fp32 (FFMA), 1 = tf32 rounded (TF32), 2 = tf32 hi + lo (TF32X3)
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                              int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,

@@ -17,15 +17,18 @@
 //      trailing update A_ij -= L_ip U_pj -- register-tiled complex products
 //      (8 or 16 rows per warp task, lane = column, rows of the left operand
 //      read as broadcast 16-byte loads).
-// The factored block goes back to the float32 matrix and the 32 x 32 inverses
-// to inv32.  A second kernel (k_block_inv, one CTA per block column of each
-// inverse) then builds the 128 x 128 inverses W = U^-1 and V = L^-1 by block
-// substitution,
+// The factored block goes back to the float32 matrix (and, for the FP32
+// block solves, the 32 x 32 inverses to inv32).  The same CTA then builds the
+// 128 x 128 inverses W = U^-1 and V = L^-1 by block substitution,
 //   U: X_ik = -sum_{m=i+1..k} G_im X_mk,  G_im = DU_i U_im   (i descending)
 //   L: X_ik = -sum_{m=k..i-1} G_im X_mk,  G_im = DL_i L_im   (i ascending)
-// with X_kk = DU_k resp. DL_k, and writes them out as the dense inverse blocks
-// of the triangular solves (dinv) and, when asked, as the tensor-core operand
-// packs of the block triangular solves (winv).
+// with X_kk = DU_k resp. DL_k: first the twelve G blocks, in place of the
+// factor's off-diagonal sub-blocks, then the X blocks by distance from the
+// diagonal (6, 4, 2 blocks of all warps' tasks), each round written out as
+// the dense inverse blocks of the triangular solves (dinv) and, when asked,
+// as the tensor-core operand packs of the block triangular solves (winv).
+// The blocks outside the triangles are zero in both; they are set once when
+// the buffers are allocated and never written here.
 //
 // Padding: a last block with nb < 128 is completed with the identity, whose
 // factors and inverses are the identity again.
@@ -112,9 +115,10 @@ __device__ __forceinline__ void zero(cf (&acc)[TM]) {
     for (int t = 0; t < TM; t++) acc[t] = cf{0.f, 0.f};
 }
 
-__device__ __forceinline__ void store_rows(const Blk C, int r0, int lane, const cf (&acc)[TMR], float sgn) {
+template <int TM>
+__device__ __forceinline__ void store_c(const Blk C, int r0, int lane, const cf (&acc)[TM], float sgn) {
 #pragma unroll
-    for (int t = 0; t < TMR; t++) st_c(C, r0 + t, lane, cf{sgn * acc[t].re, sgn * acc[t].im});
+    for (int t = 0; t < TM; t++) st_c(C, r0 + t, lane, cf{sgn * acc[t].re, sgn * acc[t].im});
 }
 
 // Step 1: LU of the 32 x 32 diagonal sub-block by warps 0-3: warp w holds
@@ -242,10 +246,56 @@ __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float(r);
 }
 
+constexpr int TM3 = 4;  // rows per warp task of the distance-3 inverse blocks
+
+// Off-diagonal sub-blocks (a, b) of the factor: U for a < b, L for a > b;
+// the first 8 and the last 4 are formed in two passes.
+__constant__ unsigned char kOff[12][2] = {{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}, {2, 3},
+                                          {1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
+
+// Block (l, k) of W = U^-1 (upper) or of V = L^-1, held in shared memory at
+// S, out to the dense inverse xr ([re, im][128][128] of that triangle) and,
+// if pl is set, to the operand packs of the tensor-core block solves: pack
+// row r holds column r of W resp. row r of V as Br = [Re | -Im] and
+// Bi = [Im | Re], in tf32 hi (planes 0, 2) and, for mode 2, lo (1, 3).
+// Blocks outside the triangles are zero in both and are never written.
+__device__ __noinline__ void emit_block(bool upper, int l, int k, const Blk S, float *xr, float *pl, int mode,
+                                        int tid) {
+    for (int idx = tid; idx < P * P; idx += kThreads) {
+        const int i = idx >> 5, j = idx & 31;
+        const cf v = ld_c(S, i, j);
+        const int o = (l * P + i) * NB + k * P + j;
+        xr[o] = v.re;
+        xr[NB * NB + o] = v.im;
+    }
+    if (!pl) return;
+    for (int idx = tid; idx < P * P; idx += kThreads) {
+        // consecutive threads write consecutive pack positions
+        const int i = upper ? (idx & 31) : (idx >> 5), j = upper ? (idx >> 5) : (idx & 31);
+        const cf v = ld_c(S, i, j);
+        const int prow = upper ? k * P + j : l * P + i;
+        const int m = upper ? l * P + i : k * P + j;
+        const int o = prow * (2 * NB) + m;
+        const float hr = tf32_rna(v.re), hi = tf32_rna(v.im);
+        pl[o] = hr;
+        pl[o + NB] = -hi;
+        pl[2 * ZS_WINV_PLANE + o] = hi;
+        pl[2 * ZS_WINV_PLANE + o + NB] = hr;
+        if (mode == 2) {
+            const float lr = tf32_rna(v.re - hr), li = tf32_rna(v.im - hi);
+            pl[ZS_WINV_PLANE + o] = lr;
+            pl[ZS_WINV_PLANE + o + NB] = -li;
+            pl[3 * ZS_WINV_PLANE + o] = li;
+            pl[3 * ZS_WINV_PLANE + o + NB] = lr;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
              const int *__restrict__ slots, int *__restrict__ pivflag, float *__restrict__ inv32,
-             int64_t inv32_stride) {
+             int64_t inv32_stride, float *__restrict__ dinv, int64_t dinv_stride, float *__restrict__ winv,
+             int mode) {
     __shared__ unsigned s_amax;
     __shared__ int s_bad;
     const int slot = slots[blockIdx.x];
@@ -296,7 +346,7 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
                          acc);
             }
             __syncthreads();
-            if (t < ntask) store_rows(b < rest ? blkA(p + 1 + b, p) : blkA(p, p + 1 + b - rest), r0, lane, acc, 1.f);
+            if (t < ntask) store_c(b < rest ? blkA(p + 1 + b, p) : blkA(p, p + 1 + b - rest), r0, lane, acc, 1.f);
             __syncthreads();
         }
         // A_ij -= L_ip U_pj, i, j > p: each task owns its output rows
@@ -316,14 +366,14 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
         __syncthreads();
     }
 
-    // ---- the factor and the 32 x 32 inverses out
+    // ---- the factor out; the 32 x 32 inverses too when the FP32 block solves want them
     for (int idx = tid; idx < nb * nb; idx += kThreads) {
         const int i = idx / nb, j = idx - i * nb;
         const int64_t g = (J + i) * ld + J + j;
         gre[g] = smem[i * LDA + j];
         gim[g] = smem[IM_A + i * LDA + j];
     }
-    {
+    if (inv32) {
         float *d32 = inv32 + (int64_t)slot * inv32_stride + (J / NB) * ZS_INV32_STRIDE;
         for (int idx = tid; idx < 8 * P * P; idx += kThreads) {
             const int w = idx >> 10, e = idx & (P * P - 1), i = e >> 5, j = e & 31;
@@ -337,152 +387,121 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
     }
     if (tid == 0 && s_bad) pivflag[slot] = 1;
 
-}
-
-// ---------------------------------------------------------------- 128 x 128 inverses
-
-// Block column k of W = U^-1 (chain 0-3, k = chain) or of V = L^-1 (chain
-// 4-7, k = chain - 4) for one frequency per CTA row.  In local block indices
-// l (U: l = i; L: l = 3 - i) both triangles read the same way: nr = number of
-// block rows that meet column k, the target row nr - 1 holds X = D_{nr-1},
-// and for l = nr-2 down to 0
-//   X_l = -sum_{m=l+1..nr-1} G_lm X_m,   G_lm = D_l F_lm,
-// with F the factor's off-diagonal sub-blocks (U_im, resp. L_{3-l,3-m}) and D
-// the 32 x 32 diagonal inverses the factorisation stored.  Every column block
-// is an independent chain; a CTA builds one and writes it to dinv (and winv).
-constexpr int SLOT = 2 * P * LDD;  // floats per sub-block slot
-constexpr int kInvSlots = 14;      // 6 F (local pairs a < b), 4 D, 4 X
-constexpr size_t kInvSmemBytes = (size_t)kInvSlots * SLOT * sizeof(float);
-
-__device__ __forceinline__ Blk slotF(int a, int b) { return {(b * (b - 1) / 2 + a) * SLOT, P * LDD, LDD}; }
-__device__ __forceinline__ Blk slotD(int l) { return {(6 + l) * SLOT, P * LDD, LDD}; }
-__device__ __forceinline__ Blk slotX(int l) { return {(10 + l) * SLOT, P * LDD, LDD}; }
-
-__global__ void __launch_bounds__(kThreads, 1)
-k_block_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
-            const float *__restrict__ inv32, int64_t inv32_stride, float *__restrict__ dinv, int64_t dinv_stride,
-            float *__restrict__ winv, int mode, const int *__restrict__ slots) {
-    const int chain = blockIdx.x, upper = chain < 4, k = chain & 3;
-    const int nr = upper ? k + 1 : 4 - k;
-    const int slot = slots[blockIdx.y];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const float *gre = z32 + (int64_t)slot * z32_stride;
-    const float *gim = gre + plane;
-    const float *d32 = inv32 + (int64_t)slot * inv32_stride + (J / NB) * ZS_INV32_STRIDE;
-    auto gblk = [upper](int l) { return upper ? l : 3 - l; };  // global block index of local l
-
-    // ---- load D_l and the factor sub-blocks F_ab (a < b < nr); padding beyond nb reads as zero
-    for (int idx = tid; idx < nr * P * P; idx += kThreads) {
-        const int l = idx >> 10, e = idx & (P * P - 1), i = e >> 5, j = e & 31;
-        const float *d = d32 + (gblk(l) * 2 + (upper ? 0 : 1)) * 2 * P * P;
-        st_c(slotD(l), i, j, cf{d[e], d[P * P + e]});
+    // ---- the 128 x 128 inverses W = U^-1 and V = L^-1 by block substitution
+    float *const xw = dinv + (int64_t)slot * dinv_stride + (J / NB) * 4 * NB * NB;  // [L, U][re, im][128][128]
+    float *const xu = xw + 2 * NB * NB, *const xl = xw;
+    float *const pu = winv ? winv + (int64_t)slot * ZS_WINV_STRIDE : nullptr;
+    float *const pv = winv ? pu + 4 * ZS_WINV_PLANE : nullptr;
+#pragma unroll 1
+    for (int k = 0; k < 4; k++) {
+        emit_block(true, k, k, blkDU(k), xu, pu, mode, tid);
+        emit_block(false, k, k, blkDL(k), xl, pv, mode, tid);
     }
-    const int npair = nr * (nr - 1) / 2;
-    for (int idx = tid; idx < npair * P * P; idx += kThreads) {
-        const int q = idx >> 10, e = idx & (P * P - 1), i = e >> 5, j = e & 31;
-        int b = 1;
-        while (b * (b + 1) / 2 <= q) b++;
-        const int a = q - b * (b - 1) / 2;
-        const int r = gblk(a) * P + i, c = gblk(b) * P + j;  // local (a, b) -> global sub-block
-        cf v = {0.f, 0.f};
-        if (r < nb && c < nb) v = cf{gre[(J + r) * ld + J + c], gim[(J + r) * ld + J + c]};
-        st_c(slotF(a, b), i, j, v);
-    }
-    __syncthreads();
-    // ---- G_ab = D_a F_ab for every pair, in place (each pair: two 16-row tasks)
-    {
-        const int t = warp, pq = t >> 1, r0 = (t & 1) * TMR;
-        int a = 0, b = 1;
-        if (t < 2 * npair) {
-            while (b * (b + 1) / 2 <= pq) b++;
-            a = pq - b * (b - 1) / 2;
-        }
+    // G_U(a, b) = DU_a U_ab (a < b) and G_L(i, m) = DL_i L_im (i > m), in place
+    // of the factor's off-diagonal sub-blocks: 12 blocks, two 16-row tasks
+    // each, as 8 blocks and then 4 (a block's rows are all read before any is
+    // overwritten).
+#pragma unroll 1
+    for (int g0 = 0; g0 < 12; g0 += 8) {
+        const int q = g0 + (warp >> 1), r0 = (warp & 1) * TMR;
+        const bool on = q < 12 && (g0 == 0 || warp < 8);
+        const int qc = q < 12 ? q : 11;
+        const int a = kOff[qc][0], b = kOff[qc][1];
+        const Blk F = blkA(a, b);
         cf acc[TMR];
         zero(acc);
-        if (t < 2 * npair) mac_rows(slotD(a), slotF(a, b), r0, lane, acc);
+        if (on) mac_rows(a < b ? blkDU(a) : blkDL(a), F, r0, lane, acc);
         __syncthreads();
-        if (t < 2 * npair) store_rows(slotF(a, b), r0, lane, acc, 1.f);
-        __syncthreads();
+        if (on) store_c(F, r0, lane, acc, 1.f);
     }
-    // ---- the chain, two rows per warp
-    for (int l = nr - 2; l >= 0; l--) {
-        cf acc[2];
+    __syncthreads();
+    // Chains, by distance from the diagonal.  Storage: the factor's diagonal
+    // sub-blocks are free now; W_12 goes to A(0,0), V_21 to A(2,2), results
+    // only written out to A(1,1) (W) and A(3,3) (V), and a result whose G
+    // block has no later use to that block.
+    //   distance 1: W_{k-1,k} = -G_U(k-1,k) DU_k,  V_{k+1,k} = -G_L(k+1,k) DL_k
+    {
+        const int q = warp >> 1, r0 = (warp & 1) * TMR;
+        const bool on = warp < 12;
+        const bool up = q < 3;
+        const int k = up ? q + 1 : q - 3;                 // column block
+        const int l = up ? k - 1 : k + 1;                 // row block
+        const Blk Gb = blkA(l, k);
+        const Blk dst = up ? (k == 1 ? blkA(1, 1) : k == 2 ? blkA(0, 0) : blkA(2, 3))
+                           : (k == 0 ? blkA(1, 0) : k == 1 ? blkA(2, 2) : blkA(3, 3));
+        cf acc[TMR];
         zero(acc);
-        for (int m = l + 1; m < nr; m++) mac_rows(slotF(l, m), m == nr - 1 ? slotD(nr - 1) : slotX(m), 2 * warp, lane, acc);
-#pragma unroll
-        for (int q = 0; q < 2; q++) st_c(slotX(l), 2 * warp + q, lane, cf{-acc[q].re, -acc[q].im});
+        if (on) mac_rows(Gb, up ? blkDU(k) : blkDL(k), r0, lane, acc);
+        __syncthreads();
+        if (on) store_c(dst, r0, lane, acc, -1.f);
         __syncthreads();
     }
-    // ---- dense inverse blocks [L, U][re, im][128][128]: block column k, zeros outside the triangle
-    auto value = [&](int row, int col32) -> cf {  // element (row, 32 k + col32) of the inverse
-        const int ib = row >> 5, l = upper ? ib : 3 - ib;
-        if (l >= nr) return cf{0.f, 0.f};
-        return ld_c(l == nr - 1 ? slotD(l) : slotX(l), row & 31, col32);
-    };
-    float *xr = dinv + (int64_t)slot * dinv_stride + (J / NB) * 4 * NB * NB + (upper ? 2 : 0) * NB * NB;
-    for (int idx = tid; idx < NB * P; idx += kThreads) {
-        const int row = idx >> 5, c = idx & 31;
-        const cf v = value(row, c);
-        xr[row * NB + k * P + c] = v.re;
-        xr[NB * NB + row * NB + k * P + c] = v.im;
-    }
-    if (!winv) return;
-    // ---- operand packs: pack row r holds column r of W (planes 0-3) resp.
-    // row r of V (planes 4-7) as Br = [Re | -Im], Bi = [Im | Re], tf32 hi (+ lo)
-    float *pl = winv + (int64_t)slot * ZS_WINV_STRIDE + (upper ? 0 : 4) * ZS_WINV_PLANE;
-    for (int idx = tid; idx < NB * P; idx += kThreads) {
-        int prow, m;
-        cf v;
-        if (upper) {  // W(m, 32 k + c) -> pack row 32 k + c, position m
-            const int c = idx >> 7;
-            m = idx & (NB - 1);
-            prow = k * P + c;
-            v = value(m, c);
-        } else {      // V(r, 32 k + c) -> pack row r, position 32 k + c
-            const int c = idx & 31;
-            prow = idx >> 5;
-            m = k * P + c;
-            v = value(prow, c);
+    emit_block(true, 0, 1, blkA(1, 1), xu, pu, mode, tid);
+    emit_block(true, 1, 2, blkA(0, 0), xu, pu, mode, tid);
+    emit_block(true, 2, 3, blkA(2, 3), xu, pu, mode, tid);
+    emit_block(false, 1, 0, blkA(1, 0), xl, pv, mode, tid);
+    emit_block(false, 2, 1, blkA(2, 2), xl, pv, mode, tid);
+    emit_block(false, 3, 2, blkA(3, 3), xl, pv, mode, tid);
+    //   distance 2: W_02 = -(G_U(0,1) W_12 + G_U(0,2) DU_2)   -> A(1,1)
+    //               W_13 = -(G_U(1,2) W_23 + G_U(1,3) DU_3)   -> A(1,3)
+    //               V_20 = -(G_L(2,1) V_10 + G_L(2,0) DL_0)   -> A(2,0)
+    //               V_31 = -(G_L(3,2) V_21 + G_L(3,1) DL_1)   -> A(3,3)
+    {
+        const int q = warp >> 2, r0 = (warp & 3) * TMU;
+        Blk g1, x1, g2, d2, dst;
+        switch (q) {
+            case 0: g1 = blkA(0, 1); x1 = blkA(0, 0); g2 = blkA(0, 2); d2 = blkDU(2); dst = blkA(1, 1); break;
+            case 1: g1 = blkA(1, 2); x1 = blkA(2, 3); g2 = blkA(1, 3); d2 = blkDU(3); dst = blkA(1, 3); break;
+            case 2: g1 = blkA(2, 1); x1 = blkA(1, 0); g2 = blkA(2, 0); d2 = blkDL(0); dst = blkA(2, 0); break;
+            default: g1 = blkA(3, 2); x1 = blkA(2, 2); g2 = blkA(3, 1); d2 = blkDL(1); dst = blkA(3, 3); break;
         }
-        const int64_t o = (int64_t)prow * (2 * NB) + m;
-        const float hr = tf32_rna(v.re), hi = tf32_rna(v.im);
-        pl[o] = hr;
-        pl[o + NB] = -hi;
-        pl[2 * ZS_WINV_PLANE + o] = hi;
-        pl[2 * ZS_WINV_PLANE + o + NB] = hr;
-        if (mode == 2) {
-            const float lr = tf32_rna(v.re - hr), li = tf32_rna(v.im - hi);
-            pl[ZS_WINV_PLANE + o] = lr;
-            pl[ZS_WINV_PLANE + o + NB] = -li;
-            pl[3 * ZS_WINV_PLANE + o] = li;
-            pl[3 * ZS_WINV_PLANE + o + NB] = lr;
-        }
+        cf acc[TMU];
+        zero(acc);
+        mac_rows(g1, x1, r0, lane, acc);
+        mac_rows(g2, d2, r0, lane, acc);
+        __syncthreads();
+        store_c(dst, r0, lane, acc, -1.f);
+        __syncthreads();
     }
+    emit_block(true, 0, 2, blkA(1, 1), xu, pu, mode, tid);
+    emit_block(true, 1, 3, blkA(1, 3), xu, pu, mode, tid);
+    emit_block(false, 2, 0, blkA(2, 0), xl, pv, mode, tid);
+    emit_block(false, 3, 1, blkA(3, 3), xl, pv, mode, tid);
+    //   distance 3: W_03 = -(G_U(0,1) W_13 + G_U(0,2) W_23 + G_U(0,3) DU_3)   -> A(0,3)
+    //               V_30 = -(G_L(3,2) V_20 + G_L(3,1) V_10 + G_L(3,0) DL_0)   -> A(3,0)
+    {
+        const bool up = warp < 8;
+        const int r0 = (warp & 7) * TM3;
+        cf acc[TM3];
+        zero(acc);
+        if (up) {
+            mac_rows(blkA(0, 1), blkA(1, 3), r0, lane, acc);
+            mac_rows(blkA(0, 2), blkA(2, 3), r0, lane, acc);
+            mac_rows(blkA(0, 3), blkDU(3), r0, lane, acc);
+        } else {
+            mac_rows(blkA(3, 2), blkA(2, 0), r0, lane, acc);
+            mac_rows(blkA(3, 1), blkA(1, 0), r0, lane, acc);
+            mac_rows(blkA(3, 0), blkDL(0), r0, lane, acc);
+        }
+        __syncthreads();
+        store_c(up ? blkA(0, 3) : blkA(3, 0), r0, lane, acc, -1.f);
+        __syncthreads();
+    }
+    emit_block(true, 0, 3, blkA(0, 3), xu, pu, mode, tid);
+    emit_block(false, 3, 0, blkA(3, 0), xl, pv, mode, tid);
 }
 
 }  // namespace
 
 cudaError_t zs_launch_diag_block(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
                                  const int *slots, int nslot, int *pivflag, float *inv32, int64_t inv32_stride,
-                                 cudaStream_t st) {
-    if (nb <= 0 || nb > NB || nslot <= 0) return cudaErrorInvalidValue;
+                                 float *dinv, int64_t dinv_stride, float *winv, int mode, cudaStream_t st) {
+    if (nb <= 0 || nb > NB || nslot <= 0 || !dinv) return cudaErrorInvalidValue;
+    if (winv && mode != 1 && mode != 2) return cudaErrorInvalidValue;
     // once per process (thread-safe initialisation of a local static)
     static const cudaError_t attr = cudaFuncSetAttribute(k_diag_block, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (attr != cudaSuccess) return attr;
     k_diag_block<<<nslot, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag, inv32,
-                                                       inv32_stride);
-    return cudaGetLastError();
-}
-
-cudaError_t zs_launch_block_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
-                                const int *slots, int nslot, const float *inv32, int64_t inv32_stride, float *dinv,
-                                int64_t dinv_stride, float *winv, int mode, cudaStream_t st) {
-    if (nb <= 0 || nb > NB || nslot <= 0) return cudaErrorInvalidValue;
-    if (winv && mode != 1 && mode != 2) return cudaErrorInvalidValue;
-    // once per process (thread-safe initialisation of a local static)
-    static const cudaError_t attr = cudaFuncSetAttribute(k_block_inv, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kInvSmemBytes);
-    if (attr != cudaSuccess) return attr;
-    k_block_inv<<<dim3(8, nslot), kThreads, kInvSmemBytes, st>>>(z32, ld, plane, z32_stride, J, nb, inv32,
-                                                                  inv32_stride, dinv, dinv_stride, winv, mode, slots);
+                                                       inv32_stride, dinv, dinv_stride, winv, mode);
     return cudaGetLastError();
 }

@@ -222,10 +222,9 @@ int factor_slots_simt(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, ln.stream);
             ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
-                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ln.stream));
-            ZS_CU(zs_launch_block_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot, ctx->inv32,
-                                      inv32_stride, ctx->dinv, ctx->dinv_stride, nullptr, 0, ln.stream));
-            sp.done(2);
+                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->dinv, ctx->dinv_stride,
+                                       nullptr, 0, ln.stream));
+            sp.done(1);
         }
         if (J + nb >= n) break;
         {
@@ -273,11 +272,9 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
         {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, ln.stream);
             ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
-                                       ctx->d_pivflag, ctx->inv32, inv32_stride, ln.stream));
-            ZS_CU(zs_launch_block_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot, ctx->inv32,
-                                      inv32_stride, ctx->dinv, ctx->dinv_stride, last ? nullptr : ctx->winv, mode,
-                                      ln.stream));
-            sp.done(2);
+                                       ctx->d_pivflag, nullptr, 0, ctx->dinv, ctx->dinv_stride,
+                                       last ? nullptr : ctx->winv, mode, ln.stream));
+            sp.done(1);
         }
         if (last) break;
         {
@@ -773,7 +770,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->z32, (size_t)S * ctx->z32_stride * sizeof(float));
     ALLOC(ctx->pack, (size_t)S * ctx->pack_stride * sizeof(float));
     ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
-    ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
+    if (gemm_mode(ctx->opts) == 0) ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
     if (gemm_mode(ctx->opts) != 0) ALLOC(ctx->winv, (size_t)S * ZS_WINV_STRIDE * sizeof(float));
     ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
     ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
@@ -823,7 +820,10 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
         cudaMemset(ctx->prog, 0, (size_t)S * 2 * sizeof(unsigned long long)) != cudaSuccess ||
         cudaMemset(ctx->d_status, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(ctx->d_pivflag, 0, S * sizeof(int)) != cudaSuccess ||
-        cudaMemset(ctx->z32, 0, (size_t)S * ctx->z32_stride * sizeof(float)) != cudaSuccess)
+        cudaMemset(ctx->z32, 0, (size_t)S * ctx->z32_stride * sizeof(float)) != cudaSuccess ||
+        // the inverse blocks outside the triangles stay zero: the factorisation writes only the triangles
+        cudaMemset(ctx->dinv, 0, (size_t)S * ctx->dinv_stride * sizeof(float)) != cudaSuccess ||
+        (ctx->winv && cudaMemset(ctx->winv, 0, (size_t)S * ZS_WINV_STRIDE * sizeof(float)) != cudaSuccess))
         return bail(ZSOLVE_ECUDA);
     if (ctx->opts.resid == ZSOLVE_RESID_DF) {
         if (cudaMalloc(&ctx->xs, (size_t)S * nrhs_max * n * sizeof(float4)) != cudaSuccess) return bail(ZSOLVE_ENOMEM);
