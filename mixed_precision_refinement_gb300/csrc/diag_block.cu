@@ -246,12 +246,65 @@ __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float(r);
 }
 
-constexpr int TM3 = 4;  // rows per warp task of the distance-3 inverse blocks
+// ---------------------------------------------------------------- inverse windows
+//
+// The 128 x 128 inverses are built in four windows W(q), q = 0..3.  W(q)
+// runs once panel q is final: for q < 3 on warps 4-15 while warps 0-3 factor
+// the next panel's diagonal sub-block, W(3) on all warps after the last
+// panel.  W(q)
+//   - writes block row q of the factor (from the diagonal on) and block
+//     column q below it back to the float32 matrix, and DU_q, DL_q out as
+//     the diagonal blocks of W and V;
+//   - forms G_U(q, b) = DU_q U_qb (b > q) and G_L(q, m) = DL_q L_qm (m < q)
+//     in place of those factor blocks (written back by now);
+//   - completes column q of W and row q of V by distance from the diagonal:
+//     W_lq = -sum_{m=l+1..q} G_U(l, m) W_mq,  V_qk = -sum_{m=k..q-1} G_L(q, m) V_mk
+//     (W_qq = DU_q, V_qq = DL_q), writing each round out.
+// Shared-memory slots of the results: a diagonal factor block once written
+// back, or an L block whose V row is complete.  V_10, V_21 and V_20 stay for
+// W(3); W_23 and W_13 live within W(3).
+// Block ids: 4 i + j for A(i, j), 16 + k for DU_k, 20 + k for DL_k.
+struct WinOut {
+    unsigned char dst, nterm, neg, eu, el, ek;  // eu: 1 = W block (el, ek), 0 = V block, 2 = not written out
+    unsigned char tp[3], tq[3];                 // terms Pm(tp) Qm(tq)
+};
+constexpr int kWinRounds = 10;
+__constant__ WinOut kWin[kWinRounds][3] = {
+    // W(0): G_U(0,1), G_U(0,2), G_U(0,3)
+    {{1, 1, 0, 2, 0, 0, {16}, {1}}, {2, 1, 0, 2, 0, 0, {16}, {2}}, {3, 1, 0, 2, 0, 0, {16}, {3}}},
+    // W(1): G_U(1,2), G_U(1,3), G_L(1,0)
+    {{6, 1, 0, 2, 0, 0, {17}, {6}}, {7, 1, 0, 2, 0, 0, {17}, {7}}, {4, 1, 0, 2, 0, 0, {21}, {4}}},
+    //       W_01 = -G_U(0,1) DU_1 -> A(1,1);  V_10 = -G_L(1,0) DL_0 -> A(0,0)
+    {{5, 1, 1, 1, 0, 1, {1}, {17}}, {0, 1, 1, 0, 1, 0, {4}, {20}}},
+    // W(2): G_U(2,3), G_L(2,0), G_L(2,1)
+    {{11, 1, 0, 2, 0, 0, {18}, {11}}, {8, 1, 0, 2, 0, 0, {22}, {8}}, {9, 1, 0, 2, 0, 0, {22}, {9}}},
+    //       W_12 = -G_U(1,2) DU_2 -> A(1,1);  V_21 = -G_L(2,1) DL_1 -> A(2,2)
+    {{5, 1, 1, 1, 1, 2, {6}, {18}}, {10, 1, 1, 0, 2, 1, {9}, {21}}},
+    //       W_02 = -(G_U(0,1) W_12 + G_U(0,2) DU_2) -> A(1,0)
+    //       V_20 = -(G_L(2,1) V_10 + G_L(2,0) DL_0) -> A(2,0)
+    {{4, 2, 1, 1, 0, 2, {1, 2}, {5, 18}}, {8, 2, 1, 0, 2, 0, {9, 8}, {0, 20}}},
+    // W(3): G_L(3,0), G_L(3,1), G_L(3,2)
+    {{12, 1, 0, 2, 0, 0, {23}, {12}}, {13, 1, 0, 2, 0, 0, {23}, {13}}, {14, 1, 0, 2, 0, 0, {23}, {14}}},
+    //       W_23 = -G_U(2,3) DU_3 -> A(1,1);  V_32 = -G_L(3,2) DL_2 -> A(1,0)
+    {{5, 1, 1, 1, 2, 3, {11}, {19}}, {4, 1, 1, 0, 3, 2, {14}, {22}}},
+    //       W_13 = -(G_U(1,2) W_23 + G_U(1,3) DU_3) -> A(2,1)
+    //       V_31 = -(G_L(3,2) V_21 + G_L(3,1) DL_1) -> A(3,3)
+    {{9, 2, 1, 1, 1, 3, {6, 7}, {5, 19}}, {15, 2, 1, 0, 3, 1, {14, 13}, {10, 21}}},
+    //       W_03 = -(G_U(0,1) W_13 + G_U(0,2) W_23 + G_U(0,3) DU_3) -> A(1,0)
+    //       V_30 = -(G_L(3,2) V_20 + G_L(3,1) V_10 + G_L(3,0) DL_0) -> A(3,3)
+    {{4, 3, 1, 1, 0, 3, {1, 2, 3}, {9, 5, 19}}, {15, 3, 1, 0, 3, 0, {14, 13, 12}, {8, 0, 20}}},
+};
+__constant__ unsigned char kWinFirst[4] = {0, 1, 3, 6};  // first round of W(q); W(q) has q + 1 rounds
+__constant__ unsigned char kWinOuts[kWinRounds] = {3, 3, 2, 3, 2, 2, 3, 2, 2, 2};
 
-// Off-diagonal sub-blocks (a, b) of the factor: U for a < b, L for a > b;
-// the first 8 and the last 4 are formed in two passes.
-__constant__ unsigned char kOff[12][2] = {{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}, {2, 3},
-                                          {1, 0}, {2, 0}, {3, 0}, {2, 1}, {3, 1}, {3, 2}};
+__device__ __forceinline__ Blk blk_id(int id) {
+    return id < 16 ? blkA(id >> 2, id & 3) : (id < 20 ? blkDU(id - 16) : blkDL(id - 20));
+}
+
+template <int NT, int BAR>
+__device__ __forceinline__ void group_sync() {
+    asm volatile("bar.sync %0, %1;" ::"n"(BAR), "n"(NT) : "memory");
+}
 
 // Block (l, k) of W = U^-1 (upper) or of V = L^-1, held in shared memory at
 // S, out to the dense inverse xr ([re, im][128][128] of that triangle) and,
@@ -259,36 +312,133 @@ __constant__ unsigned char kOff[12][2] = {{0, 1}, {0, 2}, {0, 3}, {1, 2}, {1, 3}
 // row r holds column r of W resp. row r of V as Br = [Re | -Im] and
 // Bi = [Im | Re], in tf32 hi (planes 0, 2) and, for mode 2, lo (1, 3).
 // Blocks outside the triangles are zero in both and are never written.
+// Threads t < nt of the calling group take part, four entries each.
+__device__ __forceinline__ float4 f4(float a, float b, float c, float d) { return make_float4(a, b, c, d); }
+__device__ __forceinline__ float4 tf32_4(const float4 v) {
+    return f4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+}
+__device__ __forceinline__ float4 sub4(const float4 a, const float4 b) { return f4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
+__device__ __forceinline__ float4 neg4(const float4 a) { return f4(-a.x, -a.y, -a.z, -a.w); }
+
 __device__ __noinline__ void emit_block(bool upper, int l, int k, const Blk S, float *xr, float *pl, int mode,
-                                        int tid) {
-    for (int idx = tid; idx < P * P; idx += kThreads) {
-        const int i = idx >> 5, j = idx & 31;
-        const cf v = ld_c(S, i, j);
+                                        int t, int nt) {
+    for (int idx = t; idx < P * P / 4; idx += nt) {
+        const int i = idx >> 3, j = (idx & 7) * 4;
+        const float4 re = *reinterpret_cast<const float4 *>(&smem[S.off + i * S.ld + j]);
+        const float4 im = *reinterpret_cast<const float4 *>(&smem[S.off + S.im + i * S.ld + j]);
         const int o = (l * P + i) * NB + k * P + j;
-        xr[o] = v.re;
-        xr[NB * NB + o] = v.im;
+        *reinterpret_cast<float4 *>(xr + o) = re;
+        *reinterpret_cast<float4 *>(xr + NB * NB + o) = im;
     }
     if (!pl) return;
-    for (int idx = tid; idx < P * P; idx += kThreads) {
-        // consecutive threads write consecutive pack positions
-        const int i = upper ? (idx & 31) : (idx >> 5), j = upper ? (idx >> 5) : (idx & 31);
-        const cf v = ld_c(S, i, j);
-        const int prow = upper ? k * P + j : l * P + i;
-        const int m = upper ? l * P + i : k * P + j;
-        const int o = prow * (2 * NB) + m;
-        const float hr = tf32_rna(v.re), hi = tf32_rna(v.im);
-        pl[o] = hr;
-        pl[o + NB] = -hi;
-        pl[2 * ZS_WINV_PLANE + o] = hi;
-        pl[2 * ZS_WINV_PLANE + o + NB] = hr;
+    for (int idx = t; idx < P * P / 4; idx += nt) {
+        // four consecutive pack positions per thread, consecutive threads continue the row
+        float4 re, im;
+        int o;
+        if (upper) {  // W(32 l + i0 + u, 32 k + j) -> pack row 32 k + j, position 32 l + i0 + u
+            const int j = idx >> 3, i0 = (idx & 7) * 4;
+            const cf v0 = ld_c(S, i0, j), v1 = ld_c(S, i0 + 1, j), v2 = ld_c(S, i0 + 2, j), v3 = ld_c(S, i0 + 3, j);
+            re = f4(v0.re, v1.re, v2.re, v3.re);
+            im = f4(v0.im, v1.im, v2.im, v3.im);
+            o = (k * P + j) * (2 * NB) + l * P + i0;
+        } else {      // V(32 l + i, 32 k + j0 + u) -> pack row 32 l + i, position 32 k + j0 + u
+            const int i = idx >> 3, j0 = (idx & 7) * 4;
+            re = *reinterpret_cast<const float4 *>(&smem[S.off + i * S.ld + j0]);
+            im = *reinterpret_cast<const float4 *>(&smem[S.off + S.im + i * S.ld + j0]);
+            o = (l * P + i) * (2 * NB) + k * P + j0;
+        }
+        const float4 hr = tf32_4(re), hi = tf32_4(im);
+        *reinterpret_cast<float4 *>(pl + o) = hr;
+        *reinterpret_cast<float4 *>(pl + o + NB) = neg4(hi);
+        *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o) = hi;
+        *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o + NB) = hr;
         if (mode == 2) {
-            const float lr = tf32_rna(v.re - hr), li = tf32_rna(v.im - hi);
-            pl[ZS_WINV_PLANE + o] = lr;
-            pl[ZS_WINV_PLANE + o + NB] = -li;
-            pl[3 * ZS_WINV_PLANE + o] = li;
-            pl[3 * ZS_WINV_PLANE + o + NB] = lr;
+            const float4 lr = tf32_4(sub4(re, hr)), li = tf32_4(sub4(im, hi));
+            *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o) = lr;
+            *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o + NB) = neg4(li);
+            *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o) = li;
+            *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o + NB) = lr;
         }
     }
+}
+
+struct WinArgs {
+    float *gre, *gim;
+    int64_t ld, J;
+    int nb, mode;
+    float *xu, *xl, *pu, *pv;  // dense inverse of U and L; operand packs of W and V (or null)
+};
+
+// One round of W(q): its output blocks, 32 / TM tasks of TM rows each (one
+// task per warp of the group), stored after the group's barrier (a result
+// may replace one of its own operands), then written out.
+template <int TM, int NT, int BAR>
+__device__ __forceinline__ void win_round(int r, int t, int lane, const WinArgs &w) {
+    constexpr int TPB = P / TM;
+    const int nout = kWinOuts[r];
+    const int wi = t >> 5, b = wi / TPB, r0 = (wi % TPB) * TM;
+    const bool on = b < nout;
+    cf acc[TM];
+    zero(acc);
+    if (on) {
+        const int nterm = kWin[r][b].nterm;
+#pragma unroll 1
+        for (int i = 0; i < nterm; i++) mac_rows(blk_id(kWin[r][b].tp[i]), blk_id(kWin[r][b].tq[i]), r0, lane, acc);
+    }
+    group_sync<NT, BAR>();
+    if (on) store_c(blk_id(kWin[r][b].dst), r0, lane, acc, kWin[r][b].neg ? -1.f : 1.f);
+    group_sync<NT, BAR>();
+#pragma unroll 1
+    for (int o = 0; o < nout; o++) {
+        const int eu = kWin[r][o].eu;
+        if (eu != 2)
+            emit_block(eu == 1, kWin[r][o].el, kWin[r][o].ek, blk_id(kWin[r][o].dst), eu ? w.xu : w.xl,
+                       eu ? w.pu : w.pv, w.mode, t, NT);
+    }
+}
+
+// W(q) on a group of NT threads (t = thread index in the group), barrier BAR.
+// The G round takes 8-row tasks (12 for its three blocks); the chain rounds
+// (two blocks) TMC rows.
+template <int NT, int BAR, int TMC>
+__device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArgs &w) {
+    static_assert(3 * (P / 8) * 32 <= NT && 2 * (P / TMC) * 32 <= NT, "one task per warp");
+    // write-back: block row q from the diagonal on, then block column q below
+    // it, four columns per thread (scalar where the block's last columns
+    // stop inside the four)
+    const int c0 = q * P, wrow = (NB - c0) / 4, nrow = P * wrow, ncol = (NB - c0 - P) * (P / 4);
+    for (int idx = t; idx < nrow + ncol; idx += NT) {
+        int i, j;
+        if (idx < nrow) {
+            i = c0 + idx / wrow;
+            j = c0 + (idx % wrow) * 4;
+        } else {
+            const int e = idx - nrow;
+            i = c0 + P + (e >> 3);
+            j = c0 + (e & 7) * 4;
+        }
+        if (i < w.nb && j < w.nb) {
+            const int64_t g = (w.J + i) * w.ld + w.J + j;
+            const float4 re = *reinterpret_cast<const float4 *>(&smem[i * LDA + j]);
+            const float4 im = *reinterpret_cast<const float4 *>(&smem[IM_A + i * LDA + j]);
+            if (j + 4 <= w.nb) {
+                *reinterpret_cast<float4 *>(w.gre + g) = re;
+                *reinterpret_cast<float4 *>(w.gim + g) = im;
+            } else {
+                const float r4[4] = {re.x, re.y, re.z, re.w}, i4[4] = {im.x, im.y, im.z, im.w};
+                for (int u = 0; u < w.nb - j; u++) {
+                    w.gre[g + u] = r4[u];
+                    w.gim[g + u] = i4[u];
+                }
+            }
+        }
+    }
+    emit_block(true, q, q, blkDU(q), w.xu, w.pu, w.mode, t, NT);
+    emit_block(false, q, q, blkDL(q), w.xl, w.pv, w.mode, t, NT);
+    const int r0 = kWinFirst[q];
+    win_round<8, NT, BAR>(r0, t, lane, w);
+#pragma unroll 1
+    for (int r = r0 + 1; r <= r0 + q; r++) win_round<TMC, NT, BAR>(r, t, lane, w);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -326,9 +476,25 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
     __syncthreads();
     const float tiny = 1e-30f * __uint_as_float(s_amax);
 
-    // ---- LU, one 32-column panel at a time
+    WinArgs wa;
+    wa.gre = gre;
+    wa.gim = gim;
+    wa.ld = ld;
+    wa.J = J;
+    wa.nb = nb;
+    wa.mode = mode;
+    wa.xl = dinv + (int64_t)slot * dinv_stride + (J / NB) * 4 * NB * NB;  // [L, U][re, im][128][128]
+    wa.xu = wa.xl + 2 * NB * NB;
+    wa.pu = winv ? winv + (int64_t)slot * ZS_WINV_STRIDE : nullptr;
+    wa.pv = winv ? wa.pu + 4 * ZS_WINV_PLANE : nullptr;
+
+    // ---- LU, one 32-column panel at a time; W(p - 1) beside the base LU of panel p
     for (int p = 0; p < 4; p++) {
-        if (warp < kLuWarps && base_lu(p, warp, lane, tiny) && lane == 0) s_bad = 1;
+        if (warp < kLuWarps) {
+            if (base_lu(p, warp, lane, tiny) && lane == 0) s_bad = 1;
+        } else if (p > 0) {
+            inverse_window<kThreads - kLuWarps * 32, 2, 8>(p - 1, tid - kLuWarps * 32, lane, wa);
+        }
         __syncthreads();
         base_inv(p, warp, lane);
         __syncthreads();
@@ -366,13 +532,9 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
         __syncthreads();
     }
 
-    // ---- the factor out; the 32 x 32 inverses too when the FP32 block solves want them
-    for (int idx = tid; idx < nb * nb; idx += kThreads) {
-        const int i = idx / nb, j = idx - i * nb;
-        const int64_t g = (J + i) * ld + J + j;
-        gre[g] = smem[i * LDA + j];
-        gim[g] = smem[IM_A + i * LDA + j];
-    }
+    inverse_window<kThreads, 0, 4>(3, tid, lane, wa);
+
+    // ---- the 32 x 32 inverses, when the FP32 block solves want them
     if (inv32) {
         float *d32 = inv32 + (int64_t)slot * inv32_stride + (J / NB) * ZS_INV32_STRIDE;
         for (int idx = tid; idx < 8 * P * P; idx += kThreads) {
@@ -386,109 +548,6 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
         }
     }
     if (tid == 0 && s_bad) pivflag[slot] = 1;
-
-    // ---- the 128 x 128 inverses W = U^-1 and V = L^-1 by block substitution
-    float *const xw = dinv + (int64_t)slot * dinv_stride + (J / NB) * 4 * NB * NB;  // [L, U][re, im][128][128]
-    float *const xu = xw + 2 * NB * NB, *const xl = xw;
-    float *const pu = winv ? winv + (int64_t)slot * ZS_WINV_STRIDE : nullptr;
-    float *const pv = winv ? pu + 4 * ZS_WINV_PLANE : nullptr;
-#pragma unroll 1
-    for (int k = 0; k < 4; k++) {
-        emit_block(true, k, k, blkDU(k), xu, pu, mode, tid);
-        emit_block(false, k, k, blkDL(k), xl, pv, mode, tid);
-    }
-    // G_U(a, b) = DU_a U_ab (a < b) and G_L(i, m) = DL_i L_im (i > m), in place
-    // of the factor's off-diagonal sub-blocks: 12 blocks, two 16-row tasks
-    // each, as 8 blocks and then 4 (a block's rows are all read before any is
-    // overwritten).
-#pragma unroll 1
-    for (int g0 = 0; g0 < 12; g0 += 8) {
-        const int q = g0 + (warp >> 1), r0 = (warp & 1) * TMR;
-        const bool on = q < 12 && (g0 == 0 || warp < 8);
-        const int qc = q < 12 ? q : 11;
-        const int a = kOff[qc][0], b = kOff[qc][1];
-        const Blk F = blkA(a, b);
-        cf acc[TMR];
-        zero(acc);
-        if (on) mac_rows(a < b ? blkDU(a) : blkDL(a), F, r0, lane, acc);
-        __syncthreads();
-        if (on) store_c(F, r0, lane, acc, 1.f);
-    }
-    __syncthreads();
-    // Chains, by distance from the diagonal.  Storage: the factor's diagonal
-    // sub-blocks are free now; W_12 goes to A(0,0), V_21 to A(2,2), results
-    // only written out to A(1,1) (W) and A(3,3) (V), and a result whose G
-    // block has no later use to that block.
-    //   distance 1: W_{k-1,k} = -G_U(k-1,k) DU_k,  V_{k+1,k} = -G_L(k+1,k) DL_k
-    {
-        const int q = warp >> 1, r0 = (warp & 1) * TMR;
-        const bool on = warp < 12;
-        const bool up = q < 3;
-        const int k = up ? q + 1 : q - 3;                 // column block
-        const int l = up ? k - 1 : k + 1;                 // row block
-        const Blk Gb = blkA(l, k);
-        const Blk dst = up ? (k == 1 ? blkA(1, 1) : k == 2 ? blkA(0, 0) : blkA(2, 3))
-                           : (k == 0 ? blkA(1, 0) : k == 1 ? blkA(2, 2) : blkA(3, 3));
-        cf acc[TMR];
-        zero(acc);
-        if (on) mac_rows(Gb, up ? blkDU(k) : blkDL(k), r0, lane, acc);
-        __syncthreads();
-        if (on) store_c(dst, r0, lane, acc, -1.f);
-        __syncthreads();
-    }
-    emit_block(true, 0, 1, blkA(1, 1), xu, pu, mode, tid);
-    emit_block(true, 1, 2, blkA(0, 0), xu, pu, mode, tid);
-    emit_block(true, 2, 3, blkA(2, 3), xu, pu, mode, tid);
-    emit_block(false, 1, 0, blkA(1, 0), xl, pv, mode, tid);
-    emit_block(false, 2, 1, blkA(2, 2), xl, pv, mode, tid);
-    emit_block(false, 3, 2, blkA(3, 3), xl, pv, mode, tid);
-    //   distance 2: W_02 = -(G_U(0,1) W_12 + G_U(0,2) DU_2)   -> A(1,1)
-    //               W_13 = -(G_U(1,2) W_23 + G_U(1,3) DU_3)   -> A(1,3)
-    //               V_20 = -(G_L(2,1) V_10 + G_L(2,0) DL_0)   -> A(2,0)
-    //               V_31 = -(G_L(3,2) V_21 + G_L(3,1) DL_1)   -> A(3,3)
-    {
-        const int q = warp >> 2, r0 = (warp & 3) * TMU;
-        Blk g1, x1, g2, d2, dst;
-        switch (q) {
-            case 0: g1 = blkA(0, 1); x1 = blkA(0, 0); g2 = blkA(0, 2); d2 = blkDU(2); dst = blkA(1, 1); break;
-            case 1: g1 = blkA(1, 2); x1 = blkA(2, 3); g2 = blkA(1, 3); d2 = blkDU(3); dst = blkA(1, 3); break;
-            case 2: g1 = blkA(2, 1); x1 = blkA(1, 0); g2 = blkA(2, 0); d2 = blkDL(0); dst = blkA(2, 0); break;
-            default: g1 = blkA(3, 2); x1 = blkA(2, 2); g2 = blkA(3, 1); d2 = blkDL(1); dst = blkA(3, 3); break;
-        }
-        cf acc[TMU];
-        zero(acc);
-        mac_rows(g1, x1, r0, lane, acc);
-        mac_rows(g2, d2, r0, lane, acc);
-        __syncthreads();
-        store_c(dst, r0, lane, acc, -1.f);
-        __syncthreads();
-    }
-    emit_block(true, 0, 2, blkA(1, 1), xu, pu, mode, tid);
-    emit_block(true, 1, 3, blkA(1, 3), xu, pu, mode, tid);
-    emit_block(false, 2, 0, blkA(2, 0), xl, pv, mode, tid);
-    emit_block(false, 3, 1, blkA(3, 3), xl, pv, mode, tid);
-    //   distance 3: W_03 = -(G_U(0,1) W_13 + G_U(0,2) W_23 + G_U(0,3) DU_3)   -> A(0,3)
-    //               V_30 = -(G_L(3,2) V_20 + G_L(3,1) V_10 + G_L(3,0) DL_0)   -> A(3,0)
-    {
-        const bool up = warp < 8;
-        const int r0 = (warp & 7) * TM3;
-        cf acc[TM3];
-        zero(acc);
-        if (up) {
-            mac_rows(blkA(0, 1), blkA(1, 3), r0, lane, acc);
-            mac_rows(blkA(0, 2), blkA(2, 3), r0, lane, acc);
-            mac_rows(blkA(0, 3), blkDU(3), r0, lane, acc);
-        } else {
-            mac_rows(blkA(3, 2), blkA(2, 0), r0, lane, acc);
-            mac_rows(blkA(3, 1), blkA(1, 0), r0, lane, acc);
-            mac_rows(blkA(3, 0), blkDL(0), r0, lane, acc);
-        }
-        __syncthreads();
-        store_c(up ? blkA(0, 3) : blkA(3, 0), r0, lane, acc, -1.f);
-        __syncthreads();
-    }
-    emit_block(true, 0, 3, blkA(0, 3), xu, pu, mode, tid);
-    emit_block(false, 3, 0, blkA(3, 0), xl, pv, mode, tid);
 }
 
 }  // namespace

@@ -83,7 +83,7 @@ struct zsolve_ctx {
         cudaStream_t stream = nullptr;  // lane 0: the context's stream
         cudaStream_t side = nullptr;    // packs the next block solves' operands next to the diagonal block
         bool own_stream = false;
-        cudaEvent_t ev[4] = {nullptr, nullptr, nullptr, nullptr};
+        cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
         cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
         int *d_active = nullptr, *h_active = nullptr;  // slots still refining
         unsigned *ticket = nullptr;     // triangular-solve task tickets
@@ -560,29 +560,39 @@ int assemble_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi,
     return ZSOLVE_OK;
 }
 
-// One lane's share of a batch (frequencies f0+first.. of the sweep),
-// assembled unless `assembled`, then factored and refined on ln's stream.
-// xb and ib are the batch's base (slot 0).
-int run_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi, const double *G, const double2 *b,
-             double2 *xb, int nrhs, int first, int count, zsolve_info *ib, bool assembled) {
-    const int64_t n = ctx->n;
+// One lane's share of a batch (slots first..first+count-1): assembled unless
+// `assembled`, then factored on ln's stream; ln.ev[0..2] mark the start, the
+// end of the assembly and the end of the factorisation.
+int factor_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi, const double *G, int first,
+                int count, bool assembled) {
     if (!assembled) ZS_TRY(assemble_lane(ctx, ln, L, Psi, G, first, count));
     ZS_TRY(factor_slots(ctx, ln, ctx->d_all + first, count, first));
     ZS_CU(cudaEventRecord(ln.ev[2], ln.stream));
-    zsolve_info *inf = ib ? ib + first : nullptr;
-    const int st = refine_batch(ctx, ln, b, xb, (int64_t)nrhs * n, nrhs, first, count, inf);
+    return ZSOLVE_OK;
+}
+
+// Refinement of the batch's slots 0..count-1 on ln's stream, after every
+// lane in fl[0..nl) has factored its range [lo[i], lo[i] + cnt[i]); then
+// the per-frequency timings.  xb and ib are the batch's base (slot 0).
+int refine_lanes(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *xb, int nrhs, int count, zsolve_info *ib,
+                 Lane *const *fl, const int *lo, const int *cnt, int nl) {
+    ZS_CU(cudaEventRecord(ln.ev[3], ln.stream));  // refinement starts
+    const int st = refine_batch(ctx, ln, b, xb, (int64_t)nrhs * ctx->n, nrhs, 0, count, ib);
     if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
-    ZS_CU(cudaEventRecord(ln.ev[3], ln.stream));
-    ZS_CU(cudaEventSynchronize(ln.ev[3]));
-    if (inf) {
-        float a = 0, fct = 0, r = 0;
-        cudaEventElapsedTime(&a, ln.ev[0], ln.ev[1]);
-        cudaEventElapsedTime(&fct, ln.ev[1], ln.ev[2]);
-        cudaEventElapsedTime(&r, ln.ev[2], ln.ev[3]);
-        for (int i = 0; i < count; i++) {
-            inf[i].ms_assemble = a / count;
-            inf[i].ms_factor = fct / count;
-            inf[i].ms_refine = r / count;
+    ZS_CU(cudaEventRecord(ln.ev[4], ln.stream));
+    ZS_CU(cudaEventSynchronize(ln.ev[4]));
+    if (ib) {
+        float r = 0;
+        cudaEventElapsedTime(&r, ln.ev[3], ln.ev[4]);
+        for (int k = 0; k < nl; k++) {
+            float a = 0, fct = 0;
+            cudaEventElapsedTime(&a, fl[k]->ev[0], fl[k]->ev[1]);
+            cudaEventElapsedTime(&fct, fl[k]->ev[1], fl[k]->ev[2]);
+            for (int i = lo[k]; i < lo[k] + cnt[k]; i++) {
+                ib[i].ms_assemble = a / cnt[k];
+                ib[i].ms_factor = fct / cnt[k];
+                ib[i].ms_refine = r / count;
+            }
         }
     }
     return st;
@@ -608,13 +618,19 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
         int st;
         if (ctx->opts.lanes == 1 || count < 2) {
             l0.tc_grid = ctx->num_sms;
-            st = run_lane(ctx, l0, L, Psi, G, b, xb, nrhs, 0, count, ib, false);
+            ZS_TRY(factor_lane(ctx, l0, L, Psi, G, 0, count, false));
+            Lane *fl[1] = {&l0};
+            const int lo[1] = {0}, cnt[1] = {count};
+            st = refine_lanes(ctx, l0, b, xb, nrhs, count, ib, fl, lo, cnt, 1);
         } else {
-            // lane 1 starts after lane 0's assembly (and everything queued
-            // before it on the context's stream: inputs, parameters), so that
-            // its own FP64-bound assembly runs under lane 0's factorisation and
-            // the two lanes' outer-block steps stay out of phase; the
-            // context's stream continues only after lane 1 has finished
+            // Two lanes factor the batch's halves side by side.  Lane 1
+            // starts after lane 0's assembly (and everything queued before it
+            // on the context's stream: inputs, parameters), so that its own
+            // FP64-bound assembly runs under lane 0's factorisation and the
+            // two lanes' outer-block steps stay out of phase.  The refinement
+            // then runs once over the whole batch on the context's stream: its
+            // triangular solves are latency-bound and its residuals bound by
+            // the FP64 pipe over all SMs, so two lanes of them only contend.
             const int h = (count + 1) / 2;
             // each lane's persistent tcgen05 grids leave room for the other
             // lane's diagonal blocks (one CTA per frequency)
@@ -629,7 +645,7 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
                     st1 = fail(ctx, ZSOLVE_ECUDA, "second lane: cudaSetDevice failed");
                     return;
                 }
-                st1 = run_lane(ctx, l1, L, Psi, G, b, xb, nrhs, h, count - h, ib, false);
+                st1 = factor_lane(ctx, l1, L, Psi, G, h, count - h, false);
             };
             std::thread worker;
             bool threaded = true;
@@ -638,13 +654,16 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
             } catch (...) {
                 threaded = false;  // no thread: the lanes run one after the other
             }
-            const int st0 = run_lane(ctx, l0, L, Psi, G, b, xb, nrhs, 0, h, ib, true);
+            const int st0 = factor_lane(ctx, l0, L, Psi, G, 0, h, true);
             if (threaded) worker.join();
             else lane1();
             ZS_CU(cudaEventRecord(l1.ev_join, l1.stream));
             ZS_CU(cudaStreamWaitEvent(l0.stream, l1.ev_join, 0));
-            const bool hard0 = st0 != ZSOLVE_OK && st0 != ZSOLVE_ESINGULAR;
-            st = hard0 ? st0 : (st1 != ZSOLVE_OK ? st1 : st0);
+            ZS_TRY(st0);
+            ZS_TRY(st1);
+            Lane *fl[2] = {&l0, &l1};
+            const int lo[2] = {0, h}, cnt[2] = {h, count - h};
+            st = refine_lanes(ctx, l0, b, xb, nrhs, count, ib, fl, lo, cnt, 2);
         }
         if (st != ZSOLVE_OK && first_err == ZSOLVE_OK) first_err = st;
         if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
