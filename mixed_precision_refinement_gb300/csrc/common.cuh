@@ -107,7 +107,8 @@ __device__ __forceinline__ long long progress_wait(const unsigned long long *p, 
             return -1;
         }
         if ((it & 1023u) == 0 && (*(volatile const unsigned *)status & ZS_DEV_TIMEOUT)) return -1;
-        if (it > 32) __nanosleep(it > 4096 ? 256 : 32);
+        // short sleeps once the block just before the needed one is in work
+        if (it > 32) __nanosleep(c == need || it <= 4096 ? 32 : 256);
     }
 }
 

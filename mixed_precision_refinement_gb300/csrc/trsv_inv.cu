@@ -34,20 +34,75 @@ __device__ __forceinline__ long long warp_progress(const unsigned long long *p, 
     return c;
 }
 
-constexpr int kThreads = 512;  // 16 warps, 8 rows each
+// Sum of each of NV values over the warp's 32 lanes, as a reduce-scatter:
+// at every level a lane keeps half of its values and adds the partner's
+// copy of that half (16 + 8 + ... shuffles instead of 5 NV).  Afterwards
+// lane l holds the sums with indices ((l >> s) & (NV / K - 1)) * K + u,
+// u < K, in v[0..K), K = max(NV / 32, 1), s = log2(32 K / NV) (lanes that
+// differ in their low s bits hold the same sums).
+template <int NV, int M = 16>
+__device__ __forceinline__ void reduce_scatter(float (&v)[NV], int lane) {
+    if constexpr (M >= 1) {
+        if constexpr (NV >= 2) {
+            constexpr int H = NV / 2;
+            const bool hi = (lane & M) != 0;
+            float w[H];
+#pragma unroll
+            for (int k = 0; k < H; k++) {
+                const float send = hi ? v[k] : v[k + H];
+                const float keep = hi ? v[k + H] : v[k];
+                w[k] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+            }
+            if constexpr (M > 1) {
+                reduce_scatter<H, M / 2>(w, lane);
+            }
+#pragma unroll
+            for (int k = 0; k < H; k++) v[k] = w[k];
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], M);
+            if constexpr (M > 1) reduce_scatter<NV, M / 2>(v, lane);
+        }
+    }
+}
 
+// After reduce_scatter<16 R>: the number of sums a lane holds, and the index
+// of its first one (values are laid out [row 0..7][rhs][re, im]).
+template <int R>
+struct Scatter {
+    static constexpr int NV = 16 * R;
+    static constexpr int K = NV >= 32 ? NV / 32 : 1;
+    static constexpr int SHIFT = NV >= 32 ? 0 : (NV == 16 ? 1 : (NV == 8 ? 2 : 3));
+    __device__ static int first(int lane) { return ((lane >> SHIFT) & (NV / K - 1)) * K; }
+    // one lane of each group of equal holders writes
+    __device__ static bool writer(int lane) { return (lane & ((1 << SHIFT) - 1)) == 0; }
+};
+
+constexpr int kThreads = 512;  // 16 warps, 8 rows each
+constexpr size_t kSmemBytes = (size_t)2 * TB * TB * sizeof(float);  // the task's inverse block, re and im
+
+// The critical step of a task is its last chunk (the block just before it in
+// the chain) and then the product with its inverse block.  Everything that
+// does not depend on that block's solution is started first: the inverse
+// block is copied into shared memory at the start of the task (cp.async),
+// the task's right-hand side is loaded as soon as it is final, and each
+// chunk's factor rows are loaded into registers before the wait for the
+// chunk's solution (with one right-hand side; more keep the loads after the
+// wait to stay in registers).
 template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
 k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
            const float *__restrict__ dinv, int64_t dinv_stride, float2 *__restrict__ v, int64_t v_stride,
            const int *__restrict__ slots, int nslot, unsigned long long *__restrict__ prog, unsigned epoch,
            unsigned *ticket, unsigned *status) {
+    constexpr bool kPreload = R == 1;
+    extern __shared__ __align__(16) float sinv[];  // [re, im][TB][TB]
     __shared__ cf part[TB][R];
     __shared__ cf rv[TB][R];
     __shared__ unsigned s_task, s_stop;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nblk = (int)((n + TB - 1) / TB);
     const unsigned total = 2u * (unsigned)nblk * (unsigned)nslot;
+    const uint32_t sinv_addr = (uint32_t)__cvta_generic_to_shared(sinv);
     while (true) {
         __syncthreads();
         if (tid == 0) {
@@ -66,17 +121,16 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
         const float *re = z32 + (int64_t)slot * z32_stride;
         const float *im = re + plane;
         const float *ir = dinv + (int64_t)slot * dinv_stride + (int64_t)b * 4 * TB * TB + (int64_t)phase * 2 * TB * TB;
-        const float *ii = ir + TB * TB;
         float2 *vs = v + (int64_t)slot * v_stride;
         unsigned long long *pf = prog + 2 * (int64_t)slot, *pb = pf + 1;
         const int64_t r0 = (int64_t)b * TB;
         const int rows = (int)zs::min64(TB, n - r0);
-        // the inverse block is needed last: start pulling it into L2 now
-        {
-            const char *p0 = reinterpret_cast<const char *>(ir);
-            for (int q = tid; q < 2 * TB * TB * 4 / 128; q += kThreads)
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(p0 + (int64_t)q * 128));
-        }
+        const int64_t wrow = (r0 + warp * 8) * ld;  // offset of the warp's first row
+        // the inverse block (re and im planes are contiguous) into shared memory
+        for (int q = tid; q < 2 * TB * TB / 4; q += kThreads)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sinv_addr + 16u * q), "l"(ir + 4 * q)
+                         : "memory");
+        asm volatile("cp.async.commit_group;" ::: "memory");
         cf acc[8][R];
 #pragma unroll
         for (int i = 0; i < 8; i++)
@@ -84,9 +138,34 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
             for (int r = 0; r < R; r++) acc[i][r] = cf{0.f, 0.f};
         bool ok = true;
         if (phase == 1) ok = warp_progress(pf, epoch, b, status, lane) >= 0;  // own forward result
+        // the block's right-hand side (final now: the input, resp. the forward result)
+        cf vb = cf{0.f, 0.f};
+        const int ei = tid / R, er = tid - ei * R;
+        if (tid < TB * R && ei < rows && ok) {
+            const float2 t2 = __ldcg(&vs[er * n + r0 + ei]);
+            vb = cf{t2.x, t2.y};
+        }
         const int nchunk = phase == 0 ? b : nblk - 1 - b;
         long long ready = 0;
-        for (int q = 0; q < nchunk && ok;) {
+        for (int q = 0; q < nchunk && ok; q++) {
+            const int c = phase == 0 ? q : nblk - 1 - q;
+            // lane owns 4 consecutive columns: one 16-byte load per row and plane
+            const int64_t col = (int64_t)c * TB + 4 * lane;
+            const bool full = col + 3 < n;
+            float4 ar4[8], ai4[8];
+            // the warp's 8 rows of the chunk, by pointer steps (rows past the
+            // block's end read its first row; their sums are not stored)
+            const float *pc = re + wrow + col;
+            if (kPreload && full) {
+                const float *pr = pc;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    const float *ps = warp * 8 + i < rows ? pr : re + r0 * ld + col;
+                    ar4[i] = __ldg(reinterpret_cast<const float4 *>(ps));
+                    ai4[i] = __ldg(reinterpret_cast<const float4 *>(ps + plane));
+                    pr += ld;
+                }
+            }
             if (q >= ready) {
                 ready = warp_progress(phase == 0 ? pf : pb, epoch, q, status, lane);
                 if (ready < 0) {
@@ -94,82 +173,78 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
                     break;
                 }
             }
-            const int qend = (int)(ready < nchunk ? ready : nchunk);
-            for (; q < qend; q++) {
-                const int c = phase == 0 ? q : nblk - 1 - q;
-                // lane owns 4 consecutive columns: one 16-byte load per row and plane
-                const int64_t col = (int64_t)c * TB + 4 * lane;
-                if (col + 3 < n) {
-                    cf y[4][R];
+            if (full) {
+                cf y[4][R];
+#pragma unroll
+                for (int e = 0; e < 4; e++)
+#pragma unroll
+                    for (int r = 0; r < R; r++) {
+                        const float2 t2 = __ldcg(&vs[r * n + col + e]);
+                        y[e][r] = cf{t2.x, t2.y};
+                    }
+                const float *pr = pc;
+#pragma unroll
+                for (int i = 0; i < 8; i++) {
+                    if (!kPreload) {
+                        const float *ps = warp * 8 + i < rows ? pr : re + r0 * ld + col;
+                        ar4[i] = __ldg(reinterpret_cast<const float4 *>(ps));
+                        ai4[i] = __ldg(reinterpret_cast<const float4 *>(ps + plane));
+                        pr += ld;
+                    }
+                    const cf a[4] = {cf{ar4[i].x, ai4[i].x}, cf{ar4[i].y, ai4[i].y}, cf{ar4[i].z, ai4[i].z},
+                                     cf{ar4[i].w, ai4[i].w}};
 #pragma unroll
                     for (int e = 0; e < 4; e++)
 #pragma unroll
                         for (int r = 0; r < R; r++) {
-                            const float2 t2 = __ldcg(&vs[r * n + col + e]);
-                            y[e][r] = cf{t2.x, t2.y};
+                            acc[i][r].re = fmaf(a[e].re, y[e][r].re, fmaf(-a[e].im, y[e][r].im, acc[i][r].re));
+                            acc[i][r].im = fmaf(a[e].re, y[e][r].im, fmaf(a[e].im, y[e][r].re, acc[i][r].im));
                         }
+                }
+            } else {
+                for (int e = 0; e < 4; e++) {
+                    if (col + e >= n) break;
+                    cf y[R];
+#pragma unroll
+                    for (int r = 0; r < R; r++) {
+                        const float2 t2 = __ldcg(&vs[r * n + col + e]);
+                        y[r] = cf{t2.x, t2.y};
+                    }
 #pragma unroll
                     for (int i = 0; i < 8; i++) {
                         const int li = warp * 8 + i;
-                        const int64_t g = (r0 + (li < rows ? li : 0)) * ld + col;
-                        const float4 ar4 = __ldg(reinterpret_cast<const float4 *>(re + g));
-                        const float4 ai4 = __ldg(reinterpret_cast<const float4 *>(im + g));
-                        const cf a[4] = {cf{ar4.x, ai4.x}, cf{ar4.y, ai4.y}, cf{ar4.z, ai4.z}, cf{ar4.w, ai4.w}};
-#pragma unroll
-                        for (int e = 0; e < 4; e++)
-#pragma unroll
-                            for (int r = 0; r < R; r++) {
-                                acc[i][r].re = fmaf(a[e].re, y[e][r].re, fmaf(-a[e].im, y[e][r].im, acc[i][r].re));
-                                acc[i][r].im = fmaf(a[e].re, y[e][r].im, fmaf(a[e].im, y[e][r].re, acc[i][r].im));
-                            }
-                    }
-                } else {
-                    for (int e = 0; e < 4; e++) {
-                        if (col + e >= n) break;
-                        cf y[R];
+                        const int64_t g = (r0 + (li < rows ? li : 0)) * ld + col + e;
+                        const cf a = cf{__ldg(re + g), __ldg(im + g)};
 #pragma unroll
                         for (int r = 0; r < R; r++) {
-                            const float2 t2 = __ldcg(&vs[r * n + col + e]);
-                            y[r] = cf{t2.x, t2.y};
-                        }
-#pragma unroll
-                        for (int i = 0; i < 8; i++) {
-                            const int li = warp * 8 + i;
-                            const int64_t g = (r0 + (li < rows ? li : 0)) * ld + col + e;
-                            const cf a = cf{__ldg(re + g), __ldg(im + g)};
-#pragma unroll
-                            for (int r = 0; r < R; r++) {
-                                acc[i][r].re = fmaf(a.re, y[r].re, fmaf(-a.im, y[r].im, acc[i][r].re));
-                                acc[i][r].im = fmaf(a.re, y[r].im, fmaf(a.im, y[r].re, acc[i][r].im));
-                            }
+                            acc[i][r].re = fmaf(a.re, y[r].re, fmaf(-a.im, y[r].im, acc[i][r].re));
+                            acc[i][r].im = fmaf(a.re, y[r].im, fmaf(a.im, y[r].re, acc[i][r].im));
                         }
                     }
                 }
             }
         }
+        {
+            float s[16 * R];
 #pragma unroll
-        for (int i = 0; i < 8; i++)
+            for (int i = 0; i < 8; i++)
 #pragma unroll
-            for (int r = 0; r < R; r++) {
-                float x = acc[i][r].re, y = acc[i][r].im;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    x += __shfl_xor_sync(0xffffffffu, x, o);
-                    y += __shfl_xor_sync(0xffffffffu, y, o);
+                for (int r = 0; r < R; r++) {
+                    s[(i * R + r) * 2] = acc[i][r].re;
+                    s[(i * R + r) * 2 + 1] = acc[i][r].im;
                 }
-                if (lane == 0) part[warp * 8 + i][r] = cf{x, y};
+            reduce_scatter(s, lane);
+            float *pw = reinterpret_cast<float *>(&part[warp * 8][0]);
+            if (Scatter<R>::writer(lane)) {
+                const int f = Scatter<R>::first(lane);
+#pragma unroll
+                for (int u = 0; u < Scatter<R>::K; u++) pw[f + u] = s[u];
             }
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
         if (!__syncthreads_and(ok ? 1 : 0)) continue;  // a wait gave up: uniform skip
         // right-hand side of the block's own triangle
-        for (int e = tid; e < TB * R; e += kThreads) {
-            const int i = e / R, r = e - i * R;
-            cf val = cf{0.f, 0.f};
-            if (i < rows) {
-                const float2 t2 = __ldcg(&vs[r * n + r0 + i]);
-                val = cf{t2.x - part[i][r].re, t2.y - part[i][r].im};
-            }
-            rv[i][r] = val;
-        }
+        if (tid < TB * R) rv[ei][er] = ei < rows ? cf{vb.re - part[ei][er].re, vb.im - part[ei][er].im} : cf{0.f, 0.f};
         __syncthreads();
         // y = inverse block . rv: warp w rows 8w..8w+7, lanes over columns
         cf acc2[8][R];
@@ -187,8 +262,8 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
 #pragma unroll
             for (int i = 0; i < 8; i++) {
                 const int li = warp * 8 + i;
-                const float4 ar4 = __ldg(reinterpret_cast<const float4 *>(ir + li * TB + j0));
-                const float4 ai4 = __ldg(reinterpret_cast<const float4 *>(ii + li * TB + j0));
+                const float4 ar4 = *reinterpret_cast<const float4 *>(&sinv[li * TB + j0]);
+                const float4 ai4 = *reinterpret_cast<const float4 *>(&sinv[TB * TB + li * TB + j0]);
                 const cf a[4] = {cf{ar4.x, ai4.x}, cf{ar4.y, ai4.y}, cf{ar4.z, ai4.z}, cf{ar4.w, ai4.w}};
 #pragma unroll
                 for (int e = 0; e < 4; e++)
@@ -199,23 +274,31 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
                     }
             }
         }
+        {
+            float s[16 * R];
 #pragma unroll
-        for (int i = 0; i < 8; i++)
+            for (int i = 0; i < 8; i++)
 #pragma unroll
-            for (int r = 0; r < R; r++) {
-                float x = acc2[i][r].re, y = acc2[i][r].im;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    x += __shfl_xor_sync(0xffffffffu, x, o);
-                    y += __shfl_xor_sync(0xffffffffu, y, o);
+                for (int r = 0; r < R; r++) {
+                    s[(i * R + r) * 2] = acc2[i][r].re;
+                    s[(i * R + r) * 2 + 1] = acc2[i][r].im;
                 }
-                const int li = warp * 8 + i;
-                if (lane == 0 && li < rows) __stcg(&vs[r * n + r0 + li], make_float2(x, y));
+            reduce_scatter(s, lane);
+            if (Scatter<R>::writer(lane)) {
+                const int f = Scatter<R>::first(lane);
+#pragma unroll
+                for (int u = 0; u < Scatter<R>::K; u++) {
+                    const int idx = f + u, c = idx & 1, r = (idx >> 1) % R, li = warp * 8 + (idx >> 1) / R;
+                    if (li < rows) __stcg(reinterpret_cast<float *>(&vs[r * n + r0 + li]) + c, s[u]);
+                }
             }
-        __threadfence();
+        }
+        // the barrier orders every warp's stores before thread 0's release,
+        // which (being cumulative) publishes them with the progress word
         __syncthreads();
         if (tid == 0) zs::progress_set(phase == 0 ? pf : pb, epoch, (unsigned)(phase == 0 ? b + 1 : bq + 1));
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
 template <int R>
@@ -223,8 +306,12 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
                        int64_t dinv_stride, float2 *v, int64_t v_stride, const int *slots, int nslot,
                        unsigned long long *prog, unsigned epoch, unsigned *ticket, unsigned *status, int num_sms,
                        cudaStream_t st) {
+    // once per process and instance (thread-safe initialisation of a local static)
+    static const cudaError_t attr =
+        cudaFuncSetAttribute(k_trsv_inv<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    if (attr != cudaSuccess) return attr;
     int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_trsv_inv<R>, kThreads, 0);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_trsv_inv<R>, kThreads, kSmemBytes);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) per_sm = 1;
     const int64_t nblk = (n + TB - 1) / TB;
@@ -237,7 +324,7 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
     // CTAs that are already running have claimed, so the solve progresses
     // with any number of resident CTAs -- also while another stream's kernels
     // hold part of the GPU.
-    k_trsv_inv<R><<<(unsigned)grid, kThreads, 0, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride,
+    k_trsv_inv<R><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride,
                                                        slots, nslot, prog, epoch, ticket, status);
     return cudaGetLastError();
 }
