@@ -47,13 +47,19 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
 #pragma unroll
         for (int r = 0; r < R; r++) ar[u][r] = ai[u][r] = 0.0;
     // full 128-entry steps first: the bound is the same for every lane, so the
-    // warp vote below always sees the whole warp
-    int64_t base = 0;
-    for (; base + 128 <= n; base += 128) {
-        const int64_t j = base + lane;
+    // warp vote below always sees the whole warp.  Loop counts are 32-bit and
+    // addresses advance by pointer steps: 64-bit integer tests and products
+    // can be issued to the FP64 pipe on this part, the bound of this kernel.
+    const int nn = (int)n, nfull = nn >> 7;
+    const double2 *zp = zr + lane;
+    const double2 *xp[R];
+#pragma unroll
+    for (int r = 0; r < R; r++) xp[r] = xs + r * n + lane;
+#pragma unroll 1
+    for (int s = 0; s < nfull; s++) {
         double2 z[4];
 #pragma unroll
-        for (int u = 0; u < 4; u++) z[u] = __ldcs(zr + j + 32 * u);
+        for (int u = 0; u < 4; u++) z[u] = __ldcs(zp + 32 * u);
         // warp-uniform test: every real part in these 128 entries an exact zero
         bool re0 = true;
 #pragma unroll
@@ -63,7 +69,7 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
             for (int u = 0; u < 4; u++)
 #pragma unroll
                 for (int r = 0; r < R; r++) {
-                    const double2 xv = __ldg(xs + r * n + j + 32 * u);
+                    const double2 xv = __ldg(xp[r] + 32 * u);
                     ar[u % NA][r] = fma(zs::neg_bits(z[u].y), xv.y, ar[u % NA][r]);
                     ai[u % NA][r] = fma(z[u].y, xv.x, ai[u % NA][r]);
                 }
@@ -72,24 +78,29 @@ k_residual(const double2 *__restrict__ z64, int64_t z64_stride, int64_t n, const
             for (int u = 0; u < 4; u++)
 #pragma unroll
                 for (int r = 0; r < R; r++) {
-                    const double2 xv = __ldg(xs + r * n + j + 32 * u);
+                    const double2 xv = __ldg(xp[r] + 32 * u);
                     ar[u % NA][r] = fma(z[u].x, xv.x, ar[u % NA][r]);
                     ai[u % NA][r] = fma(z[u].x, xv.y, ai[u % NA][r]);
                     ar[u % NA][r] = fma(zs::neg_bits(z[u].y), xv.y, ar[u % NA][r]);
                     ai[u % NA][r] = fma(z[u].y, xv.x, ai[u % NA][r]);
                 }
         }
+        zp += 128;
+#pragma unroll
+        for (int r = 0; r < R; r++) xp[r] += 128;
     }
-    for (int64_t j = base + lane; j < n; j += 32) {
-        const double2 z = __ldcs(zr + j);
+    for (int j = (nfull << 7) + lane; j < nn; j += 32) {
+        const double2 z = __ldcs(zp);
 #pragma unroll
         for (int r = 0; r < R; r++) {
-            const double2 xv = __ldg(xs + r * n + j);
+            const double2 xv = __ldg(xp[r]);
             ar[0][r] = fma(z.x, xv.x, ar[0][r]);
             ai[0][r] = fma(z.x, xv.y, ai[0][r]);
             ar[0][r] = fma(zs::neg_bits(z.y), xv.y, ar[0][r]);
             ai[0][r] = fma(z.y, xv.x, ai[0][r]);
+            xp[r] += 32;
         }
+        zp += 32;
     }
 #pragma unroll
     for (int r = 0; r < R; r++) {
