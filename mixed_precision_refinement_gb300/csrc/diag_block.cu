@@ -320,45 +320,60 @@ __device__ __forceinline__ float4 tf32_4(const float4 v) {
 __device__ __forceinline__ float4 sub4(const float4 a, const float4 b) { return f4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w); }
 __device__ __forceinline__ float4 neg4(const float4 a) { return f4(-a.x, -a.y, -a.z, -a.w); }
 
-__device__ __noinline__ void emit_block(bool upper, int l, int k, const Blk S, float *xr, float *pl, int mode,
-                                        int t, int nt) {
-    for (int idx = t; idx < P * P / 4; idx += nt) {
+__device__ __forceinline__ void emit_one(bool upper, int l, int k, const Blk S, float *xr, float *pl, int mode,
+                                         int idx, bool dense) {
+    if (dense) {
         const int i = idx >> 3, j = (idx & 7) * 4;
         const float4 re = *reinterpret_cast<const float4 *>(&smem[S.off + i * S.ld + j]);
         const float4 im = *reinterpret_cast<const float4 *>(&smem[S.off + S.im + i * S.ld + j]);
         const int o = (l * P + i) * NB + k * P + j;
         *reinterpret_cast<float4 *>(xr + o) = re;
         *reinterpret_cast<float4 *>(xr + NB * NB + o) = im;
+        return;
     }
-    if (!pl) return;
-    for (int idx = t; idx < P * P / 4; idx += nt) {
-        // four consecutive pack positions per thread, consecutive threads continue the row
-        float4 re, im;
-        int o;
-        if (upper) {  // W(32 l + i0 + u, 32 k + j) -> pack row 32 k + j, position 32 l + i0 + u
-            const int j = idx >> 3, i0 = (idx & 7) * 4;
-            const cf v0 = ld_c(S, i0, j), v1 = ld_c(S, i0 + 1, j), v2 = ld_c(S, i0 + 2, j), v3 = ld_c(S, i0 + 3, j);
-            re = f4(v0.re, v1.re, v2.re, v3.re);
-            im = f4(v0.im, v1.im, v2.im, v3.im);
-            o = (k * P + j) * (2 * NB) + l * P + i0;
-        } else {      // V(32 l + i, 32 k + j0 + u) -> pack row 32 l + i, position 32 k + j0 + u
-            const int i = idx >> 3, j0 = (idx & 7) * 4;
-            re = *reinterpret_cast<const float4 *>(&smem[S.off + i * S.ld + j0]);
-            im = *reinterpret_cast<const float4 *>(&smem[S.off + S.im + i * S.ld + j0]);
-            o = (l * P + i) * (2 * NB) + k * P + j0;
-        }
-        const float4 hr = tf32_4(re), hi = tf32_4(im);
-        *reinterpret_cast<float4 *>(pl + o) = hr;
-        *reinterpret_cast<float4 *>(pl + o + NB) = neg4(hi);
-        *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o) = hi;
-        *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o + NB) = hr;
-        if (mode == 2) {
-            const float4 lr = tf32_4(sub4(re, hr)), li = tf32_4(sub4(im, hi));
-            *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o) = lr;
-            *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o + NB) = neg4(li);
-            *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o) = li;
-            *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o + NB) = lr;
-        }
+    // four consecutive pack positions per thread, consecutive threads continue the row
+    float4 re, im;
+    int o;
+    if (upper) {  // W(32 l + i0 + u, 32 k + j) -> pack row 32 k + j, position 32 l + i0 + u
+        const int j = idx >> 3, i0 = (idx & 7) * 4;
+        const cf v0 = ld_c(S, i0, j), v1 = ld_c(S, i0 + 1, j), v2 = ld_c(S, i0 + 2, j), v3 = ld_c(S, i0 + 3, j);
+        re = f4(v0.re, v1.re, v2.re, v3.re);
+        im = f4(v0.im, v1.im, v2.im, v3.im);
+        o = (k * P + j) * (2 * NB) + l * P + i0;
+    } else {      // V(32 l + i, 32 k + j0 + u) -> pack row 32 l + i, position 32 k + j0 + u
+        const int i = idx >> 3, j0 = (idx & 7) * 4;
+        re = *reinterpret_cast<const float4 *>(&smem[S.off + i * S.ld + j0]);
+        im = *reinterpret_cast<const float4 *>(&smem[S.off + S.im + i * S.ld + j0]);
+        o = (l * P + i) * (2 * NB) + k * P + j0;
+    }
+    const float4 hr = tf32_4(re), hi = tf32_4(im);
+    *reinterpret_cast<float4 *>(pl + o) = hr;
+    *reinterpret_cast<float4 *>(pl + o + NB) = neg4(hi);
+    *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o) = hi;
+    *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o + NB) = hr;
+    if (mode == 2) {
+        const float4 lr = tf32_4(sub4(re, hr)), li = tf32_4(sub4(im, hi));
+        *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o) = lr;
+        *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o + NB) = neg4(li);
+        *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o) = li;
+        *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o + NB) = lr;
+    }
+}
+
+// A W block (lw, kw) at Sw and a V block (lv, kv) at Sv written out together
+// (more stores in flight per thread): work items 0..255 the W block, 256..511
+// the V block, first the dense inverses, then the packs.
+__device__ __noinline__ void emit_pair(int lw, int kw, const Blk Sw, int lv, int kv, const Blk Sv, float *xu,
+                                       float *xl, float *pu, float *pv, int mode, int t, int nt) {
+    constexpr int NI = P * P / 4;
+    for (int idx = t; idx < 2 * NI; idx += nt) {
+        if (idx < NI) emit_one(true, lw, kw, Sw, xu, pu, mode, idx, true);
+        else emit_one(false, lv, kv, Sv, xl, pv, mode, idx - NI, true);
+    }
+    if (!pu) return;
+    for (int idx = t; idx < 2 * NI; idx += nt) {
+        if (idx < NI) emit_one(true, lw, kw, Sw, xu, pu, mode, idx, false);
+        else emit_one(false, lv, kv, Sv, xl, pv, mode, idx - NI, false);
     }
 }
 
@@ -388,53 +403,47 @@ __device__ __forceinline__ void win_round(int r, int t, int lane, const WinArgs 
     group_sync<NT, BAR>();
     if (on) store_c(blk_id(kWin[r][b].dst), r0, lane, acc, kWin[r][b].neg ? -1.f : 1.f);
     group_sync<NT, BAR>();
-#pragma unroll 1
-    for (int o = 0; o < nout; o++) {
-        const int eu = kWin[r][o].eu;
-        if (eu != 2)
-            emit_block(eu == 1, kWin[r][o].el, kWin[r][o].ek, blk_id(kWin[r][o].dst), eu ? w.xu : w.xl,
-                       eu ? w.pu : w.pv, w.mode, t, NT);
-    }
+    // a chain round's outputs are one W block (0) and one V block (1); G blocks are not written out
+    if (kWin[r][0].eu != 2)
+        emit_pair(kWin[r][0].el, kWin[r][0].ek, blk_id(kWin[r][0].dst), kWin[r][1].el, kWin[r][1].ek,
+                  blk_id(kWin[r][1].dst), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
 }
 
 // W(q) on a group of NT threads (t = thread index in the group), barrier BAR.
 // The G round takes 8-row tasks (12 for its three blocks); the chain rounds
 // (two blocks) TMC rows.
 template <int NT, int BAR, int TMC>
-__device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArgs &w) {
+__device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArgs &wa) {
     static_assert(3 * (P / 8) * 32 <= NT && 2 * (P / TMC) * 32 <= NT, "one task per warp");
+    const WinArgs w = wa;  // in registers: stores through the pointers cannot alias it
     // write-back: block row q from the diagonal on, then block column q below
-    // it, four columns per thread (scalar where the block's last columns
-    // stop inside the four)
-    const int c0 = q * P, wrow = (NB - c0) / 4, nrow = P * wrow, ncol = (NB - c0 - P) * (P / 4);
-    for (int idx = t; idx < nrow + ncol; idx += NT) {
-        int i, j;
-        if (idx < nrow) {
-            i = c0 + idx / wrow;
-            j = c0 + (idx % wrow) * 4;
+    // it, four columns per thread (scalar where the block's last columns stop
+    // inside the four); offsets from the block's corner fit in 32 bits
+    float *const cre = w.gre + (w.J * w.ld + w.J), *const cim = w.gim + (w.J * w.ld + w.J);
+    const int ld = (int)w.ld, nb = w.nb, c0 = q * P;
+    auto put = [&](int i, int j) {
+        if (i >= nb || j >= nb) return;
+        const int g = i * ld + j;
+        const float4 re = *reinterpret_cast<const float4 *>(&smem[i * LDA + j]);
+        const float4 im = *reinterpret_cast<const float4 *>(&smem[IM_A + i * LDA + j]);
+        if (j + 4 <= nb) {
+            *reinterpret_cast<float4 *>(cre + g) = re;
+            *reinterpret_cast<float4 *>(cim + g) = im;
         } else {
-            const int e = idx - nrow;
-            i = c0 + P + (e >> 3);
-            j = c0 + (e & 7) * 4;
-        }
-        if (i < w.nb && j < w.nb) {
-            const int64_t g = (w.J + i) * w.ld + w.J + j;
-            const float4 re = *reinterpret_cast<const float4 *>(&smem[i * LDA + j]);
-            const float4 im = *reinterpret_cast<const float4 *>(&smem[IM_A + i * LDA + j]);
-            if (j + 4 <= w.nb) {
-                *reinterpret_cast<float4 *>(w.gre + g) = re;
-                *reinterpret_cast<float4 *>(w.gim + g) = im;
-            } else {
-                const float r4[4] = {re.x, re.y, re.z, re.w}, i4[4] = {im.x, im.y, im.z, im.w};
-                for (int u = 0; u < w.nb - j; u++) {
-                    w.gre[g + u] = r4[u];
-                    w.gim[g + u] = i4[u];
-                }
+            const float r4[4] = {re.x, re.y, re.z, re.w}, i4[4] = {im.x, im.y, im.z, im.w};
+            for (int u = 0; u < nb - j; u++) {
+                cre[g + u] = r4[u];
+                cim[g + u] = i4[u];
             }
         }
+    };
+    for (int idx = t; idx < P * (NB / 4); idx += NT) {  // rows c0.., all columns from c0 on
+        const int i = c0 + (idx >> 5), j = (idx & 31) * 4;
+        if (j >= c0) put(i, j);
     }
-    emit_block(true, q, q, blkDU(q), w.xu, w.pu, w.mode, t, NT);
-    emit_block(false, q, q, blkDL(q), w.xl, w.pv, w.mode, t, NT);
+    for (int idx = t; idx < (NB - c0 - P) * (P / 4); idx += NT)  // rows below, columns c0..c0+31
+        put(c0 + P + (idx >> 3), c0 + (idx & 7) * 4);
+    emit_pair(q, q, blkDU(q), q, q, blkDL(q), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
     const int r0 = kWinFirst[q];
     win_round<8, NT, BAR>(r0, t, lane, w);
 #pragma unroll 1
