@@ -52,8 +52,8 @@ constexpr int IM_A = NB * LDA;           // re plane -> im plane of the block
 constexpr int OFF_D = 2 * NB * LDA;      // inverse sub-blocks [8][P][LDD]: 0-3 DU_p, 4-7 DL_p
 constexpr int IM_D = 8 * P * LDD;
 constexpr int OFF_R = OFF_D + 2 * IM_D;  // pivot reciprocals [re, im][4][P]
-constexpr int OFF_ROW = OFF_R + 8 * P;   // base-LU pivot row, [2 buffers][re, im][P]
-constexpr int kSmemFloats = OFF_ROW + 4 * P;
+constexpr int OFF_ROW = OFF_R + 8 * P;   // base-LU pivot rows of the panel, [P][re, im][P]
+constexpr int kSmemFloats = OFF_ROW + 2 * P * P;
 constexpr size_t kSmemBytes = (size_t)kSmemFloats * sizeof(float);
 
 extern __shared__ __align__(16) float smem[];
@@ -121,74 +121,94 @@ __device__ __forceinline__ void store_c(const Blk C, int r0, int lane, const cf 
     for (int t = 0; t < TM; t++) st_c(C, r0 + t, lane, cf{sgn * acc[t].re, sgn * acc[t].im});
 }
 
-// Step 1: LU of the 32 x 32 diagonal sub-block by warps 0-3: warp w holds
-// rows w + 4 t (t < 8) in registers, lane = column; at step k every warp
-// reads pivot row k from a double-buffered row in shared memory, updates its
-// rows below k (multipliers broadcast from lane k), and the owner of row k+1
-// publishes it before a 128-thread barrier.  The step loop stays rolled so
-// the code fits the instruction cache.  Returns true if a pivot was tiny or
-// not finite.
+// Step 1: LU of the 32 x 32 diagonal sub-block by warps 0-3, as a wavefront:
+// warp w holds rows 8w..8w+7 in registers (lane = column).  A row is final
+// once the steps of all rows above it are applied; its owner then publishes
+// it (and its pivot's reciprocal) to shared memory, raises that row's flag
+// to the panel's epoch, and carries on with its own rows below.  A warp
+// applies the steps of the rows above its own in order, each after waiting
+// for that row's flag only -- no barrier over all four warps per step.
+// Multipliers are broadcast from lane k.  Returns true if a pivot was tiny
+// or not finite, or a wait gave up (the frequency then takes the float64
+// fallback).
 constexpr int kLuWarps = 4;
 constexpr int kLuRows = P / kLuWarps;
 
-__device__ __forceinline__ void lu_barrier() { asm volatile("bar.sync 1, %0;" ::"n"(kLuWarps * 32) : "memory"); }
+// publication of a row: its stores (by the whole warp, ordered by the warp
+// barrier before this) become visible before the flag
+__device__ __forceinline__ void row_arrive(uint32_t flag, uint32_t epoch) {
+    __threadfence_block();
+    asm volatile("st.volatile.shared.u32 [%0], %1;" ::"r"(flag), "r"(epoch) : "memory");
+}
 
-__device__ bool base_lu(int p, int w, int lane, float tiny) {
+// bounded wait for a row's flag.  Every lane polls and the warp leaves
+// together: a wait on one lane while the others block at a shuffle made each
+// step some microseconds slower on this part.
+__device__ __forceinline__ bool row_wait(uint32_t flag, uint32_t epoch) {
+    bool ok = false;
+    for (unsigned it = 0; it < ZS_SPIN_LIMIT; it++) {
+        uint32_t v;
+        asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(flag) : "memory");
+        if (__all_sync(0xffffffffu, v == epoch)) {
+            ok = true;
+            break;
+        }
+    }
+    __threadfence_block();
+    return ok;
+}
+
+// rows a[t] (t < 8, rows below step k) take step k: multiplier from lane k
+// times the pivot reciprocal r; lanes right of k subtract it times u, lane k
+// keeps it.  Branch-free so the rows' chains overlap.
+__device__ __forceinline__ void lu_step(cf (&a)[kLuRows], int t0, int k, cf r, cf u, int lane) {
+    const bool right = lane > k, piv_lane = lane == k;
+#pragma unroll
+    for (int t = 0; t < kLuRows; t++) {
+        if (t < t0) continue;  // t0 is a constant wherever the caller's loop is unrolled
+        const cf l = {__shfl_sync(0xffffffffu, a[t].re, k), __shfl_sync(0xffffffffu, a[t].im, k)};
+        const cf m = zs::cmul(l, r);
+        const cf upd = zs::cfms(a[t], m, u);
+        a[t] = right ? upd : (piv_lane ? m : a[t]);
+    }
+}
+
+__device__ bool base_lu(int p, int w, int lane, float tiny, uint32_t rowflag) {
     const Blk B = blkA(p, p);
-    float *prow = smem + OFF_ROW;
+    float *rows = smem + OFF_ROW;
+    const uint32_t epoch = (uint32_t)(p + 1);  // flags hold the last panel that published the row
     cf a[kLuRows];
 #pragma unroll
-    for (int t = 0; t < kLuRows; t++) a[t] = ld_c(B, w + kLuWarps * t, lane);
-    if (w == 0) {
-        prow[lane] = a[0].re;
-        prow[P + lane] = a[0].im;
-    }
-    lu_barrier();
+    for (int t = 0; t < kLuRows; t++) a[t] = ld_c(B, w * kLuRows + t, lane);
     bool bad = false;
+    // the rows above this warp's, in order
 #pragma unroll 1
-    for (int k = 0; k < P; k++) {
-        const float *pr = prow + (k & 1) * 2 * P;
-        const cf piv = {pr[k], pr[P + k]};
-        const cf u = {pr[lane], pr[P + lane]};
+    for (int k = 0; k < w * kLuRows; k++) {
+        if (!row_wait(rowflag + 4u * k, epoch)) bad = true;
+        const cf u = {rows[k * 2 * P + lane], rows[k * 2 * P + P + lane]};
+        const cf r = {smem[OFF_R + p * P + k], smem[OFF_R + 4 * P + p * P + k]};
+        lu_step(a, 0, k, r, u, lane);
+    }
+    // this warp's rows: publish row s, then step s on the rows below it
+#pragma unroll
+    for (int s = 0; s < kLuRows; s++) {
+        const int k = w * kLuRows + s;
+        const cf piv = {__shfl_sync(0xffffffffu, a[s].re, k), __shfl_sync(0xffffffffu, a[s].im, k)};
         const float pm = fabsf(piv.re) + fabsf(piv.im);
         bad |= !(pm > tiny) || !(pm < 1e37f);
         const cf r = crecip_fast(piv);
-        if (w == 0 && lane == k) {
+        rows[k * 2 * P + lane] = a[s].re;
+        rows[k * 2 * P + P + lane] = a[s].im;
+        if (lane == 0) {
             smem[OFF_R + p * P + k] = r.re;
             smem[OFF_R + 4 * P + p * P + k] = r.im;
         }
-        // every row below k: multiplier from lane k; lanes right of k update,
-        // lane k keeps the multiplier.  Branch-free so the eight rows' chains overlap.
-        const bool right = lane > k, piv_lane = lane == k;
-        cf l[kLuRows];
-#pragma unroll
-        for (int t = 0; t < kLuRows; t++)
-            l[t] = cf{__shfl_sync(0xffffffffu, a[t].re, k), __shfl_sync(0xffffffffu, a[t].im, k)};
-#pragma unroll
-        for (int t = 0; t < kLuRows; t++) {
-            const bool below = w + kLuWarps * t > k;
-            const cf m = zs::cmul(l[t], r);
-            const cf upd = zs::cfms(a[t], m, u);
-            const cf nv = right ? upd : (piv_lane ? m : a[t]);
-            a[t] = below ? nv : a[t];
-        }
-        const int kn = k + 1;
-        if (kn < P) {
-            if (w == (kn & (kLuWarps - 1))) {  // row k+1 is final through step k: publish it
-                const int tn = kn / kLuWarps;
-                cf v = a[0];
-#pragma unroll
-                for (int t = 1; t < kLuRows; t++)
-                    if (t == tn) v = a[t];
-                float *pw = prow + (kn & 1) * 2 * P;
-                pw[lane] = v.re;
-                pw[P + lane] = v.im;
-            }
-            lu_barrier();
-        }
+        __syncwarp();
+        if (lane == 0) row_arrive(rowflag + 4u * k, epoch);
+        lu_step(a, s + 1, k, r, a[s], lane);
     }
 #pragma unroll
-    for (int t = 0; t < kLuRows; t++) st_c(B, w + kLuWarps * t, lane, a[t]);
+    for (int t = 0; t < kLuRows; t++) st_c(B, w * kLuRows + t, lane, a[t]);
     return bad;
 }
 
@@ -250,11 +270,10 @@ __device__ __forceinline__ float tf32_rna(float x) {
 //
 // The 128 x 128 inverses are built in four windows W(q), q = 0..3.  W(q)
 // runs once panel q is final: for q < 3 on warps 4-15 while warps 0-3 factor
-// the next panel's diagonal sub-block, W(3) on all warps after the last
-// panel.  W(q)
+// the next panel's diagonal sub-block (and then write DU_q, DL_q out as the
+// diagonal blocks of W and V), W(3) on all warps after the last panel.  W(q)
 //   - writes block row q of the factor (from the diagonal on) and block
-//     column q below it back to the float32 matrix, and DU_q, DL_q out as
-//     the diagonal blocks of W and V;
+//     column q below it back to the float32 matrix (W(3) also DU_3, DL_3);
 //   - forms G_U(q, b) = DU_q U_qb (b > q) and G_L(q, m) = DL_q L_qm (m < q)
 //     in place of those factor blocks (written back by now);
 //   - completes column q of W and row q of V by distance from the diagonal:
@@ -443,7 +462,9 @@ __device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArg
     }
     for (int idx = t; idx < (NB - c0 - P) * (P / 4); idx += NT)  // rows below, columns c0..c0+31
         put(c0 + P + (idx >> 3), c0 + (idx & 7) * 4);
-    emit_pair(q, q, blkDU(q), q, q, blkDL(q), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
+    // DU_q and DL_q: by the four LU warps for q < 3 (they finish the next
+    // panel's base LU well before the window ends), here for the last panel
+    if constexpr (NT == kThreads) emit_pair(q, q, blkDU(q), q, q, blkDL(q), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
     const int r0 = kWinFirst[q];
     win_round<8, NT, BAR>(r0, t, lane, w);
 #pragma unroll 1
@@ -457,13 +478,16 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
              int mode) {
     __shared__ unsigned s_amax;
     __shared__ int s_bad;
+    __shared__ unsigned s_rowflag[P];  // publication of the base LU's rows
     const int slot = slots[blockIdx.x];
     float *gre = z32 + (int64_t)slot * z32_stride;
     float *gim = gre + plane;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t rowflag = (uint32_t)__cvta_generic_to_shared(s_rowflag);
     if (tid == 0) {
         s_amax = 0u;
         s_bad = 0;
+        for (int k = 0; k < P; k++) s_rowflag[k] = 0u;
     }
     __syncthreads();
     // ---- load (identity padding beyond nb)
@@ -500,7 +524,10 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
     // ---- LU, one 32-column panel at a time; W(p - 1) beside the base LU of panel p
     for (int p = 0; p < 4; p++) {
         if (warp < kLuWarps) {
-            if (base_lu(p, warp, lane, tiny) && lane == 0) s_bad = 1;
+            if (base_lu(p, warp, lane, tiny, rowflag) && lane == 0) s_bad = 1;
+            if (p > 0)
+                emit_pair(p - 1, p - 1, blkDU(p - 1), p - 1, p - 1, blkDL(p - 1), wa.xu, wa.xl, wa.pu, wa.pv, mode,
+                          tid, kLuWarps * 32);
         } else if (p > 0) {
             inverse_window<kThreads - kLuWarps * 32, 2, 8>(p - 1, tid - kLuWarps * 32, lane, wa);
         }
