@@ -7,8 +7,10 @@
 // One CTA (16 warps) per frequency holds the block in shared memory and walks
 // it in four 32-column panels p:
 //   1. four warps factor the 32 x 32 diagonal sub-block A_pp in registers
-//      (lane = column, eight rows per warp, multipliers broadcast by shuffle,
-//      pivot rows passed through shared memory between 128-thread barriers);
+//      as a wavefront (lane = column, eight rows per warp, multipliers
+//      broadcast by shuffle, rows published through shared memory with a
+//      flag each), while the other warps run the inverse window of panel
+//      p - 1;
 //   2. all warps invert its triangles, DU_p = U_pp^-1 and DL_p = L_pp^-1
 //      (four columns of an inverse per warp, lane = row, substitution with
 //      the solved entries broadcast by shuffle);
@@ -226,9 +228,11 @@ __device__ __forceinline__ void base_inv(int p, int warp, int lane) {
     cf x[kInvCols];
 #pragma unroll
     for (int c = 0; c < kInvCols; c++) x[c] = cf{lane == j0 + c ? 1.f : 0.f, 0.f};
+    // steps on rows whose entries of these columns are all zero change
+    // nothing: U columns start at their last row, L columns at their first
     if (upper) {
 #pragma unroll 2
-        for (int k = P - 1; k >= 0; k--) {
+        for (int k = j0 + kInvCols - 1; k >= 0; k--) {
             const cf r = {smem[OFF_R + p * P + k], smem[OFF_R + 4 * P + p * P + k]};
             const cf u = ld_c(B, lane, k);  // U(lane, k), used by rows lane < k
             const bool open = lane < k, piv_lane = lane == k;
@@ -243,7 +247,7 @@ __device__ __forceinline__ void base_inv(int p, int warp, int lane) {
         }
     } else {
 #pragma unroll 2
-        for (int k = 0; k < P; k++) {
+        for (int k = j0; k < P; k++) {
             const cf l = ld_c(B, lane, k);  // L(lane, k), used by rows lane > k
             const bool open = lane > k;
 #pragma unroll
@@ -271,7 +275,9 @@ __device__ __forceinline__ float tf32_rna(float x) {
 // The 128 x 128 inverses are built in four windows W(q), q = 0..3.  W(q)
 // runs once panel q is final: for q < 3 on warps 4-15 while warps 0-3 factor
 // the next panel's diagonal sub-block (and then write DU_q, DL_q out as the
-// diagonal blocks of W and V), W(3) on all warps after the last panel.  W(q)
+// diagonal blocks of W and V), W(3) on all warps after the last panel.
+// (Running the windows on all warps after the wavefront LU instead was
+// slower.)  W(q)
 //   - writes block row q of the factor (from the diagonal on) and block
 //     column q below it back to the float32 matrix (W(3) also DU_3, DL_3);
 //   - forms G_U(q, b) = DU_q U_qb (b > q) and G_L(q, m) = DL_q L_qm (m < q)
