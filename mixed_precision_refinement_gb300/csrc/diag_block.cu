@@ -46,8 +46,6 @@ constexpr int LDA = NB + 4; // block row stride (floats): 16-byte aligned rows
 constexpr int LDD = P + 4;  // inverse sub-block row stride
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
-constexpr int TMR = 16;     // rows per warp task where results wait for a barrier (one task per warp)
-constexpr int TMU = 8;      // rows per warp task of the in-place trailing update
 
 // shared-memory layout (floats)
 constexpr int IM_A = NB * LDA;           // re plane -> im plane of the block
@@ -86,41 +84,98 @@ __device__ __forceinline__ cf crecip_fast(cf p) {
     return {a * rd, -b * rd};
 }
 
-// acc[t] += sum_k Pm(r0 + t, k) Qm(k, lane), t < TM, k < 32
-template <int TM>
-__device__ __forceinline__ void mac_rows(const Blk Pm, const Blk Qm, int r0, int lane, cf (&acc)[TM]) {
+// Complex block products on the tensor cores, warp by warp: mma.sync
+// m16n8k8 with tf32 operands and float32 accumulation, each real product
+// split in three passes (hi*hi + hi*lo + lo*hi, hi = tf32 rounding of x,
+// lo = tf32 rounding of x - hi), which is float32-class like the tcgen05
+// kernels' 3xTF32.  On this part the legacy mma path retires 0.5 m16n8k8 per
+// SM per clock, four times the FP32 FFMA rate, with one instruction per 1024
+// products.  A task is 16 rows x 8 NTILE columns of a 32 x 32 block:
+//   C(r0 + i, c0 + j) (+)= sum_k Pm(r0 + i, k) Qm(k, c0 + j),  k < 32,
+// kept as Re P Re Q, Im P Im Q and the imaginary part (Re C = rr - ii).
+// Fragment layout of m16n8k8 (g = lane / 4, t = lane % 4): A a0 (g, t),
+// a1 (g+8, t), a2 (g, t+4), a3 (g+8, t+4); B b0 (t, g), b1 (t+4, g);
+// C c0 (g, 2t), c1 (g, 2t+1), c2 (g+8, 2t), c3 (g+8, 2t+1).
+template <int NTILE>
+struct CAcc {
+    float rr[NTILE][4], ii[NTILE][4], ri[NTILE][4];
+};
+
+template <int NTILE>
+__device__ __forceinline__ void cacc_zero(CAcc<NTILE> &c) {
+#pragma unroll
+    for (int n = 0; n < NTILE; n++)
+#pragma unroll
+        for (int q = 0; q < 4; q++) c.rr[n][q] = c.ii[n][q] = c.ri[n][q] = 0.f;
+}
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t &hi, uint32_t &lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    const float r = x - __uint_as_float(hi);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+
+__device__ __forceinline__ void mma_tf32(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int NTILE>
+__device__ __forceinline__ void cmma(const Blk Pm, const Blk Qm, int r0, int c0, int lane, CAcc<NTILE> &c) {
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll 1
-    for (int k0 = 0; k0 < P; k0 += 4) {
-        float br[4], bi[4];
+    for (int k0 = 0; k0 < P; k0 += 8) {
+        const int ra = Pm.off + (r0 + g) * Pm.ld + k0 + t;
+        uint32_t arh[4], arl[4], aih[4], ail[4];
+        const int ao[4] = {0, 8 * Pm.ld, 4, 8 * Pm.ld + 4};
 #pragma unroll
         for (int q = 0; q < 4; q++) {
-            br[q] = smem[Qm.off + (k0 + q) * Qm.ld + lane];
-            bi[q] = smem[Qm.off + Qm.im + (k0 + q) * Qm.ld + lane];
+            split_tf32(smem[ra + ao[q]], arh[q], arl[q]);
+            split_tf32(smem[Pm.im + ra + ao[q]], aih[q], ail[q]);
         }
 #pragma unroll
-        for (int t = 0; t < TM; t++) {
-            const float4 ar = *reinterpret_cast<const float4 *>(&smem[Pm.off + (r0 + t) * Pm.ld + k0]);
-            const float4 ai = *reinterpret_cast<const float4 *>(&smem[Pm.off + Pm.im + (r0 + t) * Pm.ld + k0]);
-            const float xr[4] = {ar.x, ar.y, ar.z, ar.w}, xi[4] = {ai.x, ai.y, ai.z, ai.w};
-#pragma unroll
-            for (int q = 0; q < 4; q++) {
-                acc[t].re = fmaf(xr[q], br[q], fmaf(-xi[q], bi[q], acc[t].re));
-                acc[t].im = fmaf(xr[q], bi[q], fmaf(xi[q], br[q], acc[t].im));
-            }
+        for (int n = 0; n < NTILE; n++) {
+            const int rb = Qm.off + (k0 + t) * Qm.ld + c0 + 8 * n + g;
+            uint32_t brh0, brl0, brh1, brl1, bih0, bil0, bih1, bil1;
+            split_tf32(smem[rb], brh0, brl0);
+            split_tf32(smem[rb + 4 * Qm.ld], brh1, brl1);
+            split_tf32(smem[Qm.im + rb], bih0, bil0);
+            split_tf32(smem[Qm.im + rb + 4 * Qm.ld], bih1, bil1);
+            mma_tf32(c.rr[n], arh, brh0, brh1);
+            mma_tf32(c.rr[n], arh, brl0, brl1);
+            mma_tf32(c.rr[n], arl, brh0, brh1);
+            mma_tf32(c.ii[n], aih, bih0, bih1);
+            mma_tf32(c.ii[n], aih, bil0, bil1);
+            mma_tf32(c.ii[n], ail, bih0, bih1);
+            mma_tf32(c.ri[n], arh, bih0, bih1);
+            mma_tf32(c.ri[n], arh, bil0, bil1);
+            mma_tf32(c.ri[n], arl, bih0, bih1);
+            mma_tf32(c.ri[n], aih, brh0, brh1);
+            mma_tf32(c.ri[n], aih, brl0, brl1);
+            mma_tf32(c.ri[n], ail, brh0, brh1);
         }
     }
 }
 
-template <int TM>
-__device__ __forceinline__ void zero(cf (&acc)[TM]) {
+// C(r0 + i, c0 + j) = sgn * product (store) or -= product (sub)
+template <int NTILE, bool SUB>
+__device__ __forceinline__ void cacc_out(const Blk C, int r0, int c0, int lane, const CAcc<NTILE> &c, float sgn) {
+    const int g = lane >> 2, t = lane & 3;
 #pragma unroll
-    for (int t = 0; t < TM; t++) acc[t] = cf{0.f, 0.f};
-}
-
-template <int TM>
-__device__ __forceinline__ void store_c(const Blk C, int r0, int lane, const cf (&acc)[TM], float sgn) {
+    for (int n = 0; n < NTILE; n++)
 #pragma unroll
-    for (int t = 0; t < TM; t++) st_c(C, r0 + t, lane, cf{sgn * acc[t].re, sgn * acc[t].im});
+        for (int q = 0; q < 4; q++) {
+            const int o = C.off + (r0 + g + (q >> 1) * 8) * C.ld + c0 + 8 * n + 2 * t + (q & 1);
+            const float re = c.rr[n][q] - c.ii[n][q], im = c.ri[n][q];
+            if (SUB) {
+                smem[o] -= re;
+                smem[C.im + o] -= im;
+            } else {
+                smem[o] = sgn * re;
+                smem[C.im + o] = sgn * im;
+            }
+        }
 }
 
 // Step 1: LU of the 32 x 32 diagonal sub-block by warps 0-3, as a wavefront:
@@ -409,24 +464,24 @@ struct WinArgs {
     float *xu, *xl, *pu, *pv;  // dense inverse of U and L; operand packs of W and V (or null)
 };
 
-// One round of W(q): its output blocks, 32 / TM tasks of TM rows each (one
-// task per warp of the group), stored after the group's barrier (a result
-// may replace one of its own operands), then written out.
-template <int TM, int NT, int BAR>
+// One round of W(q): its output blocks, 8 / NTILE tasks of 16 rows x 8 NTILE
+// columns each (one task per warp of the group), stored after the group's
+// barrier (a result may replace one of its own operands), then written out.
+template <int NTILE, int NT, int BAR>
 __device__ __forceinline__ void win_round(int r, int t, int lane, const WinArgs &w) {
-    constexpr int TPB = P / TM;
+    constexpr int CPB = 4 / NTILE, TPB = 2 * CPB;  // column groups, tasks per block
     const int nout = kWinOuts[r];
-    const int wi = t >> 5, b = wi / TPB, r0 = (wi % TPB) * TM;
+    const int wi = t >> 5, b = wi / TPB, rem = wi % TPB, r0 = (rem / CPB) * 16, c0 = (rem % CPB) * 8 * NTILE;
     const bool on = b < nout;
-    cf acc[TM];
-    zero(acc);
+    CAcc<NTILE> acc;
+    cacc_zero(acc);
     if (on) {
         const int nterm = kWin[r][b].nterm;
 #pragma unroll 1
-        for (int i = 0; i < nterm; i++) mac_rows(blk_id(kWin[r][b].tp[i]), blk_id(kWin[r][b].tq[i]), r0, lane, acc);
+        for (int i = 0; i < nterm; i++) cmma(blk_id(kWin[r][b].tp[i]), blk_id(kWin[r][b].tq[i]), r0, c0, lane, acc);
     }
     group_sync<NT, BAR>();
-    if (on) store_c(blk_id(kWin[r][b].dst), r0, lane, acc, kWin[r][b].neg ? -1.f : 1.f);
+    if (on) cacc_out<NTILE, false>(blk_id(kWin[r][b].dst), r0, c0, lane, acc, kWin[r][b].neg ? -1.f : 1.f);
     group_sync<NT, BAR>();
     // a chain round's outputs are one W block (0) and one V block (1); G blocks are not written out
     if (kWin[r][0].eu != 2)
@@ -435,11 +490,11 @@ __device__ __forceinline__ void win_round(int r, int t, int lane, const WinArgs 
 }
 
 // W(q) on a group of NT threads (t = thread index in the group), barrier BAR.
-// The G round takes 8-row tasks (12 for its three blocks); the chain rounds
-// (two blocks) TMC rows.
-template <int NT, int BAR, int TMC>
+// The G round takes 16 x 16 tasks (12 for its three blocks); the chain
+// rounds (two blocks) 16 x 8 TC columns.
+template <int NT, int BAR, int TC>
 __device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArgs &wa) {
-    static_assert(3 * (P / 8) * 32 <= NT && 2 * (P / TMC) * 32 <= NT, "one task per warp");
+    static_assert(3 * 4 * 32 <= NT && 2 * (8 / TC) * 32 <= NT, "one task per warp");
     const WinArgs w = wa;  // in registers: stores through the pointers cannot alias it
     // write-back: block row q from the diagonal on, then block column q below
     // it, four columns per thread (scalar where the block's last columns stop
@@ -472,9 +527,9 @@ __device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArg
     // panel's base LU well before the window ends), here for the last panel
     if constexpr (NT == kThreads) emit_pair(q, q, blkDU(q), q, q, blkDL(q), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
     const int r0 = kWinFirst[q];
-    win_round<8, NT, BAR>(r0, t, lane, w);
+    win_round<2, NT, BAR>(r0, t, lane, w);
 #pragma unroll 1
-    for (int r = r0 + 1; r <= r0 + q; r++) win_round<TMC, NT, BAR>(r, t, lane, w);
+    for (int r = r0 + 1; r <= r0 + q; r++) win_round<TC, NT, BAR>(r, t, lane, w);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -535,46 +590,42 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
                 emit_pair(p - 1, p - 1, blkDU(p - 1), p - 1, p - 1, blkDL(p - 1), wa.xu, wa.xl, wa.pu, wa.pv, mode,
                           tid, kLuWarps * 32);
         } else if (p > 0) {
-            inverse_window<kThreads - kLuWarps * 32, 2, 8>(p - 1, tid - kLuWarps * 32, lane, wa);
+            inverse_window<kThreads - kLuWarps * 32, 2, 2>(p - 1, tid - kLuWarps * 32, lane, wa);
         }
         __syncthreads();
         base_inv(p, warp, lane);
         __syncthreads();
         const int rest = 3 - p;
         if (rest == 0) break;
-        // L_ip = A_ip DU_p (tasks 0 .. 2 rest - 1), U_pj = DL_p A_pj (the next 2 rest);
-        // tasks read rows of A_pj that other tasks overwrite: write after a barrier
+        // L_ip = A_ip DU_p (tasks 0 .. 2 rest - 1), U_pj = DL_p A_pj (the next 2 rest),
+        // 16-row tasks; tasks read rows of A_pj that other tasks overwrite:
+        // write after a barrier
         {
-            cf acc[TMR];
-            zero(acc);
-            const int t = warp, ntask = 4 * rest, b = t >> 1, r0 = (t & 1) * TMR;
-            if (t < ntask) {
-                const bool lpanel = b < rest;
-                mac_rows(lpanel ? blkA(p + 1 + b, p) : blkDL(p), lpanel ? blkDU(p) : blkA(p, p + 1 + b - rest), r0, lane,
-                         acc);
-            }
+            CAcc<4> acc;
+            cacc_zero(acc);
+            const int t = warp, ntask = 4 * rest, b = t >> 1, r0 = (t & 1) * 16;
+            const bool lpanel = b < rest;
+            if (t < ntask)
+                cmma(lpanel ? blkA(p + 1 + b, p) : blkDL(p), lpanel ? blkDU(p) : blkA(p, p + 1 + b - rest), r0, 0, lane,
+                     acc);
             __syncthreads();
-            if (t < ntask) store_c(b < rest ? blkA(p + 1 + b, p) : blkA(p, p + 1 + b - rest), r0, lane, acc, 1.f);
+            if (t < ntask)
+                cacc_out<4, false>(lpanel ? blkA(p + 1 + b, p) : blkA(p, p + 1 + b - rest), r0, 0, lane, acc, 1.f);
             __syncthreads();
         }
-        // A_ij -= L_ip U_pj, i, j > p: each task owns its output rows
+        // A_ij -= L_ip U_pj, i, j > p, 16 x 16 tasks: each task owns its output
         for (int t = warp; t < 4 * rest * rest; t += kWarps) {
-            const int b = t >> 2, r0 = (t & 3) * TMU;
+            const int b = t >> 2, r0 = ((t >> 1) & 1) * 16, c0 = (t & 1) * 16;
             const int bi = p + 1 + b / rest, bj = p + 1 + b % rest;
-            cf acc[TMU];
-            zero(acc);
-            mac_rows(blkA(bi, p), blkA(p, bj), r0, lane, acc);
-            const Blk C = blkA(bi, bj);
-#pragma unroll
-            for (int q = 0; q < TMU; q++) {
-                smem[C.off + (r0 + q) * LDA + lane] -= acc[q].re;
-                smem[C.off + IM_A + (r0 + q) * LDA + lane] -= acc[q].im;
-            }
+            CAcc<2> acc;
+            cacc_zero(acc);
+            cmma(blkA(bi, p), blkA(p, bj), r0, c0, lane, acc);
+            cacc_out<2, true>(blkA(bi, bj), r0, c0, lane, acc, 1.f);
         }
         __syncthreads();
     }
 
-    inverse_window<kThreads, 0, 4>(3, tid, lane, wa);
+    inverse_window<kThreads, 0, 1>(3, tid, lane, wa);
 
     // ---- the 32 x 32 inverses, when the FP32 block solves want them
     if (inv32) {
