@@ -79,8 +79,8 @@ typedef struct {
     int force_fallback; /* testing aid: treat every frequency as stalled (default 0) */
     int profile;        /* 1: time every stage with CUDA events (zsolve_get_profile); default 0 */
     int resid;          /* ZSOLVE_RESID_* (default F64) */
-    int lanes;          /* 0 (default): a sweep batch of 2 or more frequencies is assembled and
-                           factored as two concurrent lanes (streams and host threads); 1: one lane */
+    int lanes;          /* 0 (default): a sweep batch of 2 or more frequencies runs as two
+                           concurrent lanes (streams and host threads); 1: one lane */
 } zsolve_opts;
 
 /* stages of the path, for zsolve_get_profile */
@@ -144,13 +144,15 @@ int zsolve_refine(zsolve_ctx *ctx, const void *b, void *x, int nrhs, zsolve_info
  * refine.  b (device c128, nrhs x n) is shared by all frequencies; x (device
  * c128, nf x nrhs x n) receives the solutions; info (host, nf entries) may be
  * NULL.  Frequencies are processed opts.batch at a time.  Unless opts.lanes
- * is 1, a batch of two or more frequencies is assembled and factored in two
- * lanes that run concurrently on the context's stream and on a second stream
- * of the context, each driven by its own host thread (the second one created
- * and joined inside the call); the refinement then runs over the whole batch
- * on the context's stream.  The call returns when all of it is done and the
- * context's stream is ordered after it.  Returns the first error; a
- * frequency that needed the fallback is not an error. */
+ * is 1, a batch of two or more frequencies is split into two lanes that run
+ * concurrently on the context's stream and on a second stream of the
+ * context, each driven by its own host thread (the second one created and
+ * joined inside the call).  Each lane assembles, factors and refines its
+ * half; the second lane's refinement starts once the first lane's first
+ * solve has run, so that one lane's triangular solves run beside the other's
+ * residuals.  The call returns when all of it is done and the context's
+ * stream is ordered after it.  Returns the first error; a frequency that
+ * needed the fallback is not an error. */
 int zsolve_sweep(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G,
                  const double *omega, const double *zs, int nf, const void *b, void *x,
                  int nrhs, zsolve_info *info);

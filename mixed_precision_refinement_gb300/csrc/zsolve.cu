@@ -28,6 +28,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <condition_variable>
 #include <mutex>
 #include <thread>
 #include <vector>
@@ -85,11 +86,13 @@ struct zsolve_ctx {
         bool own_stream = false;
         cudaEvent_t ev[5] = {nullptr, nullptr, nullptr, nullptr, nullptr};
         cudaEvent_t ev_fork = nullptr, ev_join = nullptr;
+        cudaEvent_t ev_stag = nullptr;  // this lane's first solve of a two-lane refinement is queued
         int *d_active = nullptr, *h_active = nullptr;  // slots still refining
         unsigned *ticket = nullptr;     // triangular-solve task tickets
         unsigned *tile_ctr = nullptr;   // tile counters of the tcgen05 launches
         unsigned *h_status = nullptr;   // pinned copy of the device status word
         int tc_grid = 0;                // CTAs of this lane's tcgen05 launches
+        int trsv_grid = 0;              // CTAs of this lane's triangular solves (0: one per SM)
     };
     Lane lane[2];
     int assembled = 0, factored = 0, fb_ready = 0;
@@ -311,7 +314,7 @@ int lowprec_solve_slots(zsolve_ctx *ctx, Lane &ln, int nrhs, const int *slots, i
         StageSpan sp(ctx, ZSOLVE_STAGE_TRSV, ln.stream);
         ZS_CU(zs_launch_trsv_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->dinv, ctx->dinv_stride,
                                  ctx->v + (int64_t)r0 * ctx->n, ctx->v_stride, R, slots, nslot, ctx->prog, epoch,
-                                 ln.ticket, ctx->d_status, ctx->num_sms, ln.stream));
+                                 ln.ticket, ctx->d_status, ln.trsv_grid ? ln.trsv_grid : ctx->num_sms, ln.stream));
         sp.done(1);
         r0 += R;
     }
@@ -434,8 +437,30 @@ int resid_selftest(zsolve_ctx *ctx) {
 
 // Refinement of slots first..first+count-1 on lane ln; x for slot s is at
 // x + s*x_stride (x is the batch's base).
+// Hand-over between the two lanes of a staggered refinement: the leading
+// lane records ev once its first solve is queued and opens the gate; the
+// other lane's host thread waits at the gate, then makes its stream wait for
+// ev.  The gate is opened on every path, so the waiting thread cannot hang.
+struct Stagger {
+    std::mutex m;
+    std::condition_variable cv;
+    bool ready = false;
+    cudaEvent_t ev = nullptr;
+    void open() {
+        {
+            std::lock_guard<std::mutex> lock(m);
+            ready = true;
+        }
+        cv.notify_all();
+    }
+    void wait() {
+        std::unique_lock<std::mutex> lock(m);
+        cv.wait(lock, [this] { return ready; });
+    }
+};
+
 int refine_batch(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *x, int64_t x_stride, int nrhs, int first,
-                 int count, zsolve_info *info) {
+                 int count, zsolve_info *info, Stagger *lead = nullptr) {
     const int64_t n = ctx->n;
     const zsolve_opts &o = ctx->opts;
     std::vector<int> active, stalled;  // slot indices
@@ -467,6 +492,10 @@ int refine_batch(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *x, int64_
             sp.done(1);
         }
         ZS_TRY(lowprec_solve_slots(ctx, ln, nrhs, ln.d_active, na));
+        if (lead) {
+            ZS_CU(cudaEventRecord(lead->ev, ln.stream));
+            lead->open();
+        }
         StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE, ln.stream);
         ZS_CU(zs_launch_update(x, x_stride, ctx->v, ctx->v_stride, n, nrhs, 1, ctx->partials, ctx->nchunks,
                                ln.d_active, na, ln.stream));
@@ -571,13 +600,15 @@ int factor_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi, c
     return ZSOLVE_OK;
 }
 
-// Refinement of the batch's slots 0..count-1 on ln's stream, after every
-// lane in fl[0..nl) has factored its range [lo[i], lo[i] + cnt[i]); then
-// the per-frequency timings.  xb and ib are the batch's base (slot 0).
-int refine_lanes(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *xb, int nrhs, int count, zsolve_info *ib,
-                 Lane *const *fl, const int *lo, const int *cnt, int nl) {
+// Refinement of the batch's slots first..first+count-1 on ln's stream, after
+// every lane in fl[0..nl) has factored its range [lo[i], lo[i] + cnt[i]) of
+// them; then the per-frequency timings.  xb and ib are the batch's base
+// (slot 0).  lead: see Stagger.
+int refine_lanes(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *xb, int nrhs, int first, int count,
+                 zsolve_info *ib, Lane *const *fl, const int *lo, const int *cnt, int nl, Stagger *lead = nullptr) {
     ZS_CU(cudaEventRecord(ln.ev[3], ln.stream));  // refinement starts
-    const int st = refine_batch(ctx, ln, b, xb, (int64_t)nrhs * ctx->n, nrhs, 0, count, ib);
+    const int st = refine_batch(ctx, ln, b, xb, (int64_t)nrhs * ctx->n, nrhs, first, count, ib ? ib + first : nullptr,
+                                lead);
     if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
     ZS_CU(cudaEventRecord(ln.ev[4], ln.stream));
     ZS_CU(cudaEventSynchronize(ln.ev[4]));
@@ -619,26 +650,31 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
         if (ctx->opts.lanes == 1 || count < 2) {
             l0.tc_grid = ctx->num_sms;
             ZS_TRY(factor_lane(ctx, l0, L, Psi, G, 0, count, false));
+            l0.trsv_grid = 0;
             Lane *fl[1] = {&l0};
             const int lo[1] = {0}, cnt[1] = {count};
-            st = refine_lanes(ctx, l0, b, xb, nrhs, count, ib, fl, lo, cnt, 1);
+            st = refine_lanes(ctx, l0, b, xb, nrhs, 0, count, ib, fl, lo, cnt, 1);
         } else {
-            // Two lanes factor the batch's halves side by side.  Lane 1
-            // starts after lane 0's assembly (and everything queued before it
-            // on the context's stream: inputs, parameters), so that its own
-            // FP64-bound assembly runs under lane 0's factorisation and the
-            // two lanes' outer-block steps stay out of phase.  The refinement
-            // then runs once over the whole batch on the context's stream: its
-            // triangular solves are latency-bound and its residuals bound by
-            // the FP64 pipe over all SMs, so two lanes of them only contend.
+            // Two lanes factor and refine the batch's halves side by side.
+            // Lane 1 starts after lane 0's assembly (and everything queued
+            // before it on the context's stream: inputs, parameters), so that
+            // its own FP64-bound assembly runs under lane 0's factorisation and
+            // the two lanes' outer-block steps stay out of phase.  Its
+            // refinement starts when lane 0's first solve has run, so that the
+            // lanes alternate: one lane's triangular solve (latency-bound)
+            // beside the other's residual (FP64-bound on every SM); the
+            // triangular solves take half of the SMs each.
             const int h = (count + 1) / 2;
             // each lane's persistent tcgen05 grids leave room for the other
             // lane's diagonal blocks (one CTA per frequency)
             l0.tc_grid = std::max(1, ctx->num_sms - (count - h));
             l1.tc_grid = std::max(1, ctx->num_sms - h);
+            l0.trsv_grid = l1.trsv_grid = std::max(1, ctx->num_sms / 2);
             ZS_TRY(assemble_lane(ctx, l0, L, Psi, G, 0, h));
             ZS_CU(cudaEventRecord(l0.ev_fork, l0.stream));
             ZS_CU(cudaStreamWaitEvent(l1.stream, l0.ev_fork, 0));
+            Stagger sg;
+            sg.ev = l0.ev_stag;
             int st1 = ZSOLVE_OK;
             auto lane1 = [&]() {
                 if (cudaSetDevice(ctx->device) != cudaSuccess) {
@@ -646,6 +682,15 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
                     return;
                 }
                 st1 = factor_lane(ctx, l1, L, Psi, G, h, count - h, false);
+                sg.wait();
+                if (st1 != ZSOLVE_OK) return;
+                if (cudaStreamWaitEvent(l1.stream, sg.ev, 0) != cudaSuccess) {
+                    st1 = fail(ctx, ZSOLVE_ECUDA, "second lane: cudaStreamWaitEvent failed");
+                    return;
+                }
+                Lane *fl[1] = {&l1};
+                const int lo[1] = {h}, cnt[1] = {count - h};
+                st1 = refine_lanes(ctx, l1, b, xb, nrhs, h, count - h, ib, fl, lo, cnt, 1);
             };
             std::thread worker;
             bool threaded = true;
@@ -654,16 +699,19 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
             } catch (...) {
                 threaded = false;  // no thread: the lanes run one after the other
             }
-            const int st0 = factor_lane(ctx, l0, L, Psi, G, 0, h, true);
+            int st0 = factor_lane(ctx, l0, L, Psi, G, 0, h, true);
+            if (st0 == ZSOLVE_OK) {
+                Lane *fl[1] = {&l0};
+                const int lo[1] = {0}, cnt[1] = {h};
+                st0 = refine_lanes(ctx, l0, b, xb, nrhs, 0, h, ib, fl, lo, cnt, 1, &sg);
+            }
+            sg.open();  // on every path
             if (threaded) worker.join();
             else lane1();
             ZS_CU(cudaEventRecord(l1.ev_join, l1.stream));
             ZS_CU(cudaStreamWaitEvent(l0.stream, l1.ev_join, 0));
-            ZS_TRY(st0);
-            ZS_TRY(st1);
-            Lane *fl[2] = {&l0, &l1};
-            const int lo[2] = {0, h}, cnt[2] = {h, count - h};
-            st = refine_lanes(ctx, l0, b, xb, nrhs, count, ib, fl, lo, cnt, 2);
+            const bool hard0 = st0 != ZSOLVE_OK && st0 != ZSOLVE_ESINGULAR;
+            st = hard0 ? st0 : (st1 != ZSOLVE_OK ? st1 : st0);
         }
         if (st != ZSOLVE_OK && first_err == ZSOLVE_OK) first_err = st;
         if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
@@ -711,6 +759,7 @@ void free_all(zsolve_ctx *c) {
             if (e) cudaEventDestroy(e);
         if (ln.ev_fork) cudaEventDestroy(ln.ev_fork);
         if (ln.ev_join) cudaEventDestroy(ln.ev_join);
+        if (ln.ev_stag) cudaEventDestroy(ln.ev_stag);
         if (ln.side) cudaStreamDestroy(ln.side);
         if (ln.own_stream && ln.stream) cudaStreamDestroy(ln.stream);
     }
@@ -819,7 +868,8 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
             if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
         if (cudaStreamCreateWithFlags(&ln.side, cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&ln.ev_fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&ln.ev_join, cudaEventDisableTiming) != cudaSuccess)
+            cudaEventCreateWithFlags(&ln.ev_join, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ln.ev_stag, cudaEventDisableTiming) != cudaSuccess)
             return bail(ZSOLVE_ECUDA);
     }
     if (cudaStreamCreateWithFlags(&ctx->lane[1].stream, cudaStreamNonBlocking) != cudaSuccess)
