@@ -159,7 +159,9 @@ int zsolve_sweep(zsolve_ctx *ctx, const double *L, const double *Psi, const doub
 
 /* zsolve_sweep with HOST pointers for L, Psi, G, b and x: copies the inputs
  * to context-owned device buffers, sweeps, and copies the solutions back.
- * Pinned host memory gives overlapped, full-speed copies. */
+ * L, Psi and G are copied in row bands on a copy stream of the context, and
+ * the first assembly follows them band by band, so the copy overlaps it.
+ * Pinned host memory gives asynchronous, full-speed copies. */
 int zsolve_sweep_host(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G,
                       const double *omega, const double *zs, int nf, const void *b, void *x,
                       int nrhs, zsolve_info *info);

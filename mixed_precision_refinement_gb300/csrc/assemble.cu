@@ -105,14 +105,15 @@ __device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, doubl
 
 __global__ void __launch_bounds__(kThreads)
 k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const double *__restrict__ G, int64_t n,
-           const ZsSlotParam *__restrict__ params, int nslot, double2 *__restrict__ z64, int64_t z64_stride,
-           float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, double mz, double one) {
+           int64_t r0, int64_t r1, const ZsSlotParam *__restrict__ params, int nslot, double2 *__restrict__ z64,
+           int64_t z64_stride, float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, double mz,
+           double one) {
     __shared__ ZsSlotParam sp[kMaxSlots];
     const Fp64Ops op{mz, one};
     const int lane = threadIdx.x & 31;
     for (int s = threadIdx.x; s < nslot; s += blockDim.x) sp[s] = params[s];
     __syncthreads();
-    for (int64_t i = blockIdx.x; i < n; i += gridDim.x) {
+    for (int64_t i = r0 + blockIdx.x; i < r1; i += gridDim.x) {
         const int64_t row = i * n, row32 = i * ld;
         // warp-uniform column walk (the tail lanes compute on a clamped index
         // and do not store), so the warp vote below always sees the full warp
@@ -152,19 +153,20 @@ k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const d
 
 }  // namespace
 
-cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n,
+cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0, int64_t r1,
                                const ZsSlotParam *params, int nslot, double2 *z64, int64_t z64_stride,
                                float *z32, int64_t ld, int64_t plane, int64_t z32_stride,
                                cudaStream_t st) {
-    if (nslot > kMaxSlots) return cudaErrorInvalidValue;
+    if (nslot > kMaxSlots || r0 < 0 || r1 > n || r0 > r1) return cudaErrorInvalidValue;
+    if (r0 == r1) return cudaSuccess;
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    int64_t blocks = n;
+    int64_t blocks = r1 - r0;
     int64_t cap = (int64_t)sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    k_assemble<<<(unsigned)blocks, kThreads, 0, st>>>(L, Psi, G, n, params, nslot, z64, z64_stride,
+    k_assemble<<<(unsigned)blocks, kThreads, 0, st>>>(L, Psi, G, n, r0, r1, params, nslot, z64, z64_stride,
                                                       z32, ld, plane, z32_stride, -0.0, 1.0);
     return cudaGetLastError();
 }

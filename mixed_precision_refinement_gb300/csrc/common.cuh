@@ -137,8 +137,9 @@ struct ZsSlotParam {
 // All return cudaGetLastError() of the launch.  Matrices of a batch are
 // strided by the given slot strides (elements).
 
-// Z64 (c128, ld n) and the complex float32 planes (re at z32, im at z32 + plane).
-cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n,
+// Z64 (c128, ld n) and the complex float32 planes (re at z32, im at z32 + plane),
+// rows r0 .. r1-1.
+cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0, int64_t r1,
                                const ZsSlotParam *params, int nslot, double2 *z64, int64_t z64_stride,
                                float *z32, int64_t ld, int64_t plane, int64_t z32_stride,
                                cudaStream_t st);

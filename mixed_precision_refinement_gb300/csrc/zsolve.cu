@@ -74,6 +74,12 @@ struct zsolve_ctx {
     int *fb_info = nullptr, *h_fb_info = nullptr;
     // device copies for the host-pointer sweep (allocated on first use)
     double *hd_L = nullptr, *hd_Psi = nullptr, *hd_G = nullptr;
+    // the host-pointer sweep copies L, Psi, G in row bands on copy_stream;
+    // the first assembly waits for each band separately
+    static constexpr int kBands = 4;
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t band_ev[kBands] = {}, ev_host = nullptr;
+    int nband = 0;
     double2 *hd_b = nullptr, *hd_x = nullptr;
     size_t hd_x_cap = 0;
     int hd_nrhs_cap = 0;
@@ -576,15 +582,24 @@ int check_nrhs(zsolve_ctx *ctx, int nrhs) {
 }
 
 // Assembly of one lane's share of a batch: slots first..first+count-1.
+// While a host-pointer sweep's inputs are still being copied (ctx->nband
+// row bands, band b's rows complete at ctx->band_ev[b]), the assembly runs
+// band by band behind the copies.
 int assemble_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi, const double *G, int first,
                   int count) {
     ZS_CU(cudaEventRecord(ln.ev[0], ln.stream));
     StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE, ln.stream);
-    ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, ctx->d_params + first, count,
-                             ctx->z64 + (int64_t)first * ctx->z64_stride, ctx->z64_stride,
-                             ctx->z32 + (int64_t)first * ctx->z32_stride, ctx->ld, ctx->plane, ctx->z32_stride,
-                             ln.stream));
-    sp.done(1);
+    const int nb = ctx->nband > 0 ? ctx->nband : 1;
+    for (int bnd = 0; bnd < nb; bnd++) {
+        const int64_t r0 = ctx->n * bnd / nb, r1 = ctx->n * (bnd + 1) / nb;
+        if (ctx->nband > 0) ZS_CU(cudaStreamWaitEvent(ln.stream, ctx->band_ev[bnd], 0));
+        ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, r0, r1, ctx->d_params + first, count,
+                                 ctx->z64 + (int64_t)first * ctx->z64_stride, ctx->z64_stride,
+                                 ctx->z32 + (int64_t)first * ctx->z32_stride, ctx->ld, ctx->plane, ctx->z32_stride,
+                                 ln.stream));
+    }
+    sp.done(nb);
+    ctx->nband = 0;  // the first assembly of a sweep waited for every band
     ZS_CU(cudaEventRecord(ln.ev[1], ln.stream));
     return ZSOLVE_OK;
 }
@@ -744,6 +759,10 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->fb_piv);
     cudaFree(c->fb_info);
     cudaFreeHost(c->h_fb_info);
+    if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+    for (auto e : c->band_ev)
+        if (e) cudaEventDestroy(e);
+    if (c->ev_host) cudaEventDestroy(c->ev_host);
     cudaFree(c->hd_L);
     cudaFree(c->hd_Psi);
     cudaFree(c->hd_G);
@@ -917,8 +936,8 @@ int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const d
     ctx->h_params[0] = ZsSlotParam{omega, zs_re, zs_im, 1.0 / omega};
     ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
     StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE, ctx->stream);
-    ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32, ctx->ld,
-                             ctx->plane, ctx->z32_stride, ctx->stream));
+    ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, 0, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32,
+                             ctx->ld, ctx->plane, ctx->z32_stride, ctx->stream));
     sp.done(1);
     ctx->assembled = 1;
     ctx->factored = 0;
@@ -983,11 +1002,33 @@ int zsolve_sweep_host(zsolve_ctx *ctx, const double *L, const double *Psi, const
         }
         ctx->hd_x_cap = xb;
     }
-    ZS_CU(cudaMemcpyAsync(ctx->hd_L, L, mb, cudaMemcpyHostToDevice, ctx->stream));
-    ZS_CU(cudaMemcpyAsync(ctx->hd_Psi, Psi, mb, cudaMemcpyHostToDevice, ctx->stream));
-    ZS_CU(cudaMemcpyAsync(ctx->hd_G, G, mb, cudaMemcpyHostToDevice, ctx->stream));
+    if (!ctx->copy_stream) {
+        if (cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&ctx->ev_host, cudaEventDisableTiming) != cudaSuccess)
+            return fail(ctx, ZSOLVE_ECUDA, "copy stream for host inputs");
+        for (auto &e : ctx->band_ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                return fail(ctx, ZSOLVE_ECUDA, "copy events for host inputs");
+    }
     ZS_CU(cudaMemcpyAsync(ctx->hd_b, b, (size_t)nrhs * n * sizeof(double2), cudaMemcpyHostToDevice, ctx->stream));
+    // L, Psi, G in row bands on the copy stream (after everything queued so
+    // far on the context's stream); the first assembly follows band by band
+    ZS_CU(cudaEventRecord(ctx->ev_host, ctx->stream));
+    ZS_CU(cudaStreamWaitEvent(ctx->copy_stream, ctx->ev_host, 0));
+    for (int bnd = 0; bnd < zsolve_ctx::kBands; bnd++) {
+        const int64_t r0 = n * bnd / zsolve_ctx::kBands, r1 = n * (bnd + 1) / zsolve_ctx::kBands;
+        const size_t off = (size_t)r0 * n, len = (size_t)(r1 - r0) * n * sizeof(double);
+        ZS_CU(cudaMemcpyAsync(ctx->hd_L + off, L + off, len, cudaMemcpyHostToDevice, ctx->copy_stream));
+        ZS_CU(cudaMemcpyAsync(ctx->hd_Psi + off, Psi + off, len, cudaMemcpyHostToDevice, ctx->copy_stream));
+        ZS_CU(cudaMemcpyAsync(ctx->hd_G + off, G + off, len, cudaMemcpyHostToDevice, ctx->copy_stream));
+        ZS_CU(cudaEventRecord(ctx->band_ev[bnd], ctx->copy_stream));
+    }
+    ctx->nband = zsolve_ctx::kBands;
     int st = sweep_impl(ctx, ctx->hd_L, ctx->hd_Psi, ctx->hd_G, omega, zs, nf, ctx->hd_b, ctx->hd_x, nrhs, info);
+    ctx->nband = 0;
+    // the copies are ordered before the context's stream continues, also
+    // when the sweep stopped before its first assembly
+    ZS_CU(cudaStreamWaitEvent(ctx->stream, ctx->band_ev[zsolve_ctx::kBands - 1], 0));
     if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
     if (xb) ZS_CU(cudaMemcpyAsync(x, ctx->hd_x, xb, cudaMemcpyDeviceToHost, ctx->stream));
     ZS_CU(cudaStreamSynchronize(ctx->stream));
