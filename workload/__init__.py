@@ -180,3 +180,40 @@ def random_rhs(n: int, nrhs: int, seed: int) -> np.ndarray:
     """nrhs x n complex N(0,1) right-hand sides."""
     rng = np.random.default_rng(seed)
     return np.ascontiguousarray(rng.normal(size=(nrhs, n)) + 1j * rng.normal(size=(nrhs, n)))
+
+
+# Resonant stand-in for the adaptive-frequency-sampling workloads.  The
+# page's presets are circuit structures whose response changes character
+# across the band (resonances); with the copper recipe above, j*omega*L
+# dominates Z at every frequency and the solution is nearly one vector times
+# 1/omega.  This variant keeps the point-cloud matrices and right-hand sides
+# of a configuration, scales Psi so that the spectrum of L^-1 Psi overlaps
+# omega^2 over the band, and uses a normalised angular frequency with a
+# skin-effect-like loss Zs = zs_scale * (1+j) * sqrt(omega).
+AFS_PSI_SCALE = 0.3
+AFS_W_LO, AFS_W_HI = 1.0, 4.0
+AFS_ZS_SCALE = 0.02
+
+
+def afs_candidates(m: int, w_lo: float = AFS_W_LO, w_hi: float = AFS_W_HI, zs_scale: float = AFS_ZS_SCALE):
+    """m evenly spaced normalised angular frequencies and their Zs."""
+    omega = np.linspace(w_lo, w_hi, m) if m > 1 else np.array([w_lo], dtype=np.float64)[:m]
+    s = zs_scale * np.sqrt(omega)
+    return omega, s + 1j * s
+
+
+def make_resonant(cfg_id: int, m: int, psi_scale: float = AFS_PSI_SCALE) -> Workload:
+    """Configuration cfg_id's L, G, B with Psi * psi_scale over m candidates."""
+    cfg = CONFIGS[cfg_id]
+    points, ports, B = draw_points_and_rhs(cfg_id)
+    L, Psi, G = kernel_matrices(points, cfg.len_l, cfg.len_psi)
+    Psi *= psi_scale
+    omega, zs = afs_candidates(m)
+    return Workload(points, L, Psi, G, omega / (2.0 * math.pi), omega, zs, B, ports)
+
+
+def make_resonant_small(n: int, seed: int, m: int, nrhs: int = 1, psi_scale: float = AFS_PSI_SCALE) -> Workload:
+    """The resonant stand-in at an arbitrary size (recipe of make_small)."""
+    wl = make_small(n, seed, nf=1, nrhs=nrhs)
+    omega, zs = afs_candidates(m)
+    return Workload(wl.points, wl.L, wl.Psi * psi_scale, wl.G, omega / (2.0 * math.pi), omega, zs, wl.B, None)
