@@ -16,6 +16,7 @@ samples of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import re
 import math
@@ -263,6 +264,70 @@ def sweep_variant(zs, torch, wl, args, resid):
         s.close()
 
 
+def afs_variant(zs, torch, args, flush):
+    """Adaptive frequency sampling over 1001 candidates (the page's point limit)
+    on the configuration's matrices: the resonant stand-in (Psi scaled so the
+    band holds resonances, normalised omega in [1, 4]) and the copper physics
+    of the configuration's own band.  Candidate points/s = 1001 / the CUDA-event
+    time of one whole zsolve_afs_sweep (exact solves, basis, evaluations and
+    x = V y at every candidate), L2 flushed before each timed call."""
+    m = 1001
+    out = {"metric": "candidate points/s, reduced-order solution x = V y formed at every candidate",
+           "m": m, "tol": 1e-4}
+    cfg = workload.CONFIGS[args.config]
+    cases = {"resonant": workload.make_resonant(args.config, m)}
+    cu = workload.make(args.config)
+    om = 2 * np.pi * np.linspace(cfg.f_lo, cfg.f_hi, m)
+    cases["copper"] = dataclasses.replace(cu, omega=om, freqs=om / (2 * np.pi), zs=workload.surface_impedance(om))
+    for name, wl in cases.items():
+        n, nrhs = wl.n, wl.B.shape[0]
+        s = zs.Solver(n, nrhs)
+        try:
+            with zs.Afs(s) as a:
+                L = torch.from_numpy(wl.L).cuda()
+                P = torch.from_numpy(wl.Psi).cuda()
+                G = torch.from_numpy(wl.G).cuda()
+                b = torch.from_numpy(wl.B).cuda()
+                x = torch.empty((m, nrhs, n), dtype=torch.complex128, device="cuda")
+                for _ in range(max(1, args.warmup - 1)):
+                    a.sweep(L, P, G, wl.omega, wl.zs, b, x)
+                st = torch.cuda.current_stream()
+                times, info, l0 = [], None, zs.zsolve_afs_launches(a.afs)
+                for _ in range(args.steps):
+                    flush.fill_(1)
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    torch.cuda.synchronize()
+                    e0.record(st)
+                    sampled, resid, info = a.sweep(L, P, G, wl.omega, wl.zs, b, x)
+                    e1.record(st)
+                    torch.cuda.synchronize()
+                    times.append(e0.elapsed_time(e1))
+                launches = (zs.zsolve_afs_launches(a.afs) - l0) / args.steps
+                ms = float(np.median(times))
+                out[name] = {
+                    "workload": (f"N={n}, {nrhs} RHS, " + (
+                        f"Psi x {workload.AFS_PSI_SCALE}, normalised omega {workload.AFS_W_LO}-{workload.AFS_W_HI}, "
+                        f"Zs = {workload.AFS_ZS_SCALE}(1+j)sqrt(omega)" if name == "resonant" else
+                        f"copper Zs, {cfg.f_lo / 1e9:g}-{cfg.f_hi / 1e9:g} GHz")),
+                    "points_per_s": m / (ms / 1e3), "ms": ms, "n_exact": info.n_exact, "q": info.q,
+                    "evals": info.evals, "converged": bool(info.converged), "max_resid": info.max_resid,
+                    "sampled": sampled,
+                    "phase_ms": {"exact": info.ms_exact, "basis": info.ms_basis, "eval": info.ms_eval,
+                                 "expand": info.ms_expand},
+                    "afs_launches": launches}
+                if args.cpu_baseline and name == "resonant":
+                    import oracle
+                    from oracle import afs as oafs
+                    t0 = time.perf_counter()
+                    oafs.afs_sweep(wl.L, wl.Psi, wl.G, wl.omega, wl.zs, wl.B)
+                    t_cpu = time.perf_counter() - t0
+                    out[name]["cpu_oracle"] = {"s": t_cpu, "cores": oracle.num_threads(), "points_per_s": m / t_cpu,
+                                               "kind": "oracle (complex128 pivoted LU exact solves, numpy model)"}
+        finally:
+            s.close()
+    return out
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -476,6 +541,8 @@ def run_ours(args):
         args.resid: {"mode_in_use": resid_mode, "points_per_s": value / ws, "resid_gbs": res_gbs,
                      "resid_hbm_frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None},
         other: sweep_variant(zs, torch, wl, args, other)}
+    if args.afs:
+        line["afs"] = afs_variant(zs, torch, args, flush)
     if args.cpu_baseline and args.gpus <= 1 and ws == 1:
         line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -494,6 +561,7 @@ def main():
     ap.add_argument("--resid", default="F64", choices=["F64", "DF"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-afs", dest="afs", action="store_false")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -239,6 +239,87 @@ int zsolve_reset_profile(zsolve_ctx *ctx);
 int zsolve_lowprec_solve_noalloc(const float *z32, int64_t ld, int64_t plane, int64_t sys_stride, int64_t n,
                                  int nsys, void *v, int64_t v_stride, int nrhs, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Adaptive frequency sampling (AFS): a reduced-order model of the sweep
+ * (malusrfworks.com, "Solving Dense Matrices Fast in the Browser", section
+ * "Fewer frequency points: adaptive frequency sampling", steps 1-4):
+ *   1. solve exactly (zsolve_sweep on the context) at a few candidate
+ *      frequencies and orthonormalise the real and imaginary parts of the
+ *      solutions into a real basis V (n x q);
+ *   2. form Z_r(omega) = j*omega*V^T L V - j*V^T Psi V/omega + Zs*V^T G V;
+ *   3. at every candidate solve Z_r y = V^T b and estimate the relative
+ *      residual ||Z(omega) V y - b|| / ||b|| from q-sized quantities only;
+ *      solve exactly next at the candidate (not yet solved exactly) with the
+ *      largest estimate;
+ *   4. stop when every estimate is below opts.tol.
+ * Readings of what the page leaves open: the first exact solves are at the
+ * two ends of the candidate list; the residual is relative and a candidate's
+ * estimate is the largest over its right-hand sides; the basis is built by
+ * two passes of classical Gram-Schmidt, dropping a vector whose norm after
+ * them is at most opts.drop times its norm before; the loop also ends when
+ * opts.max_solves exact solves have been made or the basis is full
+ * (info.converged = 0).  The output at every candidate, the exactly solved
+ * ones included, is V y.
+ * ------------------------------------------------------------------------- */
+#define ZSOLVE_AFS_MAX_BASIS 96
+
+typedef struct zsolve_afs zsolve_afs;
+
+typedef struct {
+    double tol;     /* stop when every estimated relative residual is below tol (default 1e-4) */
+    int max_solves; /* exact solves at most, >= 1 (default 32) */
+    int max_basis;  /* basis vectors at most, 1 .. ZSOLVE_AFS_MAX_BASIS (default 96) */
+    double drop;    /* orthogonalisation drop threshold, 0 <= drop < 1 (default 1e-8) */
+} zsolve_afs_opts;
+
+typedef struct {
+    int n_exact;      /* exact solves made */
+    int q;            /* basis vectors */
+    int converged;    /* 1 if every final estimate is below tol */
+    int basis_full;   /* 1 if a solution vector was left out because the basis was full */
+    int evals;        /* evaluations of the whole candidate list */
+    int fallbacks;    /* exact solves that needed the double-precision fallback */
+    double max_resid; /* largest final estimate */
+    float ms_exact, ms_basis, ms_eval, ms_expand; /* device time of each phase, summed */
+} zsolve_afs_info;
+
+/* Defaults listed in zsolve_afs_opts. */
+int zsolve_afs_default_opts(zsolve_afs_opts *opts);
+
+/* A handle for AFS sweeps of the system size of ctx (whose solver makes the
+ * exact solves and whose stream carries all of the work).  It owns the basis
+ * and its products (about 4 n max_basis float64 values), the reduced terms,
+ * and per-candidate buffers grown on demand.  ctx must outlive it.
+ * ZSOLVE_EINVAL for bad options, or if the reduced system of max_basis
+ * unknowns and the context's nrhs_max right-hand sides does not fit in
+ * 227 KB of shared memory ((q (q + nrhs) + 3 q) x 16 bytes). */
+int zsolve_afs_create(zsolve_afs **afs, zsolve_ctx *ctx, const zsolve_afs_opts *opts);
+
+/* AFS over the m candidates omega[m] (host, rad/s, > 0) with surface
+ * impedances zs[2m] (host, interleaved re, im), for the right-hand sides b
+ * (device c128, nrhs x n, the same at every candidate).
+ *   x        device c128, m x nrhs x n: the reduced-order solution V y at
+ *            every candidate (NULL: not formed)
+ *   sampled  host, room for min(m, max_solves) ints: candidate indices solved
+ *            exactly, in order (NULL allowed)
+ *   resid    host, m doubles: the final residual estimates (NULL allowed)
+ *   info     host (NULL allowed)
+ * L, Psi, G are device pointers as for zsolve_sweep.  Returns after all
+ * work is done.  ZSOLVE_EINVAL for bad arguments; an exact solve's failure
+ * status (ZSOLVE_ESINGULAR, ...) is returned as is. */
+int zsolve_afs_sweep(zsolve_afs *afs, const double *L, const double *Psi, const double *G, const double *omega,
+                     const double *zs, int m, const void *b, void *x, int nrhs, int *sampled, double *resid,
+                     zsolve_afs_info *info);
+
+/* Kernel launches the handle has made (exact solves not included). */
+int64_t zsolve_afs_launches(const zsolve_afs *afs);
+
+/* Message of the handle's last failure ("" if none). */
+const char *zsolve_afs_last_error(const zsolve_afs *afs);
+
+/* Release the handle's buffers.  NULL is allowed. */
+void zsolve_afs_destroy(zsolve_afs *afs);
+
 /* Static string for a status code. */
 const char *zsolve_strerror(int status);
 

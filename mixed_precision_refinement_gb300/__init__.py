@@ -65,6 +65,24 @@ class zsolve_info(ctypes.Structure):
         return {f: getattr(self, f) for f, _ in self._fields_}
 
 
+class zsolve_afs_opts(ctypes.Structure):
+    _fields_ = [("tol", ctypes.c_double), ("max_solves", ctypes.c_int), ("max_basis", ctypes.c_int),
+                ("drop", ctypes.c_double)]
+
+
+class zsolve_afs_info(ctypes.Structure):
+    _fields_ = [("n_exact", ctypes.c_int), ("q", ctypes.c_int), ("converged", ctypes.c_int),
+                ("basis_full", ctypes.c_int), ("evals", ctypes.c_int), ("fallbacks", ctypes.c_int),
+                ("max_resid", ctypes.c_double), ("ms_exact", ctypes.c_float), ("ms_basis", ctypes.c_float),
+                ("ms_eval", ctypes.c_float), ("ms_expand", ctypes.c_float)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+ZSOLVE_AFS_MAX_BASIS = 96
+
+
 class ZsolveError(RuntimeError):
     def __init__(self, status, message):
         super().__init__(f"zsolve status {status}: {message}")
@@ -97,6 +115,12 @@ def _load():
         "zsolve_strerror": (ctypes.c_char_p, [I]),
         "zsolve_last_error": (ctypes.c_char_p, [P]),
         "zsolve_destroy": (None, [P]),
+        "zsolve_afs_default_opts": (I, [ctypes.POINTER(zsolve_afs_opts)]),
+        "zsolve_afs_create": (I, [ctypes.POINTER(P), P, ctypes.POINTER(zsolve_afs_opts)]),
+        "zsolve_afs_sweep": (I, [P, P, P, P, P, P, I, P, P, I, P, P, ctypes.POINTER(zsolve_afs_info)]),
+        "zsolve_afs_launches": (I64, [P]),
+        "zsolve_afs_last_error": (ctypes.c_char_p, [P]),
+        "zsolve_afs_destroy": (None, [P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -307,6 +331,66 @@ def zsolve_destroy(ctx) -> None:
     _lib.zsolve_destroy(ctx)
 
 
+def zsolve_afs_default_opts() -> zsolve_afs_opts:
+    o = zsolve_afs_opts()
+    _check(None, _lib.zsolve_afs_default_opts(ctypes.byref(o)))
+    return o
+
+
+def _check_afs(afs, status):
+    if status != ZSOLVE_OK:
+        msg = _lib.zsolve_afs_last_error(afs).decode() if afs else ""
+        raise ZsolveError(status, f"{_lib.zsolve_strerror(status).decode()}: {msg}")
+
+
+def zsolve_afs_create(ctx, opts: zsolve_afs_opts | None = None) -> ctypes.c_void_p:
+    afs = ctypes.c_void_p()
+    st = _lib.zsolve_afs_create(ctypes.byref(afs), ctx, ctypes.byref(opts) if opts else None)
+    _check(None, st)
+    return afs
+
+
+def zsolve_afs_sweep(afs, L, Psi, G, omega, zs, b, x=None):
+    """x: complex128 CUDA tensor (m, nrhs, n) or None.  Returns (sampled
+    candidate indices in solve order, final residual estimates (m,), info)."""
+    for t in (L, Psi, G):
+        _require(t, "f64", True)
+    _require(b, "c128", True)
+    if x is not None:
+        _require(x, "c128", True)
+    om, zz = _sweep_args(omega, zs)
+    m = om.shape[0]
+    nrhs = b.shape[0] if b.dim() == 2 else 1
+    sampled = np.full(max(m, 1), -1, dtype=np.int32)
+    resid = np.zeros(max(m, 1), dtype=np.float64)
+    info = zsolve_afs_info()
+    _check_afs(afs, _lib.zsolve_afs_sweep(afs, _ptr(L), _ptr(Psi), _ptr(G), om.ctypes.data, zz.ctypes.data, m,
+                                          _ptr(b), _ptr(x), nrhs, sampled.ctypes.data, resid.ctypes.data,
+                                          ctypes.byref(info)))
+    return [int(k) for k in sampled[:info.n_exact]], resid[:m].copy(), info
+
+
+def zsolve_afs_launches(afs) -> int:
+    return int(_lib.zsolve_afs_launches(afs))
+
+
+def zsolve_afs_last_error(afs) -> str:
+    return _lib.zsolve_afs_last_error(afs).decode()
+
+
+def zsolve_afs_destroy(afs) -> None:
+    _lib.zsolve_afs_destroy(afs)
+
+
+def make_afs_opts(**kw) -> zsolve_afs_opts:
+    o = zsolve_afs_default_opts()
+    for k, v in kw.items():
+        if not hasattr(o, k):
+            raise KeyError(k)
+        setattr(o, k, v)
+    return o
+
+
 def raw_lib():
     """The ctypes handle of libzsolve.so (for calls with explicit status checks)."""
     return _lib
@@ -333,6 +417,34 @@ class Solver:
         if self.ctx:
             zsolve_destroy(self.ctx)
             self.ctx = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Afs:
+    """Owns one adaptive-frequency-sampling handle on a Solver's context."""
+
+    def __init__(self, solver: Solver, **opts):
+        self.solver = solver
+        self.afs = zsolve_afs_create(solver.ctx, make_afs_opts(**opts))
+
+    def sweep(self, L, Psi, G, omega, zs, b, x=None):
+        return zsolve_afs_sweep(self.afs, L, Psi, G, omega, zs, b, x)
+
+    def close(self):
+        if self.afs:
+            zsolve_afs_destroy(self.afs)
+            self.afs = None
 
     def __enter__(self):
         return self

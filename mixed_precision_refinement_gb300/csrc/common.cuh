@@ -133,6 +133,12 @@ struct ZsSlotParam {
     double omega, zs_re, zs_im, pad;
 };
 
+// Accessors of the solver context for the other translation units (afs.cu).
+struct zsolve_ctx;
+cudaStream_t zs_ctx_stream(const zsolve_ctx *ctx);
+int64_t zs_ctx_n(const zsolve_ctx *ctx);
+int zs_ctx_nrhs_max(const zsolve_ctx *ctx);
+
 // ---------------------------------------------------------------- launchers
 // All return cudaGetLastError() of the launch.  Matrices of a batch are
 // strided by the given slot strides (elements).

@@ -793,6 +793,10 @@ void free_all(zsolve_ctx *c) {
 
 }  // namespace
 
+cudaStream_t zs_ctx_stream(const zsolve_ctx *ctx) { return ctx->stream; }
+int64_t zs_ctx_n(const zsolve_ctx *ctx) { return ctx->n; }
+int zs_ctx_nrhs_max(const zsolve_ctx *ctx) { return ctx->nrhs_max; }
+
 extern "C" {
 
 int zsolve_default_opts(zsolve_opts *opts) {
