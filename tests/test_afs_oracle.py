@@ -77,8 +77,8 @@ def test_residual_estimate_equals_full_residual(res_case):
             if direct[r] > 1e-5:
                 assert est == pytest.approx(direct[r], rel=1e-6)
                 checked += 1
-            else:  # cancellation floor of the Gram form: |est - direct| <~ 1e-8
-                assert abs(est - direct[r]) < 1e-7
+            else:  # floor of the Gram form: ~sqrt(3q * eps) of the relative residual
+                assert abs(est - direct[r]) < 1e-6
     assert checked > 10
 
 

@@ -14,8 +14,12 @@ What must agree:
   1e-12 perturbation of the exact solves moves the model by <= 8e-11 (an
   amplification under 100 through the orthogonalisation and the q x q
   solves), so ~1e-9 is expected and 1e-8 leaves a factor of ten;
-- the residual estimates: within 1e-7 + 1e-5 relative (the Gram form's
-  cancellation floor is ~1e-8 of ||b||).
+- the residual estimates: within 1e-6 + 1e-5 relative.  The Gram form
+  c^H (W^T W) c - 2 Re(c^H W^T b) + ||b||^2 loses about 3q * eps * ||b||^2 of
+  the SQUARED residual to cancellation, so near convergence the relative
+  residual itself is resolved only to sqrt(3q * eps) ~ 1e-7 (q <= 96); both
+  sides then return noise of that size (or 0 where the noise is negative),
+  two orders below the stopping tolerance 1e-4.
 """
 import numpy as np
 import pytest
@@ -77,7 +81,7 @@ def compare(ref, sampled, resid, info, X, cand=None):
     assert worst <= AFS_PARITY, worst
     r_ref = np.where(np.isfinite(ref.resid), ref.resid, 1e300)
     r_got = np.where(np.isfinite(resid), resid, 1e300)
-    assert np.all(np.abs(r_got - r_ref) <= 1e-7 + 1e-5 * np.abs(r_ref))
+    assert np.all(np.abs(r_got - r_ref) <= 1e-6 + 1e-5 * np.abs(r_ref))
     return worst
 
 
