@@ -267,21 +267,23 @@ def sweep_variant(zs, torch, wl, args, resid):
 def afs_variant(zs, torch, args, flush):
     """Adaptive frequency sampling over 1001 candidates (the page's point limit)
     on the configuration's matrices: the resonant stand-in (Psi scaled so the
-    band holds resonances, normalised omega in [1, 4]) and the copper physics
-    of the configuration's own band.  Candidate points/s = 1001 / the CUDA-event
+    band holds resonances, normalised omega in [1, 4]; Psi x 0.3 takes a few
+    exact solves, Psi x 0.1 about thirty with a basis of ~64, the page's
+    "q around 20-60") and the copper physics of the configuration's own band.  Candidate points/s = 1001 / the CUDA-event
     time of one whole zsolve_afs_sweep (exact solves, basis, evaluations and
     x = V y at every candidate), L2 flushed before each timed call."""
     m = 1001
     out = {"metric": "candidate points/s, reduced-order solution x = V y formed at every candidate",
            "m": m, "tol": 1e-4}
     cfg = workload.CONFIGS[args.config]
-    cases = {"resonant": workload.make_resonant(args.config, m)}
+    cases = {"resonant": workload.make_resonant(args.config, m),
+             "resonant_psi0.1": workload.make_resonant(args.config, m, psi_scale=0.1)}
     cu = workload.make(args.config)
     om = 2 * np.pi * np.linspace(cfg.f_lo, cfg.f_hi, m)
     cases["copper"] = dataclasses.replace(cu, omega=om, freqs=om / (2 * np.pi), zs=workload.surface_impedance(om))
     for name, wl in cases.items():
         n, nrhs = wl.n, wl.B.shape[0]
-        s = zs.Solver(n, nrhs)
+        s = zs.Solver(n, nrhs, batch=2)  # the exact solves take at most two frequencies at once
         try:
             with zs.Afs(s) as a:
                 L = torch.from_numpy(wl.L).cuda()
@@ -306,9 +308,9 @@ def afs_variant(zs, torch, args, flush):
                 ms = float(np.median(times))
                 out[name] = {
                     "workload": (f"N={n}, {nrhs} RHS, " + (
-                        f"Psi x {workload.AFS_PSI_SCALE}, normalised omega {workload.AFS_W_LO}-{workload.AFS_W_HI}, "
-                        f"Zs = {workload.AFS_ZS_SCALE}(1+j)sqrt(omega)" if name == "resonant" else
-                        f"copper Zs, {cfg.f_lo / 1e9:g}-{cfg.f_hi / 1e9:g} GHz")),
+                        f"Psi x {0.1 if name.endswith('0.1') else workload.AFS_PSI_SCALE}, normalised omega "
+                        f"{workload.AFS_W_LO}-{workload.AFS_W_HI}, Zs = {workload.AFS_ZS_SCALE}(1+j)sqrt(omega)"
+                        if name.startswith("resonant") else f"copper Zs, {cfg.f_lo / 1e9:g}-{cfg.f_hi / 1e9:g} GHz")),
                     "points_per_s": m / (ms / 1e3), "ms": ms, "n_exact": info.n_exact, "q": info.q,
                     "evals": info.evals, "converged": bool(info.converged), "max_resid": info.max_resid,
                     "sampled": sampled,
