@@ -316,7 +316,15 @@ def afs_variant(zs, torch, args, flush):
                     "sampled": sampled,
                     "phase_ms": {"exact": info.ms_exact, "basis": info.ms_basis, "eval": info.ms_eval,
                                  "expand": info.ms_expand},
-                    "afs_launches": launches}
+                    "afs_launches": launches,
+                    # k_afs_eval is float64-bound: its algorithmic flops over the
+                    # evaluation phase's time (which also holds one small copy
+                    # back per pass) against the part's nominal float64 rate
+                    "eval_roofline": {
+                        "kernel": "k_afs_eval", "bound": "fp64", "unit": "TFLOP/s",
+                        "achieved": info.eval_gflop / info.ms_eval if info.ms_eval > 0 else None,
+                        "peak": FP64_NOMINAL_TFLOPS, "peak_source": "nominal float64 rate of the part",
+                        "frac": (info.eval_gflop / info.ms_eval / FP64_NOMINAL_TFLOPS) if info.ms_eval > 0 else None}}
                 if args.cpu_baseline and name == "resonant":
                     import oracle
                     from oracle import afs as oafs

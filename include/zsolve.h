@@ -280,6 +280,9 @@ typedef struct {
     int evals;        /* evaluations of the whole candidate list */
     int fallbacks;    /* exact solves that needed the double-precision fallback */
     double max_resid; /* largest final estimate */
+    double eval_gflop; /* algorithmic work of the evaluations: per candidate and pass,
+                          8/3 q^3 (complex LU, real flops) + 44 q^2 per right-hand side
+                          (8 q^2 elimination and substitution, 36 q^2 the quadratic form) */
     float ms_exact, ms_basis, ms_eval, ms_expand; /* device time of each phase, summed */
 } zsolve_afs_info;
 
@@ -289,7 +292,9 @@ int zsolve_afs_default_opts(zsolve_afs_opts *opts);
 /* A handle for AFS sweeps of the system size of ctx (whose solver makes the
  * exact solves and whose stream carries all of the work).  It owns the basis
  * and its products (about 4 n max_basis float64 values), the reduced terms,
- * and per-candidate buffers grown on demand.  ctx must outlive it.
+ * and per-candidate buffers grown on demand.  ctx must outlive it.  The exact
+ * solves take at most two frequencies at a time, so a context created with
+ * opts.batch = 2 holds all the factorisation memory AFS uses.
  * ZSOLVE_EINVAL for bad options, or if the reduced system of max_basis
  * unknowns and the context's nrhs_max right-hand sides does not fit in
  * 227 KB of shared memory ((q (q + nrhs) + 3 q) x 16 bytes). */

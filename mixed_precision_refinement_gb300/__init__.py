@@ -73,7 +73,8 @@ class zsolve_afs_opts(ctypes.Structure):
 class zsolve_afs_info(ctypes.Structure):
     _fields_ = [("n_exact", ctypes.c_int), ("q", ctypes.c_int), ("converged", ctypes.c_int),
                 ("basis_full", ctypes.c_int), ("evals", ctypes.c_int), ("fallbacks", ctypes.c_int),
-                ("max_resid", ctypes.c_double), ("ms_exact", ctypes.c_float), ("ms_basis", ctypes.c_float),
+                ("max_resid", ctypes.c_double), ("eval_gflop", ctypes.c_double),
+                ("ms_exact", ctypes.c_float), ("ms_basis", ctypes.c_float),
                 ("ms_eval", ctypes.c_float), ("ms_expand", ctypes.c_float)]
 
     def as_dict(self):

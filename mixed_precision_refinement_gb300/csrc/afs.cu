@@ -89,11 +89,11 @@ __device__ __forceinline__ double2 zfms(double2 a, double2 b, double2 c) {
 // intermediate quantities in range.
 __device__ __forceinline__ double2 zrecip(double2 a) {
     if (fabs(a.x) >= fabs(a.y)) {
-        const double t = a.y / a.x, d = a.x + a.y * t;
-        return make_double2(1.0 / d, -t / d);
+        const double t = a.y / a.x, r = 1.0 / (a.x + a.y * t);
+        return make_double2(r, -(t * r));
     }
-    const double t = a.x / a.y, d = a.y + a.x * t;
-    return make_double2(t / d, -1.0 / d);
+    const double t = a.x / a.y, r = 1.0 / (a.y + a.x * t);
+    return make_double2(t * r, -r);
 }
 
 // ------------------------------------------------------------------ basis
@@ -173,27 +173,40 @@ k_afs_project(const double *__restrict__ L, const double *__restrict__ Psi, cons
     const int cb = c0 + (int)blockIdx.y * kProjCols;
     const int kc = min(kProjCols, c0 + nc - cb);
     const double *vb = V + (int64_t)cb * n;
-    const int64_t nfull = n & ~(int64_t)31;
+    constexpr int U = 4;  // row chunks of 32 loaded ahead of their products
     for (int64_t i = gw; i < n; i += nw) {
         const double *Li = L + i * n, *Pi = Psi + i * n, *Gi = G + i * n;
         double aL[kProjCols], aP[kProjCols], aG[kProjCols];
 #pragma unroll
         for (int c = 0; c < kProjCols; c++) aL[c] = aP[c] = aG[c] = 0.0;
-        for (int64_t tw = 0; tw < n; tw += 32) {
-            const int64_t t = tw + lane;
-            const bool valid = tw < nfull || t < n;
-            const int64_t tc = valid ? t : n - 1;
-            double l = Li[tc], p = Pi[tc], g = Gi[tc];
-            if (!valid) l = p = g = 0.0;
-            const bool gz = __all_sync(0xffffffffu, zs::is_zero(zs::bits_of(g)));
-            const double *vt = vb + tc;
+        for (int64_t tw = 0; tw < n; tw += 32 * U) {
+            double l[U], p[U], g[U];
+            int64_t tc[U];
+            bool valid[U];
+            bool gnz = false;
+#pragma unroll
+            for (int u = 0; u < U; u++) {
+                const int64_t t = tw + 32 * u + lane;
+                valid[u] = t < n;
+                tc[u] = valid[u] ? t : n - 1;  // in-bounds address for the tail lanes
+                l[u] = Li[tc[u]];
+                p[u] = Pi[tc[u]];
+                g[u] = Gi[tc[u]];
+                if (!valid[u]) l[u] = p[u] = g[u] = 0.0;
+                gnz = gnz || !zs::is_zero(zs::bits_of(g[u]));
+            }
+            const bool gz = __all_sync(0xffffffffu, !gnz);
 #pragma unroll
             for (int c = 0; c < kProjCols; c++) {
                 if (c < kc) {
-                    const double v = valid ? vt[(int64_t)c * n] : 0.0;
-                    aL[c] = fma(l, v, aL[c]);
-                    aP[c] = fma(p, v, aP[c]);
-                    if (!gz) aG[c] = fma(g, v, aG[c]);
+                    const double *vc = vb + (int64_t)c * n;
+#pragma unroll
+                    for (int u = 0; u < U; u++) {
+                        const double v = valid[u] ? vc[tc[u]] : 0.0;
+                        aL[c] = fma(l[u], v, aL[c]);
+                        aP[c] = fma(p[u], v, aP[c]);
+                        if (!gz) aG[c] = fma(g[u], v, aG[c]);
+                    }
                 }
             }
         }
@@ -289,7 +302,7 @@ k_afs_gram(const double *__restrict__ V, const double *__restrict__ W, const dou
 // ------------------------------------------------------------------ evaluation
 
 __host__ __device__ inline size_t eval_smem_bytes(int q, int nrhs) {
-    return ((size_t)q * (q + nrhs) + 3 * (size_t)q) * sizeof(double2);
+    return ((size_t)q * (q + nrhs) + 4 * (size_t)q) * sizeof(double2);
 }
 
 // One CTA per candidate: Z_r = Zs.re*Gr + j*((omega*Lr - Pr/omega) + Zs.im*Gr)
@@ -305,32 +318,36 @@ k_afs_eval(const ZsSlotParam *__restrict__ par, const double *__restrict__ red, 
     __shared__ double rsum[33];
     __shared__ int piv_s, bad_s;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    constexpr int NW = kEvalThreads / 32;
     const int lda = q + nrhs;
-    double2 *A = sm, *cv = sm + (size_t)q * lda;
+    double2 *A = sm, *cv = sm + (size_t)q * lda, *rdiag = cv + 3 * q;  // rdiag[k] = 1 / pivot k
     const int64_t cand = blockIdx.x;
     const ZsSlotParam p = par[cand];
     const double w = p.omega;
     const int64_t q2 = (int64_t)qmax * qmax;
-    for (int i = warp; i < q; i += NW) {
-        for (int j = lane; j < q; j += 32) {
-            const int64_t e = (int64_t)i * qmax + j;
-            const double l = red[e], ps = red[q2 + e], g = red[2 * q2 + e];
-            // each operation rounded once, in the order the formula is written
-            A[i * lda + j] = make_double2(__dmul_rn(p.zs_re, g),
-                                          __dadd_rn(__dsub_rn(__dmul_rn(w, l), __ddiv_rn(ps, w)), __dmul_rn(p.zs_im, g)));
-        }
-        for (int r = lane; r < nrhs; r += 32) A[i * lda + q + r] = br[(int64_t)i * nrhs + r];
+    for (int f = tid; f < q * q; f += kEvalThreads) {
+        const int i = f / q, j = f - i * q;
+        const int64_t e = (int64_t)i * qmax + j;
+        const double l = red[e], ps = red[q2 + e], g = red[2 * q2 + e];
+        // each operation rounded once, in the order the formula is written
+        A[i * lda + j] = make_double2(__dmul_rn(p.zs_re, g),
+                                      __dadd_rn(__dsub_rn(__dmul_rn(w, l), __ddiv_rn(ps, w)), __dmul_rn(p.zs_im, g)));
+    }
+    for (int f = tid; f < q * nrhs; f += kEvalThreads) {
+        const int i = f / nrhs, r = f - i * nrhs;
+        A[i * lda + q + r] = br[(int64_t)i * nrhs + r];
     }
     if (tid == 0) bad_s = 0;
     __syncthreads();
     for (int k = 0; k < q; k++) {
         if (warp == 0) {
-            double best = -1.0;
+            // |re| + |im| is >= 0 (or NaN, whose pattern is above every
+            // number's), so its bit pattern orders like the value: the
+            // comparisons are integer ones, off the FP64 pipe
+            long long best = -1;
             int bi = q;
             for (int i = k + lane; i < q; i += 32) {
                 const double2 a = A[i * lda + k];
-                const double v = fabs(a.x) + fabs(a.y);
+                const long long v = __double_as_longlong(fabs(a.x) + fabs(a.y));
                 if (v > best) {
                     best = v;
                     bi = i;
@@ -338,7 +355,7 @@ k_afs_eval(const ZsSlotParam *__restrict__ par, const double *__restrict__ red, 
             }
 #pragma unroll
             for (int o = 16; o; o >>= 1) {
-                const double ob = __shfl_xor_sync(0xffffffffu, best, o);
+                const long long ob = __shfl_xor_sync(0xffffffffu, best, o);
                 const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
                 if (ob > best || (ob == best && oi < bi)) {
                     best = ob;
@@ -347,7 +364,9 @@ k_afs_eval(const ZsSlotParam *__restrict__ par, const double *__restrict__ red, 
             }
             if (lane == 0) {
                 piv_s = bi;
-                if (!(best > 0.0) || !isfinite(best) || bi >= q) bad_s = 1;
+                // zero pivot column, infinity or NaN: 0 < pattern < that of +inf
+                if (best <= 0 || best >= 0x7FF0000000000000LL || bi >= q) bad_s = 1;
+                else rdiag[k] = zrecip(A[bi * lda + k]);  // once per step, for the multipliers and the solve
             }
         }
         __syncthreads();
@@ -360,19 +379,22 @@ k_afs_eval(const ZsSlotParam *__restrict__ par, const double *__restrict__ red, 
                 A[pr * lda + j] = a;
             }
         __syncthreads();
-        const double2 inv = zrecip(A[k * lda + k]);
+        const double2 inv = rdiag[k];
         for (int i = k + 1 + tid; i < q; i += kEvalThreads) A[i * lda + k] = zmul(A[i * lda + k], inv);
         __syncthreads();
-        for (int i = k + 1 + warp; i < q; i += NW) {
-            const double2 li = A[i * lda + k];
-            for (int j = k + 1 + lane; j < lda; j += 32) A[i * lda + j] = zfms(A[i * lda + j], li, A[k * lda + j]);
+        {
+            const int rows = q - k - 1, cols = lda - k - 1;
+            for (int f = tid; f < rows * cols; f += kEvalThreads) {
+                const int i = k + 1 + f / cols, j = k + 1 + f % cols;
+                A[i * lda + j] = zfms(A[i * lda + j], A[i * lda + k], A[k * lda + j]);
+            }
         }
         __syncthreads();
     }
     const bool bad = bad_s != 0;
     if (!bad) {
         for (int i = q - 1; i >= 0; i--) {
-            if (tid < nrhs) A[i * lda + q + tid] = zmul(A[i * lda + q + tid], zrecip(A[i * lda + i]));
+            if (tid < nrhs) A[i * lda + q + tid] = zmul(A[i * lda + q + tid], rdiag[i]);
             __syncthreads();
             for (int e = tid; e < i * nrhs; e += kEvalThreads) {
                 const int t = e / nrhs, r = e - t * nrhs;
@@ -393,25 +415,26 @@ k_afs_eval(const ZsSlotParam *__restrict__ par, const double *__restrict__ red, 
             cv[2 * q + i] = make_double2(fma(p.zs_re, y.x, -(p.zs_im * y.y)), fma(p.zs_re, y.y, p.zs_im * y.x));  // Zs*y
         }
         __syncthreads();
-        // sum over rows a of W^T W:  c_a^* (M c)_a (real part) - 2 Re(c_a^* wb_a)
+        // sum over rows a of W^T W:  c_a^* (M c)_a (real part) - 2 Re(c_a^* wb_a),
+        // a thread per row; M is symmetric (both halves hold the same dot
+        // product), so row a is read as column a: consecutive threads read
+        // consecutive addresses
         double part = 0.0;
-        for (int a = warp; a < 3 * q; a += NW) {
+        for (int a = tid; a < 3 * q; a += kEvalThreads) {
             const int ka = a / q, ia = a - ka * q;
-            const double *Mrow = M + ((int64_t)ka * qmax + ia) * m3;
+            const double *Mcol = M + (int64_t)ka * qmax + ia;
             double ur = 0.0, ui = 0.0;
-            for (int bcol = lane; bcol < 3 * q; bcol += 32) {
-                const int kb = bcol / q, ib = bcol - kb * q;
-                const double mv = Mrow[(int64_t)kb * qmax + ib];
-                const double2 c = cv[bcol];
-                ur = fma(mv, c.x, ur);
-                ui = fma(mv, c.y, ui);
+            for (int kb = 0; kb < 3; kb++) {
+                const double *mc = Mcol + (int64_t)kb * qmax * m3;
+                const double2 *cb = cv + kb * q;
+                for (int ib = 0; ib < q; ib++, mc += m3) {
+                    const double mv = *mc;
+                    ur = fma(mv, cb[ib].x, ur);
+                    ui = fma(mv, cb[ib].y, ui);
+                }
             }
-            ur = warp_sum(ur, one);
-            ui = warp_sum(ui, one);
-            if (lane == 0) {
-                const double2 ca = cv[a], wv = wb[((int64_t)ka * qmax + ia) * nrhs + r];
-                part = add1(part, fma(ca.x, ur, ca.y * ui) - 2.0 * fma(ca.x, wv.x, ca.y * wv.y), one);
-            }
+            const double2 ca = cv[a], wv = wb[((int64_t)ka * qmax + ia) * nrhs + r];
+            part = add1(part, fma(ca.x, ur, ca.y * ui) - 2.0 * fma(ca.x, wv.x, ca.y * wv.y), one);
         }
         const double s = add1(block_sum(part, rsum, one), bb[r], one);
         const double b2 = bb[r];
@@ -707,6 +730,7 @@ int zsolve_afs_sweep(zsolve_afs *a, const double *L, const double *Psi, const do
         AFS_CU(cudaEventRecord(a->ev[1], s));
         inf.ms_eval += afs_span(a);
         inf.evals++;
+        inf.eval_gflop += (double)m * (8.0 / 3.0 * q * (double)q * q + 44.0 * q * (double)q * nrhs) * 1e-9;
         // step 4: stop, or solve next at the largest estimate not yet solved
         worst = 0.0;
         for (int i = 0; i < m; i++) {
