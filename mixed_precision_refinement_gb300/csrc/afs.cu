@@ -17,8 +17,9 @@
 // Kernels (all float64; the FP64 pipe, not HBM, bounds each of them on this
 // GPU except the projection's matrix reads at small basis growth):
 //   k_afs_orth    two passes of classical Gram-Schmidt for each new real
-//                 vector against the basis, drop test, normalisation (one CTA:
-//                 the vectors are appended in order);
+//                 vector against the basis, drop test, normalisation (one
+//                 cluster of 8 CTAs, rows split between them; the vectors are
+//                 appended in order);
 //   k_afs_project L, Psi, G times the new basis columns, one pass over the
 //                 three matrices per group of 8 columns;
 //   k_afs_gram    the new rows and columns of V^T L V, V^T Psi V, V^T G V and
@@ -34,13 +35,18 @@
 #include <cstring>
 #include <vector>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "zsolve.h"
+
+namespace cg = cooperative_groups;
 
 namespace {
 
 constexpr int kMaxBasis = ZSOLVE_AFS_MAX_BASIS;
-constexpr int kOrthThreads = 1024;
+constexpr int kOrthCluster = 8;   // CTAs of the orthogonalisation cluster (portable size)
+constexpr int kOrthThreads = 512;
 constexpr int kProjThreads = 256;
 constexpr int kProjCols = 8;
 constexpr int kGramThreads = 256;
@@ -105,12 +111,34 @@ __device__ __forceinline__ double2 zrecip(double2 a) {
 // exceeds drop times its norm before, else its column is reused.
 // q_out[0] = columns after the call; q_out[1] = 1 if a vector was left out
 // because V was full.
-__global__ void __launch_bounds__(kOrthThreads)
+//
+// One thread-block cluster of kOrthCluster CTAs; CTA r owns rows
+// [r*slice, (r+1)*slice) of every column.  The sums over rows (the two norms
+// and h) are formed per CTA, exchanged through distributed shared memory and
+// added in rank order by every CTA, so all CTAs hold bit-identical sums and
+// take the same keep/drop decision (the cluster barriers are reached by all).
+// Four buffers, one per kind of sum, rotate: a buffer is rewritten only after
+// the barrier that follows every CTA's reads of it.
+__global__ void __cluster_dims__(kOrthCluster, 1, 1) __launch_bounds__(kOrthThreads)
 k_afs_orth(double *__restrict__ V, int64_t n, int q0, int qmax, const double2 *__restrict__ xs, int nsrc,
            double drop, int *__restrict__ q_out, double one) {
-    __shared__ double h[kMaxBasis];
+    cg::cluster_group cl = cg::this_cluster();
+    __shared__ double part[4][kMaxBasis];  // this CTA's sums: norm before, h pass 1, h pass 2, norm after
+    __shared__ double h[kMaxBasis];        // the cluster's sums
     __shared__ double red[33];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t slice = (n + kOrthCluster - 1) / kOrthCluster;
+    const int64_t r0 = min(n, (int64_t)cl.block_rank() * slice), r1 = min(n, r0 + slice);
+    // h[0..count) = sum over the cluster's CTAs of part[buf][0..count), in rank order
+    auto cluster_sum = [&](int buf, int count) {
+        cl.sync();
+        for (int j = tid; j < count; j += kOrthThreads) {
+            double acc = 0.0;
+            for (int rk = 0; rk < kOrthCluster; rk++) acc = add1(acc, cl.map_shared_rank(&part[buf][0], rk)[j], one);
+            h[j] = acc;
+        }
+        __syncthreads();
+    };
     int q = q0, full = 0;
     for (int s = 0; s < 2 * nsrc; s++) {
         if (q >= qmax) {
@@ -120,24 +148,27 @@ k_afs_orth(double *__restrict__ V, int64_t n, int q0, int qmax, const double2 *_
         const double2 *src = xs + (int64_t)(s >> 1) * n;
         const bool imag = (s & 1) != 0;
         double *col = V + (int64_t)q * n;
-        double part = 0.0;
-        for (int64_t t = tid; t < n; t += kOrthThreads) {
+        double acc = 0.0;
+        for (int64_t t = r0 + tid; t < r1; t += kOrthThreads) {
             const double2 z = src[t];
             const double v = imag ? z.y : z.x;
             col[t] = v;
-            part = fma(v, v, part);
+            acc = fma(v, v, acc);
         }
-        const double n0 = sqrt(block_sum(part, red, one));
+        acc = block_sum(acc, red, one);
+        if (tid == 0) part[0][0] = acc;
+        cluster_sum(0, 1);
+        const double n0 = sqrt(h[0]);
         for (int pass = 0; pass < 2; pass++) {
             for (int j = warp; j < q; j += kOrthThreads / 32) {
                 const double *vj = V + (int64_t)j * n;
                 double a = 0.0;
-                for (int64_t t = lane; t < n; t += 32) a = fma(vj[t], col[t], a);
+                for (int64_t t = r0 + lane; t < r1; t += 32) a = fma(vj[t], col[t], a);
                 a = warp_sum(a, one);
-                if (lane == 0) h[j] = a;
+                if (lane == 0) part[1 + pass][j] = a;
             }
-            __syncthreads();
-            for (int64_t t = tid; t < n; t += kOrthThreads) {
+            cluster_sum(1 + pass, q);
+            for (int64_t t = r0 + tid; t < r1; t += kOrthThreads) {
                 double c = col[t];
                 const double *vt = V + t;
                 for (int j = 0; j < q; j++, vt += n) c = fma(-h[j], *vt, c);
@@ -145,16 +176,20 @@ k_afs_orth(double *__restrict__ V, int64_t n, int q0, int qmax, const double2 *_
             }
             __syncthreads();
         }
-        part = 0.0;
-        for (int64_t t = tid; t < n; t += kOrthThreads) part = fma(col[t], col[t], part);
-        const double n1 = sqrt(block_sum(part, red, one));
+        acc = 0.0;
+        for (int64_t t = r0 + tid; t < r1; t += kOrthThreads) acc = fma(col[t], col[t], acc);
+        acc = block_sum(acc, red, one);
+        if (tid == 0) part[3][0] = acc;
+        cluster_sum(3, 1);
+        const double n1 = sqrt(h[0]);
         if (n0 > 0.0 && isfinite(n0) && n1 > drop * n0) {
-            for (int64_t t = tid; t < n; t += kOrthThreads) col[t] = col[t] / n1;
+            for (int64_t t = r0 + tid; t < r1; t += kOrthThreads) col[t] = col[t] / n1;
             q++;
         }
         __syncthreads();
     }
-    if (tid == 0) {
+    cl.sync();  // no CTA leaves while another may still read its buffers
+    if (tid == 0 && cl.block_rank() == 0) {
         q_out[0] = q;
         q_out[1] = full;
     }
@@ -689,7 +724,7 @@ int zsolve_afs_sweep(zsolve_afs *a, const double *L, const double *Psi, const do
         inf.n_exact += k;
         // the real and imaginary parts into the basis, then the reduced terms
         AFS_CU(cudaEventRecord(a->ev[0], s));
-        k_afs_orth<<<1, kOrthThreads, 0, s>>>(a->V, n, q, qmax, a->xs, k * nrhs, a->o.drop, a->d_q, one);
+        k_afs_orth<<<kOrthCluster, kOrthThreads, 0, s>>>(a->V, n, q, qmax, a->xs, k * nrhs, a->o.drop, a->d_q, one);
         AFS_CU(cudaGetLastError());
         AFS_CU(cudaMemcpyAsync(a->h_q, a->d_q, 2 * sizeof(int), cudaMemcpyDeviceToHost, s));
         AFS_CU(cudaStreamSynchronize(s));
