@@ -294,10 +294,12 @@ int zsolve_afs_default_opts(zsolve_afs_opts *opts);
  * and its products (about 4 n max_basis float64 values), the reduced terms,
  * and per-candidate buffers grown on demand.  ctx must outlive it.  The exact
  * solves take at most two frequencies at a time, so a context created with
- * opts.batch = 2 holds all the factorisation memory AFS uses.
+ * opts.batch = 2 holds all the factorisation memory AFS uses.  Like a
+ * context, a handle is not thread-safe; its sweeps use the context's solver,
+ * so two handles on one context must not run at the same time.
  * ZSOLVE_EINVAL for bad options, or if the reduced system of max_basis
  * unknowns and the context's nrhs_max right-hand sides does not fit in
- * 227 KB of shared memory ((q (q + nrhs) + 3 q) x 16 bytes). */
+ * 227 KB of shared memory ((q (q + nrhs) + 4 q) x 16 bytes). */
 int zsolve_afs_create(zsolve_afs **afs, zsolve_ctx *ctx, const zsolve_afs_opts *opts);
 
 /* AFS over the m candidates omega[m] (host, rad/s, > 0) with surface

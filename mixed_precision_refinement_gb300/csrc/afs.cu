@@ -657,9 +657,6 @@ int zsolve_afs_create(zsolve_afs **out, zsolve_ctx *ctx, const zsolve_afs_opts *
     if (cudaMallocHost(&a->h_q, 2 * sizeof(int)) != cudaSuccess) return bail(ZSOLVE_ENOMEM);
     for (auto &e : a->ev)
         if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
-    if (cudaFuncSetAttribute(k_afs_eval, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)eval_smem_bytes(a->qmax, a->nrhs_max)) != cudaSuccess)
-        return bail(ZSOLVE_ECUDA);
     *out = a;
     return ZSOLVE_OK;
 }
@@ -699,6 +696,9 @@ int zsolve_afs_sweep(zsolve_afs *a, const double *L, const double *Psi, const do
     bool full = false, converged = false;
     double worst = INFINITY;
     const size_t smem_cap = eval_smem_bytes(qmax, a->nrhs_max);
+    // the limit is a property of the kernel, shared by every handle: set it
+    // for this handle's largest reduced system on each call
+    AFS_CU(cudaFuncSetAttribute(k_afs_eval, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_cap));
     bool first = true;
     while (true) {
         // step 1: exact solves at the pending candidates

@@ -238,3 +238,24 @@ def test_afs_full_size_1001_candidates(zs, torch, kind):
     cand = sorted(set(rng.choice(1001, 24, replace=False).tolist()) | set(ref.sampled))
     compare(ref, got, wl, omega, zsv, wl.B, cand=cand)
     assert got[2].converged == 1
+
+
+def test_afs_two_handles_on_one_context(zs, torch):
+    # a handle with a small basis created after one with a large basis must
+    # not shrink the shared memory the large one's evaluations need
+    wl = workload.make_resonant_small(300, 7, 41, nrhs=2, psi_scale=0.1)  # q = 56
+    ref = oafs.afs_sweep(wl.L, wl.Psi, wl.G, wl.omega, wl.zs, wl.B)
+    s = zs.Solver(wl.n, 2, batch=2)
+    try:
+        with zs.Afs(s) as big, zs.Afs(s, max_basis=8) as small:
+            L, P, G = dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G)
+            b = dev(torch, wl.B)
+            _, _, info_small = small.sweep(L, P, G, wl.omega, wl.zs, b)
+            assert info_small.q <= 8
+            x = torch.empty((len(wl.omega), 2, wl.n), dtype=torch.complex128, device="cuda")
+            sampled, resid, info = big.sweep(L, P, G, wl.omega, wl.zs, b, x)
+            torch.cuda.synchronize()
+            got = (sampled, resid, info, x.cpu().numpy())
+            compare(ref, got, wl, wl.omega, wl.zs, wl.B)
+    finally:
+        s.close()
