@@ -120,13 +120,15 @@ def trsm_flops(n, nb=128):
     return tot
 
 
-def schur_flops(n, nb=128):
-    """Useful real flops of all trailing updates of one factorisation."""
+def schur_flops(n, nb=128, lower=False):
+    """Useful real flops of all trailing updates of one factorisation (lower:
+    the symmetric mode, whose update needs only the m2 (m2 + 1) / 2 entries on
+    and below the diagonal)."""
     tot = 0
     J = 0
     while J + nb < n:
         m2 = n - J - nb
-        tot += 8 * m2 * m2 * nb
+        tot += 8 * nb * (m2 * (m2 + 1) // 2 if lower else m2 * m2)
         J += nb
     return tot
 
@@ -203,7 +205,7 @@ def profiled_pass(zs, torch, wl, args, L, P, G, b, x, flush):
     and the pass's ms per step."""
     n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
     s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm), batch=args.batch or nf, profile=1,
-                  resid=getattr(zs, "ZSOLVE_RESID_" + args.resid))
+                  resid=getattr(zs, "ZSOLVE_RESID_" + args.resid), symmetric=args.symmetric)
     try:
         for _ in range(args.warmup):
             zs.zsolve_sweep(s.ctx, L, P, G, wl.omega, wl.zs, b, x)
@@ -224,13 +226,14 @@ def profiled_pass(zs, torch, wl, args, L, P, G, b, x, flush):
         s.close()
 
 
-def sweep_variant(zs, torch, wl, args, resid):
-    """The same timed sweep with another residual arithmetic: points/s and the
-    residual stage's HBM rate (16 n^2 + 32 n nrhs bytes per evaluation over
-    its CUDA-event time)."""
+def sweep_variant(zs, torch, wl, args, resid, symmetric=None):
+    """The same timed sweep with another residual arithmetic (or factor mode):
+    points/s and the residual stage's HBM rate (16 n^2 + 32 n nrhs bytes per
+    evaluation over its CUDA-event time)."""
     n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
+    sym = args.symmetric if symmetric is None else symmetric
     s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm), batch=args.batch or nf, profile=1,
-                  resid=getattr(zs, "ZSOLVE_RESID_" + resid))
+                  resid=getattr(zs, "ZSOLVE_RESID_" + resid), symmetric=sym)
     try:
         mode = "DF" if zs.zsolve_get_resid_mode(s.ctx) == zs.ZSOLVE_RESID_DF else "F64"
         L = torch.from_numpy(wl.L).cuda()
@@ -387,7 +390,7 @@ def run_ours(args):
     # the headline pass runs without per-launch events (they add about 2 % to a
     # step); the profiled pass after it times every stage and launch
     solver = zs.Solver(n, nrhs, gemm=gemm, batch=args.batch or nf, profile=0,
-                       resid=getattr(zs, "ZSOLVE_RESID_" + args.resid))
+                       resid=getattr(zs, "ZSOLVE_RESID_" + args.resid), symmetric=args.symmetric)
     ctx = solver.ctx
     resid_mode = "DF" if zs.zsolve_get_resid_mode(ctx) == zs.ZSOLVE_RESID_DF else "F64"
     L = torch.from_numpy(wl.L).cuda()
@@ -454,7 +457,7 @@ def run_ours(args):
     n_res_calls = sum(iters)  # residual evaluations per step (one per correction)
     st = {k: v for k, v in prof.items()}
     steps = args.steps
-    schur_f = schur_flops(n) * nf
+    schur_f = schur_flops(n, lower=bool(args.symmetric)) * nf
     # factorisation time per step: the lanes' factorisation spans summed (each
     # frequency's info.ms_factor is its lane's span / the lane's frequencies),
     # so the overlap of the two lanes is not credited
@@ -529,7 +532,7 @@ def run_ours(args):
         "dtype": "f32 factor + " + ("f64" if resid_mode == "F64" else "double-float f32x2") + " residual",
         "data": "synthetic",
         "config": {"workload": workload_name(args.config), "n": n, "nf": nf, "nrhs": nrhs, "gemm": args.gemm,
-                   "resid": resid_mode,
+                   "resid": resid_mode, "factor": "symmetric (lower tiles)" if args.symmetric else "full LU update",
                    "batch": args.batch or nf, "l2": "flushed between steps (512 MB write)",
                    "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
         "lu_tflops": lu_tflops, "resid_gbs": res_gbs,
@@ -551,6 +554,12 @@ def run_ours(args):
         args.resid: {"mode_in_use": resid_mode, "points_per_s": value / ws, "resid_gbs": res_gbs,
                      "resid_hbm_frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None},
         other: sweep_variant(zs, torch, wl, args, other)}
+    # the other factorisation mode: full trailing update, or the symmetric one
+    # (lower tiles only, U12 from A21; same float64 residual and stopping rule)
+    osym = 1 - args.symmetric
+    line["factor_variants"] = {
+        ("symmetric" if args.symmetric else "full"): {"points_per_s": value / ws},
+        ("symmetric" if osym else "full"): sweep_variant(zs, torch, wl, args, args.resid, symmetric=osym)}
     if args.afs:
         line["afs"] = afs_variant(zs, torch, args, flush)
     if args.cpu_baseline and args.gpus <= 1 and ws == 1:
@@ -572,6 +581,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-afs", dest="afs", action="store_false")
+    ap.add_argument("--symmetric", type=int, default=1, choices=[0, 1],
+                    help="1 (default): trailing update on the lower tiles only (Z is complex symmetric); 0: full")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

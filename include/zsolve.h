@@ -81,6 +81,15 @@ typedef struct {
     int resid;          /* ZSOLVE_RESID_* (default F64) */
     int lanes;          /* 0 (default): a sweep batch of 2 or more frequencies runs as two
                            concurrent lanes (streams and host threads); 1: one lane */
+    int symmetric;      /* 1 (default): use that Z is complex symmetric (same page, section "Measure
+                           first": a factorisation that uses the symmetry needs half the work
+                           of LU).  The trailing update forms only the tiles on and below the
+                           diagonal, and each step's U12 solve takes A12^T from A21, so the
+                           factors are those of the unpivoted LU of the matrix the lower
+                           triangle defines (U = D L^T in exact arithmetic).  The double-
+                           precision residual still uses all of Z, so a Z that is not
+                           symmetric is still solved (refinement or the fallback).  Tensor-
+                           core modes only (ignored with ZSOLVE_GEMM_FFMA); 0: the full update */
 } zsolve_opts;
 
 /* stages of the path, for zsolve_get_profile */

@@ -43,7 +43,8 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))
 class zsolve_opts(ctypes.Structure):
     _fields_ = [("tol", ctypes.c_double), ("max_iter", ctypes.c_int), ("gemm", ctypes.c_int),
                 ("outer_block", ctypes.c_int), ("batch", ctypes.c_int), ("force_fallback", ctypes.c_int),
-                ("profile", ctypes.c_int), ("resid", ctypes.c_int), ("lanes", ctypes.c_int)]
+                ("profile", ctypes.c_int), ("resid", ctypes.c_int), ("lanes", ctypes.c_int),
+                ("symmetric", ctypes.c_int)]
 
 
 STAGES = ("assemble", "diag", "trsm", "schur", "trsv", "residual", "update", "fallback", "pack")

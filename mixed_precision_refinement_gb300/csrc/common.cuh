@@ -179,9 +179,11 @@ cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t 
 // Operand packs of the block triangular solves on the tensor cores, at outer
 // column J: A planes rows i >= J+NB = [Re A21(i,:) | Im A21(i,:)], Br planes
 // rows j >= J+NB = [Re A12(:,j) | Im A12(:,j)] (mode 1: tf32 hi; 2: hi + lo).
+// sym: Z is complex symmetric and only its lower part is current; the A12^T
+// packs are taken from A21 (equal by symmetry).
 cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                                int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots, int nslot,
-                                cudaStream_t st);
+                                int64_t J, float *pack, int64_t pack_stride, int mode, int sym, const int *slots,
+                                int nslot, cudaStream_t st);
 
 // tcgen05 kernels (schur_tc.cu).  Tensor maps are 128-byte CUtensorMap
 // objects in host memory, passed by value to the kernels.
@@ -192,8 +194,10 @@ cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane
                           void *map_out);
 // A22 -= L21 U12 for every listed slot (split: 3xTF32), at most max_grid
 // persistent CTAs that take tiles from *ctr (zero before the launch).
-cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
-                               int nslot, unsigned *ctr, unsigned *status, int max_grid, cudaStream_t st);
+// lower: only the tiles on and below the diagonal (complex-symmetric Z).
+cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, int lower,
+                               const int *slots, int nslot, unsigned *ctr, unsigned *status, int max_grid,
+                               cudaStream_t st);
 // L21 = A21 U11^-1 and U12 = L11^-1 A12 from the packs of zs_launch_pack_trsm
 // and zs_launch_diag_block; writes L21, U12 into z32 and their operand packs
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,

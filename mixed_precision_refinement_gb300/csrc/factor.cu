@@ -383,7 +383,7 @@ constexpr int kPackThreads = 256;
 
 __global__ void __launch_bounds__(kPackThreads)
 k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-            float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
+            float *__restrict__ pack, int64_t pack_stride, int mode, int sym, const int *__restrict__ slots) {
     __shared__ float s[ZS_PACK_K][33];
     const int slot = slots[blockIdx.z];
     const float *re = z32 + (int64_t)slot * z32_stride;
@@ -393,12 +393,16 @@ k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z3
     const int64_t r0 = J + NB + 32 * (int64_t)blockIdx.x;
     const int tid = threadIdx.x;
     if (blockIdx.y == 0) {
+        // sym: the matrix is complex symmetric and only its lower part is
+        // kept up to date, so A12^T(j, k) = A21(j, k): the Br planes hold the
+        // same rows as the A planes
         for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
             const int r = idx >> 8, k = idx & (ZS_PACK_K - 1);
             const int64_t i = r0 + r;
             if (i >= n) break;  // later idx only move to later rows
             const float v = (k < NB ? re : im)[i * ld + J + (k & (NB - 1))];
             pack_put(pk, pk + pp, i * ZS_PACK_K + k, v, mode);
+            if (sym) pack_put(pk + 2 * pp, pk + 3 * pp, i * ZS_PACK_K + k, v, mode);
         }
     } else {
         for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
@@ -462,12 +466,13 @@ cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t 
 }
 
 cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
-                                int64_t J, float *pack, int64_t pack_stride, int mode, const int *slots, int nslot,
-                                cudaStream_t st) {
+                                int64_t J, float *pack, int64_t pack_stride, int mode, int sym, const int *slots,
+                                int nslot, cudaStream_t st) {
     const int64_t m2 = n - J - NB;
     if (m2 <= 0 || nslot <= 0) return cudaSuccess;
     if (mode != 1 && mode != 2) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((m2 + 31) / 32), 2, (unsigned)nslot);
-    k_pack_trsm<<<grid, kPackThreads, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode, slots);
+    const dim3 grid((unsigned)((m2 + 31) / 32), sym ? 1 : 2, (unsigned)nslot);
+    k_pack_trsm<<<grid, kPackThreads, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode, sym,
+                                               slots);
     return cudaGetLastError();
 }

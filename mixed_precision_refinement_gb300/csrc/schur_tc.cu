@@ -67,7 +67,10 @@ constexpr int kTq = 8;  // tile-index queue between the roles (the producer runs
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
 // inverse packs: W = U11^-1 in planes 0-3, V = L11^-1 in planes 4-7 (Br hi, Br lo, Bi hi, Bi lo)
 enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_BI_HI = 2, WP_BI_LO = 3, WP_V = 4 };
-enum { KIND_SCHUR = 0, KIND_TRSM = 1 };
+// KIND_SCHUR_LOWER: the trailing update of a complex-symmetric matrix, whose
+// Schur complement stays symmetric: only the tiles on and below the diagonal
+// (column tile <= row tile) are formed; the next step reads only those.
+enum { KIND_SCHUR = 0, KIND_TRSM = 1, KIND_SCHUR_LOWER = 2 };
 
 constexpr int EPI_BOX = 32 * 32 * 4;  // one 32-row x 32-column fp32 box (4 KB)
 constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;  // 4 epilogue warps x 2 staging buffers
@@ -253,7 +256,7 @@ struct Tile {
 
 template <int KIND>
 __host__ __device__ __forceinline__ int tiles_per_slot(int tiles) {
-    return KIND == KIND_SCHUR ? tiles * tiles : 2 * tiles;
+    return KIND == KIND_SCHUR ? tiles * tiles : KIND == KIND_SCHUR_LOWER ? tiles * (tiles + 1) / 2 : 2 * tiles;
 }
 
 template <int KIND>
@@ -262,7 +265,16 @@ __device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const in
     const int per_slot = tiles_per_slot<KIND>(tiles);
     const int si = t / per_slot, rem = t - si * per_slot;
     x.slot = slots[si];
-    if (KIND == KIND_SCHUR) {
+    if (KIND == KIND_SCHUR_LOWER) {
+        // row-major over the lower triangle: row tile tm holds tm + 1 tiles
+        int tm = (int)((sqrtf(8.f * (float)rem + 1.f) - 1.f) * 0.5f);
+        while ((tm + 1) * (tm + 2) / 2 <= rem) tm++;
+        while (tm * (tm + 1) / 2 > rem) tm--;
+        const int tn = rem - tm * (tm + 1) / 2;
+        x.ra = (int)(base + (int64_t)tm * TM);
+        x.rb = (int)(base + (int64_t)tn * TN);
+        x.u = 0;
+    } else if (KIND == KIND_SCHUR) {
         const int tm = rem / tiles, tn = rem - tm * tiles;
         x.ra = (int)(base + (int64_t)tm * TM);
         x.rb = (int)(base + (int64_t)tn * TN);
@@ -349,9 +361,9 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 // A rows: L21 / A21 (A planes) or A12^T (Br planes); B: the pack's
                 // own Br/Bi rows, or W / V from the inverse packs
                 const int pa = (KIND == KIND_TRSM && x.u) ? PL_BR_HI : PL_A_HI;
-                const CUtensorMap *bm = KIND == KIND_SCHUR ? &tmap : &wmap;
-                const int pbr = KIND == KIND_SCHUR ? PL_BR_HI : (x.u ? WP_V : 0) + WP_BR_HI;
-                const int pbi = KIND == KIND_SCHUR ? PL_BI_HI : (x.u ? WP_V : 0) + WP_BI_HI;
+                const CUtensorMap *bm = KIND != KIND_TRSM ? &tmap : &wmap;
+                const int pbr = KIND != KIND_TRSM ? PL_BR_HI : (x.u ? WP_V : 0) + WP_BR_HI;
+                const int pbi = KIND != KIND_TRSM ? PL_BI_HI : (x.u ? WP_V : 0) + WP_BI_HI;
                 bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
@@ -483,7 +495,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
                 }
                 const int part = c >> 2, c32 = (c & 3) * 32;  // part 0 = real, 1 = imaginary
-                if (KIND == KIND_SCHUR) {
+                if (KIND != KIND_TRSM) {
                     const uint32_t sb = next_box();
                     stage_row(sb, lane, v, -1.f);
                     publish();
@@ -624,11 +636,16 @@ cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane
     return encode_f32_4d(map_out, z32, dims, strides, 32, 32);
 }
 
-cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, const int *slots,
-                               int nslot, unsigned *ctr, unsigned *status, int max_grid, cudaStream_t st) {
+cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, int lower,
+                               const int *slots, int nslot, unsigned *ctr, unsigned *status, int max_grid,
+                               cudaStream_t st) {
     if (max_grid < 1 || !ctr) return cudaErrorInvalidValue;
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
     const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
+    if (lower) {
+        if (split) return launch_kind<1, KIND_SCHUR_LOWER>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
+        return launch_kind<0, KIND_SCHUR_LOWER>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
+    }
     if (split) return launch_kind<1, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
     return launch_kind<0, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
 }

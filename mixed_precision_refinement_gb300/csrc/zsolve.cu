@@ -274,7 +274,7 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
             ZS_CU(cudaStreamWaitEvent(ln.side, ln.ev_fork, 0));
             StageSpan sp(ctx, ZSOLVE_STAGE_PACK, ln.side);
             ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                                      ctx->pack_stride, mode, slots, nslot, ln.side));
+                                      ctx->pack_stride, mode, ctx->opts.symmetric, slots, nslot, ln.side));
             sp.done(1);
             ZS_CU(cudaEventRecord(ln.ev_join, ln.side));
         }
@@ -294,8 +294,8 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
             sp.done(1);
         }
         StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR, ln.stream);
-        ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, split, slots, nslot, ctr++, ctx->d_status,
-                                 ln.tc_grid, ln.stream));
+        ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, split, ctx->opts.symmetric, slots, nslot, ctr++,
+                                 ctx->d_status, ln.tc_grid, ln.stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
@@ -810,6 +810,7 @@ int zsolve_default_opts(zsolve_opts *opts) {
     opts->profile = 0;
     opts->resid = ZSOLVE_RESID_F64;
     opts->lanes = 0;
+    opts->symmetric = 1;
     return ZSOLVE_OK;
 }
 
@@ -823,7 +824,8 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (ctx->opts.outer_block == 0) ctx->opts.outer_block = ZS_NB;
     if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
         ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0 || ctx->opts.resid < 0 ||
-        ctx->opts.resid > ZSOLVE_RESID_DF || ctx->opts.lanes < 0 || ctx->opts.lanes > 2) {
+        ctx->opts.resid > ZSOLVE_RESID_DF || ctx->opts.lanes < 0 || ctx->opts.lanes > 2 || ctx->opts.symmetric < 0 ||
+        ctx->opts.symmetric > 1) {
         delete ctx;
         return ZSOLVE_EINVAL;
     }

@@ -32,6 +32,7 @@ def test_schur_and_trsm_flops_small_cases():
     assert bench.schur_flops(128) == 0 and bench.trsm_flops(128) == 0  # one block: no update
     # two blocks: one update of a 128 x 128 block with K = 128, two 128 x 128 solves
     assert bench.schur_flops(256) == 8 * 128 ** 3
+    assert bench.schur_flops(256, lower=True) == 8 * 128 * (128 * 129 // 2)
     assert bench.trsm_flops(256) == 2 * 8 * 128 ** 3
 
 
