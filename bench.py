@@ -108,15 +108,14 @@ def diag_flops(nb=128):
     return 16.0 / 3.0 * nb ** 3
 
 
-def trsm_flops(n, nb=128, l_only=False):
+def trsm_flops(n, nb=128):
     """Useful real flops of all tensor-core block solves of one factorisation
-    (L21 = A21 U11^-1 and U12 = L11^-1 A12: 2 x m2 x nb x nb complex MACs;
-    l_only: the symmetric mode's L21 alone, U12 being D1 L21^T)."""
+    (L21 = A21 U11^-1 and U12 = L11^-1 A12: 2 x m2 x nb x nb complex MACs)."""
     tot = 0
     J = 0
     while J + nb < n:
         m2 = n - J - nb
-        tot += (1 if l_only else 2) * 8 * m2 * nb * nb
+        tot += 2 * 8 * m2 * nb * nb
         J += nb
     return tot
 
@@ -480,7 +479,7 @@ def run_ours(args):
     # with two lanes the launches run next to the other lane's kernels).
     tc_launches = max(1, st["schur"]["launches"] + (st["trsm"]["launches"] if args.gemm != "FFMA" else 0))
     tc_ms_tot = st["schur"]["ms"] + (st["trsm"]["ms"] if args.gemm != "FFMA" else 0.0)
-    tc_flops_tot = (schur_f + (trsm_flops(n, l_only=bool(args.symmetric)) * nf if args.gemm != "FFMA" else 0)) * steps
+    tc_flops_tot = (schur_f + (trsm_flops(n) * nf if args.gemm != "FFMA" else 0)) * steps
     tc_ms = tc_ms_tot / tc_launches
     tc_ach = (tc_flops_tot / tc_launches) / (tc_ms / 1e3) / 1e12 if tc_ms > 0 else None
     if args.gemm == "FFMA":

@@ -179,16 +179,11 @@ cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t 
 // Operand packs of the block triangular solves on the tensor cores, at outer
 // column J: A planes rows i >= J+NB = [Re A21(i,:) | Im A21(i,:)], Br planes
 // rows j >= J+NB = [Re A12(:,j) | Im A12(:,j)] (mode 1: tf32 hi; 2: hi + lo).
-// sym: Z is complex symmetric and only its lower part is current: only the
-// A planes (A21) are written; U12 is formed from L21 by zs_launch_sym_u12.
+// sym: Z is complex symmetric and only its lower part is current; the A12^T
+// packs are taken from A21 (equal by symmetry).
 cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                 int64_t J, float *pack, int64_t pack_stride, int mode, int sym, const int *slots,
                                 int nslot, cudaStream_t st);
-// U12 = D1 L21^T (D1 = diag(U11)) into the factor's upper row block and the
-// trailing update's Br/Bi packs, after the L21-only block solve.
-cudaError_t zs_launch_sym_u12(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-                              float *pack, int64_t pack_stride, int mode, const int *slots, int nslot,
-                              cudaStream_t st);
 
 // tcgen05 kernels (schur_tc.cu).  Tensor maps are 128-byte CUtensorMap
 // objects in host memory, passed by value to the kernels.
@@ -205,10 +200,9 @@ cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int
                                cudaStream_t st);
 // L21 = A21 U11^-1 and U12 = L11^-1 A12 from the packs of zs_launch_pack_trsm
 // and zs_launch_diag_block; writes L21, U12 into z32 and their operand packs
-// (l_only: L21 alone, for the symmetric mode)
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
-                              int64_t J, int split, int l_only, const int *slots, int nslot, unsigned *ctr,
-                              unsigned *status, int num_sms, cudaStream_t st);
+                              int64_t J, int split, const int *slots, int nslot, unsigned *ctr, unsigned *status,
+                              int num_sms, cudaStream_t st);
 
 // Pack layout (floats), per slot: six planes of n rows x 2*NB:
 //   A_hi, A_lo, Br_hi, Br_lo, Bi_hi, Bi_lo

@@ -13,8 +13,7 @@
 //   k_trsm_u    U12 = L11^-1 A12, one column per warp;
 //   k_schur_simt  A22 -= L21 U12 (FP32 FFMA; schur_tc.cu: tcgen05);
 //   k_pack_trsm A21 and A12^T as tf32 operand packs for the tensor-core
-//               block solves (schur_tc.cu);
-//   k_sym_u12   the symmetric mode's U12 = D1 L21^T (factor and packs).
+//               block solves (schur_tc.cu).
 // k_trsm_l / k_trsm_u also write L21 and U12 as K-major operand packs for
 // the trailing update: A = [Re L21 | Im L21], Br = [Re U12^T | -Im U12^T],
 // Bi = [Im U12^T | Re U12^T], so that Re(L21 U12) = A Br^T and
@@ -384,7 +383,7 @@ constexpr int kPackThreads = 256;
 
 __global__ void __launch_bounds__(kPackThreads)
 k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-            float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
+            float *__restrict__ pack, int64_t pack_stride, int mode, int sym, const int *__restrict__ slots) {
     __shared__ float s[ZS_PACK_K][33];
     const int slot = slots[blockIdx.z];
     const float *re = z32 + (int64_t)slot * z32_stride;
@@ -394,12 +393,16 @@ k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z3
     const int64_t r0 = J + NB + 32 * (int64_t)blockIdx.x;
     const int tid = threadIdx.x;
     if (blockIdx.y == 0) {
+        // sym: the matrix is complex symmetric and only its lower part is
+        // kept up to date, so A12^T(j, k) = A21(j, k): the Br planes hold the
+        // same rows as the A planes
         for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
             const int r = idx >> 8, k = idx & (ZS_PACK_K - 1);
             const int64_t i = r0 + r;
             if (i >= n) break;  // later idx only move to later rows
             const float v = (k < NB ? re : im)[i * ld + J + (k & (NB - 1))];
             pack_put(pk, pk + pp, i * ZS_PACK_K + k, v, mode);
+            if (sym) pack_put(pk + 2 * pp, pk + 3 * pp, i * ZS_PACK_K + k, v, mode);
         }
     } else {
         for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
@@ -413,60 +416,6 @@ k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z3
             const int64_t j = r0 + c;
             if (j >= n) break;
             pack_put(pk + 2 * pp, pk + 3 * pp, j * ZS_PACK_K + k, s[k][c], mode);
-        }
-    }
-}
-
-// U12 of a complex-symmetric step from L21: U12 = D1 L21^T with D1 the
-// diagonal of U11 (U = D L^T for the unpivoted LU of a symmetric matrix).
-// Writes U12 into the factor's upper row block (transposed through shared
-// memory, so both the reads of L21 rows and the writes of U12 rows are
-// coalesced) and U12^T into the trailing update's B packs:
-// Br row j = [Re U12^T(j,:) | -Im U12^T(j,:)], Bi row j = [Im U12^T(j,:) | Re U12^T(j,:)].
-// 32 rows j of L21 per CTA.
-__global__ void __launch_bounds__(kPackThreads)
-k_sym_u12(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-          float *__restrict__ pack, int64_t pack_stride, int mode, const int *__restrict__ slots) {
-    __shared__ float ur[NB][33], ui[NB][33];
-    __shared__ float dr[NB], di[NB];
-    const int slot = slots[blockIdx.y];
-    float *re = z32 + (int64_t)slot * z32_stride;
-    float *im = re + plane;
-    float *pk = pack + (int64_t)slot * pack_stride;
-    const int64_t pp = zs_pack_plane(n);
-    const int64_t r0 = J + NB + 32 * (int64_t)blockIdx.x;
-    const int tid = threadIdx.x;
-    for (int k = tid; k < NB; k += kPackThreads) {
-        const int64_t e = (J + k) * ld + J + k;
-        dr[k] = re[e];
-        di[k] = im[e];
-    }
-    __syncthreads();
-    for (int idx = tid; idx < 32 * NB; idx += kPackThreads) {
-        const int r = idx >> 7, k = idx & (NB - 1);
-        const int64_t j = r0 + r;
-        float vr = 0.f, vi = 0.f;
-        if (j < n) {
-            const float lr = re[j * ld + J + k], li = im[j * ld + J + k];
-            vr = fmaf(lr, dr[k], -li * di[k]);
-            vi = fmaf(lr, di[k], li * dr[k]);
-            const int64_t o = j * ZS_PACK_K;
-            pack_put(pk + 2 * pp, pk + 3 * pp, o + k, vr, mode);
-            pack_put(pk + 2 * pp, pk + 3 * pp, o + NB + k, -vi, mode);
-            pack_put(pk + 4 * pp, pk + 5 * pp, o + k, vi, mode);
-            pack_put(pk + 4 * pp, pk + 5 * pp, o + NB + k, vr, mode);
-        }
-        ur[k][r] = vr;
-        ui[k][r] = vi;
-    }
-    __syncthreads();
-    for (int idx = tid; idx < 32 * NB; idx += kPackThreads) {
-        const int k = idx >> 5, c = idx & 31;
-        const int64_t j = r0 + c;
-        if (j < n) {
-            const int64_t e = (J + k) * ld + j;
-            re[e] = ur[k][c];
-            im[e] = ui[k][c];
         }
     }
 }
@@ -522,19 +471,8 @@ cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int
     const int64_t m2 = n - J - NB;
     if (m2 <= 0 || nslot <= 0) return cudaSuccess;
     if (mode != 1 && mode != 2) return cudaErrorInvalidValue;
-    // symmetric: only the A planes (blockIdx.y == 0); U12 comes from L21 (k_sym_u12)
     const dim3 grid((unsigned)((m2 + 31) / 32), sym ? 1 : 2, (unsigned)nslot);
-    k_pack_trsm<<<grid, kPackThreads, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode, slots);
-    return cudaGetLastError();
-}
-
-cudaError_t zs_launch_sym_u12(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, int64_t J,
-                              float *pack, int64_t pack_stride, int mode, const int *slots, int nslot,
-                              cudaStream_t st) {
-    const int64_t m2 = n - J - NB;
-    if (m2 <= 0 || nslot <= 0) return cudaSuccess;
-    if (mode != 1 && mode != 2) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)((m2 + 31) / 32), (unsigned)nslot);
-    k_sym_u12<<<grid, kPackThreads, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode, slots);
+    k_pack_trsm<<<grid, kPackThreads, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode, sym,
+                                               slots);
     return cudaGetLastError();
 }

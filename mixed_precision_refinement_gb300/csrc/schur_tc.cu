@@ -70,14 +70,7 @@ enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_BI_HI = 2, WP_BI_LO = 3, WP_V = 4 };
 // KIND_SCHUR_LOWER: the trailing update of a complex-symmetric matrix, whose
 // Schur complement stays symmetric: only the tiles on and below the diagonal
 // (column tile <= row tile) are formed; the next step reads only those.
-// KIND_TRSM_L: the block solves of that symmetric case, L21 only (U12 = D1 L21^T
-// is formed from it by k_sym_u12 in factor.cu).
-enum { KIND_SCHUR = 0, KIND_TRSM = 1, KIND_SCHUR_LOWER = 2, KIND_TRSM_L = 3 };
-
-template <int KIND>
-__host__ __device__ constexpr bool is_trsm() {
-    return KIND == KIND_TRSM || KIND == KIND_TRSM_L;
-}
+enum { KIND_SCHUR = 0, KIND_TRSM = 1, KIND_SCHUR_LOWER = 2 };
 
 constexpr int EPI_BOX = 32 * 32 * 4;  // one 32-row x 32-column fp32 box (4 KB)
 constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;  // 4 epilogue warps x 2 staging buffers
@@ -263,10 +256,7 @@ struct Tile {
 
 template <int KIND>
 __host__ __device__ __forceinline__ int tiles_per_slot(int tiles) {
-    return KIND == KIND_SCHUR         ? tiles * tiles
-           : KIND == KIND_SCHUR_LOWER ? tiles * (tiles + 1) / 2
-           : KIND == KIND_TRSM_L      ? tiles
-                                      : 2 * tiles;
+    return KIND == KIND_SCHUR ? tiles * tiles : KIND == KIND_SCHUR_LOWER ? tiles * (tiles + 1) / 2 : 2 * tiles;
 }
 
 template <int KIND>
@@ -289,10 +279,6 @@ __device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const in
         x.ra = (int)(base + (int64_t)tm * TM);
         x.rb = (int)(base + (int64_t)tn * TN);
         x.u = 0;
-    } else if (KIND == KIND_TRSM_L) {
-        x.u = 0;
-        x.ra = (int)(base + (int64_t)rem * TM);
-        x.rb = 0;
     } else {
         x.u = rem & 1;
         x.ra = (int)(base + (int64_t)(rem >> 1) * TM);
@@ -352,7 +338,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
-            if (is_trsm<KIND>()) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&wmap) : "memory");
+            if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&wmap) : "memory");
             // Tiles are taken dynamically: the first is blockIdx.x, the next
             // ones come from the launch's counter, so CTAs that start late
             // (the SMs busy with another stream's kernel) simply take fewer.
@@ -374,10 +360,10 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 const Tile x = tile_of<KIND>(t, tiles, base, slots);
                 // A rows: L21 / A21 (A planes) or A12^T (Br planes); B: the pack's
                 // own Br/Bi rows, or W / V from the inverse packs
-                const int pa = (is_trsm<KIND>() && x.u) ? PL_BR_HI : PL_A_HI;
-                const CUtensorMap *bm = !is_trsm<KIND>() ? &tmap : &wmap;
-                const int pbr = !is_trsm<KIND>() ? PL_BR_HI : (x.u ? WP_V : 0) + WP_BR_HI;
-                const int pbi = !is_trsm<KIND>() ? PL_BI_HI : (x.u ? WP_V : 0) + WP_BI_HI;
+                const int pa = (KIND == KIND_TRSM && x.u) ? PL_BR_HI : PL_A_HI;
+                const CUtensorMap *bm = KIND != KIND_TRSM ? &tmap : &wmap;
+                const int pbr = KIND != KIND_TRSM ? PL_BR_HI : (x.u ? WP_V : 0) + WP_BR_HI;
+                const int pbi = KIND != KIND_TRSM ? PL_BI_HI : (x.u ? WP_V : 0) + WP_BI_HI;
                 bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
@@ -487,7 +473,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         };
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&cmap) : "memory");
-            if (is_trsm<KIND>()) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&pmap) : "memory");
+            if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&pmap) : "memory");
         }
         for (;; it++) {
             const bool okq = mbar_wait(smem_u32(&bar_tq[it % kTq]), (it / kTq) & 1u, &s_abort, status);
@@ -509,7 +495,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
                 }
                 const int part = c >> 2, c32 = (c & 3) * 32;  // part 0 = real, 1 = imaginary
-                if (!is_trsm<KIND>()) {
+                if (KIND != KIND_TRSM) {
                     const uint32_t sb = next_box();
                     stage_row(sb, lane, v, -1.f);
                     publish();
@@ -665,17 +651,13 @@ cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int
 }
 
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
-                              int64_t J, int split, int l_only, const int *slots, int nslot, unsigned *ctr,
-                              unsigned *status, int num_sms, cudaStream_t st) {
+                              int64_t J, int split, const int *slots, int nslot, unsigned *ctr, unsigned *status,
+                              int num_sms, cudaStream_t st) {
     if (!ctr) return cudaErrorInvalidValue;
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
     const CUtensorMap &w = *reinterpret_cast<const CUtensorMap *>(wmap);
     const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
     const CUtensorMap &p = *reinterpret_cast<const CUtensorMap *>(pmap);
-    if (l_only) {
-        if (split) return launch_kind<1, KIND_TRSM_L>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
-        return launch_kind<0, KIND_TRSM_L>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
-    }
     if (split) return launch_kind<1, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
     return launch_kind<0, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
 }

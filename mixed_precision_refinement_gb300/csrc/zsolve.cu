@@ -289,14 +289,8 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
         {
             ZS_CU(cudaStreamWaitEvent(ln.stream, ln.ev_join, 0));
             StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.stream);
-            ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J, split,
-                                    ctx->opts.symmetric, slots, nslot, ctr++, ctx->d_status, ln.tc_grid, ln.stream));
-            sp.done(1);
-        }
-        if (ctx->opts.symmetric) {  // U12 = D1 L21^T, no product (U = D L^T)
-            StageSpan sp(ctx, ZSOLVE_STAGE_PACK, ln.stream);
-            ZS_CU(zs_launch_sym_u12(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                                    ctx->pack_stride, mode, slots, nslot, ln.stream));
+            ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J, split, slots,
+                                    nslot, ctr++, ctx->d_status, ln.tc_grid, ln.stream));
             sp.done(1);
         }
         StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR, ln.stream);

@@ -34,7 +34,6 @@ def test_schur_and_trsm_flops_small_cases():
     assert bench.schur_flops(256) == 8 * 128 ** 3
     assert bench.schur_flops(256, lower=True) == 8 * 128 * (128 * 129 // 2)
     assert bench.trsm_flops(256) == 2 * 8 * 128 ** 3
-    assert bench.trsm_flops(256, l_only=True) == 8 * 128 ** 3
 
 
 def test_launch_list_shares_parse_the_committed_profile():
