@@ -82,8 +82,8 @@ typedef struct {
     int lanes;          /* 0 (default): a sweep batch of 2 or more frequencies runs as two
                            concurrent lanes (streams and host threads); 1: one lane */
     int symmetric;      /* 1 (default): use that Z is complex symmetric (same page, section "Measure
-                           first": a factorisation that uses the symmetry needs half the work
-                           of LU).  The trailing update forms only the tiles on and below the
+                           first": exploiting the symmetry halves the factorisation's work
+                           against LU).  The trailing update forms only the tiles on and below the
                            diagonal, and each step's U12 solve takes A12^T from A21, so the
                            factors are those of the unpivoted LU of the matrix the lower
                            triangle defines (U = D L^T in exact arithmetic).  The double-
@@ -252,15 +252,16 @@ int zsolve_lowprec_solve_noalloc(const float *z32, int64_t ld, int64_t plane, in
  * Adaptive frequency sampling (AFS): a reduced-order model of the sweep
  * (malusrfworks.com, "Solving Dense Matrices Fast in the Browser", section
  * "Fewer frequency points: adaptive frequency sampling", steps 1-4):
- *   1. solve exactly (zsolve_sweep on the context) at a few candidate
- *      frequencies and orthonormalise the real and imaginary parts of the
- *      solutions into a real basis V (n x q);
- *   2. form Z_r(omega) = j*omega*V^T L V - j*V^T Psi V/omega + Zs*V^T G V;
- *   3. at every candidate solve Z_r y = V^T b and estimate the relative
- *      residual ||Z(omega) V y - b|| / ||b|| from q-sized quantities only;
- *      solve exactly next at the candidate (not yet solved exactly) with the
- *      largest estimate;
- *   4. stop when every estimate is below opts.tol.
+ *   1. full solves (zsolve_sweep on the context) at a few candidates; the
+ *      real and imaginary parts of their solutions, made orthonormal, are
+ *      the columns of a real basis V (n x q);
+ *   2. the q x q system Z_r(omega) = j*omega*V^T L V - j*V^T Psi V/omega
+ *      + Zs*V^T G V;
+ *   3. at every candidate, y from Z_r y = V^T b and an estimate of the
+ *      relative residual ||Z(omega) V y - b|| / ||b|| built from q-sized
+ *      quantities only; the candidate (not yet fully solved) with the worst
+ *      estimate gets the next full solve;
+ *   4. the loop ends once every estimate is below opts.tol.
  * Readings of what the page leaves open: the first exact solves are at the
  * two ends of the candidate list; the residual is relative and a candidate's
  * estimate is the largest over its right-hand sides; the basis is built by

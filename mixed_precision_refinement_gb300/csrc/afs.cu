@@ -2,9 +2,9 @@
 // (malusrfworks.com, "Solving Dense Matrices Fast in the Browser", section
 // "Fewer frequency points: adaptive frequency sampling").
 //
-// Exact solves at a few candidate frequencies (the mixed-precision solver of
-// this library) give complex solutions whose real and imaginary parts are
-// orthonormalised into a real basis V (n x q).  With L V, Psi V, G V the
+// The library's mixed-precision solver runs at a few candidates; the real and
+// imaginary parts of its solutions, made orthonormal, are the columns of a
+// real basis V (n x q).  With L V, Psi V, G V the
 // reduced matrix Z_r(omega) = j*omega*V^T L V - j*V^T Psi V/omega + Zs*V^T G V
 // is q x q; its Galerkin solution y (Z_r y = V^T b) gives x ~ V y at every
 // candidate, and the relative residual ||Z V y - b|| / ||b|| is estimated from

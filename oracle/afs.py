@@ -6,21 +6,21 @@ Follows malusrfworks.com, "Solving Dense Matrices Fast in the Browser",
 section "Fewer frequency points: adaptive frequency sampling", whose four
 steps are taken in the page's order:
 
-1. solve exactly at a few frequencies and orthonormalise the real and
-   imaginary parts of the solutions into a real basis V;
-2. form the small matrix Z_r = j*omega*V^T L V - j*V^T Psi V/omega
-   + Zs*V^T G V (q x q);
-3. estimate the residual ||Z(omega) V y - b|| at every candidate frequency
-   and solve exactly next where it is largest;
-4. stop when the residual falls below 1e-4.
+1. a handful of candidates get full solves; the real and imaginary parts of
+   those solutions, made orthonormal, are the columns of a real basis V;
+2. projecting the three frequency-independent matrices onto V gives a q x q
+   system Z_r = j*omega*V^T L V - j*V^T Psi V/omega + Zs*V^T G V;
+3. every candidate gets the residual ||Z(omega) V y - b|| of its small-system
+   answer, and the worst one is the next full solve;
+4. the loop ends once no candidate's residual reaches 1e-4.
 
 Readings of points the page leaves open (each restated where it is used):
 - "a few frequencies" to start: the two ends of the candidate list (only the
   first if the list has one entry or one exact solve is allowed);
 - the residual is relative, ||Z V y - b||_2 / ||b||_2, per right-hand side,
   and a candidate's residual is the largest over its right-hand sides;
-- y solves the Galerkin system Z_r y = V^T b (the page's "solved at any
-  frequency in an instant" with V real, so V^T is the projection);
+- y solves the Galerkin system Z_r y = V^T b (the page solves the small
+  system at each frequency; with V real, V^T is the projection);
 - the residual estimate uses only small quantities, as the page says: with
   W = [L V | Psi V | G V] (n x 3q) and c = [j*omega*y; -j*y/omega; Zs*y],
   Z V y = W c, so ||Z V y - b||^2 = c^H (W^T W) c - 2 Re(c^H W^T b) + ||b||^2;

@@ -10,7 +10,7 @@ what the page and the mathematics fix, not against the oracle itself
 - Z_r equals V^T Z(omega) V of the assembled Z and is symmetric, since V is
   real (the page: reciprocity is kept);
 - at an exactly solved frequency the model reproduces the exact solution
-  (the page: it matches perfectly there);
+  (the page states the model reproduces the full solution there);
 - once the basis spans R^n the model is exact at every candidate;
 - every greedy pick is the candidate with the largest true residual;
 - after convergence the error obeys ||x - V y|| / ||x|| <= cond(Z) * residual;

@@ -2,8 +2,8 @@
 = 1, the default) and the full trailing update (0).
 
 Z(omega) is complex symmetric (malusrfworks.com, "Solving Dense Matrices Fast
-in the Browser", section "Measure first": a factorisation that uses the
-symmetry needs half the work of LU).  For an unpivoted LU of a complex
+in the Browser", section "Measure first": exploiting the symmetry halves the
+factorisation's work against LU).  For an unpivoted LU of a complex
 symmetric matrix U = D L^T holds in exact arithmetic, with D = diag(U); in
 this mode the trailing update forms only the lower tiles and each U12 solve
 takes A12^T from A21.  Checked here:
