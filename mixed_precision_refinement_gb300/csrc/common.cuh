@@ -5,7 +5,7 @@
 #include <stdint.h>
 
 #define ZS_NB 128           // outer block: columns factored per step of the blocked LU
-#define ZS_PANEL 32         // panel width inside the outer block ("LU in blocks of 32")
+#define ZS_PANEL 32         // panel width inside the outer block (the page factorises in blocks of 32)
 #define ZS_TB 64            // row block of the sequential-diagonal triangular solve
 #define ZS_TB2 128          // row block of the inverse-diagonal triangular solve
 #define ZS_SPIN_LIMIT (1u << 22)  // bounded waits: polls (>= 64 ns apart) before a wait gives up

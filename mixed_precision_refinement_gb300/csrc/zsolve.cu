@@ -8,7 +8,7 @@
 // factorise in low precision (step 1), solve for x (step 2), form the
 // residual in double precision (step 3), solve for a correction with the
 // low-precision factors and add it (step 4), repeating steps 3-4 -- the
-// page's "go back to step 2" is read as returning to the residual, since the
+// page's loop back to step 2 is read as a return to the residual, since the
 // first solve happens once -- until the relative correction is below tol.
 // A frequency whose refinement does not converge is solved alone by the
 // double-precision pivoted LU (same section, paragraph after the steps).
