@@ -434,7 +434,17 @@ class Solver:
 
 
 class Afs:
-    """Owns one adaptive-frequency-sampling handle on a Solver's context."""
+    """Owns one adaptive-frequency-sampling handle on a Solver's context.
+
+    Example (device tensors L, Psi, G float64 n x n; b complex128 nrhs x n)::
+
+        with Solver(n, nrhs, batch=2) as s, Afs(s, tol=1e-4) as a:
+            x = torch.empty((m, nrhs, n), dtype=torch.complex128, device="cuda")
+            sampled, resid, info = a.sweep(L, Psi, G, omega, zs, b, x)
+            # x[i] is the reduced-order solution at omega[i]; `sampled` lists
+            # the candidates solved in full, in order; info.converged is 1 if
+            # every residual estimate is below tol
+    """
 
     def __init__(self, solver: Solver, **opts):
         self.solver = solver
