@@ -351,3 +351,21 @@ def test_generator_port_excitation():
         assert 0.5e-3 < np.std(rest.real) < 2e-3 and 0.5e-3 < np.std(rest.imag) < 2e-3
     _, _, B0 = workload.draw_points_and_rhs(0)
     assert np.array_equal(B0, workload.make(0).B)
+
+
+def test_unpivoted_lu_of_complex_symmetric_is_ldlt():
+    # the symmetric factorisation mode rests on two facts: for Z = Z^T the
+    # unpivoted LU has U = D L^T with D = diag(U), and the Schur complement
+    # left after eliminating a leading block is symmetric again, so its lower
+    # part determines it
+    wl = workload.make_small(70, seed=5, nf=1)
+    Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0])
+    LU, st = oracle.lu_nopiv(Z)
+    assert st == 0
+    L = np.tril(LU, -1) + np.eye(70)
+    U = np.triu(LU)
+    D = np.diag(U)
+    assert np.abs(U - D[:, None] * L.T).max() <= 1e-12 * np.abs(U).max()
+    k = 32
+    S = Z[k:, k:] - Z[k:, :k] @ np.linalg.solve(Z[:k, :k], Z[:k, k:])
+    assert np.abs(S - S.T).max() <= 1e-12 * np.abs(S).max()
