@@ -65,40 +65,51 @@ def workload_name(cfg):
             f"{c.nrhs} RHS, Z = jwL - jPsi/w + Zs G")
 
 
-def profile_traffic(name, source):
-    """DRAM bytes per launch recorded in profiles/<name>.md by an ncu capture,
-    or None when the kernel source has changed since (the summary records the
-    sha256 of the source file it was taken with)."""
+def profile_traffic(kernel):
+    """DRAM bytes per launch of `kernel` recorded by an ncu capture in
+    profiles/traffic.json, or None when there is no record or the kernel's
+    source file has changed since (each record holds the SHA-256 of the
+    source it was measured with)."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", name + ".md")
-    src = os.path.join(ROOT, "mixed_precision_refinement_gb300", "csrc", source)
-    if not (os.path.exists(path) and os.path.exists(src)):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get("kernels", {}).get(kernel)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, rec["source"])
+    if not os.path.exists(src):
         return None
     with open(src, "rb") as f:
-        digest = hashlib.sha256(f.read()).hexdigest()
-    rec = {}
-    with open(path) as f:
-        for line in f:
-            if line.startswith("- source_sha256: ") or line.startswith("- dram_bytes_per_launch: "):
-                k, v = line[2:].split(":", 1)
-                rec[k.strip()] = v.strip().strip("`")
-    if rec.get("source_sha256") != digest or "dram_bytes_per_launch" not in rec:
-        return None
+        if hashlib.sha256(f.read()).hexdigest() != rec.get("source_sha256"):
+            return None
     return float(rec["dram_bytes_per_launch"])
 
 
-def launch_list_shares():
-    """Share of each kernel function in the committed ncu launch list of the
-    benchmark sweep (profiles/launches_sweep_n2157_21freq_tf32x3.md)."""
-    path = os.path.join(ROOT, "profiles", "launches_sweep_n2157_21freq_tf32x3.md")
-    shares = {}
-    if os.path.exists(path):
-        with open(path) as f:
-            for line in f:
-                m = re.match(r"\|\s*`(k_\w+)`\s*\|\s*\d+\s*\|\s*[\d.]+\s*\|\s*([\d.]+)\s*%", line)
-                if m:
-                    shares[m.group(1)] = float(m.group(2))
-    return shares
+# Kernels of the path and the profile stages their launches are counted in
+# (k_cgemm_tc runs both the block solves and the trailing updates in the
+# tensor-core modes; the FP32 mode has its own kernels for both).
+STAGE_KERNELS = {
+    "diag": "k_diag_block", "assemble": "k_assemble", "trsv": "k_trsv_inv", "residual": "k_residual",
+    "pack": "k_pack_trsm", "update": "k_update + k_relcorr", "fallback": "k_lu64",
+}
+
+
+def kernel_times(stage_ms, gemm):
+    """Device time per kernel (ms) from the per-stage sums of a profiled pass."""
+    out = {STAGE_KERNELS[k]: v for k, v in stage_ms.items() if k in STAGE_KERNELS}
+    if gemm == "FFMA":
+        out["k_trsm_l + k_trsm_u"] = stage_ms.get("trsm", 0.0)
+        out["k_schur_simt"] = stage_ms.get("schur", 0.0)
+    else:
+        out["k_cgemm_tc"] = stage_ms.get("trsm", 0.0) + stage_ms.get("schur", 0.0)
+    return out
+
+
+def dominant_kernel(times, candidates):
+    """The candidate with the largest device time in this run's profiled pass."""
+    return max(candidates, key=lambda k: times.get(k, 0.0))
 
 
 def diag_flops(nb=128):
@@ -466,63 +477,65 @@ def run_ours(args):
     res_bytes = n_res_calls * (16.0 * n * n + 32.0 * n * nrhs)
     res_ms = st["residual"]["ms"] / steps
     res_gbs = res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None
-    asm_bytes = 24.0 * n * n + 24.0 * n * n * nf
     stage_ms = {k: v["ms"] / steps for k, v in st.items()}
     fp32_peak = SMS * FP32_LANES * 2 * SM_MAX_MHZ * 1e6 / 1e12
-    fp64_peak = FP64_NOMINAL_TFLOPS
     tf32_peak = peaks["bf16_tflops"] * TF32_OVER_BF16
-    # The roofline object covers the dominant kernel of the path: k_cgemm_tc,
-    # the tcgen05 complex-product kernel that runs both the trailing updates
-    # and the block solves (the largest share of the ncu launch list).
-    # Achieved = useful complex-product flops per launch / mean launch
-    # duration (CUDA events around every launch, on the stream it runs on;
-    # with two lanes the launches run next to the other lane's kernels).
-    tc_launches = max(1, st["schur"]["launches"] + (st["trsm"]["launches"] if args.gemm != "FFMA" else 0))
-    tc_ms_tot = st["schur"]["ms"] + (st["trsm"]["ms"] if args.gemm != "FFMA" else 0.0)
-    tc_flops_tot = (schur_f + (trsm_flops(n) * nf if args.gemm != "FFMA" else 0)) * steps
-    tc_ms = tc_ms_tot / tc_launches
-    tc_ach = (tc_flops_tot / tc_launches) / (tc_ms / 1e3) / 1e12 if tc_ms > 0 else None
-    if args.gemm == "FFMA":
-        roof = {"kernel": "k_schur_simt", "bound": "alu", "achieved": tc_ach, "peak": fp32_peak, "unit": "TFLOP/s",
-                "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz"}
+    hbm = peaks["hbm_gbs"]
+    # Roofline objects of the path's kernels: achieved = algorithmic work per
+    # launch (flops or bytes, per unit as stated in "work") / the mean launch
+    # duration from the profiled pass (CUDA events around every launch, on
+    # the stream it runs on; with two lanes the launches run beside the other
+    # lane's kernels).
+    def obj(kernel, bound, stage_ms_tot, launches, work_tot, peak, unit, peak_source, work, **extra):
+        launches = max(1, launches)
+        lms = stage_ms_tot / launches
+        ach = (work_tot / launches) / (lms / 1e3) / (1e12 if unit == "TFLOP/s" else 1e9) if lms > 0 else None
+        o = {"kernel": kernel, "bound": bound, "achieved": ach, "peak": peak, "unit": unit,
+             "frac": (ach / peak) if ach else None, "peak_source": peak_source, "work": work,
+             "launch_ms": lms, "launches_per_step": launches / steps}
+        o.update(extra)
+        return o
+
+    rl = {}
+    tc = args.gemm != "FFMA"
+    tc_launches = st["schur"]["launches"] + (st["trsm"]["launches"] if tc else 0)
+    tc_ms_tot = st["schur"]["ms"] + (st["trsm"]["ms"] if tc else 0.0)
+    tc_flops_tot = (schur_f + (trsm_flops(n) * nf if tc else 0)) * steps
+    if tc:
+        rl["k_cgemm_tc"] = obj(
+            "k_cgemm_tc", "tensor", tc_ms_tot, tc_launches, tc_flops_tot, tf32_peak, "TFLOP/s",
+            f"tf32 = {peak_src} bf16 {peaks['bf16_tflops']} x 1.1/2.25",
+            "useful complex-product flops (8 per complex MAC) of the trailing updates and block solves; "
+            "the 3xTF32 split runs 3x that on the pipe", traffic=None)
     else:
-        roof = {"kernel": "k_cgemm_tc (trailing updates + block solves)", "bound": "tensor", "achieved": tc_ach,
-                "peak": tf32_peak, "unit": "TFLOP/s",
-                "peak_source": f"tf32 = {peak_src} bf16 {peaks['bf16_tflops']} x 1.1/2.25",
-                "flops": "useful complex-product flops (8 per complex MAC); the 3xTF32 split runs 3x that on the pipe"}
-    roof["frac"] = (roof["achieved"] / roof["peak"]) if roof.get("achieved") and roof.get("peak") else None
-    tb = profile_traffic("k_cgemm_tc_n2157", "schur_tc.cu") if (args.config == 1 and args.gemm == "TF32X3") else None
-    roof["traffic"] = tb
-    roof["launch_ms"] = tc_ms
-    # k_diag_block: one CTA per frequency; algorithmic flops per launch = the
-    # frequencies one launch covers x diag_flops, over the mean launch time
+        rl["k_schur_simt"] = obj(
+            "k_schur_simt", "alu", st["schur"]["ms"], st["schur"]["launches"], schur_f * steps, fp32_peak,
+            "TFLOP/s", "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz", "useful trailing-update flops")
+    # k_diag_block: one CTA per frequency; the frequencies one launch covers x diag_flops
     d_launches = max(1, st["diag"]["launches"])
-    d_ms = st["diag"]["ms"] / d_launches
-    d_units = nf * steps * ((n + 127) // 128) / d_launches  # frequencies per launch
-    d_ach = d_units * diag_flops() / (d_ms / 1e3) / 1e12 if d_ms > 0 else None
-    droof = {"kernel": "k_diag_block (diagonal-block LU + triangle inverses)", "bound": "alu",
-             "achieved": d_ach, "peak": fp32_peak, "unit": "TFLOP/s",
-             "peak_source": "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz",
-             "flops": f"16/3 x 128^3 real flop per frequency, {d_units:.1f} frequencies (one CTA each) per launch",
-             "frac": (d_ach / fp32_peak) if d_ach else None,
-             "frac_of_busy_sms": (d_ach / (fp32_peak * d_units / SMS)) if d_ach else None,
-             "traffic": profile_traffic("k_diag_block_n2157", "diag_block.cu") if args.config == 1 else None,
-             "launch_ms": d_ms}
-    # the roofline object covers the kernel with the largest share of the
-    # committed ncu launch list; the other one goes with the rest
-    shares = launch_list_shares()
-    diag_dominant = shares.get("k_diag_block", 0.0) > shares.get("k_cgemm_tc", 0.0)
-    # the other bounded kernels, for context
-    asm_ms = stage_ms["assemble"]
-    rooflines = {
-        "residual": {"kernel": "k_residual" if resid_mode == "F64" else "k_residual_df", "bound": "hbm",
-                     "achieved": res_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None},
-        "assemble": {"kernel": "k_assemble", "bound": "hbm", "unit": "GB/s", "peak": peaks["hbm_gbs"],
-                     "achieved": asm_bytes / (asm_ms / 1e3) / 1e9 if asm_ms > 0 else None},
-    }
-    if rooflines["assemble"]["achieved"]:
-        rooflines["assemble"]["frac"] = rooflines["assemble"]["achieved"] / peaks["hbm_gbs"]
+    d_units = nf * steps * ((n + 127) // 128) / d_launches
+    dobj = obj("k_diag_block", "alu", st["diag"]["ms"], d_launches, diag_flops() * d_units * d_launches,
+               fp32_peak, "TFLOP/s", "FP32 FFMA: 152 SMs x 128 lanes x 2 flop x 2070 MHz",
+               f"16/3 x 128^3 real flop per frequency, {d_units:.1f} frequencies (one CTA each) per launch",
+               traffic=profile_traffic("k_diag_block") if args.config == 1 else None)
+    if dobj["achieved"]:
+        dobj["frac_of_busy_sms"] = dobj["achieved"] / (fp32_peak * d_units / SMS)
+    rl["k_diag_block"] = dobj
+    # triangular solves: the float32 factors (8 n^2 bytes) once per solve and frequency
+    n_solves = sum(i.iters + 1 for i in infos if not i.fallback)
+    rl["k_trsv_inv"] = obj("k_trsv_inv", "hbm", st["trsv"]["ms"], st["trsv"]["launches"],
+                           n_solves * 8.0 * n * n * math.ceil(nrhs / 4) * steps, hbm, "GB/s", f"{peak_src} copy",
+                           "8 n^2 bytes of float32 factors per solve and frequency")
+    rl["k_residual"] = obj("k_residual" if resid_mode == "F64" else "k_residual_df", "hbm", st["residual"]["ms"],
+                           st["residual"]["launches"], res_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
+                           "16 n^2 + 32 n nrhs bytes per evaluation and frequency")
+    lanes = 2 if nf >= 2 else 1
+    rl["k_assemble"] = obj("k_assemble", "hbm", st["assemble"]["ms"], st["assemble"]["launches"],
+                           (24.0 * n * n * lanes + 24.0 * n * n * nf) * steps, hbm, "GB/s", f"{peak_src} copy",
+                           "24 n^2 bytes of L, Psi, G read once per lane + 24 n^2 written per frequency")
+    ktimes = kernel_times(stage_ms, args.gemm)
+    dom = dominant_kernel(ktimes, list(rl))
+    tot_k = sum(ktimes.values())
     launches = sum(v["launches"] for v in launch_counts.values())
     h2d = 3 * 8 * n * n + 16 * n * nrhs
     d2h = 16 * nf * nrhs * n
@@ -536,9 +549,10 @@ def run_ours(args):
                    "batch": args.batch or nf, "l2": "flushed between steps (512 MB write)",
                    "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
         "lu_tflops": lu_tflops, "resid_gbs": res_gbs,
-        "roofline": droof if diag_dominant else roof,
-        "rooflines_other": dict(rooflines, **({"cgemm_tc": roof} if diag_dominant else {"diag_block": droof})),
-        "launch_list_share_pct": {k: shares.get(k) for k in ("k_diag_block", "k_cgemm_tc")},
+        # the kernel with the largest device time in this run's profiled pass
+        "roofline": rl[dom],
+        "rooflines_other": {k: v for k, v in rl.items() if k != dom},
+        "kernel_time_share_pct": {k: round(100.0 * v / tot_k, 2) for k, v in ktimes.items()} if tot_k else None,
         "stage_ms_per_step": stage_ms,
         "stage_note": "from a second pass of the same steps with CUDA events around every launch "
                       f"({prof_ms_step:.3f} ms per step with the events); per-stage sums of per-launch device "

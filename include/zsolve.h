@@ -90,6 +90,9 @@ typedef struct {
                            precision residual still uses all of Z, so a Z that is not
                            symmetric is still solved (refinement or the fallback).  Tensor-
                            core modes only (ignored with ZSOLVE_GEMM_FFMA); 0: the full update */
+    int wait_limit;     /* polls before a wait of the triangular solve for another task's block gives
+                           up with ZSOLVE_ETIMEOUT (0, the default: 2^22, about a second); a small
+                           value lets a test see a wait give up quickly (zsolve_selftest_wait) */
 } zsolve_opts;
 
 /* stages of the path, for zsolve_get_profile */
@@ -124,28 +127,39 @@ typedef struct {
 int zsolve_default_opts(zsolve_opts *opts);
 
 /* Create a context for n x n systems with up to nrhs_max right-hand sides.
- * opts may be NULL (defaults).  Allocates the device workspaces. */
+ * opts may be NULL (defaults).  Allocates the device workspaces.
+ * Passage: section "Double-precision answers from a GPU without double
+ * precision" (the factors, residual and correction the steps keep) and
+ * section "Measure first" (the memory a dense complex system of size n takes). */
 int zsolve_create(zsolve_ctx **ctx, int64_t n, int nrhs_max, const zsolve_opts *opts);
 
-/* Enqueue subsequent work on `stream` (a cudaStream_t; NULL = default stream). */
+/* Enqueue subsequent work on `stream` (a cudaStream_t; NULL = default stream).
+ * No passage: the page runs one queue of GPU work; this names it. */
 int zsolve_set_stream(zsolve_ctx *ctx, void *stream);
 
 /* Z(omega) = j*omega*L - j*Psi/omega + Zs*G, written in float64 (kept for the
  * residual) and rounded to complex float32 (to be factorised), in one pass
  * over L, Psi, G (device, n x n float64).  omega > 0; zs_re + j*zs_im is
- * Zs(omega), computed by the caller. */
+ * Zs(omega), computed by the caller.
+ * Passage: section "Fewer frequency points: adaptive frequency sampling", the
+ * form of Z with L, Psi, G independent of frequency. */
 int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G,
                     double omega, double zs_re, double zs_im);
 
 /* Unpivoted LU of the complex float32 copy of the assembled Z, in place:
  * 32-column panels inside 128-column outer blocks, trailing update by the
- * opts.gemm arithmetic.  Records whether a pivot was tiny or non-finite. */
+ * opts.gemm arithmetic.  Records whether a pivot was tiny or non-finite.
+ * Passage: section "Double-precision answers from a GPU without double
+ * precision", step 1 (single-precision LU in blocks of 32, no pivoting). */
 int zsolve_factor(zsolve_ctx *ctx);
 
 /* Refine x for nrhs right-hand sides b (device c128, nrhs x n) against the
  * assembled and factored Z; x (device c128, nrhs x n) is output only.  A
  * stalled refinement or a flagged pivot switches this call to the float64
- * pivoted LU (info->fallback = 1).  info (host) may be NULL. */
+ * pivoted LU (info->fallback = 1).  info (host) may be NULL.
+ * Passage: section "Double-precision answers from a GPU without double
+ * precision", steps 2-4 and the paragraph after them (the stopping test and
+ * the switch to a direct solve when the refinement does not converge). */
 int zsolve_refine(zsolve_ctx *ctx, const void *b, void *x, int nrhs, zsolve_info *info);
 
 /* The whole sweep: for each of nf frequencies omega[f] (host array) with
@@ -162,6 +176,9 @@ int zsolve_refine(zsolve_ctx *ctx, const void *b, void *x, int nrhs, zsolve_info
  * residuals.  The call returns when all of it is done and the context's
  * stream is ordered after it.  Returns the first error; a frequency that
  * needed the fallback is not an error. */
+/* Passage: the page's introduction and section "Fewer frequency points" (a
+ * sweep is the same solve at every frequency of a list), with the steps of
+ * zsolve_assemble, zsolve_factor and zsolve_refine at each frequency. */
 int zsolve_sweep(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G,
                  const double *omega, const double *zs, int nf, const void *b, void *x,
                  int nrhs, zsolve_info *info);
@@ -184,6 +201,16 @@ int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int 
  * rounded to complex float32, solved in float32, and d returned as c128.
  * v, d: device c128, nrhs x n. */
 int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs);
+
+/* Check of the bounded device-side waits (failure detection without a GPU
+ * fault): runs the low-precision solve of the factored single system with
+ * its first task withheld, so that every other task waits for a block that no
+ * task computes.  Each wait gives up after opts.wait_limit polls and raises
+ * the device status bit; the call returns ZSOLVE_ETIMEOUT, the expected
+ * result (ZSOLVE_OK would mean that a wait did not give up).  The status bit
+ * is cleared on return, so the context stays usable.  The contents of the
+ * context's solve buffer are left undefined. */
+int zsolve_selftest_wait(zsolve_ctx *ctx, int nrhs);
 
 /* x = Z^-1 b by the float64 LU with partial pivoting of the assembled Z (the
  * fallback on its own).  b, x: device c128, nrhs x n. */
@@ -337,13 +364,13 @@ const char *zsolve_afs_last_error(const zsolve_afs *afs);
 /* Release the handle's buffers.  NULL is allowed. */
 void zsolve_afs_destroy(zsolve_afs *afs);
 
-/* Static string for a status code. */
+/* Static string for a status code.  No passage: error reporting of the library. */
 const char *zsolve_strerror(int status);
 
 /* Message of the last failure in this context ("" if none). */
 const char *zsolve_last_error(const zsolve_ctx *ctx);
 
-/* Release every workspace.  NULL is allowed. */
+/* Release every workspace.  NULL is allowed.  No passage: resource release. */
 void zsolve_destroy(zsolve_ctx *ctx);
 
 #ifdef __cplusplus

@@ -44,7 +44,7 @@ class zsolve_opts(ctypes.Structure):
     _fields_ = [("tol", ctypes.c_double), ("max_iter", ctypes.c_int), ("gemm", ctypes.c_int),
                 ("outer_block", ctypes.c_int), ("batch", ctypes.c_int), ("force_fallback", ctypes.c_int),
                 ("profile", ctypes.c_int), ("resid", ctypes.c_int), ("lanes", ctypes.c_int),
-                ("symmetric", ctypes.c_int)]
+                ("symmetric", ctypes.c_int), ("wait_limit", ctypes.c_int)]
 
 
 STAGES = ("assemble", "diag", "trsm", "schur", "trsv", "residual", "update", "fallback", "pack")
@@ -107,6 +107,7 @@ def _load():
         "zsolve_residual": (I, [P, P, P, P, I]),
         "zsolve_lowprec_solve": (I, [P, P, P, I]),
         "zsolve_fallback_solve": (I, [P, P, P, I]),
+        "zsolve_selftest_wait": (I, [P, I]),
         "zsolve_get_z64": (I, [P, P]),
         "zsolve_get_z32": (I, [P, P, P]),
         "zsolve_pivot_flag": (I, [P, ctypes.POINTER(I)]),
@@ -275,6 +276,11 @@ def zsolve_fallback_solve(ctx, b, x) -> None:
     _require(x, "c128", True)
     nrhs = b.shape[0] if b.dim() == 2 else 1
     _check(ctx, _lib.zsolve_fallback_solve(ctx, _ptr(b), _ptr(x), nrhs))
+
+
+def zsolve_selftest_wait(ctx, nrhs: int = 1) -> int:
+    """Status of the bounded-wait check (ZSOLVE_ETIMEOUT when the waits give up as they should)."""
+    return int(_lib.zsolve_selftest_wait(ctx, int(nrhs)))
 
 
 def zsolve_get_z64(ctx, dst) -> None:

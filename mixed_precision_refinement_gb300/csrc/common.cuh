@@ -97,12 +97,12 @@ __device__ __forceinline__ long long progress_read(const unsigned long long *p, 
 }
 
 __device__ __forceinline__ long long progress_wait(const unsigned long long *p, unsigned epoch, long long need,
-                                                   unsigned *status) {
+                                                   unsigned *status, unsigned limit = ZS_SPIN_LIMIT) {
     unsigned it = 0;
     while (true) {
         long long c = progress_read(p, epoch);
         if (c > need) return c;
-        if (++it > ZS_SPIN_LIMIT) {
+        if (++it > limit) {
             atomicOr(status, ZS_DEV_TIMEOUT);
             return -1;
         }
@@ -232,10 +232,15 @@ cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int6
 #define ZS_WINV_STRIDE (8 * ZS_WINV_PLANE)
 inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }
 // Triangular solves with 128-row blocks and the inverse diagonal blocks; nrhs 1, 2 or 4 per launch.
+// wait_limit: polls before a wait for another task's block gives up (raising
+// ZS_DEV_TIMEOUT in *status).  first_ticket: the task ticket starts here
+// (0 in every solve; a positive value withholds the first tasks, so that the
+// bounded waits can be shown to give up -- a testing aid).
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                const float *dinv, int64_t dinv_stride, float2 *v, int64_t v_stride, int nrhs,
                                const int *slots, int nslot, unsigned long long *prog, unsigned epoch, unsigned *ticket,
-                               unsigned *status, int num_sms, cudaStream_t st);
+                               unsigned *status, int num_sms, cudaStream_t st, unsigned wait_limit = ZS_SPIN_LIMIT,
+                               unsigned first_ticket = 0);
 
 // r = b - Z64 x.  out_c64 != NULL: writes float2 (rounded); else writes c128 to out_c128.
 // Launches one kernel per chunk of 8/4/2/1 right-hand sides (zs_rhs_chunks).

@@ -26,9 +26,9 @@ constexpr int TB = ZS_TB2;  // 128
 // lane 0 waits until more than `need` blocks are complete; the warp barrier
 // orders the other lanes' loads after its acquire
 __device__ __forceinline__ long long warp_progress(const unsigned long long *p, unsigned epoch, long long need,
-                                                   unsigned *status, int lane) {
+                                                   unsigned *status, int lane, unsigned limit) {
     long long c = 0;
-    if (lane == 0) c = zs::progress_wait(p, epoch, need, status);
+    if (lane == 0) c = zs::progress_wait(p, epoch, need, status, limit);
     c = __shfl_sync(0xffffffffu, c, 0);
     __syncwarp();
     return c;
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
            const float *__restrict__ dinv, int64_t dinv_stride, float2 *__restrict__ v, int64_t v_stride,
            const int *__restrict__ slots, int nslot, unsigned long long *__restrict__ prog, unsigned epoch,
-           unsigned *ticket, unsigned *status) {
+           unsigned *ticket, unsigned *status, unsigned wait_limit) {
     constexpr bool kPreload = R == 1;
     extern __shared__ __align__(16) float sinv[];  // [re, im][TB][TB]
     __shared__ cf part[TB][R];
@@ -137,7 +137,7 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
 #pragma unroll
             for (int r = 0; r < R; r++) acc[i][r] = cf{0.f, 0.f};
         bool ok = true;
-        if (phase == 1) ok = warp_progress(pf, epoch, b, status, lane) >= 0;  // own forward result
+        if (phase == 1) ok = warp_progress(pf, epoch, b, status, lane, wait_limit) >= 0;  // own forward result
         // the block's right-hand side (final now: the input, resp. the forward result)
         cf vb = cf{0.f, 0.f};
         const int ei = tid / R, er = tid - ei * R;
@@ -167,7 +167,7 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
                 }
             }
             if (q >= ready) {
-                ready = warp_progress(phase == 0 ? pf : pb, epoch, q, status, lane);
+                ready = warp_progress(phase == 0 ? pf : pb, epoch, q, status, lane, wait_limit);
                 if (ready < 0) {
                     ok = false;
                     break;
@@ -305,7 +305,7 @@ template <int R>
 cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, const float *dinv,
                        int64_t dinv_stride, float2 *v, int64_t v_stride, const int *slots, int nslot,
                        unsigned long long *prog, unsigned epoch, unsigned *ticket, unsigned *status, int num_sms,
-                       cudaStream_t st) {
+                       cudaStream_t st, unsigned wait_limit, unsigned first_ticket) {
     // once per process and instance (thread-safe initialisation of a local static)
     static const cudaError_t attr =
         cudaFuncSetAttribute(k_trsv_inv<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
@@ -318,14 +318,22 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
     int64_t grid = (int64_t)per_sm * num_sms;
     const int64_t tasks = 2 * nblk * nslot;
     if (grid > tasks) grid = tasks;
-    e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
+    if (first_ticket == 0) {
+        e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
+    } else {
+        // withheld tasks (testing aid): the value is staged by the copy
+        // before the call returns, so a local is a valid source
+        const unsigned t0 = first_ticket;
+        e = cudaMemcpyAsync(ticket, &t0, sizeof(unsigned), cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    }
     if (e != cudaSuccess) return e;
     // A plain launch: a task waits only on tasks with smaller tickets, which
     // CTAs that are already running have claimed, so the solve progresses
     // with any number of resident CTAs -- also while another stream's kernels
     // hold part of the GPU.
     k_trsv_inv<R><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride,
-                                                       slots, nslot, prog, epoch, ticket, status);
+                                                       slots, nslot, prog, epoch, ticket, status, wait_limit);
     return cudaGetLastError();
 }
 
@@ -334,17 +342,18 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                const float *dinv, int64_t dinv_stride, float2 *v, int64_t v_stride, int nrhs,
                                const int *slots, int nslot, unsigned long long *prog, unsigned epoch, unsigned *ticket,
-                               unsigned *status, int num_sms, cudaStream_t st) {
+                               unsigned *status, int num_sms, cudaStream_t st, unsigned wait_limit,
+                               unsigned first_ticket) {
     switch (nrhs) {
         case 1:
             return launch_inv<1>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
-                                 epoch, ticket, status, num_sms, st);
+                                 epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
         case 2:
             return launch_inv<2>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
-                                 epoch, ticket, status, num_sms, st);
+                                 epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
         case 4:
             return launch_inv<4>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
-                                 epoch, ticket, status, num_sms, st);
+                                 epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
         default:
             return cudaErrorInvalidValue;
     }

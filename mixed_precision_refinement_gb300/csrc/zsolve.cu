@@ -42,6 +42,7 @@ struct zsolve_ctx {
     int nrhs_max = 0;
     zsolve_opts opts{};
     int device = 0, num_sms = 0;
+    unsigned wait_limit = ZS_SPIN_LIMIT;  // polls before a triangular-solve wait gives up
     cudaStream_t stream = nullptr;
     int S = 1;  // frequencies held at once
     int64_t ld = 0, plane = 0, z32_stride = 0, z64_stride = 0, pack_stride = 0, v_stride = 0;
@@ -310,8 +311,10 @@ int factor_slots(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot, int fir
 
 // ------------------------------------------------------------------ solves
 
-// v <- (LU)^-1 v for the listed slots, right-hand sides in chunks of 4/2/1
-int lowprec_solve_slots(zsolve_ctx *ctx, Lane &ln, int nrhs, const int *slots, int nslot) {
+// v <- (LU)^-1 v for the listed slots, right-hand sides in chunks of 4/2/1.
+// first_ticket > 0 withholds the first tasks of each launch (testing aid of
+// the bounded waits, zsolve_selftest_wait); 0 in every solve.
+int lowprec_solve_slots(zsolve_ctx *ctx, Lane &ln, int nrhs, const int *slots, int nslot, unsigned first_ticket = 0) {
     int r0 = 0;
     while (r0 < nrhs) {
         const int left = nrhs - r0;
@@ -320,7 +323,8 @@ int lowprec_solve_slots(zsolve_ctx *ctx, Lane &ln, int nrhs, const int *slots, i
         StageSpan sp(ctx, ZSOLVE_STAGE_TRSV, ln.stream);
         ZS_CU(zs_launch_trsv_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->dinv, ctx->dinv_stride,
                                  ctx->v + (int64_t)r0 * ctx->n, ctx->v_stride, R, slots, nslot, ctx->prog, epoch,
-                                 ln.ticket, ctx->d_status, ln.trsv_grid ? ln.trsv_grid : ctx->num_sms, ln.stream));
+                                 ln.ticket, ctx->d_status, ln.trsv_grid ? ln.trsv_grid : ctx->num_sms, ln.stream,
+                                 ctx->wait_limit, first_ticket));
         sp.done(1);
         r0 += R;
     }
@@ -811,6 +815,7 @@ int zsolve_default_opts(zsolve_opts *opts) {
     opts->resid = ZSOLVE_RESID_F64;
     opts->lanes = 0;
     opts->symmetric = 1;
+    opts->wait_limit = 0;
     return ZSOLVE_OK;
 }
 
@@ -825,12 +830,13 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
         ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0 || ctx->opts.resid < 0 ||
         ctx->opts.resid > ZSOLVE_RESID_DF || ctx->opts.lanes < 0 || ctx->opts.lanes > 2 || ctx->opts.symmetric < 0 ||
-        ctx->opts.symmetric > 1) {
+        ctx->opts.symmetric > 1 || ctx->opts.wait_limit < 0) {
         delete ctx;
         return ZSOLVE_EINVAL;
     }
     ctx->n = n;
     ctx->nrhs_max = nrhs_max;
+    if (ctx->opts.wait_limit > 0) ctx->wait_limit = (unsigned)ctx->opts.wait_limit;
     auto bail = [&](int code) {
         free_all(ctx);
         delete ctx;
@@ -1066,6 +1072,16 @@ int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs) {
     StageSpan sp(ctx, ZSOLVE_STAGE_UPDATE, ctx->stream);
     ZS_CU(zs_launch_widen(ctx->v, (double2 *)d, cnt, ctx->stream));
     sp.done(1);
+    return check_device_status(ctx, ctx->lane[0]);
+}
+
+int zsolve_selftest_wait(zsolve_ctx *ctx, int nrhs) {
+    if (!ctx) return ZSOLVE_EINVAL;
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "zsolve_selftest_wait before zsolve_factor");
+    // every task but the first waits, directly or through the chain, for the
+    // first block, which no task computes
+    ZS_TRY(lowprec_solve_slots(ctx, ctx->lane[0], nrhs, ctx->d_all, 1, 1u));
     return check_device_status(ctx, ctx->lane[0]);
 }
 

@@ -121,12 +121,9 @@ def evaluate(Lr, Pr, Gr, M, wb, br, bb, omega, zs):
 
 
 def afs_sweep(L, Psi, G, omega, zs, B, tol: float = 1e-4, max_solves: int = 32,
-              max_basis: int = 96, drop: float = 1e-8, exact_solver=None) -> AfsResult:
+              max_basis: int = 96, drop: float = 1e-8) -> AfsResult:
     """The adaptive frequency sampling loop over the candidate list omega.
-
-    exact_solver(k) -> (nrhs, n) may replace the oracle's direct solve at
-    candidate k (tests use it to feed both sides the same exact solutions).
-    """
+    The exact solves are the oracle's own assembly and direct solve."""
     L, Psi, G = (np.asarray(a, dtype=np.float64) for a in (L, Psi, G))
     B = np.atleast_2d(np.asarray(B, dtype=np.complex128))
     omega = np.asarray(omega, dtype=np.float64)
@@ -141,10 +138,7 @@ def afs_sweep(L, Psi, G, omega, zs, B, tol: float = 1e-4, max_solves: int = 32,
     while m > 0:
         # step 1: exact solves, real and imaginary parts into the basis
         for k in pending:
-            if exact_solver is not None:
-                Xk = np.atleast_2d(exact_solver(k))
-            else:
-                Xk = solve(assemble(L, Psi, G, omega[k], zs[k]), B)
+            Xk = solve(assemble(L, Psi, G, omega[k], zs[k]), B)
             exact[k] = Xk
             sampled.append(k)
             for r in range(nrhs):

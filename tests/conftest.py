@@ -28,3 +28,13 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def config1_oracle():
+    """The oracle's direct solves of the N=2157 workload at all 21 frequencies
+    (complex128 pivoted LU; a few seconds), shared by the full-size tests."""
+    import oracle
+    import workload
+    wl = workload.make(1)
+    return wl, oracle.solve_sweep(wl)

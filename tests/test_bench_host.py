@@ -1,8 +1,9 @@
 """Host-side arithmetic of bench.py, without a GPU: the flop counts behind
-the roofline objects, the parser of the committed ncu launch list, and the
-source-hash check that keeps a recorded DRAM traffic figure from outliving
-the kernel it was measured on."""
+the roofline objects, the choice of the roofline kernel from a run's own
+per-stage times, and the source-hash check that keeps a recorded DRAM
+traffic figure from outliving the kernel it was measured on."""
 import hashlib
+import json
 import os
 
 import pytest
@@ -36,11 +37,16 @@ def test_schur_and_trsm_flops_small_cases():
     assert bench.trsm_flops(256) == 2 * 8 * 128 ** 3
 
 
-def test_launch_list_shares_parse_the_committed_profile():
-    shares = bench.launch_list_shares()
-    assert "k_cgemm_tc" in shares and "k_diag_block" in shares
-    assert sum(shares.values()) == pytest.approx(100.0, abs=1.5)
-    assert max(shares, key=shares.get) in ("k_cgemm_tc", "k_diag_block")
+def test_dominant_kernel_from_stage_times():
+    stage = {"assemble": 1.0, "diag": 3.9, "trsm": 1.9, "schur": 2.2, "trsv": 1.4, "residual": 1.7,
+             "update": 0.1, "fallback": 0.0, "pack": 1.2}
+    t = bench.kernel_times(stage, "TF32X3")
+    assert t["k_cgemm_tc"] == pytest.approx(4.1) and t["k_diag_block"] == 3.9
+    assert bench.dominant_kernel(t, ["k_diag_block", "k_cgemm_tc", "k_residual"]) == "k_cgemm_tc"
+    stage["diag"] = 4.5
+    assert bench.dominant_kernel(bench.kernel_times(stage, "TF32X3"), ["k_diag_block", "k_cgemm_tc"]) == "k_diag_block"
+    f = bench.kernel_times(stage, "FFMA")
+    assert "k_cgemm_tc" not in f and f["k_schur_simt"] == 2.2
 
 
 def test_profile_traffic_follows_the_source_hash(tmp_path, monkeypatch):
@@ -50,11 +56,20 @@ def test_profile_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     src = src_dir / "k.cu"
     src.write_bytes(b"// kernel source\n")
     digest = hashlib.sha256(src.read_bytes()).hexdigest()
-    (tmp_path / "profiles" / "k_n.md").write_text(
-        f"# k\n\n- dram_bytes_per_launch: `12345`\n- source_sha256: `{digest}`\n")
+    rec = {"kernels": {"k": {"dram_bytes_per_launch": 12345, "source_sha256": digest,
+                             "source": "mixed_precision_refinement_gb300/csrc/k.cu"}}}
+    (tmp_path / "profiles" / "traffic.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.profile_traffic("k_n", "k.cu") == 12345.0
+    assert bench.profile_traffic("k") == 12345.0
     src.write_bytes(b"// kernel source, changed\n")
-    assert bench.profile_traffic("k_n", "k.cu") is None
-    assert bench.profile_traffic("missing", "k.cu") is None
+    assert bench.profile_traffic("k") is None
+    assert bench.profile_traffic("missing") is None
     assert os.path.exists(src)
+
+
+def test_committed_traffic_records_are_well_formed():
+    with open(os.path.join(bench.ROOT, "profiles", "traffic.json")) as f:
+        rec = json.load(f)["kernels"]
+    for k, r in rec.items():
+        assert k.startswith("k_") and r["dram_bytes_per_launch"] > 0
+        assert os.path.exists(os.path.join(bench.ROOT, r["source"])) and len(r["source_sha256"]) == 64

@@ -8,9 +8,13 @@ Checked against the oracle:
 - every (frequency, right-hand side): the oracle's float64 normwise backward
   error eta = ||b - Z x|| / (||Z||_F ||x|| + ||b||), with Z assembled by the
   oracle, below ETA;
-- sampled frequencies of the two configurations whose complex128 pivoted LU
-  the oracle finishes in seconds: the oracle's direct solve, to the parity
-  bound 1e-10.
+- sampled frequencies: the oracle's complex128 pivoted-LU direct solve,
+  element by element to the parity bound 1e-10.  N = 6614: five frequencies
+  spread over the band, both ends (0.5 and 20 GHz) included; N = 8000: its
+  one frequency; N = 16384: 1 GHz, the low end of its band, where jwL
+  dominates Z most and cond(Z) is largest.  Each direct solve costs the
+  oracle (N^3/3 complex updates on the host cores) seconds at N = 6614 and
+  N = 8000 and a few minutes at N = 16384; the time is printed.
 
 Bound on eta: once the relative correction is below 1e-11 the backward
 error is set by the rounding of the float64 residual sums, which grows like
@@ -18,6 +22,8 @@ sqrt(n) * 2^-53; the test allows 16 sqrt(n) 2^-53 (1.4e-13 at n = 6614,
 2.3e-13 at n = 16384).  A solution that is only float32-accurate sits near
 1e-7, six orders of magnitude above.
 """
+import time
+
 import numpy as np
 import pytest
 
@@ -66,8 +72,8 @@ def sweep(zs, torch, wl):
     return X, infos
 
 
-@pytest.mark.timeout(1200)
-@pytest.mark.parametrize("cfg,sampled", [(2, (0, 40)), (3, (0,)), (4, ())])
+@pytest.mark.timeout(1800)
+@pytest.mark.parametrize("cfg,sampled", [(2, (0, 10, 20, 30, 40)), (3, (0,)), (4, (0,))])
 def test_full_size_configuration(zs, torch, cfg, sampled):
     wl = workload.make(cfg)
     n = wl.n
@@ -83,7 +89,12 @@ def test_full_size_configuration(zs, torch, cfg, sampled):
         worst = max(worst, float(eta.max()))
         assert np.all(eta < eta_max), (f, eta, eta_max)
         if f in sampled:
+            t0 = time.perf_counter()
             ref = oracle.solve(Z, wl.B)
-            assert np.all(rel_err(X[f], ref) <= PARITY), (f, rel_err(X[f], ref))
+            err = rel_err(X[f], ref)
+            print(f"config {cfg} frequency {f}: oracle direct solve {time.perf_counter() - t0:.1f} s on "
+                  f"{oracle.num_threads()} threads, max relative error {err.max():.2e}")
+            assert np.all(err <= PARITY), (f, err)
+            del ref
         del Z, R
     print(f"config {cfg}: worst normwise backward error {worst:.3e} (bound {eta_max:.3e})")

@@ -452,11 +452,12 @@ def test_argument_errors(zs, torch):
 
 
 @pytest.mark.parametrize("gemm,resid", [("FFMA", "F64"), ("TF32X3", "F64"), ("TF32X3", "DF")])
-def test_config1_full_sweep_sampled(zs, torch, gemm, resid):
+def test_config1_full_sweep_every_frequency(zs, torch, config1_oracle, gemm, resid):
     """N=2157, all 21 frequencies in one batched sweep (as the benchmark runs
-    it): oracle direct solves on a sample of frequencies, and for every
-    frequency the oracle's double-precision backward error of the returned x."""
-    wl = workload.make(1)
+    it): the oracle's direct solve at every frequency, element by element to
+    the parity bound, and the oracle's double-precision backward error of
+    every returned x."""
+    wl, ref_all = config1_oracle
     nf = len(wl.omega)
     s = zs.Solver(wl.n, 1, batch=nf, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm), resid=getattr(zs, "ZSOLVE_RESID_" + resid))
     try:
@@ -473,8 +474,7 @@ def test_config1_full_sweep_sampled(zs, torch, gemm, resid):
             eta = np.linalg.norm(R, axis=1) / (np.linalg.norm(Z) * np.linalg.norm(X[f], axis=1)
                                                + np.linalg.norm(wl.B, axis=1))
             assert np.all(eta < 1e-15), (f, eta)
-        for f in (0, nf // 2, nf - 1):
-            ref = oracle.solve_sweep(wl, [f])[0]
-            assert np.all(rel_err(X[f], ref) <= PARITY)
+        errs = np.array([rel_err(X[f], ref_all[f]).max() for f in range(nf)])
+        assert np.all(errs <= PARITY), errs
     finally:
         s.close()

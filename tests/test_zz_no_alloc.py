@@ -1,5 +1,6 @@
-"""The allocation-free solve (zsolve_lowprec_solve_noalloc) against the
-context-based one (zsolve_lowprec_solve), through the C-ABI.
+"""The allocation-free solve (zsolve_lowprec_solve_noalloc), through the
+C-ABI, against the oracle's complex128 substitution with the same float32
+factors and against the context-based solve (zsolve_lowprec_solve).
 
 It is for callers that cannot allocate device memory where they solve (a
 pool-managed application, a real-time loop, a plug-in whose host framework
@@ -13,14 +14,22 @@ import ctypes
 import numpy as np
 import pytest
 
+import oracle
 import workload
 
 pytestmark = pytest.mark.gpu
 
 # the context path applies the diagonal blocks through explicit inverses and
 # the allocation-free one by substitution: both are float32 solves with the
-# same factors, held to the tolerance the low-precision solve tests use
+# same factors, held to the tolerance the low-precision solve tests use (the
+# oracle solves with those factors in complex128)
 TOL = 1e-4
+
+
+def _oracle_solve(fac_re, fac_im, B):
+    """The oracle's unit-lower / upper substitution with the float32 factors."""
+    LU = fac_re.astype(np.float64) + 1j * fac_im.astype(np.float64)
+    return oracle.lu_solve(LU, None, oracle.cast_c64(B).astype(np.complex128))
 
 
 def _factored(zs, torch, wl, f):
@@ -50,6 +59,9 @@ def test_noalloc_solve_matches_context_solve_on_two_calls():
         ref = torch.empty_like(b)
         zs.zsolve_lowprec_solve(s.ctx, b, ref)
         ref = ref.cpu().numpy()
+        F = fac.cpu().numpy()
+        exact = _oracle_solve(F[: n * n].reshape(n, n), F[n * n:].reshape(n, n), wl.B)
+        assert np.all(_rel(ref, exact) <= TOL)
         lib = zs.raw_lib()
         for _ in range(2):  # the second call finds the previous call's scratch contents
             v = b.to(torch.complex64).contiguous()
@@ -58,6 +70,7 @@ def test_noalloc_solve_matches_context_solve_on_two_calls():
                                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
             assert st == zs.ZSOLVE_OK, zs.zsolve_strerror(st)
             got = v.cpu().numpy().astype(np.complex128)
+            assert np.all(_rel(got, exact) <= TOL)
             assert np.all(_rel(got, ref) <= TOL)
     finally:
         s.close()
@@ -82,11 +95,14 @@ def test_noalloc_solve_two_systems_and_limits():
             refs.append(r.cpu().numpy())
         finally:
             s.close()
+    F = fac.cpu().numpy()
+    exact = [_oracle_solve(F[f, : n * n].reshape(n, n), F[f, n * n:].reshape(n, n), wl.B) for f in range(2)]
     for _ in range(2):
         v = torch.stack([b, b]).to(torch.complex64).contiguous()
         zs.zsolve_lowprec_solve_noalloc(fac, n, n * n, 2 * n * n, n, 2, v, nrhs * n, nrhs)
         got = v.cpu().numpy().astype(np.complex128)
         for f in range(2):
+            assert np.all(_rel(got[f], exact[f]) <= TOL)
             assert np.all(_rel(got[f], refs[f]) <= TOL)
     lib = zs.raw_lib()
     v = torch.zeros(65 * n, dtype=torch.complex64, device="cuda")

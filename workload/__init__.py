@@ -217,3 +217,30 @@ def make_resonant_small(n: int, seed: int, m: int, nrhs: int = 1, psi_scale: flo
     wl = make_small(n, seed, nf=1, nrhs=nrhs)
     omega, zs = afs_candidates(m)
     return Workload(wl.points, wl.L, wl.Psi * psi_scale, wl.G, omega / (2.0 * math.pi), omega, zs, wl.B, None)
+
+
+def make_growth(n: int, seed: int, eps: float = 3e-9, nf: int = 1, nrhs: int = 1,
+                f_lo: float = 1e9, f_hi: float = 5e9) -> Workload:
+    """A well-conditioned system on which the unpivoted low-precision LU fails.
+
+    L is the identity with a tiny leading entry eps and a dense first row and
+    column v (N(0, 1/n) entries); Psi and G are zero, so Z = j*omega*L.  The
+    leading pivot is small (eps relative) but far above any tiny-pivot test;
+    eliminating it adds entries of size |v|^2/eps to the trailing block, in
+    whose float32 rounding the identity is lost.  Z itself stays well
+    conditioned (2-norm condition about 3), so its double-precision solution is well
+    defined, while the refinement on float32 factors stalls (relative
+    corrections near 1).
+    """
+    rng = np.random.default_rng(seed)
+    v = rng.normal(0.0, 1.0 / math.sqrt(n), n - 1)
+    L = np.eye(n)
+    L[0, 0] = eps
+    L[0, 1:] = v
+    L[1:, 0] = v
+    B = rng.normal(0.0, 1.0, (nrhs, n)) + 1j * rng.normal(0.0, 1.0, (nrhs, n))
+    freqs = np.linspace(f_lo, f_hi, nf) if nf > 1 else np.array([f_lo])
+    omega = 2.0 * math.pi * freqs
+    Z0 = np.zeros((n, n))
+    return Workload(np.zeros((n, 2)), L, Z0, Z0.copy(), freqs, omega, surface_impedance(omega),
+                    np.ascontiguousarray(B), None)
