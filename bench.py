@@ -36,6 +36,13 @@ import numpy as np  # noqa: E402
 import workload  # noqa: E402
 
 METRIC = "solved freq points/s at N=2157; LU TFLOP/s; FP64 residual GEMV HBM GB/s"
+RESID_NAMES = {0: "F64", 1: "DF", 2: "FX", 3: "LPG"}
+RESID_ARITH = {
+    "F64": "float64 DFMA GEMV over the assembled Z",
+    "DF": "double-float (2 x float32, ~46 bits)",
+    "FX": "exact 72-bit fixed-point products and sums on the integer pipes, float64-accurate",
+    "LPG": "float64 DFMA from L, Psi, G, four frequencies per pass (no assembled Z read)",
+}
 UNIT = "freq points/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 SMS, FP32_LANES, SM_MAX_MHZ = 152, 128, 2070.0
@@ -215,7 +222,7 @@ def profiled_pass(zs, torch, wl, args, L, P, G, b, x, flush):
     and the tensor-core kernels' mean launch duration.  Returns the profile
     and the pass's ms per step."""
     n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
-    s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm), batch=args.batch or nf, profile=1,
+    s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm_eff), batch=args.batch or nf, profile=1,
                   resid=getattr(zs, "ZSOLVE_RESID_" + args.resid), symmetric=args.symmetric)
     try:
         for _ in range(args.warmup):
@@ -243,10 +250,10 @@ def sweep_variant(zs, torch, wl, args, resid, symmetric=None):
     evaluation over its CUDA-event time)."""
     n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
     sym = args.symmetric if symmetric is None else symmetric
-    s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm), batch=args.batch or nf, profile=1,
+    s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm_eff), batch=args.batch or nf, profile=1,
                   resid=getattr(zs, "ZSOLVE_RESID_" + resid), symmetric=sym)
     try:
-        mode = "DF" if zs.zsolve_get_resid_mode(s.ctx) == zs.ZSOLVE_RESID_DF else "F64"
+        mode = RESID_NAMES[zs.zsolve_get_resid_mode(s.ctx)]
         L = torch.from_numpy(wl.L).cuda()
         P = torch.from_numpy(wl.Psi).cuda()
         G = torch.from_numpy(wl.G).cuda()
@@ -271,9 +278,12 @@ def sweep_variant(zs, torch, wl, args, resid, symmetric=None):
         res_bytes = iters / args.steps * (16.0 * n * n + 32.0 * n * nrhs)
         peaks, _ = load_peaks()
         gbs = res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None
-        return {"mode_in_use": mode, "points_per_s": nf / (ms / 1e3), "resid_gbs": gbs,
-                "resid_hbm_frac": (gbs / peaks["hbm_gbs"]) if gbs else None,
-                "arith": "float64 DFMA" if mode == "F64" else "double-float (2 x float32, ~46 bits)"}
+        out = {"mode_in_use": mode, "points_per_s": nf / (ms / 1e3), "resid_ms_per_step": res_ms,
+               "resid_gbs": gbs, "resid_hbm_frac": (gbs / peaks["hbm_gbs"]) if gbs else None,
+               "arith": RESID_ARITH[mode]}
+        if mode == "LPG":  # reads L, Psi, G (24 n^2) once per group of 4 frequencies, not Z (16 n^2 each)
+            out["note"] = "resid_gbs counts the float64 Z bytes the GEMV would read, for comparison"
+        return out
     finally:
         s.close()
 
@@ -352,6 +362,62 @@ def afs_variant(zs, torch, args, flush):
     return out
 
 
+def large_configs(zs, torch, args):
+    """The metric's large-system figures (one bounded pass each, headline
+    settings, no variants): configuration 3 (N=8000, one frequency, 8 RHS)
+    and configuration 4 (N=16384, 11 frequencies, 4 RHS).  Per configuration:
+    points/s of whole sweeps (CUDA events on the launching stream, inputs
+    resident, L2 flushed before each), the factorisation rate (8 N^3 / 3 real
+    flops per frequency over the lanes' factorisation spans), and the
+    residual's rate (16 N^2 + 32 N nrhs bytes per evaluation and frequency
+    over the residual stage's device time, per-launch CUDA events)."""
+    out = {}
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    for cfg, warm, steps, batch in ((3, 2, 2, 1), (4, 1, 1, 6)):
+        wl = workload.make(cfg)
+        n, nf, nrhs = wl.n, len(wl.omega), wl.B.shape[0]
+        s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + args.gemm_eff), batch=batch, profile=1,
+                      resid=getattr(zs, "ZSOLVE_RESID_" + args.resid), symmetric=args.symmetric)
+        try:
+            L = torch.from_numpy(wl.L).cuda()
+            P = torch.from_numpy(wl.Psi).cuda()
+            G = torch.from_numpy(wl.G).cuda()
+            b = torch.from_numpy(wl.B).cuda()
+            x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+            for _ in range(warm):
+                zs.zsolve_sweep(s.ctx, L, P, G, wl.omega, wl.zs, b, x)
+            torch.cuda.synchronize()
+            zs.zsolve_reset_profile(s.ctx)
+            st = torch.cuda.current_stream()
+            ms, infos = 0.0, None
+            for _ in range(steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                infos = zs.zsolve_sweep(s.ctx, L, P, G, wl.omega, wl.zs, b, x)
+                e1.record(st)
+                torch.cuda.synchronize()
+                ms += e0.elapsed_time(e1)
+            ms /= steps
+            prof = zs.zsolve_get_profile(s.ctx).as_dict()
+            fac_ms = sum(i.ms_factor for i in infos)
+            iters = [i.iters for i in infos]
+            res_ms = prof["residual"]["ms"] / steps
+            res_bytes = sum(iters) * (16.0 * n * n + 32.0 * n * nrhs)
+            out[f"config{cfg}"] = {
+                "workload": workload_name(cfg), "n": n, "nf": nf, "nrhs": nrhs, "batch": batch,
+                "warmup": warm, "steps": steps, "ms_per_sweep": ms, "points_per_s": nf / (ms / 1e3),
+                "lu_tflops": (8.0 * n ** 3 / 3.0 * nf) / (fac_ms / 1e3) / 1e12 if fac_ms > 0 else None,
+                "resid_gbs": res_bytes / (res_ms / 1e3) / 1e9 if res_ms > 0 else None,
+                "iters": iters, "fallbacks": sum(i.fallback for i in infos),
+                "stage_ms_per_sweep": {k: v["ms"] / steps for k, v in prof.items()}}
+            del L, P, G, b, x
+        finally:
+            s.close()
+            torch.cuda.empty_cache()
+    return out
+
+
 def run_reference(args):
     ws, rank, _ = dist_env()
     if rank != 0:
@@ -403,7 +469,7 @@ def run_ours(args):
     solver = zs.Solver(n, nrhs, gemm=gemm, batch=args.batch or nf, profile=0,
                        resid=getattr(zs, "ZSOLVE_RESID_" + args.resid), symmetric=args.symmetric)
     ctx = solver.ctx
-    resid_mode = "DF" if zs.zsolve_get_resid_mode(ctx) == zs.ZSOLVE_RESID_DF else "F64"
+    resid_mode = RESID_NAMES[zs.zsolve_get_resid_mode(ctx)]
     L = torch.from_numpy(wl.L).cuda()
     P = torch.from_numpy(wl.Psi).cuda()
     G = torch.from_numpy(wl.G).cuda()
@@ -418,6 +484,10 @@ def run_ours(args):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
+    # the arithmetic in use (AUTO: picked by its probe in the first warm-up
+    # sweep); the profiled pass and the variants keep it fixed
+    choice = zs.zsolve_get_gemm_choice(ctx)
+    args.gemm_eff = {zs.ZSOLVE_GEMM_TF32: "TF32", zs.ZSOLVE_GEMM_TF32X3: "TF32X3", zs.ZSOLVE_GEMM_FFMA: "FFMA"}[choice.chosen]
     zs.zsolve_reset_profile(ctx)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -497,7 +567,7 @@ def run_ours(args):
         return o
 
     rl = {}
-    tc = args.gemm != "FFMA"
+    tc = args.gemm_eff != "FFMA"
     tc_launches = st["schur"]["launches"] + (st["trsm"]["launches"] if tc else 0)
     tc_ms_tot = st["schur"]["ms"] + (st["trsm"]["ms"] if tc else 0.0)
     tc_flops_tot = (schur_f + (trsm_flops(n) * nf if tc else 0)) * steps
@@ -526,14 +596,15 @@ def run_ours(args):
     rl["k_trsv_inv"] = obj("k_trsv_inv", "hbm", st["trsv"]["ms"], st["trsv"]["launches"],
                            n_solves * 8.0 * n * n * math.ceil(nrhs / 4) * steps, hbm, "GB/s", f"{peak_src} copy",
                            "8 n^2 bytes of float32 factors per solve and frequency")
-    rl["k_residual"] = obj("k_residual" if resid_mode == "F64" else "k_residual_df", "hbm", st["residual"]["ms"],
+    rl["k_residual"] = obj({"F64": "k_residual", "DF": "k_residual_df", "FX": "k_residual_fx",
+                            "LPG": "k_residual_lpg"}[resid_mode], "hbm", st["residual"]["ms"],
                            st["residual"]["launches"], res_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
                            "16 n^2 + 32 n nrhs bytes per evaluation and frequency")
     lanes = 2 if nf >= 2 else 1
     rl["k_assemble"] = obj("k_assemble", "hbm", st["assemble"]["ms"], st["assemble"]["launches"],
                            (24.0 * n * n * lanes + 24.0 * n * n * nf) * steps, hbm, "GB/s", f"{peak_src} copy",
                            "24 n^2 bytes of L, Psi, G read once per lane + 24 n^2 written per frequency")
-    ktimes = kernel_times(stage_ms, args.gemm)
+    ktimes = kernel_times(stage_ms, args.gemm_eff)
     dom = dominant_kernel(ktimes, list(rl))
     tot_k = sum(ktimes.values())
     launches = sum(v["launches"] for v in launch_counts.values())
@@ -542,9 +613,11 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32 factor + " + ("f64" if resid_mode == "F64" else "double-float f32x2") + " residual",
+        "dtype": "f32 factor + " + {"F64": "f64", "DF": "double-float f32x2", "FX": "f64-accurate int fixed-point",
+                                    "LPG": "f64"}[resid_mode] + " residual",
         "data": "synthetic",
-        "config": {"workload": workload_name(args.config), "n": n, "nf": nf, "nrhs": nrhs, "gemm": args.gemm,
+        "config": {"workload": workload_name(args.config), "n": n, "nf": nf, "nrhs": nrhs,
+                   "gemm": args.gemm if args.gemm == args.gemm_eff else f"{args.gemm} -> {args.gemm_eff}",
                    "resid": resid_mode, "factor": "symmetric (lower tiles)" if args.symmetric else "full LU update",
                    "batch": args.batch or nf, "l2": "flushed between steps (512 MB write)",
                    "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
@@ -558,16 +631,19 @@ def run_ours(args):
                       f"({prof_ms_step:.3f} ms per step with the events); per-stage sums of per-launch device "
                       "times; the two lanes run side by side, so the stages add up to more than a step",
         "iters": iters, "fallbacks": sum(i.fallback for i in infos),
+        "gemm_choice": choice.as_dict(),
         "gpu_launches": int(launches),
         "e2e": {"value": ws * nf / e2e_s, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "clocks": clocks, "wall_s": wall,
     }
     solver.close()
-    other = "DF" if args.resid == "F64" else "F64"
     line["resid_variants"] = {
         args.resid: {"mode_in_use": resid_mode, "points_per_s": value / ws, "resid_gbs": res_gbs,
-                     "resid_hbm_frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None},
-        other: sweep_variant(zs, torch, wl, args, other)}
+                     "resid_hbm_frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None,
+                     "arith": RESID_ARITH[resid_mode]}}
+    for other in ("F64", "FX", "DF", "LPG"):
+        if other != args.resid:
+            line["resid_variants"][other] = sweep_variant(zs, torch, wl, args, other)
     # the other factorisation mode: full trailing update, or the symmetric one
     # (lower tiles only, U12 from A21; same float64 residual and stopping rule)
     osym = 1 - args.symmetric
@@ -576,6 +652,8 @@ def run_ours(args):
         ("symmetric" if osym else "full"): sweep_variant(zs, torch, wl, args, args.resid, symmetric=osym)}
     if args.afs:
         line["afs"] = afs_variant(zs, torch, args, flush)
+    if args.large and args.config == 1:
+        line["large"] = large_configs(zs, torch, args)
     if args.cpu_baseline and args.gpus <= 1 and ws == 1:
         line["cpu_baseline"] = cpu_baseline(args.config, budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
@@ -589,12 +667,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=1)
-    ap.add_argument("--gemm", default="TF32X3", choices=["TF32", "TF32X3", "FFMA"])
+    ap.add_argument("--gemm", default="AUTO", choices=["AUTO", "TF32", "TF32X3", "FFMA"])
     ap.add_argument("--batch", type=int, default=0)
-    ap.add_argument("--resid", default="F64", choices=["F64", "DF"])
+    ap.add_argument("--resid", default="F64", choices=["F64", "DF", "FX", "LPG"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-afs", dest="afs", action="store_false")
+    ap.add_argument("--no-large", dest="large", action="store_false",
+                    help="skip the N=8000 and N=16384 passes of the default line")
     ap.add_argument("--symmetric", type=int, default=1, choices=[0, 1],
                     help="1 (default): trailing update on the lower tiles only (Z is complex symmetric); 0: full")
     args = ap.parse_args()

@@ -58,7 +58,7 @@ extern "C" {
 #define ZSOLVE_ETIMEOUT (-7)   /* a bounded device-side wait gave up (dependency never satisfied) */
 
 /* arithmetic of the trailing (Schur) update of the low-precision factorisation */
-#define ZSOLVE_GEMM_AUTO 0   /* TF32X3 */
+#define ZSOLVE_GEMM_AUTO 0   /* picked per context by measured convergence and speed (zsolve_get_gemm_choice) */
 #define ZSOLVE_GEMM_TF32 1   /* one tf32 tensor-core product per term (tcgen05) */
 #define ZSOLVE_GEMM_TF32X3 2 /* split hi/lo tf32, three products per term (tcgen05) */
 #define ZSOLVE_GEMM_FFMA 3   /* FP32 fused multiply-add on the CUDA cores */
@@ -67,6 +67,13 @@ extern "C" {
 #define ZSOLVE_RESID_F64 0 /* float64 multiply-adds (DFMA); default */
 #define ZSOLVE_RESID_DF 1  /* double-float on the FP32 pipes, about 46 bits (the page's GPU residual);
                               checked against the float64 kernel when the context is created */
+#define ZSOLVE_RESID_FX 2  /* float64-accurate on the integer pipes: Z and x turned exactly into
+                              72-bit fixed point (three 24-bit limbs), products and sums exact in
+                              64-bit integers, each lane's sum rounded once to float64 */
+#define ZSOLVE_RESID_LPG 3 /* zsolve_sweep: r = b - (j w L x - j Psi x / w + Zs G x) in float64 from
+                              the sweep's L, Psi, G, several frequencies per pass over them, without
+                              the assembled float64 Z (zsolve_residual_lpg); calls on the single
+                              system of zsolve_assemble keep the float64 GEMV (F64) */
 
 typedef struct zsolve_ctx zsolve_ctx; /* opaque */
 
@@ -121,7 +128,27 @@ typedef struct {
     float ms_assemble; /* device time of the stages (batched: the batch's time / batch size) */
     float ms_factor;
     float ms_refine;
+    int gemm;          /* arithmetic of this frequency's factors: ZSOLVE_GEMM_TF32, _TF32X3 or _FFMA */
 } zsolve_info;
+
+/* The choice of ZSOLVE_GEMM_AUTO.  The first zsolve_sweep of a context
+ * created with gemm = AUTO solves its first frequency alone once in each
+ * arithmetic (assembly, factorisation and refinement, timed with CUDA events
+ * on the context's stream) and keeps, among the arithmetics whose refinement
+ * converged without the fallback, the fastest (TF32X3 if none converged).
+ * Until then, and for contexts with a fixed arithmetic, `chosen` is the
+ * arithmetic in use and the rest is zero.  Arrays are indexed by
+ * ZSOLVE_GEMM_TF32 - 1, ZSOLVE_GEMM_TF32X3 - 1, ZSOLVE_GEMM_FFMA - 1.
+ * Passage: section "Double-precision answers from a GPU without double
+ * precision" -- how low the factorisation's precision may go is set by
+ * whether the refinement still converges; the page factorises in float32. */
+typedef struct {
+    int done;        /* 1 once the probe has run */
+    int chosen;      /* ZSOLVE_GEMM_TF32, _TF32X3 or _FFMA: the arithmetic in use */
+    float ms[3];     /* probe: device time of assembly + factorisation + refinement */
+    int iters[3];    /* probe: corrections made */
+    int fallback[3]; /* probe: 1 if the refinement stalled (the float64 fallback solved it) */
+} zsolve_gemm_probe;
 
 /* Fill *opts with the defaults listed above. */
 int zsolve_default_opts(zsolve_opts *opts);
@@ -197,6 +224,16 @@ int zsolve_sweep_host(zsolve_ctx *ctx, const double *L, const double *Psi, const
 /* r = b - Z x with the float64 Z (step 3).  b, x, r: device c128, nrhs x n. */
 int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int nrhs);
 
+/* r = b - Z x for the single system of zsolve_assemble (its omega and Zs),
+ * computed from L, Psi, G (device, n x n float64, as passed to
+ * zsolve_assemble) without the assembled Z: r = b - (j w L x - j Psi x / w +
+ * Zs G x), three float64 products per entry (the residual mode
+ * ZSOLVE_RESID_LPG of the sweeps).  b, x, r: device c128, nrhs x n.
+ * Passage: step 3 (the residual in double precision) with the form of Z of
+ * section "Fewer frequency points: adaptive frequency sampling". */
+int zsolve_residual_lpg(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const void *b,
+                        const void *x, void *r, int nrhs);
+
 /* d = (L U)^-1 v with the low-precision factors (steps 2 and 4): v is
  * rounded to complex float32, solved in float32, and d returned as c128.
  * v, d: device c128, nrhs x n. */
@@ -215,6 +252,10 @@ int zsolve_selftest_wait(zsolve_ctx *ctx, int nrhs);
 /* x = Z^-1 b by the float64 LU with partial pivoting of the assembled Z (the
  * fallback on its own).  b, x: device c128, nrhs x n. */
 int zsolve_fallback_solve(zsolve_ctx *ctx, const void *b, void *x, int nrhs);
+
+/* The arithmetic of the factorisation in use and, for ZSOLVE_GEMM_AUTO, the
+ * measurements it was picked on (zsolve_gemm_probe). */
+int zsolve_get_gemm_choice(zsolve_ctx *ctx, zsolve_gemm_probe *out);
 
 /* Residual arithmetic in use (ZSOLVE_RESID_*) in *mode.  A context created
  * with ZSOLVE_RESID_DF first compares the double-float residual with the

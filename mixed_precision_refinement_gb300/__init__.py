@@ -36,6 +36,8 @@ ZSOLVE_GEMM_FFMA = 3
 
 ZSOLVE_RESID_F64 = 0
 ZSOLVE_RESID_DF = 1
+ZSOLVE_RESID_FX = 2
+ZSOLVE_RESID_LPG = 3
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zsolve.h")
 
@@ -60,10 +62,21 @@ class zsolve_profile(ctypes.Structure):
 class zsolve_info(ctypes.Structure):
     _fields_ = [("iters", ctypes.c_int), ("fallback", ctypes.c_int), ("status", ctypes.c_int),
                 ("pivot_flag", ctypes.c_int), ("relcorr", ctypes.c_double), ("ms_assemble", ctypes.c_float),
-                ("ms_factor", ctypes.c_float), ("ms_refine", ctypes.c_float)]
+                ("ms_factor", ctypes.c_float), ("ms_refine", ctypes.c_float), ("gemm", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class zsolve_gemm_probe(ctypes.Structure):
+    _fields_ = [("done", ctypes.c_int), ("chosen", ctypes.c_int), ("ms", ctypes.c_float * 3),
+                ("iters", ctypes.c_int * 3), ("fallback", ctypes.c_int * 3)]
+
+    def as_dict(self):
+        names = ("TF32", "TF32X3", "FFMA")
+        return {"done": self.done, "chosen": {1: "TF32", 2: "TF32X3", 3: "FFMA"}.get(self.chosen, self.chosen),
+                "probe": {nm: {"ms": float(self.ms[k]), "iters": int(self.iters[k]),
+                               "fallback": int(self.fallback[k])} for k, nm in enumerate(names)}}
 
 
 class zsolve_afs_opts(ctypes.Structure):
@@ -105,6 +118,7 @@ def _load():
         "zsolve_sweep": (I, [P, P, P, P, P, P, I, P, P, I, ctypes.POINTER(zsolve_info)]),
         "zsolve_sweep_host": (I, [P, P, P, P, P, P, I, P, P, I, ctypes.POINTER(zsolve_info)]),
         "zsolve_residual": (I, [P, P, P, P, I]),
+        "zsolve_residual_lpg": (I, [P, P, P, P, P, P, P, I]),
         "zsolve_lowprec_solve": (I, [P, P, P, I]),
         "zsolve_fallback_solve": (I, [P, P, P, I]),
         "zsolve_selftest_wait": (I, [P, I]),
@@ -114,6 +128,7 @@ def _load():
         "zsolve_lowprec_solve_noalloc": (I, [P, I64, I64, I64, I64, I, P, I64, I, P]),
         "zsolve_get_profile": (I, [P, ctypes.POINTER(zsolve_profile)]),
         "zsolve_get_resid_mode": (I, [P, ctypes.POINTER(I)]),
+        "zsolve_get_gemm_choice": (I, [P, ctypes.POINTER(zsolve_gemm_probe)]),
         "zsolve_reset_profile": (I, [P]),
         "zsolve_strerror": (ctypes.c_char_p, [I]),
         "zsolve_last_error": (ctypes.c_char_p, [P]),
@@ -264,6 +279,15 @@ def zsolve_residual(ctx, b, x, r) -> None:
     _check(ctx, _lib.zsolve_residual(ctx, _ptr(b), _ptr(x), _ptr(r), nrhs))
 
 
+def zsolve_residual_lpg(ctx, L, Psi, G, b, x, r) -> None:
+    for t in (L, Psi, G):
+        _require(t, "f64", True)
+    for t in (b, x, r):
+        _require(t, "c128", True)
+    nrhs = b.shape[0] if b.dim() == 2 else 1
+    _check(ctx, _lib.zsolve_residual_lpg(ctx, _ptr(L), _ptr(Psi), _ptr(G), _ptr(b), _ptr(x), _ptr(r), nrhs))
+
+
 def zsolve_lowprec_solve(ctx, v, d) -> None:
     _require(v, "c128", True)
     _require(d, "c128", True)
@@ -314,6 +338,12 @@ def zsolve_lowprec_solve_noalloc(z32, ld: int, plane: int, sys_stride: int, n: i
 def zsolve_get_profile(ctx) -> zsolve_profile:
     p = zsolve_profile()
     _check(ctx, _lib.zsolve_get_profile(ctx, ctypes.byref(p)))
+    return p
+
+
+def zsolve_get_gemm_choice(ctx) -> zsolve_gemm_probe:
+    p = zsolve_gemm_probe()
+    _check(ctx, _lib.zsolve_get_gemm_choice(ctx, ctypes.byref(p)))
     return p
 
 

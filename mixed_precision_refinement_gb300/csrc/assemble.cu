@@ -35,6 +35,10 @@
 //    -0 and 1 arrive as kernel arguments so that the compiler cannot fold
 //    the fma back into a plain multiply or add.
 //
+// When asked (zexp != NULL), the kernel also records for every row and
+// frequency the largest biased exponent of the row's float64 entries (real
+// and imaginary parts): the scale of the fixed-point residual (resid_fx.cu).
+//
 // Bound: FP64 pipe (then HBM).  Algorithmic bytes per launch = 24 n^2 (read)
 // + 24 n^2 per frequency (16 written as float64 complex, 8 as float32 complex).
 #include "common.cuh"
@@ -74,9 +78,9 @@ struct Fp64Ops {
 // otherwise the whole warp multiplies, which gives the same result for the
 // entries whose G is zero.  A per-entry choice would be if-converted and the
 // FP64 pipe would issue the products for every warp with most lanes off.
-__device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, double p, double g, bool warp_gzero,
-                                          bool valid, double2 *__restrict__ z64e, float *__restrict__ z32e,
-                                          int64_t plane, const Fp64Ops &op) {
+__device__ __forceinline__ int one_entry(const ZsSlotParam &sp, double l, double p, double g, bool warp_gzero,
+                                         bool valid, double2 *__restrict__ z64e, float *__restrict__ z32e,
+                                         int64_t plane, const Fp64Ops &op) {
     const double w = sp.omega, r = sp.pad;  // pad holds RN(1/omega)
     const double q0 = op.mul(p, r);
     // RN(p / w); a zero first quotient is already exact (and keeps its sign)
@@ -101,17 +105,29 @@ __device__ __forceinline__ void one_entry(const ZsSlotParam &sp, double l, doubl
         __stcs(z32e, d2f_rn(re));
         __stcs(z32e + plane, d2f_rn(im));
     }
+    // the larger biased exponent of the two parts (0 for an entry not stored)
+    const int er = (int)((zs::bits_of(re).hi >> 20) & 0x7FFu), ei = (int)((zs::bits_of(im).hi >> 20) & 0x7FFu);
+    return valid ? max(er, ei) : 0;
+}
+
+// per-slot exponent maxima of the current row: the warp's maximum, then one
+// shared-memory atomic per warp
+__device__ __forceinline__ void row_max(int *s_exp, int s, int e, int lane) {
+    const int m = __reduce_max_sync(0xffffffffu, e);
+    if (lane == 0) atomicMax(s_exp + s, m);
 }
 
 __global__ void __launch_bounds__(kThreads)
 k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const double *__restrict__ G, int64_t n,
            int64_t r0, int64_t r1, const ZsSlotParam *__restrict__ params, int nslot, double2 *__restrict__ z64,
-           int64_t z64_stride, float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, double mz,
-           double one) {
+           int64_t z64_stride, float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride,
+           int *__restrict__ zexp, double mz, double one) {
     __shared__ ZsSlotParam sp[kMaxSlots];
+    __shared__ int s_exp[kMaxSlots];
     const Fp64Ops op{mz, one};
     const int lane = threadIdx.x & 31;
     for (int s = threadIdx.x; s < nslot; s += blockDim.x) sp[s] = params[s];
+    for (int s = threadIdx.x; s < kMaxSlots; s += blockDim.x) s_exp[s] = 0;
     __syncthreads();
     for (int64_t i = r0 + blockIdx.x; i < r1; i += gridDim.x) {
         const int64_t row = i * n, row32 = i * ld;
@@ -134,19 +150,34 @@ k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const d
             for (; s + 4 <= nslot; s += 4) {
                 double2 *zp1 = zp + z64_stride, *zp2 = zp1 + z64_stride, *zp3 = zp2 + z64_stride;
                 float *zq1 = zq + z32_stride, *zq2 = zq1 + z32_stride, *zq3 = zq2 + z32_stride;
-                one_entry(sp[s], l, p, g, warp_gzero, valid, zp, zq, plane, op);
-                one_entry(sp[s + 1], l, p, g, warp_gzero, valid, zp1, zq1, plane, op);
-                one_entry(sp[s + 2], l, p, g, warp_gzero, valid, zp2, zq2, plane, op);
-                one_entry(sp[s + 3], l, p, g, warp_gzero, valid, zp3, zq3, plane, op);
+                const int e0 = one_entry(sp[s], l, p, g, warp_gzero, valid, zp, zq, plane, op);
+                const int e1 = one_entry(sp[s + 1], l, p, g, warp_gzero, valid, zp1, zq1, plane, op);
+                const int e2 = one_entry(sp[s + 2], l, p, g, warp_gzero, valid, zp2, zq2, plane, op);
+                const int e3 = one_entry(sp[s + 3], l, p, g, warp_gzero, valid, zp3, zq3, plane, op);
+                if (zexp) {
+                    row_max(s_exp, s, e0, lane);
+                    row_max(s_exp, s + 1, e1, lane);
+                    row_max(s_exp, s + 2, e2, lane);
+                    row_max(s_exp, s + 3, e3, lane);
+                }
                 zp = zp3 + z64_stride;
                 zq = zq3 + z32_stride;
             }
 #pragma unroll 1
             for (; s < nslot; s++) {
-                one_entry(sp[s], l, p, g, warp_gzero, valid, zp, zq, plane, op);
+                const int e = one_entry(sp[s], l, p, g, warp_gzero, valid, zp, zq, plane, op);
+                if (zexp) row_max(s_exp, s, e, lane);
                 zp += z64_stride;
                 zq += z32_stride;
             }
+        }
+        if (zexp) {  // the row's maxima out, and reset for the next row
+            __syncthreads();
+            for (int s = threadIdx.x; s < nslot; s += blockDim.x) {
+                zexp[(int64_t)s * n + i] = s_exp[s];
+                s_exp[s] = 0;
+            }
+            __syncthreads();
         }
     }
 }
@@ -156,7 +187,7 @@ k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const d
 cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0, int64_t r1,
                                const ZsSlotParam *params, int nslot, double2 *z64, int64_t z64_stride,
                                float *z32, int64_t ld, int64_t plane, int64_t z32_stride,
-                               cudaStream_t st) {
+                               cudaStream_t st, int *zexp) {
     if (nslot > kMaxSlots || r0 < 0 || r1 > n || r0 > r1) return cudaErrorInvalidValue;
     if (r0 == r1) return cudaSuccess;
     int dev = 0, sms = 148;
@@ -167,6 +198,6 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     k_assemble<<<(unsigned)blocks, kThreads, 0, st>>>(L, Psi, G, n, r0, r1, params, nslot, z64, z64_stride,
-                                                      z32, ld, plane, z32_stride, -0.0, 1.0);
+                                                      z32, ld, plane, z32_stride, zexp, -0.0, 1.0);
     return cudaGetLastError();
 }

@@ -144,11 +144,12 @@ int zs_ctx_nrhs_max(const zsolve_ctx *ctx);
 // strided by the given slot strides (elements).
 
 // Z64 (c128, ld n) and the complex float32 planes (re at z32, im at z32 + plane),
-// rows r0 .. r1-1.
+// rows r0 .. r1-1.  zexp (NULL: not recorded): per slot n ints, the largest
+// biased exponent of each row of the slot's Z64.
 cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0, int64_t r1,
                                const ZsSlotParam *params, int nslot, double2 *z64, int64_t z64_stride,
                                float *z32, int64_t ld, int64_t plane, int64_t z32_stride,
-                               cudaStream_t st);
+                               cudaStream_t st, int *zexp = nullptr);
 
 // Factorisation steps at outer-block column J for nslot slots listed in slots[].
 // inv32: per slot and outer block, ZS_INV32_STRIDE floats:
@@ -265,6 +266,29 @@ cudaError_t zs_launch_residual_df(const double2 *z64, int64_t z64_stride, int64_
                                   double2 *out_c128, int64_t out128_stride, const int *slots, int nslot,
                                   cudaStream_t st);
 cudaError_t zs_launch_selftest_fill(double2 *z, double2 *x, int64_t n, int zero_re, cudaStream_t st);
+
+// r = b - (j w L x - j Psi x / w + Zs G x) from L, Psi, G (n x n float64) for
+// every listed slot (params indexed by slot), groups of frequencies per pass
+// over a row (resid_lpg.cu).  Output as zs_launch_residual.
+cudaError_t zs_launch_residual_lpg(const double *L, const double *Psi, const double *G, int64_t n,
+                                   const ZsSlotParam *params, const double2 *b, const double2 *x, int64_t x_stride,
+                                   int nrhs, float2 *out_c64, int64_t out64_stride, double2 *out_c128,
+                                   int64_t out128_stride, const int *slots, int nslot, cudaStream_t st);
+
+// Fixed-point residual (resid_fx.cu): x split into exact 24-bit limbs per
+// right-hand side (xl: per slot xl_stride bytes, zs_fx_x_bytes(n) per right-hand side; xe: per
+// (slot, rhs) the scale exponent, index slot * nrhs_max + r), then r = b - Z64 x
+// with exact integer products and sums.  zexp: per slot n ints, the largest
+// biased exponent of each row of Z64 (written by zs_launch_assemble).
+int64_t zs_fx_x_bytes(int64_t n);  // bytes of one right-hand side's limbs
+cudaError_t zs_launch_split_fx(const double2 *x, int64_t x_stride, int64_t n, int nrhs, unsigned char *xl,
+                               int64_t xl_stride, int *xe, int nrhs_max, const int *slots, int nslot, cudaStream_t st);
+// ndf (0..3): of every four 32-column sub-steps, how many take float64 products (DFMA) instead.
+cudaError_t zs_launch_residual_fx(const double2 *z64, int64_t z64_stride, const int *zexp, int64_t n, const double2 *b,
+                                  const double2 *x, int64_t x_stride, const unsigned char *xl, int64_t xl_stride,
+                                  const int *xe, int nrhs_max, int nrhs, float2 *out_c64, int64_t out64_stride,
+                                  double2 *out_c128, int64_t out128_stride, const int *slots, int nslot, int ndf,
+                                  cudaStream_t st);
 
 // v = (float2) b for every listed slot
 cudaError_t zs_launch_cast_rhs(const double2 *b, int64_t n, int nrhs, float2 *v, int64_t v_stride,

@@ -24,6 +24,7 @@
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -43,6 +44,10 @@ struct zsolve_ctx {
     zsolve_opts opts{};
     int device = 0, num_sms = 0;
     unsigned wait_limit = ZS_SPIN_LIMIT;  // polls before a triangular-solve wait gives up
+    // arithmetic of the factorisation in use: 0 FFMA, 1 TF32, 2 TF32X3 (opts.gemm,
+    // or for ZSOLVE_GEMM_AUTO the probe's choice, TF32X3 until the probe ran)
+    int gemm_eff = 2;
+    zsolve_gemm_probe probe{};
     cudaStream_t stream = nullptr;
     int S = 1;  // frequencies held at once
     int64_t ld = 0, plane = 0, z32_stride = 0, z64_stride = 0, pack_stride = 0, v_stride = 0;
@@ -59,6 +64,13 @@ struct zsolve_ctx {
     alignas(64) unsigned char z32_map[128] = {};     // TMA tensor map over the float32 matrices
     float2 *v = nullptr;
     float4 *xs = nullptr;  // double-float split of x (residual mode DF)
+    // the sweep's L, Psi, G while a sweep runs (residual mode LPG), else null
+    const double *cur_L = nullptr, *cur_Psi = nullptr, *cur_G = nullptr;
+    ZsSlotParam single{};  // frequency of the last zsolve_assemble
+    unsigned char *xl = nullptr;  // fixed-point limbs of x (residual mode FX)
+    int *xe = nullptr;     // their scale exponents, per (slot, rhs)
+    int *zexp = nullptr;   // residual mode FX: per slot and row of Z64, its largest exponent
+    int fx_ndf = 1;        // residual mode FX: sub-steps of four taken in float64 (ZSOLVE_FX_NDF)
     int resid_mode = ZSOLVE_RESID_F64;
     double *partials = nullptr;
     int nchunks = 0;
@@ -215,6 +227,10 @@ int gemm_mode(const zsolve_opts &o) {
     }
 }
 
+// ZSOLVE_GEMM_* of an internal mode and back
+int gemm_public(int mode) { return mode == 0 ? ZSOLVE_GEMM_FFMA : mode == 1 ? ZSOLVE_GEMM_TF32 : ZSOLVE_GEMM_TF32X3; }
+int gemm_internal(int pub) { return pub == ZSOLVE_GEMM_FFMA ? 0 : pub == ZSOLVE_GEMM_TF32 ? 1 : 2; }
+
 size_t slot_bytes(int64_t n, int64_t ld) {
     return (size_t)n * n * sizeof(double2) + (size_t)2 * n * ld * sizeof(float) +
            (size_t)6 * zs_pack_plane(n) * sizeof(float) + (size_t)zs_dinv_stride(n) * sizeof(float) +
@@ -262,7 +278,7 @@ constexpr int kMaxCtr = 256;  // tile counters per factorisation (2 per outer bl
 
 int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     const int64_t n = ctx->n;
-    const int mode = gemm_mode(ctx->opts), split = mode == 2 ? 1 : 0;
+    const int mode = ctx->gemm_eff, split = mode == 2 ? 1 : 0;
     const int64_t inv32_stride = zs_inv32_slot_stride(n);
     if (2 * ((n + ZS_NB - 1) / ZS_NB) > kMaxCtr) return fail(ctx, ZSOLVE_EINVAL, "n too large for the tile counters");
     ZS_CU(cudaMemsetAsync(ln.tile_ctr, 0, kMaxCtr * sizeof(unsigned), ln.stream));
@@ -306,7 +322,7 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
 // with the rest following it (the lane's range)
 int factor_slots(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot, int first) {
     ZS_CU(cudaMemsetAsync(ctx->d_pivflag + first, 0, sizeof(int) * nslot, ln.stream));
-    return gemm_mode(ctx->opts) == 0 ? factor_slots_simt(ctx, ln, slots, nslot) : factor_slots_tc(ctx, ln, slots, nslot);
+    return ctx->gemm_eff == 0 ? factor_slots_simt(ctx, ln, slots, nslot) : factor_slots_tc(ctx, ln, slots, nslot);
 }
 
 // ------------------------------------------------------------------ solves
@@ -389,7 +405,21 @@ int residual_slots(zsolve_ctx *ctx, Lane &ln, const double2 *b, const double2 *x
                    float2 *o64, int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot,
                    StageSpan *sp) {
     const int64_t n = ctx->n;
-    if (ctx->resid_mode == ZSOLVE_RESID_DF) {
+    if (ctx->resid_mode == ZSOLVE_RESID_LPG && ctx->cur_L) {
+        ZS_CU(zs_launch_residual_lpg(ctx->cur_L, ctx->cur_Psi, ctx->cur_G, n, ctx->d_params, b, x, x_stride, nrhs, o64,
+                                     o64s, o128, o128s, slots, nslot, ln.stream));
+        sp->done(nrhs);
+    } else if (ctx->resid_mode == ZSOLVE_RESID_FX) {
+        const int64_t xl_stride = (int64_t)ctx->nrhs_max * zs_fx_x_bytes(n);
+        ZS_CU(zs_launch_split_fx(x, x_stride, n, nrhs, ctx->xl, xl_stride, ctx->xe, ctx->nrhs_max, slots, nslot,
+                                 ln.stream));
+        ZS_CU(zs_launch_residual_fx(ctx->z64, ctx->z64_stride, ctx->zexp, n, b, x, x_stride, ctx->xl, xl_stride,
+                                    ctx->xe, ctx->nrhs_max, nrhs, o64, o64s, o128, o128s, slots, nslot, ctx->fx_ndf,
+                                    ln.stream));
+        int chunks = 0;
+        for (int r = nrhs; r > 0; chunks++) r -= r >= 4 ? 4 : r >= 2 ? 2 : 1;
+        sp->done(1 + chunks);
+    } else if (ctx->resid_mode == ZSOLVE_RESID_DF) {
         const int64_t xs_stride = (int64_t)ctx->nrhs_max * n;
         ZS_CU(zs_launch_split_x(x, x_stride, n, nrhs, ctx->xs, xs_stride, slots, nslot, ln.stream));
         ZS_CU(zs_launch_residual_df(ctx->z64, ctx->z64_stride, n, b, ctx->xs, xs_stride, nrhs, o64, o64s, o128, o128s,
@@ -564,6 +594,7 @@ int refine_batch(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *x, int64_
             info[i].relcorr = last[i];
             info[i].fallback = 0;
             info[i].status = ZSOLVE_OK;
+            info[i].gemm = gemm_public(ctx->gemm_eff);
         }
     for (int s : stalled) {
         const int i = s - first;
@@ -600,7 +631,7 @@ int assemble_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi,
         ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, r0, r1, ctx->d_params + first, count,
                                  ctx->z64 + (int64_t)first * ctx->z64_stride, ctx->z64_stride,
                                  ctx->z32 + (int64_t)first * ctx->z32_stride, ctx->ld, ctx->plane, ctx->z32_stride,
-                                 ln.stream));
+                                 ln.stream, ctx->zexp ? ctx->zexp + (int64_t)first * ctx->n : nullptr));
     }
     sp.done(nb);
     ctx->nband = 0;  // the first assembly of a sweep waited for every band
@@ -648,12 +679,65 @@ int refine_lanes(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *xb, int n
     return st;
 }
 
+// ZSOLVE_GEMM_AUTO: the arithmetic of the factorisation picked by measured
+// convergence and speed.  Frequency `f` of the first sweep is solved alone
+// (assembly, factorisation, refinement) once in each arithmetic -- TF32,
+// TF32X3, FFMA -- on lane 0, with its device time (CUDA events) and its
+// correction count recorded; the context then keeps, among the arithmetics
+// whose refinement converged without the fallback, the one with the smallest
+// time (TF32X3 if none did).  x receives the probe solutions (overwritten by
+// the sweep afterwards).
+int auto_probe(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, double omega, double zre,
+               double zim, const double2 *b, double2 *x, int nrhs) {
+    Lane &ln = ctx->lane[0];
+    ctx->h_params[0] = ZsSlotParam{omega, zre, zim, 1.0 / omega};
+    ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ln.stream));
+    zsolve_gemm_probe pr{};
+    for (int k = 0; k < 3; k++) {  // index k = ZSOLVE_GEMM_TF32 - 1, TF32X3 - 1, FFMA - 1
+        ctx->gemm_eff = gemm_internal(k + 1);
+        ln.tc_grid = ctx->num_sms;
+        ln.trsv_grid = 0;
+        ZS_TRY(factor_lane(ctx, ln, L, Psi, G, 0, 1, false));  // records ln.ev[0] first
+        zsolve_info inf{};
+        const int st = refine_batch(ctx, ln, b, x, 0, nrhs, 0, 1, &inf);
+        if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
+        ZS_CU(cudaEventRecord(ln.ev[4], ln.stream));
+        ZS_CU(cudaEventSynchronize(ln.ev[4]));
+        float ms = 0.f;
+        ZS_CU(cudaEventElapsedTime(&ms, ln.ev[0], ln.ev[4]));
+        pr.ms[k] = ms;
+        pr.iters[k] = inf.iters;
+        pr.fallback[k] = inf.fallback || st != ZSOLVE_OK;
+    }
+    int best = -1;
+    for (int k = 0; k < 3; k++)
+        if (!pr.fallback[k] && (best < 0 || pr.ms[k] < pr.ms[best])) best = k;
+    pr.done = 1;
+    pr.chosen = best < 0 ? ZSOLVE_GEMM_TF32X3 : best + 1;
+    ctx->probe = pr;
+    ctx->gemm_eff = gemm_internal(pr.chosen);
+    return ZSOLVE_OK;
+}
+
 int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const double *omega,
                const double *zs, int nf, const double2 *b, double2 *x, int nrhs, zsolve_info *info) {
     const int64_t n = ctx->n;
     for (int f = 0; f < nf; f++)
         if (!(omega[f] > 0.0) || !isfinite(omega[f]) || !isfinite(zs[2 * f]) || !isfinite(zs[2 * f + 1]))
             return fail(ctx, ZSOLVE_EINVAL, "frequency %d: omega must be positive and finite, Zs finite", f);
+    ctx->cur_L = L;
+    ctx->cur_Psi = Psi;
+    ctx->cur_G = G;
+    struct Clear {  // the pointers are borrowed for this call only
+        zsolve_ctx *c;
+        ~Clear() { c->cur_L = c->cur_Psi = c->cur_G = nullptr; }
+    } clear_ptrs{ctx};
+    if (ctx->opts.gemm == ZSOLVE_GEMM_AUTO && !ctx->probe.done && nf > 0) {
+        // the host-pointer sweep's inputs may still be in flight: the probe's
+        // assembly waits for every band, the sweep's first one then runs plain
+        ZS_TRY(auto_probe(ctx, L, Psi, G, omega[0], zs[0], zs[1], b, x, nrhs));
+        ctx->nband = 0;
+    }
     Lane &l0 = ctx->lane[0], &l1 = ctx->lane[1];
     int first_err = ZSOLVE_OK;
     for (int f0 = 0; f0 < nf; f0 += ctx->S) {
@@ -749,6 +833,9 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->winv);
     cudaFree(c->v);
     cudaFree(c->xs);
+    cudaFree(c->xl);
+    cudaFree(c->xe);
+    cudaFree(c->zexp);
     cudaFree(c->partials);
     cudaFree(c->d_relcorr);
     cudaFreeHost(c->h_relcorr);
@@ -829,14 +916,17 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (ctx->opts.outer_block == 0) ctx->opts.outer_block = ZS_NB;
     if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
         ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0 || ctx->opts.resid < 0 ||
-        ctx->opts.resid > ZSOLVE_RESID_DF || ctx->opts.lanes < 0 || ctx->opts.lanes > 2 || ctx->opts.symmetric < 0 ||
+        ctx->opts.resid > ZSOLVE_RESID_LPG || ctx->opts.lanes < 0 || ctx->opts.lanes > 2 || ctx->opts.symmetric < 0 ||
         ctx->opts.symmetric > 1 || ctx->opts.wait_limit < 0) {
         delete ctx;
         return ZSOLVE_EINVAL;
     }
     ctx->n = n;
     ctx->nrhs_max = nrhs_max;
+    ctx->gemm_eff = gemm_mode(ctx->opts);
+    ctx->probe.chosen = ctx->opts.gemm == ZSOLVE_GEMM_AUTO ? ZSOLVE_GEMM_TF32X3 : ctx->opts.gemm;
     if (ctx->opts.wait_limit > 0) ctx->wait_limit = (unsigned)ctx->opts.wait_limit;
+    if (const char *e = getenv("ZSOLVE_FX_NDF")) ctx->fx_ndf = std::min(3, std::max(0, atoi(e)));
     auto bail = [&](int code) {
         free_all(ctx);
         delete ctx;
@@ -869,8 +959,10 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->z32, (size_t)S * ctx->z32_stride * sizeof(float));
     ALLOC(ctx->pack, (size_t)S * ctx->pack_stride * sizeof(float));
     ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
-    if (gemm_mode(ctx->opts) == 0) ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
-    if (gemm_mode(ctx->opts) != 0) ALLOC(ctx->winv, (size_t)S * ZS_WINV_STRIDE * sizeof(float));
+    // AUTO may pick any arithmetic: it holds the workspaces of both kinds
+    const bool is_auto = ctx->opts.gemm == ZSOLVE_GEMM_AUTO;
+    if (is_auto || gemm_mode(ctx->opts) == 0) ALLOC(ctx->inv32, (size_t)S * zs_inv32_slot_stride(n) * sizeof(float));
+    if (is_auto || gemm_mode(ctx->opts) != 0) ALLOC(ctx->winv, (size_t)S * ZS_WINV_STRIDE * sizeof(float));
     ALLOC(ctx->v, (size_t)S * ctx->v_stride * sizeof(float2));
     ALLOC(ctx->partials, (size_t)S * nrhs_max * ctx->nchunks * 2 * sizeof(double));
     ALLOC(ctx->d_relcorr, (size_t)S * nrhs_max * sizeof(double));
@@ -908,7 +1000,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ctx->lane[1].own_stream = true;
     ctx->lane[0].stream = ctx->stream;
     ctx->lane[0].tc_grid = ctx->lane[1].tc_grid = ctx->num_sms;
-    if (gemm_mode(ctx->opts) != 0 &&
+    if (ctx->winv &&
         (zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 128, ctx->pack_map) != cudaSuccess ||
          zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 32, ctx->packst_map) != cudaSuccess ||
          zs_tc_winv_map(ctx->winv, S, ctx->winv_map) != cudaSuccess ||
@@ -925,6 +1017,14 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
         cudaMemset(ctx->dinv, 0, (size_t)S * ctx->dinv_stride * sizeof(float)) != cudaSuccess ||
         (ctx->winv && cudaMemset(ctx->winv, 0, (size_t)S * ZS_WINV_STRIDE * sizeof(float)) != cudaSuccess))
         return bail(ZSOLVE_ECUDA);
+    ctx->resid_mode = (ctx->opts.resid == ZSOLVE_RESID_FX || ctx->opts.resid == ZSOLVE_RESID_LPG) ? ctx->opts.resid
+                                                                                                  : ZSOLVE_RESID_F64;
+    if (ctx->opts.resid == ZSOLVE_RESID_FX) {
+        if (cudaMalloc(&ctx->xl, (size_t)S * nrhs_max * zs_fx_x_bytes(n)) != cudaSuccess ||
+            cudaMalloc(&ctx->xe, (size_t)S * nrhs_max * sizeof(int)) != cudaSuccess ||
+            cudaMalloc(&ctx->zexp, (size_t)S * n * sizeof(int)) != cudaSuccess)
+            return bail(ZSOLVE_ENOMEM);
+    }
     if (ctx->opts.resid == ZSOLVE_RESID_DF) {
         if (cudaMalloc(&ctx->xs, (size_t)S * nrhs_max * n * sizeof(float4)) != cudaSuccess) return bail(ZSOLVE_ENOMEM);
         if (resid_selftest(ctx) != ZSOLVE_OK) return bail(ZSOLVE_ECUDA);
@@ -946,10 +1046,11 @@ int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const d
     if (!(omega > 0.0) || !isfinite(omega) || !isfinite(zs_re) || !isfinite(zs_im))
         return fail(ctx, ZSOLVE_EINVAL, "omega must be positive and finite, Zs finite");
     ctx->h_params[0] = ZsSlotParam{omega, zs_re, zs_im, 1.0 / omega};
+    ctx->single = ctx->h_params[0];
     ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
     StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE, ctx->stream);
     ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, 0, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32,
-                             ctx->ld, ctx->plane, ctx->z32_stride, ctx->stream));
+                             ctx->ld, ctx->plane, ctx->z32_stride, ctx->stream, ctx->zexp));
     sp.done(1);
     ctx->assembled = 1;
     ctx->factored = 0;
@@ -1058,6 +1159,21 @@ int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int 
     return ZSOLVE_OK;
 }
 
+int zsolve_residual_lpg(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const void *b,
+                        const void *x, void *r, int nrhs) {
+    if (!ctx || !L || !Psi || !G || !b || !x || !r) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_residual_lpg before zsolve_assemble");
+    ctx->h_params[0] = ctx->single;  // slot 0 holds the single system's frequency again
+    ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
+    StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL, ctx->stream);
+    ZS_CU(zs_launch_residual_lpg(L, Psi, G, ctx->n, ctx->d_params, (const double2 *)b, (const double2 *)x, 0, nrhs,
+                                 nullptr, 0, (double2 *)r, 0, ctx->d_all, 1, ctx->stream));
+    sp.done(nrhs);
+    ZS_CU(cudaStreamSynchronize(ctx->stream));
+    return ZSOLVE_OK;
+}
+
 int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs) {
     if (!ctx || !v || !d) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
     ZS_TRY(check_nrhs(ctx, nrhs));
@@ -1137,6 +1253,13 @@ int zsolve_reset_profile(zsolve_ctx *ctx) {
         ctx->prof_launches[i] = 0;
         ctx->prof_ms[i] = 0.0;
     }
+    return ZSOLVE_OK;
+}
+
+int zsolve_get_gemm_choice(zsolve_ctx *ctx, zsolve_gemm_probe *out) {
+    if (!ctx || !out) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    *out = ctx->probe;
+    out->chosen = gemm_public(ctx->gemm_eff);
     return ZSOLVE_OK;
 }
 

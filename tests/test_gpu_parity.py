@@ -150,11 +150,12 @@ def test_assemble_term_isolation(zs, torch):
 # ---------------------------------------------------------------- stages
 
 
-@pytest.mark.parametrize("n,nrhs", [(1, 1), (64, 2), (237, 1), (257, 3), (300, 8), (2157, 1)])
-def test_residual_against_oracle(zs, torch, n, nrhs):
+@pytest.mark.parametrize("resid", ["F64", "FX"])
+@pytest.mark.parametrize("n,nrhs", [(1, 1), (64, 2), (237, 1), (257, 3), (300, 8), (2157, 1), (1000, 7)])
+def test_residual_against_oracle(zs, torch, n, nrhs, resid):
     wl = workload.make_small(n, seed=10 + n, nf=1, nrhs=nrhs)
     X = workload.random_rhs(n, nrhs, seed=3)
-    s = zs.Solver(n, nrhs)
+    s = zs.Solver(n, nrhs, resid=getattr(zs, "ZSOLVE_RESID_" + resid))
     try:
         zs.zsolve_assemble(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega[0],
                            wl.zs[0].real, wl.zs[0].imag)
@@ -166,6 +167,95 @@ def test_residual_against_oracle(zs, torch, n, nrhs):
         # different summation order: bounded by a few ulps of sum |z||x| per row
         scale = np.abs(X) @ np.abs(Z).T + np.abs(wl.B)
         assert np.all(np.abs(r.cpu().numpy() - ref) <= 4 * n * 2.3e-16 * scale + 1e-300)
+    finally:
+        s.close()
+
+
+def _fx_case(kind, n, nrhs):
+    """Inputs that stress the fixed-point residual: its per-lane scale, its
+    real-part path, zeros, and x spread over many binades."""
+    wl = workload.make_small(n, seed=600 + n, nf=1, nrhs=nrhs)
+    L, Psi, G = wl.L, wl.Psi, wl.G
+    X = workload.random_rhs(n, nrhs, seed=5)
+    rng = np.random.default_rng(n)
+    if kind == "dense_g":      # Re Z dense: every step takes the real-part products
+        G = workload.random_symmetric_real(n, seed=n, scale=0.5)
+    elif kind == "x_spread":   # x entries from 1e-30 to 1e30 (and exact zeros)
+        X = X * 10.0 ** rng.uniform(-30, 30, size=X.shape)
+        X[:, ::7] = 0.0
+    elif kind == "z_spread":   # Z entries over 60 binades, some exactly zero
+        f = 2.0 ** rng.integers(-30, 30, size=n)
+        L = L * np.outer(f, f)
+        Psi = np.zeros_like(Psi)
+        L[3, :] = 0.0
+        L[:, 3] = 0.0
+        L[3, 3] = 1.0
+    elif kind == "x_zero":     # one right-hand side exactly zero: r = b
+        X[0] = 0.0
+    return workload.Workload(wl.points, L, Psi, G, wl.freqs, wl.omega, wl.zs, wl.B, None), X
+
+
+@pytest.mark.parametrize("kind", ["dense_g", "x_spread", "z_spread", "x_zero"])
+@pytest.mark.parametrize("n,nrhs", [(33, 1), (300, 2), (1000, 4)])
+def test_residual_fx_edge_cases(zs, torch, kind, n, nrhs):
+    wl, X = _fx_case(kind, n, nrhs)
+    s = zs.Solver(n, nrhs, resid=zs.ZSOLVE_RESID_FX)
+    try:
+        zs.zsolve_assemble(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega[0],
+                           wl.zs[0].real, wl.zs[0].imag)
+        b, x = dev(torch, wl.B), dev(torch, X)
+        r = torch.empty_like(b)
+        zs.zsolve_residual(s.ctx, b, x, r)
+        Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0])
+        ref = oracle.residual(Z, X, wl.B)
+        R = r.cpu().numpy()
+        # the float64 GEMV's own bound, row by row
+        scale = np.abs(X) @ np.abs(Z).T + np.abs(wl.B)
+        assert np.all(np.abs(R - ref) <= 4 * n * 2.3e-16 * scale + 1e-300)
+        if kind == "x_zero":
+            assert np.array_equal(R[0], wl.B[0])
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("n,nrhs", [(1, 1), (64, 2), (237, 1), (300, 3), (2157, 1)])
+def test_residual_lpg_against_oracle(zs, torch, n, nrhs):
+    # r = b - (j w L x - j Psi x / w + Zs G x) from L, Psi, G: each of the
+    # three float64 sums is bounded by its own terms, so the bound is the
+    # float64 GEMV's with |Z| replaced by w|L| + |Psi|/w + |Zs||G|
+    wl = workload.make_small(n, seed=110 + n, nf=1, nrhs=nrhs)
+    X = workload.random_rhs(n, nrhs, seed=6)
+    s = zs.Solver(n, nrhs)
+    try:
+        L, P, G = dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G)
+        zs.zsolve_assemble(s.ctx, L, P, G, wl.omega[0], wl.zs[0].real, wl.zs[0].imag)
+        b, x = dev(torch, wl.B), dev(torch, X)
+        r = torch.empty_like(b)
+        zs.zsolve_residual_lpg(s.ctx, L, P, G, b, x, r)
+        Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0])
+        ref = oracle.residual(Z, X, wl.B)
+        w = wl.omega[0]
+        terms = w * np.abs(wl.L) + np.abs(wl.Psi) / w + abs(wl.zs[0]) * np.abs(wl.G)
+        scale = np.abs(X) @ terms.T + np.abs(wl.B)
+        assert np.all(np.abs(r.cpu().numpy() - ref) <= 4 * (n + 4) * 2.3e-16 * scale + 1e-300)
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("resid", ["FX", "LPG"])
+@pytest.mark.parametrize("n,nrhs,nf", [(130, 2, 3), (700, 1, 3), (301, 4, 2), (1, 1, 2), (257, 1, 9)])
+def test_sweep_parity_fixed_point_and_lpg_residual(zs, torch, n, nrhs, nf, resid):
+    wl = workload.make_small(n, seed=85 + n, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
+    ref = oracle.solve_sweep(wl)
+    s = zs.Solver(n, nrhs, resid=getattr(zs, "ZSOLVE_RESID_" + resid))
+    try:
+        x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+        infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
+                                dev(torch, wl.B), x)
+        X = x.cpu().numpy()
+        for f in range(nf):
+            assert infos[f].status == 0 and infos[f].fallback == 0, infos[f].as_dict()
+            assert np.all(rel_err(X[f], ref[f]) <= PARITY), (f, rel_err(X[f], ref[f]))
     finally:
         s.close()
 
@@ -451,7 +541,8 @@ def test_argument_errors(zs, torch):
 # ---------------------------------------------------------------- full size (the benchmark launch)
 
 
-@pytest.mark.parametrize("gemm,resid", [("FFMA", "F64"), ("TF32X3", "F64"), ("TF32X3", "DF")])
+@pytest.mark.parametrize("gemm,resid", [("FFMA", "F64"), ("TF32X3", "F64"), ("TF32X3", "DF"), ("TF32X3", "FX"),
+                                        ("TF32X3", "LPG")])
 def test_config1_full_sweep_every_frequency(zs, torch, config1_oracle, gemm, resid):
     """N=2157, all 21 frequencies in one batched sweep (as the benchmark runs
     it): the oracle's direct solve at every frequency, element by element to
