@@ -86,8 +86,9 @@ typedef struct {
     int force_fallback; /* testing aid: treat every frequency as stalled (default 0) */
     int profile;        /* 1: time every stage with CUDA events (zsolve_get_profile); default 0 */
     int resid;          /* ZSOLVE_RESID_* (default F64) */
-    int lanes;          /* 0 (default): a sweep batch of 2 or more frequencies runs as two
-                           concurrent lanes (streams and host threads); 1: one lane */
+    int lanes;          /* 0 (default) or 2: a sweep batch of 2 or more frequencies runs as two
+                           concurrent lanes (streams and host threads); 3: three lanes for a
+                           batch of 3 or more; 1: one lane */
     int symmetric;      /* 1 (default): use that Z is complex symmetric (same page, section "Measure
                            first": exploiting the symmetry halves the factorisation's work
                            against LU).  The trailing update forms only the tiles on and below the

@@ -103,7 +103,7 @@ __device__ __forceinline__ long long progress_wait(const unsigned long long *p, 
         long long c = progress_read(p, epoch);
         if (c > need) return c;
         if (++it > limit) {
-            atomicOr(status, ZS_DEV_TIMEOUT);
+            atomicOr(status, ZS_DEV_TIMEOUT | (0x80u << 8));  // site: a triangular-solve progress word
             return -1;
         }
         if ((it & 1023u) == 0 && (*(volatile const unsigned *)status & ZS_DEV_TIMEOUT)) return -1;

@@ -61,7 +61,9 @@ constexpr int kThreads = 192;
 constexpr int A_BYTES = TM * KC * 4;       // 16 KB
 constexpr int B_BYTES = 2 * TN * KC * 4;   // 32 KB (Br rows then Bi rows)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t kWaitLimit = 1u << 24;
+// try_wait polls before a wait gives up: about a second here (a poll that
+// finds the phase incomplete suspends for some microseconds)
+constexpr uint32_t kWaitLimit = 1u << 19;
 constexpr int kTq = 8;  // tile-index queue between the roles (the producer runs at most a few tiles ahead)
 
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
@@ -111,15 +113,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait; gives up if another role already did (abort flag) or after
-// kWaitLimit polls, raising the device status bit.
+// kWaitLimit polls, raising the device status bit and recording the wait
+// site in bits 8-15 of the status word (kernel kind << 4 | role wait 1-5).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                          unsigned *status) {
+                                          unsigned *status, unsigned site) {
     uint32_t it = 0;
     while (!mbar_try_wait(bar, parity)) {
         if (*abort_flag) return false;
         if (++it > kWaitLimit) {
             *abort_flag = 1;
-            atomicOr(status, ZS_DEV_TIMEOUT);
+            atomicOr(status, ZS_DEV_TIMEOUT | (site << 8));
             return false;
         }
     }
@@ -349,7 +352,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
             while (true) {
                 if (t >= total) t = -1;
                 const uint32_t st0 = g % C::STAGES, ph0 = (g / C::STAGES) & 1u;
-                if (!mbar_wait(smem_u32(&bar_empty[st0]), ph0 ^ 1u, &s_abort, status)) break;
+                if (!mbar_wait(smem_u32(&bar_empty[st0]), ph0 ^ 1u, &s_abort, status, 1u | (KIND << 4))) break;
                 s_tq[it % kTq] = t;
                 mbar_arrive(smem_u32(&bar_tq[it % kTq]));
                 if (t < 0) {
@@ -367,7 +370,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
-                    if (kc > 0 && !mbar_wait(smem_u32(&bar_empty[st]), ph ^ 1u, &s_abort, status)) {
+                    if (kc > 0 && !mbar_wait(smem_u32(&bar_empty[st]), ph ^ 1u, &s_abort, status, 1u | (KIND << 4))) {
                         ok = false;
                         break;
                     }
@@ -405,20 +408,20 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
             while (true) {
                 // the first stage of the next tile (or the end marker) tells which
                 const uint32_t st0 = g % C::STAGES, ph0 = (g / C::STAGES) & 1u;
-                if (!mbar_wait(smem_u32(&bar_full[st0]), ph0, &s_abort, status)) break;
+                if (!mbar_wait(smem_u32(&bar_full[st0]), ph0, &s_abort, status, 2u | (KIND << 4))) break;
                 if (s_tq[it % kTq] < 0) {
                     g++;
                     mbar_arrive(smem_u32(&bar_accf[it & 1u]));  // the epilogue's turn to see the end
                     break;
                 }
                 const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
-                if (!mbar_wait(smem_u32(&bar_acce[buf]), aph ^ 1u, &s_abort, status)) break;
+                if (!mbar_wait(smem_u32(&bar_acce[buf]), aph ^ 1u, &s_abort, status, 3u | (KIND << 4))) break;
                 tc_fence_after();
                 const uint32_t d = tmem + buf * 256u;
                 bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
-                    if (kc > 0 && !mbar_wait(smem_u32(&bar_full[st]), ph, &s_abort, status)) {
+                    if (kc > 0 && !mbar_wait(smem_u32(&bar_full[st]), ph, &s_abort, status, 2u | (KIND << 4))) {
                         ok = false;
                         break;
                     }
@@ -476,11 +479,11 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
             if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&pmap) : "memory");
         }
         for (;; it++) {
-            const bool okq = mbar_wait(smem_u32(&bar_tq[it % kTq]), (it / kTq) & 1u, &s_abort, status);
+            const bool okq = mbar_wait(smem_u32(&bar_tq[it % kTq]), (it / kTq) & 1u, &s_abort, status, 4u | (KIND << 4));
             if (!__all_sync(0xffffffffu, okq)) break;
             const int t = s_tq[it % kTq];
             const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
-            const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status);
+            const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status, 5u | (KIND << 4));
             if (!__all_sync(0xffffffffu, ok) || t < 0) break;
             tc_fence_after();
             const Tile x = tile_of<KIND>(t, tiles, base, slots);

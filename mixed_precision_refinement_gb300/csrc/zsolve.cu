@@ -38,6 +38,8 @@
 #include "common.cuh"
 
 
+constexpr int kMaxLanes = 3;
+
 struct zsolve_ctx {
     int64_t n = 0;
     int nrhs_max = 0;
@@ -97,8 +99,9 @@ struct zsolve_ctx {
     size_t hd_x_cap = 0;
     int hd_nrhs_cap = 0;
     // A lane: one group of a batch's frequencies, run on its own stream with
-    // its own scratch (lane 0 on the context's stream; lane 1, for batches of
-    // two or more, on a second stream driven by a second host thread).
+    // its own scratch (lane 0 on the context's stream; the others, for
+    // batches of two or more, on streams of their own, each driven by a host
+    // thread of its own).
     struct Lane {
         cudaStream_t stream = nullptr;  // lane 0: the context's stream
         cudaStream_t side = nullptr;    // packs the next block solves' operands next to the diagonal block
@@ -113,7 +116,7 @@ struct zsolve_ctx {
         int tc_grid = 0;                // CTAs of this lane's tcgen05 launches
         int trsv_grid = 0;              // CTAs of this lane's triangular solves (0: one per SM)
     };
-    Lane lane[2];
+    Lane lane[kMaxLanes];
     int assembled = 0, factored = 0, fb_ready = 0;
     std::mutex err_mu, prof_mu, fb_mu;  // error text; profile records; fallback workspace
     // stage profile: launch counts always, event-timed spans with opts.profile
@@ -351,9 +354,14 @@ int check_device_status(zsolve_ctx *ctx, Lane &ln) {
     ZS_CU(cudaMemcpyAsync(ln.h_status, ctx->d_status, sizeof(unsigned), cudaMemcpyDeviceToHost, ln.stream));
     ZS_CU(cudaStreamSynchronize(ln.stream));
     if (*ln.h_status & ZS_DEV_TIMEOUT) {
+        const unsigned code = *ln.h_status;
         *ln.h_status = 0;
         ZS_CU(cudaMemsetAsync(ctx->d_status, 0, sizeof(unsigned), ln.stream));
-        return fail(ctx, ZSOLVE_ETIMEOUT, "a bounded device-side wait gave up (triangular solve or trailing update)");
+        // bits 8-15: the wait sites that gave up (0x80: a triangular-solve
+        // progress word; else tcgen05 kernel kind << 4 | role wait 1-5)
+        return fail(ctx, ZSOLVE_ETIMEOUT,
+                    "a bounded device-side wait gave up (triangular solve or trailing update; sites 0x%02x)",
+                    (code >> 8) & 0xFFu);
     }
     return ZSOLVE_OK;
 }
@@ -738,7 +746,7 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
         ZS_TRY(auto_probe(ctx, L, Psi, G, omega[0], zs[0], zs[1], b, x, nrhs));
         ctx->nband = 0;
     }
-    Lane &l0 = ctx->lane[0], &l1 = ctx->lane[1];
+    Lane &l0 = ctx->lane[0];
     int first_err = ZSOLVE_OK;
     for (int f0 = 0; f0 < nf; f0 += ctx->S) {
         const int count = std::min(ctx->S, nf - f0);
@@ -758,63 +766,95 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
             const int lo[1] = {0}, cnt[1] = {count};
             st = refine_lanes(ctx, l0, b, xb, nrhs, 0, count, ib, fl, lo, cnt, 1);
         } else {
-            // Two lanes factor and refine the batch's halves side by side.
-            // Lane 1 starts after lane 0's assembly (and everything queued
-            // before it on the context's stream: inputs, parameters), so that
-            // its own FP64-bound assembly runs under lane 0's factorisation and
-            // the two lanes' outer-block steps stay out of phase.  Its
-            // refinement starts when lane 0's first solve has run, so that the
-            // lanes alternate: one lane's triangular solve (latency-bound)
-            // beside the other's residual (FP64-bound on every SM); the
-            // triangular solves take half of the SMs each.
-            const int h = (count + 1) / 2;
-            // each lane's persistent tcgen05 grids leave room for the other
-            // lane's diagonal blocks (one CTA per frequency)
-            l0.tc_grid = std::max(1, ctx->num_sms - (count - h));
-            l1.tc_grid = std::max(1, ctx->num_sms - h);
-            l0.trsv_grid = l1.trsv_grid = std::max(1, ctx->num_sms / 2);
-            ZS_TRY(assemble_lane(ctx, l0, L, Psi, G, 0, h));
-            ZS_CU(cudaEventRecord(l0.ev_fork, l0.stream));
-            ZS_CU(cudaStreamWaitEvent(l1.stream, l0.ev_fork, 0));
-            Stagger sg;
-            sg.ev = l0.ev_stag;
-            int st1 = ZSOLVE_OK;
-            auto lane1 = [&]() {
-                if (cudaSetDevice(ctx->device) != cudaSuccess) {
-                    st1 = fail(ctx, ZSOLVE_ECUDA, "second lane: cudaSetDevice failed");
-                    return;
+            // K lanes (2, or 3 with opts.lanes = 3) factor and refine parts of
+            // the batch side by side, lane k on its own stream and host thread
+            // (lane 0 on the caller's).  Lane k starts after lane k-1's
+            // assembly (lane 0 after everything queued before it on the
+            // context's stream: inputs, parameters), so that its own FP64-bound
+            // assembly runs under the earlier lanes' factorisations and the
+            // lanes' outer-block steps stay out of phase.  Its refinement
+            // starts when lane k-1's first solve has run, so that the lanes
+            // alternate: one lane's triangular solve (latency-bound) beside
+            // another's residual (FP64-bound on every SM); the triangular
+            // solves take 1/K of the SMs each.
+            const int K = (ctx->opts.lanes == 3 && count >= 3) ? 3 : 2;
+            int lo[kMaxLanes], cnt[kMaxLanes];
+            for (int k = 0, at = 0; k < K; k++) {
+                cnt[k] = count / K + (k < count % K ? 1 : 0);
+                lo[k] = at;
+                at += cnt[k];
+            }
+            for (int k = 0; k < K; k++) {
+                // each lane's persistent tcgen05 grids leave room for the
+                // other lanes' diagonal blocks (one CTA per frequency)
+                ctx->lane[k].tc_grid = std::max(1, ctx->num_sms - (count - cnt[k]));
+                ctx->lane[k].trsv_grid = std::max(1, ctx->num_sms / K);
+            }
+            Stagger asm_gate[kMaxLanes], ref_gate[kMaxLanes];  // lane k's assembly / first solve queued
+            int stk[kMaxLanes] = {};
+            for (int k = 0; k < K; k++) {
+                asm_gate[k].ev = ctx->lane[k].ev[1];  // recorded by assemble_lane at its end
+                ref_gate[k].ev = ctx->lane[k].ev_stag;
+            }
+            // the whole of lane k; opens both of its gates on every path
+            auto run_lane = [&](int k) {
+                Lane &ln = ctx->lane[k];
+                int st_k = ZSOLVE_OK;
+                if (k > 0 && cudaSetDevice(ctx->device) != cudaSuccess)
+                    st_k = fail(ctx, ZSOLVE_ECUDA, "lane %d: cudaSetDevice failed", k);
+                if (k > 0) {
+                    asm_gate[k - 1].wait();
+                    if (st_k == ZSOLVE_OK && cudaStreamWaitEvent(ln.stream, asm_gate[k - 1].ev, 0) != cudaSuccess)
+                        st_k = fail(ctx, ZSOLVE_ECUDA, "lane %d: cudaStreamWaitEvent failed", k);
                 }
-                st1 = factor_lane(ctx, l1, L, Psi, G, h, count - h, false);
-                sg.wait();
-                if (st1 != ZSOLVE_OK) return;
-                if (cudaStreamWaitEvent(l1.stream, sg.ev, 0) != cudaSuccess) {
-                    st1 = fail(ctx, ZSOLVE_ECUDA, "second lane: cudaStreamWaitEvent failed");
-                    return;
+                if (st_k == ZSOLVE_OK) st_k = assemble_lane(ctx, ln, L, Psi, G, lo[k], cnt[k]);
+                asm_gate[k].open();
+                if (st_k == ZSOLVE_OK) st_k = factor_lane(ctx, ln, L, Psi, G, lo[k], cnt[k], true);
+                if (k > 0) {
+                    ref_gate[k - 1].wait();
+                    if (st_k == ZSOLVE_OK && cudaStreamWaitEvent(ln.stream, ref_gate[k - 1].ev, 0) != cudaSuccess)
+                        st_k = fail(ctx, ZSOLVE_ECUDA, "lane %d: cudaStreamWaitEvent failed", k);
                 }
-                Lane *fl[1] = {&l1};
-                const int lo[1] = {h}, cnt[1] = {count - h};
-                st1 = refine_lanes(ctx, l1, b, xb, nrhs, h, count - h, ib, fl, lo, cnt, 1);
+                if (st_k == ZSOLVE_OK) {
+                    Lane *fl[1] = {&ln};
+                    const int lo1[1] = {lo[k]}, cnt1[1] = {cnt[k]};
+                    st_k = refine_lanes(ctx, ln, b, xb, nrhs, lo[k], cnt[k], ib, fl, lo1, cnt1, 1,
+                                        k + 1 < K ? &ref_gate[k] : nullptr);
+                }
+                ref_gate[k].open();
+                stk[k] = st_k;
             };
-            std::thread worker;
-            bool threaded = true;
-            try {
-                worker = std::thread(lane1);
-            } catch (...) {
-                threaded = false;  // no thread: the lanes run one after the other
+            std::thread workers[kMaxLanes];
+            bool threaded[kMaxLanes] = {};
+            for (int k = 1; k < K; k++) {
+                try {
+                    workers[k] = std::thread(run_lane, k);
+                    threaded[k] = true;
+                } catch (...) {
+                    threaded[k] = false;  // no thread: this lane runs after lane 0
+                }
             }
-            int st0 = factor_lane(ctx, l0, L, Psi, G, 0, h, true);
-            if (st0 == ZSOLVE_OK) {
-                Lane *fl[1] = {&l0};
-                const int lo[1] = {0}, cnt[1] = {h};
-                st0 = refine_lanes(ctx, l0, b, xb, nrhs, 0, h, ib, fl, lo, cnt, 1, &sg);
+            run_lane(0);
+            for (int k = 1; k < K; k++) {
+                if (threaded[k]) workers[k].join();
+                else run_lane(k);
             }
-            sg.open();  // on every path
-            if (threaded) worker.join();
-            else lane1();
-            ZS_CU(cudaEventRecord(l1.ev_join, l1.stream));
-            ZS_CU(cudaStreamWaitEvent(l0.stream, l1.ev_join, 0));
-            const bool hard0 = st0 != ZSOLVE_OK && st0 != ZSOLVE_ESINGULAR;
-            st = hard0 ? st0 : (st1 != ZSOLVE_OK ? st1 : st0);
+            for (int k = 1; k < K; k++) {
+                ZS_CU(cudaEventRecord(ctx->lane[k].ev_join, ctx->lane[k].stream));
+                ZS_CU(cudaStreamWaitEvent(l0.stream, ctx->lane[k].ev_join, 0));
+            }
+            st = ZSOLVE_OK;
+            for (int k = 0; k < K; k++)  // the first hard error, else the first singular fallback
+                if (stk[k] != ZSOLVE_OK && stk[k] != ZSOLVE_ESINGULAR) {
+                    st = stk[k];
+                    break;
+                }
+            if (st == ZSOLVE_OK)
+                for (int k = 0; k < K; k++)
+                    if (stk[k] != ZSOLVE_OK) {
+                        st = stk[k];
+                        break;
+                    }
         }
         if (st != ZSOLVE_OK && first_err == ZSOLVE_OK) first_err = st;
         if (st != ZSOLVE_OK && st != ZSOLVE_ESINGULAR) return st;
@@ -916,7 +956,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (ctx->opts.outer_block == 0) ctx->opts.outer_block = ZS_NB;
     if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
         ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0 || ctx->opts.resid < 0 ||
-        ctx->opts.resid > ZSOLVE_RESID_LPG || ctx->opts.lanes < 0 || ctx->opts.lanes > 2 || ctx->opts.symmetric < 0 ||
+        ctx->opts.resid > ZSOLVE_RESID_LPG || ctx->opts.lanes < 0 || ctx->opts.lanes > 3 || ctx->opts.symmetric < 0 ||
         ctx->opts.symmetric > 1 || ctx->opts.wait_limit < 0) {
         delete ctx;
         return ZSOLVE_EINVAL;
@@ -974,7 +1014,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOCH(ctx->h_pivflag, S * sizeof(int));
     ALLOC(ctx->prog, (size_t)S * 2 * sizeof(unsigned long long));
     ALLOC(ctx->d_status, sizeof(unsigned));
-    for (int l = 0; l < 2; l++) {
+    for (int l = 0; l < kMaxLanes; l++) {
         Lane &ln = ctx->lane[l];
         ALLOC(ln.d_active, S * sizeof(int));
         ALLOCH(ln.h_active, S * sizeof(int));
@@ -985,7 +1025,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     }
 #undef ALLOC
 #undef ALLOCH
-    for (int l = 0; l < 2; l++) {
+    for (int l = 0; l < kMaxLanes; l++) {
         Lane &ln = ctx->lane[l];
         for (auto &e : ln.ev)
             if (cudaEventCreate(&e) != cudaSuccess) return bail(ZSOLVE_ECUDA);
@@ -995,11 +1035,13 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
             cudaEventCreateWithFlags(&ln.ev_stag, cudaEventDisableTiming) != cudaSuccess)
             return bail(ZSOLVE_ECUDA);
     }
-    if (cudaStreamCreateWithFlags(&ctx->lane[1].stream, cudaStreamNonBlocking) != cudaSuccess)
-        return bail(ZSOLVE_ECUDA);
-    ctx->lane[1].own_stream = true;
+    for (int l = 1; l < kMaxLanes; l++) {
+        if (cudaStreamCreateWithFlags(&ctx->lane[l].stream, cudaStreamNonBlocking) != cudaSuccess)
+            return bail(ZSOLVE_ECUDA);
+        ctx->lane[l].own_stream = true;
+    }
     ctx->lane[0].stream = ctx->stream;
-    ctx->lane[0].tc_grid = ctx->lane[1].tc_grid = ctx->num_sms;
+    for (auto &ln : ctx->lane) ln.tc_grid = ctx->num_sms;
     if (ctx->winv &&
         (zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 128, ctx->pack_map) != cudaSuccess ||
          zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 32, ctx->packst_map) != cudaSuccess ||

@@ -388,13 +388,13 @@ def test_sweep_ragged_parity(zs, torch, n, nrhs, nf, batch, gemm):
 @pytest.mark.parametrize("gemm", ["FFMA", "TF32X3"])
 @pytest.mark.parametrize("n,nrhs,nf,batch", [(300, 2, 5, 5), (257, 1, 7, 4), (129, 3, 2, 0)])
 def test_sweep_two_lanes_match_one_lane(zs, torch, n, nrhs, nf, batch, gemm):
-    """A batch split over two concurrent lanes (streams and host threads) runs
-    the same kernels on the same per-frequency data as one lane: the solutions
-    agree bit for bit, and both match the oracle."""
+    """A batch split over two or three concurrent lanes (streams and host
+    threads) runs the same kernels on the same per-frequency data as one lane:
+    the solutions agree bit for bit, and all match the oracle."""
     wl = workload.make_small(n, seed=70 + n, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
     ref = oracle.solve_sweep(wl)
     out = {}
-    for lanes in (1, 2):
+    for lanes in (1, 2, 3):
         s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm), batch=batch, lanes=lanes)
         try:
             x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
@@ -406,8 +406,8 @@ def test_sweep_two_lanes_match_one_lane(zs, torch, n, nrhs, nf, batch, gemm):
                 assert np.all(rel_err(out[lanes][0][f], ref[f]) <= PARITY)
         finally:
             s.close()
-    assert out[1][1] == out[2][1]
-    assert np.array_equal(out[1][0], out[2][0])
+    assert out[1][1] == out[2][1] == out[3][1]
+    assert np.array_equal(out[1][0], out[2][0]) and np.array_equal(out[1][0], out[3][0])
 
 
 def test_sweep_term_isolation_parity(zs, torch):
