@@ -232,16 +232,21 @@ cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int6
 #define ZS_WINV_PLANE (ZS_NB * ZS_PACK_K)
 #define ZS_WINV_STRIDE (8 * ZS_WINV_PLANE)
 inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }
-// Triangular solves with 128-row blocks and the inverse diagonal blocks; nrhs 1, 2 or 4 per launch.
+// Triangular solves with 128-row blocks and the inverse diagonal blocks:
+// per slot, ngroup independent groups of nrhs (1, 2 or 4) right-hand sides
+// each (group g = rows g*nrhs .. g*nrhs+nrhs-1 of the slot's v), solved as
+// separate dependency chains side by side in one launch.
+// prog: two progress words per (slot, group), at 2 * (slot * ZS_TRSV_MAX_GROUPS + g).
 // wait_limit: polls before a wait for another task's block gives up (raising
 // ZS_DEV_TIMEOUT in *status).  first_ticket: the task ticket starts here
 // (0 in every solve; a positive value withholds the first tasks, so that the
 // bounded waits can be shown to give up -- a testing aid).
+#define ZS_TRSV_MAX_GROUPS 8
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                const float *dinv, int64_t dinv_stride, float2 *v, int64_t v_stride, int nrhs,
-                               const int *slots, int nslot, unsigned long long *prog, unsigned epoch, unsigned *ticket,
-                               unsigned *status, int num_sms, cudaStream_t st, unsigned wait_limit = ZS_SPIN_LIMIT,
-                               unsigned first_ticket = 0);
+                               int ngroup, const int *slots, int nslot, unsigned long long *prog, unsigned epoch,
+                               unsigned *ticket, unsigned *status, int num_sms, cudaStream_t st,
+                               unsigned wait_limit = ZS_SPIN_LIMIT, unsigned first_ticket = 0);
 
 // r = b - Z64 x.  out_c64 != NULL: writes float2 (rounded); else writes c128 to out_c128.
 // Launches one kernel per chunk of 8/4/2/1 right-hand sides (zs_rhs_chunks).

@@ -14,6 +14,12 @@
 // task waits only on tasks with smaller tickets, claimed by running CTAs; each
 // wait is bounded and raises the status bit instead of hanging.
 //
+// The chains of one launch are (slot, right-hand-side group) pairs: with few
+// frequencies and several right-hand sides, groups of fewer right-hand sides
+// give more chains side by side (each a short latency-bound critical path),
+// at the price of reading the slot's factors once per group; the groups of a
+// slot advance together, so most of those repeated reads hit the L2.
+//
 // Bound: HBM for the off-diagonal blocks (8 n^2 bytes per frequency per
 // solve) plus the dependency chain's latency (n / 128 steps per direction).
 #include "common.cuh"
@@ -92,8 +98,8 @@ template <int R>
 __global__ void __launch_bounds__(kThreads, 1)
 k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
            const float *__restrict__ dinv, int64_t dinv_stride, float2 *__restrict__ v, int64_t v_stride,
-           const int *__restrict__ slots, int nslot, unsigned long long *__restrict__ prog, unsigned epoch,
-           unsigned *ticket, unsigned *status, unsigned wait_limit) {
+           int ngroup, const int *__restrict__ slots, int nslot, unsigned long long *__restrict__ prog,
+           unsigned epoch, unsigned *ticket, unsigned *status, unsigned wait_limit) {
     constexpr bool kPreload = R == 1;
     extern __shared__ __align__(16) float sinv[];  // [re, im][TB][TB]
     __shared__ cf part[TB][R];
@@ -101,7 +107,8 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
     __shared__ unsigned s_task, s_stop;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nblk = (int)((n + TB - 1) / TB);
-    const unsigned total = 2u * (unsigned)nblk * (unsigned)nslot;
+    const unsigned nchain = (unsigned)nslot * (unsigned)ngroup;
+    const unsigned total = 2u * (unsigned)nblk * nchain;
     const uint32_t sinv_addr = (uint32_t)__cvta_generic_to_shared(sinv);
     while (true) {
         __syncthreads();
@@ -112,17 +119,18 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
         __syncthreads();
         const unsigned t = s_task;
         if (t >= total || s_stop) break;
-        const int phase = (int)(t / ((unsigned)nblk * nslot));
-        const unsigned rem = t - (unsigned)phase * nblk * nslot;
-        const int si = (int)(rem % (unsigned)nslot);
-        const int bq = (int)(rem / (unsigned)nslot);
+        const int phase = (int)(t / ((unsigned)nblk * nchain));
+        const unsigned rem = t - (unsigned)phase * nblk * nchain;
+        const int ci = (int)(rem % nchain);  // chain: slot si, group g
+        const int bq = (int)(rem / nchain);
         const int b = phase == 0 ? bq : nblk - 1 - bq;
+        const int si = ci / ngroup, g = ci - si * ngroup;
         const int slot = slots[si];
         const float *re = z32 + (int64_t)slot * z32_stride;
         const float *im = re + plane;
         const float *ir = dinv + (int64_t)slot * dinv_stride + (int64_t)b * 4 * TB * TB + (int64_t)phase * 2 * TB * TB;
-        float2 *vs = v + (int64_t)slot * v_stride;
-        unsigned long long *pf = prog + 2 * (int64_t)slot, *pb = pf + 1;
+        float2 *vs = v + (int64_t)slot * v_stride + (int64_t)g * R * n;
+        unsigned long long *pf = prog + 2 * ((int64_t)slot * ZS_TRSV_MAX_GROUPS + g), *pb = pf + 1;
         const int64_t r0 = (int64_t)b * TB;
         const int rows = (int)zs::min64(TB, n - r0);
         const int64_t wrow = (r0 + warp * 8) * ld;  // offset of the warp's first row
@@ -303,7 +311,7 @@ k_trsv_inv(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32
 
 template <int R>
 cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n, const float *dinv,
-                       int64_t dinv_stride, float2 *v, int64_t v_stride, const int *slots, int nslot,
+                       int64_t dinv_stride, float2 *v, int64_t v_stride, int ngroup, const int *slots, int nslot,
                        unsigned long long *prog, unsigned epoch, unsigned *ticket, unsigned *status, int num_sms,
                        cudaStream_t st, unsigned wait_limit, unsigned first_ticket) {
     // once per process and instance (thread-safe initialisation of a local static)
@@ -316,7 +324,7 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
     if (per_sm < 1) per_sm = 1;
     const int64_t nblk = (n + TB - 1) / TB;
     int64_t grid = (int64_t)per_sm * num_sms;
-    const int64_t tasks = 2 * nblk * nslot;
+    const int64_t tasks = 2 * nblk * nslot * ngroup;
     if (grid > tasks) grid = tasks;
     if (first_ticket == 0) {
         e = cudaMemsetAsync(ticket, 0, sizeof(unsigned), st);
@@ -332,8 +340,9 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
     // CTAs that are already running have claimed, so the solve progresses
     // with any number of resident CTAs -- also while another stream's kernels
     // hold part of the GPU.
-    k_trsv_inv<R><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride,
-                                                       slots, nslot, prog, epoch, ticket, status, wait_limit);
+    k_trsv_inv<R><<<(unsigned)grid, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v,
+                                                                v_stride, ngroup, slots, nslot, prog, epoch, ticket,
+                                                                status, wait_limit);
     return cudaGetLastError();
 }
 
@@ -341,19 +350,20 @@ cudaError_t launch_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_
 
 cudaError_t zs_launch_trsv_inv(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                const float *dinv, int64_t dinv_stride, float2 *v, int64_t v_stride, int nrhs,
-                               const int *slots, int nslot, unsigned long long *prog, unsigned epoch, unsigned *ticket,
-                               unsigned *status, int num_sms, cudaStream_t st, unsigned wait_limit,
+                               int ngroup, const int *slots, int nslot, unsigned long long *prog, unsigned epoch,
+                               unsigned *ticket, unsigned *status, int num_sms, cudaStream_t st, unsigned wait_limit,
                                unsigned first_ticket) {
+    if (ngroup < 1 || ngroup > ZS_TRSV_MAX_GROUPS || nslot < 1) return cudaErrorInvalidValue;
     switch (nrhs) {
         case 1:
-            return launch_inv<1>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
-                                 epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
+            return launch_inv<1>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, ngroup, slots, nslot,
+                                 prog, epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
         case 2:
-            return launch_inv<2>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
-                                 epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
+            return launch_inv<2>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, ngroup, slots, nslot,
+                                 prog, epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
         case 4:
-            return launch_inv<4>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, slots, nslot, prog,
-                                 epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
+            return launch_inv<4>(z32, ld, plane, z32_stride, n, dinv, dinv_stride, v, v_stride, ngroup, slots, nslot,
+                                 prog, epoch, ticket, status, num_sms, st, wait_limit, first_ticket);
         default:
             return cudaErrorInvalidValue;
     }

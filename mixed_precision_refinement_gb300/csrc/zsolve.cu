@@ -73,6 +73,7 @@ struct zsolve_ctx {
     int *xe = nullptr;     // their scale exponents, per (slot, rhs)
     int *zexp = nullptr;   // residual mode FX: per slot and row of Z64, its largest exponent
     int fx_ndf = 1;        // residual mode FX: sub-steps of four taken in float64 (ZSOLVE_FX_NDF)
+    int trsv_r = 0;        // right-hand sides per triangular-solve chain; 0: chosen per solve (ZSOLVE_TRSV_R)
     int resid_mode = ZSOLVE_RESID_F64;
     double *partials = nullptr;
     int nchunks = 0;
@@ -80,7 +81,7 @@ struct zsolve_ctx {
     ZsSlotParam *d_params = nullptr, *h_params = nullptr;
     int *d_all = nullptr;    // 0..S-1
     int *d_pivflag = nullptr, *h_pivflag = nullptr;
-    unsigned long long *prog = nullptr;  // triangular-solve progress words, 2 per slot
+    unsigned long long *prog = nullptr;  // triangular-solve progress words, 2 per (slot, right-hand-side group)
     std::atomic<unsigned> epoch{0};      // triangular-solve launches, unique across lanes
     unsigned *d_status = nullptr;
     // fallback workspace (allocated on first use)
@@ -330,22 +331,41 @@ int factor_slots(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot, int fir
 
 // ------------------------------------------------------------------ solves
 
-// v <- (LU)^-1 v for the listed slots, right-hand sides in chunks of 4/2/1.
-// first_ticket > 0 withholds the first tasks of each launch (testing aid of
-// the bounded waits, zsolve_selftest_wait); 0 in every solve.
+// Right-hand sides per chain of a triangular solve: the largest of 4, 2, 1
+// whose chains (slots x groups) hold at least two tasks per CTA of the
+// launch (a chain keeps up to n / 128 block tasks in work at once: one per
+// block row, each taking the blocks left of it as the wavefront passes), else
+// 1.  A chain's critical path is 2 n / 128 dependent block steps, shorter per
+// step with fewer right-hand sides; the factors are read once per chain,
+// mostly from the L2, since the chains of a slot advance together.
+int trsv_rhs_per_chain(const zsolve_ctx *ctx, int left, int nslot, int grid) {
+    if (ctx->trsv_r > 0) return std::min(ctx->trsv_r, left >= 4 ? 4 : left >= 2 ? 2 : 1);
+    const int64_t nblk = (ctx->n + ZS_TB2 - 1) / ZS_TB2;
+    for (int R = 4; R > 1; R >>= 1)
+        if (left >= R && (int64_t)nslot * std::min(left / R, ZS_TRSV_MAX_GROUPS) * nblk >= 2 * (int64_t)grid)
+            return R;
+    return 1;
+}
+
+// v <- (LU)^-1 v for the listed slots: the right-hand sides in groups of R
+// (4, 2 or 1), up to ZS_TRSV_MAX_GROUPS groups per launch, every (slot,
+// group) an independent chain.  first_ticket > 0 withholds the first tasks
+// of each launch (testing aid of the bounded waits, zsolve_selftest_wait);
+// 0 in every solve.
 int lowprec_solve_slots(zsolve_ctx *ctx, Lane &ln, int nrhs, const int *slots, int nslot, unsigned first_ticket = 0) {
     int r0 = 0;
     while (r0 < nrhs) {
         const int left = nrhs - r0;
-        const int R = left >= 4 ? 4 : left >= 2 ? 2 : 1;
+        const int grid = ln.trsv_grid ? ln.trsv_grid : ctx->num_sms;
+        const int R = trsv_rhs_per_chain(ctx, left, nslot, grid);
+        const int groups = std::min(left / R, ZS_TRSV_MAX_GROUPS);
         const unsigned epoch = ctx->epoch.fetch_add(1u) + 1u;
         StageSpan sp(ctx, ZSOLVE_STAGE_TRSV, ln.stream);
         ZS_CU(zs_launch_trsv_inv(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, ctx->n, ctx->dinv, ctx->dinv_stride,
-                                 ctx->v + (int64_t)r0 * ctx->n, ctx->v_stride, R, slots, nslot, ctx->prog, epoch,
-                                 ln.ticket, ctx->d_status, ln.trsv_grid ? ln.trsv_grid : ctx->num_sms, ln.stream,
-                                 ctx->wait_limit, first_ticket));
+                                 ctx->v + (int64_t)r0 * ctx->n, ctx->v_stride, R, groups, slots, nslot, ctx->prog,
+                                 epoch, ln.ticket, ctx->d_status, grid, ln.stream, ctx->wait_limit, first_ticket));
         sp.done(1);
-        r0 += R;
+        r0 += R * groups;
     }
     return ZSOLVE_OK;
 }
@@ -967,6 +987,11 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ctx->probe.chosen = ctx->opts.gemm == ZSOLVE_GEMM_AUTO ? ZSOLVE_GEMM_TF32X3 : ctx->opts.gemm;
     if (ctx->opts.wait_limit > 0) ctx->wait_limit = (unsigned)ctx->opts.wait_limit;
     if (const char *e = getenv("ZSOLVE_FX_NDF")) ctx->fx_ndf = std::min(3, std::max(0, atoi(e)));
+    // right-hand sides per triangular-solve chain (1, 2 or 4; unset: chosen per solve)
+    if (const char *e = getenv("ZSOLVE_TRSV_R")) {
+        const int r = atoi(e);
+        ctx->trsv_r = (r == 1 || r == 2 || r == 4) ? r : 0;
+    }
     auto bail = [&](int code) {
         free_all(ctx);
         delete ctx;
@@ -1012,7 +1037,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ALLOC(ctx->d_all, S * sizeof(int));
     ALLOC(ctx->d_pivflag, S * sizeof(int));
     ALLOCH(ctx->h_pivflag, S * sizeof(int));
-    ALLOC(ctx->prog, (size_t)S * 2 * sizeof(unsigned long long));
+    ALLOC(ctx->prog, (size_t)S * 2 * ZS_TRSV_MAX_GROUPS * sizeof(unsigned long long));
     ALLOC(ctx->d_status, sizeof(unsigned));
     for (int l = 0; l < kMaxLanes; l++) {
         Lane &ln = ctx->lane[l];
@@ -1051,7 +1076,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     std::vector<int> all(S);
     for (int s = 0; s < S; s++) all[s] = s;
     if (cudaMemcpy(ctx->d_all, all.data(), S * sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(ctx->prog, 0, (size_t)S * 2 * sizeof(unsigned long long)) != cudaSuccess ||
+        cudaMemset(ctx->prog, 0, (size_t)S * 2 * ZS_TRSV_MAX_GROUPS * sizeof(unsigned long long)) != cudaSuccess ||
         cudaMemset(ctx->d_status, 0, sizeof(unsigned)) != cudaSuccess ||
         cudaMemset(ctx->d_pivflag, 0, S * sizeof(int)) != cudaSuccess ||
         cudaMemset(ctx->z32, 0, (size_t)S * ctx->z32_stride * sizeof(float)) != cudaSuccess ||
@@ -1237,8 +1262,8 @@ int zsolve_selftest_wait(zsolve_ctx *ctx, int nrhs) {
     if (!ctx) return ZSOLVE_EINVAL;
     ZS_TRY(check_nrhs(ctx, nrhs));
     if (!ctx->factored) return fail(ctx, ZSOLVE_ESTATE, "zsolve_selftest_wait before zsolve_factor");
-    // every task but the first waits, directly or through the chain, for the
-    // first block, which no task computes
+    // every task of the first chain but its first waits, directly or through
+    // the chain, for that chain's first block, which no task computes
     ZS_TRY(lowprec_solve_slots(ctx, ctx->lane[0], nrhs, ctx->d_all, 1, 1u));
     return check_device_status(ctx, ctx->lane[0]);
 }
