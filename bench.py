@@ -36,12 +36,14 @@ import numpy as np  # noqa: E402
 import workload  # noqa: E402
 
 METRIC = "solved freq points/s at N=2157; LU TFLOP/s; FP64 residual GEMV HBM GB/s"
-RESID_NAMES = {0: "F64", 1: "DF", 2: "FX", 3: "LPG"}
+RESID_NAMES = {0: "F64", 1: "DF", 2: "FX", 3: "LPG", 4: "OZ"}
 RESID_ARITH = {
     "F64": "float64 DFMA GEMV over the assembled Z",
     "DF": "double-float (2 x float32, ~46 bits)",
     "FX": "exact 72-bit fixed-point products and sums on the integer pipes, float64-accurate",
     "LPG": "float64 DFMA from L, Psi, G, four frequencies per pass (no assembled Z read)",
+    "OZ": "L x, Psi x, G x of a lane's frequencies as one bf16 tensor-core product with error-free splitting "
+          "(8 digits of 7 bits per value, exact digit products and sums), rounded once to float64",
 }
 UNIT = "freq points/s"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -111,6 +113,21 @@ def kernel_times(stage_ms, gemm):
         out["k_schur_simt"] = stage_ms.get("schur", 0.0)
     else:
         out["k_cgemm_tc"] = stage_ms.get("trsm", 0.0) + stage_ms.get("schur", 0.0)
+    return out
+
+
+def oz_lane_evaluations(iters, lanes):
+    """Residual evaluations per sweep in the mode OZ: each lane evaluates its
+    frequencies together, once per correction of its slowest frequency (the
+    lanes split the batch as the library does: lane k takes nf / K, the first
+    nf % K one more)."""
+    nf = len(iters)
+    out, at = 0, 0
+    for k in range(lanes):
+        c = nf // lanes + (1 if k < nf % lanes else 0)
+        if c:
+            out += max(iters[at:at + c])
+        at += c
     return out
 
 
@@ -281,7 +298,7 @@ def sweep_variant(zs, torch, wl, args, resid, symmetric=None):
         out = {"mode_in_use": mode, "points_per_s": nf / (ms / 1e3), "resid_ms_per_step": res_ms,
                "resid_gbs": gbs, "resid_hbm_frac": (gbs / peaks["hbm_gbs"]) if gbs else None,
                "arith": RESID_ARITH[mode]}
-        if mode == "LPG":  # reads L, Psi, G (24 n^2) once per group of 4 frequencies, not Z (16 n^2 each)
+        if mode in ("LPG", "OZ"):  # read L, Psi, G (or their digits), not Z (16 n^2 per frequency)
             out["note"] = "resid_gbs counts the float64 Z bytes the GEMV would read, for comparison"
         return out
     finally:
@@ -596,10 +613,23 @@ def run_ours(args):
     rl["k_trsv_inv"] = obj("k_trsv_inv", "hbm", st["trsv"]["ms"], st["trsv"]["launches"],
                            n_solves * 8.0 * n * n * math.ceil(nrhs / 4) * steps, hbm, "GB/s", f"{peak_src} copy",
                            "8 n^2 bytes of float32 factors per solve and frequency")
-    rl["k_residual"] = obj({"F64": "k_residual", "DF": "k_residual_df", "FX": "k_residual_fx",
-                            "LPG": "k_residual_lpg"}[resid_mode], "hbm", st["residual"]["ms"],
-                           st["residual"]["launches"], res_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
-                           "16 n^2 + 32 n nrhs bytes per evaluation and frequency")
+    if resid_mode == "OZ":
+        # per sweep: the digits of L, Psi, G formed once (24 n^2 read, 48 n^2
+        # written); per evaluation of a lane's frequencies: the 48 n^2 bytes of
+        # digits read by the tensor-core product (x's digits and the partial
+        # products are O(n) per column)
+        lanes_eval = oz_lane_evaluations(iters, 2 if nf >= 2 else 1)
+        oz_bytes = 72.0 * n * n + lanes_eval * 48.0 * n * n
+        rl["k_residual"] = obj("k_oz_gemm", "hbm", st["residual"]["ms"], st["residual"]["launches"],
+                               oz_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
+                               "48 n^2 bytes of digits per evaluation of a lane's frequencies, plus 72 n^2 per "
+                               "sweep to form them; over the residual stage's device time (digit formation, "
+                               "product, combination)", evaluations_per_step=lanes_eval)
+    else:
+        rl["k_residual"] = obj({"F64": "k_residual", "DF": "k_residual_df", "FX": "k_residual_fx",
+                                "LPG": "k_residual_lpg"}[resid_mode], "hbm", st["residual"]["ms"],
+                               st["residual"]["launches"], res_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
+                               "16 n^2 + 32 n nrhs bytes per evaluation and frequency")
     lanes = 2 if nf >= 2 else 1
     rl["k_assemble"] = obj("k_assemble", "hbm", st["assemble"]["ms"], st["assemble"]["launches"],
                            (24.0 * n * n * lanes + 24.0 * n * n * nf) * steps, hbm, "GB/s", f"{peak_src} copy",
@@ -614,7 +644,8 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32 factor + " + {"F64": "f64", "DF": "double-float f32x2", "FX": "f64-accurate int fixed-point",
-                                    "LPG": "f64"}[resid_mode] + " residual",
+                                    "LPG": "f64", "OZ": "f64-accurate bf16 tensor-core split"}[resid_mode]
+                 + " residual",
         "data": "synthetic",
         "config": {"workload": workload_name(args.config), "n": n, "nf": nf, "nrhs": nrhs,
                    "gemm": args.gemm if args.gemm == args.gemm_eff else f"{args.gemm} -> {args.gemm_eff}",
@@ -641,7 +672,7 @@ def run_ours(args):
         args.resid: {"mode_in_use": resid_mode, "points_per_s": value / ws, "resid_gbs": res_gbs,
                      "resid_hbm_frac": (res_gbs / peaks["hbm_gbs"]) if res_gbs else None,
                      "arith": RESID_ARITH[resid_mode]}}
-    for other in ("F64", "FX", "DF", "LPG"):
+    for other in ("F64", "FX", "DF", "LPG", "OZ"):
         if other != args.resid:
             line["resid_variants"][other] = sweep_variant(zs, torch, wl, args, other)
     # the other factorisation mode: full trailing update, or the symmetric one
@@ -669,7 +700,7 @@ def main():
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--gemm", default="AUTO", choices=["AUTO", "TF32", "TF32X3", "FFMA"])
     ap.add_argument("--batch", type=int, default=0)
-    ap.add_argument("--resid", default="F64", choices=["F64", "DF", "FX", "LPG"])
+    ap.add_argument("--resid", default="OZ", choices=["F64", "DF", "FX", "LPG", "OZ"])
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--no-afs", dest="afs", action="store_false")

@@ -74,6 +74,11 @@ extern "C" {
                               the sweep's L, Psi, G, several frequencies per pass over them, without
                               the assembled float64 Z (zsolve_residual_lpg); calls on the single
                               system of zsolve_assemble keep the float64 GEMV (F64) */
+#define ZSOLVE_RESID_OZ 4  /* zsolve_sweep: the same form, L x, Psi x, G x of all of a batch's
+                              frequencies as one product on the bf16 tensor cores with error-free
+                              splitting (8 digits of 7 bits per value, exact digit products and
+                              sums, one rounding to float64 per output; zsolve_residual_oz);
+                              calls on the single system keep the float64 GEMV (F64) */
 
 typedef struct zsolve_ctx zsolve_ctx; /* opaque */
 
@@ -234,6 +239,24 @@ int zsolve_residual(zsolve_ctx *ctx, const void *b, const void *x, void *r, int 
  * section "Fewer frequency points: adaptive frequency sampling". */
 int zsolve_residual_lpg(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const void *b,
                         const void *x, void *r, int nrhs);
+
+/* r = b - Z x for the single system of zsolve_assemble (its omega and Zs),
+ * from L, Psi, G (device, n x n float64, as passed to zsolve_assemble) by
+ * the residual mode ZSOLVE_RESID_OZ: the products L x, Psi x, G x on the
+ * bf16 tensor cores with error-free splitting (Ozaki et al., "Error-free
+ * transformations of matrix multiplication by using fast routines of matrix
+ * multiplication and its applications", 2012), then r = b - (j w L x -
+ * j Psi x / w + Zs G x) in float64.  Error: that of the float64 combination,
+ * plus at most 2^-54 of each row's largest |entry| times sum |x| (and of
+ * x's largest |entry| times the row's sum |entry|).  A non-finite value in a
+ * row of L, Psi, G or in x gives NaN residuals for it.  The first call
+ * allocates about 48 n^2 bytes of digits; each call forms them from L, Psi,
+ * G again.  b, x, r: device c128, nrhs x n.  Returns ZSOLVE_ETIMEOUT if a
+ * bounded device-side wait gave up.  Passage: step 3 (the residual in double
+ * precision) with the form of Z of section "Fewer frequency points: adaptive
+ * frequency sampling". */
+int zsolve_residual_oz(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const void *b,
+                       const void *x, void *r, int nrhs);
 
 /* d = (L U)^-1 v with the low-precision factors (steps 2 and 4): v is
  * rounded to complex float32, solved in float32, and d returned as c128.

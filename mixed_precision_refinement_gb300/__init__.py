@@ -38,6 +38,7 @@ ZSOLVE_RESID_F64 = 0
 ZSOLVE_RESID_DF = 1
 ZSOLVE_RESID_FX = 2
 ZSOLVE_RESID_LPG = 3
+ZSOLVE_RESID_OZ = 4
 
 HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "zsolve.h")
 
@@ -119,6 +120,7 @@ def _load():
         "zsolve_sweep_host": (I, [P, P, P, P, P, P, I, P, P, I, ctypes.POINTER(zsolve_info)]),
         "zsolve_residual": (I, [P, P, P, P, I]),
         "zsolve_residual_lpg": (I, [P, P, P, P, P, P, P, I]),
+        "zsolve_residual_oz": (I, [P, P, P, P, P, P, P, I]),
         "zsolve_lowprec_solve": (I, [P, P, P, I]),
         "zsolve_fallback_solve": (I, [P, P, P, I]),
         "zsolve_selftest_wait": (I, [P, I]),
@@ -286,6 +288,15 @@ def zsolve_residual_lpg(ctx, L, Psi, G, b, x, r) -> None:
         _require(t, "c128", True)
     nrhs = b.shape[0] if b.dim() == 2 else 1
     _check(ctx, _lib.zsolve_residual_lpg(ctx, _ptr(L), _ptr(Psi), _ptr(G), _ptr(b), _ptr(x), _ptr(r), nrhs))
+
+
+def zsolve_residual_oz(ctx, L, Psi, G, b, x, r) -> None:
+    for t in (L, Psi, G):
+        _require(t, "f64", True)
+    for t in (b, x, r):
+        _require(t, "c128", True)
+    nrhs = b.shape[0] if b.dim() == 2 else 1
+    _check(ctx, _lib.zsolve_residual_oz(ctx, _ptr(L), _ptr(Psi), _ptr(G), _ptr(b), _ptr(x), _ptr(r), nrhs))
 
 
 def zsolve_lowprec_solve(ctx, v, d) -> None:

@@ -280,6 +280,25 @@ cudaError_t zs_launch_residual_lpg(const double *L, const double *Psi, const dou
                                    int nrhs, float2 *out_c64, int64_t out64_stride, double2 *out_c128,
                                    int64_t out128_stride, const int *slots, int nslot, cudaStream_t st);
 
+// Residual from L, Psi, G on the bf16 tensor cores with error-free splitting
+// (resid_oz.cu).  The digits of A' = [L; Psi; G] (8 planes of 3n rows x
+// zs_oz_n_pad(n) bf16, bytes 16 * 3n * n_pad) and their row scales (ea, 3n
+// ints) are formed once per set of L, Psi, G, rows r0..r1-1 of each matrix
+// per call; amap (a CUtensorMap, 64-byte aligned) describes them.  Per
+// evaluation: the digits of x (xdig: 8 planes of ncol_cap rows x n_pad bf16,
+// ex: ncol_cap ints, ncol = 2 nslot nrhs <= ncol_cap), the partial products
+// (part: part_cap doubles) and then r as zs_launch_residual.
+int64_t zs_oz_n_pad(int64_t n);
+int zs_oz_ncol_alloc(int ncol);
+cudaError_t zs_launch_oz_split_a(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0,
+                                 int64_t r1, void *dig, int *ea, cudaStream_t st);
+cudaError_t zs_oz_a_map(const void *dig, int64_t n, void *map_out);
+cudaError_t zs_launch_residual_oz(const void *amap, const int *ea, int64_t n, const ZsSlotParam *params,
+                                  const double2 *b, const double2 *x, int64_t x_stride, int nrhs, float2 *out_c64,
+                                  int64_t out64_stride, double2 *out_c128, int64_t out128_stride, const int *slots,
+                                  int nslot, void *xdig, int *ex, int ncol_cap, double *part, int64_t part_cap,
+                                  unsigned *status, int num_sms, cudaStream_t st);
+
 // Fixed-point residual (resid_fx.cu): x split into exact 24-bit limbs per
 // right-hand side (xl: per slot xl_stride bytes, zs_fx_x_bytes(n) per right-hand side; xe: per
 // (slot, rhs) the scale exponent, index slot * nrhs_max + r), then r = b - Z64 x

@@ -74,6 +74,13 @@ struct zsolve_ctx {
     int *zexp = nullptr;   // residual mode FX: per slot and row of Z64, its largest exponent
     int fx_ndf = 1;        // residual mode FX: sub-steps of four taken in float64 (ZSOLVE_FX_NDF)
     int trsv_r = 0;        // right-hand sides per triangular-solve chain; 0: chosen per solve (ZSOLVE_TRSV_R)
+    // residual mode OZ: digits of A' = [L; Psi; G] (allocated on first use),
+    // their row scales and tensor map; oz_ready while they hold the current
+    // sweep's L, Psi, G
+    void *oz_a = nullptr;
+    int *oz_ea = nullptr;
+    alignas(64) unsigned char oz_amap[128] = {};
+    bool oz_ready = false;
     int resid_mode = ZSOLVE_RESID_F64;
     double *partials = nullptr;
     int nchunks = 0;
@@ -116,6 +123,12 @@ struct zsolve_ctx {
         unsigned *h_status = nullptr;   // pinned copy of the device status word
         int tc_grid = 0;                // CTAs of this lane's tcgen05 launches
         int trsv_grid = 0;              // CTAs of this lane's triangular solves (0: one per SM)
+        // residual mode OZ: digits of x, their scales, the partial products
+        void *oz_x = nullptr;
+        int *oz_ex = nullptr;
+        double *oz_part = nullptr;
+        int oz_ncol_cap = 0;
+        int64_t oz_part_cap = 0;
     };
     Lane lane[kMaxLanes];
     int assembled = 0, factored = 0, fb_ready = 0;
@@ -428,12 +441,69 @@ int fallback_slot(zsolve_ctx *ctx, Lane &ln, int slot, const double2 *b, double2
     return ZSOLVE_OK;
 }
 
+// Workspaces of the residual mode OZ (on first use): the digits of A' and,
+// per lane, those of x for every column a lane can hold (2 S nrhs_max) and
+// partial products for up to four K splits.
+int ensure_oz(zsolve_ctx *ctx) {
+    if (ctx->oz_a) return ZSOLVE_OK;
+    const int64_t n = ctx->n, n_pad = zs_oz_n_pad(n);
+    const int ncol_cap = zs_oz_ncol_alloc(2 * ctx->S * ctx->nrhs_max);
+    bool ok = cudaMalloc(&ctx->oz_a, (size_t)8 * 3 * n * n_pad * 2) == cudaSuccess &&
+              cudaMalloc(&ctx->oz_ea, (size_t)3 * n * sizeof(int)) == cudaSuccess &&
+              zs_oz_a_map(ctx->oz_a, n, ctx->oz_amap) == cudaSuccess;
+    for (auto &ln : ctx->lane) {
+        if (!ok) break;
+        ln.oz_ncol_cap = ncol_cap;
+        ln.oz_part_cap = (int64_t)4 * 3 * n * ncol_cap;
+        ok = cudaMalloc(&ln.oz_x, (size_t)8 * ncol_cap * n_pad * 2) == cudaSuccess &&
+             cudaMalloc(&ln.oz_ex, (size_t)ncol_cap * sizeof(int)) == cudaSuccess &&
+             cudaMalloc(&ln.oz_part, (size_t)ln.oz_part_cap * sizeof(double)) == cudaSuccess;
+    }
+    if (!ok) {
+        cudaGetLastError();
+        cudaFree(ctx->oz_a);
+        cudaFree(ctx->oz_ea);
+        ctx->oz_a = nullptr;
+        ctx->oz_ea = nullptr;
+        for (auto &ln : ctx->lane) {
+            cudaFree(ln.oz_x);
+            cudaFree(ln.oz_ex);
+            cudaFree(ln.oz_part);
+            ln.oz_x = nullptr;
+            ln.oz_ex = nullptr;
+            ln.oz_part = nullptr;
+        }
+        return fail(ctx, ZSOLVE_ENOMEM, "residual mode OZ: workspace allocation failed (n=%lld)", (long long)n);
+    }
+    return ZSOLVE_OK;
+}
+
+// The digits of A' = [L; Psi; G] on `st`.  While a host-pointer sweep's inputs
+// are still being copied, band by band behind the copies (as the assembly).
+int oz_split_inputs(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, cudaStream_t st) {
+    ZS_TRY(ensure_oz(ctx));
+    StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL, st);
+    const int nb = ctx->nband > 0 ? ctx->nband : 1;
+    for (int bnd = 0; bnd < nb; bnd++) {
+        const int64_t r0 = ctx->n * bnd / nb, r1 = ctx->n * (bnd + 1) / nb;
+        if (ctx->nband > 0) ZS_CU(cudaStreamWaitEvent(st, ctx->band_ev[bnd], 0));
+        ZS_CU(zs_launch_oz_split_a(L, Psi, G, ctx->n, r0, r1, ctx->oz_a, ctx->oz_ea, st));
+    }
+    sp.done(nb);
+    return ZSOLVE_OK;
+}
+
 // r = b - Z x for the listed slots in the context's residual arithmetic.
 int residual_slots(zsolve_ctx *ctx, Lane &ln, const double2 *b, const double2 *x, int64_t x_stride, int nrhs,
                    float2 *o64, int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot,
                    StageSpan *sp) {
     const int64_t n = ctx->n;
-    if (ctx->resid_mode == ZSOLVE_RESID_LPG && ctx->cur_L) {
+    if (ctx->resid_mode == ZSOLVE_RESID_OZ && ctx->oz_ready) {
+        ZS_CU(zs_launch_residual_oz(ctx->oz_amap, ctx->oz_ea, n, ctx->d_params, b, x, x_stride, nrhs, o64, o64s, o128,
+                                    o128s, slots, nslot, ln.oz_x, ln.oz_ex, ln.oz_ncol_cap, ln.oz_part,
+                                    ln.oz_part_cap, ctx->d_status, ctx->num_sms, ln.stream));
+        sp->done(3);
+    } else if (ctx->resid_mode == ZSOLVE_RESID_LPG && ctx->cur_L) {
         ZS_CU(zs_launch_residual_lpg(ctx->cur_L, ctx->cur_Psi, ctx->cur_G, n, ctx->d_params, b, x, x_stride, nrhs, o64,
                                      o64s, o128, o128s, slots, nslot, ln.stream));
         sp->done(nrhs);
@@ -758,8 +828,16 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
     ctx->cur_G = G;
     struct Clear {  // the pointers are borrowed for this call only
         zsolve_ctx *c;
-        ~Clear() { c->cur_L = c->cur_Psi = c->cur_G = nullptr; }
+        ~Clear() {
+            c->cur_L = c->cur_Psi = c->cur_G = nullptr;
+            c->oz_ready = false;
+        }
     } clear_ptrs{ctx};
+    if (ctx->resid_mode == ZSOLVE_RESID_OZ && nf > 0) {
+        // before every lane's work: the other lanes start after lane 0's assembly
+        ZS_TRY(oz_split_inputs(ctx, L, Psi, G, ctx->lane[0].stream));
+        ctx->oz_ready = true;
+    }
     if (ctx->opts.gemm == ZSOLVE_GEMM_AUTO && !ctx->probe.done && nf > 0) {
         // the host-pointer sweep's inputs may still be in flight: the probe's
         // assembly waits for every band, the sweep's first one then runs plain
@@ -896,6 +974,8 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->xl);
     cudaFree(c->xe);
     cudaFree(c->zexp);
+    cudaFree(c->oz_a);
+    cudaFree(c->oz_ea);
     cudaFree(c->partials);
     cudaFree(c->d_relcorr);
     cudaFreeHost(c->h_relcorr);
@@ -925,6 +1005,9 @@ void free_all(zsolve_ctx *c) {
         cudaFree(ln.ticket);
         cudaFree(ln.tile_ctr);
         cudaFreeHost(ln.h_status);
+        cudaFree(ln.oz_x);
+        cudaFree(ln.oz_ex);
+        cudaFree(ln.oz_part);
         for (auto &e : ln.ev)
             if (e) cudaEventDestroy(e);
         if (ln.ev_fork) cudaEventDestroy(ln.ev_fork);
@@ -976,7 +1059,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (ctx->opts.outer_block == 0) ctx->opts.outer_block = ZS_NB;
     if (ctx->opts.outer_block != ZS_NB || ctx->opts.max_iter < 0 || !(ctx->opts.tol > 0.0) || ctx->opts.gemm < 0 ||
         ctx->opts.gemm > ZSOLVE_GEMM_FFMA || ctx->opts.batch < 0 || ctx->opts.resid < 0 ||
-        ctx->opts.resid > ZSOLVE_RESID_LPG || ctx->opts.lanes < 0 || ctx->opts.lanes > 3 || ctx->opts.symmetric < 0 ||
+        ctx->opts.resid > ZSOLVE_RESID_OZ || ctx->opts.lanes < 0 || ctx->opts.lanes > 3 || ctx->opts.symmetric < 0 ||
         ctx->opts.symmetric > 1 || ctx->opts.wait_limit < 0) {
         delete ctx;
         return ZSOLVE_EINVAL;
@@ -1084,8 +1167,11 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
         cudaMemset(ctx->dinv, 0, (size_t)S * ctx->dinv_stride * sizeof(float)) != cudaSuccess ||
         (ctx->winv && cudaMemset(ctx->winv, 0, (size_t)S * ZS_WINV_STRIDE * sizeof(float)) != cudaSuccess))
         return bail(ZSOLVE_ECUDA);
-    ctx->resid_mode = (ctx->opts.resid == ZSOLVE_RESID_FX || ctx->opts.resid == ZSOLVE_RESID_LPG) ? ctx->opts.resid
-                                                                                                  : ZSOLVE_RESID_F64;
+    ctx->resid_mode = (ctx->opts.resid == ZSOLVE_RESID_FX || ctx->opts.resid == ZSOLVE_RESID_LPG ||
+                       ctx->opts.resid == ZSOLVE_RESID_OZ)
+                          ? ctx->opts.resid
+                          : ZSOLVE_RESID_F64;
+    if (ctx->opts.resid == ZSOLVE_RESID_OZ && ensure_oz(ctx) != ZSOLVE_OK) return bail(ZSOLVE_ENOMEM);
     if (ctx->opts.resid == ZSOLVE_RESID_FX) {
         if (cudaMalloc(&ctx->xl, (size_t)S * nrhs_max * zs_fx_x_bytes(n)) != cudaSuccess ||
             cudaMalloc(&ctx->xe, (size_t)S * nrhs_max * sizeof(int)) != cudaSuccess ||
@@ -1239,6 +1325,24 @@ int zsolve_residual_lpg(zsolve_ctx *ctx, const double *L, const double *Psi, con
     sp.done(nrhs);
     ZS_CU(cudaStreamSynchronize(ctx->stream));
     return ZSOLVE_OK;
+}
+
+int zsolve_residual_oz(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, const void *b,
+                       const void *x, void *r, int nrhs) {
+    if (!ctx || !L || !Psi || !G || !b || !x || !r) return fail(ctx, ZSOLVE_EINVAL, "NULL argument");
+    ZS_TRY(check_nrhs(ctx, nrhs));
+    if (!ctx->assembled) return fail(ctx, ZSOLVE_ESTATE, "zsolve_residual_oz before zsolve_assemble");
+    ctx->h_params[0] = ctx->single;  // slot 0 holds the single system's frequency again
+    ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
+    ZS_TRY(oz_split_inputs(ctx, L, Psi, G, ctx->stream));
+    Lane &ln = ctx->lane[0];
+    StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL, ctx->stream);
+    ZS_CU(zs_launch_residual_oz(ctx->oz_amap, ctx->oz_ea, ctx->n, ctx->d_params, (const double2 *)b,
+                                (const double2 *)x, 0, nrhs, nullptr, 0, (double2 *)r, 0, ctx->d_all, 1, ln.oz_x,
+                                ln.oz_ex, ln.oz_ncol_cap, ln.oz_part, ln.oz_part_cap, ctx->d_status, ctx->num_sms,
+                                ctx->stream));
+    sp.done(3);
+    return check_device_status(ctx, ln);  // synchronises
 }
 
 int zsolve_lowprec_solve(zsolve_ctx *ctx, const void *v, void *d, int nrhs) {

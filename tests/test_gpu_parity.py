@@ -242,12 +242,115 @@ def test_residual_lpg_against_oracle(zs, torch, n, nrhs):
         s.close()
 
 
-@pytest.mark.parametrize("resid", ["FX", "LPG"])
+U64 = 2.0 ** -53
+
+
+def _lpg_scale(wl, X):
+    w = wl.omega[0]
+    terms = w * np.abs(wl.L) + np.abs(wl.Psi) / w + abs(wl.zs[0]) * np.abs(wl.G)
+    return np.abs(X) @ terms.T + np.abs(wl.B)
+
+
+def _oz_bound(wl, X):
+    """Error bound of the tensor-core residual (mode OZ), per entry of r:
+    the float64 combination's, as for the L, Psi, G residual, plus the
+    splitting's.  For one product sum Y_i = sum_j a_ij x_j (a row of L, Psi
+    or G; the real or imaginary part of x) the 8 digits of 7 bits keep every
+    entry to 2^-55 of its row's (column's) largest |entry|, and the digit
+    products left out (levels k_a + k_x >= 8, at most 15 - l pairs of digits
+    |d| <= 64 at weight 2^(7 (14 - l))) add at most 2^-51.2 max|a| max|x| per
+    term: below 2^-49 n max_j|a_ij| max|x| in all.  A residual component
+    combines w Y_L, Y_Psi / w and both parts of Zs Y_G."""
+    n = wl.n
+    w, z = wl.omega[0], abs(wl.zs[0])
+    amax = w * np.abs(wl.L).max(axis=1) + np.abs(wl.Psi).max(axis=1) / w + 2 * z * np.abs(wl.G).max(axis=1)
+    xmax = np.maximum(np.abs(X.real).max(axis=1), np.abs(X.imag).max(axis=1))
+    return 4 * (n + 4) * 2.3e-16 * _lpg_scale(wl, X) + 2.0 ** -49 * n * np.outer(xmax, amax) + 1e-300
+
+
+def _oz_residual(zs, torch, wl, X):
+    n, nrhs = wl.n, X.shape[0]
+    s = zs.Solver(n, nrhs)
+    try:
+        L, P, G = dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G)
+        zs.zsolve_assemble(s.ctx, L, P, G, wl.omega[0], wl.zs[0].real, wl.zs[0].imag)
+        b, x = dev(torch, wl.B), dev(torch, X)
+        r = torch.empty_like(b)
+        zs.zsolve_residual_oz(s.ctx, L, P, G, b, x, r)
+        return r.cpu().numpy()
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("n,nrhs", [(1, 1), (7, 1), (64, 2), (129, 1), (237, 3), (300, 16), (2157, 1), (1000, 5)])
+def test_residual_oz_against_oracle(zs, torch, n, nrhs):
+    wl = workload.make_small(n, seed=130 + n, nf=1, nrhs=nrhs)
+    X = workload.random_rhs(n, nrhs, seed=8)
+    R = _oz_residual(zs, torch, wl, X)
+    Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0])
+    ref = oracle.residual(Z, X, wl.B)
+    err = np.abs(R - ref)
+    assert np.all(err <= _oz_bound(wl, X)), (err / _oz_bound(wl, X)).max()
+    # and in practice at the float64 level of the terms (a dropped digit
+    # level or a wrong scale would show far above this)
+    assert err.max() <= 64 * U64 * _lpg_scale(wl, X).max()
+
+
+@pytest.mark.parametrize("kind", ["dense_g", "x_spread", "z_spread", "x_zero"])
+@pytest.mark.parametrize("n,nrhs", [(33, 1), (300, 2), (1000, 4)])
+def test_residual_oz_edge_cases(zs, torch, kind, n, nrhs):
+    wl, X = _fx_case(kind, n, nrhs)
+    R = _oz_residual(zs, torch, wl, X)
+    Z = oracle.assemble(wl.L, wl.Psi, wl.G, wl.omega[0], wl.zs[0])
+    ref = oracle.residual(Z, X, wl.B)
+    assert np.all(np.abs(R - ref) <= _oz_bound(wl, X))
+    if kind == "x_zero":
+        assert np.array_equal(R[0], wl.B[0])
+
+
+def test_residual_oz_non_finite(zs, torch):
+    # a NaN in x (or an infinity in a row of L) gives NaN residuals there, so
+    # that the refinement sees a non-finite correction and stops
+    n, nrhs = 200, 2
+    wl = workload.make_small(n, seed=7, nf=1, nrhs=nrhs)
+    X = workload.random_rhs(n, nrhs, seed=9)
+    X[0, 17] = complex(np.nan, 0.0)
+    R = _oz_residual(zs, torch, wl, X)
+    assert np.all(np.isnan(R[0]))
+    assert np.all(np.isfinite(R[1]))
+    L = wl.L.copy()
+    L[5, 9] = np.inf
+    wl2 = workload.Workload(wl.points, L, wl.Psi, wl.G, wl.freqs, wl.omega, wl.zs, wl.B, None)
+    X[0, 17] = 1.0
+    R = _oz_residual(zs, torch, wl2, X)
+    assert np.all(np.isnan(R[:, 5])) and np.all(np.isfinite(np.delete(R, 5, axis=1)))
+
+
+@pytest.mark.parametrize("resid", ["FX", "LPG", "OZ"])
 @pytest.mark.parametrize("n,nrhs,nf", [(130, 2, 3), (700, 1, 3), (301, 4, 2), (1, 1, 2), (257, 1, 9)])
 def test_sweep_parity_fixed_point_and_lpg_residual(zs, torch, n, nrhs, nf, resid):
     wl = workload.make_small(n, seed=85 + n, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
     ref = oracle.solve_sweep(wl)
     s = zs.Solver(n, nrhs, resid=getattr(zs, "ZSOLVE_RESID_" + resid))
+    try:
+        x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+        infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
+                                dev(torch, wl.B), x)
+        X = x.cpu().numpy()
+        for f in range(nf):
+            assert infos[f].status == 0 and infos[f].fallback == 0, infos[f].as_dict()
+            assert np.all(rel_err(X[f], ref[f]) <= PARITY), (f, rel_err(X[f], ref[f]))
+    finally:
+        s.close()
+
+
+@pytest.mark.parametrize("n,nrhs,nf,batch,lanes", [(300, 1, 20, 20, 1), (257, 4, 6, 6, 2), (130, 3, 12, 12, 3)])
+def test_sweep_parity_oz_many_columns(zs, torch, n, nrhs, nf, batch, lanes):
+    # more than 32 columns of x in one evaluation (several column groups),
+    # several right-hand sides per slot, and three lanes
+    wl = workload.make_small(n, seed=140 + n, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
+    ref = oracle.solve_sweep(wl)
+    s = zs.Solver(n, nrhs, batch=batch, lanes=lanes, resid=zs.ZSOLVE_RESID_OZ)
     try:
         x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
         infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
@@ -461,9 +564,12 @@ def test_sweep_term_isolation_parity(zs, torch):
         s.close()
 
 
-def test_sweep_host_matches_device(zs, torch):
+@pytest.mark.parametrize("resid", ["F64", "OZ"])
+def test_sweep_host_matches_device(zs, torch, resid):
+    # the host-pointer sweep copies L, Psi, G in row bands that the first
+    # assembly (and the OZ residual's digits of L, Psi, G) follow band by band
     wl = workload.make_small(200, seed=50, nf=3, nrhs=2)
-    s = zs.Solver(200, 2, gemm=zs.ZSOLVE_GEMM_FFMA)
+    s = zs.Solver(200, 2, gemm=zs.ZSOLVE_GEMM_FFMA, resid=getattr(zs, "ZSOLVE_RESID_" + resid))
     try:
         x = torch.empty((3, 2, 200), dtype=torch.complex128, device="cuda")
         zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
@@ -571,7 +677,7 @@ def test_argument_errors(zs, torch):
 
 
 @pytest.mark.parametrize("gemm,resid", [("FFMA", "F64"), ("TF32X3", "F64"), ("TF32X3", "DF"), ("TF32X3", "FX"),
-                                        ("TF32X3", "LPG")])
+                                        ("TF32X3", "LPG"), ("TF32X3", "OZ")])
 def test_config1_full_sweep_every_frequency(zs, torch, config1_oracle, gemm, resid):
     """N=2157, all 21 frequencies in one batched sweep (as the benchmark runs
     it): the oracle's direct solve at every frequency, element by element to
