@@ -200,10 +200,15 @@ cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int
                                const int *slots, int nslot, unsigned *ctr, unsigned *status, int max_grid,
                                cudaStream_t st);
 // L21 = A21 U11^-1 and U12 = L11^-1 A12 from the packs of zs_launch_pack_trsm
-// and zs_launch_diag_block; writes L21, U12 into z32 and their operand packs
+// and zs_launch_diag_block; writes L21, U12 into z32 and their operand packs.
+// sym: Z complex symmetric (A12 = A21^T, U11 = D11 L11^T): one product per row
+// tile, U12^T = A21 L11^-T, and L21 = U12^T D11^-1 with D11^-1 the diagonal of
+// the float32 inverse blocks (dinv, per slot dinv_stride floats); the packs
+// then need only A21's rows in the A planes.
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
-                              int64_t J, int split, const int *slots, int nslot, unsigned *ctr, unsigned *status,
-                              int num_sms, cudaStream_t st);
+                              int64_t J, int split, int sym, const float *dinv, int64_t dinv_stride,
+                              const int *slots, int nslot, unsigned *ctr, unsigned *status, int num_sms,
+                              cudaStream_t st);
 
 // Pack layout (floats), per slot: six planes of n rows x 2*NB:
 //   A_hi, A_lo, Br_hi, Br_lo, Bi_hi, Bi_lo

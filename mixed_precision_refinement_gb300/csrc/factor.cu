@@ -47,6 +47,19 @@ __device__ __forceinline__ void pack_put(float *hi, float *lo, int64_t off, floa
     }
 }
 
+// Four consecutive floats of an operand pack (16-byte aligned offset).
+__device__ __forceinline__ void pack_put4(float *hi, float *lo, int64_t off, float4 v, int mode) {
+    if (mode == 0) {
+        *reinterpret_cast<float4 *>(hi + off) = v;
+        return;
+    }
+    const float4 h = make_float4(tf32_rna(v.x), tf32_rna(v.y), tf32_rna(v.z), tf32_rna(v.w));
+    *reinterpret_cast<float4 *>(hi + off) = h;
+    if (mode == 2)
+        *reinterpret_cast<float4 *>(lo + off) =
+            make_float4(tf32_rna(v.x - h.x), tf32_rna(v.y - h.y), tf32_rna(v.z - h.z), tf32_rna(v.w - h.w));
+}
+
 // ---------------------------------------------------------------- L21 = A21 U11^-1
 
 // Both block solves run in four 32-column steps with the inverted 32x32
@@ -378,7 +391,8 @@ k_schur_simt(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
 
 // Operand packs of the block triangular solves (blockIdx.y = 0: rows of A21
 // into the A planes; 1: columns of A12, transposed through shared memory,
-// into the Br planes), 32 rows or columns per CTA.
+// into the Br planes), 32 rows or columns per CTA.  sym: only the A planes
+// (the symmetric block solve takes A12^T = A21 from them).
 constexpr int kPackThreads = 256;
 
 __global__ void __launch_bounds__(kPackThreads)
@@ -393,16 +407,14 @@ k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z3
     const int64_t r0 = J + NB + 32 * (int64_t)blockIdx.x;
     const int tid = threadIdx.x;
     if (blockIdx.y == 0) {
-        // sym: the matrix is complex symmetric and only its lower part is
-        // kept up to date, so A12^T(j, k) = A21(j, k): the Br planes hold the
-        // same rows as the A planes
-        for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
-            const int r = idx >> 8, k = idx & (ZS_PACK_K - 1);
+        // four consecutive k per thread: 16-byte loads (ld and J are multiples
+        // of 32 floats) and stores (pack rows of 256 floats)
+        for (int idx = tid; idx < 32 * ZS_PACK_K / 4; idx += kPackThreads) {
+            const int r = idx >> 6, k = 4 * (idx & (ZS_PACK_K / 4 - 1));
             const int64_t i = r0 + r;
             if (i >= n) break;  // later idx only move to later rows
-            const float v = (k < NB ? re : im)[i * ld + J + (k & (NB - 1))];
-            pack_put(pk, pk + pp, i * ZS_PACK_K + k, v, mode);
-            if (sym) pack_put(pk + 2 * pp, pk + 3 * pp, i * ZS_PACK_K + k, v, mode);
+            const float4 v = *reinterpret_cast<const float4 *>((k < NB ? re : im) + i * ld + J + (k & (NB - 1)));
+            pack_put4(pk, pk + pp, i * ZS_PACK_K + k, v, mode);
         }
     } else {
         for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {

@@ -72,7 +72,16 @@ enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_BI_HI = 2, WP_BI_LO = 3, WP_V = 4 };
 // KIND_SCHUR_LOWER: the trailing update of a complex-symmetric matrix, whose
 // Schur complement stays symmetric: only the tiles on and below the diagonal
 // (column tile <= row tile) are formed; the next step reads only those.
-enum { KIND_SCHUR = 0, KIND_TRSM = 1, KIND_SCHUR_LOWER = 2 };
+// KIND_TRSM_SYM: the block solves of a complex-symmetric matrix in one
+// product per row tile: with A12 = A21^T and U11 = D11 L11^T (D11 = diag U11),
+// U12^T = A21 L11^-T from the MMAs, and L21 = A21 U11^-1 = U12^T D11^-1 in the
+// epilogue, which writes both (half the MMAs and operand loads of KIND_TRSM).
+enum { KIND_SCHUR = 0, KIND_TRSM = 1, KIND_SCHUR_LOWER = 2, KIND_TRSM_SYM = 3 };
+
+template <int KIND>
+constexpr bool is_trsm() {
+    return KIND == KIND_TRSM || KIND == KIND_TRSM_SYM;
+}
 
 constexpr int EPI_BOX = 32 * 32 * 4;  // one 32-row x 32-column fp32 box (4 KB)
 constexpr int EPI_BYTES = 4 * 2 * EPI_BOX;  // 4 epilogue warps x 2 staging buffers
@@ -252,14 +261,18 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 }
 
 // Tile t of the launch: frequency slot, output row tile, column tile
-// (KIND_SCHUR) or solve (KIND_TRSM: 0 = L21, 1 = U12^T, interleaved).
+// (KIND_SCHUR) or solve (KIND_TRSM: 0 = L21, 1 = U12^T, interleaved;
+// KIND_TRSM_SYM: both from one product per row tile).
 struct Tile {
     int slot, ra, u, rb;
 };
 
 template <int KIND>
 __host__ __device__ __forceinline__ int tiles_per_slot(int tiles) {
-    return KIND == KIND_SCHUR ? tiles * tiles : KIND == KIND_SCHUR_LOWER ? tiles * (tiles + 1) / 2 : 2 * tiles;
+    return KIND == KIND_SCHUR         ? tiles * tiles
+           : KIND == KIND_SCHUR_LOWER ? tiles * (tiles + 1) / 2
+           : KIND == KIND_TRSM_SYM    ? tiles
+                                      : 2 * tiles;
 }
 
 template <int KIND>
@@ -277,6 +290,10 @@ __device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const in
         x.ra = (int)(base + (int64_t)tm * TM);
         x.rb = (int)(base + (int64_t)tn * TN);
         x.u = 0;
+    } else if (KIND == KIND_TRSM_SYM) {
+        x.ra = (int)(base + (int64_t)rem * TM);
+        x.rb = 0;
+        x.u = 0;
     } else if (KIND == KIND_SCHUR) {
         const int tm = rem / tiles, tn = rem - tm * tiles;
         x.ra = (int)(base + (int64_t)tm * TM);
@@ -290,13 +307,15 @@ __device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const in
     return x;
 }
 
-// tmap: operand packs (boxes 32 x 128); wmap: inverse packs (KIND_TRSM);
-// cmap: float32 matrices (boxes 32 x 32); pmap: operand packs (boxes 32 x 32, KIND_TRSM stores).
+// tmap: operand packs (boxes 32 x 128); wmap: inverse packs (block solves);
+// cmap: float32 matrices (boxes 32 x 32); pmap: operand packs (boxes 32 x 32, block-solve stores);
+// dinv (KIND_TRSM_SYM): the float32 inverse diagonal blocks, per slot dinv_stride floats.
 template <int SPLIT, int KIND>
 __global__ void __launch_bounds__(kThreads, 1)
 k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap wmap,
            const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap pmap, int64_t n, int64_t J,
-           const int *__restrict__ slots, int nslot, unsigned *__restrict__ ctr, unsigned *__restrict__ status) {
+           const int *__restrict__ slots, int nslot, unsigned *__restrict__ ctr, unsigned *__restrict__ status,
+           const float *__restrict__ dinv, int64_t dinv_stride) {
     using C = Cfg<SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[C::STAGES], bar_empty[C::STAGES], bar_accf[2], bar_acce[2], bar_drain;
@@ -341,7 +360,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         // ------------------------------------------------ TMA producer
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&tmap) : "memory");
-            if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&wmap) : "memory");
+            if (is_trsm<KIND>()) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&wmap) : "memory");
             // Tiles are taken dynamically: the first is blockIdx.x, the next
             // ones come from the launch's counter, so CTAs that start late
             // (the SMs busy with another stream's kernel) simply take fewer.
@@ -364,9 +383,10 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 // A rows: L21 / A21 (A planes) or A12^T (Br planes); B: the pack's
                 // own Br/Bi rows, or W / V from the inverse packs
                 const int pa = (KIND == KIND_TRSM && x.u) ? PL_BR_HI : PL_A_HI;
-                const CUtensorMap *bm = KIND != KIND_TRSM ? &tmap : &wmap;
-                const int pbr = KIND != KIND_TRSM ? PL_BR_HI : (x.u ? WP_V : 0) + WP_BR_HI;
-                const int pbi = KIND != KIND_TRSM ? PL_BI_HI : (x.u ? WP_V : 0) + WP_BI_HI;
+                const bool use_v = KIND == KIND_TRSM_SYM || x.u;  // B = L11^-1 (else U11^-1)
+                const CUtensorMap *bm = !is_trsm<KIND>() ? &tmap : &wmap;
+                const int pbr = !is_trsm<KIND>() ? PL_BR_HI : (use_v ? WP_V : 0) + WP_BR_HI;
+                const int pbi = !is_trsm<KIND>() ? PL_BI_HI : (use_v ? WP_V : 0) + WP_BI_HI;
                 bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
@@ -409,13 +429,17 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 // the first stage of the next tile (or the end marker) tells which
                 const uint32_t st0 = g % C::STAGES, ph0 = (g / C::STAGES) & 1u;
                 if (!mbar_wait(smem_u32(&bar_full[st0]), ph0, &s_abort, status, 2u | (KIND << 4))) break;
-                if (s_tq[it % kTq] < 0) {
-                    g++;
-                    mbar_arrive(smem_u32(&bar_accf[it & 1u]));  // the epilogue's turn to see the end
-                    break;
-                }
+                // the accumulator buffer must be free (the epilogue has read the
+                // tile two back) also before the end marker completes its next
+                // phase: otherwise a slow epilogue could find that barrier two
+                // phases on, with the parity it waits for, and wait for ever
                 const uint32_t buf = it & 1u, aph = (it >> 1) & 1u;
                 if (!mbar_wait(smem_u32(&bar_acce[buf]), aph ^ 1u, &s_abort, status, 3u | (KIND << 4))) break;
+                if (s_tq[it % kTq] < 0) {
+                    g++;
+                    mbar_arrive(smem_u32(&bar_accf[buf]));  // the epilogue's turn to see the end
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t d = tmem + buf * 256u;
                 bool ok = true;
@@ -476,7 +500,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
         };
         if (lane == 0) {
             asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&cmap) : "memory");
-            if (KIND == KIND_TRSM) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&pmap) : "memory");
+            if (is_trsm<KIND>()) asm volatile("prefetch.tensormap [%0];" ::"l"((uint64_t)&pmap) : "memory");
         }
         for (;; it++) {
             const bool okq = mbar_wait(smem_u32(&bar_tq[it % kTq]), (it / kTq) & 1u, &s_abort, status, 4u | (KIND << 4));
@@ -488,6 +512,103 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
             tc_fence_after();
             const Tile x = tile_of<KIND>(t, tiles, base, slots);
             const int row0 = x.ra + quad * 32;  // this warp's 32 output rows
+            if (KIND == KIND_TRSM_SYM) {
+                // The accumulator holds U12^T for the tile's rows (Re in chunks
+                // 0-3, Im in chunks 4-7); per group of 32 columns both parts.
+                // D11^-1 is the diagonal of U11^-1 (an upper triangle's inverse
+                // has the reciprocal diagonal), taken from the float32 inverses.
+                const float *dre = dinv + (int64_t)x.slot * dinv_stride + (J / NB) * 4 * NB * NB + 2 * NB * NB;
+                const float *dim = dre + NB * NB;
+#pragma unroll 1
+                for (int g = 0; g < 4; g++) {
+                    float vr[32], vi[32];
+                    const uint32_t tl = tmem + buf * 256u + ((uint32_t)(quad * 32) << 16);
+                    tmem_ld32(tl + (uint32_t)(g * 32), vr);
+                    tmem_ld32(tl + (uint32_t)((g + 4) * 32), vi);
+                    if (g == 3) {  // accumulator fully read: hand it back to the MMA warp
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
+                    }
+                    const int c32 = g * 32;
+#pragma unroll
+                    for (int part = 0; part < 2; part++) {
+                        const float(&v)[32] = part ? vi : vr;
+                        // U12(J + c32 + t, i) into the float32 factor (transposed boxes)
+                        uint32_t sb = next_box();
+                        stage_col(sb, lane, v);
+                        publish();
+                        if (lane == 0) {
+                            tma_store_4d(&cmap, sb, row0, (int)J + c32, part, x.slot);
+                            bulk_commit();
+                        }
+                        // trailing-update operand rows: Br = [Re U12^T | -Im U12^T], Bi = [Im U12^T | Re U12^T]
+                        float h[32];
+#pragma unroll
+                        for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q]);
+#pragma unroll 1
+                        for (int lo = 0; lo <= SPLIT; lo++) {
+                            if (lo) {
+#pragma unroll
+                                for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q] - h[q]);
+                            }
+                            sb = next_box();
+                            stage_row(sb, lane, h, part ? -1.f : 1.f);
+                            publish();
+                            if (lane == 0) {
+                                tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_BR_HI + lo, x.slot);
+                                bulk_commit();
+                            }
+                            sb = next_box();
+                            stage_row(sb, lane, h, 1.f);
+                            publish();
+                            if (lane == 0) {
+                                tma_store_4d(&pmap, sb, (1 - part) * NB + c32, row0, PL_BI_HI + lo, x.slot);
+                                bulk_commit();
+                            }
+                        }
+                    }
+                    // L21(i, J + c32 + t) = U12^T(i, c32 + t) * D11^-1(c32 + t)
+#pragma unroll
+                    for (int q = 0; q < 32; q++) {
+                        const int k = c32 + q;
+                        const float dr = __ldg(dre + k * (NB + 1)), di = __ldg(dim + k * (NB + 1));
+                        const float a = vr[q], b = vi[q];
+                        vr[q] = fmaf(a, dr, -b * di);
+                        vi[q] = fmaf(a, di, b * dr);
+                    }
+#pragma unroll
+                    for (int part = 0; part < 2; part++) {
+                        const float(&v)[32] = part ? vi : vr;
+                        uint32_t sb = next_box();
+                        stage_row(sb, lane, v, 1.f);
+                        publish();
+                        if (lane == 0) {
+                            tma_store_4d(&cmap, sb, (int)J + c32, row0, part, x.slot);
+                            bulk_commit();
+                        }
+                        // next step's block-solve operand rows: A = [Re L21 | Im L21]
+                        float h[32];
+#pragma unroll
+                        for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q]);
+#pragma unroll 1
+                        for (int lo = 0; lo <= SPLIT; lo++) {
+                            if (lo) {
+#pragma unroll
+                                for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q] - h[q]);
+                            }
+                            sb = next_box();
+                            stage_row(sb, lane, h, 1.f);
+                            publish();
+                            if (lane == 0) {
+                                tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_A_HI + lo, x.slot);
+                                bulk_commit();
+                            }
+                        }
+                    }
+                }
+                continue;
+            }
 #pragma unroll 1
             for (int c = 0; c < 8; c++) {
                 float v[32];
@@ -580,7 +701,8 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 template <int SPLIT, int KIND>
 cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const CUtensorMap &cmap,
                         const CUtensorMap &pmap, int64_t n, int64_t J, const int *slots, int nslot, unsigned *ctr,
-                        unsigned *status, int max_grid, cudaStream_t st) {
+                        unsigned *status, int max_grid, cudaStream_t st, const float *dinv = nullptr,
+                        int64_t dinv_stride = 0) {
     using C = Cfg<SPLIT>;
     // once per process (thread-safe initialisation of a local static)
     static const cudaError_t attr = cudaFuncSetAttribute(k_cgemm_tc<SPLIT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -592,7 +714,7 @@ cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const 
     if (total <= 0) return cudaSuccess;
     const int grid = (int)(total < max_grid ? total : max_grid);
     k_cgemm_tc<SPLIT, KIND><<<grid, kThreads, C::SMEM, st>>>(tmap, wmap, cmap, pmap, n, J, slots, nslot, ctr,
-                                                             status);
+                                                             status, dinv, dinv_stride);
     return cudaGetLastError();
 }
 
@@ -654,13 +776,21 @@ cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int
 }
 
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
-                              int64_t J, int split, const int *slots, int nslot, unsigned *ctr, unsigned *status,
-                              int num_sms, cudaStream_t st) {
-    if (!ctr) return cudaErrorInvalidValue;
+                              int64_t J, int split, int sym, const float *dinv, int64_t dinv_stride,
+                              const int *slots, int nslot, unsigned *ctr, unsigned *status, int num_sms,
+                              cudaStream_t st) {
+    if (!ctr || (sym && !dinv)) return cudaErrorInvalidValue;
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
     const CUtensorMap &w = *reinterpret_cast<const CUtensorMap *>(wmap);
     const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
     const CUtensorMap &p = *reinterpret_cast<const CUtensorMap *>(pmap);
+    if (sym) {
+        if (split)
+            return launch_kind<1, KIND_TRSM_SYM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st, dinv,
+                                                 dinv_stride);
+        return launch_kind<0, KIND_TRSM_SYM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st, dinv,
+                                             dinv_stride);
+    }
     if (split) return launch_kind<1, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
     return launch_kind<0, KIND_TRSM>(m, w, c, p, n, J, slots, nslot, ctr, status, num_sms, st);
 }

@@ -74,6 +74,7 @@ struct zsolve_ctx {
     int *zexp = nullptr;   // residual mode FX: per slot and row of Z64, its largest exponent
     int fx_ndf = 1;        // residual mode FX: sub-steps of four taken in float64 (ZSOLVE_FX_NDF)
     int trsv_r = 0;        // right-hand sides per triangular-solve chain; 0: chosen per solve (ZSOLVE_TRSV_R)
+    int tc_cap = 0;        // testing aid: at most this many CTAs per tcgen05 launch (ZSOLVE_TC_GRID; 0: no cap)
     // residual mode OZ: digits of A' = [L; Psi; G] (allocated on first use),
     // their row scales and tensor map; oz_ready while they hold the current
     // sweep's L, Psi, G
@@ -293,6 +294,10 @@ int factor_slots_simt(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
 // counters (zeroed once per factorisation).
 constexpr int kMaxCtr = 256;  // tile counters per factorisation (2 per outer block)
 
+int tc_grid(const zsolve_ctx *ctx, const Lane &ln) {
+    return ctx->tc_cap > 0 ? std::min(ln.tc_grid, ctx->tc_cap) : ln.tc_grid;
+}
+
 int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     const int64_t n = ctx->n;
     const int mode = ctx->gemm_eff, split = mode == 2 ? 1 : 0;
@@ -323,13 +328,14 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
         {
             ZS_CU(cudaStreamWaitEvent(ln.stream, ln.ev_join, 0));
             StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.stream);
-            ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J, split, slots,
-                                    nslot, ctr++, ctx->d_status, ln.tc_grid, ln.stream));
+            ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J, split,
+                                    ctx->opts.symmetric, ctx->dinv, ctx->dinv_stride, slots, nslot, ctr++,
+                                    ctx->d_status, tc_grid(ctx, ln), ln.stream));
             sp.done(1);
         }
         StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR, ln.stream);
         ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, split, ctx->opts.symmetric, slots, nslot, ctr++,
-                                 ctx->d_status, ln.tc_grid, ln.stream));
+                                 ctx->d_status, tc_grid(ctx, ln), ln.stream));
         sp.done(1);
     }
     return ZSOLVE_OK;
@@ -1070,6 +1076,8 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ctx->probe.chosen = ctx->opts.gemm == ZSOLVE_GEMM_AUTO ? ZSOLVE_GEMM_TF32X3 : ctx->opts.gemm;
     if (ctx->opts.wait_limit > 0) ctx->wait_limit = (unsigned)ctx->opts.wait_limit;
     if (const char *e = getenv("ZSOLVE_FX_NDF")) ctx->fx_ndf = std::min(3, std::max(0, atoi(e)));
+    // testing aid: few CTAs per tcgen05 launch, so that each takes many tiles
+    if (const char *e = getenv("ZSOLVE_TC_GRID")) ctx->tc_cap = std::max(0, atoi(e));
     // right-hand sides per triangular-solve chain (1, 2 or 4; unset: chosen per solve)
     if (const char *e = getenv("ZSOLVE_TRSV_R")) {
         const int r = atoi(e);

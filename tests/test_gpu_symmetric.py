@@ -127,6 +127,38 @@ def test_symmetric_config1_full_sweep(zs, torch, config1_oracle, sym):
         s.close()
 
 
+@pytest.mark.parametrize("sym", [1, 0])
+@pytest.mark.parametrize("gemm", ["TF32X3", "TF32"])
+def test_tcgen05_many_tiles_per_cta(zs, torch, monkeypatch, gemm, sym):
+    """The tcgen05 launches capped at 2, 3 or 8 CTAs (ZSOLVE_TC_GRID, a
+    testing aid), so that every CTA takes many tiles and the epilogue, the
+    MMA issuer and the loads drift apart by the most their barriers allow:
+    the sweep is bit-identical to the uncapped one (a tile's result does not
+    depend on the CTA that forms it) and matches the oracle."""
+    n, nrhs, nf = 1000, 2, 3
+    wl = workload.make_small(n, seed=77, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
+    ref = oracle.solve_sweep(wl)
+    out = {}
+    for cap in ("", "2", "3", "8"):
+        if cap:
+            monkeypatch.setenv("ZSOLVE_TC_GRID", cap)
+        else:
+            monkeypatch.delenv("ZSOLVE_TC_GRID", raising=False)
+        s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm), batch=nf, symmetric=sym)
+        try:
+            x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+            infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega,
+                                    wl.zs, dev(torch, wl.B), x)
+            out[cap] = x.cpu().numpy()
+        finally:
+            s.close()
+        assert all(i.status == 0 for i in infos)
+        for f in range(nf):
+            assert np.all(rel_err(out[cap][f], ref[f]) <= PARITY), (cap, f)
+    for cap in ("2", "3", "8"):
+        assert np.array_equal(out[cap], out[""]), cap
+
+
 def test_symmetric_mode_with_a_nonsymmetric_input(zs, torch):
     # G made non-symmetric: the factors are those of the matrix the lower
     # triangle defines, but the float64 residual uses all of Z, so the
