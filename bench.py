@@ -593,7 +593,8 @@ def run_ours(args):
             "k_cgemm_tc", "tensor", tc_ms_tot, tc_launches, tc_flops_tot, tf32_peak, "TFLOP/s",
             f"tf32 = {peak_src} bf16 {peaks['bf16_tflops']} x 1.1/2.25",
             "useful complex-product flops (8 per complex MAC) of the trailing updates and block solves; "
-            "the 3xTF32 split runs 3x that on the pipe", traffic=None)
+            "the 3xTF32 split runs 3x that on the pipe",
+            traffic=profile_traffic("k_cgemm_tc") if (args.config == 1 and args.gemm_eff == "TF32X3") else None)
     else:
         rl["k_schur_simt"] = obj(
             "k_schur_simt", "alu", st["schur"]["ms"], st["schur"]["launches"], schur_f * steps, fp32_peak,
@@ -624,7 +625,8 @@ def run_ours(args):
                                oz_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
                                "48 n^2 bytes of digits per evaluation of a lane's frequencies, plus 72 n^2 per "
                                "sweep to form them; over the residual stage's device time (digit formation, "
-                               "product, combination)", evaluations_per_step=lanes_eval)
+                               "product, combination)", evaluations_per_step=lanes_eval,
+                               traffic_k_oz_gemm=profile_traffic("k_oz_gemm") if args.config == 1 else None)
     else:
         rl["k_residual"] = obj({"F64": "k_residual", "DF": "k_residual_df", "FX": "k_residual_fx",
                                 "LPG": "k_residual_lpg"}[resid_mode], "hbm", st["residual"]["ms"],
