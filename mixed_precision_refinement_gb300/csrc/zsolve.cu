@@ -82,6 +82,10 @@ struct zsolve_ctx {
     int *oz_ea = nullptr;
     alignas(64) unsigned char oz_amap[128] = {};
     bool oz_ready = false;
+    // the sweep forms the digits on a stream of their own, beside the first
+    // assembly; every residual waits for oz_done
+    cudaStream_t oz_stream = nullptr;
+    cudaEvent_t oz_start = nullptr, oz_done = nullptr;
     int resid_mode = ZSOLVE_RESID_F64;
     double *partials = nullptr;
     int nchunks = 0;
@@ -102,7 +106,9 @@ struct zsolve_ctx {
     // the first assembly waits for each band separately
     static constexpr int kBands = 4;
     cudaStream_t copy_stream = nullptr;
+    cudaStream_t copy_aux[2] = {nullptr, nullptr};  // Psi's and G's bands, beside L's
     cudaEvent_t band_ev[kBands] = {}, ev_host = nullptr;
+    cudaEvent_t aux_ev[kBands][2] = {};
     int nband = 0;
     double2 *hd_b = nullptr, *hd_x = nullptr;
     size_t hd_x_cap = 0;
@@ -456,7 +462,10 @@ int ensure_oz(zsolve_ctx *ctx) {
     const int ncol_cap = zs_oz_ncol_alloc(2 * ctx->S * ctx->nrhs_max);
     bool ok = cudaMalloc(&ctx->oz_a, (size_t)8 * 3 * n * n_pad * 2) == cudaSuccess &&
               cudaMalloc(&ctx->oz_ea, (size_t)3 * n * sizeof(int)) == cudaSuccess &&
-              zs_oz_a_map(ctx->oz_a, n, ctx->oz_amap) == cudaSuccess;
+              zs_oz_a_map(ctx->oz_a, n, ctx->oz_amap) == cudaSuccess &&
+              (ctx->oz_stream || cudaStreamCreateWithFlags(&ctx->oz_stream, cudaStreamNonBlocking) == cudaSuccess) &&
+              (ctx->oz_start || cudaEventCreateWithFlags(&ctx->oz_start, cudaEventDisableTiming) == cudaSuccess) &&
+              (ctx->oz_done || cudaEventCreateWithFlags(&ctx->oz_done, cudaEventDisableTiming) == cudaSuccess);
     for (auto &ln : ctx->lane) {
         if (!ok) break;
         ln.oz_ncol_cap = ncol_cap;
@@ -484,10 +493,16 @@ int ensure_oz(zsolve_ctx *ctx) {
     return ZSOLVE_OK;
 }
 
-// The digits of A' = [L; Psi; G] on `st`.  While a host-pointer sweep's inputs
-// are still being copied, band by band behind the copies (as the assembly).
-int oz_split_inputs(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, cudaStream_t st) {
+// The digits of A' = [L; Psi; G], after everything queued so far on `after`,
+// on the digits' own stream, so that the first assembly runs beside them;
+// oz_done marks their end (every residual waits for it).  While a
+// host-pointer sweep's inputs are still being copied, band by band behind the
+// copies (as the assembly).
+int oz_split_inputs(zsolve_ctx *ctx, const double *L, const double *Psi, const double *G, cudaStream_t after) {
     ZS_TRY(ensure_oz(ctx));
+    cudaStream_t st = ctx->oz_stream;
+    ZS_CU(cudaEventRecord(ctx->oz_start, after));
+    ZS_CU(cudaStreamWaitEvent(st, ctx->oz_start, 0));
     StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL, st);
     const int nb = ctx->nband > 0 ? ctx->nband : 1;
     for (int bnd = 0; bnd < nb; bnd++) {
@@ -496,6 +511,7 @@ int oz_split_inputs(zsolve_ctx *ctx, const double *L, const double *Psi, const d
         ZS_CU(zs_launch_oz_split_a(L, Psi, G, ctx->n, r0, r1, ctx->oz_a, ctx->oz_ea, st));
     }
     sp.done(nb);
+    ZS_CU(cudaEventRecord(ctx->oz_done, st));
     return ZSOLVE_OK;
 }
 
@@ -505,6 +521,7 @@ int residual_slots(zsolve_ctx *ctx, Lane &ln, const double2 *b, const double2 *x
                    StageSpan *sp) {
     const int64_t n = ctx->n;
     if (ctx->resid_mode == ZSOLVE_RESID_OZ && ctx->oz_ready) {
+        ZS_CU(cudaStreamWaitEvent(ln.stream, ctx->oz_done, 0));
         ZS_CU(zs_launch_residual_oz(ctx->oz_amap, ctx->oz_ea, n, ctx->d_params, b, x, x_stride, nrhs, o64, o64s, o128,
                                     o128s, slots, nslot, ln.oz_x, ln.oz_ex, ln.oz_ncol_cap, ln.oz_part,
                                     ln.oz_part_cap, ctx->d_status, ctx->num_sms, ln.stream));
@@ -836,6 +853,9 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
         zsolve_ctx *c;
         ~Clear() {
             c->cur_L = c->cur_Psi = c->cur_G = nullptr;
+            // on every exit the context's stream follows the digits of L, Psi,
+            // G (read from the caller's inputs), so that the caller may reuse them
+            if (c->oz_ready) cudaStreamWaitEvent(c->stream, c->oz_done, 0);
             c->oz_ready = false;
         }
     } clear_ptrs{ctx};
@@ -982,6 +1002,9 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->zexp);
     cudaFree(c->oz_a);
     cudaFree(c->oz_ea);
+    if (c->oz_stream) cudaStreamDestroy(c->oz_stream);
+    if (c->oz_start) cudaEventDestroy(c->oz_start);
+    if (c->oz_done) cudaEventDestroy(c->oz_done);
     cudaFree(c->partials);
     cudaFree(c->d_relcorr);
     cudaFreeHost(c->h_relcorr);
@@ -997,6 +1020,11 @@ void free_all(zsolve_ctx *c) {
     cudaFree(c->fb_info);
     cudaFreeHost(c->h_fb_info);
     if (c->copy_stream) cudaStreamDestroy(c->copy_stream);
+    for (auto q : c->copy_aux)
+        if (q) cudaStreamDestroy(q);
+    for (auto &pair : c->aux_ev)
+        for (auto e : pair)
+            if (e) cudaEventDestroy(e);
     for (auto e : c->band_ev)
         if (e) cudaEventDestroy(e);
     if (c->ev_host) cudaEventDestroy(c->ev_host);
@@ -1278,23 +1306,35 @@ int zsolve_sweep_host(zsolve_ctx *ctx, const double *L, const double *Psi, const
     }
     if (!ctx->copy_stream) {
         if (cudaStreamCreateWithFlags(&ctx->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&ctx->copy_aux[0], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaStreamCreateWithFlags(&ctx->copy_aux[1], cudaStreamNonBlocking) != cudaSuccess ||
             cudaEventCreateWithFlags(&ctx->ev_host, cudaEventDisableTiming) != cudaSuccess)
-            return fail(ctx, ZSOLVE_ECUDA, "copy stream for host inputs");
+            return fail(ctx, ZSOLVE_ECUDA, "copy streams for host inputs");
         for (auto &e : ctx->band_ev)
             if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
                 return fail(ctx, ZSOLVE_ECUDA, "copy events for host inputs");
+        for (auto &pair : ctx->aux_ev)
+            for (auto &e : pair)
+                if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess)
+                    return fail(ctx, ZSOLVE_ECUDA, "copy events for host inputs");
     }
     ZS_CU(cudaMemcpyAsync(ctx->hd_b, b, (size_t)nrhs * n * sizeof(double2), cudaMemcpyHostToDevice, ctx->stream));
-    // L, Psi, G in row bands on the copy stream (after everything queued so
-    // far on the context's stream); the first assembly follows band by band
+    // L, Psi, G in row bands on three copy streams, one per matrix (after
+    // everything queued so far on the context's stream); band b is complete
+    // at band_ev[b], and the first assembly follows band by band
     ZS_CU(cudaEventRecord(ctx->ev_host, ctx->stream));
     ZS_CU(cudaStreamWaitEvent(ctx->copy_stream, ctx->ev_host, 0));
+    for (auto q : ctx->copy_aux) ZS_CU(cudaStreamWaitEvent(q, ctx->ev_host, 0));
     for (int bnd = 0; bnd < zsolve_ctx::kBands; bnd++) {
         const int64_t r0 = n * bnd / zsolve_ctx::kBands, r1 = n * (bnd + 1) / zsolve_ctx::kBands;
         const size_t off = (size_t)r0 * n, len = (size_t)(r1 - r0) * n * sizeof(double);
         ZS_CU(cudaMemcpyAsync(ctx->hd_L + off, L + off, len, cudaMemcpyHostToDevice, ctx->copy_stream));
-        ZS_CU(cudaMemcpyAsync(ctx->hd_Psi + off, Psi + off, len, cudaMemcpyHostToDevice, ctx->copy_stream));
-        ZS_CU(cudaMemcpyAsync(ctx->hd_G + off, G + off, len, cudaMemcpyHostToDevice, ctx->copy_stream));
+        ZS_CU(cudaMemcpyAsync(ctx->hd_Psi + off, Psi + off, len, cudaMemcpyHostToDevice, ctx->copy_aux[0]));
+        ZS_CU(cudaMemcpyAsync(ctx->hd_G + off, G + off, len, cudaMemcpyHostToDevice, ctx->copy_aux[1]));
+        for (int q = 0; q < 2; q++) {
+            ZS_CU(cudaEventRecord(ctx->aux_ev[bnd][q], ctx->copy_aux[q]));
+            ZS_CU(cudaStreamWaitEvent(ctx->copy_stream, ctx->aux_ev[bnd][q], 0));
+        }
         ZS_CU(cudaEventRecord(ctx->band_ev[bnd], ctx->copy_stream));
     }
     ctx->nband = zsolve_ctx::kBands;
@@ -1343,6 +1383,7 @@ int zsolve_residual_oz(zsolve_ctx *ctx, const double *L, const double *Psi, cons
     ctx->h_params[0] = ctx->single;  // slot 0 holds the single system's frequency again
     ZS_CU(cudaMemcpyAsync(ctx->d_params, ctx->h_params, sizeof(ZsSlotParam), cudaMemcpyHostToDevice, ctx->stream));
     ZS_TRY(oz_split_inputs(ctx, L, Psi, G, ctx->stream));
+    ZS_CU(cudaStreamWaitEvent(ctx->stream, ctx->oz_done, 0));
     Lane &ln = ctx->lane[0];
     StageSpan sp(ctx, ZSOLVE_STAGE_RESIDUAL, ctx->stream);
     ZS_CU(zs_launch_residual_oz(ctx->oz_amap, ctx->oz_ea, ctx->n, ctx->d_params, (const double2 *)b,

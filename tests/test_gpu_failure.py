@@ -94,9 +94,17 @@ def test_natural_stall_reaches_fallback(zs, torch, gemm, n, nrhs, nf):
         X = x.cpu().numpy()
         for f in range(nf):
             i = infos[f]
-            # no pivot was flagged: the refinement itself gave up
-            assert i.status == 0 and i.pivot_flag == 0 and i.fallback == 1, i.as_dict()
-            assert 1 <= i.iters <= 10, i.as_dict()
+            assert i.status == 0 and i.fallback == 1, i.as_dict()
+            if gemm == "TF32" and i.pivot_flag:
+                # with 10-bit products the trailing matrix I - v v^T / eps loses
+                # its identity part entirely and can cancel to an exactly zero
+                # pivot, which the pivot test catches before any correction
+                assert i.iters == 0, i.as_dict()
+            else:
+                # no pivot was flagged: the refinement itself gave up
+                assert i.pivot_flag == 0 and 1 <= i.iters <= 10, i.as_dict()
             assert np.all(rel_err(X[f], ref[f]) <= PARITY), (f, rel_err(X[f], ref[f]))
+        if gemm != "TF32":
+            assert all(i.pivot_flag == 0 for i in infos)
     finally:
         s.close()
