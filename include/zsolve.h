@@ -78,7 +78,8 @@ extern "C" {
                               frequencies as one product on the bf16 tensor cores with error-free
                               splitting (8 digits of 7 bits per value, exact digit products and
                               sums, one rounding to float64 per output; zsolve_residual_oz);
-                              calls on the single system keep the float64 GEMV (F64) */
+                              evaluations of fewer than 4 (frequency, right-hand side) pairs, and
+                              calls on the single system, take the float64 GEMV (F64) */
 
 typedef struct zsolve_ctx zsolve_ctx; /* opaque */
 

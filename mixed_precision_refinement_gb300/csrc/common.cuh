@@ -180,8 +180,9 @@ cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t 
 // Operand packs of the block triangular solves on the tensor cores, at outer
 // column J: A planes rows i >= J+NB = [Re A21(i,:) | Im A21(i,:)], Br planes
 // rows j >= J+NB = [Re A12(:,j) | Im A12(:,j)] (mode 1: tf32 hi; 2: hi + lo).
-// sym: Z is complex symmetric and only its lower part is current; the A12^T
-// packs are taken from A21 (equal by symmetry).
+// sym: Z is complex symmetric and only its lower part is current: 1, the A
+// planes only (the one-product symmetric block solve); 2, the A12^T packs
+// taken from A21 too (equal by symmetry; the two-product solve).
 cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                 int64_t J, float *pack, int64_t pack_stride, int mode, int sym, const int *slots,
                                 int nslot, cudaStream_t st);
@@ -196,8 +197,13 @@ cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane
 // A22 -= L21 U12 for every listed slot (split: 3xTF32), at most max_grid
 // persistent CTAs that take tiles from *ctr (zero before the launch).
 // lower: only the tiles on and below the diagonal (complex-symmetric Z).
+// part: ZS_PART_ALL, or ZS_PART_COL0 (the first 128-column tile: the next
+// step's diagonal block and A21) and ZS_PART_REST (the other tiles).
+#define ZS_PART_ALL 0
+#define ZS_PART_COL0 1
+#define ZS_PART_REST 2
 cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, int lower,
-                               const int *slots, int nslot, unsigned *ctr, unsigned *status, int max_grid,
+                               int part, const int *slots, int nslot, unsigned *ctr, unsigned *status, int max_grid,
                                cudaStream_t st);
 // L21 = A21 U11^-1 and U12 = L11^-1 A12 from the packs of zs_launch_pack_trsm
 // and zs_launch_diag_block; writes L21, U12 into z32 and their operand packs.

@@ -267,8 +267,18 @@ struct Tile {
     int slot, ra, u, rb;
 };
 
+// Parts of a trailing update (the Schur kinds): all its tiles, the first
+// column tile only (the next outer step's panel: its diagonal block and
+// A21), or the others -- so that the next diagonal block can start while the
+// rest of the update runs.
+enum { PART_ALL = ZS_PART_ALL, PART_COL0 = ZS_PART_COL0, PART_REST = ZS_PART_REST };
+
 template <int KIND>
-__host__ __device__ __forceinline__ int tiles_per_slot(int tiles) {
+__host__ __device__ __forceinline__ int tiles_per_slot(int tiles, int part) {
+    if (KIND == KIND_SCHUR || KIND == KIND_SCHUR_LOWER) {
+        if (part == PART_COL0) return tiles;
+        if (part == PART_REST) return KIND == KIND_SCHUR ? tiles * (tiles - 1) : tiles * (tiles - 1) / 2;
+    }
     return KIND == KIND_SCHUR         ? tiles * tiles
            : KIND == KIND_SCHUR_LOWER ? tiles * (tiles + 1) / 2
            : KIND == KIND_TRSM_SYM    ? tiles
@@ -276,12 +286,31 @@ __host__ __device__ __forceinline__ int tiles_per_slot(int tiles) {
 }
 
 template <int KIND>
-__device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const int *slots) {
+__device__ __forceinline__ Tile tile_of(int t, int tiles, int64_t base, const int *slots, int part) {
     Tile x;
-    const int per_slot = tiles_per_slot<KIND>(tiles);
+    const int per_slot = tiles_per_slot<KIND>(tiles, part);
     const int si = t / per_slot, rem = t - si * per_slot;
     x.slot = slots[si];
-    if (KIND == KIND_SCHUR_LOWER) {
+    if ((KIND == KIND_SCHUR || KIND == KIND_SCHUR_LOWER) && part == PART_COL0) {
+        x.ra = (int)(base + (int64_t)rem * TM);
+        x.rb = (int)base;
+        x.u = 0;
+    } else if (KIND == KIND_SCHUR_LOWER && part == PART_REST) {
+        // row-major over the lower triangle without its first column: row
+        // tile tm >= 1 holds tiles tn = 1 .. tm
+        int tm = (int)((1.f + sqrtf(8.f * (float)rem + 1.f)) * 0.5f);
+        while (tm * (tm - 1) / 2 > rem) tm--;
+        while ((tm + 1) * tm / 2 <= rem) tm++;
+        const int tn = 1 + rem - tm * (tm - 1) / 2;
+        x.ra = (int)(base + (int64_t)tm * TM);
+        x.rb = (int)(base + (int64_t)tn * TN);
+        x.u = 0;
+    } else if (KIND == KIND_SCHUR && part == PART_REST) {
+        const int tm = rem / (tiles - 1), tn = 1 + rem - tm * (tiles - 1);
+        x.ra = (int)(base + (int64_t)tm * TM);
+        x.rb = (int)(base + (int64_t)tn * TN);
+        x.u = 0;
+    } else if (KIND == KIND_SCHUR_LOWER) {
         // row-major over the lower triangle: row tile tm holds tm + 1 tiles
         int tm = (int)((sqrtf(8.f * (float)rem + 1.f) - 1.f) * 0.5f);
         while ((tm + 1) * (tm + 2) / 2 <= rem) tm++;
@@ -315,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUtensorMap wmap,
            const __grid_constant__ CUtensorMap cmap, const __grid_constant__ CUtensorMap pmap, int64_t n, int64_t J,
            const int *__restrict__ slots, int nslot, unsigned *__restrict__ ctr, unsigned *__restrict__ status,
-           const float *__restrict__ dinv, int64_t dinv_stride) {
+           const float *__restrict__ dinv, int64_t dinv_stride, int part) {
     using C = Cfg<SPLIT>;
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[C::STAGES], bar_empty[C::STAGES], bar_accf[2], bar_acce[2], bar_drain;
@@ -329,7 +358,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
     const int64_t base = J + NB;
     const int64_t m2 = n - base;
     const int tiles = (int)((m2 + TM - 1) / TM);
-    const int total = tiles_per_slot<KIND>(tiles) * nslot;
+    const int total = tiles_per_slot<KIND>(tiles, part) * nslot;
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -379,7 +408,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     g++;
                     break;
                 }
-                const Tile x = tile_of<KIND>(t, tiles, base, slots);
+                const Tile x = tile_of<KIND>(t, tiles, base, slots, part);
                 // A rows: L21 / A21 (A planes) or A12^T (Br planes); B: the pack's
                 // own Br/Bi rows, or W / V from the inverse packs
                 const int pa = (KIND == KIND_TRSM && x.u) ? PL_BR_HI : PL_A_HI;
@@ -510,7 +539,7 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
             const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status, 5u | (KIND << 4));
             if (!__all_sync(0xffffffffu, ok) || t < 0) break;
             tc_fence_after();
-            const Tile x = tile_of<KIND>(t, tiles, base, slots);
+            const Tile x = tile_of<KIND>(t, tiles, base, slots, part);
             const int row0 = x.ra + quad * 32;  // this warp's 32 output rows
             if (KIND == KIND_TRSM_SYM) {
                 // The accumulator holds U12^T for the tile's rows (Re in chunks
@@ -702,7 +731,7 @@ template <int SPLIT, int KIND>
 cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const CUtensorMap &cmap,
                         const CUtensorMap &pmap, int64_t n, int64_t J, const int *slots, int nslot, unsigned *ctr,
                         unsigned *status, int max_grid, cudaStream_t st, const float *dinv = nullptr,
-                        int64_t dinv_stride = 0) {
+                        int64_t dinv_stride = 0, int part = PART_ALL) {
     using C = Cfg<SPLIT>;
     // once per process (thread-safe initialisation of a local static)
     static const cudaError_t attr = cudaFuncSetAttribute(k_cgemm_tc<SPLIT, KIND>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -710,11 +739,11 @@ cudaError_t launch_kind(const CUtensorMap &tmap, const CUtensorMap &wmap, const 
     const int64_t m2 = n - J - NB;
     if (m2 <= 0 || nslot <= 0) return cudaSuccess;
     const int tiles = (int)((m2 + TM - 1) / TM);
-    const int64_t total = (int64_t)tiles_per_slot<KIND>(tiles) * nslot;
+    const int64_t total = (int64_t)tiles_per_slot<KIND>(tiles, part) * nslot;
     if (total <= 0) return cudaSuccess;
     const int grid = (int)(total < max_grid ? total : max_grid);
     k_cgemm_tc<SPLIT, KIND><<<grid, kThreads, C::SMEM, st>>>(tmap, wmap, cmap, pmap, n, J, slots, nslot, ctr,
-                                                             status, dinv, dinv_stride);
+                                                             status, dinv, dinv_stride, part);
     return cudaGetLastError();
 }
 
@@ -762,17 +791,21 @@ cudaError_t zs_tc_z32_map(const float *z32, int64_t n, int64_t ld, int64_t plane
 }
 
 cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int64_t J, int split, int lower,
-                               const int *slots, int nslot, unsigned *ctr, unsigned *status, int max_grid,
+                               int part, const int *slots, int nslot, unsigned *ctr, unsigned *status, int max_grid,
                                cudaStream_t st) {
-    if (max_grid < 1 || !ctr) return cudaErrorInvalidValue;
+    if (max_grid < 1 || !ctr || part < PART_ALL || part > PART_REST) return cudaErrorInvalidValue;
     const CUtensorMap &m = *reinterpret_cast<const CUtensorMap *>(map);
     const CUtensorMap &c = *reinterpret_cast<const CUtensorMap *>(cmap);
     if (lower) {
-        if (split) return launch_kind<1, KIND_SCHUR_LOWER>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
-        return launch_kind<0, KIND_SCHUR_LOWER>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
+        if (split)
+            return launch_kind<1, KIND_SCHUR_LOWER>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st, nullptr,
+                                                    0, part);
+        return launch_kind<0, KIND_SCHUR_LOWER>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st, nullptr, 0,
+                                                part);
     }
-    if (split) return launch_kind<1, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
-    return launch_kind<0, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st);
+    if (split)
+        return launch_kind<1, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st, nullptr, 0, part);
+    return launch_kind<0, KIND_SCHUR>(m, m, c, m, n, J, slots, nslot, ctr, status, max_grid, st, nullptr, 0, part);
 }
 
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,

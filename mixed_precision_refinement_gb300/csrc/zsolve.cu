@@ -60,8 +60,11 @@ struct zsolve_ctx {
     float *inv32 = nullptr; // inverses of the 32x32 diagonal sub-blocks of the current outer block
     int64_t dinv_stride = 0;
     float *winv = nullptr;  // tensor-core operand packs of the current diagonal block's inverses
-    alignas(64) unsigned char pack_map[128] = {};    // TMA tensor map over the operand packs (32 x 128 boxes)
-    alignas(64) unsigned char packst_map[128] = {};  // the same packs, 32 x 32 boxes for stores
+    // TMA tensor maps over the two sets of operand packs (32 x 128 boxes for
+    // loads; 32 x 32 boxes for stores): outer steps alternate between them when
+    // the next step's diagonal block runs ahead of the trailing update
+    alignas(64) unsigned char pack_map[2][128] = {};
+    alignas(64) unsigned char packst_map[2][128] = {};
     alignas(64) unsigned char winv_map[128] = {};    // TMA tensor map over the inverse packs
     alignas(64) unsigned char z32_map[128] = {};     // TMA tensor map over the float32 matrices
     float2 *v = nullptr;
@@ -74,6 +77,7 @@ struct zsolve_ctx {
     int *zexp = nullptr;   // residual mode FX: per slot and row of Z64, its largest exponent
     int fx_ndf = 1;        // residual mode FX: sub-steps of four taken in float64 (ZSOLVE_FX_NDF)
     int trsv_r = 0;        // right-hand sides per triangular-solve chain; 0: chosen per solve (ZSOLVE_TRSV_R)
+    int lookahead = -1;    // next diagonal block ahead of the trailing update: -1 for few frequencies, 0 never, 1 always (ZSOLVE_LOOKAHEAD)
     int tc_cap = 0;        // testing aid: at most this many CTAs per tcgen05 launch (ZSOLVE_TC_GRID; 0: no cap)
     // residual mode OZ: digits of A' = [L; Psi; G] (allocated on first use),
     // their row scales and tensor map; oz_ready while they hold the current
@@ -130,6 +134,7 @@ struct zsolve_ctx {
         unsigned *h_status = nullptr;   // pinned copy of the device status word
         int tc_grid = 0;                // CTAs of this lane's tcgen05 launches
         int trsv_grid = 0;              // CTAs of this lane's triangular solves (0: one per SM)
+        bool alone = true;              // no other lane runs beside this one (the next diagonal block may run ahead)
         // residual mode OZ: digits of x, their scales, the partial products
         void *oz_x = nullptr;
         int *oz_ex = nullptr;
@@ -257,7 +262,7 @@ int gemm_internal(int pub) { return pub == ZSOLVE_GEMM_FFMA ? 0 : pub == ZSOLVE_
 
 size_t slot_bytes(int64_t n, int64_t ld) {
     return (size_t)n * n * sizeof(double2) + (size_t)2 * n * ld * sizeof(float) +
-           (size_t)6 * zs_pack_plane(n) * sizeof(float) + (size_t)zs_dinv_stride(n) * sizeof(float) +
+           (size_t)12 * zs_pack_plane(n) * sizeof(float) + (size_t)zs_dinv_stride(n) * sizeof(float) +
            (size_t)zs_inv32_slot_stride(n) * sizeof(float) + (size_t)ZS_WINV_STRIDE * sizeof(float);
 }
 
@@ -298,7 +303,16 @@ int factor_slots_simt(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
 // the side stream while the diagonal block is factored; the tcgen05 block
 // solves wait for both.  The tcgen05 kernels take tiles from per-launch
 // counters (zeroed once per factorisation).
-constexpr int kMaxCtr = 256;  // tile counters per factorisation (2 per outer block)
+//
+// With few frequencies the chain of diagonal blocks (one CTA per frequency)
+// bounds the factorisation.  Then each step's trailing update runs in two
+// launches: first its first column tile -- the next step's diagonal block and
+// A21 -- after which the side stream factors the next diagonal block and packs
+// the next A21 while the main stream finishes the update.  The packs of
+// consecutive steps alternate between two buffers, since the next step's are
+// written while this step's are still read.
+constexpr int kMaxCtr = 512;         // tile counters per factorisation (at most 3 per outer block)
+constexpr int kLookaheadSlots = 4;   // frequencies per lane up to which the next diagonal block runs ahead
 
 int tc_grid(const zsolve_ctx *ctx, const Lane &ln) {
     return ctx->tc_cap > 0 ? std::min(ln.tc_grid, ctx->tc_cap) : ln.tc_grid;
@@ -306,44 +320,107 @@ int tc_grid(const zsolve_ctx *ctx, const Lane &ln) {
 
 int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     const int64_t n = ctx->n;
-    const int mode = ctx->gemm_eff, split = mode == 2 ? 1 : 0;
-    const int64_t inv32_stride = zs_inv32_slot_stride(n);
-    if (2 * ((n + ZS_NB - 1) / ZS_NB) > kMaxCtr) return fail(ctx, ZSOLVE_EINVAL, "n too large for the tile counters");
+    const int mode = ctx->gemm_eff, split = mode == 2 ? 1 : 0, sym = ctx->opts.symmetric;
+    const int64_t nblk = (n + ZS_NB - 1) / ZS_NB;
+    if (3 * nblk > kMaxCtr) return fail(ctx, ZSOLVE_EINVAL, "n too large for the tile counters");
     ZS_CU(cudaMemsetAsync(ln.tile_ctr, 0, kMaxCtr * sizeof(unsigned), ln.stream));
     unsigned *ctr = ln.tile_ctr;
-    for (int64_t J = 0; J < n; J += ZS_NB) {
-        const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
-        const bool last = J + nb >= n;
-        if (!last) {
-            ZS_CU(cudaEventRecord(ln.ev_fork, ln.stream));
-            ZS_CU(cudaStreamWaitEvent(ln.side, ln.ev_fork, 0));
-            StageSpan sp(ctx, ZSOLVE_STAGE_PACK, ln.side);
-            ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J, ctx->pack,
-                                      ctx->pack_stride, mode, ctx->opts.symmetric, slots, nslot, ln.side));
-            sp.done(1);
-            ZS_CU(cudaEventRecord(ln.ev_join, ln.side));
-        }
-        {
-            StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, ln.stream);
-            ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
-                                       ctx->d_pivflag, nullptr, 0, ctx->dinv, ctx->dinv_stride,
-                                       last ? nullptr : ctx->winv, mode, ln.stream));
-            sp.done(1);
-        }
-        if (last) break;
-        {
-            ZS_CU(cudaStreamWaitEvent(ln.stream, ln.ev_join, 0));
-            StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.stream);
-            ZS_CU(zs_launch_trsm_tc(ctx->pack_map, ctx->winv_map, ctx->z32_map, ctx->packst_map, n, J, split,
-                                    ctx->opts.symmetric, ctx->dinv, ctx->dinv_stride, slots, nslot, ctr++,
-                                    ctx->d_status, tc_grid(ctx, ln), ln.stream));
-            sp.done(1);
-        }
-        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR, ln.stream);
-        ZS_CU(zs_launch_schur_tc(ctx->pack_map, ctx->z32_map, n, J, split, ctx->opts.symmetric, slots, nslot, ctr++,
-                                 ctx->d_status, tc_grid(ctx, ln), ln.stream));
+    // The symmetric mode only: its packs read A21 alone, which the first
+    // column tile holds (the full mode's pack of A12 would wait for the rest).
+    // By default for a lane that runs alone with few frequencies (beside
+    // another lane, that lane's kernels fill the SMs the diagonal chain leaves
+    // idle, and running ahead only adds contention), and when the rest of an
+    // update is long enough to hide a diagonal block: on average over the
+    // steps nslot T^2 / 6 tiles (T = the first step's row tiles), at least two
+    // waves of the grid.  (N=8000 with one frequency: 18.4 against 20.0 ms a
+    // sweep; N=2157 with one: slower, the rest of each update being short.)
+    const int64_t T = (n - 1) / ZS_NB;
+    const bool ahead = sym && (ctx->lookahead > 0 ||
+                               (ctx->lookahead < 0 && ln.alone && nslot <= kLookaheadSlots &&
+                                (int64_t)nslot * T * T >= 12 * (int64_t)tc_grid(ctx, ln)));
+    // The symmetric mode's block solve in one product per row tile (its
+    // epilogue writes both factors) where the row tiles of all frequencies
+    // fill at least half the GPU's SMs; else the two-product form, whose CTAs
+    // split the work of a row tile (a frequency's chain of steps is shorter
+    // then).  The choice depends on the step and the batch, not on the grid.
+    auto one_product = [&](int64_t J) {
+        const int64_t rows = (n - J - ZS_NB + ZS_NB - 1) / ZS_NB * nslot;
+        return sym && 2 * rows >= ctx->num_sms;
+    };
+    auto pack = [&](int64_t J, int buf, cudaStream_t st) -> int {
+        StageSpan sp(ctx, ZSOLVE_STAGE_PACK, st);
+        ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J,
+                                  ctx->pack + (int64_t)buf * ctx->S * ctx->pack_stride, ctx->pack_stride, mode,
+                                  sym ? (one_product(J) ? 1 : 2) : 0, slots, nslot, st));
         sp.done(1);
+        return ZSOLVE_OK;
+    };
+    auto diag = [&](int64_t J, cudaStream_t st) -> int {
+        const int nb = (int)std::min<int64_t>(ZS_NB, n - J);
+        StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, st);
+        ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
+                                   ctx->d_pivflag, nullptr, 0, ctx->dinv, ctx->dinv_stride,
+                                   J + nb >= n ? nullptr : ctx->winv, mode, st));
+        sp.done(1);
+        return ZSOLVE_OK;
+    };
+    auto trsm = [&](int64_t J, int buf) -> int {
+        StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.stream);
+        ZS_CU(zs_launch_trsm_tc(ctx->pack_map[buf], ctx->winv_map, ctx->z32_map, ctx->packst_map[buf], n, J, split,
+                                one_product(J) ? 1 : 0, ctx->dinv, ctx->dinv_stride, slots, nslot, ctr++,
+                                ctx->d_status, tc_grid(ctx, ln), ln.stream));
+        sp.done(1);
+        return ZSOLVE_OK;
+    };
+    auto schur = [&](int64_t J, int buf, int part, int grid) -> int {
+        StageSpan sp(ctx, ZSOLVE_STAGE_SCHUR, ln.stream);
+        ZS_CU(zs_launch_schur_tc(ctx->pack_map[buf], ctx->z32_map, n, J, split, sym, part, slots, nslot, ctr++,
+                                 ctx->d_status, grid, ln.stream));
+        sp.done(1);
+        return ZSOLVE_OK;
+    };
+    auto fork = [&]() -> int {  // the side stream follows the main stream from here
+        ZS_CU(cudaEventRecord(ln.ev_fork, ln.stream));
+        ZS_CU(cudaStreamWaitEvent(ln.side, ln.ev_fork, 0));
+        return ZSOLVE_OK;
+    };
+    if (!ahead) {
+        for (int64_t J = 0; J < n; J += ZS_NB) {
+            const bool last = J + ZS_NB >= n;
+            if (!last) {
+                ZS_TRY(fork());
+                ZS_TRY(pack(J, 0, ln.side));
+                ZS_CU(cudaEventRecord(ln.ev_join, ln.side));
+            }
+            ZS_TRY(diag(J, ln.stream));
+            if (last) break;
+            ZS_CU(cudaStreamWaitEvent(ln.stream, ln.ev_join, 0));
+            ZS_TRY(trsm(J, 0));
+            ZS_TRY(schur(J, 0, ZS_PART_ALL, tc_grid(ctx, ln)));
+        }
+        return ZSOLVE_OK;
     }
+    // step 0's diagonal block and packs; then per step: block solves, the
+    // first column tile of the update, the next diagonal block and packs on
+    // the side stream beside the rest of the update
+    ZS_TRY(fork());
+    if (ZS_NB < n) ZS_TRY(pack(0, 0, ln.side));
+    ZS_TRY(diag(0, ln.side));
+    ZS_CU(cudaEventRecord(ln.ev_join, ln.side));
+    for (int64_t J = 0; J + ZS_NB < n; J += ZS_NB) {
+        const int buf = (int)((J / ZS_NB) & 1);
+        ZS_CU(cudaStreamWaitEvent(ln.stream, ln.ev_join, 0));  // this step's diagonal block and packs
+        ZS_TRY(trsm(J, buf));
+        ZS_TRY(schur(J, buf, ZS_PART_COL0, tc_grid(ctx, ln)));
+        ZS_TRY(fork());
+        const int64_t J1 = J + ZS_NB;
+        ZS_TRY(diag(J1, ln.side));
+        if (J1 + ZS_NB < n) ZS_TRY(pack(J1, buf ^ 1, ln.side));
+        ZS_CU(cudaEventRecord(ln.ev_join, ln.side));
+        // leave an SM per frequency to the next diagonal block
+        ZS_TRY(schur(J, buf, ZS_PART_REST, std::max(1, tc_grid(ctx, ln) - nslot)));
+    }
+    ZS_CU(cudaStreamWaitEvent(ln.stream, ln.ev_join, 0));  // the last diagonal block
     return ZSOLVE_OK;
 }
 
@@ -516,11 +593,15 @@ int oz_split_inputs(zsolve_ctx *ctx, const double *L, const double *Psi, const d
 }
 
 // r = b - Z x for the listed slots in the context's residual arithmetic.
+constexpr int kOzMinPairs = 4;
 int residual_slots(zsolve_ctx *ctx, Lane &ln, const double2 *b, const double2 *x, int64_t x_stride, int nrhs,
                    float2 *o64, int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot,
                    StageSpan *sp) {
     const int64_t n = ctx->n;
-    if (ctx->resid_mode == ZSOLVE_RESID_OZ && ctx->oz_ready) {
+    // OZ reads its 48 n^2 bytes of digits whatever the number of columns;
+    // below four (frequency, right-hand side) pairs the float64 GEMV over Z64
+    // (16 n^2 bytes and 2-4 DFMA per entry and pair) is the faster one
+    if (ctx->resid_mode == ZSOLVE_RESID_OZ && ctx->oz_ready && (int64_t)nslot * nrhs >= kOzMinPairs) {
         ZS_CU(cudaStreamWaitEvent(ln.stream, ctx->oz_done, 0));
         ZS_CU(zs_launch_residual_oz(ctx->oz_amap, ctx->oz_ea, n, ctx->d_params, b, x, x_stride, nrhs, o64, o64s, o128,
                                     o128s, slots, nslot, ln.oz_x, ln.oz_ex, ln.oz_ncol_cap, ln.oz_part,
@@ -913,7 +994,14 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
                 // other lanes' diagonal blocks (one CTA per frequency)
                 ctx->lane[k].tc_grid = std::max(1, ctx->num_sms - (count - cnt[k]));
                 ctx->lane[k].trsv_grid = std::max(1, ctx->num_sms / K);
+                ctx->lane[k].alone = false;
             }
+            struct Alone {  // lane 0 runs alone again after the batch (the probe, single-system calls)
+                zsolve_ctx *c;
+                ~Alone() {
+                    for (auto &l : c->lane) l.alone = true;
+                }
+            } alone_again{ctx};
             Stagger asm_gate[kMaxLanes], ref_gate[kMaxLanes];  // lane k's assembly / first solve queued
             int stk[kMaxLanes] = {};
             for (int k = 0; k < K; k++) {
@@ -1104,6 +1192,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ctx->probe.chosen = ctx->opts.gemm == ZSOLVE_GEMM_AUTO ? ZSOLVE_GEMM_TF32X3 : ctx->opts.gemm;
     if (ctx->opts.wait_limit > 0) ctx->wait_limit = (unsigned)ctx->opts.wait_limit;
     if (const char *e = getenv("ZSOLVE_FX_NDF")) ctx->fx_ndf = std::min(3, std::max(0, atoi(e)));
+    if (const char *e = getenv("ZSOLVE_LOOKAHEAD")) ctx->lookahead = std::min(1, std::max(-1, atoi(e)));
     // testing aid: few CTAs per tcgen05 launch, so that each takes many tiles
     if (const char *e = getenv("ZSOLVE_TC_GRID")) ctx->tc_cap = std::max(0, atoi(e));
     // right-hand sides per triangular-solve chain (1, 2 or 4; unset: chosen per solve)
@@ -1141,7 +1230,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (cudaMallocHost(&(p), (bytes)) != cudaSuccess) return bail(ZSOLVE_ENOMEM)
     ALLOC(ctx->z64, (size_t)S * ctx->z64_stride * sizeof(double2));
     ALLOC(ctx->z32, (size_t)S * ctx->z32_stride * sizeof(float));
-    ALLOC(ctx->pack, (size_t)S * ctx->pack_stride * sizeof(float));
+    ALLOC(ctx->pack, (size_t)2 * S * ctx->pack_stride * sizeof(float));
     ALLOC(ctx->dinv, (size_t)S * ctx->dinv_stride * sizeof(float));
     // AUTO may pick any arithmetic: it holds the workspaces of both kinds
     const bool is_auto = ctx->opts.gemm == ZSOLVE_GEMM_AUTO;
@@ -1187,8 +1276,12 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     ctx->lane[0].stream = ctx->stream;
     for (auto &ln : ctx->lane) ln.tc_grid = ctx->num_sms;
     if (ctx->winv &&
-        (zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 128, ctx->pack_map) != cudaSuccess ||
-         zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 32, ctx->packst_map) != cudaSuccess ||
+        (zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 128, ctx->pack_map[0]) != cudaSuccess ||
+         zs_tc_pack_map(ctx->pack, n, S, ctx->pack_stride, 32, ctx->packst_map[0]) != cudaSuccess ||
+         zs_tc_pack_map(ctx->pack + (int64_t)S * ctx->pack_stride, n, S, ctx->pack_stride, 128, ctx->pack_map[1]) !=
+             cudaSuccess ||
+         zs_tc_pack_map(ctx->pack + (int64_t)S * ctx->pack_stride, n, S, ctx->pack_stride, 32, ctx->packst_map[1]) !=
+             cudaSuccess ||
          zs_tc_winv_map(ctx->winv, S, ctx->winv_map) != cudaSuccess ||
          zs_tc_z32_map(ctx->z32, n, ctx->ld, ctx->plane, S, ctx->z32_stride, ctx->z32_map) != cudaSuccess))
         return bail(ZSOLVE_ECUDA);

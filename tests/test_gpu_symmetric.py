@@ -159,6 +159,33 @@ def test_tcgen05_many_tiles_per_cta(zs, torch, monkeypatch, gemm, sym):
         assert np.array_equal(out[cap], out[""]), cap
 
 
+@pytest.mark.parametrize("gemm", ["TF32X3", "TF32"])
+@pytest.mark.parametrize("n,nrhs,nf,batch", [(1000, 2, 1, 1), (700, 1, 3, 3), (129, 1, 2, 2), (2157, 1, 2, 2),
+                                              (300, 4, 9, 9)])
+def test_lookahead_matches_plain_order(zs, torch, monkeypatch, gemm, n, nrhs, nf, batch):
+    """The next diagonal block ahead of the trailing update (ZSOLVE_LOOKAHEAD
+    = 1; by default for up to 4 frequencies per lane) against the plain
+    order (0): bit-identical sweeps, since every tile, block and pack is
+    formed by the same arithmetic; and the oracle's solutions."""
+    wl = workload.make_small(n, seed=300 + n, nf=nf, nrhs=nrhs, f_lo=0.5e9, f_hi=20e9)
+    ref = oracle.solve_sweep(wl)
+    out = {}
+    for ahead in ("0", "1"):
+        monkeypatch.setenv("ZSOLVE_LOOKAHEAD", ahead)
+        s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm), batch=batch)
+        try:
+            x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
+            infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega,
+                                    wl.zs, dev(torch, wl.B), x)
+            out[ahead] = x.cpu().numpy()
+        finally:
+            s.close()
+        assert all(i.status == 0 and i.fallback == 0 for i in infos)
+        for f in range(nf):
+            assert np.all(rel_err(out[ahead][f], ref[f]) <= PARITY), (ahead, f)
+    assert np.array_equal(out["0"], out["1"])
+
+
 def test_symmetric_mode_with_a_nonsymmetric_input(zs, torch):
     # G made non-symmetric: the factors are those of the matrix the lower
     # triangle defines, but the float64 residual uses all of Z, so the
