@@ -292,14 +292,18 @@ cudaError_t zs_launch_residual_lpg(const double *L, const double *Psi, const dou
                                    int64_t out128_stride, const int *slots, int nslot, cudaStream_t st);
 
 // Residual from L, Psi, G on the bf16 tensor cores with error-free splitting
-// (resid_oz.cu).  The digits of A' = [L; Psi; G] (8 planes of 3n rows x
-// zs_oz_n_pad(n) bf16, bytes 16 * 3n * n_pad) and their row scales (ea, 3n
+// (resid_oz.cu).  The digits of A' = [L; Psi; G] (8 planes, stored tile-major
+// in units of 128 rows x 128 K, zs_oz_a_bytes(n) bytes, zero before the first
+// use) and their row scales (ea, 3n
 // ints) are formed once per set of L, Psi, G, rows r0..r1-1 of each matrix
 // per call; amap (a CUtensorMap, 64-byte aligned) describes them.  Per
 // evaluation: the digits of x (xdig: 8 planes of ncol_cap rows x n_pad bf16,
 // ex: ncol_cap ints, ncol = 2 nslot nrhs <= ncol_cap), the partial products
-// (part: part_cap doubles) and then r as zs_launch_residual.
+// (part: part_cap doubles; the product runs on up to num_sms CTAs, fewer if
+// a tile's K range would be split into more segments than part holds) and
+// then r as zs_launch_residual.
 int64_t zs_oz_n_pad(int64_t n);
+int64_t zs_oz_a_bytes(int64_t n);  // bytes of A's digits (tile-major, zero padded)
 int zs_oz_ncol_alloc(int ncol);
 cudaError_t zs_launch_oz_split_a(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0,
                                  int64_t r1, void *dig, int *ea, cudaStream_t st);

@@ -52,6 +52,8 @@
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace {
@@ -59,14 +61,14 @@ namespace {
 constexpr int kDig = 8;         // digits per value
 constexpr int TM = 128;         // rows of A' per tile (TMEM lanes)
 constexpr int W = 32;           // X columns per group (N of one digit block)
-constexpr int KS = 16;          // K per stage: one 32-byte swizzle row of bf16
+constexpr int KS = 32;          // K per stage: one 64-byte swizzle row of bf16 (two MMA K steps)
 constexpr int KCH = 128;        // K per accumulator flush
 constexpr int kStepsPerCh = KCH / KS;
-constexpr int A_SLICE = TM * KS * 2;        // 4 KB: one digit plane of the A tile
-constexpr int X_SLICE = W * KS * 2;         // 1 KB
-constexpr int A_STAGE = kDig * A_SLICE;     // 32 KB
-constexpr int STAGE = A_STAGE + kDig * X_SLICE;  // 40 KB
-constexpr int STAGES = 5;
+constexpr int A_SLICE = TM * KS * 2;        // 8 KB: one digit plane of the A tile
+constexpr int X_SLICE = W * KS * 2;         // 2 KB
+constexpr int A_STAGE = kDig * A_SLICE;     // 64 KB
+constexpr int STAGE = A_STAGE + kDig * X_SLICE;  // 80 KB
+constexpr int STAGES = 2;
 constexpr int SMEM = STAGES * STAGE + 1024;  // + alignment slack
 constexpr int kEpiWarps = 8;
 constexpr int kThreads = 64 + 32 * kEpiWarps;  // warp 0 TMA, warp 1 MMA and TMEM, warps 2-9 epilogue
@@ -140,11 +142,20 @@ __device__ __forceinline__ void write_digits8(const double (&a)[8], int q, __nv_
     }
 }
 
+// Tile-major layout of A's digits: unit (row tile t, K chunk c) holds the 8
+// planes of 128 rows x 128 K, 256 KB contiguous, so that the product streams
+// whole units from HBM: element (row, j) of plane p sits at
+// ((((t nch + c) 8 + p) 128 + row % 128) 128 + j % 128).  Rows past 3n and
+// K past n are zero.
+__host__ __device__ __forceinline__ int64_t oz_a_offset(int64_t row, int64_t j, int p, int64_t nch) {
+    return ((((row / TM) * nch + j / KCH) * kDig + p) * TM + row % TM) * KCH + j % KCH;
+}
+
 // Digits of A' = [L; Psi; G], rows r0..r1-1 of each matrix: one warp per
 // row; ea[row] = the row's largest biased exponent, or -1 if the row holds a
 // non-finite value.
 __global__ void __launch_bounds__(256) k_oz_split_a(const double *__restrict__ L, const double *__restrict__ Psi,
-                                                    const double *__restrict__ G, int64_t n, int64_t n_pad,
+                                                    const double *__restrict__ G, int64_t n, int64_t nch,
                                                     int64_t r0, int64_t r1, __nv_bfloat16 *__restrict__ dig,
                                                     int *__restrict__ ea) {
     const int lane = threadIdx.x & 31;
@@ -163,12 +174,11 @@ __global__ void __launch_bounds__(256) k_oz_split_a(const double *__restrict__ L
     q = __reduce_max_sync(0xffffffffu, q);
     fin = __all_sync(0xffffffffu, fin);
     if (lane == 0) ea[row] = fin ? q : -1;
-    const int64_t plane = 3 * n * n_pad;
-    for (int64_t j0 = 8 * lane; j0 < n_pad; j0 += 256) {
+    for (int64_t j0 = 8 * lane; j0 < nch * KCH; j0 += 256) {
         double a[8];
 #pragma unroll
         for (int u = 0; u < 8; u++) a[u] = (j0 + u < n && fin) ? __ldg(src + j0 + u) : 0.0;
-        write_digits8(a, q, dig + row * n_pad + j0, plane);
+        write_digits8(a, q, dig + oz_a_offset(row, j0, 0, nch), (int64_t)TM * KCH);
     }
 }
 
@@ -249,6 +259,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     }
     return true;
 }
+__device__ __forceinline__ void tma_load_5d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, int c3,
+                                            int c4, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(bar)
+        : "memory");
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
                                             uint32_t bar) {
     asm volatile(
@@ -264,14 +282,16 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                  : "memory");
 }
 
-// K-major operand, 32-byte swizzle: rows of 32 bytes (16 bf16), 8-row groups 256 bytes apart.
+// K-major operand, 64-byte swizzle: rows of 64 bytes (32 bf16), 8-row groups
+// 512 bytes apart; an MMA K step of 16 (32 bytes) inside the row advances the
+// start address.
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
     uint64_t d = 0;
     d |= (uint64_t)((addr >> 4) & 0x3FFF);  // start address
     d |= (uint64_t)1 << 16;                 // leading byte offset (unused for this layout)
-    d |= (uint64_t)(256 >> 4) << 32;        // stride byte offset
+    d |= (uint64_t)(512 >> 4) << 32;        // stride byte offset
     d |= (uint64_t)1 << 46;                 // descriptor version
-    d |= (uint64_t)6 << 61;                 // SWIZZLE_32B
+    d |= (uint64_t)4 << 61;                 // SWIZZLE_64B
     return d;
 }
 
@@ -291,9 +311,9 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
         : "memory");
 }
 
-// 32 lanes x 16 consecutive fp32 columns of the accumulator
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-    uint32_t r[16];
+// 32 lanes x 16 consecutive fp32 columns of the accumulator, asynchronously:
+// the registers hold the values after the next tmem_wait()
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
         "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
@@ -301,10 +321,8 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr)
         : "memory");
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 16; i++) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // An integer-valued float with |v| <= 2^22 as an int: v + 1.5 * 2^23 lies in
 // [2^23, 2^24] with unit spacing, so its low bits are v (two FP32/INT ops).
@@ -312,23 +330,30 @@ __device__ __forceinline__ int int_of(float v) {
     return (int)(__float_as_uint(v + 12582912.0f) - 0x4B400000u);
 }
 
-// One CTA: the 128 rows of A' from row0, X columns col0..col0+31, K chunks
-// [ch0, ch1) of 128.  part: [split][3n][ncol_alloc] float64 partial products.
+// Work units: (column group g, row tile t of A', K chunk c of 128), in the
+// order u = (g * tiles + t) * nch + c.  CTA k of the G takes the units
+// [k U / G, (k + 1) U / G) (U units in all): a contiguous run, so every SM
+// has work whatever the number of row tiles, and a tile's K range is split
+// among at most a few consecutive CTAs.  CTA k writes its part of tile
+// q = g * tiles + t as segment k - first_cta(q) of part:
+// part[segment][3n][ncol_alloc] float64.
+__host__ __device__ __forceinline__ int64_t oz_cta_of(int64_t u, int64_t U, int64_t G) {
+    return ((u + 1) * G - 1) / U;  // the CTA whose run holds unit u
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 k_oz_gemm(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUtensorMap xmap,
           const int *__restrict__ ea, const int *__restrict__ ex, int64_t rows, int ncol, int ncol_alloc, int nch,
-          int chunks_per_split, double *__restrict__ part, unsigned *__restrict__ status) {
+          int tiles, int64_t units, double *__restrict__ part, unsigned *__restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
     __shared__ __align__(8) uint64_t bar_full[STAGES], bar_empty[STAGES], bar_accf[2], bar_acce[2], bar_drain;
     __shared__ uint32_t s_tmem;
     __shared__ volatile int s_abort;
     const uint32_t base_addr = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t row0 = (int64_t)blockIdx.x * TM;
-    const int col0 = blockIdx.y * W;
-    const int split = blockIdx.z;
-    const int ch0 = split * chunks_per_split, ch1 = min(nch, ch0 + chunks_per_split);
-    const int nchunk = ch1 - ch0;  // >= 1 (the host sizes the splits)
+    const int64_t G = gridDim.x, k = blockIdx.x;
+    const int64_t u_begin = k * units / G, u_end = (k + 1) * units / G;  // at least one unit (G <= units)
+    const int nchunk = (int)(u_end - u_begin);
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -367,9 +392,10 @@ k_oz_gemm(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUte
                 const uint32_t fb = smem_u32(&bar_full[st]);
                 mbar_expect_tx(fb, STAGE);
                 const uint32_t sa = base_addr + st * STAGE;
-                const int k0 = ch0 * KCH + (int)g * KS;
-                tma_load_3d(sa, &amap, k0, (int)row0, 0, fb);
-                tma_load_3d(sa + A_STAGE, &xmap, k0, col0, 0, fb);
+                const int64_t u = u_begin + g / kStepsPerCh, q = u / nch;
+                const int c = (int)(u - q * nch), kin = (int)(g % kStepsPerCh) * KS;
+                tma_load_5d(sa, &amap, kin, 0, 0, c, (int)(q % tiles), fb);
+                tma_load_3d(sa + A_STAGE, &xmap, c * KCH + kin, (int)(q / tiles) * W, 0, fb);
             }
             // our own copies in flight: wait (bounded) for the last stages to land
             for (uint32_t q = g > (uint32_t)STAGES ? g - STAGES : 0; q < g; q++) {
@@ -396,11 +422,14 @@ k_oz_gemm(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUte
                     }
                     tc_fence_after();
                     const uint32_t sa = base_addr + st * STAGE;
-                    const uint64_t bd = smem_desc(sa + A_STAGE);
 #pragma unroll
-                    for (int k = 0; k < kDig; k++)  // A digit k against X digits 0 .. 7-k: level blocks k .. 7
-                        mma_bf16(d + (uint32_t)(W * k), smem_desc(sa + k * A_SLICE), bd, idesc_for(k),
-                                 (s > 0 || k > 0) ? 1u : 0u);
+                    for (int ks = 0; ks < KS / 16; ks++) {
+                        const uint64_t bd = smem_desc(sa + A_STAGE + 32 * ks);
+#pragma unroll
+                        for (int k = 0; k < kDig; k++)  // A digit k against X digits 0 .. 7-k: level blocks k .. 7
+                            mma_bf16(d + (uint32_t)(W * k), smem_desc(sa + k * A_SLICE + 32 * ks), bd, idesc_for(k),
+                                     (s > 0 || ks > 0 || k > 0) ? 1u : 0u);
+                    }
                     mma_commit(smem_u32(&bar_empty[st]));  // stage free once these MMAs finish
                 }
                 if (ok) mma_commit(smem_u32(&bar_accf[buf]));  // chunk's level sums ready
@@ -419,31 +448,25 @@ k_oz_gemm(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUte
         long long ga[16], gb[16];               // levels 0-3 and 4-7 (7 bits apart within each)
 #pragma unroll
         for (int i = 0; i < 16; i++) ga[i] = gb[i] = 0;
-        bool ok = true;
         for (int c = 0; c < nchunk; c++) {
             const uint32_t buf = (uint32_t)c & 1u, aph = ((uint32_t)c >> 1) & 1u;
-            ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status, kSite | 4u);
-            if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-            }
+            const bool ok = mbar_wait(smem_u32(&bar_accf[buf]), aph, &s_abort, status, kSite | 4u);
+            if (!__all_sync(0xffffffffu, ok)) break;
             tc_fence_after();
             const uint32_t t0 = tmem + buf * 256u + (uint32_t)(16 * half) + lane_base;
 #pragma unroll
             for (int grp = 0; grp < 2; grp++) {
-                int p[2][16];  // level pairs (2 lv, 2 lv + 1) of the group, 7 bits apart: < 2^30
+                // the group's four level blocks in flight together, one wait
+                uint32_t v[4][16];
 #pragma unroll
-                for (int pr = 0; pr < 2; pr++) {
-                    float hi[16], lo[16];
-                    const int lv = 4 * grp + 2 * pr;
-                    tmem_ld16(t0 + (uint32_t)(W * lv), hi);
-                    tmem_ld16(t0 + (uint32_t)(W * (lv + 1)), lo);
-#pragma unroll
-                    for (int i = 0; i < 16; i++) p[pr][i] = int_of(hi[i]) * 128 + int_of(lo[i]);
-                }
+                for (int l = 0; l < 4; l++) tmem_ld16(t0 + (uint32_t)(W * (4 * grp + l)), v[l]);
+                tmem_wait();
 #pragma unroll
                 for (int i = 0; i < 16; i++) {
-                    const long long t = (long long)p[0][i] * 16384 + p[1][i];
+                    // level pairs 7 bits apart (< 2^30), then the pairs 14 bits apart
+                    const int p0 = int_of(__uint_as_float(v[0][i])) * 128 + int_of(__uint_as_float(v[1][i]));
+                    const int p1 = int_of(__uint_as_float(v[2][i])) * 128 + int_of(__uint_as_float(v[3][i]));
+                    const long long t = ((long long)p0 << 14) + p1;
                     if (grp == 0) ga[i] += t;
                     else gb[i] += t;
                 }
@@ -451,23 +474,31 @@ k_oz_gemm(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUte
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));  // accumulator free for chunk c + 2
-        }
-        // Y = 2^(Ea + Ex + 77) (ga + 2^-28 gb), rounded once; a non-finite row
-        // or column gives NaN
-        const int64_t row = row0 + quad * 32 + lane;
-        if (ok && row < rows) {
-            const int qa = ea[row];
-            double *dst = part + ((int64_t)split * rows + row) * ncol_alloc + col0 + 16 * half;
-            const double two_m28 = 3.7252902984619141e-09;  // 2^-28
+            // the end of this CTA's part of a tile: Y = 2^(Ea + Ex + 77) (ga +
+            // 2^-28 gb), rounded once, as the tile's segment k - first CTA; a
+            // non-finite row or column gives NaN
+            const int64_t u = u_begin + c, q = u / nch;
+            if (u + 1 < u_end && (u + 1) / nch == q) continue;
+            const int64_t seg = k - oz_cta_of(q * nch, units, G);
+            const int64_t row = (q % tiles) * TM + quad * 32 + lane;
+            const int col0 = (int)(q / tiles) * W + 16 * half;
+            if (row < rows) {
+                const int qa = ea[row];
+                double *dst = part + (seg * rows + row) * ncol_alloc + col0;
+                const double two_m28 = 3.7252902984619141e-09;  // 2^-28
 #pragma unroll
-            for (int i = 0; i < 16; i++) {
-                const int c = col0 + 16 * half + i;
-                if (c >= ncol) break;
-                const int qx = ex[c];
-                // 2^(Ea + Ex + 98 - 21) = 2^(qa + qx - 2077); ga, gb are exact integers below 2^53
-                dst[i] = (qa < 0 || qx < 0) ? __longlong_as_double(0x7FF8000000000000ll)
-                                            : ldexp(__fma_rn((double)gb[i], two_m28, (double)ga[i]), qa + qx - 2077);
+                for (int i = 0; i < 16; i++) {
+                    const int cx = col0 + i;
+                    if (cx >= ncol) break;
+                    const int qx = ex[cx];
+                    // 2^(Ea + Ex + 98 - 21) = 2^(qa + qx - 2077); ga, gb are exact integers below 2^53
+                    dst[i] = (qa < 0 || qx < 0)
+                                 ? __longlong_as_double(0x7FF8000000000000ll)
+                                 : ldexp(__fma_rn((double)gb[i], two_m28, (double)ga[i]), qa + qx - 2077);
+                }
             }
+#pragma unroll
+            for (int i = 0; i < 16; i++) ga[i] = gb[i] = 0;
         }
     }
     tc_fence_before();
@@ -479,26 +510,32 @@ k_oz_gemm(const __grid_constant__ CUtensorMap amap, const __grid_constant__ CUte
 }
 
 // r_f = b - (j w (L x_f) - j (Psi x_f) / w + Zs_f (G x_f)) from the partial
-// products of the splits, one thread per (row, slot index, right-hand side).
-__global__ void k_oz_combine(const double *__restrict__ part, int nsplit, int64_t n, int ncol_alloc,
-                             const ZsSlotParam *__restrict__ params, const double2 *__restrict__ b, int nrhs,
-                             const int *__restrict__ slots, int nslot, float2 *__restrict__ out64,
-                             int64_t out64_stride, double2 *__restrict__ out128, int64_t out128_stride) {
+// products, one thread per (row, slot index, right-hand side): the segments of
+// each tile are summed in a fixed order.
+__global__ void k_oz_combine(const double *__restrict__ part, int64_t n, int ncol_alloc, int nch, int tiles,
+                             int64_t units, int64_t grid, const ZsSlotParam *__restrict__ params,
+                             const double2 *__restrict__ b, int nrhs, const int *__restrict__ slots, int nslot,
+                             float2 *__restrict__ out64, int64_t out64_stride, double2 *__restrict__ out128,
+                             int64_t out128_stride) {
     const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= n * nslot * nrhs) return;
     const int64_t i = t % n;
     const int kr = (int)(t / n);  // k * nrhs + r
     const int k = kr / nrhs, r = kr - k * nrhs;
-    const int c = 2 * kr;         // columns (re, im) of x_{slots[k]}[r]
+    const int c = 2 * kr;         // columns (re, im) of x_{slots[k]}[r], in one column group
     const int64_t rows = 3 * n;
     double y[3][2] = {{0.0, 0.0}, {0.0, 0.0}, {0.0, 0.0}};
-    for (int s = 0; s < nsplit; s++)
 #pragma unroll
-        for (int m = 0; m < 3; m++) {
-            const double2 v = *reinterpret_cast<const double2 *>(part + ((int64_t)s * rows + m * n + i) * ncol_alloc + c);
+    for (int m = 0; m < 3; m++) {
+        const int64_t row = m * n + i;
+        const int64_t q = (int64_t)(c / W) * tiles + row / TM, u0 = q * nch;
+        const int64_t k0 = oz_cta_of(u0, units, grid), k1 = oz_cta_of(u0 + nch - 1, units, grid);
+        for (int64_t sg = 0; sg <= k1 - k0; sg++) {
+            const double2 v = *reinterpret_cast<const double2 *>(part + (sg * rows + row) * ncol_alloc + c);
             y[m][0] += v.x;
             y[m][1] += v.y;
         }
+    }
     const int slot = slots[k];
     const ZsSlotParam sp = params[slot];
     const double w = sp.omega, rw = sp.pad;  // pad = RN(1/omega)
@@ -525,7 +562,7 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     return fn;
 }
 
-// dims (K = n, rows, digit plane = 8); boxes of 16 K x box_rows rows x 8 planes, 32-byte swizzle
+// dims (K = n, rows, digit plane = 8); boxes of 32 K x box_rows rows x 8 planes, 64-byte swizzle
 cudaError_t encode_digits(void *map_out, const __nv_bfloat16 *base, int64_t n, int64_t n_pad, int64_t rows,
                           int64_t rows_alloc, int box_rows) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
@@ -535,7 +572,7 @@ cudaError_t encode_digits(void *map_out, const __nv_bfloat16 *base, int64_t n, i
     const cuuint32_t box[3] = {(cuuint32_t)KS, (cuuint32_t)box_rows, (cuuint32_t)kDig};
     const cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = enc(reinterpret_cast<CUtensorMap *>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, (void *)base,
-                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                     dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -543,6 +580,10 @@ cudaError_t encode_digits(void *map_out, const __nv_bfloat16 *base, int64_t n, i
 }  // namespace
 
 int64_t zs_oz_n_pad(int64_t n) { return (n + 7) / 8 * 8; }
+int64_t zs_oz_a_bytes(int64_t n) {
+    const int64_t tiles = (3 * n + TM - 1) / TM, nch = (n + KCH - 1) / KCH;
+    return tiles * nch * kDig * TM * KCH * 2;
+}
 int zs_oz_ncol_alloc(int ncol) { return (ncol + W - 1) / W * W; }
 
 cudaError_t zs_launch_oz_split_a(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0,
@@ -550,13 +591,27 @@ cudaError_t zs_launch_oz_split_a(const double *L, const double *Psi, const doubl
     if (n < 1 || r0 < 0 || r1 > n || r0 > r1) return cudaErrorInvalidValue;
     if (r1 == r0) return cudaSuccess;
     const int64_t warps = 3 * (r1 - r0);
-    k_oz_split_a<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(L, Psi, G, n, zs_oz_n_pad(n), r0, r1,
+    k_oz_split_a<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(L, Psi, G, n, (n + KCH - 1) / KCH, r0, r1,
                                                                static_cast<__nv_bfloat16 *>(dig), ea);
     return cudaGetLastError();
 }
 
+// dims (K in chunk = 128, row in tile = 128, plane = 8, chunk = nch, tile);
+// boxes of KS K x 128 rows x 8 planes of one unit, 64-byte swizzle
 cudaError_t zs_oz_a_map(const void *dig, int64_t n, void *map_out) {
-    return encode_digits(map_out, static_cast<const __nv_bfloat16 *>(dig), n, zs_oz_n_pad(n), 3 * n, 3 * n, TM);
+    PFN_cuTensorMapEncodeTiled_v12000 enc = get_encode();
+    if (!enc) return cudaErrorNotSupported;
+    const int64_t tiles = (3 * n + TM - 1) / TM, nch = (n + KCH - 1) / KCH;
+    const cuuint64_t dims[5] = {(cuuint64_t)KCH, (cuuint64_t)TM, (cuuint64_t)kDig, (cuuint64_t)nch,
+                                (cuuint64_t)tiles};
+    const cuuint64_t unit = (cuuint64_t)kDig * TM * KCH * 2;
+    const cuuint64_t strides[4] = {(cuuint64_t)KCH * 2, (cuuint64_t)TM * KCH * 2, unit, unit * nch};
+    const cuuint32_t box[5] = {(cuuint32_t)KS, (cuuint32_t)TM, (cuuint32_t)kDig, 1, 1};
+    const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(reinterpret_cast<CUtensorMap *>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, (void *)dig, dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 cudaError_t zs_launch_residual_oz(const void *amap, const int *ea, int64_t n, const ZsSlotParam *params,
@@ -579,23 +634,28 @@ cudaError_t zs_launch_residual_oz(const void *amap, const int *ea, int64_t n, co
     alignas(64) CUtensorMap xmap;
     e = encode_digits(&xmap, xd, n, n_pad, ncol, ncol_alloc, W);
     if (e != cudaSuccess) return e;
-    // K splits: about one CTA per SM over the row tiles and column groups
-    const int row_tiles = (int)((rows + TM - 1) / TM), col_groups = ncol_alloc / W;
+    // the units over one CTA per SM (fewer if there are fewer units, or if the
+    // segments of the most split tile would not fit the partial buffer)
+    const int tiles = (int)((rows + TM - 1) / TM), col_groups = ncol_alloc / W;
     const int nch = (int)((n + KCH - 1) / KCH);
-    int nsplit = num_sms / (row_tiles * col_groups);
-    nsplit = nsplit < 1 ? 1 : nsplit > nch ? nch : nsplit;
-    while ((int64_t)nsplit * rows * ncol_alloc > part_cap && nsplit > 1) nsplit--;
-    if ((int64_t)nsplit * rows * ncol_alloc > part_cap) return cudaErrorInvalidValue;
-    const int cps = (nch + nsplit - 1) / nsplit;
-    nsplit = (nch + cps - 1) / cps;  // every split has at least one chunk
+    const int64_t units = (int64_t)col_groups * tiles * nch;
+    int64_t grid = std::min<int64_t>(num_sms, units);
+    auto max_segments = [&](int64_t G) {
+        int64_t most = 0;
+        for (int64_t q = 0; q < (int64_t)col_groups * tiles; q++)
+            most = std::max(most, oz_cta_of(q * nch + nch - 1, units, G) - oz_cta_of(q * nch, units, G) + 1);
+        return most;
+    };
+    while (grid > 1 && max_segments(grid) * rows * ncol_alloc > part_cap) grid--;
+    if (max_segments(grid) * rows * ncol_alloc > part_cap) return cudaErrorInvalidValue;
     const CUtensorMap &am = *reinterpret_cast<const CUtensorMap *>(amap);
-    k_oz_gemm<<<dim3((unsigned)row_tiles, (unsigned)col_groups, (unsigned)nsplit), kThreads, SMEM, st>>>(
-        am, xmap, ea, ex, rows, ncol, ncol_alloc, nch, cps, part, status);
+    k_oz_gemm<<<(unsigned)grid, kThreads, SMEM, st>>>(am, xmap, ea, ex, rows, ncol, ncol_alloc, nch, tiles, units, part,
+                                                     status);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int64_t threads = n * nslot * nrhs;
-    k_oz_combine<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(part, nsplit, n, ncol_alloc, params, b, nrhs,
-                                                                   slots, nslot, out_c64, out64_stride, out_c128,
-                                                                   out128_stride);
+    k_oz_combine<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(part, n, ncol_alloc, nch, tiles, units, grid,
+                                                                   params, b, nrhs, slots, nslot, out_c64,
+                                                                   out64_stride, out_c128, out128_stride);
     return cudaGetLastError();
 }

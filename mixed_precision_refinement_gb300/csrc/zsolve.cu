@@ -532,12 +532,14 @@ int fallback_slot(zsolve_ctx *ctx, Lane &ln, int slot, const double2 *b, double2
 
 // Workspaces of the residual mode OZ (on first use): the digits of A' and,
 // per lane, those of x for every column a lane can hold (2 S nrhs_max) and
-// partial products for up to four K splits.
+// partial products for up to eight CTAs' segments of a tile's K range.
 int ensure_oz(zsolve_ctx *ctx) {
     if (ctx->oz_a) return ZSOLVE_OK;
     const int64_t n = ctx->n, n_pad = zs_oz_n_pad(n);
     const int ncol_cap = zs_oz_ncol_alloc(2 * ctx->S * ctx->nrhs_max);
-    bool ok = cudaMalloc(&ctx->oz_a, (size_t)8 * 3 * n * n_pad * 2) == cudaSuccess &&
+    // the padding of the tile-major digits (rows past 3n) is never written: zero once
+    bool ok = cudaMalloc(&ctx->oz_a, (size_t)zs_oz_a_bytes(n)) == cudaSuccess &&
+              cudaMemset(ctx->oz_a, 0, (size_t)zs_oz_a_bytes(n)) == cudaSuccess &&
               cudaMalloc(&ctx->oz_ea, (size_t)3 * n * sizeof(int)) == cudaSuccess &&
               zs_oz_a_map(ctx->oz_a, n, ctx->oz_amap) == cudaSuccess &&
               (ctx->oz_stream || cudaStreamCreateWithFlags(&ctx->oz_stream, cudaStreamNonBlocking) == cudaSuccess) &&
@@ -546,7 +548,7 @@ int ensure_oz(zsolve_ctx *ctx) {
     for (auto &ln : ctx->lane) {
         if (!ok) break;
         ln.oz_ncol_cap = ncol_cap;
-        ln.oz_part_cap = (int64_t)4 * 3 * n * ncol_cap;
+        ln.oz_part_cap = (int64_t)8 * 3 * n * ncol_cap;  // up to 8 CTAs' segments of a tile
         ok = cudaMalloc(&ln.oz_x, (size_t)8 * ncol_cap * n_pad * 2) == cudaSuccess &&
              cudaMalloc(&ln.oz_ex, (size_t)ncol_cap * sizeof(int)) == cudaSuccess &&
              cudaMalloc(&ln.oz_part, (size_t)ln.oz_part_cap * sizeof(double)) == cudaSuccess;
