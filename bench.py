@@ -655,6 +655,10 @@ def run_ours(args):
                    "batch": args.batch or nf, "l2": "flushed between steps (512 MB write)",
                    "parallelism": f"{ws} independent replicas" if ws > 1 else "single GPU"},
         "lu_tflops": lu_tflops, "resid_gbs": res_gbs,
+        "resid_gbs_basis": "16 n^2 + 32 n nrhs bytes per frequency and evaluation (what the float64 GEMV over Z "
+                           "reads) over the residual stage's device time"
+                           + ("; the OZ mode reads 48 n^2 bytes of digits per evaluation of a lane's frequencies "
+                              "instead: its own rate is rooflines_other.k_residual" if resid_mode == "OZ" else ""),
         # the kernel with the largest device time in this run's profiled pass
         "roofline": rl[dom],
         "rooflines_other": {k: v for k, v in rl.items() if k != dom},
