@@ -220,7 +220,9 @@ cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cma
 //   A_hi, A_lo, Br_hi, Br_lo, Bi_hi, Bi_lo
 // A row i   = [Re L21(i,:) | Im L21(i,:)]
 // Br row j  = [Re U12(:,j) | -Im U12(:,j)]   (Cr = A . Br)
-// Bi row j  = [Im U12(:,j) |  Re U12(:,j)]   (Ci = A . Bi)
+// Bi row j  = [Im U12(:,j) |  Re U12(:,j)]   (Ci = A . Bi; written by the FP32
+//                                             path only: the tensor-core update
+//                                             takes Bi from Br's K halves)
 #define ZS_PACK_K (2 * ZS_NB)
 __host__ __device__ inline int64_t zs_pack_plane(int64_t n) { return n * (int64_t)ZS_PACK_K; }
 

@@ -8,10 +8,13 @@
 // the block triangular solves (K = 2 x 128 real):
 //   Re(L21 U12) = A . Br^T,  Im(L21 U12) = A . Bi^T,
 //   A = [Re L21 | Im L21],  Br = [Re U12^T | -Im U12^T],  Bi = [Im U12^T | Re U12^T].
-// One CTA owns a 128-row x 128-column complex output tile: a single
-// tcgen05.mma of shape M=128, N=256 covers both the real part (columns 0-127
-// of the accumulator, B rows from Br) and the imaginary part (columns
-// 128-255, B rows from Bi) in one fp32 TMEM accumulator of 256 columns.
+// Bi is Br with its K halves swapped and the first half negated, so only Br
+// is stored: for a 32-wide K chunk at k, Bi's chunk is -Br's at k + 128 (k <
+// 128) or Br's at k - 128.  One CTA owns a 128-row x 128-column complex
+// output tile in one fp32 TMEM accumulator of 256 columns: per K step one
+// tcgen05.mma of M=128, N=128 for the real part (columns 0-127, B = Br's
+// chunk) and one for the imaginary part (columns 128-255, B = Br's other
+// chunk, negated by the instruction's negate-B bit where the sign is -).
 //   split = 0: kind::tf32, operands rounded to tf32 once;
 //   split = 1: 3xTF32 -- x = hi + lo with hi, lo tf32; the product is formed
 //              as hi.hi + hi.lo + lo.hi (the lo.lo term is below fp32
@@ -218,13 +221,18 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr) {
 // Instruction descriptor, kind::tf32: D fp32, A/B tf32, both K-major, M=128, N=256.
 constexpr uint32_t kIdesc = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(256 >> 3) << 17) |
                             ((uint32_t)(128 >> 4) << 24);
+// the same with N = 128 (one part of a trailing update), and with B negated (bit 14)
+constexpr uint32_t kIdesc128 = (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(128 >> 3) << 17) |
+                               ((uint32_t)(128 >> 4) << 24);
+constexpr uint32_t kIdesc128Neg = kIdesc128 | (1u << 14);
 
-__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate) {
+__device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t accumulate,
+                                         uint32_t idesc = kIdesc) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a), "l"(b), "r"(kIdesc), "r"(accumulate)
+        "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -427,14 +435,19 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     mbar_expect_tx(fb, C::STAGE_BYTES);
                     const uint32_t sa = base_addr + st * C::STAGE_BYTES;
                     const int k0 = kc * KC;
+                    // the second B half: the block solves' Bi rows; for a trailing
+                    // update Br's other K half (Bi chunk k = -+ Br chunk k +- 128,
+                    // the sign applied by the MMA), so that no Bi pack is written
+                    const int pb2 = is_trsm<KIND>() ? pbi : pbr;
+                    const int k2 = is_trsm<KIND>() ? k0 : (k0 + NB) % KTOT;
                     tma_load_4d(sa, &tmap, k0, x.ra, pa, x.slot, fb);
                     tma_load_4d(sa + A_BYTES, bm, k0, x.rb, pbr, x.slot, fb);
-                    tma_load_4d(sa + A_BYTES + B_BYTES / 2, bm, k0, x.rb, pbi, x.slot, fb);
+                    tma_load_4d(sa + A_BYTES + B_BYTES / 2, bm, k2, x.rb, pb2, x.slot, fb);
                     if (SPLIT) {  // lo planes follow their hi planes
                         const uint32_t sl = sa + A_BYTES + B_BYTES;
                         tma_load_4d(sl, &tmap, k0, x.ra, pa + 1, x.slot, fb);
                         tma_load_4d(sl + A_BYTES, bm, k0, x.rb, pbr + 1, x.slot, fb);
-                        tma_load_4d(sl + A_BYTES + B_BYTES / 2, bm, k0, x.rb, pbi + 1, x.slot, fb);
+                        tma_load_4d(sl + A_BYTES + B_BYTES / 2, bm, k2, x.rb, pb2 + 1, x.slot, fb);
                     }
                 }
                 if (!ok) break;
@@ -485,15 +498,35 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                         const uint64_t ah = smem_desc(sa + ks * 32);
                         const uint64_t bh = smem_desc(sa + A_BYTES + ks * 32);
                         const uint32_t acc = (kc | ks) ? 1u : 0u;
-                        if (SPLIT) {
-                            const uint32_t sl = sa + A_BYTES + B_BYTES;
-                            const uint64_t al = smem_desc(sl + ks * 32);
-                            const uint64_t bl = smem_desc(sl + A_BYTES + ks * 32);
-                            mma_tf32(d, al, bh, acc);
-                            mma_tf32(d, ah, bl, 1u);
-                            mma_tf32(d, ah, bh, 1u);
+                        const uint32_t sl = sa + A_BYTES + B_BYTES;
+                        const uint64_t al = smem_desc(sl + ks * 32);
+                        const uint64_t bl = smem_desc(sl + A_BYTES + ks * 32);
+                        if (is_trsm<KIND>()) {  // one N = 256 product: Br rows, then Bi rows
+                            if (SPLIT) {
+                                mma_tf32(d, al, bh, acc);
+                                mma_tf32(d, ah, bl, 1u);
+                                mma_tf32(d, ah, bh, 1u);
+                            } else {
+                                mma_tf32(d, ah, bh, acc);
+                            }
                         } else {
-                            mma_tf32(d, ah, bh, acc);
+                            // real part (columns 0-127) from Br, imaginary part
+                            // (columns 128-255) from Br's other K half, negated
+                            // in the first half of K
+                            const uint64_t bh2 = smem_desc(sa + A_BYTES + B_BYTES / 2 + ks * 32);
+                            const uint64_t bl2 = smem_desc(sl + A_BYTES + B_BYTES / 2 + ks * 32);
+                            const uint32_t id2 = kc * KC < NB ? kIdesc128Neg : kIdesc128;
+                            if (SPLIT) {
+                                mma_tf32(d, al, bh, acc, kIdesc128);
+                                mma_tf32(d, ah, bl, 1u, kIdesc128);
+                                mma_tf32(d, ah, bh, 1u, kIdesc128);
+                                mma_tf32(d + 128u, al, bh2, acc, id2);
+                                mma_tf32(d + 128u, ah, bl2, 1u, id2);
+                                mma_tf32(d + 128u, ah, bh2, 1u, id2);
+                            } else {
+                                mma_tf32(d, ah, bh, acc, kIdesc128);
+                                mma_tf32(d + 128u, ah, bh2, acc, id2);
+                            }
                         }
                     }
                     mma_commit(smem_u32(&bar_empty[st]));  // stage free once these MMAs finish
@@ -571,7 +604,8 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                             tma_store_4d(&cmap, sb, row0, (int)J + c32, part, x.slot);
                             bulk_commit();
                         }
-                        // trailing-update operand rows: Br = [Re U12^T | -Im U12^T], Bi = [Im U12^T | Re U12^T]
+                        // trailing-update operand rows: Br = [Re U12^T | -Im U12^T] (the
+                        // update takes Bi = [Im U12^T | Re U12^T] from it)
                         float h[32];
 #pragma unroll
                         for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q]);
@@ -586,13 +620,6 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                             publish();
                             if (lane == 0) {
                                 tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_BR_HI + lo, x.slot);
-                                bulk_commit();
-                            }
-                            sb = next_box();
-                            stage_row(sb, lane, h, 1.f);
-                            publish();
-                            if (lane == 0) {
-                                tma_store_4d(&pmap, sb, (1 - part) * NB + c32, row0, PL_BI_HI + lo, x.slot);
                                 bulk_commit();
                             }
                         }
@@ -685,19 +712,12 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                             tma_store_4d(&pmap, sb, c * 32, row0, PL_A_HI + lo, x.slot);
                             bulk_commit();
                         }
-                    } else {  // Br row j = [Re U12^T | -Im U12^T], Bi row j = [Im U12^T | Re U12^T]
+                    } else {  // Br row j = [Re U12^T | -Im U12^T] (the trailing update derives Bi from it)
                         sb = next_box();
                         stage_row(sb, lane, h, part ? -1.f : 1.f);
                         publish();
                         if (lane == 0) {
                             tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_BR_HI + lo, x.slot);
-                            bulk_commit();
-                        }
-                        sb = next_box();
-                        stage_row(sb, lane, h, 1.f);
-                        publish();
-                        if (lane == 0) {
-                            tma_store_4d(&pmap, sb, (1 - part) * NB + c32, row0, PL_BI_HI + lo, x.slot);
                             bulk_commit();
                         }
                     }

@@ -79,6 +79,7 @@ struct zsolve_ctx {
     int trsv_r = 0;        // right-hand sides per triangular-solve chain; 0: chosen per solve (ZSOLVE_TRSV_R)
     int lookahead = -1;    // next diagonal block ahead of the trailing update: -1 for few frequencies, 0 never, 1 always (ZSOLVE_LOOKAHEAD)
     int tc_cap = 0;        // testing aid: at most this many CTAs per tcgen05 launch (ZSOLVE_TC_GRID; 0: no cap)
+    int trsv_cap = 0;      // tuning aid: CTAs of each lane's triangular solves in a multi-lane batch (ZSOLVE_TRSV_CTAS; 0: SMs / lanes)
     // residual mode OZ: digits of A' = [L; Psi; G] (allocated on first use),
     // their row scales and tensor map; oz_ready while they hold the current
     // sweep's L, Psi, G
@@ -995,7 +996,7 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
                 // each lane's persistent tcgen05 grids leave room for the
                 // other lanes' diagonal blocks (one CTA per frequency)
                 ctx->lane[k].tc_grid = std::max(1, ctx->num_sms - (count - cnt[k]));
-                ctx->lane[k].trsv_grid = std::max(1, ctx->num_sms / K);
+                ctx->lane[k].trsv_grid = ctx->trsv_cap > 0 ? ctx->trsv_cap : std::max(1, ctx->num_sms / K);
                 ctx->lane[k].alone = false;
             }
             struct Alone {  // lane 0 runs alone again after the batch (the probe, single-system calls)
@@ -1197,6 +1198,7 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (const char *e = getenv("ZSOLVE_LOOKAHEAD")) ctx->lookahead = std::min(1, std::max(-1, atoi(e)));
     // testing aid: few CTAs per tcgen05 launch, so that each takes many tiles
     if (const char *e = getenv("ZSOLVE_TC_GRID")) ctx->tc_cap = std::max(0, atoi(e));
+    if (const char *e = getenv("ZSOLVE_TRSV_CTAS")) ctx->trsv_cap = std::max(0, atoi(e));
     // right-hand sides per triangular-solve chain (1, 2 or 4; unset: chosen per solve)
     if (const char *e = getenv("ZSOLVE_TRSV_R")) {
         const int r = atoi(e);
