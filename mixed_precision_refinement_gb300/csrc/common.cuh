@@ -241,7 +241,8 @@ cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int6
 // = 8 planes of 128 rows x 256:
 //   planes 0-3 W = U^-1: Br(j) = [Re W(:,j) | -Im W(:,j)], Bi(j) = [Im W(:,j) | Re W(:,j)]
 //   planes 4-7 V = L^-1: Br(k) = [Re V(k,:) | -Im V(k,:)], Bi(k) = [Im V(k,:) | Re V(k,:)]
-// each as Br hi, Br lo, Bi hi, Bi lo.
+// each as Br hi, Br lo, Bi hi, Bi lo; only the Br planes are written (the
+// tensor-core block solve takes Bi from Br's K halves).
 #define ZS_WINV_PLANE (ZS_NB * ZS_PACK_K)
 #define ZS_WINV_STRIDE (8 * ZS_WINV_PLANE)
 inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }

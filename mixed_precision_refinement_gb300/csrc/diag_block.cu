@@ -426,17 +426,15 @@ __device__ __forceinline__ void emit_one(bool upper, int l, int k, const Blk S, 
         im = *reinterpret_cast<const float4 *>(&smem[S.off + S.im + i * S.ld + j0]);
         o = (l * P + i) * (2 * NB) + k * P + j0;
     }
+    // the Br planes only (hi, lo): the tensor-core block solve takes Bi from
+    // Br's K halves
     const float4 hr = tf32_4(re), hi = tf32_4(im);
     *reinterpret_cast<float4 *>(pl + o) = hr;
     *reinterpret_cast<float4 *>(pl + o + NB) = neg4(hi);
-    *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o) = hi;
-    *reinterpret_cast<float4 *>(pl + 2 * ZS_WINV_PLANE + o + NB) = hr;
     if (mode == 2) {
         const float4 lr = tf32_4(sub4(re, hr)), li = tf32_4(sub4(im, hi));
         *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o) = lr;
         *reinterpret_cast<float4 *>(pl + ZS_WINV_PLANE + o + NB) = neg4(li);
-        *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o) = li;
-        *reinterpret_cast<float4 *>(pl + 3 * ZS_WINV_PLANE + o + NB) = lr;
     }
 }
 

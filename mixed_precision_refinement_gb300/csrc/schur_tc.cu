@@ -418,12 +418,11 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 }
                 const Tile x = tile_of<KIND>(t, tiles, base, slots, part);
                 // A rows: L21 / A21 (A planes) or A12^T (Br planes); B: the pack's
-                // own Br/Bi rows, or W / V from the inverse packs
+                // own Br rows, or W / V from the inverse packs (their Br planes)
                 const int pa = (KIND == KIND_TRSM && x.u) ? PL_BR_HI : PL_A_HI;
                 const bool use_v = KIND == KIND_TRSM_SYM || x.u;  // B = L11^-1 (else U11^-1)
                 const CUtensorMap *bm = !is_trsm<KIND>() ? &tmap : &wmap;
                 const int pbr = !is_trsm<KIND>() ? PL_BR_HI : (use_v ? WP_V : 0) + WP_BR_HI;
-                const int pbi = !is_trsm<KIND>() ? PL_BI_HI : (use_v ? WP_V : 0) + WP_BI_HI;
                 bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
@@ -435,11 +434,11 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     mbar_expect_tx(fb, C::STAGE_BYTES);
                     const uint32_t sa = base_addr + st * C::STAGE_BYTES;
                     const int k0 = kc * KC;
-                    // the second B half: the block solves' Bi rows; for a trailing
-                    // update Br's other K half (Bi chunk k = -+ Br chunk k +- 128,
-                    // the sign applied by the MMA), so that no Bi pack is written
-                    const int pb2 = is_trsm<KIND>() ? pbi : pbr;
-                    const int k2 = is_trsm<KIND>() ? k0 : (k0 + NB) % KTOT;
+                    // the second B half: Br's other K half (Bi chunk k = -+ Br
+                    // chunk k +- 128, the sign applied by the MMA), so that no Bi
+                    // plane is written, of the operand packs or the inverse packs
+                    const int pb2 = pbr;
+                    const int k2 = (k0 + NB) % KTOT;
                     tma_load_4d(sa, &tmap, k0, x.ra, pa, x.slot, fb);
                     tma_load_4d(sa + A_BYTES, bm, k0, x.rb, pbr, x.slot, fb);
                     tma_load_4d(sa + A_BYTES + B_BYTES / 2, bm, k2, x.rb, pb2, x.slot, fb);
@@ -501,32 +500,22 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                         const uint32_t sl = sa + A_BYTES + B_BYTES;
                         const uint64_t al = smem_desc(sl + ks * 32);
                         const uint64_t bl = smem_desc(sl + A_BYTES + ks * 32);
-                        if (is_trsm<KIND>()) {  // one N = 256 product: Br rows, then Bi rows
-                            if (SPLIT) {
-                                mma_tf32(d, al, bh, acc);
-                                mma_tf32(d, ah, bl, 1u);
-                                mma_tf32(d, ah, bh, 1u);
-                            } else {
-                                mma_tf32(d, ah, bh, acc);
-                            }
+                        // real part (columns 0-127) from Br, imaginary part
+                        // (columns 128-255) from Br's other K half, negated in
+                        // the first half of K
+                        const uint64_t bh2 = smem_desc(sa + A_BYTES + B_BYTES / 2 + ks * 32);
+                        const uint64_t bl2 = smem_desc(sl + A_BYTES + B_BYTES / 2 + ks * 32);
+                        const uint32_t id2 = kc * KC < NB ? kIdesc128Neg : kIdesc128;
+                        if (SPLIT) {
+                            mma_tf32(d, al, bh, acc, kIdesc128);
+                            mma_tf32(d, ah, bl, 1u, kIdesc128);
+                            mma_tf32(d, ah, bh, 1u, kIdesc128);
+                            mma_tf32(d + 128u, al, bh2, acc, id2);
+                            mma_tf32(d + 128u, ah, bl2, 1u, id2);
+                            mma_tf32(d + 128u, ah, bh2, 1u, id2);
                         } else {
-                            // real part (columns 0-127) from Br, imaginary part
-                            // (columns 128-255) from Br's other K half, negated
-                            // in the first half of K
-                            const uint64_t bh2 = smem_desc(sa + A_BYTES + B_BYTES / 2 + ks * 32);
-                            const uint64_t bl2 = smem_desc(sl + A_BYTES + B_BYTES / 2 + ks * 32);
-                            const uint32_t id2 = kc * KC < NB ? kIdesc128Neg : kIdesc128;
-                            if (SPLIT) {
-                                mma_tf32(d, al, bh, acc, kIdesc128);
-                                mma_tf32(d, ah, bl, 1u, kIdesc128);
-                                mma_tf32(d, ah, bh, 1u, kIdesc128);
-                                mma_tf32(d + 128u, al, bh2, acc, id2);
-                                mma_tf32(d + 128u, ah, bl2, 1u, id2);
-                                mma_tf32(d + 128u, ah, bh2, 1u, id2);
-                            } else {
-                                mma_tf32(d, ah, bh, acc, kIdesc128);
-                                mma_tf32(d + 128u, ah, bh2, acc, id2);
-                            }
+                            mma_tf32(d, ah, bh, acc, kIdesc128);
+                            mma_tf32(d + 128u, ah, bh2, acc, id2);
                         }
                     }
                     mma_commit(smem_u32(&bar_empty[st]));  // stage free once these MMAs finish
