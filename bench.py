@@ -16,7 +16,9 @@ samples of the same workload instead.
 from __future__ import annotations
 
 import argparse
+import atexit
 import dataclasses
+import datetime
 import json
 import re
 import math
@@ -169,23 +171,37 @@ def schur_flops(n, nb=128, lower=False):
 
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi every 50 ms from before the warm-up steps; only the samples
+    whose own timestamps fall inside the timed span [mark, stop] are kept (the
+    tool's output may be block-buffered, so the rows are read at the end)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index):
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.proc = None
+        self.t0 = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+                 "-lms", "50"], stdout=self.file, stderr=subprocess.DEVNULL)
+            atexit.register(self._end)
         except (OSError, ValueError):
             self.proc = None
+
+    def _end(self):
+        if self.proc is not None and self.proc.poll() is None:
+            self.proc.kill()
+
+    def mark(self):
+        self.t0 = datetime.datetime.now()
 
     def stop(self):
         if self.proc is None:
             return None
+        t1 = datetime.datetime.now()
+        time.sleep(0.1)  # the sample taken at the end of the span
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -195,22 +211,25 @@ class ClockSampler:
         self.file.seek(0)
         rows = [r.split(",") for r in self.file.read().strip().splitlines() if r.strip()]
         os.unlink(self.file.name)
-        sm, smax, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        timed = []
         for r in rows:
             r = [x.strip() for x in r]
             try:
-                sm.append(float(r[1]))
-                smax = max(smax, float(r[2]))
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f")
+                timed.append((ts, float(r[2]), float(r[3]), r[6:10]))
             except (ValueError, IndexError):
                 continue
-            for nm, v in zip(names, r[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
+        t0 = self.t0 or t1
+        lo, hi = t0 - datetime.timedelta(milliseconds=25), t1 + datetime.timedelta(milliseconds=60)
+        inside = [t for t in timed if lo <= t[0] <= hi]
+        if not inside:  # a span shorter than the period: the first sample after its start
+            inside = [t for t in timed if t[0] >= lo][:1]
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = {nm for t in inside for nm, v in zip(names, t[3]) if v.lower().startswith("active")}
+        return {"sm_mhz": statistics.median(t[1] for t in inside), "sm_max_mhz": max(t[2] for t in inside),
+                "reasons": sorted(reasons), "samples": len(inside)}
 
 
 def cpu_baseline(cfg, budget_s=10.0, max_freqs=None):
@@ -498,6 +517,8 @@ def run_ours(args):
     def step():
         return zs.zsolve_sweep(ctx, L, P, G, wl.omega, wl.zs, b, x)
 
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -507,10 +528,11 @@ def run_ours(args):
     args.gemm_eff = {zs.ZSOLVE_GEMM_TF32: "TF32", zs.ZSOLVE_GEMM_TF32X3: "TF32X3", zs.ZSOLVE_GEMM_FFMA: "FFMA"}[choice.chosen]
     zs.zsolve_reset_profile(ctx)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    if sampler:
+        sampler.mark()
     wall0 = time.perf_counter()
     infos = None
     for i in range(args.steps):
@@ -700,7 +722,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)  # ~0.2 s timed: the clock sampler (200 ms) sees it
+    ap.add_argument("--steps", type=int, default=100)  # ~0.6 s timed: about 12 clock samples
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=1)

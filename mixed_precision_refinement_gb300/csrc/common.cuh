@@ -238,13 +238,13 @@ cudaError_t zs_launch_trsv_seq(const float *z32, int64_t ld, int64_t plane, int6
 // Inverses of the 128x128 diagonal blocks of L (unit lower) and U (upper):
 // per slot [block][L, U][re, im][128][128] floats.  Operand packs of one
 // block's inverses for the tensor-core solves, per slot ZS_WINV_STRIDE floats
-// = 8 planes of 128 rows x 256:
-//   planes 0-3 W = U^-1: Br(j) = [Re W(:,j) | -Im W(:,j)], Bi(j) = [Im W(:,j) | Re W(:,j)]
-//   planes 4-7 V = L^-1: Br(k) = [Re V(k,:) | -Im V(k,:)], Bi(k) = [Im V(k,:) | Re V(k,:)]
-// each as Br hi, Br lo, Bi hi, Bi lo; only the Br planes are written (the
-// tensor-core block solve takes Bi from Br's K halves).
+// = 4 planes of 128 rows x 256:
+//   planes 0-1 W = U^-1: Br(j) = [Re W(:,j) | -Im W(:,j)], hi and lo
+//   planes 2-3 V = L^-1: Br(k) = [Re V(k,:) | -Im V(k,:)], hi and lo
+// No Bi = [Im | Re] plane is kept: the tensor-core block solve takes Bi from
+// Br's other K half, with the sign on the MMA's negate-B.
 #define ZS_WINV_PLANE (ZS_NB * ZS_PACK_K)
-#define ZS_WINV_STRIDE (8 * ZS_WINV_PLANE)
+#define ZS_WINV_STRIDE (4 * ZS_WINV_PLANE)
 inline int64_t zs_dinv_stride(int64_t n) { return ((n + ZS_TB2 - 1) / ZS_TB2) * 4 * ZS_TB2 * ZS_TB2; }
 // Triangular solves with 128-row blocks and the inverse diagonal blocks:
 // per slot, ngroup independent groups of nrhs (1, 2 or 4) right-hand sides

@@ -578,7 +578,7 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
     wa.xl = dinv + (int64_t)slot * dinv_stride + (J / NB) * 4 * NB * NB;  // [L, U][re, im][128][128]
     wa.xu = wa.xl + 2 * NB * NB;
     wa.pu = winv ? winv + (int64_t)slot * ZS_WINV_STRIDE : nullptr;
-    wa.pv = winv ? wa.pu + 4 * ZS_WINV_PLANE : nullptr;
+    wa.pv = winv ? wa.pu + 2 * ZS_WINV_PLANE : nullptr;
 
     // ---- LU, one 32-column panel at a time; W(p - 1) beside the base LU of panel p
     for (int p = 0; p < 4; p++) {

@@ -71,7 +71,7 @@ constexpr int kTq = 8;  // tile-index queue between the roles (the producer runs
 
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
 // inverse packs: W = U11^-1 in planes 0-3, V = L11^-1 in planes 4-7 (Br hi, Br lo, Bi hi, Bi lo)
-enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_BI_HI = 2, WP_BI_LO = 3, WP_V = 4 };
+enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_V = 2 };
 // KIND_SCHUR_LOWER: the trailing update of a complex-symmetric matrix, whose
 // Schur complement stays symmetric: only the tiles on and below the diagonal
 // (column tile <= row tile) are formed; the next step reads only those.
@@ -437,16 +437,15 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                     // the second B half: Br's other K half (Bi chunk k = -+ Br
                     // chunk k +- 128, the sign applied by the MMA), so that no Bi
                     // plane is written, of the operand packs or the inverse packs
-                    const int pb2 = pbr;
                     const int k2 = (k0 + NB) % KTOT;
                     tma_load_4d(sa, &tmap, k0, x.ra, pa, x.slot, fb);
                     tma_load_4d(sa + A_BYTES, bm, k0, x.rb, pbr, x.slot, fb);
-                    tma_load_4d(sa + A_BYTES + B_BYTES / 2, bm, k2, x.rb, pb2, x.slot, fb);
+                    tma_load_4d(sa + A_BYTES + B_BYTES / 2, bm, k2, x.rb, pbr, x.slot, fb);
                     if (SPLIT) {  // lo planes follow their hi planes
                         const uint32_t sl = sa + A_BYTES + B_BYTES;
                         tma_load_4d(sl, &tmap, k0, x.ra, pa + 1, x.slot, fb);
                         tma_load_4d(sl + A_BYTES, bm, k0, x.rb, pbr + 1, x.slot, fb);
-                        tma_load_4d(sl + A_BYTES + B_BYTES / 2, bm, k2, x.rb, pb2 + 1, x.slot, fb);
+                        tma_load_4d(sl + A_BYTES + B_BYTES / 2, bm, k2, x.rb, pbr + 1, x.slot, fb);
                     }
                 }
                 if (!ok) break;
@@ -782,9 +781,9 @@ cudaError_t zs_tc_pack_map(const float *pack, int64_t n, int nslots, int64_t pac
     return encode_f32_4d(map_out, pack, dims, strides, KC, (cuuint32_t)box_rows);
 }
 
-// Tensor map over the inverse packs: dims (K = 256, rows = 128, plane = 8, slot = S), boxes of 32 x 128.
+// Tensor map over the inverse packs: dims (K = 256, rows = 128, plane = 4, slot = S), boxes of 32 x 128.
 cudaError_t zs_tc_winv_map(const float *winv, int nslots, void *map_out) {
-    const cuuint64_t dims[4] = {(cuuint64_t)KTOT, (cuuint64_t)NB, 8, (cuuint64_t)nslots};
+    const cuuint64_t dims[4] = {(cuuint64_t)KTOT, (cuuint64_t)NB, 4, (cuuint64_t)nslots};
     const cuuint64_t strides[3] = {(cuuint64_t)KTOT * 4, (cuuint64_t)ZS_WINV_PLANE * 4,
                                    (cuuint64_t)ZS_WINV_STRIDE * 4};
     return encode_f32_4d(map_out, winv, dims, strides, KC, NB);
