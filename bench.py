@@ -655,9 +655,20 @@ def run_ours(args):
                                st["residual"]["launches"], res_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
                                "16 n^2 + 32 n nrhs bytes per evaluation and frequency")
     lanes = 2 if nf >= 2 else 1
-    rl["k_assemble"] = obj("k_assemble", "hbm", st["assemble"]["ms"], st["assemble"]["launches"],
-                           (24.0 * n * n * lanes + 24.0 * n * n * nf) * steps, hbm, "GB/s", f"{peak_src} copy",
-                           "24 n^2 bytes of L, Psi, G read once per lane + 24 n^2 written per frequency")
+    # a lane whose residual reads L, Psi, G (LPG; OZ with four or more pairs)
+    # assembles the float32 planes alone (k_assemble32: 8 n^2 written per
+    # frequency), the others the float64 matrix too (k_assemble: 24 n^2)
+    asm_bytes, only32 = 0.0, []
+    for k in range(lanes):
+        c = nf // lanes + (1 if k < nf % lanes else 0)
+        o32 = resid_mode == "LPG" or (resid_mode == "OZ" and c * nrhs >= 4)
+        only32.append(o32)
+        asm_bytes += 24.0 * n * n + (8.0 if o32 else 24.0) * n * n * c
+    asm_kernel = "k_assemble32" if all(only32) else "k_assemble" if not any(only32) else "k_assemble32 + k_assemble"
+    rl["k_assemble"] = obj(asm_kernel, "hbm", st["assemble"]["ms"], st["assemble"]["launches"],
+                           asm_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
+                           "24 n^2 bytes of L, Psi, G read once per lane + 8 n^2 (float32 planes alone) or 24 n^2 "
+                           "(with the float64 matrix) written per frequency")
     ktimes = kernel_times(stage_ms, args.gemm_eff)
     dom = dominant_kernel(ktimes, list(rl))
     tot_k = sum(ktimes.values())

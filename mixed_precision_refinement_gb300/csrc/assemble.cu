@@ -41,6 +41,21 @@
 //
 // Bound: FP64 pipe (then HBM).  Algorithmic bytes per launch = 24 n^2 (read)
 // + 24 n^2 per frequency (16 written as float64 complex, 8 as float32 complex).
+//
+// k_assemble32 forms the float32 planes alone, for sweeps whose residual
+// never reads the float64 matrix (the tensor-core residual works from L, Psi
+// and G; so does the grouped one).  It issues no float64 arithmetic per
+// frequency: every input is split once into a pair of floats, hi = RN32(x)
+// and lo = RN32(x - hi) (one DFMA for the exact difference, the roundings on
+// the bit pattern), and per frequency the entry is formed in double-float
+// arithmetic (products with their exact FMA errors, Knuth's TwoSum for the
+// sums; T. J. Dekker, "A floating-point technique for extending the available
+// precision", Numer. Math. 1971) and rounded once.  The pair carries about 44
+// bits, so the result is RN32 of the float64 entry except where that entry
+// lies within about 2^-20 of its float32 ulp from a rounding midpoint (or
+// where omega L and Psi/omega cancel to that degree), where it may be one
+// float32 ulp away: the factorisation of either matrix serves the
+// refinement alike.  Bound: HBM, 24 n^2 read + 8 n^2 per frequency written.
 #include "common.cuh"
 
 namespace {
@@ -102,8 +117,10 @@ __device__ __forceinline__ int one_entry(const ZsSlotParam &sp, double l, double
     }
     if (valid) {
         __stcs(z64e, make_double2(re, im));
-        __stcs(z32e, d2f_rn(re));
-        __stcs(z32e + plane, d2f_rn(im));
+        if (plane >= 0) {  // plane < 0: the float64 matrix only
+            __stcs(z32e, d2f_rn(re));
+            __stcs(z32e + plane, d2f_rn(im));
+        }
     }
     // the larger biased exponent of the two parts (0 for an entry not stored)
     const int er = (int)((zs::bits_of(re).hi >> 20) & 0x7FFu), ei = (int)((zs::bits_of(im).hi >> 20) & 0x7FFu);
@@ -182,6 +199,116 @@ k_assemble(const double *__restrict__ L, const double *__restrict__ Psi, const d
     }
 }
 
+// ---------------------------------------------------------------- float32 planes only
+
+__device__ __noinline__ double f2d_slow(float x) { return (double)x; }
+
+// float32 -> float64 from the bit pattern (the hardware conversion for
+// subnormals, infinities and NaN)
+__device__ __forceinline__ double f2d_bits(float x) {
+    const unsigned u = __float_as_uint(x), e = (u >> 23) & 0xFFu;
+    if ((u & 0x7FFFFFFFu) == 0u) return zs::double_of(0u, u);  // signed zero
+    if (e == 0u || e == 0xFFu) return f2d_slow(x);
+    return zs::double_of(u << 29, (u & 0x80000000u) | ((e + 896u) << 20) | ((u & 0x7FFFFFu) >> 3));
+}
+
+// x = hi + lo + O(2^-48 |x|): hi = RN32(x), lo = RN32(x - hi) (mone = -1 at run time)
+struct F2 {
+    float h, l;
+};
+__device__ __forceinline__ F2 split2(double x, double mone) {
+    const float h = d2f_rn(x);
+    return {h, d2f_rn(__fma_rn(f2d_bits(h), mone, x))};
+}
+
+// a * b for pairs, as a pair (h, l) with h = RN(ah bh)
+__device__ __forceinline__ F2 mul2(F2 a, F2 b) {
+    const float h = __fmul_rn(a.h, b.h);
+    return {h, __fmaf_rn(a.h, b.l, __fmaf_rn(a.l, b.h, __fmaf_rn(a.h, b.h, -h)))};
+}
+
+// a + b for pairs (TwoSum of the high parts; the low parts added to its error)
+__device__ __forceinline__ F2 add2(F2 a, F2 b) {
+    const float s = __fadd_rn(a.h, b.h);
+    const float v = __fsub_rn(s, a.h);
+    const float e = __fadd_rn(__fsub_rn(a.h, __fsub_rn(s, v)), __fsub_rn(b.h, v));
+    return {s, __fadd_rn(e, __fadd_rn(a.l, b.l))};
+}
+__device__ __forceinline__ F2 neg2(F2 a) { return {-a.h, -a.l}; }
+// RN32 of the pair; a zero low part leaves the high part, sign of zero included
+__device__ __forceinline__ float round2(F2 a) { return a.l == 0.f ? a.h : __fadd_rn(a.h, a.l); }
+
+struct SlotF {  // a frequency's constants as pairs: omega, RN(1/omega), Zs
+    F2 w, r, zr, zi;
+};
+
+// both float32 parts of one entry at one frequency; warp_gzero as in one_entry
+__device__ __forceinline__ void one_entry32(const SlotF &sf, F2 l, F2 p, F2 g, bool warp_gzero, bool valid,
+                                            float *__restrict__ z32e, int64_t plane) {
+    const F2 t = add2(mul2(sf.w, l), neg2(mul2(sf.r, p)));  // omega L - Psi / omega
+    float re, im;
+    if (warp_gzero) {
+        // Zs.re * (+-0) and t + Zs.im * (+-0): zeros, with the signs the
+        // float64 formula gives them
+        const unsigned gs = __float_as_uint(g.h) & 0x80000000u;
+        const unsigned zr = (__float_as_uint(sf.zr.h) & 0x80000000u) ^ gs;
+        const unsigned zi = (__float_as_uint(sf.zi.h) & 0x80000000u) ^ gs;
+        re = __uint_as_float(zr);
+        const float tv = round2(t);
+        const unsigned tb = __float_as_uint(tv);
+        im = (tb & 0x7FFFFFFFu) == 0u ? __uint_as_float(tb & zi) : tv;
+    } else {
+        re = round2(mul2(sf.zr, g));
+        im = round2(add2(t, mul2(sf.zi, g)));
+    }
+    if (valid) {
+        __stcs(z32e, re);
+        __stcs(z32e + plane, im);
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+k_assemble32(const double *__restrict__ L, const double *__restrict__ Psi, const double *__restrict__ G, int64_t n,
+             int64_t r0, int64_t r1, const ZsSlotParam *__restrict__ params, int nslot, float *__restrict__ z32,
+             int64_t ld, int64_t plane, int64_t z32_stride, double mone) {
+    __shared__ SlotF sf[kMaxSlots];
+    const int lane = threadIdx.x & 31;
+    for (int s = threadIdx.x; s < nslot; s += blockDim.x) {
+        const ZsSlotParam q = params[s];
+        sf[s] = SlotF{split2(q.omega, mone), split2(q.pad, mone), split2(q.zs_re, mone), split2(q.zs_im, mone)};
+    }
+    __syncthreads();
+    for (int64_t i = r0 + blockIdx.x; i < r1; i += gridDim.x) {
+        const int64_t row = i * n, row32 = i * ld;
+        for (int64_t jw = threadIdx.x - lane; jw < n; jw += blockDim.x) {
+            const int64_t jv = jw + lane;
+            const bool valid = jv < n;
+            const int64_t j = valid ? jv : n - 1;
+            const int64_t e = row + j;
+            const double gd = __ldcs(G + e);
+            const F2 l = split2(__ldcs(L + e), mone), p = split2(__ldcs(Psi + e), mone);
+            const bool warp_gzero = __all_sync(0xffffffffu, zs::is_zero(zs::bits_of(gd)));
+            const F2 g = warp_gzero ? F2{__uint_as_float(zs::bits_of(gd).hi & 0x80000000u), 0.f} : split2(gd, mone);
+            float *zq = z32 + row32 + j;
+            int s = 0;
+#pragma unroll 1
+            for (; s + 4 <= nslot; s += 4) {
+                float *zq1 = zq + z32_stride, *zq2 = zq1 + z32_stride, *zq3 = zq2 + z32_stride;
+                one_entry32(sf[s], l, p, g, warp_gzero, valid, zq, plane);
+                one_entry32(sf[s + 1], l, p, g, warp_gzero, valid, zq1, plane);
+                one_entry32(sf[s + 2], l, p, g, warp_gzero, valid, zq2, plane);
+                one_entry32(sf[s + 3], l, p, g, warp_gzero, valid, zq3, plane);
+                zq = zq3 + z32_stride;
+            }
+#pragma unroll 1
+            for (; s < nslot; s++) {
+                one_entry32(sf[s], l, p, g, warp_gzero, valid, zq, plane);
+                zq += z32_stride;
+            }
+        }
+    }
+}
+
 }  // namespace
 
 cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0, int64_t r1,
@@ -197,7 +324,24 @@ cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double 
     int64_t cap = (int64_t)sms * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    k_assemble<<<(unsigned)blocks, kThreads, 0, st>>>(L, Psi, G, n, r0, r1, params, nslot, z64, z64_stride,
-                                                      z32, ld, plane, z32_stride, zexp, -0.0, 1.0);
+    k_assemble<<<(unsigned)blocks, kThreads, 0, st>>>(L, Psi, G, n, r0, r1, params, nslot, z64, z64_stride, z32, ld,
+                                                      z32 ? plane : -1, z32_stride, zexp, -0.0, 1.0);
+    return cudaGetLastError();
+}
+
+cudaError_t zs_launch_assemble32(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0,
+                                 int64_t r1, const ZsSlotParam *params, int nslot, float *z32, int64_t ld,
+                                 int64_t plane, int64_t z32_stride, cudaStream_t st) {
+    if (nslot > kMaxSlots || r0 < 0 || r1 > n || r0 > r1 || !z32) return cudaErrorInvalidValue;
+    if (r0 == r1) return cudaSuccess;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    int64_t blocks = r1 - r0;
+    int64_t cap = (int64_t)sms * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    k_assemble32<<<(unsigned)blocks, kThreads, 0, st>>>(L, Psi, G, n, r0, r1, params, nslot, z32, ld, plane,
+                                                        z32_stride, -1.0);
     return cudaGetLastError();
 }

@@ -143,13 +143,18 @@ int zs_ctx_nrhs_max(const zsolve_ctx *ctx);
 // All return cudaGetLastError() of the launch.  Matrices of a batch are
 // strided by the given slot strides (elements).
 
-// Z64 (c128, ld n) and the complex float32 planes (re at z32, im at z32 + plane),
-// rows r0 .. r1-1.  zexp (NULL: not recorded): per slot n ints, the largest
+// Z64 (c128, ld n) and the complex float32 planes (re at z32, im at z32 + plane;
+// z32 = NULL: Z64 alone), rows r0 .. r1-1.  zexp (NULL: not recorded): per slot n ints, the largest
 // biased exponent of each row of the slot's Z64.
 cudaError_t zs_launch_assemble(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0, int64_t r1,
                                const ZsSlotParam *params, int nslot, double2 *z64, int64_t z64_stride,
                                float *z32, int64_t ld, int64_t plane, int64_t z32_stride,
                                cudaStream_t st, int *zexp = nullptr);
+// The float32 planes alone, rows r0 .. r1-1, without float64 arithmetic per
+// frequency (double-float evaluation rounded once; assemble.cu)
+cudaError_t zs_launch_assemble32(const double *L, const double *Psi, const double *G, int64_t n, int64_t r0,
+                                 int64_t r1, const ZsSlotParam *params, int nslot, float *z32, int64_t ld,
+                                 int64_t plane, int64_t z32_stride, cudaStream_t st);
 
 // Factorisation steps at outer-block column J for nslot slots listed in slots[].
 // inv32: per slot and outer block, ZS_INV32_STRIDE floats:

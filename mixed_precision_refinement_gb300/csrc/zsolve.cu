@@ -142,8 +142,15 @@ struct zsolve_ctx {
         double *oz_part = nullptr;
         int oz_ncol_cap = 0;
         int64_t oz_part_cap = 0;
+        // whether this lane's float64 matrices were formed: where the residual
+        // works from L, Psi, G alone (OZ, LPG) a sweep assembles the float32
+        // planes only, and the fallback then forms a stalled frequency's
+        // float64 matrix from the call's inputs
+        bool z64_formed = true;
     };
     Lane lane[kMaxLanes];
+    int cur_nrhs = 0;  // right-hand sides of the running sweep call
+    bool asm32_planes = false;  // testing aid: zsolve_assemble's float32 planes from the float32-only kernel
     int assembled = 0, factored = 0, fb_ready = 0;
     std::mutex err_mu, prof_mu, fb_mu;  // error text; profile records; fallback workspace
     // stage profile: launch counts always, event-timed spans with opts.profile
@@ -509,8 +516,17 @@ int fallback_slot(zsolve_ctx *ctx, Lane &ln, int slot, const double2 *b, double2
     std::lock_guard<std::mutex> lock(ctx->fb_mu);
     ZS_TRY(ensure_fallback(ctx));
     const int64_t n = ctx->n;
-    ZS_CU(cudaMemcpyAsync(ctx->fb_a, ctx->z64 + (int64_t)slot * ctx->z64_stride, (size_t)n * n * sizeof(double2),
-                          cudaMemcpyDeviceToDevice, ln.stream));
+    if (ln.z64_formed) {
+        ZS_CU(cudaMemcpyAsync(ctx->fb_a, ctx->z64 + (int64_t)slot * ctx->z64_stride, (size_t)n * n * sizeof(double2),
+                              cudaMemcpyDeviceToDevice, ln.stream));
+    } else {
+        // the sweep assembled the float32 planes alone: this frequency's
+        // float64 matrix from the call's inputs, straight into the workspace
+        if (!ctx->cur_L || !ctx->cur_Psi || !ctx->cur_G)
+            return fail(ctx, ZSOLVE_ESTATE, "fallback without the float64 matrix or the sweep's inputs");
+        ZS_CU(zs_launch_assemble(ctx->cur_L, ctx->cur_Psi, ctx->cur_G, n, 0, n, ctx->d_params + slot, 1, ctx->fb_a,
+                                 0, nullptr, ctx->ld, ctx->plane, 0, ln.stream));
+    }
     int64_t cnt = 0;
     StageSpan sp(ctx, ZSOLVE_STAGE_FALLBACK, ln.stream);
     ZS_CU(zs_lu64_factor(ctx->fb_a, n, ctx->fb_piv, ctx->fb_info, ln.stream, &cnt));
@@ -596,15 +612,17 @@ int oz_split_inputs(zsolve_ctx *ctx, const double *L, const double *Psi, const d
 }
 
 // r = b - Z x for the listed slots in the context's residual arithmetic.
-constexpr int kOzMinPairs = 4;
+constexpr int kOzMinPairs = 4;  // fewer (frequency, right-hand side) pairs: the OZ mode's GEMV
 int residual_slots(zsolve_ctx *ctx, Lane &ln, const double2 *b, const double2 *x, int64_t x_stride, int nrhs,
                    float2 *o64, int64_t o64s, double2 *o128, int64_t o128s, const int *slots, int nslot,
                    StageSpan *sp) {
     const int64_t n = ctx->n;
     // OZ reads its 48 n^2 bytes of digits whatever the number of columns;
     // below four (frequency, right-hand side) pairs the float64 GEMV over Z64
-    // (16 n^2 bytes and 2-4 DFMA per entry and pair) is the faster one
-    if (ctx->resid_mode == ZSOLVE_RESID_OZ && ctx->oz_ready && (int64_t)nslot * nrhs >= kOzMinPairs) {
+    // (16 n^2 bytes and 2-4 DFMA per entry and pair) is the faster one, where
+    // the lane's float64 matrices were formed
+    if (ctx->resid_mode == ZSOLVE_RESID_OZ && ctx->oz_ready &&
+        ((int64_t)nslot * nrhs >= kOzMinPairs || !ln.z64_formed)) {
         ZS_CU(cudaStreamWaitEvent(ln.stream, ctx->oz_done, 0));
         ZS_CU(zs_launch_residual_oz(ctx->oz_amap, ctx->oz_ea, n, ctx->d_params, b, x, x_stride, nrhs, o64, o64s, o128,
                                     o128s, slots, nslot, ln.oz_x, ln.oz_ex, ln.oz_ncol_cap, ln.oz_part,
@@ -821,6 +839,17 @@ int check_nrhs(zsolve_ctx *ctx, int nrhs) {
     return ZSOLVE_OK;
 }
 
+// A sweep lane of `count` frequencies whose residual reads L, Psi, G rather
+// than the float64 matrices: LPG, and OZ where its tensor-core product serves
+// (four or more (frequency, right-hand side) pairs; the OZ residual then keeps
+// to the product as the lane's frequencies converge).  Its assembly forms the
+// float32 planes alone.
+bool z32_only(const zsolve_ctx *ctx, int count) {
+    if (!ctx->cur_L) return false;
+    return ctx->resid_mode == ZSOLVE_RESID_LPG ||
+           (ctx->resid_mode == ZSOLVE_RESID_OZ && (int64_t)count * ctx->cur_nrhs >= kOzMinPairs);
+}
+
 // Assembly of one lane's share of a batch: slots first..first+count-1.
 // While a host-pointer sweep's inputs are still being copied (ctx->nband
 // row bands, band b's rows complete at ctx->band_ev[b]), the assembly runs
@@ -830,13 +859,21 @@ int assemble_lane(zsolve_ctx *ctx, Lane &ln, const double *L, const double *Psi,
     ZS_CU(cudaEventRecord(ln.ev[0], ln.stream));
     StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE, ln.stream);
     const int nb = ctx->nband > 0 ? ctx->nband : 1;
+    const bool only32 = z32_only(ctx, count);
+    ln.z64_formed = !only32;
     for (int bnd = 0; bnd < nb; bnd++) {
         const int64_t r0 = ctx->n * bnd / nb, r1 = ctx->n * (bnd + 1) / nb;
         if (ctx->nband > 0) ZS_CU(cudaStreamWaitEvent(ln.stream, ctx->band_ev[bnd], 0));
-        ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, r0, r1, ctx->d_params + first, count,
-                                 ctx->z64 + (int64_t)first * ctx->z64_stride, ctx->z64_stride,
-                                 ctx->z32 + (int64_t)first * ctx->z32_stride, ctx->ld, ctx->plane, ctx->z32_stride,
-                                 ln.stream, ctx->zexp ? ctx->zexp + (int64_t)first * ctx->n : nullptr));
+        if (only32)
+            ZS_CU(zs_launch_assemble32(L, Psi, G, ctx->n, r0, r1, ctx->d_params + first, count,
+                                       ctx->z32 + (int64_t)first * ctx->z32_stride, ctx->ld, ctx->plane,
+                                       ctx->z32_stride, ln.stream));
+        else
+            ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, r0, r1, ctx->d_params + first, count,
+                                     ctx->z64 + (int64_t)first * ctx->z64_stride, ctx->z64_stride,
+                                     ctx->z32 + (int64_t)first * ctx->z32_stride, ctx->ld, ctx->plane,
+                                     ctx->z32_stride, ln.stream,
+                                     ctx->zexp ? ctx->zexp + (int64_t)first * ctx->n : nullptr));
     }
     sp.done(nb);
     ctx->nband = 0;  // the first assembly of a sweep waited for every band
@@ -933,6 +970,7 @@ int sweep_impl(zsolve_ctx *ctx, const double *L, const double *Psi, const double
     ctx->cur_L = L;
     ctx->cur_Psi = Psi;
     ctx->cur_G = G;
+    ctx->cur_nrhs = nrhs;
     struct Clear {  // the pointers are borrowed for this call only
         zsolve_ctx *c;
         ~Clear() {
@@ -1198,6 +1236,9 @@ int zsolve_create(zsolve_ctx **out, int64_t n, int nrhs_max, const zsolve_opts *
     if (const char *e = getenv("ZSOLVE_LOOKAHEAD")) ctx->lookahead = std::min(1, std::max(-1, atoi(e)));
     // testing aid: few CTAs per tcgen05 launch, so that each takes many tiles
     if (const char *e = getenv("ZSOLVE_TC_GRID")) ctx->tc_cap = std::max(0, atoi(e));
+    // testing aid: zsolve_assemble rewrites its float32 planes with the kernel
+    // that sweeps with the OZ or LPG residual use, so that they can be compared
+    if (const char *e = getenv("ZSOLVE_ASM32")) ctx->asm32_planes = atoi(e) != 0;
     if (const char *e = getenv("ZSOLVE_TRSV_CTAS")) ctx->trsv_cap = std::max(0, atoi(e));
     // right-hand sides per triangular-solve chain (1, 2 or 4; unset: chosen per solve)
     if (const char *e = getenv("ZSOLVE_TRSV_R")) {
@@ -1337,7 +1378,11 @@ int zsolve_assemble(zsolve_ctx *ctx, const double *L, const double *Psi, const d
     StageSpan sp(ctx, ZSOLVE_STAGE_ASSEMBLE, ctx->stream);
     ZS_CU(zs_launch_assemble(L, Psi, G, ctx->n, 0, ctx->n, ctx->d_params, 1, ctx->z64, ctx->z64_stride, ctx->z32,
                              ctx->ld, ctx->plane, ctx->z32_stride, ctx->stream, ctx->zexp));
+    if (ctx->asm32_planes)
+        ZS_CU(zs_launch_assemble32(L, Psi, G, ctx->n, 0, ctx->n, ctx->d_params, 1, ctx->z32, ctx->ld, ctx->plane,
+                                   ctx->z32_stride, ctx->stream));
     sp.done(1);
+    ctx->lane[0].z64_formed = true;
     ctx->assembled = 1;
     ctx->factored = 0;
     return ZSOLVE_OK;

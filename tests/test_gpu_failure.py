@@ -81,12 +81,17 @@ def test_bounded_wait_gives_up_and_context_stays_usable(zs, torch, n, nrhs):
         s.close()
 
 
+@pytest.mark.parametrize("resid", ["F64", "OZ", "LPG"])
 @pytest.mark.parametrize("gemm", ["FFMA", "TF32X3", "TF32"])
 @pytest.mark.parametrize("n,nrhs,nf", [(130, 1, 1), (300, 2, 3)])
-def test_natural_stall_reaches_fallback(zs, torch, gemm, n, nrhs, nf):
+def test_natural_stall_reaches_fallback(zs, torch, gemm, n, nrhs, nf, resid):
+    # OZ and LPG: a lane whose residual reads L, Psi, G assembles the float32
+    # planes alone (OZ: four or more pairs; with 3 frequencies x 2 right-hand
+    # sides the lanes hold 4 and 2), so the fallback forms the float64 matrix
     wl = workload.make_growth(n, seed=n, nf=nf, nrhs=nrhs)
     ref = oracle.solve_sweep(wl)
-    s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm), batch=nf)
+    s = zs.Solver(n, nrhs, gemm=getattr(zs, "ZSOLVE_GEMM_" + gemm), batch=nf,
+                  resid=getattr(zs, "ZSOLVE_RESID_" + resid))
     try:
         x = torch.empty((nf, nrhs, n), dtype=torch.complex128, device="cuda")
         infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,

@@ -128,6 +128,50 @@ def test_assemble_bit_exact_full_size_and_signed_zeros(zs, torch):
         s.close()
 
 
+def _ulp_distance32(a, b):
+    """|a - b| in float32 ulps (ordered integer images of the bit patterns)."""
+    def ordered(x):
+        i = np.ascontiguousarray(x, dtype=np.float32).view(np.int32).astype(np.int64)
+        return np.where(i < 0, -(i & 0x7FFFFFFF), i)
+    return np.abs(ordered(a) - ordered(b))
+
+
+@pytest.mark.parametrize("case", ["small", "full_size", "signed_zeros"])
+def test_assemble32_within_one_ulp(zs, torch, monkeypatch, case):
+    """The float32-only assembly (used by sweeps whose residual reads L, Psi,
+    G) against RN32 of the oracle's float64 matrix: every entry within one
+    float32 ulp, nearly all equal, zeros with the same sign.  ZSOLVE_ASM32=1
+    (a testing aid) makes zsolve_assemble rewrite the float32 planes with it."""
+    monkeypatch.setenv("ZSOLVE_ASM32", "1")
+    if case == "signed_zeros":
+        n = 64
+        rng = np.random.default_rng(3)
+        vals = np.array([0.0, -0.0, 0.25, 1.0, -0.5, 3.0])
+        L, P, G = (rng.choice(vals, size=(n, n)) for _ in range(3))
+        cases = [(L, P, G, 2 * math.pi * 1.3e9, zsv) for zsv in
+                 (complex(-0.01, -0.02), complex(0.01, -0.02), complex(-0.01, 0.02), complex(0.0, 0.0))]
+    else:
+        wl = workload.make(1) if case == "full_size" else workload.make_small(301, seed=5, nf=3)
+        n = wl.n
+        cases = [(wl.L, wl.Psi, wl.G, wl.omega[f], wl.zs[f]) for f in (0, len(wl.omega) // 2, len(wl.omega) - 1)]
+    s = zs.Solver(n, 1)
+    try:
+        re = torch.empty((n, n), dtype=torch.float32, device="cuda")
+        im = torch.empty_like(re)
+        for L, P, G, w, zsv in cases:
+            zs.zsolve_assemble(s.ctx, dev(torch, L), dev(torch, P), dev(torch, G), w, zsv.real, zsv.imag)
+            zs.zsolve_get_z32(s.ctx, re, im)
+            c64 = oracle.cast_c64(oracle.assemble(L, P, G, w, zsv))
+            for got, want in ((re.cpu().numpy(), c64.real), (im.cpu().numpy(), c64.imag)):
+                d = _ulp_distance32(got, want)
+                assert d.max() <= 1, d.max()
+                assert np.count_nonzero(d) <= 1e-4 * d.size, np.count_nonzero(d)
+                zero = want == 0
+                assert np.array_equal(np.signbit(got[zero]), np.signbit(want[zero]))
+    finally:
+        s.close()
+
+
 def test_assemble_term_isolation(zs, torch):
     # L = 0, G = 0, and a balanced scaling: each term of Z must appear exactly
     n = 70
@@ -599,9 +643,13 @@ def test_fallback_solve_direct(zs, torch):
         s.close()
 
 
-def test_forced_fallback_sweep(zs, torch):
+@pytest.mark.parametrize("resid", ["F64", "OZ", "LPG"])
+def test_forced_fallback_sweep(zs, torch, resid):
+    # with OZ (four or more pairs per lane) and LPG the sweep assembles the
+    # float32 planes alone: the fallback forms the float64 matrix itself
     wl = workload.make_small(97, seed=61, nf=2, nrhs=2)
-    s = zs.Solver(97, 2, gemm=zs.ZSOLVE_GEMM_FFMA, force_fallback=1)
+    s = zs.Solver(97, 2, gemm=zs.ZSOLVE_GEMM_FFMA, force_fallback=1, resid=getattr(zs, "ZSOLVE_RESID_" + resid),
+                  lanes=1)
     try:
         x = torch.empty((2, 2, 97), dtype=torch.complex128, device="cuda")
         infos = zs.zsolve_sweep(s.ctx, dev(torch, wl.L), dev(torch, wl.Psi), dev(torch, wl.G), wl.omega, wl.zs,
