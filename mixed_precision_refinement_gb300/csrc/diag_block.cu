@@ -551,17 +551,33 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
     __syncthreads();
     // ---- load (identity padding beyond nb)
     float amax = 0.f;
-    for (int idx = tid; idx < NB * NB; idx += kThreads) {
-        const int i = idx >> 7, j = idx & (NB - 1);
-        float a = (i == j) ? 1.f : 0.f, b = 0.f;
-        if (i < nb && j < nb) {
-            const int64_t g = (J + i) * ld + J + j;
-            a = gre[g];
-            b = gim[g];
-            amax = fmaxf(amax, fabsf(a) + fabsf(b));
+    if (nb == NB) {
+        // a whole block: 16-byte loads (rows of ld floats, ld a multiple of
+        // 32, and J a multiple of 128), all of a thread's in flight at once
+        const float *bre = gre + J * ld + J, *bim = gim + J * ld + J;
+#pragma unroll
+        for (int u = 0; u < NB * NB / 4 / kThreads; u++) {
+            const int idx = tid + u * kThreads, i = idx >> 5, j = (idx & 31) * 4;
+            const float4 a = __ldcg(reinterpret_cast<const float4 *>(bre + i * ld + j));
+            const float4 b = __ldcg(reinterpret_cast<const float4 *>(bim + i * ld + j));
+            amax = fmaxf(amax, fmaxf(fmaxf(fabsf(a.x) + fabsf(b.x), fabsf(a.y) + fabsf(b.y)),
+                                     fmaxf(fabsf(a.z) + fabsf(b.z), fabsf(a.w) + fabsf(b.w))));
+            *reinterpret_cast<float4 *>(&smem[i * LDA + j]) = a;
+            *reinterpret_cast<float4 *>(&smem[IM_A + i * LDA + j]) = b;
         }
-        smem[i * LDA + j] = a;
-        smem[IM_A + i * LDA + j] = b;
+    } else {
+        for (int idx = tid; idx < NB * NB; idx += kThreads) {
+            const int i = idx >> 7, j = idx & (NB - 1);
+            float a = (i == j) ? 1.f : 0.f, b = 0.f;
+            if (i < nb && j < nb) {
+                const int64_t g = (J + i) * ld + J + j;
+                a = gre[g];
+                b = gim[g];
+                amax = fmaxf(amax, fabsf(a) + fabsf(b));
+            }
+            smem[i * LDA + j] = a;
+            smem[IM_A + i * LDA + j] = b;
+        }
     }
     if (!(amax <= 3.0e38f)) amax = 3.0e38f;  // non-finite inputs: the pivot test flags them
     atomicMax(&s_amax, __float_as_uint(amax));
