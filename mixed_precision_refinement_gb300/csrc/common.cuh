@@ -167,10 +167,13 @@ inline int64_t zs_inv32_slot_stride(int64_t n) { return ((n + 127) / 128) * ZS_I
 // outside the triangles from the allocation on: only the triangles are
 // written) and, if winv != NULL, their operand packs (mode 1: tf32 hi; 2: hi
 // + lo); if inv32 != NULL, the 32x32 sub-block inverses.  pivflag[slot] = 1
-// on a tiny or non-finite pivot.
+// on a tiny or non-finite pivot.  sym = 1: the symmetric mode's form, the
+// lower blocks alone factored and U = D L^T within the block (its upper
+// blocks and U^-1 = L^-T D^-1 formed from L), for a block that is symmetric.
 cudaError_t zs_launch_diag_block(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
                                  const int *slots, int nslot, int *pivflag, float *inv32, int64_t inv32_stride,
-                                 float *dinv, int64_t dinv_stride, float *winv, int mode, cudaStream_t st);
+                                 float *dinv, int64_t dinv_stride, float *winv, int mode, int sym,
+                                 cudaStream_t st);
 // mode: 0 = pack plain fp32 (FFMA), 1 = tf32 rounded (TF32), 2 = tf32 hi + lo (TF32X3)
 cudaError_t zs_launch_trsm_l(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                              int64_t J, const float *inv32, int64_t inv32_stride, float *pack, int64_t pack_stride,

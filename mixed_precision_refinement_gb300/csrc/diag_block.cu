@@ -319,6 +319,37 @@ __device__ __forceinline__ void base_inv(int p, int warp, int lane) {
     for (int c = 0; c < kInvCols; c++) st_c(D, lane, j0 + c, x[c]);
 }
 
+// Step 2 of the symmetric mode, where U = D L^T is taken to hold (D the
+// pivots; an unpivoted LU of a complex symmetric matrix has this form):
+// DL_p = L_pp^-1 only, warp w taking columns w and 31 - w (the forward
+// substitution of column j has 32 - j steps, so every warp has 33), and
+// DU_p = U_pp^-1 = DL_p^T D_p^-1 from it: DU(i, j) = DL(j, i) / d_j.
+__device__ __forceinline__ void base_inv_sym(int p, int warp, int lane) {
+    const Blk B = blkA(p, p);
+    const int jc[2] = {warp, P - 1 - warp};
+    cf x[2];
+#pragma unroll
+    for (int c = 0; c < 2; c++) x[c] = cf{lane == jc[c] ? 1.f : 0.f, 0.f};
+#pragma unroll 2
+    for (int k = jc[0]; k < P; k++) {
+        const cf l = ld_c(B, lane, k);  // L(lane, k), used by rows lane > k
+        const bool open = lane > k;
+#pragma unroll
+        for (int c = 0; c < 2; c++) {
+            const cf xk = {__shfl_sync(0xffffffffu, x[c].re, k), __shfl_sync(0xffffffffu, x[c].im, k)};
+            const cf upd = zs::cfms(x[c], l, xk);
+            x[c].re = open ? upd.re : x[c].re;
+            x[c].im = open ? upd.im : x[c].im;
+        }
+    }
+    const cf rl = {smem[OFF_R + p * P + lane], smem[OFF_R + 4 * P + p * P + lane]};  // 1 / d_lane
+#pragma unroll
+    for (int c = 0; c < 2; c++) {
+        st_c(blkDL(p), lane, jc[c], x[c]);
+        st_c(blkDU(p), jc[c], lane, zs::cmul(x[c], rl));
+    }
+}
+
 __device__ __forceinline__ float tf32_rna(float x) {
     uint32_t r;
     asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
@@ -376,6 +407,27 @@ __constant__ WinOut kWin[kWinRounds][3] = {
 };
 __constant__ unsigned char kWinFirst[4] = {0, 1, 3, 6};  // first round of W(q); W(q) has q + 1 rounds
 __constant__ unsigned char kWinOuts[kWinRounds] = {3, 3, 2, 3, 2, 2, 3, 2, 2, 2};
+
+// The symmetric mode's windows: the V chain alone (no G_U blocks, no W
+// blocks: those are emitted from the V blocks), in the same rounds and
+// shared-memory slots as above.  W(0) has nothing to form.
+__constant__ WinOut kWinSym[kWinRounds][3] = {
+    {},
+    // W(1): G_L(1,0);  V_10 = -G_L(1,0) DL_0 -> A(0,0)
+    {{4, 1, 0, 2, 0, 0, {21}, {4}}},
+    {{0, 1, 1, 0, 1, 0, {4}, {20}}},
+    // W(2): G_L(2,0), G_L(2,1);  V_21 = -G_L(2,1) DL_1 -> A(2,2);
+    //       V_20 = -(G_L(2,1) V_10 + G_L(2,0) DL_0) -> A(2,0)
+    {{8, 1, 0, 2, 0, 0, {22}, {8}}, {9, 1, 0, 2, 0, 0, {22}, {9}}},
+    {{10, 1, 1, 0, 2, 1, {9}, {21}}},
+    {{8, 2, 1, 0, 2, 0, {9, 8}, {0, 20}}},
+    // W(3): G_L(3,0), G_L(3,1), G_L(3,2);  V_32 -> A(1,0);  V_31 -> A(3,3);  V_30 -> A(3,3)
+    {{12, 1, 0, 2, 0, 0, {23}, {12}}, {13, 1, 0, 2, 0, 0, {23}, {13}}, {14, 1, 0, 2, 0, 0, {23}, {14}}},
+    {{4, 1, 1, 0, 3, 2, {14}, {22}}},
+    {{15, 2, 1, 0, 3, 1, {14, 13}, {10, 21}}},
+    {{15, 3, 1, 0, 3, 0, {14, 13, 12}, {8, 0, 20}}},
+};
+__constant__ unsigned char kWinSymOuts[kWinRounds] = {0, 1, 1, 2, 1, 1, 3, 1, 1, 1};
 
 __device__ __forceinline__ Blk blk_id(int id) {
     return id < 16 ? blkA(id >> 2, id & 3) : (id < 20 ? blkDU(id - 16) : blkDL(id - 20));
@@ -455,6 +507,54 @@ __device__ __noinline__ void emit_pair(int lw, int kw, const Blk Sw, int lv, int
     }
 }
 
+// Symmetric mode: V block (q, k) at Sv (q > k) out as emit_one does, and
+// with it W block (k, q) of W = U^-1 = V^T D^-1: W(32k + a, 32q + b) =
+// V(32q + b, 32k + a) / d_(32q + b).  Its dense block reads V's columns;
+// its pack row 32q + b (column 32q + b of W) is V's pack row 32q + b
+// times 1 / d_(32q + b).
+__device__ __forceinline__ void emit_w_of_v(int q, int k, const Blk Sv, float *xu, float *pu, int mode, int idx,
+                                            bool dense) {
+    const float *rre = smem + OFF_R + q * P, *rim = rre + 4 * P;  // 1 / d of V's rows
+    if (dense) {
+        const int a = idx >> 3, b0 = (idx & 7) * 4;
+        cf w[4];
+#pragma unroll
+        for (int u = 0; u < 4; u++) w[u] = zs::cmul(ld_c(Sv, b0 + u, a), cf{rre[b0 + u], rim[b0 + u]});
+        const int o = (k * P + a) * NB + q * P + b0;
+        *reinterpret_cast<float4 *>(xu + o) = f4(w[0].re, w[1].re, w[2].re, w[3].re);
+        *reinterpret_cast<float4 *>(xu + NB * NB + o) = f4(w[0].im, w[1].im, w[2].im, w[3].im);
+        return;
+    }
+    const int j = idx >> 3, i0 = (idx & 7) * 4;
+    const float4 vr = *reinterpret_cast<const float4 *>(&smem[Sv.off + j * Sv.ld + i0]);
+    const float4 vi = *reinterpret_cast<const float4 *>(&smem[Sv.off + Sv.im + j * Sv.ld + i0]);
+    const float cr = rre[j], ci = rim[j];
+    const float4 re = f4(vr.x * cr - vi.x * ci, vr.y * cr - vi.y * ci, vr.z * cr - vi.z * ci, vr.w * cr - vi.w * ci);
+    const float4 im = f4(vr.x * ci + vi.x * cr, vr.y * ci + vi.y * cr, vr.z * ci + vi.z * cr, vr.w * ci + vi.w * cr);
+    const int o = (q * P + j) * (2 * NB) + k * P + i0;
+    const float4 hr = tf32_4(re), hi = tf32_4(im);
+    *reinterpret_cast<float4 *>(pu + o) = hr;
+    *reinterpret_cast<float4 *>(pu + o + NB) = neg4(hi);
+    if (mode == 2) {
+        *reinterpret_cast<float4 *>(pu + ZS_WINV_PLANE + o) = tf32_4(sub4(re, hr));
+        *reinterpret_cast<float4 *>(pu + ZS_WINV_PLANE + o + NB) = neg4(tf32_4(sub4(im, hi)));
+    }
+}
+
+__device__ __noinline__ void emit_v_w(int q, int k, const Blk Sv, float *xu, float *xl, float *pu, float *pv, int mode,
+                                      int t, int nt) {
+    constexpr int NI = P * P / 4;
+    for (int idx = t; idx < 2 * NI; idx += nt) {
+        if (idx < NI) emit_one(false, q, k, Sv, xl, pv, mode, idx, true);
+        else emit_w_of_v(q, k, Sv, xu, pu, mode, idx - NI, true);
+    }
+    if (!pu) return;
+    for (int idx = t; idx < 2 * NI; idx += nt) {
+        if (idx < NI) emit_one(false, q, k, Sv, xl, pv, mode, idx, false);
+        else emit_w_of_v(q, k, Sv, xu, pu, mode, idx - NI, false);
+    }
+}
+
 struct WinArgs {
     float *gre, *gim;
     int64_t ld, J;
@@ -465,32 +565,40 @@ struct WinArgs {
 // One round of W(q): its output blocks, 8 / NTILE tasks of 16 rows x 8 NTILE
 // columns each (one task per warp of the group), stored after the group's
 // barrier (a result may replace one of its own operands), then written out.
-template <int NTILE, int NT, int BAR>
+template <int NTILE, int NT, int BAR, bool SYM>
 __device__ __forceinline__ void win_round(int r, int t, int lane, const WinArgs &w) {
     constexpr int CPB = 4 / NTILE, TPB = 2 * CPB;  // column groups, tasks per block
-    const int nout = kWinOuts[r];
+    const WinOut(*kWinT)[3] = SYM ? kWinSym : kWin;
+    const int nout = SYM ? kWinSymOuts[r] : kWinOuts[r];
+    if (nout == 0) return;
     const int wi = t >> 5, b = wi / TPB, rem = wi % TPB, r0 = (rem / CPB) * 16, c0 = (rem % CPB) * 8 * NTILE;
     const bool on = b < nout;
     CAcc<NTILE> acc;
     cacc_zero(acc);
     if (on) {
-        const int nterm = kWin[r][b].nterm;
+        const int nterm = kWinT[r][b].nterm;
 #pragma unroll 1
-        for (int i = 0; i < nterm; i++) cmma(blk_id(kWin[r][b].tp[i]), blk_id(kWin[r][b].tq[i]), r0, c0, lane, acc);
+        for (int i = 0; i < nterm; i++) cmma(blk_id(kWinT[r][b].tp[i]), blk_id(kWinT[r][b].tq[i]), r0, c0, lane, acc);
     }
     group_sync<NT, BAR>();
-    if (on) cacc_out<NTILE, false>(blk_id(kWin[r][b].dst), r0, c0, lane, acc, kWin[r][b].neg ? -1.f : 1.f);
+    if (on) cacc_out<NTILE, false>(blk_id(kWinT[r][b].dst), r0, c0, lane, acc, kWinT[r][b].neg ? -1.f : 1.f);
     group_sync<NT, BAR>();
-    // a chain round's outputs are one W block (0) and one V block (1); G blocks are not written out
-    if (kWin[r][0].eu != 2)
-        emit_pair(kWin[r][0].el, kWin[r][0].ek, blk_id(kWin[r][0].dst), kWin[r][1].el, kWin[r][1].ek,
-                  blk_id(kWin[r][1].dst), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
+    // a chain round's outputs are one W block (0) and one V block (1), or in
+    // the symmetric mode one V block, emitted with its W block; G blocks are
+    // not written out
+    if (SYM) {
+        if (kWinT[r][0].eu != 2)
+            emit_v_w(kWinT[r][0].el, kWinT[r][0].ek, blk_id(kWinT[r][0].dst), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
+    } else if (kWinT[r][0].eu != 2) {
+        emit_pair(kWinT[r][0].el, kWinT[r][0].ek, blk_id(kWinT[r][0].dst), kWinT[r][1].el, kWinT[r][1].ek,
+                  blk_id(kWinT[r][1].dst), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
+    }
 }
 
 // W(q) on a group of NT threads (t = thread index in the group), barrier BAR.
 // The G round takes 16 x 16 tasks (12 for its three blocks); the chain
 // rounds (two blocks) 16 x 8 TC columns.
-template <int NT, int BAR, int TC>
+template <int NT, int BAR, int TC, bool SYM>
 __device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArgs &wa) {
     static_assert(3 * 4 * 32 <= NT && 2 * (8 / TC) * 32 <= NT, "one task per warp");
     const WinArgs w = wa;  // in registers: stores through the pointers cannot alias it
@@ -525,11 +633,14 @@ __device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArg
     // panel's base LU well before the window ends), here for the last panel
     if constexpr (NT == kThreads) emit_pair(q, q, blkDU(q), q, q, blkDL(q), w.xu, w.xl, w.pu, w.pv, w.mode, t, NT);
     const int r0 = kWinFirst[q];
-    win_round<2, NT, BAR>(r0, t, lane, w);
+    win_round<2, NT, BAR, SYM>(r0, t, lane, w);
+    // the symmetric mode's chain rounds form one block: 16 x 8 tasks
+    constexpr int TCR = SYM ? 1 : TC;
 #pragma unroll 1
-    for (int r = r0 + 1; r <= r0 + q; r++) win_round<TC, NT, BAR>(r, t, lane, w);
+    for (int r = r0 + 1; r <= r0 + q; r++) win_round<TCR, NT, BAR, SYM>(r, t, lane, w);
 }
 
+template <bool SYM>
 __global__ void __launch_bounds__(kThreads, 1)
 k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
              const int *__restrict__ slots, int *__restrict__ pivflag, float *__restrict__ inv32,
@@ -604,13 +715,46 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
                 emit_pair(p - 1, p - 1, blkDU(p - 1), p - 1, p - 1, blkDL(p - 1), wa.xu, wa.xl, wa.pu, wa.pv, mode,
                           tid, kLuWarps * 32);
         } else if (p > 0) {
-            inverse_window<kThreads - kLuWarps * 32, 2, 2>(p - 1, tid - kLuWarps * 32, lane, wa);
+            inverse_window<kThreads - kLuWarps * 32, 2, 2, SYM>(p - 1, tid - kLuWarps * 32, lane, wa);
         }
         __syncthreads();
-        base_inv(p, warp, lane);
+        if (SYM) base_inv_sym(p, warp, lane);
+        else base_inv(p, warp, lane);
         __syncthreads();
         const int rest = 3 - p;
         if (rest == 0) break;
+        if (SYM) {
+            // L_ip = A_ip DU_p in 16 x 16 tasks, four per block
+            {
+                CAcc<2> acc;
+                cacc_zero(acc);
+                const int t = warp, b = t >> 2, r0 = ((t >> 1) & 1) * 16, c0 = (t & 1) * 16;
+                const bool on = t < 4 * rest;
+                if (on) cmma(blkA(p + 1 + b, p), blkDU(p), r0, c0, lane, acc);
+                __syncthreads();
+                if (on) cacc_out<2, false>(blkA(p + 1 + b, p), r0, c0, lane, acc, 1.f);
+                __syncthreads();
+            }
+            // U_pj = D_p L_jp^T, the upper factor's blocks of this panel
+            for (int idx = tid; idx < rest * P * P; idx += kThreads) {
+                const int jb = idx >> 10, a = (idx >> 5) & 31, c = idx & 31;
+                st_c(blkA(p, p + 1 + jb), a, c, zs::cmul(ld_c(blkA(p, p), a, a), ld_c(blkA(p + 1 + jb, p), c, a)));
+            }
+            __syncthreads();
+            // A_ij -= L_ip U_pj on the blocks on and below the diagonal, 16 x 16 tasks
+            for (int t = warp; t < 2 * rest * (rest + 1); t += kWarps) {
+                const int b = t >> 2, r0 = ((t >> 1) & 1) * 16, c0 = (t & 1) * 16;
+                int i = 0;
+                while ((i + 1) * (i + 2) / 2 <= b) i++;
+                const int bi = p + 1 + i, bj = p + 1 + b - i * (i + 1) / 2;
+                CAcc<2> acc;
+                cacc_zero(acc);
+                cmma(blkA(bi, p), blkA(p, bj), r0, c0, lane, acc);
+                cacc_out<2, true>(blkA(bi, bj), r0, c0, lane, acc, 1.f);
+            }
+            __syncthreads();
+            continue;
+        }
         // L_ip = A_ip DU_p (tasks 0 .. 2 rest - 1), U_pj = DL_p A_pj (the next 2 rest),
         // 16-row tasks; tasks read rows of A_pj that other tasks overwrite:
         // write after a barrier
@@ -639,7 +783,7 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
         __syncthreads();
     }
 
-    inverse_window<kThreads, 0, 1>(3, tid, lane, wa);
+    inverse_window<kThreads, 0, 1, SYM>(3, tid, lane, wa);
 
     // ---- the 32 x 32 inverses, when the FP32 block solves want them
     if (inv32) {
@@ -661,13 +805,23 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
 
 cudaError_t zs_launch_diag_block(float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
                                  const int *slots, int nslot, int *pivflag, float *inv32, int64_t inv32_stride,
-                                 float *dinv, int64_t dinv_stride, float *winv, int mode, cudaStream_t st) {
+                                 float *dinv, int64_t dinv_stride, float *winv, int mode, int sym, cudaStream_t st) {
     if (nb <= 0 || nb > NB || nslot <= 0 || !dinv) return cudaErrorInvalidValue;
     if (winv && mode != 1 && mode != 2) return cudaErrorInvalidValue;
     // once per process (thread-safe initialisation of a local static)
-    static const cudaError_t attr = cudaFuncSetAttribute(k_diag_block, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
+    static const cudaError_t attr = [] {
+        const cudaError_t a = cudaFuncSetAttribute(k_diag_block<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kSmemBytes);
+        return a != cudaSuccess ? a
+                                : cudaFuncSetAttribute(k_diag_block<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       (int)kSmemBytes);
+    }();
     if (attr != cudaSuccess) return attr;
-    k_diag_block<<<nslot, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag, inv32,
-                                                       inv32_stride, dinv, dinv_stride, winv, mode);
+    if (sym)
+        k_diag_block<true><<<nslot, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag,
+                                                                 inv32, inv32_stride, dinv, dinv_stride, winv, mode);
+    else
+        k_diag_block<false><<<nslot, kThreads, kSmemBytes, st>>>(z32, ld, plane, z32_stride, J, nb, slots, pivflag,
+                                                                  inv32, inv32_stride, dinv, dinv_stride, winv, mode);
     return cudaGetLastError();
 }

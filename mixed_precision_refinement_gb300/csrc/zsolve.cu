@@ -286,7 +286,7 @@ int factor_slots_simt(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
             StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, ln.stream);
             ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
                                        ctx->d_pivflag, ctx->inv32, inv32_stride, ctx->dinv, ctx->dinv_stride,
-                                       nullptr, 0, ln.stream));
+                                       nullptr, 0, 0, ln.stream));
             sp.done(1);
         }
         if (J + nb >= n) break;
@@ -368,7 +368,7 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
         StageSpan sp(ctx, ZSOLVE_STAGE_DIAG, st);
         ZS_CU(zs_launch_diag_block(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, J, nb, slots, nslot,
                                    ctx->d_pivflag, nullptr, 0, ctx->dinv, ctx->dinv_stride,
-                                   J + nb >= n ? nullptr : ctx->winv, mode, st));
+                                   J + nb >= n ? nullptr : ctx->winv, mode, sym, st));
         sp.done(1);
         return ZSOLVE_OK;
     };
