@@ -75,12 +75,16 @@ __device__ __forceinline__ void st_c(const Blk &B, int r, int c, cf v) {
 // Reciprocal of a complex pivot, scaled so the squared modulus stays in
 // range, with the hardware's approximate reciprocal (a few ulp: the factor
 // is a float32 approximation that the float64 refinement corrects anyway).
-// Pivots of modulus near or above 2^126 are flagged by the caller.
+// The scale is the power of two 2^-e, e the exponent of the larger part,
+// made from the bit pattern, so that one reciprocal sits on the wavefront's
+// path per pivot.  Zero, subnormal, huge or non-finite pivots are flagged by
+// the caller (the result is then not used).
 __device__ __forceinline__ cf crecip_fast(cf p) {
     const float s = fmaxf(fabsf(p.re), fabsf(p.im));
-    const float rs = __fdividef(1.f, s);
-    const float a = p.re * rs, b = p.im * rs;
-    const float rd = __fdividef(1.f, fmaf(a, a, b * b)) * rs;
+    const int e = min(max((__float_as_int(s) >> 23) - 127, -126), 126);
+    const float sc = __int_as_float((127 - e) << 23);  // 2^-e
+    const float a = p.re * sc, b = p.im * sc;         // the larger in [1, 2)
+    const float rd = __fdividef(1.f, fmaf(a, a, b * b)) * sc;
     return {a * rd, -b * rd};
 }
 
