@@ -668,7 +668,9 @@ def run_ours(args):
     rl["k_assemble"] = obj(asm_kernel, "hbm", st["assemble"]["ms"], st["assemble"]["launches"],
                            asm_bytes * steps, hbm, "GB/s", f"{peak_src} copy",
                            "24 n^2 bytes of L, Psi, G read once per lane + 8 n^2 (float32 planes alone) or 24 n^2 "
-                           "(with the float64 matrix) written per frequency")
+                           "(with the float64 matrix) written per frequency",
+                           traffic=profile_traffic("k_assemble32")
+                           if (args.config == 1 and asm_kernel == "k_assemble32") else None)
     ktimes = kernel_times(stage_ms, args.gemm_eff)
     dom = dominant_kernel(ktimes, list(rl))
     tot_k = sum(ktimes.values())
