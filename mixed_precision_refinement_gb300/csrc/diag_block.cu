@@ -644,6 +644,25 @@ __device__ __noinline__ void inverse_window(int q, int t, int lane, const WinArg
     for (int r = r0 + 1; r <= r0 + q; r++) win_round<TCR, NT, BAR, SYM>(r, t, lane, w);
 }
 
+// Symmetric mode: the part of panel q's update that the next panel's base LU
+// does not wait for, A_ij -= L_iq U_qj on the blocks q < j <= i except
+// (q + 1, q + 1), in 16 x 16 tasks by the threads t < nt of a group.  It
+// runs beside the next panel's base LU; that panel's products read it only
+// after the barrier that ends the LU.
+__device__ __forceinline__ void sym_update_rest(int q, int t, int nt, int lane) {
+    const int rest = 3 - q, ntask = 4 * (rest * (rest + 1) / 2 - 1);
+    for (int task = t >> 5; task < ntask; task += nt >> 5) {
+        const int b = (task >> 2) + 1, r0 = ((task >> 1) & 1) * 16, c0 = (task & 1) * 16;  // b = 0 is the diagonal block
+        int i = 0;
+        while ((i + 1) * (i + 2) / 2 <= b) i++;
+        const int bi = q + 1 + i, bj = q + 1 + b - i * (i + 1) / 2;
+        CAcc<2> acc;
+        cacc_zero(acc);
+        cmma(blkA(bi, q), blkA(q, bj), r0, c0, lane, acc);
+        cacc_out<2, true>(blkA(bi, bj), r0, c0, lane, acc, 1.f);
+    }
+}
+
 template <bool SYM>
 __global__ void __launch_bounds__(kThreads, 1)
 k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t J, int nb,
@@ -720,6 +739,7 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
                           tid, kLuWarps * 32);
         } else if (p > 0) {
             inverse_window<kThreads - kLuWarps * 32, 2, 2, SYM>(p - 1, tid - kLuWarps * 32, lane, wa);
+            if (SYM) sym_update_rest(p - 1, tid - kLuWarps * 32, kThreads - kLuWarps * 32, lane);
         }
         __syncthreads();
         if (SYM) base_inv_sym(p, warp, lane);
@@ -745,16 +765,14 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
                 st_c(blkA(p, p + 1 + jb), a, c, zs::cmul(ld_c(blkA(p, p), a, a), ld_c(blkA(p + 1 + jb, p), c, a)));
             }
             __syncthreads();
-            // A_ij -= L_ip U_pj on the blocks on and below the diagonal, 16 x 16 tasks
-            for (int t = warp; t < 2 * rest * (rest + 1); t += kWarps) {
-                const int b = t >> 2, r0 = ((t >> 1) & 1) * 16, c0 = (t & 1) * 16;
-                int i = 0;
-                while ((i + 1) * (i + 2) / 2 <= b) i++;
-                const int bi = p + 1 + i, bj = p + 1 + b - i * (i + 1) / 2;
-                CAcc<2> acc;
+            // the next diagonal block first, A_(p+1)(p+1) -= L_(p+1)p U_p(p+1), in
+            // 16 x 8 tasks; the rest of the update runs beside the next base LU
+            if (warp < 8) {
+                const int r0 = (warp >> 2) * 16, c0 = (warp & 3) * 8;
+                CAcc<1> acc;
                 cacc_zero(acc);
-                cmma(blkA(bi, p), blkA(p, bj), r0, c0, lane, acc);
-                cacc_out<2, true>(blkA(bi, bj), r0, c0, lane, acc, 1.f);
+                cmma(blkA(p + 1, p), blkA(p, p + 1), r0, c0, lane, acc);
+                cacc_out<1, true>(blkA(p + 1, p + 1), r0, c0, lane, acc, 1.f);
             }
             __syncthreads();
             continue;
