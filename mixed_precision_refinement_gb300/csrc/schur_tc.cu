@@ -175,6 +175,20 @@ __device__ __forceinline__ float tf32_rna(float x) {
     return __uint_as_float(r);
 }
 
+using zs::cf;
+
+// A square root of a complex float (the principal one): with t = sqrt((|a| +
+// |z|) / 2), (t, b / 2t) for a >= 0, else (|b| / 2t, +-t) with the sign of b.
+// |z| is formed from the larger part so that it does not overflow.  Only
+// S^2 = z matters to its one caller, not the branch.
+__device__ __forceinline__ cf csqrt_f(cf z) {
+    const float a = fabsf(z.re), b = fabsf(z.im), m = fmaxf(a, b);
+    if (m == 0.f) return cf{0.f, 0.f};
+    const float n = fminf(a, b) / m, mod = m * sqrtf(1.f + n * n);
+    const float t = sqrtf(0.5f * (a + mod)), u = 0.5f * b / t;
+    return z.re >= 0.f ? cf{t, copysignf(u, z.im)} : cf{u, copysignf(t, z.im)};
+}
+
 // Row `lane` of a 32x32 fp32 box in 128B-swizzled shared memory: 16-byte unit
 // j of row r sits at unit (j ^ (r & 7)).  sgn = -1 stores the negated values.
 __device__ __forceinline__ void stage_row(uint32_t sb, int lane, const float (&v)[32], float sgn) {
@@ -422,7 +436,10 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 const int pa = (KIND == KIND_TRSM && x.u) ? PL_BR_HI : PL_A_HI;
                 const bool use_v = KIND == KIND_TRSM_SYM || x.u;  // B = L11^-1 (else U11^-1)
                 const CUtensorMap *bm = !is_trsm<KIND>() ? &tmap : &wmap;
-                const int pbr = !is_trsm<KIND>() ? PL_BR_HI : (use_v ? WP_V : 0) + WP_BR_HI;
+                // the symmetric update's B is M's own rows (the A planes, see the MMA issue)
+                const int pbr = KIND == KIND_SCHUR_LOWER ? PL_A_HI
+                                : !is_trsm<KIND>()       ? PL_BR_HI
+                                                         : (use_v ? WP_V : 0) + WP_BR_HI;
                 bool ok = true;
                 for (int kc = 0; kc < NKC; kc++, g++) {
                     const uint32_t st = g % C::STAGES, ph = (g / C::STAGES) & 1u;
@@ -501,19 +518,24 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                         const uint64_t bl = smem_desc(sl + A_BYTES + ks * 32);
                         // real part (columns 0-127) from Br, imaginary part
                         // (columns 128-255) from Br's other K half, negated in
-                        // the first half of K
+                        // the first half of K.  The symmetric update's B rows
+                        // are M = [Re M | Im M] (the A planes): Br = [Re M | -Im M]
+                        // is them negated in the second half of K, and
+                        // Bi = [Im M | Re M] their other K half as it is.
                         const uint64_t bh2 = smem_desc(sa + A_BYTES + B_BYTES / 2 + ks * 32);
                         const uint64_t bl2 = smem_desc(sl + A_BYTES + B_BYTES / 2 + ks * 32);
-                        const uint32_t id2 = kc * KC < NB ? kIdesc128Neg : kIdesc128;
+                        constexpr bool kBfromA = KIND == KIND_SCHUR_LOWER;
+                        const uint32_t id1 = kBfromA && kc * KC >= NB ? kIdesc128Neg : kIdesc128;
+                        const uint32_t id2 = !kBfromA && kc * KC < NB ? kIdesc128Neg : kIdesc128;
                         if (SPLIT) {
-                            mma_tf32(d, al, bh, acc, kIdesc128);
-                            mma_tf32(d, ah, bl, 1u, kIdesc128);
-                            mma_tf32(d, ah, bh, 1u, kIdesc128);
+                            mma_tf32(d, al, bh, acc, id1);
+                            mma_tf32(d, ah, bl, 1u, id1);
+                            mma_tf32(d, ah, bh, 1u, id1);
                             mma_tf32(d + 128u, al, bh2, acc, id2);
                             mma_tf32(d + 128u, ah, bl2, 1u, id2);
                             mma_tf32(d + 128u, ah, bh2, 1u, id2);
                         } else {
-                            mma_tf32(d, ah, bh, acc, kIdesc128);
+                            mma_tf32(d, ah, bh, acc, id1);
                             mma_tf32(d + 128u, ah, bh2, acc, id2);
                         }
                     }
@@ -567,6 +589,10 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                 // 0-3, Im in chunks 4-7); per group of 32 columns both parts.
                 // D11^-1 is the diagonal of U11^-1 (an upper triangle's inverse
                 // has the reciprocal diagonal), taken from the float32 inverses.
+                // Out go U12 into the float32 factor, the trailing update's
+                // operand rows M = U12^T S, S^2 = D11^-1 (any root of each
+                // entry: M M^T = U12^T D11^-1 U12 = L21 U12 whichever), and
+                // L21 = M S = U12^T D11^-1 into the factor.
                 const float *dre = dinv + (int64_t)x.slot * dinv_stride + (J / NB) * 4 * NB * NB + 2 * NB * NB;
                 const float *dim = dre + NB * NB;
 #pragma unroll 1
@@ -581,72 +607,59 @@ k_cgemm_tc(const __grid_constant__ CUtensorMap tmap, const __grid_constant__ CUt
                         if (lane == 0) mbar_arrive(smem_u32(&bar_acce[buf]));
                     }
                     const int c32 = g * 32;
+                    // S(c32 + lane), one column per lane, shared by shuffles below
+                    const cf sg = csqrt_f(cf{__ldg(dre + (c32 + lane) * (NB + 1)), __ldg(dim + (c32 + lane) * (NB + 1))});
 #pragma unroll
                     for (int part = 0; part < 2; part++) {
-                        const float(&v)[32] = part ? vi : vr;
                         // U12(J + c32 + t, i) into the float32 factor (transposed boxes)
-                        uint32_t sb = next_box();
-                        stage_col(sb, lane, v);
+                        const uint32_t sb = next_box();
+                        stage_col(sb, lane, part ? vi : vr);
                         publish();
                         if (lane == 0) {
                             tma_store_4d(&cmap, sb, row0, (int)J + c32, part, x.slot);
                             bulk_commit();
                         }
-                        // trailing-update operand rows: Br = [Re U12^T | -Im U12^T] (the
-                        // update takes Bi = [Im U12^T | Re U12^T] from it)
-                        float h[32];
-#pragma unroll
-                        for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q]);
-#pragma unroll 1
-                        for (int lo = 0; lo <= SPLIT; lo++) {
-                            if (lo) {
-#pragma unroll
-                                for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q] - h[q]);
-                            }
-                            sb = next_box();
-                            stage_row(sb, lane, h, part ? -1.f : 1.f);
-                            publish();
-                            if (lane == 0) {
-                                tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_BR_HI + lo, x.slot);
-                                bulk_commit();
-                            }
-                        }
                     }
-                    // L21(i, J + c32 + t) = U12^T(i, c32 + t) * D11^-1(c32 + t)
+#pragma unroll 2
+                    for (int step = 0; step < 2; step++) {
+                        // step 0: M = U12^T S (operand rows); step 1: L21 = M S (the factor)
 #pragma unroll
-                    for (int q = 0; q < 32; q++) {
-                        const int k = c32 + q;
-                        const float dr = __ldg(dre + k * (NB + 1)), di = __ldg(dim + k * (NB + 1));
-                        const float a = vr[q], b = vi[q];
-                        vr[q] = fmaf(a, dr, -b * di);
-                        vi[q] = fmaf(a, di, b * dr);
-                    }
-#pragma unroll
-                    for (int part = 0; part < 2; part++) {
-                        const float(&v)[32] = part ? vi : vr;
-                        uint32_t sb = next_box();
-                        stage_row(sb, lane, v, 1.f);
-                        publish();
-                        if (lane == 0) {
-                            tma_store_4d(&cmap, sb, (int)J + c32, row0, part, x.slot);
-                            bulk_commit();
+                        for (int q = 0; q < 32; q++) {
+                            const float sr = __shfl_sync(0xffffffffu, sg.re, q), si = __shfl_sync(0xffffffffu, sg.im, q);
+                            const float a = vr[q], b = vi[q];
+                            vr[q] = fmaf(a, sr, -b * si);
+                            vi[q] = fmaf(a, si, b * sr);
                         }
-                        // next step's block-solve operand rows: A = [Re L21 | Im L21]
-                        float h[32];
 #pragma unroll
-                        for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q]);
-#pragma unroll 1
-                        for (int lo = 0; lo <= SPLIT; lo++) {
-                            if (lo) {
-#pragma unroll
-                                for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q] - h[q]);
+                        for (int part = 0; part < 2; part++) {
+                            const float(&v)[32] = part ? vi : vr;
+                            if (step == 1) {
+                                const uint32_t sb = next_box();
+                                stage_row(sb, lane, v, 1.f);
+                                publish();
+                                if (lane == 0) {
+                                    tma_store_4d(&cmap, sb, (int)J + c32, row0, part, x.slot);
+                                    bulk_commit();
+                                }
+                                continue;
                             }
-                            sb = next_box();
-                            stage_row(sb, lane, h, 1.f);
-                            publish();
-                            if (lane == 0) {
-                                tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_A_HI + lo, x.slot);
-                                bulk_commit();
+                            // M's rows [Re M | Im M] in the A planes, tf32 hi (and lo)
+                            float h[32];
+#pragma unroll
+                            for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q]);
+#pragma unroll 1
+                            for (int lo = 0; lo <= SPLIT; lo++) {
+                                if (lo) {
+#pragma unroll
+                                    for (int q = 0; q < 32; q++) h[q] = tf32_rna(v[q] - h[q]);
+                                }
+                                const uint32_t sb = next_box();
+                                stage_row(sb, lane, h, 1.f);
+                                publish();
+                                if (lane == 0) {
+                                    tma_store_4d(&pmap, sb, part * NB + c32, row0, PL_A_HI + lo, x.slot);
+                                    bulk_commit();
+                                }
                             }
                         }
                     }

@@ -346,15 +346,12 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     const bool ahead = sym && (ctx->lookahead > 0 ||
                                (ctx->lookahead < 0 && ln.alone && nslot <= kLookaheadSlots &&
                                 (int64_t)nslot * T * T >= 12 * (int64_t)tc_grid(ctx, ln)));
-    // The symmetric mode's block solve in one product per row tile (its
-    // epilogue writes both factors) where the row tiles of all frequencies
-    // fill at least half the GPU's SMs; else the two-product form, whose CTAs
-    // split the work of a row tile (a frequency's chain of steps is shorter
-    // then).  The choice depends on the step and the batch, not on the grid.
-    auto one_product = [&](int64_t J) {
-        const int64_t rows = (n - J - ZS_NB + ZS_NB - 1) / ZS_NB * nslot;
-        return sym && 2 * rows >= ctx->num_sms;
-    };
+    // The symmetric mode's block solve: one product per row tile, its
+    // epilogue writing both factors and the update's one operand pack
+    // M = U12^T S (S^2 = D11^-1), from which the lower update takes both of
+    // its operands.  The full mode's two-product form writes L21 and U12^T
+    // packs instead.
+    auto one_product = [&](int64_t) { return sym != 0; };
     auto pack = [&](int64_t J, int buf, cudaStream_t st) -> int {
         StageSpan sp(ctx, ZSOLVE_STAGE_PACK, st);
         ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J,
