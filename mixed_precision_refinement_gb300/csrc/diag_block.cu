@@ -504,8 +504,10 @@ __device__ __noinline__ void emit_pair(int lw, int kw, const Blk Sw, int lv, int
         if (idx < NI) emit_one(true, lw, kw, Sw, xu, pu, mode, idx, true);
         else emit_one(false, lv, kv, Sv, xl, pv, mode, idx - NI, true);
     }
-    if (!pu) return;
-    for (int idx = t; idx < 2 * NI; idx += nt) {
+    if (!pv) return;  // no packs at all (the last diagonal block)
+    // the packs; without pu (the symmetric mode, whose block solves read V's alone) V's only
+    const int first = pu ? 0 : NI;
+    for (int idx = first + t; idx < 2 * NI; idx += nt) {
         if (idx < NI) emit_one(true, lw, kw, Sw, xu, pu, mode, idx, false);
         else emit_one(false, lv, kv, Sv, xl, pv, mode, idx - NI, false);
     }
@@ -552,8 +554,9 @@ __device__ __noinline__ void emit_v_w(int q, int k, const Blk Sv, float *xu, flo
         if (idx < NI) emit_one(false, q, k, Sv, xl, pv, mode, idx, true);
         else emit_w_of_v(q, k, Sv, xu, pu, mode, idx - NI, true);
     }
-    if (!pu) return;
-    for (int idx = t; idx < 2 * NI; idx += nt) {
+    if (!pv) return;
+    const int last = pu ? 2 * NI : NI;  // W's pack rows only if someone reads them
+    for (int idx = t; idx < last; idx += nt) {
         if (idx < NI) emit_one(false, q, k, Sv, xl, pv, mode, idx, false);
         else emit_w_of_v(q, k, Sv, xu, pu, mode, idx - NI, false);
     }
@@ -727,8 +730,9 @@ k_diag_block(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
     wa.mode = mode;
     wa.xl = dinv + (int64_t)slot * dinv_stride + (J / NB) * 4 * NB * NB;  // [L, U][re, im][128][128]
     wa.xu = wa.xl + 2 * NB * NB;
-    wa.pu = winv ? winv + (int64_t)slot * ZS_WINV_STRIDE : nullptr;
-    wa.pv = winv ? wa.pu + 2 * ZS_WINV_PLANE : nullptr;
+    wa.pv = winv ? winv + (int64_t)slot * ZS_WINV_STRIDE + 2 * ZS_WINV_PLANE : nullptr;
+    // the symmetric mode's block solves take V's pack alone: no W pack
+    wa.pu = winv && !SYM ? winv + (int64_t)slot * ZS_WINV_STRIDE : nullptr;
 
     // ---- LU, one 32-column panel at a time; W(p - 1) beside the base LU of panel p
     for (int p = 0; p < 4; p++) {
