@@ -726,15 +726,37 @@ int refine_batch(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *x, int64_
     std::vector<int> active, stalled;  // slot indices
     std::vector<double> prev(count, INFINITY), last(count, 1.0);
     std::vector<int> grow(count, 0), iters(count, 0);
-    // slots whose factorisation met a bad pivot go straight to the fallback
+    // Slots whose factorisation met a bad pivot go to the fallback.  The flags
+    // come back with the first correction norms, so that the first solve is
+    // queued behind the factorisation without a wait on the host; a flagged
+    // slot's first solve and correction are wasted work, and its x is then
+    // the fallback's.  (A forced fallback, or no corrections, reads them here.)
     ZS_CU(cudaMemcpyAsync(ctx->h_pivflag + first, ctx->d_pivflag + first, sizeof(int) * count,
                           cudaMemcpyDeviceToHost, ln.stream));
-    ZS_CU(cudaStreamSynchronize(ln.stream));
-    for (int i = 0; i < count; i++) {
-        const int s = first + i;
-        if (info) info[i].pivot_flag = ctx->h_pivflag[s];
-        if (ctx->h_pivflag[s] || o.force_fallback) stalled.push_back(s);
-        else active.push_back(s);
+    bool flags_read = false;
+    auto take_flags = [&]() {
+        flags_read = true;
+        std::vector<int> keep;
+        for (int i = 0; i < count; i++) {
+            const int s = first + i;
+            if (info) info[i].pivot_flag = ctx->h_pivflag[s];
+        }
+        for (int s : active) {
+            if (ctx->h_pivflag[s]) stalled.push_back(s);
+            else keep.push_back(s);
+        }
+        active.swap(keep);
+    };
+    if (o.force_fallback) {
+        ZS_CU(cudaStreamSynchronize(ln.stream));
+        for (int i = 0; i < count; i++) stalled.push_back(first + i);
+        take_flags();
+    } else {
+        for (int i = 0; i < count; i++) active.push_back(first + i);
+        if (o.max_iter < 1) {
+            ZS_CU(cudaStreamSynchronize(ln.stream));
+            take_flags();
+        }
     }
     auto upload_active = [&]() -> int {
         for (size_t i = 0; i < active.size(); i++) ln.h_active[i] = active[i];
@@ -781,6 +803,7 @@ int refine_batch(zsolve_ctx *ctx, Lane &ln, const double2 *b, double2 *x, int64_
         ZS_CU(cudaMemcpyAsync(ctx->h_relcorr + (int64_t)first * nrhs, ctx->d_relcorr + (int64_t)first * nrhs,
                               sizeof(double) * (size_t)count * nrhs, cudaMemcpyDeviceToHost, ln.stream));
         ZS_TRY(check_device_status(ctx, ln));  // synchronises
+        if (!flags_read) take_flags();  // the flagged slots leave before their norms count
         std::vector<int> next;
         for (int s : active) {
             const int i = s - first;
