@@ -188,9 +188,8 @@ cudaError_t zs_launch_schur_simt(float *z32, int64_t ld, int64_t plane, int64_t 
 // Operand packs of the block triangular solves on the tensor cores, at outer
 // column J: A planes rows i >= J+NB = [Re A21(i,:) | Im A21(i,:)], Br planes
 // rows j >= J+NB = [Re A12(:,j) | Im A12(:,j)] (mode 1: tf32 hi; 2: hi + lo).
-// sym: Z is complex symmetric and only its lower part is current: 1, the A
-// planes only (the one-product symmetric block solve); 2, the A12^T packs
-// taken from A21 too (equal by symmetry; the two-product solve).
+// sym = 1: Z is complex symmetric and only its lower part is current; the A
+// planes only (all the symmetric block solve reads).
 cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int64_t z32_stride, int64_t n,
                                 int64_t J, float *pack, int64_t pack_stride, int mode, int sym, const int *slots,
                                 int nslot, cudaStream_t st);
@@ -218,7 +217,9 @@ cudaError_t zs_launch_schur_tc(const void *map, const void *cmap, int64_t n, int
 // sym: Z complex symmetric (A12 = A21^T, U11 = D11 L11^T): one product per row
 // tile, U12^T = A21 L11^-T, and L21 = U12^T D11^-1 with D11^-1 the diagonal of
 // the float32 inverse blocks (dinv, per slot dinv_stride floats); the packs
-// then need only A21's rows in the A planes.
+// then need only A21's rows in the A planes, and the epilogue writes U12 and
+// L21 into z32 and the update's one operand pack M = U12^T S, S^2 = D11^-1
+// entrywise, into the A planes (the lower update takes both operands from M).
 cudaError_t zs_launch_trsm_tc(const void *map, const void *wmap, const void *cmap, const void *pmap, int64_t n,
                               int64_t J, int split, int sym, const float *dinv, int64_t dinv_stride,
                               const int *slots, int nslot, unsigned *ctr, unsigned *status, int num_sms,

@@ -392,9 +392,8 @@ k_schur_simt(float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z32_str
 // Operand packs of the block triangular solves (blockIdx.y = 0: rows of A21
 // into the A planes; 1: columns of A12, transposed through shared memory,
 // into the Br planes), 32 rows or columns per CTA.  sym (a complex-symmetric
-// matrix, whose upper part is not kept current; A12^T = A21): 1, only the A
-// planes (the one-product symmetric block solve); 2, A21's rows into both the
-// A and the Br planes (the two-product solve).
+// matrix, whose upper part is not kept current): the A planes only, all the
+// symmetric block solve reads.
 constexpr int kPackThreads = 256;
 
 __global__ void __launch_bounds__(kPackThreads)
@@ -417,7 +416,6 @@ k_pack_trsm(const float *__restrict__ z32, int64_t ld, int64_t plane, int64_t z3
             if (i >= n) break;  // later idx only move to later rows
             const float4 v = *reinterpret_cast<const float4 *>((k < NB ? re : im) + i * ld + J + (k & (NB - 1)));
             pack_put4(pk, pk + pp, i * ZS_PACK_K + k, v, mode);
-            if (sym == 2) pack_put4(pk + 2 * pp, pk + 3 * pp, i * ZS_PACK_K + k, v, mode);
         }
     } else {
         for (int idx = tid; idx < 32 * ZS_PACK_K; idx += kPackThreads) {
@@ -485,7 +483,7 @@ cudaError_t zs_launch_pack_trsm(const float *z32, int64_t ld, int64_t plane, int
                                 int nslot, cudaStream_t st) {
     const int64_t m2 = n - J - NB;
     if (m2 <= 0 || nslot <= 0) return cudaSuccess;
-    if (mode != 1 && mode != 2) return cudaErrorInvalidValue;
+    if ((mode != 1 && mode != 2) || sym < 0 || sym > 1) return cudaErrorInvalidValue;
     const dim3 grid((unsigned)((m2 + 31) / 32), sym ? 1 : 2, (unsigned)nslot);
     k_pack_trsm<<<grid, kPackThreads, 0, st>>>(z32, ld, plane, z32_stride, n, J, pack, pack_stride, mode, sym,
                                                slots);

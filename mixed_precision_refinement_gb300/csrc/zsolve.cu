@@ -351,12 +351,11 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     // M = U12^T S (S^2 = D11^-1), from which the lower update takes both of
     // its operands.  The full mode's two-product form writes L21 and U12^T
     // packs instead.
-    auto one_product = [&](int64_t) { return sym != 0; };
     auto pack = [&](int64_t J, int buf, cudaStream_t st) -> int {
         StageSpan sp(ctx, ZSOLVE_STAGE_PACK, st);
         ZS_CU(zs_launch_pack_trsm(ctx->z32, ctx->ld, ctx->plane, ctx->z32_stride, n, J,
                                   ctx->pack + (int64_t)buf * ctx->S * ctx->pack_stride, ctx->pack_stride, mode,
-                                  sym ? (one_product(J) ? 1 : 2) : 0, slots, nslot, st));
+                                  sym, slots, nslot, st));
         sp.done(1);
         return ZSOLVE_OK;
     };
@@ -372,7 +371,7 @@ int factor_slots_tc(zsolve_ctx *ctx, Lane &ln, const int *slots, int nslot) {
     auto trsm = [&](int64_t J, int buf) -> int {
         StageSpan sp(ctx, ZSOLVE_STAGE_TRSM, ln.stream);
         ZS_CU(zs_launch_trsm_tc(ctx->pack_map[buf], ctx->winv_map, ctx->z32_map, ctx->packst_map[buf], n, J, split,
-                                one_product(J) ? 1 : 0, ctx->dinv, ctx->dinv_stride, slots, nslot, ctr++,
+                                sym, ctx->dinv, ctx->dinv_stride, slots, nslot, ctr++,
                                 ctx->d_status, tc_grid(ctx, ln), ln.stream));
         sp.done(1);
         return ZSOLVE_OK;
