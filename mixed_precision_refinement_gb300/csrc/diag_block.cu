@@ -32,6 +32,14 @@
 // The blocks outside the triangles are zero in both; they are set once when
 // the buffers are allocated and never written here.
 //
+// The symmetric mode's instance (SYM = true) takes U = D L^T as the
+// definition of the block's U side (D the pivots; an unpivoted LU of a
+// complex-symmetric matrix has this form): per panel it forms DL_p alone and
+// DU_p = DL_p^T D_p^-1, L_ip = A_ip DU_p and U_pj = D_p L_jp^T, and updates
+// only the blocks on and below the diagonal (the next diagonal block first,
+// the rest beside the next panel's base LU).  Its windows form V alone and
+// emit W = V^T D^-1 from it; no W operand pack is written.
+//
 // Padding: a last block with nb < 128 is completed with the identity, whose
 // factors and inverses are the identity again.
 #include "common.cuh"

@@ -37,6 +37,12 @@
 // tile's epilogue overwrites the very pack rows its own MMAs consumed, which
 // is safe: the accumulator is complete only after every load of the tile.
 //
+// The symmetric mode (kinds SCHUR_LOWER and TRSM_SYM, below) needs one pack
+// only: the block solve writes M = U12^T S with S^2 = D11^-1 entrywise into
+// the A planes, and since M M^T = L21 U12, the lower update reads both of its
+// operands from M's rows: B's real part is [Re M | Im M] with the negate-B
+// bit on the second K half, B's imaginary part its K halves swapped, as is.
+//
 // Warp roles (192 threads, persistent over the tiles of every frequency in
 // the batch): warp 0 issues TMA loads (128B-swizzled K-major tiles of 32
 // fp32) into a ring of shared-memory stages; warp 1 owns TMEM (512 columns:
@@ -62,7 +68,7 @@ constexpr int NKC = KTOT / KC;    // 8 K chunks
 constexpr int TM = 128, TN = 128; // complex output tile
 constexpr int kThreads = 192;
 constexpr int A_BYTES = TM * KC * 4;       // 16 KB
-constexpr int B_BYTES = 2 * TN * KC * 4;   // 32 KB (Br rows then Bi rows)
+constexpr int B_BYTES = 2 * TN * KC * 4;   // 32 KB (B rows at chunk k, then the same rows at chunk k +- 128)
 constexpr uint32_t TMEM_COLS = 512;
 // try_wait polls before a wait gives up: about a second here (a poll that
 // finds the phase incomplete suspends for some microseconds)
@@ -70,7 +76,7 @@ constexpr uint32_t kWaitLimit = 1u << 19;
 constexpr int kTq = 8;  // tile-index queue between the roles (the producer runs at most a few tiles ahead)
 
 enum { PL_A_HI = 0, PL_A_LO = 1, PL_BR_HI = 2, PL_BR_LO = 3, PL_BI_HI = 4, PL_BI_LO = 5 };
-// inverse packs: W = U11^-1 in planes 0-3, V = L11^-1 in planes 4-7 (Br hi, Br lo, Bi hi, Bi lo)
+// inverse packs: W = U11^-1 in planes 0-1, V = L11^-1 in planes 2-3 (Br hi, Br lo each)
 enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_V = 2 };
 // KIND_SCHUR_LOWER: the trailing update of a complex-symmetric matrix, whose
 // Schur complement stays symmetric: only the tiles on and below the diagonal
@@ -78,7 +84,9 @@ enum { WP_BR_HI = 0, WP_BR_LO = 1, WP_V = 2 };
 // KIND_TRSM_SYM: the block solves of a complex-symmetric matrix in one
 // product per row tile: with A12 = A21^T and U11 = D11 L11^T (D11 = diag U11),
 // U12^T = A21 L11^-T from the MMAs, and L21 = A21 U11^-1 = U12^T D11^-1 in the
-// epilogue, which writes both (half the MMAs and operand loads of KIND_TRSM).
+// epilogue, which writes both factors and the update's pack M (half the MMAs
+// and operand loads of KIND_TRSM, and a third fewer stores than with
+// separate L21 and U12^T packs).
 enum { KIND_SCHUR = 0, KIND_TRSM = 1, KIND_SCHUR_LOWER = 2, KIND_TRSM_SYM = 3 };
 
 template <int KIND>
